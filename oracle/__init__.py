@@ -1,0 +1,280 @@
+"""fp64 CPU oracle for the MXFP4 routed-expert MoE layer (ctypes front end).
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product (the
+CUDA library and its binding) never imports it and shares no code with it.
+
+All arithmetic lives in ``k3oracle.c`` (plain C99, double precision); this
+module only marshals numpy arrays.  Parity status per function is listed in
+``k3oracle.c`` and in the tests under ``tests/test_oracle_*.py``.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "k3oracle.c")
+_SO = os.path.join(_HERE, "libk3oracle.so")
+_lib = None
+
+
+def build(force=False):
+    """Compile the oracle with gcc: plain C, fp64, contraction off."""
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + ".%d.tmp" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared", "-fopenmp",
+                               "-ffp-contract=off", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+class Mat(ctypes.Structure):
+    _fields_ = [("packed", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("rows", ctypes.c_int), ("in_", ctypes.c_int)]
+
+
+class Expert(ctypes.Structure):
+    _fields_ = [("gate", Mat), ("up", Mat), ("down", Mat)]
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_SO)
+        p, i, d = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+        L.orc_set_threads.argtypes = [i]
+        L.orc_max_threads.restype = i
+        L.orc_e2m1_value.restype = d
+        L.orc_e2m1_value.argtypes = [i]
+        L.orc_e8m0_value.restype = d
+        L.orc_e8m0_value.argtypes = [i]
+        L.orc_code.restype = i
+        L.orc_code.argtypes = [p, i, i]
+        L.orc_weight.restype = d
+        L.orc_weight.argtypes = [p, i, i]
+        L.orc_dequant.argtypes = [p, p]
+        L.orc_matvec.argtypes = [p, p, p]
+        L.orc_matvec_groupwise.argtypes = [p, p, p]
+        L.orc_matrix_bytes.restype = ctypes.c_int64
+        L.orc_matrix_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+        L.orc_expert_bytes.restype = ctypes.c_int64
+        L.orc_expert_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+        L.orc_silu.restype = d
+        L.orc_silu.argtypes = [d]
+        L.orc_round_bf16.restype = d
+        L.orc_round_bf16.argtypes = [d]
+        L.orc_expert_forward_ex.argtypes = [p, p, p, i, p]
+        L.orc_bf16_value.restype = d
+        L.orc_bf16_value.argtypes = [ctypes.c_uint16]
+        L.orc_router_logits.argtypes = [p, p, p, i, i, i]
+        L.orc_topk_one.restype = d
+        L.orc_topk.argtypes = [p, p, p, p, p, i, i, i]
+        L.orc_combine.argtypes = [p, p, i, i, p, p, i, p, i]
+        L.orc_layer_forward.argtypes = [p, p, p, p, p, i, i, i, i, p, p, p, i]
+        L.orc_rmsnorm.argtypes = [p, p, i, d]
+        L.orc_cache_lru.restype = ctypes.c_longlong
+        L.orc_cache_lru.argtypes = [p, p, p, i, i, p, i]
+        L.orc_cache_belady.restype = ctypes.c_longlong
+        L.orc_cache_belady.argtypes = [p, p, i, i]
+        _lib = L
+    return _lib
+
+
+def set_threads(n):
+    lib().orc_set_threads(int(n))
+
+
+def max_threads():
+    return lib().orc_max_threads()
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def make_mat(packed, scales):
+    packed = _c(packed, np.uint8)
+    scales = _c(scales, np.uint8)
+    rows, half = packed.shape
+    assert scales.shape == (rows, (2 * half) // 32)
+    m = Mat(packed.ctypes.data, scales.ctypes.data, rows, 2 * half)
+    m._keep = (packed, scales)
+    return m
+
+
+def make_expert(ex):
+    """ctypes Expert from a dict with gate/up/down packed+scales planes."""
+    g = make_mat(ex["gate_packed"], ex["gate_scales"])
+    u = make_mat(ex["up_packed"], ex["up_scales"])
+    dn = make_mat(ex["down_packed"], ex["down_scales"])
+    e = Expert(g, u, dn)
+    e._keep = (g, u, dn)
+    return e
+
+
+# ------------------------------------------------------------------ format
+
+def e2m1_value(code):
+    return lib().orc_e2m1_value(int(code))
+
+
+def e8m0_value(e):
+    return lib().orc_e8m0_value(int(e))
+
+
+def code(packed, scales, r, j):
+    m = make_mat(packed, scales)
+    return lib().orc_code(ctypes.byref(m), r, j)
+
+
+def dequant(packed, scales):
+    m = make_mat(packed, scales)
+    out = np.empty((m.rows, m.in_), np.float64)
+    lib().orc_dequant(_p(out), ctypes.byref(m))
+    return out
+
+
+def matvec(packed, scales, x):
+    m = make_mat(packed, scales)
+    x = _c(x, np.float64)
+    assert x.shape == (m.in_,)
+    y = np.empty(m.rows, np.float64)
+    lib().orc_matvec(_p(y), ctypes.byref(m), _p(x))
+    return y
+
+
+def matvec_groupwise(packed, scales, x):
+    m = make_mat(packed, scales)
+    x = _c(x, np.float64)
+    y = np.empty(m.rows, np.float64)
+    lib().orc_matvec_groupwise(_p(y), ctypes.byref(m), _p(x))
+    return y
+
+
+def matrix_bytes(rows, cols):
+    return lib().orc_matrix_bytes(rows, cols)
+
+
+def expert_bytes(d, f):
+    return lib().orc_expert_bytes(d, f)
+
+
+# ------------------------------------------------------------------ expert
+
+def silu(z):
+    return lib().orc_silu(float(z))
+
+
+def round_bf16(v):
+    return lib().orc_round_bf16(float(v))
+
+
+def expert_forward(ex, x, h_bf16=False, want_h=False):
+    e = make_expert(ex)
+    x = _c(x, np.float64)
+    d = e.gate.in_
+    f = e.gate.rows
+    assert x.shape == (d,)
+    y = np.empty(d, np.float64)
+    h = np.empty(f, np.float64) if want_h else None
+    lib().orc_expert_forward_ex(_p(y), ctypes.byref(e), _p(x), int(bool(h_bf16)), _p(h))
+    return (y, h) if want_h else y
+
+
+# ------------------------------------------------------------------ router
+
+def bf16_value(bits):
+    return lib().orc_bf16_value(int(bits))
+
+
+def router_logits(x, Wr_bits):
+    x = _c(np.atleast_2d(x), np.float64)
+    Wr = _c(Wr_bits, np.uint16)
+    T, d = x.shape
+    E = Wr.shape[0]
+    assert Wr.shape == (E, d)
+    out = np.empty((T, E), np.float64)
+    lib().orc_router_logits(_p(out), _p(x), _p(Wr), T, E, d)
+    return out
+
+
+def topk(logits, k, bias=None):
+    """(ids ascending int32 [T,k], softmax weights [T,k], margins [T])."""
+    logits = _c(np.atleast_2d(logits), np.float64)
+    T, E = logits.shape
+    b = None if bias is None else _c(bias, np.float64)
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    m = np.empty(T, np.float64)
+    lib().orc_topk(_p(ids), _p(w), _p(m), _p(logits), _p(b), T, E, k)
+    return ids, w, m
+
+
+def _expert_table(experts, E):
+    """experts: dict id -> expert dict (only the ids that are read)."""
+    tab = (Expert * E)()
+    keep = []
+    for e, ex in experts.items():
+        ce = make_expert(ex)
+        tab[e] = ce
+        keep.append(ce)
+    tab._keep = keep
+    return tab
+
+
+def combine(x, ids, w, experts, E, h_bf16=False):
+    x = _c(np.atleast_2d(x), np.float64)
+    T, d = x.shape
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float64)
+    k = ids.shape[1]
+    need = set(int(v) for v in ids.ravel())
+    assert need <= set(experts), "missing expert weights for ids %s" % sorted(need - set(experts))
+    tab = _expert_table(experts, E)
+    out = np.empty((T, d), np.float64)
+    lib().orc_combine(_p(out), _p(x), T, d, _p(ids), _p(w), k,
+                      ctypes.cast(tab, ctypes.c_void_p), int(bool(h_bf16)))
+    return out
+
+
+def layer_forward(x, Wr_bits, k, experts, bias=None, h_bf16=False):
+    """Full layer. `experts` must hold (at least) every expert selected."""
+    x = _c(np.atleast_2d(x), np.float64)
+    T, d = x.shape
+    E = Wr_bits.shape[0]
+    logits = router_logits(x, Wr_bits)
+    ids, w, m = topk(logits, k, bias)
+    out = combine(x, ids, w, experts, E, h_bf16)
+    return out, ids, w, m
+
+
+def rmsnorm(x, eps):
+    x = _c(x, np.float64)
+    y = np.empty_like(x)
+    lib().orc_rmsnorm(_p(y), _p(x), x.size, float(eps))
+    return y
+
+
+# ------------------------------------------------------------------- cache
+
+def cache_lru(keys, batch_len, capacity, pinned=()):
+    keys = _c(keys, np.int64)
+    bl = _c(batch_len, np.int32)
+    pn = _c(np.asarray(pinned, np.int64), np.int64)
+    hit = np.zeros(keys.size, np.uint8)
+    h = lib().orc_cache_lru(_p(hit), _p(keys), _p(bl), bl.size, int(capacity),
+                            _p(pn) if pn.size else None, pn.size)
+    return h, hit
+
+
+def cache_belady(keys, batch_len, capacity):
+    keys = _c(keys, np.int64)
+    bl = _c(batch_len, np.int32)
+    return lib().orc_cache_belady(_p(keys), _p(bl), bl.size, int(capacity))
