@@ -1,0 +1,328 @@
+/*
+ * k3moe.h -- C ABI of the GB300 (sm_103a) MXFP4 routed-expert MoE library.
+ *
+ * The library computes the routed-expert layer of a mixture-of-experts
+ * decoder straight from packed MXFP4 weights: router logits, top-k selection
+ * with softmax combine weights, and for every selected expert the gate/up
+ * products, SwiGLU, the down product and the weighted combine.  The 4-bit
+ * codes are decoded in registers; no weight is ever expanded to float in
+ * memory.
+ *
+ * Sources of the operations (page title, section):
+ *  [EXPL]  "kimi-k3-in-c" explainer, ai.thesatyajit.com
+ *  [ENG]   "kimi-k3-in-c: A 176 KB Engine That Runs a 2.78T-Parameter MoE in
+ *          8 GB of RAM", aniketkarneai.com
+ *  [LOCAL] "Running Kimi K3 locally: activation sparsity as architecture",
+ *          zorost.com
+ *  [HOW]   "How kimi-k3-in-c Runs a 2.8-Trillion-Parameter Model on 8 GB of
+ *          RAM", dimitriaigle.fr
+ *
+ * Conventions for every call:
+ *  - Pointers are DEVICE pointers unless the parameter name starts with
+ *    `host_`.  Device buffers must be 16-byte aligned.
+ *  - The caller owns every buffer it passes; the library owns only the objects
+ *    it creates (layer, cache) and frees them in the matching destroy call.
+ *  - Work is enqueued on the caller's stream `s` (a cudaStream_t; NULL is the
+ *    legacy default stream) and returns before the GPU finishes.  Outputs are
+ *    valid once the stream has reached that point.
+ *  - Every call returns a status: K3MOE_OK (0) or a negative K3MOE_E* code.
+ *    Invalid arguments are refused with K3MOE_EINVAL before anything is
+ *    enqueued; nothing is guessed or defaulted (a zero or inconsistent size is
+ *    an error).  No call exits the process or throws.
+ *  - A NaN E8M0 scale (byte 255) is not an error: its 32-group contributes 0
+ *    [ENG, "What byte-identical actually costs"].
+ *  - Device kernels never trap.  Errors detected on the device (a bounded
+ *    wait that ran out) are recorded in a device error word that
+ *    k3moe_device_error() reads and clears.
+ */
+#ifndef K3MOE_H
+#define K3MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status codes */
+
+#define K3MOE_OK        0
+#define K3MOE_EINVAL   (-1)  /* bad argument: size, alignment, null pointer   */
+#define K3MOE_ENOMEM   (-2)  /* an allocation the call needs failed           */
+#define K3MOE_ECUDA    (-3)  /* a CUDA runtime call failed                    */
+#define K3MOE_ETIMEOUT (-4)  /* a bounded device or host wait ran out          */
+#define K3MOE_EBUSY    (-5)  /* cache: no evictable slot for a batch          */
+#define K3MOE_ENODEV   (-6)  /* no usable sm_103 device                       */
+
+/* Input activation types for k3moe_layer_forward. */
+#define K3MOE_F32  0
+#define K3MOE_BF16 1
+
+typedef struct CUstream_st *k3moe_stream; /* same object as cudaStream_t */
+
+/* Human-readable name of a status code (static string). */
+const char *k3moe_strerror(int status);
+
+/* Library ABI version, (major << 16) | minor. */
+int k3moe_version(void);
+
+/* Reads and clears the device error word of the current device
+ * (0 = none, else a K3MOE_E* code).  Synchronises the device. */
+int k3moe_device_error(void);
+
+/* ---------------------------------------------------------- packed format */
+
+/*
+ * One MXFP4 matrix W[rows][in] in the pages' canonical layout [EXPL,
+ * "Reduction one: the experts already ship at half a byte"]:
+ *   packed : [rows][in/2] bytes, two 4-bit E2M1 codes per byte; the LOW nibble
+ *            holds the even-index weight, the high nibble the odd one [LOCAL,
+ *            "What are the four reductions, and why is the answer unchanged?"]
+ *   scales : [rows][in/32] bytes, one E8M0 exponent e per 32 consecutive
+ *            weights of a row; value = E2M1(code) * 2^(e-127); e = 255 zeroes
+ *            the group.
+ * 0.53125 bytes per weight [ENG, "The four reductions"].  `in` must be a
+ * multiple of 32.  Both planes must be 16-byte aligned.
+ */
+typedef struct {
+    const uint8_t *packed;
+    const uint8_t *scales;
+    int32_t rows;
+    int32_t in;
+} k3moe_mat;
+
+/* One routed expert: gate and up are [f x d], down is [d x f]. */
+typedef struct {
+    k3moe_mat gate;
+    k3moe_mat up;
+    k3moe_mat down;
+} k3moe_expert;
+
+/* Packed bytes of a rows x in matrix: rows * (in/2 + in/32); -1 if invalid. */
+int64_t k3moe_matrix_bytes(int32_t rows, int32_t in);
+
+/* Packed bytes of one expert, 3 matrices; 17,547,264 for d=7168, f=1536
+ * [ENG, "The four reductions"; EXPL, "Reduction one"].  -1 if invalid. */
+int64_t k3moe_expert_bytes(int32_t d, int32_t f);
+
+/*
+ * HBM layout of one expert: a single blob of k3moe_expert_bytes(d, f) bytes
+ * holding, in order, gate.packed, gate.scales, up.packed, up.scales,
+ * down.packed, down.scales (every plane size is a multiple of 16 bytes for
+ * d, f multiples of 32).  k3moe_expert_view fills *out with the six plane
+ * pointers inside `blob` (pure host arithmetic, no CUDA call).
+ */
+int k3moe_expert_view(k3moe_expert *host_out, const void *blob, int32_t d, int32_t f);
+
+/*
+ * Packs the six canonical planes (each in host or device memory) into one
+ * expert blob (device memory, caller-owned, k3moe_expert_bytes(d, f) bytes),
+ * by stream-ordered copies on `s`.  Plane shapes as in k3moe_mat.
+ */
+int k3moe_pack_expert(void *blob, const uint8_t *gate_packed, const uint8_t *gate_scales,
+                      const uint8_t *up_packed, const uint8_t *up_scales,
+                      const uint8_t *down_packed, const uint8_t *down_scales, int32_t d,
+                      int32_t f, k3moe_stream s);
+
+/* ------------------------------------------------------ expert products */
+
+/*
+ * y[rows] = W x for one packed matrix: the pages' primitive
+ * k3_matmul_mxfp4 [EXPL, "Reduction one"], here with fp32 accumulation.
+ * x: fp32 [W->in]; y: fp32 [W->rows]. `host_W` is a host struct holding
+ * device plane pointers.
+ */
+int k3moe_matmul_mxfp4(float *y, const float *x, const k3moe_mat *host_W, k3moe_stream s);
+
+/*
+ * One expert, one token: y = W_down (silu(W_gate x) * (W_up x)),
+ * silu(z) = z / (1 + e^-z).  x fp32 [d], y fp32 [d].
+ * `workspace` is caller-owned device scratch of at least
+ * k3moe_expert_gemv_workspace(d, f) bytes (it holds the SwiGLU output h).
+ */
+size_t k3moe_expert_gemv_workspace(int32_t d, int32_t f);
+int k3moe_expert_gemv(float *y, const float *x, const k3moe_expert *host_e, int32_t d,
+                      int32_t f, void *workspace, size_t workspace_bytes, k3moe_stream s);
+
+/* ----------------------------------------------------------------- layer */
+
+/*
+ * A routed-expert MoE layer with all experts resident in HBM.
+ *  n_experts  E (896 on the pages [ENG, intro]), top_k (16)
+ *  d, f       hidden and expert intermediate sizes (multiples of 32)
+ *  router_w   bf16 [E x d] row-major (the router is part of the bf16 trunk)
+ *  sel_bias   fp32 [E] added to the logits for SELECTION only, or NULL.  The
+ *             combine weights always come from the unbiased logits [LOCAL,
+ *             "How is the C engine actually built?", invariant 3].
+ *  host_experts  host array of E expert views (device plane pointers); the
+ *             table is copied at create, the weights are not.  NULL makes a
+ *             router-only layer (route and experts_t1 only, for experts that
+ *             live in an expert cache).
+ *  max_tokens the largest T that forward will be called with (sizes the
+ *             library-owned scratch).
+ * Returns K3MOE_EINVAL on any zero/invalid field, K3MOE_ENOMEM if the scratch
+ * cannot be allocated.
+ */
+typedef struct {
+    int32_t n_experts;
+    int32_t top_k;
+    int32_t d;
+    int32_t f;
+    const uint16_t *router_w;
+    const float *sel_bias;
+    const k3moe_expert *host_experts;
+    int32_t max_tokens;
+} k3moe_layer_desc;
+
+typedef struct k3moe_layer k3moe_layer;
+
+int k3moe_layer_create(k3moe_layer **host_out, const k3moe_layer_desc *host_desc);
+int k3moe_layer_destroy(k3moe_layer *L);
+
+/*
+ * Routing only: logits = X W_r^T (fp32 accumulation), the top_k experts by
+ * logit + sel_bias (ties to the lower id), ids ascending, and w = softmax of
+ * the unbiased logits over the chosen set.
+ *  X    [T x d], x_dtype K3MOE_F32 or K3MOE_BF16
+ *  ids  int32 [T x top_k] (out), w fp32 [T x top_k] (out)
+ */
+int k3moe_layer_route(k3moe_layer *L, const void *X, int x_dtype, int32_t T, int32_t *ids,
+                      float *w, k3moe_stream s);
+
+/*
+ * The whole layer: out[t] = sum_j w[t][j] * expert_{ids[t][j]}(X[t]).
+ *  X    [T x d] (x_dtype), out fp32 [T x d]
+ *  ids_out / w_out  optional (NULL allowed) copies of the routing result.
+ * 1 <= T <= max_tokens.  T = 1 runs the fused batch-1 path; T > 1 groups the
+ * (token, slot) pairs by expert and runs grouped products.
+ */
+int k3moe_layer_forward(k3moe_layer *L, const void *X, int x_dtype, int32_t T, float *out,
+                        int32_t *ids_out, float *w_out, k3moe_stream s);
+
+/*
+ * Timing hook: when set, every later k3moe_layer_forward records
+ * host_events[0] on its stream before the first kernel, [1] after routing,
+ * [2] after the gate/up products and [3] after the down products and combine
+ * (cudaEvent_t handles, created and owned by the caller).  n = 0 clears it.
+ */
+int k3moe_layer_set_events(k3moe_layer *L, void *const *host_events, int32_t n);
+
+/*
+ * Batch-1 experts for an explicit expert list, e.g. slots handed out by the
+ * expert cache: out = sum_j w[j] * expert_j(x) over host_sel[0..k).
+ *  host_sel  host array of k expert views (device pointers), k <= 16
+ *  w         fp32 [k] combine weights (device)
+ *  x         fp32 [d], out fp32 [d]
+ */
+int k3moe_layer_experts_t1(k3moe_layer *L, const float *x, const k3moe_expert *host_sel,
+                           const float *w, int32_t k, float *out, k3moe_stream s);
+
+/*
+ * RMSNorm with residual, as used between streamed layers:
+ *  u = x / sqrt(mean(x^2) + eps)   (epsilon inside the square root [ENG,
+ *  "What byte-identical actually costs"]; unit gain).  x fp32 [n], u fp32 [n].
+ */
+int k3moe_rmsnorm(float *u, const float *x, int32_t n, float eps, k3moe_stream s);
+
+/* x += delta, fp32 [n]. */
+int k3moe_residual_add(float *x, const float *delta, int32_t n, k3moe_stream s);
+
+/* ------------------------------------------------------------ expert cache */
+
+/*
+ * HBM-resident LRU cache of expert blobs fed from pinned host memory
+ * [EXPL, "The cache the project exists for", "The bug the code confesses
+ * to"; HOW, "The LRU cache: which experts to keep hot"].
+ *
+ * Keys are (layer * n_experts + expert).  The arena holds
+ * floor(capacity_bytes / expert_bytes) slots.  Each slot is EMPTY, INFLIGHT
+ * (reserved by a batch whose copy has not been waited for) or holds a key.
+ * A batch acquire first marks its hits, then gives every miss a DISTINCT slot
+ * (an EMPTY one, else the least recently used slot that is neither pinned nor
+ * used by the same batch), marks it INFLIGHT, and issues one host->HBM copy of
+ * expert_bytes per miss on a library-owned side stream; the caller's
+ * `compute` stream is made to wait for those copies (events), so kernels
+ * enqueued on it afterwards see the data.
+ *
+ *  host_blobs  host array of n_layers * n_experts pointers to each expert's
+ *              blob in host memory (pinned by the caller for full speed).
+ * create returns K3MOE_ENOMEM if the arena cannot be allocated (it refuses
+ * up front instead of failing later), K3MOE_EINVAL if it holds < 1 slot.
+ */
+typedef struct k3moe_cache k3moe_cache;
+
+typedef struct {
+    int64_t lookups;
+    int64_t hits;
+    int64_t misses;
+    int64_t evictions;
+    int64_t h2d_bytes;  /* bytes copied host -> HBM for misses            */
+    int64_t hbm_bytes;  /* expert bytes handed to kernels (hits + misses) */
+    int32_t slots;
+    int32_t pinned;
+    int32_t inflight;
+    int32_t reserved;
+} k3moe_cache_stats;
+
+int k3moe_cache_create(k3moe_cache **host_out, size_t capacity_bytes, size_t expert_bytes,
+                       const void *const *host_blobs, int32_t n_layers, int32_t n_experts);
+int k3moe_cache_destroy(k3moe_cache *C);
+
+/*
+ * Resolves n keys (host array) to device blob pointers (host_blobs_out[n]).
+ * host_hit_out (optional) receives 1 per hit, 0 per miss.  Returns
+ * K3MOE_EBUSY if a miss finds no evictable slot (nothing is changed then).
+ */
+int k3moe_cache_acquire(k3moe_cache *C, const int64_t *host_keys, int32_t n,
+                        void **host_blobs_out, uint8_t *host_hit_out, k3moe_stream compute);
+
+/* Ends the use of every slot handed out since the previous release: records
+ * on `compute` the point after which those slots may be overwritten (a later
+ * miss that evicts one of them makes its copy wait for that point).  Slots
+ * acquired and not yet released are never evicted. */
+int k3moe_cache_release(k3moe_cache *C, k3moe_stream compute);
+
+/* Pins a key: it is loaded if absent (stream-ordered on `compute`) and never
+ * evicted afterwards.  K3MOE_EBUSY if no slot can hold it. */
+int k3moe_cache_pin(k3moe_cache *C, int64_t key, k3moe_stream compute);
+
+int k3moe_cache_get_stats(k3moe_cache *C, k3moe_cache_stats *host_out);
+
+/* Request histogram: n_layers * n_experts counters of how often each key was
+ * asked for [EXPL, "The cache the project exists for"].  Host memory owned
+ * by the cache; valid until destroy. */
+const uint32_t *k3moe_cache_histogram(const k3moe_cache *C);
+
+/*
+ * Copier interface, for tests of the host logic without a GPU: the cache
+ * calls alloc_arena once at create, copy() per miss (after the slot's last
+ * release), wait() before handing a copied slot's pointer out, release() per
+ * slot in k3moe_cache_release, and free_arena at destroy.  Return 0 on
+ * success, a negative K3MOE_E* code on failure.  A failed copy leaves its slot
+ * EMPTY and the key uncached, and acquire returns the copier's code.  A cache
+ * created with a copier makes no CUDA call; its `compute` arguments are
+ * passed through untouched.
+ */
+typedef struct {
+    void *ctx;
+    int (*alloc_arena)(void *ctx, size_t bytes, void **arena_out);
+    int (*free_arena)(void *ctx, void *arena);
+    int (*copy)(void *ctx, int32_t slot, void *dst, const void *src, size_t bytes);
+    int (*wait)(void *ctx, int32_t slot);
+    int (*release)(void *ctx, int32_t slot);
+} k3moe_copier;
+
+int k3moe_cache_create_with_copier(k3moe_cache **host_out, size_t capacity_bytes,
+                                   size_t expert_bytes, const void *const *host_blobs,
+                                   int32_t n_layers, int32_t n_experts,
+                                   const k3moe_copier *host_copier);
+
+/* Slot index that holds `key`, or -1 (for tests). */
+int32_t k3moe_cache_slot_of(const k3moe_cache *C, int64_t key);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* K3MOE_H */

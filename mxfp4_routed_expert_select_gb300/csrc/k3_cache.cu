@@ -1,0 +1,371 @@
+// k3_cache.cu -- HBM-resident LRU expert cache fed from pinned host memory.
+//
+// What the pages describe for the CPU engine's expert cache ("kimi-k3-in-c"
+// explainer, "The cache the project exists for" and "The bug the code
+// confesses to"; "How kimi-k3-in-c Runs...", "The LRU cache"), rebuilt for
+// one GPU: the arena is one cudaMalloc of `slots` expert blobs in HBM; a miss
+// is one cudaMemcpyAsync of the expert's blob on a side stream; the caller's
+// compute stream waits on per-slot events, so the host never blocks.
+//
+// Slot states: a key (>= 0), EMPTY, or INFLIGHT.  INFLIGHT marks a slot that
+// a batch has reserved for a copy and not yet published.  Victim selection
+// skips INFLIGHT slots, so two misses of one batch can never be given the
+// same slot -- the failure the explainer page reports for the CPU engine,
+// where an "empty" fast path handed one slot to several parallel reads.
+//
+// Replacement: a batch's hits are marked first (most recently used, in use);
+// each miss then takes the lowest-index EMPTY slot, else the least recently
+// used slot (lowest index on ties) that is neither pinned nor in use.  Slots
+// stay "in use" from acquire until k3moe_cache_release, which records on the
+// compute stream the point after which they may be overwritten.
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "k3moe.h"
+
+namespace {
+
+constexpr int64_t kEmpty = -1;
+constexpr int64_t kInflight = -2;
+
+// Default copier: device arena, side stream, per-slot copy/release events.
+struct CudaCopier {
+    cudaStream_t side = nullptr;
+    cudaStream_t compute = nullptr;  // set per call
+    std::vector<cudaEvent_t> copied, released;
+    std::vector<char> has_release;
+};
+
+int cuda_alloc(void *ctx, size_t bytes, void **out)
+{
+    (void)ctx;
+    if (cudaMalloc(out, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return K3MOE_ENOMEM;
+    }
+    return K3MOE_OK;
+}
+int cuda_free(void *ctx, void *p)
+{
+    (void)ctx;
+    return cudaFree(p) == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
+}
+int cuda_copy(void *ctx, int32_t slot, void *dst, const void *src, size_t bytes)
+{
+    CudaCopier *c = (CudaCopier *)ctx;
+    if (c->has_release[slot] && cudaStreamWaitEvent(c->side, c->released[slot], 0) != cudaSuccess)
+        return K3MOE_ECUDA;
+    if (cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, c->side) != cudaSuccess)
+        return K3MOE_ECUDA;
+    if (cudaEventRecord(c->copied[slot], c->side) != cudaSuccess) return K3MOE_ECUDA;
+    return K3MOE_OK;
+}
+int cuda_wait(void *ctx, int32_t slot)
+{
+    CudaCopier *c = (CudaCopier *)ctx;
+    return cudaStreamWaitEvent(c->compute, c->copied[slot], 0) == cudaSuccess ? K3MOE_OK
+                                                                               : K3MOE_ECUDA;
+}
+int cuda_release(void *ctx, int32_t slot)
+{
+    CudaCopier *c = (CudaCopier *)ctx;
+    if (cudaEventRecord(c->released[slot], c->compute) != cudaSuccess) return K3MOE_ECUDA;
+    c->has_release[slot] = 1;
+    return K3MOE_OK;
+}
+
+}  // namespace
+
+struct k3moe_cache {
+    size_t expert_bytes = 0;
+    int32_t n_layers = 0, n_experts = 0;
+    int64_t nkeys = 0;
+    std::vector<const void *> host;
+    int32_t slots = 0;
+    uint8_t *arena = nullptr;
+    std::vector<int64_t> key;       // per slot: key, kEmpty or kInflight
+    std::vector<int64_t> last;      // per slot: recency stamp
+    std::vector<uint8_t> pin;       // per slot
+    std::vector<int32_t> in_use;    // per slot: acquired and not released
+    std::vector<int32_t> where;     // per key: slot or -1
+    std::vector<uint32_t> hist;     // per key: requests
+    k3moe_cache_stats st;
+    int64_t now = 0;
+    k3moe_copier cp;
+    CudaCopier *cuda = nullptr;     // when the default copier is used
+    std::vector<int32_t> used;      // slots handed out since the last release
+};
+
+static void cache_free(k3moe_cache *C)
+{
+    if (!C) return;
+    if (C->arena) C->cp.free_arena(C->cp.ctx, C->arena);
+    if (C->cuda) {
+        for (auto e : C->cuda->copied) cudaEventDestroy(e);
+        for (auto e : C->cuda->released) cudaEventDestroy(e);
+        if (C->cuda->side) cudaStreamDestroy(C->cuda->side);
+        delete C->cuda;
+    }
+    delete C;
+}
+
+static int cache_init(k3moe_cache **out, size_t capacity_bytes, size_t expert_bytes,
+                      const void *const *host_blobs, int32_t n_layers, int32_t n_experts,
+                      const k3moe_copier *cp, bool use_cuda)
+{
+    if (!out) return K3MOE_EINVAL;
+    *out = nullptr;
+    if (expert_bytes == 0 || expert_bytes % 16 || !host_blobs || n_layers <= 0 || n_experts <= 0)
+        return K3MOE_EINVAL;
+    const size_t slots = capacity_bytes / expert_bytes;
+    if (slots < 1 || slots > (1u << 30)) return K3MOE_EINVAL;
+    const int64_t nkeys = (int64_t)n_layers * n_experts;
+    for (int64_t q = 0; q < nkeys; q++)
+        if (!host_blobs[q]) return K3MOE_EINVAL;
+    k3moe_cache *C = new (std::nothrow) k3moe_cache;
+    if (!C) return K3MOE_ENOMEM;
+    C->expert_bytes = expert_bytes;
+    C->n_layers = n_layers;
+    C->n_experts = n_experts;
+    C->nkeys = nkeys;
+    C->host.assign(host_blobs, host_blobs + nkeys);
+    C->slots = (int32_t)slots;
+    C->key.assign(slots, kEmpty);
+    C->last.assign(slots, -1);
+    C->pin.assign(slots, 0);
+    C->in_use.assign(slots, 0);
+    C->where.assign(nkeys, -1);
+    C->hist.assign(nkeys, 0);
+    memset(&C->st, 0, sizeof(C->st));
+    C->st.slots = C->slots;
+    if (use_cuda) {
+        C->cuda = new (std::nothrow) CudaCopier;
+        if (!C->cuda) {
+            delete C;
+            return K3MOE_ENOMEM;
+        }
+        C->cp = {C->cuda, cuda_alloc, cuda_free, cuda_copy, cuda_wait, cuda_release};
+        if (cudaStreamCreateWithFlags(&C->cuda->side, cudaStreamNonBlocking) != cudaSuccess) {
+            cudaGetLastError();
+            cache_free(C);
+            return K3MOE_ECUDA;
+        }
+        C->cuda->copied.resize(slots);
+        C->cuda->released.resize(slots);
+        C->cuda->has_release.assign(slots, 0);
+        for (size_t s = 0; s < slots; s++) {
+            if (cudaEventCreateWithFlags(&C->cuda->copied[s], cudaEventDisableTiming) !=
+                    cudaSuccess ||
+                cudaEventCreateWithFlags(&C->cuda->released[s], cudaEventDisableTiming) !=
+                    cudaSuccess) {
+                cudaGetLastError();
+                cache_free(C);
+                return K3MOE_ECUDA;
+            }
+        }
+    } else {
+        C->cp = *cp;
+    }
+    void *arena = nullptr;
+    int rc = C->cp.alloc_arena(C->cp.ctx, slots * expert_bytes, &arena);
+    if (rc != K3MOE_OK || !arena) {
+        cache_free(C);
+        return rc != K3MOE_OK ? rc : K3MOE_ENOMEM;
+    }
+    C->arena = (uint8_t *)arena;
+    *out = C;
+    return K3MOE_OK;
+}
+
+// Victim for one miss: lowest-index EMPTY slot, else the least recently used
+// slot that is not pinned, not in use and not INFLIGHT.  `taken` marks slots
+// already planned for this batch.
+static int32_t pick_victim(const k3moe_cache *C, const std::vector<char> &taken)
+{
+    for (int32_t s = 0; s < C->slots; s++)
+        if (!taken[s] && C->key[s] == kEmpty) return s;
+    int32_t v = -1;
+    for (int32_t s = 0; s < C->slots; s++) {
+        if (taken[s] || C->pin[s] || C->in_use[s] || C->key[s] == kInflight) continue;
+        if (v < 0 || C->last[s] < C->last[v]) v = s;
+    }
+    return v;
+}
+
+extern "C" {
+
+int k3moe_cache_create(k3moe_cache **out, size_t capacity_bytes, size_t expert_bytes,
+                       const void *const *host_blobs, int32_t n_layers, int32_t n_experts)
+{
+    return cache_init(out, capacity_bytes, expert_bytes, host_blobs, n_layers, n_experts, nullptr,
+                      true);
+}
+
+int k3moe_cache_create_with_copier(k3moe_cache **out, size_t capacity_bytes,
+                                   size_t expert_bytes, const void *const *host_blobs,
+                                   int32_t n_layers, int32_t n_experts, const k3moe_copier *cp)
+{
+    if (!cp || !cp->alloc_arena || !cp->free_arena || !cp->copy || !cp->wait || !cp->release)
+        return K3MOE_EINVAL;
+    return cache_init(out, capacity_bytes, expert_bytes, host_blobs, n_layers, n_experts, cp,
+                      false);
+}
+
+int k3moe_cache_destroy(k3moe_cache *C)
+{
+    if (!C) return K3MOE_EINVAL;
+    if (C->cuda && C->cuda->side) cudaStreamSynchronize(C->cuda->side);
+    cache_free(C);
+    return K3MOE_OK;
+}
+
+int k3moe_cache_acquire(k3moe_cache *C, const int64_t *keys, int32_t n, void **blobs_out,
+                        uint8_t *hit_out, k3moe_stream compute)
+{
+    if (!C || !keys || !blobs_out || n <= 0) return K3MOE_EINVAL;
+    for (int32_t i = 0; i < n; i++)
+        if (keys[i] < 0 || keys[i] >= C->nkeys) return K3MOE_EINVAL;
+    if (C->cuda) C->cuda->compute = reinterpret_cast<cudaStream_t>(compute);
+
+    // plan: hits, then one distinct victim per distinct missing key
+    std::vector<char> taken(C->slots, 0);
+    std::vector<int32_t> slot_of(n, -1);
+    std::vector<char> is_hit(n, 0);
+    for (int32_t i = 0; i < n; i++) {
+        const int32_t s = C->where[keys[i]];
+        if (s >= 0) {
+            slot_of[i] = s;
+            is_hit[i] = 1;
+            taken[s] = 1;
+        }
+    }
+    std::vector<int32_t> victims;
+    for (int32_t i = 0; i < n; i++) {
+        if (slot_of[i] >= 0) continue;
+        int32_t dup = -1;
+        for (int32_t q = 0; q < i; q++)
+            if (keys[q] == keys[i] && slot_of[q] >= 0) { dup = slot_of[q]; break; }
+        if (dup >= 0) {
+            slot_of[i] = dup;
+            is_hit[i] = 1;  // a repeated key is a hit the second time
+            continue;
+        }
+        const int32_t v = pick_victim(C, taken);
+        if (v < 0) return K3MOE_EBUSY;  // nothing committed yet
+        taken[v] = 1;
+        slot_of[i] = v;
+        victims.push_back(i);
+    }
+
+    // commit: recency and use marks for every slot of the batch
+    for (int32_t i = 0; i < n; i++) {
+        C->hist[keys[i]]++;
+        const int32_t s = slot_of[i];
+        C->last[s] = C->now;
+        if (!C->in_use[s]) C->used.push_back(s);
+        C->in_use[s] = 1;
+    }
+    for (int32_t i : victims) {
+        const int32_t s = slot_of[i];
+        if (C->key[s] >= 0) {
+            C->where[C->key[s]] = -1;
+            C->st.evictions++;
+        }
+        C->key[s] = kInflight;
+    }
+    int rc = K3MOE_OK;
+    for (int32_t i : victims) {
+        const int32_t s = slot_of[i];
+        int r = C->cp.copy(C->cp.ctx, s, C->arena + (size_t)s * C->expert_bytes, C->host[keys[i]],
+                           C->expert_bytes);
+        if (r != K3MOE_OK) {
+            C->key[s] = kEmpty;
+            if (rc == K3MOE_OK) rc = r;
+            continue;
+        }
+        C->st.h2d_bytes += (int64_t)C->expert_bytes;
+    }
+    for (int32_t i : victims) {
+        const int32_t s = slot_of[i];
+        if (C->key[s] != kInflight) continue;
+        int r = C->cp.wait(C->cp.ctx, s);
+        if (r != K3MOE_OK) {
+            C->key[s] = kEmpty;
+            if (rc == K3MOE_OK) rc = r;
+            continue;
+        }
+        C->key[s] = keys[i];
+        C->where[keys[i]] = s;
+    }
+    for (int32_t i = 0; i < n; i++) {
+        blobs_out[i] = C->arena + (size_t)slot_of[i] * C->expert_bytes;
+        if (hit_out) hit_out[i] = is_hit[i];
+    }
+    int64_t nh = 0;
+    for (int32_t i = 0; i < n; i++) nh += is_hit[i];
+    C->st.lookups += n;
+    C->st.hits += nh;
+    C->st.misses += n - nh;
+    C->st.hbm_bytes += (int64_t)n * (int64_t)C->expert_bytes;
+    C->now++;
+    return rc;
+}
+
+int k3moe_cache_release(k3moe_cache *C, k3moe_stream compute)
+{
+    if (!C) return K3MOE_EINVAL;
+    if (C->cuda) C->cuda->compute = reinterpret_cast<cudaStream_t>(compute);
+    int rc = K3MOE_OK;
+    for (int32_t s : C->used) {
+        int r = C->cp.release(C->cp.ctx, s);
+        if (r != K3MOE_OK && rc == K3MOE_OK) rc = r;
+        C->in_use[s] = 0;
+    }
+    C->used.clear();
+    return rc;
+}
+
+int k3moe_cache_pin(k3moe_cache *C, int64_t key, k3moe_stream compute)
+{
+    if (!C || key < 0 || key >= C->nkeys) return K3MOE_EINVAL;
+    void *blob = nullptr;
+    // pinning is not a request: keep the request counters as they were
+    const k3moe_cache_stats before = C->st;
+    const uint32_t h = C->hist[key];
+    int rc = k3moe_cache_acquire(C, &key, 1, &blob, nullptr, compute);
+    C->st.lookups = before.lookups;
+    C->st.hits = before.hits;
+    C->st.misses = before.misses;
+    C->st.hbm_bytes = before.hbm_bytes;
+    C->hist[key] = h;
+    if (rc != K3MOE_OK) return rc;
+    const int32_t s = C->where[key];
+    if (s >= 0 && !C->pin[s]) {
+        C->pin[s] = 1;
+        C->st.pinned++;
+    }
+    return k3moe_cache_release(C, compute);
+}
+
+int k3moe_cache_get_stats(k3moe_cache *C, k3moe_cache_stats *out)
+{
+    if (!C || !out) return K3MOE_EINVAL;
+    *out = C->st;
+    int32_t inflight = 0;
+    for (int32_t s = 0; s < C->slots; s++) inflight += (C->key[s] == kInflight);
+    out->inflight = inflight;
+    return K3MOE_OK;
+}
+
+const uint32_t *k3moe_cache_histogram(const k3moe_cache *C) { return C ? C->hist.data() : nullptr; }
+
+int32_t k3moe_cache_slot_of(const k3moe_cache *C, int64_t key)
+{
+    if (!C || key < 0 || key >= C->nkeys) return -1;
+    return C->where[key];
+}
+
+}  // extern "C"

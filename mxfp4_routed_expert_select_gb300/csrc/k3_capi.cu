@@ -1,0 +1,434 @@
+// k3_capi.cu -- the extern "C" entry points of k3moe.h: argument checks,
+// library-owned layer scratch, and the launch sequence of each call.
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "k3_device.cuh"
+
+namespace k3 {
+int num_sms();
+
+// One zero-initialised int per device for errors found on the device.
+int *device_error_word()
+{
+    static int *words[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (!words[dev]) {
+        int *p = nullptr;
+        if (cudaMalloc(&p, sizeof(int)) != cudaSuccess || cudaMemset(p, 0, sizeof(int)) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        words[dev] = p;
+    }
+    return words[dev];
+}
+int launch_rows_t1(int mode, const float *x, const ExpertSrc &src, int k, int in, int rows,
+                   float *out, cudaStream_t s);
+int launch_down_t1(const float *h, const ExpertSrc &src, const float *w, int k, int d, int f,
+                   float *out, cudaStream_t s);
+int launch_route_t1(const void *x, int xdt, const uint16_t *Wr, int E, int d, float *logits,
+                    const float *bias, int k, int32_t *ids, float *w, unsigned *ticket,
+                    cudaStream_t s);
+int route_multi_nsplit(int T, int E, int d);
+int launch_route_multi(const void *X, int xdt, int T, const uint16_t *Wr, int E, int d,
+                       float *part, int nsplit, float *logits, const float *bias, int k,
+                       int32_t *ids, float *w, cudaStream_t s);
+int launch_group(const int32_t *ids, int npairs, int E, int nt, int32_t *offsets, int32_t *perm,
+                 int4 *items, int32_t *n_items, cudaStream_t s);
+int grouped_nt();
+int launch_grouped_gateup(const void *X, int xdt, const DevExpert *table, const int32_t *perm,
+                          const int4 *items, const int32_t *n_items, int max_items, int k, int d,
+                          int f, float *h, cudaStream_t s);
+int launch_grouped_down(const float *h, const DevExpert *table, const int32_t *perm,
+                        const int4 *items, const int32_t *n_items, int max_items, int k, int d,
+                        int f, const float *wsel, float *Y, cudaStream_t s);
+int launch_combine(const float *Y, int T, int k, int d, float *out, cudaStream_t s);
+int launch_rmsnorm(float *u, const float *x, int n, float eps, cudaStream_t s);
+int launch_residual(float *x, const float *dlt, int n, cudaStream_t s);
+}  // namespace k3
+
+using k3::DevExpert;
+using k3::ExpertSrc;
+
+#define K3_TRY(expr)                 \
+    do {                             \
+        int _st = (expr);            \
+        if (_st != K3MOE_OK) return _st; \
+    } while (0)
+#define K3_CUDA(expr)                                     \
+    do {                                                  \
+        if ((expr) != cudaSuccess) {                      \
+            cudaGetLastError();                           \
+            return K3MOE_ECUDA;                           \
+        }                                                 \
+    } while (0)
+
+static inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+static inline cudaStream_t cs(k3moe_stream s) { return reinterpret_cast<cudaStream_t>(s); }
+
+static bool valid_dims(int32_t d, int32_t f)
+{
+    return d > 0 && f > 0 && d % 32 == 0 && f % 32 == 0 && d <= 16384 && f <= 2048;
+}
+
+static bool valid_mat(const k3moe_mat &m, int rows, int in)
+{
+    return m.packed && m.scales && aligned16(m.packed) && aligned16(m.scales) && m.rows == rows &&
+           m.in == in;
+}
+
+static bool valid_expert(const k3moe_expert &e, int d, int f)
+{
+    return valid_mat(e.gate, f, d) && valid_mat(e.up, f, d) && valid_mat(e.down, d, f);
+}
+
+static DevExpert to_dev(const k3moe_expert &e)
+{
+    DevExpert x;
+    x.gp = e.gate.packed;
+    x.gs = e.gate.scales;
+    x.up = e.up.packed;
+    x.us = e.up.scales;
+    x.dp = e.down.packed;
+    x.ds = e.down.scales;
+    return x;
+}
+
+extern "C" {
+
+const char *k3moe_strerror(int st)
+{
+    switch (st) {
+    case K3MOE_OK: return "ok";
+    case K3MOE_EINVAL: return "invalid argument";
+    case K3MOE_ENOMEM: return "out of memory";
+    case K3MOE_ECUDA: return "CUDA runtime error";
+    case K3MOE_ETIMEOUT: return "bounded wait timed out";
+    case K3MOE_EBUSY: return "no evictable cache slot";
+    case K3MOE_ENODEV: return "no usable device";
+    default: return "unknown status";
+    }
+}
+
+int k3moe_version(void) { return (1 << 16) | 0; }
+
+int k3moe_device_error(void)
+{
+    int *word = k3::device_error_word();
+    if (!word) return K3MOE_ECUDA;
+    int v = 0;
+    K3_CUDA(cudaDeviceSynchronize());
+    K3_CUDA(cudaMemcpy(&v, word, sizeof(int), cudaMemcpyDeviceToHost));
+    K3_CUDA(cudaMemset(word, 0, sizeof(int)));
+    return v;
+}
+
+int64_t k3moe_matrix_bytes(int32_t rows, int32_t in)
+{
+    if (rows <= 0 || in <= 0 || in % 32) return -1;
+    return (int64_t)rows * (in / 2 + in / 32);
+}
+
+int64_t k3moe_expert_bytes(int32_t d, int32_t f)
+{
+    if (d <= 0 || f <= 0 || d % 32 || f % 32) return -1;
+    return 2 * k3moe_matrix_bytes(f, d) + k3moe_matrix_bytes(d, f);
+}
+
+int k3moe_expert_view(k3moe_expert *out, const void *blob, int32_t d, int32_t f)
+{
+    if (!out || !blob || d <= 0 || f <= 0 || d % 32 || f % 32 || !aligned16(blob))
+        return K3MOE_EINVAL;
+    const uint8_t *b = (const uint8_t *)blob;
+    const size_t gpB = (size_t)f * d / 2, gsB = (size_t)f * d / 32;
+    const size_t dpB = (size_t)d * f / 2;
+    out->gate = {b, b + gpB, f, d};
+    b += gpB + gsB;
+    out->up = {b, b + gpB, f, d};
+    b += gpB + gsB;
+    out->down = {b, b + dpB, d, f};
+    return K3MOE_OK;
+}
+
+int k3moe_pack_expert(void *blob, const uint8_t *gp, const uint8_t *gs, const uint8_t *up,
+                      const uint8_t *us, const uint8_t *dp, const uint8_t *ds, int32_t d,
+                      int32_t f, k3moe_stream s)
+{
+    k3moe_expert v;
+    K3_TRY(k3moe_expert_view(&v, blob, d, f));
+    if (!gp || !gs || !up || !us || !dp || !ds) return K3MOE_EINVAL;
+    const size_t pB = (size_t)f * d / 2, sB = (size_t)f * d / 32;
+    K3_CUDA(cudaMemcpyAsync((void *)v.gate.packed, gp, pB, cudaMemcpyDefault, cs(s)));
+    K3_CUDA(cudaMemcpyAsync((void *)v.gate.scales, gs, sB, cudaMemcpyDefault, cs(s)));
+    K3_CUDA(cudaMemcpyAsync((void *)v.up.packed, up, pB, cudaMemcpyDefault, cs(s)));
+    K3_CUDA(cudaMemcpyAsync((void *)v.up.scales, us, sB, cudaMemcpyDefault, cs(s)));
+    K3_CUDA(cudaMemcpyAsync((void *)v.down.packed, dp, pB, cudaMemcpyDefault, cs(s)));
+    K3_CUDA(cudaMemcpyAsync((void *)v.down.scales, ds, sB, cudaMemcpyDefault, cs(s)));
+    return K3MOE_OK;
+}
+
+int k3moe_matmul_mxfp4(float *y, const float *x, const k3moe_mat *W, k3moe_stream s)
+{
+    if (!y || !x || !W || !W->packed || !W->scales) return K3MOE_EINVAL;
+    if (W->rows <= 0 || W->in <= 0 || W->in % 32 || W->in > 16384) return K3MOE_EINVAL;
+    if (!aligned16(y) || !aligned16(x) || !aligned16(W->packed) || !aligned16(W->scales))
+        return K3MOE_EINVAL;
+    ExpertSrc src;
+    memset(&src, 0, sizeof(src));
+    src.inl[0].gp = W->packed;
+    src.inl[0].gs = W->scales;
+    return k3::launch_rows_t1(0, x, src, 1, W->in, W->rows, y, cs(s));
+}
+
+size_t k3moe_expert_gemv_workspace(int32_t d, int32_t f)
+{
+    if (!valid_dims(d, f)) return 0;
+    return (size_t)f * sizeof(float);
+}
+
+int k3moe_expert_gemv(float *y, const float *x, const k3moe_expert *e, int32_t d, int32_t f,
+                      void *ws, size_t ws_bytes, k3moe_stream s)
+{
+    if (!y || !x || !e || !ws || !valid_dims(d, f) || !valid_expert(*e, d, f)) return K3MOE_EINVAL;
+    if (!aligned16(y) || !aligned16(x) || !aligned16(ws) ||
+        ws_bytes < k3moe_expert_gemv_workspace(d, f))
+        return K3MOE_EINVAL;
+    ExpertSrc src;
+    memset(&src, 0, sizeof(src));
+    src.inl[0] = to_dev(*e);
+    float *h = (float *)ws;
+    K3_TRY(k3::launch_rows_t1(1, x, src, 1, d, f, h, cs(s)));
+    return k3::launch_down_t1(h, src, nullptr, 1, d, f, y, cs(s));
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ layer
+
+struct k3moe_layer {
+    int E, k, d, f, maxT;
+    const uint16_t *Wr;
+    const float *bias;
+    DevExpert *table;    // [E]
+    float *logits;       // [maxT * E]
+    float *part;         // [nsplit * maxT * E]
+    int nsplit;
+    int32_t *ids;        // [maxT * k]
+    float *w;            // [maxT * k]
+    float *h;            // [maxT * k * f]
+    float *Y;            // [maxT * k * d]  (T > 1)
+    int32_t *offsets;    // [E + 1]
+    int32_t *perm;       // [maxT * k]
+    int4 *items;         // [maxT * k]
+    int32_t *n_items;    // [1]
+    unsigned *ticket;    // [1]
+    cudaEvent_t ev[4];   // optional timing events (caller-owned)
+    int nev;
+    bool router_only;    // created without a resident expert table
+};
+
+static void layer_free(k3moe_layer *L)
+{
+    if (!L) return;
+    void *ptrs[] = {L->table, L->logits, L->part, L->ids,     L->w,       L->h,
+                    L->Y,     L->offsets, L->perm, L->items, L->n_items, L->ticket};
+    for (void *p : ptrs)
+        if (p) cudaFree(p);
+    delete L;
+}
+
+extern "C" {
+
+int k3moe_layer_create(k3moe_layer **out, const k3moe_layer_desc *D)
+{
+    if (!out || !D) return K3MOE_EINVAL;
+    *out = nullptr;
+    if (D->n_experts <= 0 || D->top_k <= 0 || D->top_k > 16 || D->top_k > D->n_experts ||
+        !valid_dims(D->d, D->f) || !D->router_w || D->max_tokens <= 0 ||
+        !aligned16(D->router_w) || (D->sel_bias && ((uintptr_t)D->sel_bias & 3u)))
+        return K3MOE_EINVAL;
+    if (D->host_experts)
+        for (int e = 0; e < D->n_experts; e++)
+            if (!valid_expert(D->host_experts[e], D->d, D->f)) return K3MOE_EINVAL;
+    k3moe_layer *L = new (std::nothrow) k3moe_layer;
+    if (!L) return K3MOE_ENOMEM;
+    memset(L, 0, sizeof(*L));
+    L->E = D->n_experts;
+    L->k = D->top_k;
+    L->d = D->d;
+    L->f = D->f;
+    L->maxT = D->max_tokens;
+    L->Wr = D->router_w;
+    L->bias = D->sel_bias;
+    L->nsplit = k3::route_multi_nsplit(L->maxT, L->E, L->d);
+    const size_t pairs = (size_t)L->maxT * L->k;
+    bool ok = true;
+    auto alloc = [&](void **p, size_t bytes) {
+        if (ok && cudaMalloc(p, bytes ? bytes : 16) != cudaSuccess) {
+            cudaGetLastError();
+            ok = false;
+        }
+    };
+    alloc((void **)&L->table, sizeof(DevExpert) * L->E);
+    alloc((void **)&L->logits, sizeof(float) * L->maxT * L->E);
+    alloc((void **)&L->part, sizeof(float) * L->nsplit * (size_t)L->maxT * L->E);
+    alloc((void **)&L->ids, sizeof(int32_t) * pairs);
+    alloc((void **)&L->w, sizeof(float) * pairs);
+    alloc((void **)&L->h, sizeof(float) * pairs * L->f);
+    alloc((void **)&L->Y, sizeof(float) * pairs * L->d);
+    alloc((void **)&L->offsets, sizeof(int32_t) * (L->E + 1));
+    alloc((void **)&L->perm, sizeof(int32_t) * pairs);
+    alloc((void **)&L->items, sizeof(int4) * pairs);
+    alloc((void **)&L->n_items, sizeof(int32_t));
+    alloc((void **)&L->ticket, sizeof(unsigned));
+    if (!ok) {
+        layer_free(L);
+        return K3MOE_ENOMEM;
+    }
+    DevExpert *tmp = (DevExpert *)malloc(sizeof(DevExpert) * L->E);
+    if (!tmp) {
+        layer_free(L);
+        return K3MOE_ENOMEM;
+    }
+    for (int e = 0; e < L->E; e++) {
+        if (D->host_experts)
+            tmp[e] = to_dev(D->host_experts[e]);
+        else
+            memset(&tmp[e], 0, sizeof(DevExpert));
+    }
+    L->router_only = D->host_experts == nullptr;
+    cudaError_t st = cudaMemcpy(L->table, tmp, sizeof(DevExpert) * L->E, cudaMemcpyHostToDevice);
+    free(tmp);
+    if (st == cudaSuccess) st = cudaMemset(L->ticket, 0, sizeof(unsigned));
+    if (st != cudaSuccess) {
+        cudaGetLastError();
+        layer_free(L);
+        return K3MOE_ECUDA;
+    }
+    *out = L;
+    return K3MOE_OK;
+}
+
+int k3moe_layer_destroy(k3moe_layer *L)
+{
+    if (!L) return K3MOE_EINVAL;
+    layer_free(L);
+    return K3MOE_OK;
+}
+
+static int route_into(k3moe_layer *L, const void *X, int xdt, int32_t T, cudaStream_t s)
+{
+    if (T == 1)
+        return k3::launch_route_t1(X, xdt, L->Wr, L->E, L->d, L->logits, L->bias, L->k, L->ids,
+                                   L->w, L->ticket, s);
+    return k3::launch_route_multi(X, xdt, T, L->Wr, L->E, L->d, L->part, L->nsplit, L->logits,
+                                  L->bias, L->k, L->ids, L->w, s);
+}
+
+static bool valid_call(k3moe_layer *L, const void *X, int xdt, int32_t T)
+{
+    return L && X && aligned16(X) && (xdt == K3MOE_F32 || xdt == K3MOE_BF16) && T >= 1 &&
+           T <= L->maxT;
+}
+
+int k3moe_layer_route(k3moe_layer *L, const void *X, int xdt, int32_t T, int32_t *ids, float *w,
+                      k3moe_stream s)
+{
+    if (!valid_call(L, X, xdt, T) || !ids || !w) return K3MOE_EINVAL;
+    K3_TRY(route_into(L, X, xdt, T, cs(s)));
+    K3_CUDA(cudaMemcpyAsync(ids, L->ids, sizeof(int32_t) * T * L->k, cudaMemcpyDeviceToDevice,
+                            cs(s)));
+    K3_CUDA(cudaMemcpyAsync(w, L->w, sizeof(float) * T * L->k, cudaMemcpyDeviceToDevice, cs(s)));
+    return K3MOE_OK;
+}
+
+int k3moe_layer_forward(k3moe_layer *L, const void *X, int xdt, int32_t T, float *out,
+                        int32_t *ids_out, float *w_out, k3moe_stream s)
+{
+    if (!valid_call(L, X, xdt, T) || !out || !aligned16(out) || L->router_only)
+        return K3MOE_EINVAL;
+    cudaStream_t st = cs(s);
+    if (L->nev) K3_CUDA(cudaEventRecord(L->ev[0], st));
+    K3_TRY(route_into(L, X, xdt, T, st));
+    if (L->nev) K3_CUDA(cudaEventRecord(L->ev[1], st));
+    if (T == 1 && xdt == K3MOE_F32) {
+        ExpertSrc src;
+        memset(&src, 0, sizeof(src));
+        src.table = L->table;
+        src.ids = L->ids;
+        K3_TRY(k3::launch_rows_t1(1, (const float *)X, src, L->k, L->d, L->f, L->h, st));
+        if (L->nev) K3_CUDA(cudaEventRecord(L->ev[2], st));
+        K3_TRY(k3::launch_down_t1(L->h, src, L->w, L->k, L->d, L->f, out, st));
+    } else {
+        const int npairs = T * L->k;
+        K3_TRY(k3::launch_group(L->ids, npairs, L->E, k3::grouped_nt(), L->offsets, L->perm,
+                                L->items, L->n_items, st));
+        K3_TRY(k3::launch_grouped_gateup(X, xdt, L->table, L->perm, L->items, L->n_items, npairs,
+                                         L->k, L->d, L->f, L->h, st));
+        if (L->nev) K3_CUDA(cudaEventRecord(L->ev[2], st));
+        K3_TRY(k3::launch_grouped_down(L->h, L->table, L->perm, L->items, L->n_items, npairs,
+                                       L->k, L->d, L->f, L->w, L->Y, st));
+        K3_TRY(k3::launch_combine(L->Y, T, L->k, L->d, out, st));
+    }
+    if (L->nev) K3_CUDA(cudaEventRecord(L->ev[3], st));
+    if (ids_out)
+        K3_CUDA(cudaMemcpyAsync(ids_out, L->ids, sizeof(int32_t) * T * L->k,
+                                cudaMemcpyDeviceToDevice, st));
+    if (w_out)
+        K3_CUDA(cudaMemcpyAsync(w_out, L->w, sizeof(float) * T * L->k, cudaMemcpyDeviceToDevice,
+                                st));
+    return K3MOE_OK;
+}
+
+int k3moe_layer_set_events(k3moe_layer *L, void *const *host_events, int32_t n)
+{
+    if (!L || n < 0 || (n > 0 && (n < 4 || !host_events))) return K3MOE_EINVAL;
+    L->nev = n ? 4 : 0;
+    for (int i = 0; i < L->nev; i++) {
+        if (!host_events[i]) {
+            L->nev = 0;
+            return K3MOE_EINVAL;
+        }
+        L->ev[i] = (cudaEvent_t)host_events[i];
+    }
+    return K3MOE_OK;
+}
+
+int k3moe_layer_experts_t1(k3moe_layer *L, const float *x, const k3moe_expert *sel,
+                           const float *w, int32_t k, float *out, k3moe_stream s)
+{
+    if (!L || !x || !sel || !w || !out || k < 1 || k > k3::kMaxInline || k > L->k)
+        return K3MOE_EINVAL;
+    if (!aligned16(x) || !aligned16(out)) return K3MOE_EINVAL;
+    ExpertSrc src;
+    memset(&src, 0, sizeof(src));
+    for (int j = 0; j < k; j++) {
+        if (!valid_expert(sel[j], L->d, L->f)) return K3MOE_EINVAL;
+        src.inl[j] = to_dev(sel[j]);
+    }
+    K3_TRY(k3::launch_rows_t1(1, x, src, k, L->d, L->f, L->h, cs(s)));
+    return k3::launch_down_t1(L->h, src, w, k, L->d, L->f, out, cs(s));
+}
+
+int k3moe_rmsnorm(float *u, const float *x, int32_t n, float eps, k3moe_stream s)
+{
+    if (!u || !x || n <= 0 || !(eps >= 0.f)) return K3MOE_EINVAL;
+    return k3::launch_rmsnorm(u, x, n, eps, cs(s));
+}
+
+int k3moe_residual_add(float *x, const float *delta, int32_t n, k3moe_stream s)
+{
+    if (!x || !delta || n <= 0) return K3MOE_EINVAL;
+    return k3::launch_residual(x, delta, n, cs(s));
+}
+
+}  // extern "C"

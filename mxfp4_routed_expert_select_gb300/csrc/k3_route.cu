@@ -1,0 +1,322 @@
+// k3_route.cu -- router logits, top-k selection with softmax combine weights,
+// and grouping of (token, slot) pairs by expert (sm_103a).
+//
+// Router: logits[t][e] = sum_i W_r[e][i] x[t][i], W_r bf16, fp32 accumulate.
+// Selection: the top_k largest (logit + sel_bias), ties to the lower id; the
+// combine weights are the softmax of the UNBIASED logits over the chosen set
+// ("Running Kimi K3 locally", "How is the C engine actually built?",
+// invariant 3).  ids are written in ascending order.
+#include "k3_device.cuh"
+
+namespace k3 {
+
+int num_sms();
+
+// Selection key: larger is better; ties broken toward the lower id.
+K3_DEV bool better(float a, int ia, float b, int ib) { return a > b || (a == b && ia < ib); }
+
+// One warp selects the top k (k <= 32) of E scores for one token.
+// logit: unbiased logits [E] (any memory space readable by ld.cg),
+// bias: [E] or null.  Writes ids ascending and softmax weights.
+K3_DEV void warp_topk(const float *logit, const float *bias, int E, int k, int32_t *ids_out,
+                      float *w_out, int lane)
+{
+    // each lane scans its strided slice; chosen elements are marked by
+    // remembering the last selected (score, id) and skipping anything that
+    // ranks at or above it.
+    float last_s = INFINITY;
+    int last_i = -1;
+    int my_id = -1;
+    for (int r = 0; r < k; r++) {
+        float bs = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int e = lane; e < E; e += 32) {
+            float sc = __ldcg(logit + e) + (bias ? __ldg(bias + e) : 0.f);
+            // candidates rank strictly below the previously chosen one
+            bool below = (last_i < 0) || better(last_s, last_i, sc, e);
+            if (below && better(sc, e, bs, bi)) { bs = sc; bi = e; }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            float os = __shfl_xor_sync(0xffffffffu, bs, off);
+            int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (better(os, oi, bs, bi)) { bs = os; bi = oi; }
+        }
+        last_s = bs;
+        last_i = bi;
+        if (lane == r) my_id = bi;
+    }
+    // ascending ids: rank of my id among the k chosen
+    int pos = 0;
+    for (int q = 0; q < k; q++) {
+        int other = __shfl_sync(0xffffffffu, my_id, q);
+        if (lane < k && other < my_id) pos++;
+    }
+    float l = (lane < k) ? __ldcg(logit + my_id) : -INFINITY;
+    float mx = l;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float ex = (lane < k) ? expf(l - mx) : 0.f;
+    float sum = warp_sum(ex);
+    if (lane < k) {
+        ids_out[pos] = my_id;
+        w_out[pos] = ex / sum;
+    }
+}
+
+// ------------------------------------------------------- batch-1 router
+// One warp per expert row: 16-byte loads of 8 bf16 weights, x read through
+// L1.  The last CTA to finish (ticket counter, no waiting) runs the top-k.
+template <typename XT>
+K3_DEV void load_x8(const XT *x, int i, float (&xv)[8]);
+template <>
+K3_DEV void load_x8<float>(const float *x, int i, float (&xv)[8])
+{
+    float4 a = __ldg(reinterpret_cast<const float4 *>(x + i));
+    float4 b = __ldg(reinterpret_cast<const float4 *>(x + i + 4));
+    xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
+    xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
+}
+template <>
+K3_DEV void load_x8<__nv_bfloat16>(const __nv_bfloat16 *x, int i, float (&xv)[8])
+{
+    uint4 a = __ldg(reinterpret_cast<const uint4 *>(x + i));
+    uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        xv[2 * q] = __uint_as_float(w[q] << 16);
+        xv[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+    }
+}
+
+K3_DEV float bf16x8_dot(uint4 wv, const float (&xv)[8], float acc)
+{
+    uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        acc = fmaf(__uint_as_float(w[q] << 16), xv[2 * q], acc);
+        acc = fmaf(__uint_as_float(w[q] & 0xffff0000u), xv[2 * q + 1], acc);
+    }
+    return acc;
+}
+
+template <typename XT>
+__global__ void __launch_bounds__(256) k3_router_t1(const XT *__restrict__ x,
+                                                    const uint16_t *__restrict__ Wr, int E, int d,
+                                                    float *logits, const float *bias, int k,
+                                                    int32_t *ids, float *w, unsigned *ticket)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int e = blockIdx.x * (blockDim.x >> 5) + warp;
+    if (e < E) {
+        const uint16_t *row = Wr + (size_t)e * d;
+        float acc0 = 0.f, acc1 = 0.f;
+        const int nchunk = d >> 3;
+        int c = lane;
+        for (; c + 32 < nchunk; c += 64) {
+            uint4 w0 = ld_stream16(row + 8 * c);
+            uint4 w1 = ld_stream16(row + 8 * (c + 32));
+            float x0[8], x1[8];
+            load_x8<XT>(x, 8 * c, x0);
+            load_x8<XT>(x, 8 * (c + 32), x1);
+            acc0 = bf16x8_dot(w0, x0, acc0);
+            acc1 = bf16x8_dot(w1, x1, acc1);
+        }
+        for (; c < nchunk; c += 32) {
+            uint4 w0 = ld_stream16(row + 8 * c);
+            float x0[8];
+            load_x8<XT>(x, 8 * c, x0);
+            acc0 = bf16x8_dot(w0, x0, acc0);
+        }
+        float acc = warp_sum(acc0 + acc1);
+        if (lane == 0) logits[e] = acc;
+    }
+    // last CTA does the selection
+    __shared__ unsigned s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (warp == 0) warp_topk(logits, bias, E, k, ids, w, lane);
+    if (threadIdx.x == 0) *ticket = 0;  // ready for the next launch on this stream
+}
+
+// ------------------------------------------------- multi-token router
+// Tiled SGEMM: logits[T][E] (split-K partials, summed in fixed order by the
+// top-k kernel).  CTA tile: 64 experts x 64 tokens, K step 32, 256 threads,
+// each thread 4 x 4 outputs.
+constexpr int RT_E = 64, RT_T = 64, RT_K = 32;
+
+template <typename XT>
+K3_DEV float to_f(XT v);
+template <>
+K3_DEV float to_f<float>(float v) { return v; }
+template <>
+K3_DEV float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename XT>
+__global__ void __launch_bounds__(256) k3_router_tiled(const XT *__restrict__ X, int T,
+                                                       const uint16_t *__restrict__ Wr, int E,
+                                                       int d, int ksplit_len,
+                                                       float *__restrict__ part)
+{
+    __shared__ float sW[RT_K][RT_E + 4];
+    __shared__ float sX[RT_K][RT_T + 4];
+    const int e0 = blockIdx.x * RT_E, t0 = blockIdx.y * RT_T;
+    const int kbeg = blockIdx.z * ksplit_len;
+    const int kend = min(kbeg + ksplit_len, d);
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    float acc[4][4] = {};
+    for (int kk = kbeg; kk < kend; kk += RT_K) {
+        for (int idx = threadIdx.x; idx < RT_K * RT_E; idx += 256) {
+            const int ee = idx / RT_K, kc = idx % RT_K;
+            const int e = e0 + ee, kx = kk + kc;
+            float v = 0.f;
+            if (e < E && kx < kend) v = __uint_as_float((uint32_t)Wr[(size_t)e * d + kx] << 16);
+            sW[kc][ee] = v;
+        }
+        for (int idx = threadIdx.x; idx < RT_K * RT_T; idx += 256) {
+            const int tt = idx / RT_K, kc = idx % RT_K;
+            const int t = t0 + tt, kx = kk + kc;
+            float v = 0.f;
+            if (t < T && kx < kend) v = to_f<XT>(X[(size_t)t * d + kx]);
+            sX[kc][tt] = v;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kc = 0; kc < RT_K; kc++) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) a[i] = sW[kc][ty * 4 + i];
+#pragma unroll
+            for (int i = 0; i < 4; i++) b[i] = sX[kc][tx * 4 + i];
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+#pragma unroll
+                for (int jx = 0; jx < 4; jx++) acc[i][jx] = fmaf(a[i], b[jx], acc[i][jx]);
+        }
+        __syncthreads();
+    }
+    float *p = part + (size_t)blockIdx.z * T * E;
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+#pragma unroll
+        for (int jx = 0; jx < 4; jx++) {
+            const int e = e0 + ty * 4 + i, t = t0 + tx * 4 + jx;
+            if (e < E && t < T) p[(size_t)t * E + e] = acc[i][jx];
+        }
+}
+
+// Sums split-K partials in fixed order, then selects per token (warp/token).
+__global__ void __launch_bounds__(256) k3_topk_multi(const float *__restrict__ part, int nsplit,
+                                                     int T, int E, const float *bias, int k,
+                                                     float *logits, int32_t *ids, float *w)
+{
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    float *lg = logits + (size_t)t * E;
+    for (int e = lane; e < E; e += 32) {
+        float s = 0.f;
+        for (int z = 0; z < nsplit; z++) s += part[((size_t)z * T + t) * E + e];
+        lg[e] = s;
+    }
+    __syncwarp();
+    warp_topk(lg, bias, E, k, ids + (size_t)t * k, w + (size_t)t * k, lane);
+}
+
+// ---------------------------------------------------------------- grouping
+// counts[E] -> offsets[E+1] (exclusive scan) -> perm[pairs] grouped by expert
+// (order inside a group is arbitrary; every pair's arithmetic is independent
+// of its position) -> a work list of (expert, first pair, n pairs) items of at
+// most `nt` pairs each.
+__global__ void __launch_bounds__(1024) k3_group(const int32_t *__restrict__ ids, int npairs,
+                                                 int E, int nt, int32_t *offsets, int32_t *perm,
+                                                 int4 *items, int32_t *n_items)
+{
+    extern __shared__ int32_t sh[];  // cnt[E], off[E+1], fill[E]
+    int32_t *cnt = sh, *off = sh + E, *fill = sh + 2 * E + 1;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) { cnt[e] = 0; fill[e] = 0; }
+    __syncthreads();
+    for (int p = threadIdx.x; p < npairs; p += blockDim.x) atomicAdd(&cnt[ids[p]], 1);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0, it = 0;
+        for (int e = 0; e < E; e++) {
+            off[e] = run;
+            for (int b = 0; b < cnt[e]; b += nt) {
+                items[it] = make_int4(e, run + b, min(nt, cnt[e] - b), 0);
+                it++;
+            }
+            run += cnt[e];
+        }
+        off[E] = run;
+        *n_items = it;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = off[e];
+    for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
+        const int e = ids[p];
+        const int slot = atomicAdd(&fill[e], 1);
+        perm[off[e] + slot] = p;
+    }
+}
+
+// ------------------------------------------------------------- launchers
+
+int launch_route_t1(const void *x, int xdt, const uint16_t *Wr, int E, int d, float *logits,
+                    const float *bias, int k, int32_t *ids, float *w, unsigned *ticket,
+                    cudaStream_t s)
+{
+    const int threads = 256, wpb = threads / 32;
+    const int grid = (E + wpb - 1) / wpb;
+    if (xdt == K3MOE_F32)
+        k3_router_t1<float><<<grid, threads, 0, s>>>((const float *)x, Wr, E, d, logits, bias, k,
+                                                     ids, w, ticket);
+    else
+        k3_router_t1<__nv_bfloat16><<<grid, threads, 0, s>>>((const __nv_bfloat16 *)x, Wr, E, d,
+                                                             logits, bias, k, ids, w, ticket);
+    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
+}
+
+int route_multi_nsplit(int T, int E, int d)
+{
+    const long tiles = (long)((E + RT_E - 1) / RT_E) * ((T + RT_T - 1) / RT_T);
+    long want = (2L * num_sms() + tiles - 1) / tiles;
+    int maxs = d / 256;
+    if (maxs < 1) maxs = 1;
+    if (want > maxs) want = maxs;
+    if (want < 1) want = 1;
+    return (int)want;
+}
+
+int launch_route_multi(const void *X, int xdt, int T, const uint16_t *Wr, int E, int d,
+                       float *part, int nsplit, float *logits, const float *bias, int k,
+                       int32_t *ids, float *w, cudaStream_t s)
+{
+    int klen = (d + nsplit - 1) / nsplit;
+    klen = (klen + RT_K - 1) / RT_K * RT_K;
+    const int ns = (d + klen - 1) / klen;
+    dim3 grid((E + RT_E - 1) / RT_E, (T + RT_T - 1) / RT_T, ns);
+    if (xdt == K3MOE_F32)
+        k3_router_tiled<float><<<grid, 256, 0, s>>>((const float *)X, T, Wr, E, d, klen, part);
+    else
+        k3_router_tiled<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16 *)X, T, Wr, E,
+                                                            d, klen, part);
+    k3_topk_multi<<<(T + 7) / 8, 256, 0, s>>>(part, ns, T, E, bias, k, logits, ids, w);
+    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
+}
+
+int launch_group(const int32_t *ids, int npairs, int E, int nt, int32_t *offsets, int32_t *perm,
+                 int4 *items, int32_t *n_items, cudaStream_t s)
+{
+    const size_t smem = (size_t)(3 * E + 1) * sizeof(int32_t);
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(k3_group, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    k3_group<<<1, 1024, smem, s>>>(ids, npairs, E, nt, offsets, perm, items, n_items);
+    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
+}
+
+}  // namespace k3

@@ -1,0 +1,164 @@
+"""GPU parity of the routed-expert layer (router, top-k, experts, combine)
+against the fp64 oracle: ids bit-exact on margin-checked tokens, combine
+weights and outputs within tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_helpers import (TOL, Pool, margin_subs, rel_err, router_tensor, tokens,
+                         tokens_device)
+from mxfp4_routed_expert_select_gb300 import k3moe as k
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(layer, X, T, K):
+    out = torch.empty((T, layer.d), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    layer.forward(X, T, out, ids, w)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
+
+
+def _check(pool, Wr_bits, bias, K, Xd, out, ids, w, sample=None, h_bf16=False):
+    T = Xd.shape[0]
+    lg = oracle.router_logits(Xd, Wr_bits)
+    rids, rw, m = oracle.topk(lg, K, None if bias is None else bias.astype(np.float64))
+    assert np.all(m >= 1e-3)
+    assert np.array_equal(ids, rids)
+    assert np.allclose(w, rw, rtol=2e-5, atol=1e-7)
+    rows = range(T) if sample is None else sample
+    for t in rows:
+        ref = oracle.combine(Xd[t:t + 1], rids[t:t + 1], rw[t:t + 1], pool.experts(rids[t]),
+                             pool.E, h_bf16)[0]
+        e = rel_err(out[t], ref)
+        assert e <= TOL, (t, e)
+
+
+# ------------------------------------------------------------ small layers
+
+@pytest.fixture(scope="module")
+def small():
+    E, K, d, f = 64, 8, 512, 256
+    pool = Pool(5, 0, E, d, f)
+    Wr_bits = synth.router_bf16(5, 0, E, d)
+    bias = synth.bias_normal(5, 0, E)
+    return pool, Wr_bits, bias, E, K, d, f
+
+
+@pytest.mark.parametrize("T,bf16,use_bias", [(1, False, False), (1, False, True), (1, True, False),
+                                             (3, False, False), (17, True, True),
+                                             (64, False, False)])
+def test_small_layer(small, T, bf16, use_bias):
+    pool, Wr_bits, bias, E, K, d, f = small
+    b = bias if use_bias else None
+    subs = margin_subs(5, T, d, Wr_bits, K, b, bf16=bf16)
+    Xd = tokens(5, np.arange(T), d, subs, bf16)
+    X = tokens_device(5, T, d, subs, bf16)
+    L = k.Layer(E, K, d, f, router_tensor(Wr_bits), pool.views,
+                None if b is None else torch.from_numpy(b).cuda(), max_tokens=max(T, 64))
+    out, ids, w = _run(L, X, T, K)
+    _check(pool, Wr_bits, b, K, Xd, out, ids, w)
+    L.close()
+
+
+def test_ties_go_to_lower_ids_and_bias_only_selects(small):
+    """W_r = 0: every logit is 0, the k lowest ids win with equal weights.
+    With a bias that favours the top ids, those are chosen, but the weights
+    stay the softmax of the (equal) unbiased logits."""
+    pool, Wr_bits, bias, E, K, d, f = small
+    zero = torch.zeros((E, d), dtype=torch.int16, device="cuda")
+    X = tokens_device(5, 1, d, [0])
+    L = k.Layer(E, K, d, f, zero, pool.views, max_tokens=1)
+    out, ids, w = _run(L, X, 1, K)
+    assert list(ids[0]) == list(range(K)) and np.allclose(w, 1.0 / K)
+    bb = torch.from_numpy(np.arange(E, dtype=np.float32)).cuda()
+    L2 = k.Layer(E, K, d, f, zero, pool.views, bb, max_tokens=1)
+    out, ids, w = _run(L2, X, 1, K)
+    assert list(ids[0]) == list(range(E - K, E)) and np.allclose(w, 1.0 / K)
+    L.close()
+    L2.close()
+
+
+def test_degenerate_top_k(small):
+    pool, Wr_bits, bias, E, K, d, f = small
+    for kk in (1, 16):
+        subs = margin_subs(5, 2, d, Wr_bits, kk)
+        Xd = tokens(5, np.arange(2), d, subs)
+        X = tokens_device(5, 2, d, subs)
+        L = k.Layer(E, kk, d, f, router_tensor(Wr_bits), pool.views, max_tokens=2)
+        for T in (1, 2):
+            out, ids, w = _run(L, X[:T].contiguous(), T, kk)
+            _check(pool, Wr_bits, None, kk, Xd[:T], out, ids, w)
+        L.close()
+
+
+def test_invalid_calls_are_refused(small):
+    pool, Wr_bits, bias, E, K, d, f = small
+    L = k.Layer(E, K, d, f, router_tensor(Wr_bits), pool.views, max_tokens=4)
+    X = tokens_device(5, 4, d, [0] * 4)
+    out = torch.empty((5, d), dtype=torch.float32, device="cuda")
+    for T in (0, 5):
+        with pytest.raises(k.K3Error) as ei:
+            L.forward(X, T, out)
+        assert ei.value.status == k.K3MOE_EINVAL
+    L.close()
+    with pytest.raises(k.K3Error):
+        k.Layer(E, E + 1, d, f, router_tensor(Wr_bits), pool.views)
+
+
+# ------------------------------------------------ full-size 896-expert layer
+
+D, F, E896, K16 = 7168, 1536, 896, 16
+
+
+@pytest.fixture(scope="module")
+def full():
+    pool = Pool(1, 0, E896, D, F)
+    Wr_bits = synth.router_bf16(1, 0, E896, D)
+    Wr = router_tensor(Wr_bits)
+    bias = synth.bias_normal(1, 0, E896)
+    L = k.Layer(E896, K16, D, F, Wr, pool.views, max_tokens=4096)
+    Lb = k.Layer(E896, K16, D, F, Wr, pool.views, torch.from_numpy(bias).cuda(), max_tokens=4096)
+    yield pool, Wr_bits, bias, L, Lb
+    L.close()
+    Lb.close()
+
+
+def test_full_decode_batch1(full):
+    """896 experts resident, x fp32, top-16, batch 1 (several tokens)."""
+    pool, Wr_bits, bias, L, Lb = full
+    T = 4
+    subs = margin_subs(1, T, D, Wr_bits, K16)
+    Xd = tokens(1, np.arange(T), D, subs)
+    X = tokens_device(1, T, D, subs)
+    for t in range(T):
+        out, ids, w = _run(L, X[t:t + 1].contiguous(), 1, K16)
+        _check(pool, Wr_bits, None, K16, Xd[t:t + 1], out, ids, w)
+
+
+def test_full_batched_decode_64(full):
+    """64 fp32 tokens grouped by expert; ids of all, outputs sampled."""
+    pool, Wr_bits, bias, L, Lb = full
+    T = 64
+    subs = margin_subs(1, T, D, Wr_bits, K16)
+    Xd = tokens(1, np.arange(T), D, subs)
+    X = tokens_device(1, T, D, subs)
+    out, ids, w = _run(L, X, T, K16)
+    _check(pool, Wr_bits, None, K16, Xd, out, ids, w, sample=[0, 1, 31, 62, 63])
+
+
+def test_full_prefill_4096_bf16_biased(full):
+    """4096 bf16 tokens with a per-expert selection bias ~ N(0,1)."""
+    pool, Wr_bits, bias, L, Lb = full
+    T = 4096
+    subs = margin_subs(1, T, D, Wr_bits, K16, bias, bf16=True)
+    Xd = tokens(1, np.arange(T), D, subs, bf16=True)
+    X = tokens_device(1, T, D, subs, bf16=True)
+    out, ids, w = _run(Lb, X, T, K16)
+    _check(pool, Wr_bits, bias, K16, Xd, out, ids, w, sample=[0, 1777, 4095])
+    counts = np.bincount(ids.ravel(), minlength=E896)
+    assert counts.max() > 3 * counts.mean()  # the bias makes loads uneven
