@@ -201,10 +201,36 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int x_dtype, int32_t T, f
                         int32_t *ids_out, float *w_out, k3moe_stream s);
 
 /*
+ * Layer options (value 0/1):
+ *  K3MOE_OPT_FUSED_T1  batch-1 fp32 forward runs as one persistent
+ *                      cooperative kernel (router, top-k, experts, combine)
+ *                      when the shape allows it (d % 1024 == 0, d <= 7168,
+ *                      f % 512 == 0, f <= 2048); default 1.  0 selects the
+ *                      three-kernel path.
+ *  K3MOE_OPT_ACT_F16   on the fused batch-1 path, round the activations of
+ *                      the expert products to f16 (11 significant bits, one
+ *                      power-of-two scale per 16 activations) and use one
+ *                      fp32-accumulating FMA per weight; default 0, which
+ *                      keeps each activation as an exact f16 hi + lo pair
+ *                      (two FMAs per weight, fp32-class products).  The
+ *                      rounding adds a relative error of order 2^-12 per
+ *                      activation; the router is fp32 either way.
+ * k3moe_layer_fused_t1 returns 1 when a batch-1 fp32 forward of this layer
+ * would run fused, else 0 (negative on error).  After a device-side timeout
+ * (k3moe_device_error() == K3MOE_ETIMEOUT) a layer must be recreated.
+ */
+#define K3MOE_OPT_FUSED_T1 1
+#define K3MOE_OPT_ACT_F16  2
+int k3moe_layer_set_option(k3moe_layer *L, int32_t option, int32_t value);
+int k3moe_layer_fused_t1(const k3moe_layer *L);
+
+/*
  * Timing hook: when set, every later k3moe_layer_forward records
  * host_events[0] on its stream before the first kernel, [1] after routing,
  * [2] after the gate/up products and [3] after the down products and combine
  * (cudaEvent_t handles, created and owned by the caller).  n = 0 clears it.
+ * On the fused batch-1 path the whole layer is one kernel: [1] and [2] are
+ * recorded together with [3] after it.
  */
 int k3moe_layer_set_events(k3moe_layer *L, void *const *host_events, int32_t n);
 

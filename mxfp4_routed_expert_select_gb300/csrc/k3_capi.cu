@@ -53,6 +53,10 @@ int launch_grouped_down(const float *h, const DevExpert *table, const int32_t *p
 int launch_combine(const float *Y, int T, int k, int d, float *out, cudaStream_t s);
 int launch_rmsnorm(float *u, const float *x, int n, float eps, cudaStream_t s);
 int launch_residual(float *x, const float *dlt, int n, cudaStream_t s);
+bool fused_t1_supported(int E, int k, int d, int f);
+int launch_fused_t1(const float *x, const uint16_t *Wr, const float *bias, const DevExpert *table,
+                    int E, int k, int d, int f, float *logits, int32_t *ids, float *w, float *h,
+                    float *Y, float *out, unsigned *gbar, bool act16, cudaStream_t s);
 }  // namespace k3
 
 using k3::DevExpert;
@@ -234,13 +238,16 @@ struct k3moe_layer {
     cudaEvent_t ev[4];   // optional timing events (caller-owned)
     int nev;
     bool router_only;    // created without a resident expert table
+    bool fused;          // K3MOE_OPT_FUSED_T1
+    bool act16;          // K3MOE_OPT_ACT_F16
+    unsigned *gbar;      // [2] grid-barrier counters of the fused kernel
 };
 
 static void layer_free(k3moe_layer *L)
 {
     if (!L) return;
-    void *ptrs[] = {L->table, L->logits, L->part, L->ids,     L->w,       L->h,
-                    L->Y,     L->offsets, L->perm, L->items, L->n_items, L->ticket};
+    void *ptrs[] = {L->table, L->logits, L->part,  L->ids,     L->w,      L->h,    L->Y,
+                    L->offsets, L->perm, L->items, L->n_items, L->ticket, L->gbar};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete L;
@@ -252,13 +259,14 @@ int k3moe_layer_create(k3moe_layer **out, const k3moe_layer_desc *D)
 {
     if (!out || !D) return K3MOE_EINVAL;
     *out = nullptr;
-    if (D->n_experts <= 0 || D->top_k <= 0 || D->top_k > 16 || D->top_k > D->n_experts ||
+    if (D->n_experts <= 0 || D->n_experts > 1024 || D->top_k <= 0 || D->top_k > 16 || D->top_k > D->n_experts ||
         !valid_dims(D->d, D->f) || !D->router_w || D->max_tokens <= 0 ||
         !aligned16(D->router_w) || (D->sel_bias && ((uintptr_t)D->sel_bias & 3u)))
         return K3MOE_EINVAL;
     if (D->host_experts)
         for (int e = 0; e < D->n_experts; e++)
             if (!valid_expert(D->host_experts[e], D->d, D->f)) return K3MOE_EINVAL;
+    if (!k3::device_error_word()) return K3MOE_ECUDA;  // allocate before any capture
     k3moe_layer *L = new (std::nothrow) k3moe_layer;
     if (!L) return K3MOE_ENOMEM;
     memset(L, 0, sizeof(*L));
@@ -290,6 +298,9 @@ int k3moe_layer_create(k3moe_layer **out, const k3moe_layer_desc *D)
     alloc((void **)&L->items, sizeof(int4) * pairs);
     alloc((void **)&L->n_items, sizeof(int32_t));
     alloc((void **)&L->ticket, sizeof(unsigned));
+    alloc((void **)&L->gbar, 2 * sizeof(unsigned));
+    L->fused = true;
+    L->act16 = false;
     if (!ok) {
         layer_free(L);
         return K3MOE_ENOMEM;
@@ -309,6 +320,7 @@ int k3moe_layer_create(k3moe_layer **out, const k3moe_layer_desc *D)
     cudaError_t st = cudaMemcpy(L->table, tmp, sizeof(DevExpert) * L->E, cudaMemcpyHostToDevice);
     free(tmp);
     if (st == cudaSuccess) st = cudaMemset(L->ticket, 0, sizeof(unsigned));
+    if (st == cudaSuccess) st = cudaMemset(L->gbar, 0, 2 * sizeof(unsigned));
     if (st != cudaSuccess) {
         cudaGetLastError();
         layer_free(L);
@@ -358,6 +370,23 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int xdt, int32_t T, float
         return K3MOE_EINVAL;
     cudaStream_t st = cs(s);
     if (L->nev) K3_CUDA(cudaEventRecord(L->ev[0], st));
+    if (T == 1 && xdt == K3MOE_F32 && k3moe_layer_fused_t1(L) == 1) {
+        K3_TRY(k3::launch_fused_t1((const float *)X, L->Wr, L->bias, L->table, L->E, L->k, L->d,
+                                   L->f, L->logits, L->ids, L->w, L->h, L->Y, out, L->gbar,
+                                   L->act16, st));
+        if (L->nev) {
+            K3_CUDA(cudaEventRecord(L->ev[1], st));
+            K3_CUDA(cudaEventRecord(L->ev[2], st));
+            K3_CUDA(cudaEventRecord(L->ev[3], st));
+        }
+        if (ids_out)
+            K3_CUDA(cudaMemcpyAsync(ids_out, L->ids, sizeof(int32_t) * L->k,
+                                    cudaMemcpyDeviceToDevice, st));
+        if (w_out)
+            K3_CUDA(cudaMemcpyAsync(w_out, L->w, sizeof(float) * L->k, cudaMemcpyDeviceToDevice,
+                                    st));
+        return K3MOE_OK;
+    }
     K3_TRY(route_into(L, X, xdt, T, st));
     if (L->nev) K3_CUDA(cudaEventRecord(L->ev[1], st));
     if (T == 1 && xdt == K3MOE_F32) {
@@ -387,6 +416,26 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int xdt, int32_t T, float
         K3_CUDA(cudaMemcpyAsync(w_out, L->w, sizeof(float) * T * L->k, cudaMemcpyDeviceToDevice,
                                 st));
     return K3MOE_OK;
+}
+
+int k3moe_layer_set_option(k3moe_layer *L, int32_t option, int32_t value)
+{
+    if (!L || (value != 0 && value != 1)) return K3MOE_EINVAL;
+    if (option == K3MOE_OPT_FUSED_T1) {
+        L->fused = value != 0;
+        return K3MOE_OK;
+    }
+    if (option == K3MOE_OPT_ACT_F16) {
+        L->act16 = value != 0;
+        return K3MOE_OK;
+    }
+    return K3MOE_EINVAL;
+}
+
+int k3moe_layer_fused_t1(const k3moe_layer *L)
+{
+    if (!L) return K3MOE_EINVAL;
+    return (L->fused && !L->router_only && k3::fused_t1_supported(L->E, L->k, L->d, L->f)) ? 1 : 0;
 }
 
 int k3moe_layer_set_events(k3moe_layer *L, void *const *host_events, int32_t n)

@@ -18,6 +18,13 @@
 
 namespace k3 {
 
+// Device error word (bounded waits that ran out write K3MOE_ETIMEOUT here);
+// one int per device, allocated by the host side (k3::device_error_word()).
+K3_DEV void set_device_error(int *err, int code)
+{
+    if (err) atomicCAS(err, 0, code);
+}
+
 // Device-side expert view: the six plane pointers of one expert.
 struct DevExpert {
     const uint8_t *gp, *gs, *up, *us, *dp, *ds;
@@ -107,6 +114,100 @@ K3_DEV float dot16(uint2 q, const float2 *x)
     return (a.x + a.y) + (b.x + b.y);
 }
 
+// ---------------------------------------------------------------------------
+// Split-activation decode (the hot path).  16 activations of one lane are
+// kept as f16 halves: x * 2^s = hi + lo with hi = f16(x * 2^s) and
+// lo = f16(x * 2^s - hi), 2^s chosen per 16 activations so that the largest
+// is in [2^9, 2^10) (all hi, lo normal in f16).  A weight decoded by
+// cvt.rn.f16x2.e2m1x2 is exact in f16, so both w * hi and w * lo are formed
+// exactly and accumulated in fp32 by the mixed-precision fma.rn.f32.f16, which
+// issues on the FMA pipe at full rate.  x is represented to ~2^-22 of its
+// group maximum, so the products match an fp32 dot product to within fp32
+// accumulation rounding.  Cost: 0.5 (decode) + 2 (FMA) instructions per
+// weight, all on the ALU/FMA pipes; converting decoded weights to fp32 goes
+// through the much slower f16 pipe instead.
+struct XHalf16 {
+    uint16_t hi[16];  // f16 bits of x * 2^s
+    uint16_t lo[16];
+    float inv;        // 2^-s
+};
+
+K3_DEV void split16(const float *v, XHalf16 &o)
+{
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; i++) m = fmaxf(m, fabsf(v[i]));
+    int s = 0;
+    if (m > 0.f && m < 3.0e38f) {
+        int ex = ((__float_as_uint(m) >> 23) & 0xff) - 127;  // floor(log2 m) for normal m
+        if (ex < -126) ex = -126;
+        s = 9 - ex;
+        if (s > 120) s = 120;
+        if (s < -120) s = -120;
+    }
+    const float sc = ldexpf(1.0f, s);
+    o.inv = ldexpf(1.0f, -s);
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+        const float a = v[i] * sc;
+        const __half ha = __float2half_rn(a);
+        const __half la = __float2half_rn(a - __half2float(ha));
+        o.hi[i] = __half_as_ushort(ha);
+        o.lo[i] = __half_as_ushort(la);
+    }
+}
+
+// acc += w * x with w, x f16 (exact product), fp32 accumulate.
+K3_DEV float mfma(uint16_t w, uint16_t x, float acc)
+{
+    asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc) : "h"(w), "h"(x));
+    return acc;
+}
+K3_DEV uint16_t lo16(uint32_t v) { return (uint16_t)(v & 0xffffu); }
+K3_DEV uint16_t hi16(uint32_t v) { return (uint16_t)(v >> 16); }
+
+// Dot product of 16 weights (two 32-bit words of codes, low nibble first)
+// with a split slice, returned in units of 2^s (multiply by x.inv).
+K3_DEV float dot16_split(uint32_t w0, uint32_t w1, const XHalf16 &x)
+{
+    uint32_t h[8];
+    e2m1x8_to_half2x4(w0, h[0], h[1], h[2], h[3]);
+    e2m1x8_to_half2x4(w1, h[4], h[5], h[6], h[7]);
+    float a = 0.f, b = 0.f, c = 0.f, d = 0.f;
+#pragma unroll
+    for (int p = 0; p < 8; p++) {
+        a = mfma(lo16(h[p]), x.hi[2 * p], a);
+        b = mfma(hi16(h[p]), x.hi[2 * p + 1], b);
+        c = mfma(lo16(h[p]), x.lo[2 * p], c);
+        d = mfma(hi16(h[p]), x.lo[2 * p + 1], d);
+    }
+    return (a + b) + (c + d);
+}
+
+// Same product with only the f16-rounded activations (x.hi): one FMA per
+// weight.  Activations carry 11 significant bits (relative rounding <= 2^-11),
+// products and sums stay exact-product / fp32-accumulate.
+K3_DEV float dot16_hi(uint32_t w0, uint32_t w1, const XHalf16 &x)
+{
+    uint32_t h[8];
+    e2m1x8_to_half2x4(w0, h[0], h[1], h[2], h[3]);
+    e2m1x8_to_half2x4(w1, h[4], h[5], h[6], h[7]);
+    float a = 0.f, b = 0.f, c = 0.f, d = 0.f;
+#pragma unroll
+    for (int p = 0; p < 8; p += 2) {
+        a = mfma(lo16(h[p]), x.hi[2 * p], a);
+        b = mfma(hi16(h[p]), x.hi[2 * p + 1], b);
+        c = mfma(lo16(h[p + 1]), x.hi[2 * p + 2], c);
+        d = mfma(hi16(h[p + 1]), x.hi[2 * p + 3], d);
+    }
+    return (a + b) + (c + d);
+}
+template <bool ACT16>
+K3_DEV float dot16_any(uint32_t w0, uint32_t w1, const XHalf16 &x)
+{
+    return ACT16 ? dot16_hi(w0, w1, x) : dot16_split(w0, w1, x);
+}
+
 // Streaming loads: weights are read exactly once, keep them out of L1.
 K3_DEV uint4 ld_stream16(const void *p)
 {
@@ -128,6 +229,87 @@ K3_DEV uint32_t ld_stream_u8(const uint8_t *p)
 {
     uint16_t v;
     asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(v) : "l"(p));
+    return (uint32_t)v;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + bulk-copy (TMA engine, non-tensor form) helpers.  Every wait is
+// bounded by a global-timer deadline; a wait that runs out records
+// K3MOE_ETIMEOUT in the device error word and returns false.
+K3_DEV uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+K3_DEV void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+K3_DEV void mbar_arrive(uint32_t bar)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+                 : "memory");
+}
+K3_DEV void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+K3_DEV uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legal wait
+// try_wait with a suspend-time hint: a warp whose barrier phase has not
+// completed is parked by the hardware (up to the hint) instead of spinning,
+// so waiting warps do not take issue slots from working ones.
+K3_DEV uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity), "r"(20000u)
+                 : "memory");
+    return ok;
+}
+K3_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int *err)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t n = 1;; n++) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+            set_device_error(err, K3MOE_ETIMEOUT);
+            return false;
+        }
+    }
+}
+// Bulk copy global -> shared (16-byte aligned addresses, size a multiple of
+// 16), completion counted on `bar`.
+K3_DEV void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+K3_DEV uint4 lds128(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+K3_DEV uint2 lds64(uint32_t a)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+K3_DEV uint32_t lds_u8(uint32_t a)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(a));
     return (uint32_t)v;
 }
 
@@ -181,11 +363,5 @@ K3_DEV float warp_sum(float v)
 
 K3_DEV float silu(float z) { return z / (1.0f + expf(-z)); }
 
-// Device error word (bounded waits that ran out write K3MOE_ETIMEOUT here);
-// one int per device, allocated by the host side (k3::device_error_word()).
-K3_DEV void set_device_error(int *err, int code)
-{
-    if (err) atomicCAS(err, 0, code);
-}
 
 }  // namespace k3

@@ -16,25 +16,30 @@ int num_sms();
 K3_DEV bool better(float a, int ia, float b, int ib) { return a > b || (a == b && ia < ib); }
 
 // One warp selects the top k (k <= 32) of E scores for one token.
-// logit: unbiased logits [E] (any memory space readable by ld.cg),
-// bias: [E] or null.  Writes ids ascending and softmax weights.
+// logit: unbiased logits [E] (read with ld.cg: they may have been written by
+// other CTAs of the same kernel), bias: [E] or null.  The scores are loaded
+// once into registers (E <= 32 * TK_MAXPL); k rounds of a warp argmax follow.
+// Writes ids ascending and the softmax weights of the unbiased logits.
+constexpr int TK_MAXPL = 32;  // E <= 1024
 K3_DEV void warp_topk(const float *logit, const float *bias, int E, int k, int32_t *ids_out,
                       float *w_out, int lane)
 {
-    // each lane scans its strided slice; chosen elements are marked by
-    // remembering the last selected (score, id) and skipping anything that
-    // ranks at or above it.
-    float last_s = INFINITY;
-    int last_i = -1;
+    float sc[TK_MAXPL];
+#pragma unroll
+    for (int q = 0; q < TK_MAXPL; q++) {
+        const int e = lane + 32 * q;
+        sc[q] = -INFINITY;
+        if (e < E) sc[q] = __ldcg(logit + e) + (bias ? __ldg(bias + e) : 0.f);
+    }
+    unsigned taken = 0;  // bit q: my element q already chosen
     int my_id = -1;
     for (int r = 0; r < k; r++) {
         float bs = -INFINITY;
         int bi = 0x7fffffff;
-        for (int e = lane; e < E; e += 32) {
-            float sc = __ldcg(logit + e) + (bias ? __ldg(bias + e) : 0.f);
-            // candidates rank strictly below the previously chosen one
-            bool below = (last_i < 0) || better(last_s, last_i, sc, e);
-            if (below && better(sc, e, bs, bi)) { bs = sc; bi = e; }
+#pragma unroll
+        for (int q = 0; q < TK_MAXPL; q++) {
+            const int e = lane + 32 * q;
+            if (e < E && !((taken >> q) & 1u) && better(sc[q], e, bs, bi)) { bs = sc[q]; bi = e; }
         }
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) {
@@ -42,8 +47,7 @@ K3_DEV void warp_topk(const float *logit, const float *bias, int E, int k, int32
             int oi = __shfl_xor_sync(0xffffffffu, bi, off);
             if (better(os, oi, bs, bi)) { bs = os; bi = oi; }
         }
-        last_s = bs;
-        last_i = bi;
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
         if (lane == r) my_id = bi;
     }
     // ascending ids: rank of my id among the k chosen

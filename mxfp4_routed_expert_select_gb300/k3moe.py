@@ -22,6 +22,8 @@ K3MOE_EBUSY = -5
 K3MOE_ENODEV = -6
 K3MOE_F32 = 0
 K3MOE_BF16 = 1
+K3MOE_OPT_FUSED_T1 = 1
+K3MOE_OPT_ACT_F16 = 2
 
 
 class K3Error(RuntimeError):
@@ -89,6 +91,8 @@ SIGNATURES = {
     "k3moe_layer_forward": (ctypes.c_int, [_P, _P, ctypes.c_int, _I, _P, _P, _P, _P]),
     "k3moe_layer_experts_t1": (ctypes.c_int, [_P, _P, _P, _P, _I, _P, _P]),
     "k3moe_layer_set_events": (ctypes.c_int, [_P, _P, _I]),
+    "k3moe_layer_set_option": (ctypes.c_int, [_P, _I, _I]),
+    "k3moe_layer_fused_t1": (ctypes.c_int, [_P]),
     "k3moe_rmsnorm": (ctypes.c_int, [_P, _P, _I, _F, _P]),
     "k3moe_residual_add": (ctypes.c_int, [_P, _P, _I, _P]),
     "k3moe_cache_create": (ctypes.c_int, [_P, _SZ, _SZ, _P, _I, _I]),
@@ -247,8 +251,15 @@ class Layer:
         check(lib().k3moe_layer_route(self.h, _ptr(X), dt, T, _ptr(ids), _ptr(w), _stream(stream)),
               "k3moe_layer_route")
 
+    def set_option(self, option, value):
+        check(lib().k3moe_layer_set_option(self.h, option, int(value)), "k3moe_layer_set_option")
+
+    def fused_t1(self):
+        return lib().k3moe_layer_fused_t1(self.h) == 1
+
     def set_events(self, events):
-        """events: 4 torch.cuda.Event (or None to clear)."""
+        """events: 4 torch.cuda.Event (or None to clear); each must have been
+        recorded once (torch creates the CUDA event lazily)."""
         if not events:
             check(lib().k3moe_layer_set_events(self.h, None, 0), "k3moe_layer_set_events")
             return

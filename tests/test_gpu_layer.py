@@ -29,7 +29,8 @@ def _check(pool, Wr_bits, bias, K, Xd, out, ids, w, sample=None, h_bf16=False):
     rids, rw, m = oracle.topk(lg, K, None if bias is None else bias.astype(np.float64))
     assert np.all(m >= 1e-3)
     assert np.array_equal(ids, rids)
-    assert np.allclose(w, rw, rtol=2e-5, atol=1e-7)
+    # fp32 logits over d terms carry ~1e-5 absolute error; w inherits it
+    assert np.allclose(w, rw, rtol=2e-4, atol=1e-7)
     rows = range(T) if sample is None else sample
     for t in rows:
         ref = oracle.combine(Xd[t:t + 1], rids[t:t + 1], rw[t:t + 1], pool.experts(rids[t]),
@@ -162,3 +163,87 @@ def test_full_prefill_4096_bf16_biased(full):
     _check(pool, Wr_bits, bias, K16, Xd, out, ids, w, sample=[0, 1777, 4095])
     counts = np.bincount(ids.ravel(), minlength=E896)
     assert counts.max() > 3 * counts.mean()  # the bias makes loads uneven
+
+
+# ------------------------------------------- fused batch-1 kernel vs oracle
+
+@pytest.fixture(scope="module")
+def fusable():
+    E, d, f = 48, 1024, 512
+    pool = Pool(6, 0, E, d, f)
+    Wr_bits = synth.router_bf16(6, 0, E, d)
+    bias = synth.bias_normal(6, 0, E)
+    return pool, Wr_bits, bias, E, d, f
+
+
+@pytest.mark.parametrize("K,use_bias,act16", [(1, False, False), (8, True, False), (16, False, False),
+                                              (16, True, True)])
+def test_fused_batch1_matches_oracle_and_unfused(fusable, K, use_bias, act16):
+    pool, Wr_bits, bias, E, d, f = fusable
+    b = bias if use_bias else None
+    bt = None if b is None else torch.from_numpy(b).cuda()
+    T = 3
+    subs = margin_subs(6, T, d, Wr_bits, K, b)
+    Xd = tokens(6, np.arange(T), d, subs)
+    X = tokens_device(6, T, d, subs)
+    L = k.Layer(E, K, d, f, router_tensor(Wr_bits), pool.views, bt, max_tokens=1)
+    assert L.fused_t1()
+    if act16:
+        L.set_option(k.K3MOE_OPT_ACT_F16, 1)
+    L2 = k.Layer(E, K, d, f, router_tensor(Wr_bits), pool.views, bt, max_tokens=1)
+    L2.set_option(k.K3MOE_OPT_FUSED_T1, 0)
+    assert not L2.fused_t1()
+    for t in range(T):
+        out, ids, w = _run(L, X[t:t + 1].contiguous(), 1, K)
+        _check(pool, Wr_bits, b, K, Xd[t:t + 1], out, ids, w)
+        out2, ids2, w2 = _run(L2, X[t:t + 1].contiguous(), 1, K)
+        assert np.array_equal(ids, ids2)
+        # f16 activations: relative rounding 2^-12 per activation
+        assert rel_err(out, out2) <= (1e-3 if act16 else 1e-5)
+    # repeated launches reuse the grid-barrier counters
+    for _ in range(5):
+        out_again, _, _ = _run(L, X[0:1].contiguous(), 1, K)
+    out0, _, _ = _run(L, X[0:1].contiguous(), 1, K)
+    assert np.array_equal(out_again, out0)
+    assert k.device_error() == 0
+    L.close()
+    L2.close()
+
+
+def test_full_decode_batch1_unfused_path(full):
+    pool, Wr_bits, bias, L, Lb = full
+    assert L.fused_t1()
+    T = 2
+    subs = margin_subs(1, T, D, Wr_bits, K16)
+    Xd = tokens(1, np.arange(T), D, subs)
+    X = tokens_device(1, T, D, subs)
+    L.set_option(k.K3MOE_OPT_FUSED_T1, 0)
+    try:
+        for t in range(T):
+            out, ids, w = _run(L, X[t:t + 1].contiguous(), 1, K16)
+            _check(pool, Wr_bits, None, K16, Xd[t:t + 1], out, ids, w)
+    finally:
+        L.set_option(k.K3MOE_OPT_FUSED_T1, 1)
+
+
+def test_full_decode_batch1_f16_activations(full):
+    """The opt-in f16-activation mode on the full layer stays inside the
+    2e-3 bound; the measured error is printed for the record."""
+    pool, Wr_bits, bias, L, Lb = full
+    T = 3
+    subs = margin_subs(1, T, D, Wr_bits, K16)
+    Xd = tokens(1, np.arange(T), D, subs)
+    X = tokens_device(1, T, D, subs)
+    L.set_option(k.K3MOE_OPT_ACT_F16, 1)
+    try:
+        errs = []
+        for t in range(T):
+            out, ids, w = _run(L, X[t:t + 1].contiguous(), 1, K16)
+            _check(pool, Wr_bits, None, K16, Xd[t:t + 1], out, ids, w)
+            lg = oracle.router_logits(Xd[t:t + 1], Wr_bits)
+            rids, rw, _ = oracle.topk(lg, K16)
+            ref = oracle.combine(Xd[t:t + 1], rids, rw, pool.experts(rids[0]), pool.E)[0]
+            errs.append(rel_err(out[0], ref))
+        print("f16-activation max rel err per token:", ["%.2e" % e for e in errs])
+    finally:
+        L.set_option(k.K3MOE_OPT_ACT_F16, 0)
