@@ -176,6 +176,19 @@ def run_ours(args, rank, world, dev_index):
         step(i)
     torch.cuda.synchronize()
 
+    # The timed steps replay a CUDA graph holding G_STEPS consecutive layer
+    # forwards (different tokens and router copies), as a decode loop would:
+    # no host launch overhead inside the step.
+    G_STEPS = 32
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(G_STEPS):
+                step(i)
+        graph.replay()
+        torch.cuda.synchronize()
+
     # per-kernel events on the launching stream for the first steps of the
     # timed region
     n_ev = min(args.steps, 2000)
@@ -191,16 +204,25 @@ def run_ours(args, rank, world, dev_index):
     time.sleep(0.3)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(s)
-    for i in range(args.steps):
-        L = layers[i % N_ROUTER_COPIES]
-        if i < n_ev:
-            L.set_events(evs[i])
-        elif i == n_ev:
-            for l in layers:
-                l.set_events(None)
-        step(i)
-    t_end.record(s)
+    if graph is not None:
+        s = torch.cuda.current_stream()
+        n_rep = (args.steps + G_STEPS - 1) // G_STEPS
+        args.steps = n_rep * G_STEPS
+        t_start.record(s)
+        for _ in range(n_rep):
+            graph.replay()
+        t_end.record(s)
+    else:
+        t_start.record(s)
+        for i in range(args.steps):
+            L = layers[i % N_ROUTER_COPIES]
+            if i < n_ev:
+                L.set_events(evs[i])
+            elif i == n_ev:
+                for l in layers:
+                    l.set_events(None)
+            step(i)
+        t_end.record(s)
     torch.cuda.synchronize()
     clocks = clock.stop()
     for l in layers:
@@ -212,6 +234,15 @@ def run_ours(args, rank, world, dev_index):
         tt = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         ms = float(tt.item())
+    if graph is not None:
+        # the fused kernel's own duration, events on its stream around each launch
+        for i in range(n_ev):
+            L = layers[i % N_ROUTER_COPIES]
+            L.set_events(evs[i])
+            step(i)
+        for l in layers:
+            l.set_events(None)
+        torch.cuda.synchronize()
     route_ms = [e[0].elapsed_time(e[1]) for e in evs]
     gu_ms = [e[1].elapsed_time(e[2]) for e in evs]
     dn_ms = [e[2].elapsed_time(e[3]) for e in evs]
@@ -225,14 +256,26 @@ def run_ours(args, rank, world, dev_index):
         for i in range(args.warmup):
             step(i)
         torch.cuda.synchronize()
+        g16 = None
+        if not args.no_graph:
+            g16 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g16):
+                for i in range(G_STEPS):
+                    step(i)
+            g16.replay()
+            torch.cuda.synchronize()
         a0 = torch.cuda.Event(enable_timing=True)
         a1 = torch.cuda.Event(enable_timing=True)
         a0.record(s)
-        for i in range(args.steps):
-            step(i)
+        if g16 is not None:
+            for _ in range(args.steps // G_STEPS):
+                g16.replay()
+        else:
+            for i in range(args.steps):
+                step(i)
         a1.record(s)
         torch.cuda.synchronize()
-        ams = a0.elapsed_time(a1) / args.steps
+        ams = a0.elapsed_time(a1) / (args.steps if g16 is None else (args.steps // G_STEPS) * G_STEPS)
         for l in layers:
             l.set_option(k.K3MOE_OPT_ACT_F16, 0)
         act16 = {"value": round(world * 1e3 / ams, 2), "unit": "tokens/s", "ms_per_step": round(ams, 5),
@@ -272,7 +315,10 @@ def run_ours(args, rank, world, dev_index):
     peak, peak_src = measured_peaks()
     gu_avg = statistics.mean(gu_ms)
     if fused:
-        k_ms = statistics.mean([a + b + c for a, b, c in zip(route_ms, gu_ms, dn_ms)])
+        # one kernel per step: its average duration over the timed region is at
+        # most the step time (graph replay gaps count against it)
+        eager_ms = statistics.mean([a + b + c for a, b, c in zip(route_ms, gu_ms, dn_ms)])
+        k_ms = ms / args.steps if graph is not None else eager_ms
         k_name, k_bytes = "k3_moe_t1_fused (router + top-k + 16 experts + combine)", LAYER_BYTES
     else:
         k_ms, k_name, k_bytes = gu_avg, "k3_rows_pipe (gate/up + SwiGLU, 16 experts)", GATEUP_BYTES
@@ -294,12 +340,14 @@ def run_ours(args, rank, world, dev_index):
         "config": {"workload": "moe_layer_decode_b1: 896 experts d=7168 f=1536 resident (15.7 GB), "
                                "router bf16 [896x7168], top-16, softmax combine",
                    "global_batch": world, "seq_len": 1, "parallelism": "replicas" if world > 1 else "single",
+                   "launch": "cuda graph of 32 steps, replayed" if graph is not None else "host launch per step",
                    "l2": "inputs larger than L2: %d rotated router copies (%.0f MB) + 896 experts "
                          "(16 random per token, 281 MB/token) + %d distinct tokens"
                          % (N_ROUTER_COPIES, N_ROUTER_COPIES * ROUTER_BYTES / 1e6, N_TOKENS)},
         "layer_hbm": {"bytes_per_token": LAYER_BYTES, "gbs": round(layer_gbs, 1),
                       "frac_of_peak": round(layer_gbs / peak, 4), "frac_of_8tbs": round(layer_gbs / 8000, 4)},
-        "kernels_ms": ({"fused_layer": round(k_ms, 5), "steps_sampled": n_ev} if fused else
+        "kernels_ms": ({"fused_layer": round(k_ms, 5), "fused_layer_eager_events": round(eager_ms, 5),
+                        "steps_sampled": n_ev} if fused else
                        {"route_topk": round(statistics.mean(route_ms), 5),
                         "gate_up_swiglu": round(gu_avg, 5),
                         "down_combine": round(statistics.mean(dn_ms), 5), "steps_sampled": n_ev}),
@@ -376,6 +424,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch every step from the host")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

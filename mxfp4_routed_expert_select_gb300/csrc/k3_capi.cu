@@ -56,7 +56,8 @@ int launch_residual(float *x, const float *dlt, int n, cudaStream_t s);
 bool fused_t1_supported(int E, int k, int d, int f);
 int launch_fused_t1(const float *x, const uint16_t *Wr, const float *bias, const DevExpert *table,
                     int E, int k, int d, int f, float *logits, int32_t *ids, float *w, float *h,
-                    float *Y, float *out, unsigned *gbar, bool act16, cudaStream_t s);
+                    float *Y, float *out, unsigned long long *ctr, bool act16, cudaStream_t s);
+int fused_t1_counters();
 }  // namespace k3
 
 using k3::DevExpert;
@@ -240,14 +241,14 @@ struct k3moe_layer {
     bool router_only;    // created without a resident expert table
     bool fused;          // K3MOE_OPT_FUSED_T1
     bool act16;          // K3MOE_OPT_ACT_F16
-    unsigned *gbar;      // [2] grid-barrier counters of the fused kernel
+    unsigned long long *ctr;  // monotonic cross-CTA counters of the fused kernel
 };
 
 static void layer_free(k3moe_layer *L)
 {
     if (!L) return;
     void *ptrs[] = {L->table, L->logits, L->part,  L->ids,     L->w,      L->h,    L->Y,
-                    L->offsets, L->perm, L->items, L->n_items, L->ticket, L->gbar};
+                    L->offsets, L->perm, L->items, L->n_items, L->ticket, L->ctr};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete L;
@@ -298,7 +299,7 @@ int k3moe_layer_create(k3moe_layer **out, const k3moe_layer_desc *D)
     alloc((void **)&L->items, sizeof(int4) * pairs);
     alloc((void **)&L->n_items, sizeof(int32_t));
     alloc((void **)&L->ticket, sizeof(unsigned));
-    alloc((void **)&L->gbar, 2 * sizeof(unsigned));
+    alloc((void **)&L->ctr, sizeof(unsigned long long) * k3::fused_t1_counters());
     L->fused = true;
     L->act16 = false;
     if (!ok) {
@@ -320,7 +321,8 @@ int k3moe_layer_create(k3moe_layer **out, const k3moe_layer_desc *D)
     cudaError_t st = cudaMemcpy(L->table, tmp, sizeof(DevExpert) * L->E, cudaMemcpyHostToDevice);
     free(tmp);
     if (st == cudaSuccess) st = cudaMemset(L->ticket, 0, sizeof(unsigned));
-    if (st == cudaSuccess) st = cudaMemset(L->gbar, 0, 2 * sizeof(unsigned));
+    if (st == cudaSuccess)
+        st = cudaMemset(L->ctr, 0, sizeof(unsigned long long) * k3::fused_t1_counters());
     if (st != cudaSuccess) {
         cudaGetLastError();
         layer_free(L);
@@ -372,7 +374,7 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int xdt, int32_t T, float
     if (L->nev) K3_CUDA(cudaEventRecord(L->ev[0], st));
     if (T == 1 && xdt == K3MOE_F32 && k3moe_layer_fused_t1(L) == 1) {
         K3_TRY(k3::launch_fused_t1((const float *)X, L->Wr, L->bias, L->table, L->E, L->k, L->d,
-                                   L->f, L->logits, L->ids, L->w, L->h, L->Y, out, L->gbar,
+                                   L->f, L->logits, L->ids, L->w, L->h, L->Y, out, L->ctr,
                                    L->act16, st));
         if (L->nev) {
             K3_CUDA(cudaEventRecord(L->ev[1], st));

@@ -2,25 +2,30 @@
 // cooperative kernel (one CTA per SM).
 //
 //   phase R  router logits  (bf16 W_r rows streamed, fp32 x)
-//   -- grid barrier --
+//   -- grid barrier (the only one) --
 //   phase T  top-k + softmax (every CTA computes the same selection)
 //   phase G  gate/up products + SwiGLU of the k experts -> h   (MXFP4)
-//   -- grid barrier --
-//   phase D  down products -> w_j * y_j                          (MXFP4)
-//   -- grid barrier --
-//   phase C  combine: out[i] = sum_j w_j y_j[i]  (fixed order)
+//            each finished stage bumps its expert's "h rows done" counter
+//   phase D  down products -> w_j * y_j, once its expert's h is complete
+//            (waits only on the 1-2 experts this CTA needs); each finished
+//            64-row block bumps that block's counter and the k-th arrival
+//            sums the k contributions in fixed order: out = sum_j w_j y_j
 //
 // Weight bytes move global -> shared memory by cp.async.bulk, issued by one
 // producer lane into a ring of S slots guarded by full/empty mbarriers.  The
-// producer never takes part in the grid barriers: it streams the router rows
-// at once, the gate/up rows as soon as this CTA knows the selection, and the
-// down rows right after, so the down weights are already arriving while the
-// compute warps wait at the second grid barrier.  Fourteen compute warps read
-// their column slice of each staged row from shared memory and decode E2M1 in
-// registers (k3_device.cuh, split-activation form).  The last warp to finish a
-// stage (per-slot ticket) sums the column slices in fixed order, so results
-// are deterministic.  Every wait is bounded (2 s) and records K3MOE_ETIMEOUT
-// in the device error word instead of hanging.
+// producer never waits for the compute warps except for ring space: it
+// streams the router rows at once, the gate/up rows as soon as this CTA knows
+// the selection, and the down rows right after.  A stage is consumed by one
+// group of warps that together cover all columns (lane = one 32- or
+// 16-column slice); groups take stages in turn and drift independently.  The
+// last warp of a group to finish a stage (per-slot ticket) sums the column
+// slices in fixed order, so results are deterministic.
+//
+// Cross-CTA counters are 64-bit and only ever grow: launch number `gen`
+// (1, 2, ...) makes the targets gen * grid, gen * (f / 8) and gen * k, so no
+// counter is ever reset.  `gen` lives on the device (read at entry, advanced
+// by the last CTA to leave), so a captured launch replays correctly.  Every wait is bounded (2 s) and records
+// K3MOE_ETIMEOUT in the device error word instead of hanging.
 #include "k3_device.cuh"
 
 namespace k3 {
@@ -32,9 +37,14 @@ constexpr int FU_NCW = 14;       // compute warps
 constexpr int FU_THREADS = (FU_NCW + 1) * 32;
 constexpr int FU_RR = 2;         // router rows per stage
 constexpr int FU_RG = 8;         // gate/up rows per stage
-constexpr int FU_RD = 64;        // down rows per stage
+constexpr int FU_RD = 64;        // down rows per stage (and combine block)
 constexpr int FU_MAXK = 16;
 constexpr int FU_REDMAX = 256;   // floats of per-slot reduction buffer
+constexpr int FU_CTR_H = 1;      // counters: [0] grid barrier,
+constexpr int FU_CTR_Y = 1 + FU_MAXK;  // [1..16] h per expert, [17..] y per block
+constexpr int FU_CTR_EXIT = FU_CTR_Y + 7168 / FU_RD;  // CTAs done with this launch
+constexpr int FU_CTR_GEN = FU_CTR_EXIT + 1;            // launches completed
+constexpr int FU_NCTR = FU_CTR_GEN + 1;
 
 struct FusedArgs {
     const float *x;          // [d]
@@ -48,7 +58,8 @@ struct FusedArgs {
     float *h;                // [k][f]
     float *Y;                // [k][d]
     float *out;              // [d]
-    unsigned *gbar;          // [2] arrivals, exits
+    unsigned long long *ctr; // [FU_NCTR] monotonic counters
+    unsigned long long gen;  // launch number, >= 1 (set on the device)
     int *err;
     int S;                   // ring slots
     uint32_t slotB;          // bytes per slot
@@ -59,30 +70,37 @@ K3_DEV void named_sync(int id, int nthreads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-K3_DEV unsigned ld_acquire(const unsigned *p)
+K3_DEV unsigned long long ld_acquire64(const unsigned long long *p)
 {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 
+// Spin (bounded) until *p >= target.
+K3_DEV bool wait_counter(const unsigned long long *p, unsigned long long target, int *err)
+{
+    if (ld_acquire64(p) >= target) return true;
+    const uint64_t t0 = global_ns();
+    while (ld_acquire64(p) < target) {
+        __nanosleep(32);
+        if (global_ns() - t0 > kWaitLimitNs) {
+            set_device_error(err, K3MOE_ETIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
 // Grid barrier among the compute warps of every CTA (the producer warps do
-// not take part).  Returns false when the wait ran out.
-K3_DEV bool grid_barrier(const FusedArgs &a, unsigned target, int *abort_flag)
+// not take part).  Returns false when the wait ran out (or had run out).
+K3_DEV bool grid_barrier(const FusedArgs &a, int *abort_flag)
 {
     named_sync(1, FU_NCW * 32);
     if (threadIdx.x == 0 && *(volatile int *)abort_flag == 0) {
         __threadfence();
-        atomicAdd(&a.gbar[0], 1u);
-        const uint64_t t0 = global_ns();
-        while (ld_acquire(&a.gbar[0]) < target) {
-            __nanosleep(64);
-            if (global_ns() - t0 > kWaitLimitNs) {
-                set_device_error(a.err, K3MOE_ETIMEOUT);
-                *abort_flag = 1;
-                break;
-            }
-        }
+        atomicAdd(&a.ctr[0], 1ull);
+        if (!wait_counter(&a.ctr[0], a.gen * gridDim.x, a.err)) *abort_flag = 1;
         __threadfence();
     }
     named_sync(1, FU_NCW * 32);
@@ -107,18 +125,85 @@ K3_DEV float bf16x8_dotf(uint4 wv, const float *xv, float acc)
     return acc;
 }
 
-K3_DEV bool fu_better(float a, int ia, float b, int ib) { return a > b || (a == b && ia < ib); }
+// order-preserving map of an fp32 score to uint32 (larger score -> larger key)
+K3_DEV uint32_t okey(float v)
+{
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// One warp: the top k of E scores (logit + bias), ties to the lower id, by a
+// radix search for the k-th largest key; ids ascending and softmax weights of
+// the unbiased logits over the chosen set into sel_ids / sel_w.
+K3_DEV void warp_topk_radix(const FusedArgs &a, int *sel_ids, float *sel_w, int lane)
+{
+    const int E = a.E, k = a.k;
+    uint32_t key[32];
+#pragma unroll
+    for (int q = 0; q < 32; q++) {
+        const int e = lane + 32 * q;
+        key[q] = 0u;  // below every real key (okey of -inf is 0x007fffff)
+        if (e < E) key[q] = okey(__ldcg(a.logits + e) + (a.bias ? __ldg(a.bias + e) : 0.f));
+    }
+    // largest T with count(key >= T) >= k
+    uint32_t T = 0u;
+    for (int b = 31; b >= 0; b--) {
+        const uint32_t cand = T | (1u << b);
+        uint32_t c0 = 0, c1 = 0;
+#pragma unroll
+        for (int q = 0; q < 32; q += 2) {
+            c0 += key[q] >= cand;
+            c1 += key[q + 1] >= cand;
+        }
+        if (__reduce_add_sync(0xffffffffu, c0 + c1) >= (unsigned)k) T = cand;
+    }
+    // everything above T is in; ties at T fill the rest in id order
+    uint32_t cgt = 0;
+#pragma unroll
+    for (int q = 0; q < 32; q++) cgt += key[q] > T;
+    const int need = k - (int)__reduce_add_sync(0xffffffffu, cgt);
+    const uint32_t lt = (1u << lane) - 1u;
+    int eq_before = 0, sel_before = 0;
+#pragma unroll
+    for (int q = 0; q < 32; q++) {
+        const int e = lane + 32 * q;
+        const bool eq = (e < E) && key[q] == T;
+        const unsigned beq = __ballot_sync(0xffffffffu, eq);
+        const bool pick_eq = eq && (eq_before + __popc(beq & lt)) < need;
+        const bool sel = ((e < E) && key[q] > T) || pick_eq;
+        const unsigned bsel = __ballot_sync(0xffffffffu, sel);
+        if (sel) sel_ids[sel_before + __popc(bsel & lt)] = e;
+        eq_before += __popc(beq);
+        sel_before += __popc(bsel);
+    }
+    __syncwarp();
+    const int my_id = (lane < k) ? sel_ids[lane] : 0;
+    const float l = (lane < k) ? __ldcg(a.logits + my_id) : -INFINITY;
+    float mx = l;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float ex = (lane < k) ? expf(l - mx) : 0.f;
+    const float sum = warp_sum(ex);
+    if (lane < k) sel_w[lane] = ex / sum;
+    if (lane < k && blockIdx.x == 0) {
+        a.ids[lane] = my_id;
+        a.w[lane] = ex / sum;
+    }
+    __syncwarp();
+}
 
 template <bool ACT16>
 __global__ void __launch_bounds__(FU_THREADS, 1) k3_moe_t1_fused(FusedArgs a)
 {
+    a.gen = ld_acquire64(&a.ctr[FU_CTR_GEN]) + 1;
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int S = a.S;
     const uint32_t slotB = a.slotB;
     float *red = reinterpret_cast<float *>(smem + (size_t)S * slotB);       // [S][FU_REDMAX]
     int *cnt = reinterpret_cast<int *>(red + (size_t)S * FU_REDMAX);        // [S]
-    int *sel_ids = cnt + S;                                                 // [FU_MAXK]
+    unsigned *rel = reinterpret_cast<unsigned *>(cnt + S);                  // [S] releases
+    int *sel_ids = reinterpret_cast<int *>(rel + S);                        // [FU_MAXK]
     float *sel_w = reinterpret_cast<float *>(sel_ids + FU_MAXK);            // [FU_MAXK]
     int *abort_flag = reinterpret_cast<int *>(sel_w + FU_MAXK);             // [1]
     uint64_t *bars = reinterpret_cast<uint64_t *>(
@@ -143,8 +228,9 @@ __global__ void __launch_bounds__(FU_THREADS, 1) k3_moe_t1_fused(FusedArgs a)
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; i++) {
             mbar_init(full0 + 8 * i, 1);
-            mbar_init(empty0 + 8 * i, FU_NCW);
+            mbar_init(empty0 + 8 * i, 1);  // the finishing warp of the consuming group
             cnt[i] = 0;
+            rel[i] = 0;
         }
         mbar_init(topk_bar, 1);
         *abort_flag = 0;
@@ -203,327 +289,255 @@ __global__ void __launch_bounds__(FU_THREADS, 1) k3_moe_t1_fused(FusedArgs a)
     }
 
     // ============================================================ compute warps
-    int it = 0;  // ring position, in step with the producer
-    unsigned gen = 0;
+    bool dead = false;  // a wait ran out: skip the remaining work, keep the barriers
+    // A group takes every ngrp-th stage, so it may come to a slot while the
+    // slot still holds an older stage of another group.  Parity waits only
+    // tell adjacent phases apart, so first wait until the slot's previous
+    // occupant has been released (rel counts releases per slot); then the
+    // full barrier is at most one phase away and its parity is unambiguous.
     auto stage_wait = [&](int idx) -> bool {
-        return mbar_wait(full0 + 8 * (idx % S), (idx / S) & 1, a.err);
+        if (dead) return false;
+        const int slot = idx % S;
+        const unsigned need = (unsigned)(idx / S);
+        if (*(volatile unsigned *)&rel[slot] < need) {
+            const uint64_t t0 = global_ns();
+            for (uint32_t n = 1; *(volatile unsigned *)&rel[slot] < need; n++) {
+                __nanosleep(20);
+                if ((n & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+                    set_device_error(a.err, K3MOE_ETIMEOUT);
+                    dead = true;
+                    *(volatile int *)abort_flag = 1;
+                    return false;
+                }
+            }
+        }
+        if (!mbar_wait(full0 + 8 * slot, (idx / S) & 1, a.err)) {
+            dead = true;
+            *(volatile int *)abort_flag = 1;
+        }
+        return !dead;
     };
-    // ticket: returns true for the last of the FU_NCW warps on this slot
-    auto ticket = [&](int slot) -> bool {
+    // ticket among the `gsize` warps of a group: true for the last one
+    auto ticket = [&](int slot, int gsize) -> bool {
         __syncwarp();
         int last = 0;
         if (lane == 0) {
             __threadfence_block();
-            last = (atomicAdd(&cnt[slot], 1) == FU_NCW - 1);
+            last = (atomicAdd(&cnt[slot], 1) == gsize - 1);
         }
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) __threadfence_block();
         return last != 0;
     };
-    auto release = [&](int slot, bool last) {
-        if (last && lane == 0) cnt[slot] = 0;
+    auto release = [&](int slot) {
+        if (lane == 0) {
+            cnt[slot] = 0;
+            __threadfence_block();
+            *(volatile unsigned *)&rel[slot] = *(volatile unsigned *)&rel[slot] + 1u;
+            mbar_arrive(empty0 + 8 * slot);
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * slot);
     };
+    const int ncolG = d / 1024;                  // warps per group, 32 columns per lane
+    const int ngrpG = FU_NCW / ncolG;            // groups in phases R and G
+    const int cG = warp % ncolG, grpG = warp / ncolG;
+    const bool inG = grpG < ngrpG;
+    const int gcol = cG * 32 + lane;             // this lane's group of 32 columns
 
     // ------------------------------------------------------ phase R: router
     {
-        const int ncol = d / 1024;              // 32 columns per lane
-        const int rs_n = FU_NCW / ncol;
-        const int c = warp % ncol, rs = warp / ncol;
-        const bool wact = warp < ncol * rs_n;
-        const int g = c * 32 + lane;             // group of 32 columns
         float xv[32];
 #pragma unroll
         for (int q = 0; q < 8; q++) {
-            float4 t = __ldg(reinterpret_cast<const float4 *>(a.x + 32 * g) + q);
+            float4 t = __ldg(reinterpret_cast<const float4 *>(a.x + 32 * gcol) + q);
             xv[4 * q] = t.x; xv[4 * q + 1] = t.y; xv[4 * q + 2] = t.z; xv[4 * q + 3] = t.w;
         }
-        for (int s = 0; s < nR; s++, it++) {
+        for (int s = inG ? grpG : nR; s < nR; s += ngrpG) {
+            const int it = s;
             const int slot = it % S;
-            if (!stage_wait(it)) { *(volatile int *)abort_flag = 1; break; }
+            if (!stage_wait(it)) break;
             const int e0 = (r_lo + s) * FU_RR;
             const int nr = min(FU_RR, E - e0);
-            if (wact) {
-                for (int row = rs; row < nr; row += rs_n) {
-                    const uint32_t rb = sbase + slot * slotB + row * rRowB + 64 * g;
-                    float acc = 0.f;
+            for (int row = 0; row < nr; row++) {
+                const uint32_t rb = sbase + slot * slotB + row * rRowB + 64 * gcol;
+                float acc = 0.f;
 #pragma unroll
-                    for (int q = 0; q < 4; q++) acc = bf16x8_dotf(lds128(rb + 16 * q), xv + 8 * q, acc);
-                    acc = warp_sum(acc);
-                    if (lane == 0) red[(size_t)slot * FU_REDMAX + row * ncol + c] = acc;
+                for (int q = 0; q < 4; q++) acc = bf16x8_dotf(lds128(rb + 16 * q), xv + 8 * q, acc);
+                acc = warp_sum(acc);
+                if (lane == 0) red[(size_t)slot * FU_REDMAX + row * ncolG + cG] = acc;
+            }
+            if (ticket(slot, ncolG)) {
+                if (lane < nr) {
+                    float sum = 0.f;
+                    for (int cc = 0; cc < ncolG; cc++) sum += red[(size_t)slot * FU_REDMAX + lane * ncolG + cc];
+                    a.logits[e0 + lane] = sum;
                 }
+                release(slot);
             }
-            const bool last = ticket(slot);
-            if (last && lane < nr) {
-                float sum = 0.f;
-                for (int cc = 0; cc < ncol; cc++) sum += red[(size_t)slot * FU_REDMAX + lane * ncol + cc];
-                a.logits[e0 + lane] = sum;
-            }
-            release(slot, last);
         }
     }
-    if (!grid_barrier(a, gridDim.x * (++gen), abort_flag)) return;
+    if (!grid_barrier(a, abort_flag)) return;
 
     // ------------------------------------------------------ phase T: top-k
-    // Two levels: every compute warp selects the top k of its slice of the
-    // E scores (scores in registers, k rounds of a warp argmax), writes the k
-    // candidates to shared memory; warp 0 then selects the top k of the
-    // FU_NCW * k candidates.  Order: larger score first, ties to lower id.
-    {
-        float *cand_s = red;                                                  // [FU_NCW][FU_MAXK]
-        int *cand_i = reinterpret_cast<int *>(red + FU_NCW * FU_MAXK);       // [FU_NCW][FU_MAXK]
-        const int per = (E + FU_NCW - 1) / FU_NCW;                           // slice length <= 74
-        const int e_lo = warp * per;
-        float sc[3];
-        int si[3];
-#pragma unroll
-        for (int q = 0; q < 3; q++) {
-            const int e = e_lo + lane + 32 * q;
-            const bool in = (lane + 32 * q < per) && e < E;
-            sc[q] = in ? __ldcg(a.logits + e) + (a.bias ? __ldg(a.bias + e) : 0.f) : -INFINITY;
-            si[q] = in ? e : 0x7fffffff;
+    if (warp == 0) {
+        warp_topk_radix(a, sel_ids, sel_w, lane);
+        if (lane == 0) {
+            __threadfence_block();
+            mbar_arrive(topk_bar);  // the producer may now stream expert rows
         }
-        for (int r = 0; r < k; r++) {
-            float bs = -INFINITY;
-            int bi = 0x7fffffff;
-#pragma unroll
-            for (int q = 0; q < 3; q++)
-                if (fu_better(sc[q], si[q], bs, bi)) { bs = sc[q]; bi = si[q]; }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
-                const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (fu_better(os, oi, bs, bi)) { bs = os; bi = oi; }
-            }
-#pragma unroll
-            for (int q = 0; q < 3; q++)
-                if (si[q] == bi) { sc[q] = -INFINITY; si[q] = 0x7fffffff; }
-            if (lane == 0) {
-                cand_s[warp * FU_MAXK + r] = bs;
-                cand_i[warp * FU_MAXK + r] = bi;
-            }
-        }
-        named_sync(1, FU_NCW * 32);
-        if (warp == 0) {
-            constexpr int NC = (FU_NCW * FU_MAXK + 31) / 32;  // candidates per lane
-            float cs[NC];
-            int ci[NC];
-#pragma unroll
-            for (int q = 0; q < NC; q++) {
-                const int c = lane + 32 * q;
-                const bool in = c < FU_NCW * FU_MAXK && (c % FU_MAXK) < k;
-                cs[q] = in ? cand_s[c] : -INFINITY;
-                ci[q] = in ? cand_i[c] : 0x7fffffff;
-            }
-            int my_id = -1;
-            for (int r = 0; r < k; r++) {
-                float bs = -INFINITY;
-                int bi = 0x7fffffff;
-#pragma unroll
-                for (int q = 0; q < NC; q++)
-                    if (fu_better(cs[q], ci[q], bs, bi)) { bs = cs[q]; bi = ci[q]; }
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) {
-                    const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-                    const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                    if (fu_better(os, oi, bs, bi)) { bs = os; bi = oi; }
-                }
-#pragma unroll
-                for (int q = 0; q < NC; q++)
-                    if (ci[q] == bi) { cs[q] = -INFINITY; ci[q] = 0x7fffffff; }
-                if (lane == r) my_id = bi;
-            }
-            int pos = 0;
-            for (int q = 0; q < k; q++) {
-                const int other = __shfl_sync(0xffffffffu, my_id, q);
-                if (lane < k && other < my_id) pos++;
-            }
-            const float l = (lane < k) ? __ldcg(a.logits + my_id) : -INFINITY;
-            float mx = l;
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float ex = (lane < k) ? expf(l - mx) : 0.f;
-            const float sum = warp_sum(ex);
-            if (lane < k) {
-                sel_ids[pos] = my_id;
-                sel_w[pos] = ex / sum;
-                if (blockIdx.x == 0) {
-                    a.ids[pos] = my_id;
-                    a.w[pos] = ex / sum;
-                }
-            }
-            __syncwarp();
-            if (lane == 0) {
-                __threadfence_block();
-                mbar_arrive(topk_bar);  // the producer may now stream expert rows
-            }
-        }
-        named_sync(1, FU_NCW * 32);
     }
+    named_sync(1, FU_NCW * 32);
 
     // ------------------------------------------------------ phase G: gate/up
-    {
-        const int ncol = d / 1024;
-        const int rs_n = FU_NCW / ncol;
-        const int c = warp % ncol, rs = warp / ncol;
-        const bool wact = warp < ncol * rs_n;
-        const int g = c * 32 + lane;
+    if (inG) {
         XHalf16 xa, xb;
         {
             float v[32];
 #pragma unroll
             for (int q = 0; q < 8; q++) {
-                float4 t = __ldg(reinterpret_cast<const float4 *>(a.x + 32 * g) + q);
+                float4 t = __ldg(reinterpret_cast<const float4 *>(a.x + 32 * gcol) + q);
                 v[4 * q] = t.x; v[4 * q + 1] = t.y; v[4 * q + 2] = t.z; v[4 * q + 3] = t.w;
             }
             split16(v, xa);
             split16(v + 16, xb);
         }
-        constexpr int NT = 4;  // rows per warp per stage (FU_RG / 2 row sets at most)
-        for (int s = 0; s < nG; s++, it++) {
+        for (int s = grpG; s < nG; s += ngrpG) {
+            const int it = nR + s;
             const int slot = it % S;
-            if (!stage_wait(it)) { *(volatile int *)abort_flag = 1; break; }
+            if (!stage_wait(it)) break;
             const int q0 = (g_lo + s) * FU_RG;
-            if (wact) {
-                const uint32_t base = sbase + slot * slotB;
-                // rows rs, rs + rs_n, ... of the stage (at most NT per warp)
-                float v[2 * NT];
+            const uint32_t base = sbase + slot * slotB;
+#pragma unroll 1
+            for (int r0 = 0; r0 < FU_RG; r0 += 4) {  // 4 rows x 2 matrices at a time
+                float v[8];                          // [m][row - r0]
 #pragma unroll
-                for (int t = 0; t < NT; t++) {
-                    const int row = rs + t * rs_n;
+                for (int t = 0; t < 4; t++) {
 #pragma unroll
                     for (int m = 0; m < 2; m++) {
-                        float val = 0.f;
-                        if (row < FU_RG) {
-                            const uint32_t mb = base + m * gMatB;
-                            const uint4 qv = lds128(mb + row * (uint32_t)gRowB + 16 * g);
-                            const uint32_t e = lds_u8(mb + FU_RG * (uint32_t)gRowB + row * (uint32_t)gRowS + g);
-                            const float dd = dot16_any<ACT16>(qv.x, qv.y, xa) * xa.inv +
-                                             dot16_any<ACT16>(qv.z, qv.w, xb) * xb.inv;
-                            val = (e == 255u) ? 0.f : dd * e8m0_scale(e);
-                        }
-                        v[m * NT + t] = val;
+                        const int row = r0 + t;
+                        const uint32_t mb = base + m * gMatB;
+                        const uint4 qv = lds128(mb + row * (uint32_t)gRowB + 16 * gcol);
+                        const uint32_t e = lds_u8(mb + FU_RG * (uint32_t)gRowB + row * (uint32_t)gRowS + gcol);
+                        const float dd = dot16_any<ACT16>(qv.x, qv.y, xa) * xa.inv +
+                                         dot16_any<ACT16>(qv.z, qv.w, xb) * xb.inv;
+                        v[m * 4 + t] = (e == 255u) ? 0.f : dd * e8m0_scale(e);
                     }
                 }
-                warp_transpose_reduce<2 * NT>(v, lane);
-                constexpr int LPV = 32 / (2 * NT);
-                if ((lane % LPV) == 0) {
-                    const int vi = sel_of<2 * NT>(lane);
-                    const int t = vi % NT, m = vi / NT;
-                    const int row = rs + t * rs_n;
-                    if (row < FU_RG) red[(size_t)slot * FU_REDMAX + (row * 2 + m) * ncol + c] = v[0];
+                warp_transpose_reduce<8>(v, lane);
+                if ((lane & 3) == 0) {
+                    const int vi = sel_of<8>(lane);  // m * 4 + t
+                    const int m = vi >> 2, row = r0 + (vi & 3);
+                    red[(size_t)slot * FU_REDMAX + (m * FU_RG + row) * ncolG + cG] = v[0];
                 }
             }
-            const bool last = ticket(slot);
-            if (last && lane < FU_RG) {
-                float gs = 0.f, us = 0.f;
-                for (int cc = 0; cc < ncol; cc++) {
-                    gs += red[(size_t)slot * FU_REDMAX + (lane * 2 + 0) * ncol + cc];
-                    us += red[(size_t)slot * FU_REDMAX + (lane * 2 + 1) * ncol + cc];
+            if (ticket(slot, ncolG)) {
+                if (lane < FU_RG) {
+                    float gs = 0.f, us = 0.f;
+                    for (int cc = 0; cc < ncolG; cc++) {
+                        gs += red[(size_t)slot * FU_REDMAX + lane * ncolG + cc];
+                        us += red[(size_t)slot * FU_REDMAX + (FU_RG + lane) * ncolG + cc];
+                    }
+                    a.h[q0 + lane] = silu(gs) * us;
                 }
-                a.h[q0 + lane] = silu(gs) * us;
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence();
+                    atomicAdd(&a.ctr[FU_CTR_H + q0 / f], 1ull);  // h rows of expert j done
+                }
+                release(slot);
             }
-            release(slot, last);
         }
     }
-    if (!grid_barrier(a, gridDim.x * (++gen), abort_flag)) return;
 
     // ------------------------------------------------------ phase D: down
     {
-        const int ncol = f / 512;                // 16 columns per lane
-        const int rs_n = FU_NCW / ncol;
-        const int c = warp % ncol, rs = warp / ncol;
-        const bool wact = warp < ncol * rs_n;
-        const int hg = c * 32 + lane;            // half-group of 16 columns
-        const int qd0 = d_lo * FU_RD, qd1 = d_hi * FU_RD;
-        const int jA = (nD > 0) ? qd0 / d : 0;
-        const int jB = (nD > 0) ? (qd1 - 1) / d : 0;  // a CTA's share spans <= 2 experts
-        XHalf16 hA, hB;
-        {
-            float v[16];
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                float4 t = __ldcg(reinterpret_cast<const float4 *>(a.h + (size_t)jA * f + 16 * hg) + q);
-                v[4 * q] = t.x; v[4 * q + 1] = t.y; v[4 * q + 2] = t.z; v[4 * q + 3] = t.w;
+        const int ncolD = f / 512;               // warps per group, 16 columns per lane
+        const int ngrpD = FU_NCW / ncolD;
+        const int cD = warp % ncolD, grpD = warp / ncolD;
+        const int hg = cD * 32 + lane;           // half-group of 16 columns
+        if (grpD < ngrpD && nD > 0 && !dead) {
+            const int qd0 = d_lo * FU_RD, qd1 = d_hi * FU_RD;
+            const int jA = qd0 / d, jB = (qd1 - 1) / d;  // a CTA's share spans <= 2 experts
+            const unsigned long long need = a.gen * (unsigned long long)(f / FU_RG);
+            bool ok = true;
+            if (lane == 0) ok = wait_counter(&a.ctr[FU_CTR_H + jA], need, a.err) &&
+                                wait_counter(&a.ctr[FU_CTR_H + jB], need, a.err);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) {
+                dead = true;
+                *(volatile int *)abort_flag = 1;
             }
-            split16(v, hA);
+            // the group's stages come in expert order: load h_j when j changes
+            XHalf16 hx;
+            int cur_j = -1;
+            for (int s = grpD; s < nD; s += ngrpD) {
+                const int it = nR + nG + s;
+                const int slot = it % S;
+                if (!stage_wait(it)) break;
+                const int q0 = (d_lo + s) * FU_RD;
+                const int j = q0 / d;
+                if (j != cur_j) {
+                    float v[16];
 #pragma unroll
-            for (int q = 0; q < 4; q++) {
-                float4 t = __ldcg(reinterpret_cast<const float4 *>(a.h + (size_t)jB * f + 16 * hg) + q);
-                v[4 * q] = t.x; v[4 * q + 1] = t.y; v[4 * q + 2] = t.z; v[4 * q + 3] = t.w;
-            }
-            split16(v, hB);
-        }
-        for (int s = 0; s < nD; s++, it++) {
-            const int slot = it % S;
-            if (!stage_wait(it)) { *(volatile int *)abort_flag = 1; break; }
-            const int q0 = (d_lo + s) * FU_RD;
-            const int j = q0 / d;
-            if (wact) {
-                XHalf16 hx;
-                const bool useA = (j == jA);
-#pragma unroll
-                for (int q = 0; q < 16; q++) {
-                    hx.hi[q] = useA ? hA.hi[q] : hB.hi[q];
-                    hx.lo[q] = useA ? hA.lo[q] : hB.lo[q];
+                    for (int q = 0; q < 4; q++) {
+                        float4 t = __ldcg(reinterpret_cast<const float4 *>(a.h + (size_t)j * f + 16 * hg) + q);
+                        v[4 * q] = t.x; v[4 * q + 1] = t.y; v[4 * q + 2] = t.z; v[4 * q + 3] = t.w;
+                    }
+                    split16(v, hx);
+                    cur_j = j;
                 }
-                hx.inv = useA ? hA.inv : hB.inv;
                 const uint32_t base = sbase + slot * slotB;
-                for (int t0 = 0; rs + t0 * rs_n < FU_RD; t0 += 8) {
+                for (int t0 = 0; t0 < FU_RD; t0 += 8) {
                     float v[8];
 #pragma unroll
                     for (int t = 0; t < 8; t++) {
-                        const int row = rs + (t0 + t) * rs_n;
-                        float val = 0.f;
-                        if (row < FU_RD) {
-                            const uint2 qv = lds64(base + row * (uint32_t)dRowB + 8 * hg);
-                            const uint32_t e = lds_u8(base + FU_RD * (uint32_t)dRowB + row * (uint32_t)dRowS + (hg >> 1));
-                            const float dd = dot16_any<ACT16>(qv.x, qv.y, hx) * hx.inv;
-                            val = (e == 255u) ? 0.f : dd * e8m0_scale(e);
-                        }
-                        v[t] = val;
+                        const int row = t0 + t;
+                        const uint2 qv = lds64(base + row * (uint32_t)dRowB + 8 * hg);
+                        const uint32_t e = lds_u8(base + FU_RD * (uint32_t)dRowB + row * (uint32_t)dRowS + (hg >> 1));
+                        const float dd = dot16_any<ACT16>(qv.x, qv.y, hx) * hx.inv;
+                        v[t] = (e == 255u) ? 0.f : dd * e8m0_scale(e);
                     }
                     warp_transpose_reduce<8>(v, lane);
                     if ((lane & 3) == 0) {
                         const int t = sel_of<8>(lane);
-                        const int row = rs + (t0 + t) * rs_n;
-                        if (row < FU_RD) red[(size_t)slot * FU_REDMAX + row * ncol + c] = v[0];
+                        red[(size_t)slot * FU_REDMAX + (t0 + t) * ncolD + cD] = v[0];
+                    }
+                }
+                if (ticket(slot, ncolD)) {
+                    const float wj = sel_w[j];
+                    for (int row = lane; row < FU_RD; row += 32) {
+                        float sum = 0.f;
+                        for (int cc = 0; cc < ncolD; cc++) sum += red[(size_t)slot * FU_REDMAX + row * ncolD + cc];
+                        a.Y[q0 + row] = sum * wj;
+                    }
+                    release(slot);
+                    // combine this 64-row block once all k experts wrote it
+                    const int blk = (q0 - j * d) / FU_RD;
+                    unsigned long long old = 0;
+                    if (lane == 0) {
+                        __threadfence();
+                        old = atomicAdd(&a.ctr[FU_CTR_Y + blk], 1ull);
+                    }
+                    old = __shfl_sync(0xffffffffu, old, 0);
+                    if (old + 1 == a.gen * (unsigned long long)k) {
+                        __threadfence();
+                        const int i0 = blk * FU_RD;
+                        for (int row = lane; row < FU_RD; row += 32) {
+                            float acc = 0.f;
+                            for (int jj = 0; jj < k; jj++) acc += __ldcg(a.Y + (size_t)jj * d + i0 + row);
+                            a.out[i0 + row] = acc;
+                        }
                     }
                 }
             }
-            const bool last = ticket(slot);
-            if (last) {
-                const float wj = sel_w[j];
-                for (int row = lane; row < FU_RD; row += 32) {
-                    float sum = 0.f;
-                    for (int cc = 0; cc < ncol; cc++) sum += red[(size_t)slot * FU_REDMAX + row * ncol + cc];
-                    a.Y[q0 + row] = sum * wj;
-                }
-            }
-            release(slot, last);
         }
     }
-    if (!grid_barrier(a, gridDim.x * (++gen), abort_flag)) return;
-
-    // ------------------------------------------------------ phase C: combine
-    {
-        int i_lo, i_hi;
-        share(d, blockIdx.x, gridDim.x, i_lo, i_hi);
-        for (int i = i_lo + threadIdx.x; i < i_hi; i += FU_NCW * 32) {
-            float acc = 0.f;
-            for (int j = 0; j < k; j++) acc += __ldcg(a.Y + (size_t)j * d + i);
-            a.out[i] = acc;
-        }
-    }
-    // the last CTA out resets the barrier counters for the next launch
+    // the last CTA to leave advances the launch number
     named_sync(1, FU_NCW * 32);
     if (threadIdx.x == 0) {
-        const unsigned old = atomicAdd(&a.gbar[1], 1u);
-        if (old == gridDim.x - 1) {
-            atomicExch(&a.gbar[0], 0u);
-            atomicExch(&a.gbar[1], 0u);
-        }
+        __threadfence();
+        const unsigned long long old = atomicAdd(&a.ctr[FU_CTR_EXIT], 1ull);
+        if (old + 1 == a.gen * (unsigned long long)gridDim.x) atomicAdd(&a.ctr[FU_CTR_GEN], 1ull);
     }
 }
 
@@ -534,8 +548,10 @@ bool fused_t1_supported(int E, int k, int d, int f)
 {
     return d % 1024 == 0 && d >= 1024 && d <= 7168 && f % 512 == 0 && f >= 512 && f <= 2048 &&
            k >= 1 && k <= FU_MAXK && E >= k && E <= 1024 && (k * f) % FU_RG == 0 &&
-           (k * d) % FU_RD == 0 && FU_RD * (f / 2) + FU_RD * (f / 32) > 0;
+           d % FU_RD == 0;
 }
+
+int fused_t1_counters() { return FU_NCTR; }
 
 size_t fused_t1_smem(int d, int f, int *S_out, uint32_t *slot_out)
 {
@@ -545,11 +561,10 @@ size_t fused_t1_smem(int d, int f, int *S_out, uint32_t *slot_out)
     size_t slot = rB > gB ? rB : gB;
     if (dB > slot) slot = dB;
     slot = (slot + 127) & ~(size_t)127;
-    const size_t tail = 0;
     int S = 8;
     auto total = [&](int s) {
-        return (size_t)s * slot + (size_t)s * FU_REDMAX * 4 + (size_t)s * 4 + FU_MAXK * 8 + 4 + 8 +
-               (2 * s + 1) * 8 + tail;
+        return (size_t)s * slot + (size_t)s * FU_REDMAX * 4 + (size_t)s * 8 + FU_MAXK * 8 + 4 + 8 +
+               (2 * s + 1) * 8;
     };
     while (S > 2 && total(S) > 220 * 1024) S--;
     *S_out = S;
@@ -559,7 +574,7 @@ size_t fused_t1_smem(int d, int f, int *S_out, uint32_t *slot_out)
 
 int launch_fused_t1(const float *x, const uint16_t *Wr, const float *bias, const DevExpert *table,
                     int E, int k, int d, int f, float *logits, int32_t *ids, float *w, float *h,
-                    float *Y, float *out, unsigned *gbar, bool act16, cudaStream_t s)
+                    float *Y, float *out, unsigned long long *ctr, bool act16, cudaStream_t s)
 {
     FusedArgs a;
     a.x = x;
@@ -576,7 +591,8 @@ int launch_fused_t1(const float *x, const uint16_t *Wr, const float *bias, const
     a.h = h;
     a.Y = Y;
     a.out = out;
-    a.gbar = gbar;
+    a.ctr = ctr;
+    a.gen = 0;
     a.err = device_error_word();
     int S = 0;
     uint32_t slot = 0;
@@ -584,17 +600,20 @@ int launch_fused_t1(const float *x, const uint16_t *Wr, const float *bias, const
     a.S = S;
     a.slotB = slot;
     auto kern = act16 ? k3_moe_t1_fused<true> : k3_moe_t1_fused<false>;
+    // one-time set-up per instantiation: shared-memory limit and a residency
+    // check (one CTA per SM is required for the grid barrier)
     static size_t configured[2] = {0, 0};
     if (smem > configured[act16]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
             return K3MOE_ECUDA;
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, FU_THREADS, smem) !=
+                cudaSuccess ||
+            per_sm < 1)
+            return K3MOE_ECUDA;
         configured[act16] = smem;
     }
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, FU_THREADS, smem) != cudaSuccess ||
-        per_sm < 1)
-        return K3MOE_ECUDA;
     const int grid = num_sms();  // one CTA per SM, all co-resident
     void *args[] = {&a};
     if (cudaLaunchCooperativeKernel((const void *)kern, dim3(grid), dim3(FU_THREADS), args, smem, s) !=

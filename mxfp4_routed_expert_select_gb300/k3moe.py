@@ -11,7 +11,8 @@ import os
 import numpy as np
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-SO = os.path.join(HERE, "libk3moe.so")
+# K3MOE_LIBRARY may name another build of the same library (e.g. a debug build)
+SO = os.environ.get("K3MOE_LIBRARY") or os.path.join(HERE, "libk3moe.so")
 
 K3MOE_OK = 0
 K3MOE_EINVAL = -1
