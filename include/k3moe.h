@@ -145,6 +145,29 @@ size_t k3moe_expert_gemv_workspace(int32_t d, int32_t f);
 int k3moe_expert_gemv(float *y, const float *x, const k3moe_expert *host_e, int32_t d,
                       int32_t f, void *workspace, size_t workspace_bytes, k3moe_stream s);
 
+/*
+ * k3moe_expert_gemv without a workspace, for callers that cannot allocate
+ * device memory on the call path: code running while a stream is captured in
+ * global capture mode, threads with a no-allocation rule, plug-ins that must
+ * not touch the host application's allocator, systems that budget device
+ * memory once at start-up.  (The pages have no counterpart; this is a
+ * deployment convenience of this library.)
+ *  - Same arguments, layout and result as k3moe_expert_gemv, minus the
+ *    workspace; the SwiGLU intermediate lives in a file-scope device array of
+ *    K3MOE_NOALLOC_MAX_F floats held by every device that loads the library
+ *    until the process exits.  f > K3MOE_NOALLOC_MAX_F is refused with
+ *    K3MOE_EINVAL.
+ *  - Allocates nothing: no cudaMalloc/cudaFree or allocating library call.
+ *  - The first call on a device (with that device current) looks up the
+ *    array's device address; make that first call before any stream capture.
+ *  - All calls on a device share the array: calls whose kernels overlap on the
+ *    GPU race, so serialise them.  Each call overwrites the array fully before
+ *    reading it.
+ */
+#define K3MOE_NOALLOC_MAX_F 2048
+int k3moe_expert_gemv_noalloc(float *y, const float *x, const k3moe_expert *host_e, int32_t d,
+                              int32_t f, k3moe_stream s);
+
 /* ----------------------------------------------------------------- layer */
 
 /*

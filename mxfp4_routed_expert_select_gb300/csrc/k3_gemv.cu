@@ -417,7 +417,7 @@ int *device_error_word();
 constexpr int kPipeR = 4;
 template <int NM>
 static int launch_rows_pipe(const float *x, const ExpertSrc &src, int k, int in, int rows,
-                            float *out, cudaStream_t s)
+                            float *out, int *err, cudaStream_t s)
 {
     const int G = in / 32;
     const int ncol = (G + 31) / 32;
@@ -447,17 +447,18 @@ static int launch_rows_pipe(const float *x, const ExpertSrc &src, int k, int in,
     const int nstage = (int)((total + kPipeR - 1) / kPipeR);
     int grid = num_sms();
     if (grid > nstage) grid = nstage;
-    kern<<<grid, threads, smem, s>>>(x, src, k, in, rows, out, nstage, S, device_error_word());
+    kern<<<grid, threads, smem, s>>>(x, src, k, in, rows, out, nstage, S, err);
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
 }
 
 // rows kernel: MODE 0 (one matrix) or 1 (gate/up SwiGLU over k experts).
-int launch_rows_t1(int mode, const float *x, const ExpertSrc &src, int k, int in, int rows,
-                   float *out, cudaStream_t s)
+// `err` is the device error word the pipelined kernel reports timeouts to.
+int launch_rows_t1_err(int mode, const float *x, const ExpertSrc &src, int k, int in, int rows,
+                       float *out, int *err, cudaStream_t s)
 {
     {
-        const int st = mode ? launch_rows_pipe<2>(x, src, k, in, rows, out, s)
-                            : launch_rows_pipe<1>(x, src, k, in, rows, out, s);
+        const int st = mode ? launch_rows_pipe<2>(x, src, k, in, rows, out, err, s)
+                            : launch_rows_pipe<1>(x, src, k, in, rows, out, err, s);
         if (st != K3MOE_EINVAL) return st;
     }
     const int G = in / 32;
@@ -490,6 +491,12 @@ int launch_rows_t1(int mode, const float *x, const ExpertSrc &src, int k, int in
         k3_rows_t1<0, kUrows><<<grid, threads, smem, s>>>(x, src, k, in, rows, out, rpc);
     }
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
+}
+
+int launch_rows_t1(int mode, const float *x, const ExpertSrc &src, int k, int in, int rows,
+                   float *out, cudaStream_t s)
+{
+    return launch_rows_t1_err(mode, x, src, k, in, rows, out, device_error_word(), s);
 }
 
 template <int HPL>

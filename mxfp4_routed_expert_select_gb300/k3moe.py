@@ -25,6 +25,7 @@ K3MOE_F32 = 0
 K3MOE_BF16 = 1
 K3MOE_OPT_FUSED_T1 = 1
 K3MOE_OPT_ACT_F16 = 2
+K3MOE_NOALLOC_MAX_F = 2048
 
 
 class K3Error(RuntimeError):
@@ -86,6 +87,7 @@ SIGNATURES = {
     "k3moe_matmul_mxfp4": (ctypes.c_int, [_P, _P, _P, _P]),
     "k3moe_expert_gemv_workspace": (_SZ, [_I, _I]),
     "k3moe_expert_gemv": (ctypes.c_int, [_P, _P, _P, _I, _I, _P, _SZ, _P]),
+    "k3moe_expert_gemv_noalloc": (ctypes.c_int, [_P, _P, _P, _I, _I, _P]),
     "k3moe_layer_create": (ctypes.c_int, [_P, _P]),
     "k3moe_layer_destroy": (ctypes.c_int, [_P]),
     "k3moe_layer_route": (ctypes.c_int, [_P, _P, ctypes.c_int, _I, _P, _P, _P]),
@@ -206,6 +208,12 @@ def expert_gemv(y, x, expert, d, f, workspace, stream=None):
     nbytes = workspace.numel() * workspace.element_size()
     check(lib().k3moe_expert_gemv(_ptr(y), _ptr(x), ctypes.byref(expert), d, f, _ptr(workspace),
                                   nbytes, _stream(stream)), "k3moe_expert_gemv")
+
+
+def expert_gemv_noalloc(y, x, expert, d, f, stream=None):
+    """k3moe_expert_gemv without a workspace (static device scratch)."""
+    check(lib().k3moe_expert_gemv_noalloc(_ptr(y), _ptr(x), ctypes.byref(expert), d, f,
+                                          _stream(stream)), "k3moe_expert_gemv_noalloc")
 
 
 def rmsnorm(u, x, eps, stream=None):
