@@ -9,7 +9,13 @@ token through the whole layer (router + top-k + 16 experts + combine).
 
 Prints ONE JSON line (rank 0).  `value` is tokens/s of the whole job (every
 rank runs independent tokens: weak scaling, no collective on the data path).
-Extra workloads for development: --workload expert|decode64|prefill4096.
+Other workloads of the same layer, one JSON line each (not the headline):
+  --workload expert       one expert GEMV (gate/up + SwiGLU + down), 1 token
+  --workload decode64     batched decode, 64 tokens, grouped by expert
+  --workload prefill4096  4096 bf16 tokens, selection bias ~N(0,1)
+  --workload stream       4 layers x 896 experts in pinned host memory behind
+                          an 8 GB HBM LRU cache, 256 tokens, RMSNorm +
+                          residual, Zipf(1.1) selection bias
 """
 import argparse
 import json
@@ -417,6 +423,386 @@ def run_reference(args):
     }
 
 
+# ------------------------------------------------------ other workloads
+
+def _timed(steps, warmup, step, dev_index, world, graph_steps=0):
+    """Warm-up, then `steps` steps between two events on the current stream
+    (optionally replaying a CUDA graph of `graph_steps` steps); clocks are
+    sampled meanwhile.  Returns (ms total, steps actually timed, clocks)."""
+    import torch
+    s = torch.cuda.current_stream()
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    graph = None
+    if graph_steps:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(graph_steps):
+                step(i)
+        graph.replay()
+        torch.cuda.synchronize()
+        steps = max(1, (steps + graph_steps - 1) // graph_steps) * graph_steps
+    clock = ClockSampler(dev_index)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clock.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(s)
+    if graph is not None:
+        for _ in range(steps // graph_steps):
+            graph.replay()
+    else:
+        for i in range(steps):
+            step(i)
+    t1.record(s)
+    torch.cuda.synchronize()
+    clocks = clock.stop()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        torch.distributed.barrier()
+        tt = torch.tensor([ms], device=torch.device("cuda", dev_index))
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    return ms, steps, clocks
+
+
+def _kernel_events(layer, step, n, sync=True):
+    """Per-phase durations (ms) of `n` eager forwards, from the layer's four
+    events recorded on its stream: [route, route->gate/up, gate/up->end]."""
+    import torch
+    s = torch.cuda.current_stream()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    for q in evs:
+        for e in q:
+            e.record(s)
+    torch.cuda.synchronize()
+    for i in range(n):
+        layer.set_events(evs[i])
+        step(i)
+    layer.set_events(None)
+    torch.cuda.synchronize()
+    return ([q[0].elapsed_time(q[1]) for q in evs], [q[1].elapsed_time(q[2]) for q in evs],
+            [q[2].elapsed_time(q[3]) for q in evs])
+
+
+def _base_line(metric, value, unit, world, args, ms_step, dtype, config, clocks):
+    return {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+            "data": "synthetic (seeded SplitMix64: uniform E2M1 codes, E8M0 in [120,130], "
+                    "x ~ N(0,1), W_r ~ N(0,0.02) bf16)",
+            "config": config, "clocks": clocks}
+
+
+def _roofline(name, nbytes, k_ms, bound="hbm"):
+    peak, src = measured_peaks()
+    ach = nbytes / (k_ms * 1e-3) / 1e9
+    return {"kernel": name, "bound": bound, "achieved": round(ach, 1), "peak": peak,
+            "peak_source": src, "unit": "GB/s", "frac": round(ach / peak, 4), "traffic": None,
+            "algorithmic_bytes": int(nbytes)}
+
+
+def _e2e(step_host, n, world, dev_index, h2d, d2h, unit_per_step=1):
+    import torch
+    s = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for i in range(n):
+        step_host(i)
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([ms], device=torch.device("cuda", dev_index))
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    return {"value": round(n * unit_per_step * world / (ms * 1e-3), 2), "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n}
+
+
+def run_expert(args, rank, world, dev_index):
+    """One expert GEMV per step, rotating over the 896 resident experts and
+    1024 tokens (17.5 MB per expert: every step reads HBM, not L2)."""
+    import torch
+    import synth
+    from mxfp4_routed_expert_select_gb300 import k3moe as k
+    dev = torch.device("cuda", dev_index)
+    torch.cuda.set_device(dev)
+    blobs, views = build_pool(dev)
+    X = torch.from_numpy(np.stack([synth.token_f32(1, rank * N_TOKENS + t, D)
+                                   for t in range(N_TOKENS)])).to(dev)
+    y = torch.empty(D, dtype=torch.float32, device=dev)
+    ws = torch.empty(k.expert_gemv_workspace(D, F) // 4 + 4, dtype=torch.float32, device=dev)
+    perm = synth.permutation(E, synth.tag(synth.K_MISC, 1, 0, 7))
+
+    def step(i):
+        k.expert_gemv(y, X[i % N_TOKENS], views[int(perm[i % E])], D, F, ws)
+
+    ms, steps, clocks = _timed(args.steps, args.warmup, step, dev_index, world, 32)
+    args.steps = steps
+    per = ms / steps
+    nbytes = EXPERT_BYTES + 2 * D * 4
+    xh = torch.empty((N_TOKENS, D), dtype=torch.float32, pin_memory=True)
+    xh.copy_(X.cpu())
+    yh = torch.empty(D, dtype=torch.float32, pin_memory=True)
+    xd = torch.empty(D, dtype=torch.float32, device=dev)
+
+    def step_host(i):
+        xd.copy_(xh[i % N_TOKENS], non_blocking=True)
+        k.expert_gemv(y, xd, views[int(perm[i % E])], D, F, ws)
+        yh.copy_(y, non_blocking=True)
+
+    e2e = _e2e(step_host, min(steps, 5000), world, dev_index, D * 4, D * 4)
+    e2e["unit"] = "expert GEMVs/s"
+    line = _base_line("single MXFP4 expert GEMV (1 token, d=7168, f=1536) per second",
+                      round(steps * world / (ms * 1e-3), 2), "expert GEMVs/s", world, args, per,
+                      "mxfp4 weights (e2m1 + e8m0), fp32 activations and accumulation",
+                      {"workload": "expert_gemv_b1: one expert d=7168 f=1536 (17,547,264 B), "
+                                   "x fp32 [7168], y fp32 [7168]",
+                       "launch": "cuda graph of 32 steps, replayed",
+                       "l2": "inputs larger than L2: 896 distinct experts (15.7 GB) rotated"}, clocks)
+    line.update({"roofline": _roofline("k3_rows_t1 + k3_down_t1 (one expert, gate/up + SwiGLU, "
+                                       "down)", nbytes, per),
+                 "e2e": e2e, "gpu_launches": 2 * steps,
+                 "expert_hbm": {"bytes_per_gemv": nbytes, "gbs": round(nbytes / (per * 1e-3) / 1e9, 1)}})
+    return line
+
+
+def run_batched(args, rank, world, dev_index, T, bf16, use_bias):
+    """The layer on T tokens per step: the grouped path (router, top-k,
+    grouping by expert, grouped gate/up + SwiGLU, grouped down, combine)."""
+    import torch
+    import synth
+    from mxfp4_routed_expert_select_gb300 import k3moe as k
+    dev = torch.device("cuda", dev_index)
+    torch.cuda.set_device(dev)
+    blobs, views = build_pool(dev)
+    Wr_bits = synth.router_bf16(1, 0, E, D)
+    Wr0 = torch.from_numpy(Wr_bits.view(np.int16)).to(dev)
+    bias = None
+    if use_bias:
+        bias = torch.from_numpy(synth.bias_normal(1, 0, E).astype(np.float32)).to(dev)
+    NB = max(2, min(16, (1 << 28) // (T * D * (2 if bf16 else 4))))
+    n_r = 4 if T >= 1024 else 16
+    routers = [Wr0] + [Wr0.clone() for _ in range(n_r - 1)]
+    layers = [k.Layer(E, K, D, F, r, views, bias, max_tokens=T) for r in routers]
+    if bf16:
+        Xs = [torch.from_numpy(synth.tokens_bf16(1, T, D, t0=rank * NB * T + b * T).view(np.int16))
+              .to(dev).view(torch.bfloat16) for b in range(NB)]
+    else:
+        Xs = [torch.from_numpy(synth.tokens_f32(1, T, D, t0=rank * NB * T + b * T)).to(dev)
+              for b in range(NB)]
+    out = torch.empty((T, D), dtype=torch.float32, device=dev)
+    ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+
+    def step(i):
+        layers[i % n_r].forward(Xs[i % NB], T, out)
+
+    # distinct experts per batch (the weight bytes a batch must read)
+    U = []
+    for b in range(NB):
+        layers[0].forward(Xs[b], T, out, ids)
+        torch.cuda.synchronize()
+        U.append(len(np.unique(ids.cpu().numpy())))
+    Umean = statistics.mean(U)
+    graph_steps = 8 if T <= 64 else 0
+    ms, steps, clocks = _timed(args.steps, args.warmup, step, dev_index, world, graph_steps)
+    args.steps = steps
+    per = ms / steps
+    r_ms, gu_ms, dn_ms = _kernel_events(layers[0], lambda i: layers[0].forward(Xs[i % NB], T, out),
+                                        min(steps, 64 if T <= 64 else 8))
+    xb = T * D * (2 if bf16 else 4)
+    w_bytes = Umean * EXPERT_BYTES
+    step_bytes = w_bytes + ROUTER_BYTES + xb + T * D * 4
+    gu_bytes = Umean * 2 * (F * D // 2 + F * D // 32) + xb
+    flops = 2 * T * K * 3 * D * F + 2 * T * E * D
+    xh = torch.empty(tuple(Xs[0].shape), dtype=Xs[0].dtype, pin_memory=True)
+    xh.copy_(Xs[0].cpu())
+    oh = torch.empty((T, D), dtype=torch.float32, pin_memory=True)
+    xd = torch.empty_like(Xs[0])
+
+    def step_host(i):
+        xd.copy_(xh, non_blocking=True)
+        layers[i % n_r].forward(xd, T, out)
+        oh.copy_(out, non_blocking=True)
+
+    e2e = _e2e(step_host, min(steps, 200 if T <= 64 else 5), world, dev_index, xb, T * D * 4, T)
+    e2e["unit"] = "tokens/s"
+    name = "decode%d" % T if T <= 64 else "prefill%d" % T
+    desc = ("moe_layer_%s: 896 experts d=7168 f=1536 resident (15.7 GB), router bf16 [896x7168], "
+            "top-16, X %s [%dx7168]%s, grouped by expert" %
+            (name, "bf16" if bf16 else "fp32", T, ", selection bias ~N(0,1)" if use_bias else ""))
+    line = _base_line("MoE-layer tokens/s (%d tokens per step, 896 experts, top-16, MXFP4)" % T,
+                      round(steps * T * world / (ms * 1e-3), 2), "tokens/s", world, args, per,
+                      "mxfp4 weights (e2m1 + e8m0), %s activations, fp32 accumulation" %
+                      ("bf16" if bf16 else "fp32"),
+                      {"workload": desc, "global_batch": T * world, "seq_len": 1,
+                       "launch": ("cuda graph of %d steps, replayed" % graph_steps) if graph_steps
+                       else "host launch per step",
+                       "l2": "inputs larger than L2: %d token batches, %d router copies, %.0f distinct "
+                             "experts (%.2f GB) per batch" % (NB, n_r, Umean, w_bytes / 1e9)}, clocks)
+    line.update({
+        "roofline": _roofline("k3_grouped_rows (gate/up + SwiGLU over the batch's experts)",
+                              gu_bytes, statistics.mean(gu_ms)),
+        "step_bytes": {"distinct_experts": Umean, "bytes": int(step_bytes),
+                       "gbs": round(step_bytes / (per * 1e-3) / 1e9, 1)},
+        "tflops": round(flops / (per * 1e-3) / 1e12, 2),
+        "kernels_ms": {"route_topk": round(statistics.mean(r_ms), 4),
+                       "group_gate_up_swiglu": round(statistics.mean(gu_ms), 4),
+                       "down_combine": round(statistics.mean(dn_ms), 4)},
+        "e2e": e2e, "gpu_launches": 6 * steps})
+    for l in layers:
+        l.close()
+    return line
+
+
+def _mem_available():
+    try:
+        with open("/proc/meminfo") as fh:
+            for ln in fh:
+                if ln.startswith("MemAvailable:"):
+                    return int(ln.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def run_stream(args, rank, world, dev_index, n_layers=4, cache_bytes=8_000_000_000, n_tok=256):
+    """Host-streamed pool: n_layers x 896 experts in pinned host memory, an
+    HBM LRU cache of `cache_bytes`, batch-1 tokens through all layers with
+    RMSNorm + residual (k3moe_stream_decode)."""
+    import torch
+    import synth
+    from mxfp4_routed_expert_select_gb300 import k3moe as k
+    dev = torch.device("cuda", dev_index)
+    torch.cuda.set_device(dev)
+    eb = k.expert_bytes(D, F)
+    need = n_layers * E * eb
+    if _mem_available() < need + 32 * (1 << 30):
+        raise SystemExit("stream workload needs %.1f GB of host memory (+32 GB headroom); %.1f GB "
+                         "available" % (need / 1e9, _mem_available() / 1e9))
+    t0 = time.time()
+    host = torch.empty((n_layers * E, eb), dtype=torch.uint8, pin_memory=True)
+    for l in range(n_layers):
+        for e in range(E):
+            views = k.host_plane_views(host[l * E + e].data_ptr(), D, F)
+            ex = synth.expert(2, l, e, D, F)
+            for nm, arr in views.items():
+                arr[...] = ex[nm]
+    log("host pool: %d x %d experts (%.2f GB) in %.1f s" % (n_layers, E, need / 1e9, time.time() - t0))
+    layers = []
+    for l in range(n_layers):
+        Wr = torch.from_numpy(synth.router_bf16(2, l, E, D).view(np.int16)).to(dev)
+        b = torch.from_numpy(synth.bias_zipf(2, l, E).astype(np.float32)).to(dev)
+        layers.append(k.Layer(E, K, D, F, Wr, None, b, max_tokens=1))
+        layers[-1]._hold = (Wr, b)
+    base = host.data_ptr()
+    cache = k.Cache(cache_bytes, eb, [base + q * eb for q in range(n_layers * E)], n_layers, E)
+    n_w = max(args.warmup, 3)
+    X = torch.from_numpy(synth.tokens_f32(2, n_w + n_tok + 64, D, t0=rank * 100000)).to(dev)
+    out = torch.empty_like(X)
+    # the host link, measured in this run: pinned host -> HBM copies of one expert
+    probe = torch.empty(eb, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+    rates = []
+    for rep in range(3):  # the same 16 experts three times; the best pass counts
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        p0.record(s)
+        for q in range(16):
+            probe.copy_(host[(q * 37) % (n_layers * E)], non_blocking=True)
+        p1.record(s)
+        torch.cuda.synchronize()
+        rates.append(16 * eb / (p0.elapsed_time(p1) * 1e-3) / 1e9)
+    h2d_gbs = max(rates)
+    del probe
+    k.stream_decode(layers, cache, X[:n_w], n_w, out[:n_w], 1e-6, want_trace=False)
+    st0 = cache.stats()
+    clock = ClockSampler(dev_index)
+    clock.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    e0.record(s)
+    ids, hits = k.stream_decode(layers, cache, X[n_w:n_w + n_tok], n_tok, out[n_w:n_w + n_tok], 1e-6)
+    e1.record(s)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - w0
+    clocks = clock.stop()
+    ms = e0.elapsed_time(e1)
+    st1 = cache.stats()
+    look = st1["lookups"] - st0["lookups"]
+    nh = st1["hits"] - st0["hits"]
+    h2d = st1["h2d_bytes"] - st0["h2d_bytes"]
+    hbm = st1["hbm_bytes"] - st0["hbm_bytes"]
+    peak, src = measured_peaks()
+    ideal_s = (look * eb) / (peak * 1e9) + h2d / (h2d_gbs * 1e9)
+    # e2e: tokens from pinned host memory, the result read back, per token
+    xh = torch.empty((64, D), dtype=torch.float32, pin_memory=True)
+    xh.copy_(X[n_w + n_tok:].cpu())
+    oh = torch.empty((64, D), dtype=torch.float32, pin_memory=True)
+    xd = torch.empty(D, dtype=torch.float32, device=dev)
+    od = torch.empty(D, dtype=torch.float32, device=dev)
+
+    def step_host(i):
+        xd.copy_(xh[i], non_blocking=True)
+        k.stream_decode(layers, cache, xd, 1, od, 1e-6, want_trace=False)
+        oh[i].copy_(od, non_blocking=True)
+
+    n_e = 32
+    e2e = _e2e(step_host, n_e, world, dev_index, D * 4, D * 4)
+    e2e["unit"] = "tokens/s"
+    args.steps = n_tok
+    line = _base_line("host-streamed MoE decode tokens/s (4 layers x 896 experts in pinned host "
+                      "memory, 8 GB HBM LRU cache)", round(n_tok * world / (ms * 1e-3), 3), "tokens/s",
+                      world, args, ms / n_tok,
+                      "mxfp4 weights (e2m1 + e8m0), fp32 activations and accumulation",
+                      {"workload": "stream_decode_b1: %d layers x 896 experts d=7168 f=1536 (%.2f GB) "
+                                   "in pinned host memory, HBM LRU cache %.1f GB (%d slots), %d tokens, "
+                                   "RMSNorm + residual, Zipf(1.1) selection bias" %
+                                   (n_layers, need / 1e9, cache_bytes / 1e9, st1["slots"], n_tok),
+                       "global_batch": world, "seq_len": 1,
+                       "launch": "host loop in the library (rmsnorm, route, ids to host, cache acquire, "
+                                 "experts, residual, release)",
+                       "l2": "inputs larger than L2 (expert slots 17.5 MB each, 64 per token)",
+                       "warmup_tokens": n_w}, clocks)
+    line.update({
+        "cache": {"lookups": look, "hits": nh, "hit_rate": round(nh / max(look, 1), 4),
+                  "h2d_bytes": h2d, "hbm_expert_bytes": hbm,
+                  "h2d_bytes_per_token": round(h2d / n_tok), "hbm_bytes_per_token": round(hbm / n_tok),
+                  "slots": st1["slots"]},
+        "host_link_gbs": round(h2d_gbs, 1), "host_link_probe_passes_gbs": [round(r, 1) for r in rates],
+        "h2d_achieved_gbs": round(h2d / (ms * 1e-3) / 1e9, 1),
+        "roofline": {"kernel": "whole step (expert bytes from HBM + misses over the host link)",
+                     "bound": "hbm+host-link", "achieved": round(ideal_s / (ms * 1e-3), 4),
+                     "peak": 1.0, "peak_source": "ideal time = hits and misses at %s HBM %.0f GB/s and "
+                     "measured host link %.1f GB/s" % (src, peak, h2d_gbs), "unit": "ideal/measured",
+                     "frac": round(ideal_s / (ms * 1e-3), 4), "traffic": None},
+        "wall_s": round(wall, 3), "e2e": e2e, "gpu_launches": 5 * n_layers * n_tok})
+    cache.close()
+    for l in layers:
+        l.close()
+    return line
+
+
+WORKLOADS = {
+    "expert": lambda a, r, w, d: run_expert(a, r, w, d),
+    "decode64": lambda a, r, w, d: run_batched(a, r, w, d, 64, False, False),
+    "prefill4096": lambda a, r, w, d: run_batched(a, r, w, d, 4096, True, True),
+    "stream": lambda a, r, w, d: run_stream(a, r, w, d),
+}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -425,6 +811,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch every step from the host")
+    ap.add_argument("--workload", default="decode1", choices=["decode1"] + sorted(WORKLOADS))
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -447,6 +834,13 @@ def main():
     if world > 1:
         torch.distributed.barrier()
         __graft_entry__.build()
+    if args.workload != "decode1":
+        res = WORKLOADS[args.workload](args, rank, world, local)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
     res = run_ours(args, rank, world, local)
     if rank == 0:
         if not args.no_cpu_baseline:

@@ -370,6 +370,39 @@ int k3moe_cache_create_with_copier(k3moe_cache **host_out, size_t capacity_bytes
 /* Slot index that holds `key`, or -1 (for tests). */
 int32_t k3moe_cache_slot_of(const k3moe_cache *C, int64_t key);
 
+/* --------------------------------------------------- streamed decode loop */
+
+/*
+ * Batch-1 decode of T tokens through n_layers MoE layers whose experts live
+ * in host memory behind an expert cache (the pages' streaming design [EXPL,
+ * "The cache the project exists for"; HOW, "The LRU cache"], with the host
+ * pool in pinned RAM instead of NVMe).  For every token t and layer l:
+ *   u   = x / sqrt(mean(x^2) + eps)                 (RMSNorm, unit gain)
+ *   ids, w = top-k routing of u by layer l's router (+ selection bias)
+ *   the k ids go to the host (one small D2H copy; the stream is synchronised)
+ *   slots = k3moe_cache_acquire(keys l * n_experts + ids)   (misses copied)
+ *   x  += sum_j w_j * expert_{ids_j}(u)              (experts read from slots)
+ *   k3moe_cache_release
+ *  desc.host_layers  host array of n_layers layers (router-only layers are
+ *                    fine: created with host_experts = NULL); all with the
+ *                    same n_experts, top_k, d, f; top_k <= 16
+ *  desc.cache        keys layer * n_experts + expert, blobs of
+ *                    k3moe_expert_bytes(d, f)
+ *  X  fp32 [T x d] input hidden states, out fp32 [T x d] after the last layer
+ *  host_ids_out  optional int32 [T][n_layers][top_k] (ascending ids)
+ *  host_hit_out  optional uint8 [T][n_layers][top_k] cache hit flags
+ * Returns the first failing status (the cache's K3MOE_EBUSY included).
+ */
+typedef struct {
+    int32_t n_layers;
+    k3moe_layer *const *host_layers;
+    k3moe_cache *cache;
+    float eps;
+} k3moe_stream_desc;
+
+int k3moe_stream_decode(const k3moe_stream_desc *host_desc, const float *X, int32_t T, float *out,
+                        int32_t *host_ids_out, uint8_t *host_hit_out, k3moe_stream s);
+
 #ifdef __cplusplus
 }
 #endif

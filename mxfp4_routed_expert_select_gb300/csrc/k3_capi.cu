@@ -5,6 +5,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "k3_device.cuh"
 
@@ -483,3 +484,96 @@ int k3moe_residual_add(float *x, const float *delta, int32_t n, k3moe_stream s)
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------ streamed decode loop
+
+extern "C" int k3moe_stream_decode(const k3moe_stream_desc *D, const float *X, int32_t T,
+                                   float *out, int32_t *host_ids_out, uint8_t *host_hit_out,
+                                   k3moe_stream s)
+{
+    if (!D || !D->host_layers || !D->cache || D->n_layers <= 0 || !X || !out || T <= 0 ||
+        !(D->eps >= 0.f) || !aligned16(X) || !aligned16(out))
+        return K3MOE_EINVAL;
+    const k3moe_layer *L0 = D->host_layers[0];
+    if (!L0) return K3MOE_EINVAL;
+    const int E = L0->E, k = L0->k, d = L0->d, f = L0->f;
+    if (k > k3::kMaxInline) return K3MOE_EINVAL;
+    for (int l = 0; l < D->n_layers; l++) {
+        const k3moe_layer *L = D->host_layers[l];
+        if (!L || L->E != E || L->k != k || L->d != d || L->f != f) return K3MOE_EINVAL;
+    }
+    cudaStream_t st = cs(s);
+    float *xcur = nullptr, *u = nullptr, *delta = nullptr, *wdev = nullptr;
+    int32_t *iddev = nullptr, *idhost = nullptr;
+    int rc = K3MOE_OK;
+    auto fail = [&](int code) {
+        if (rc == K3MOE_OK) rc = code;
+    };
+    if (cudaMalloc(&xcur, sizeof(float) * d) != cudaSuccess ||
+        cudaMalloc(&u, sizeof(float) * d) != cudaSuccess ||
+        cudaMalloc(&delta, sizeof(float) * d) != cudaSuccess ||
+        cudaMalloc(&wdev, sizeof(float) * k) != cudaSuccess ||
+        cudaMalloc(&iddev, sizeof(int32_t) * k) != cudaSuccess ||
+        cudaMallocHost(&idhost, sizeof(int32_t) * k) != cudaSuccess) {
+        cudaGetLastError();
+        fail(K3MOE_ENOMEM);
+    }
+    std::vector<int64_t> keys(k);
+    std::vector<void *> blobs(k);
+    std::vector<uint8_t> hits(k);
+    std::vector<k3moe_expert> views(k);
+    for (int t = 0; t < T && rc == K3MOE_OK; t++) {
+        if (cudaMemcpyAsync(xcur, X + (size_t)t * d, sizeof(float) * d, cudaMemcpyDeviceToDevice,
+                            st) != cudaSuccess) {
+            fail(K3MOE_ECUDA);
+            break;
+        }
+        for (int l = 0; l < D->n_layers && rc == K3MOE_OK; l++) {
+            k3moe_layer *L = D->host_layers[l];
+            int r = k3moe_rmsnorm(u, xcur, d, D->eps, s);
+            if (r == K3MOE_OK) r = k3moe_layer_route(L, u, K3MOE_F32, 1, iddev, wdev, s);
+            if (r != K3MOE_OK) {
+                fail(r);
+                break;
+            }
+            if (cudaMemcpyAsync(idhost, iddev, sizeof(int32_t) * k, cudaMemcpyDeviceToHost, st) !=
+                    cudaSuccess ||
+                cudaStreamSynchronize(st) != cudaSuccess) {
+                cudaGetLastError();
+                fail(K3MOE_ECUDA);
+                break;
+            }
+            for (int j = 0; j < k; j++) keys[j] = (int64_t)l * E + idhost[j];
+            r = k3moe_cache_acquire(D->cache, keys.data(), k, blobs.data(), hits.data(), s);
+            if (r != K3MOE_OK) {
+                fail(r);
+                break;
+            }
+            for (int j = 0; j < k && r == K3MOE_OK; j++) r = k3moe_expert_view(&views[j], blobs[j], d, f);
+            if (r == K3MOE_OK) r = k3moe_layer_experts_t1(L, u, views.data(), wdev, k, delta, s);
+            if (r == K3MOE_OK) r = k3moe_residual_add(xcur, delta, d, s);
+            const int rr = k3moe_cache_release(D->cache, s);
+            if (r == K3MOE_OK) r = rr;
+            if (r != K3MOE_OK) {
+                fail(r);
+                break;
+            }
+            const size_t o = ((size_t)t * D->n_layers + l) * k;
+            if (host_ids_out) memcpy(host_ids_out + o, idhost, sizeof(int32_t) * k);
+            if (host_hit_out) memcpy(host_hit_out + o, hits.data(), k);
+        }
+        if (rc == K3MOE_OK &&
+            cudaMemcpyAsync(out + (size_t)t * d, xcur, sizeof(float) * d, cudaMemcpyDeviceToDevice,
+                            st) != cudaSuccess)
+            fail(K3MOE_ECUDA);
+    }
+    cudaStreamSynchronize(st);
+    cudaGetLastError();
+    cudaFree(xcur);
+    cudaFree(u);
+    cudaFree(delta);
+    cudaFree(wdev);
+    cudaFree(iddev);
+    cudaFreeHost(idhost);
+    return rc;
+}

@@ -61,6 +61,11 @@ class CacheStats(ctypes.Structure):
         return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
 
 
+class StreamDesc(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("host_layers", ctypes.c_void_p),
+                ("cache", ctypes.c_void_p), ("eps", ctypes.c_float)]
+
+
 ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
                             ctypes.POINTER(ctypes.c_void_p))
 FREE_FN = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p)
@@ -107,6 +112,7 @@ SIGNATURES = {
     "k3moe_cache_histogram": (ctypes.POINTER(ctypes.c_uint32), [_P]),
     "k3moe_cache_create_with_copier": (ctypes.c_int, [_P, _SZ, _SZ, _P, _I, _I, _P]),
     "k3moe_cache_slot_of": (_I, [_P, _I64]),
+    "k3moe_stream_decode": (ctypes.c_int, [_P, _P, _I, _P, _P, _P, _P]),
 }
 
 _lib = None
@@ -355,3 +361,19 @@ class Cache:
             self.close()
         except Exception:
             pass
+
+
+def stream_decode(layers, cache, X, T, out, eps=1e-6, stream=None, want_trace=True):
+    """k3moe_stream_decode: T tokens through len(layers) layers over `cache`.
+    Returns (ids [T, L, k], hits [T, L, k]) as numpy arrays when want_trace."""
+    nl = len(layers)
+    arr = (ctypes.c_void_p * nl)(*[l.h.value for l in layers])
+    desc = StreamDesc(nl, ctypes.cast(arr, ctypes.c_void_p), cache.h.value, eps)
+    kk = layers[0].k
+    ids = np.zeros((T, nl, kk), np.int32) if want_trace else None
+    hits = np.zeros((T, nl, kk), np.uint8) if want_trace else None
+    check(lib().k3moe_stream_decode(ctypes.byref(desc), _ptr(X), T, _ptr(out),
+                                    None if ids is None else ids.ctypes.data,
+                                    None if hits is None else hits.ctypes.data, _stream(stream)),
+          "k3moe_stream_decode")
+    return ids, hits
