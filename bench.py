@@ -343,13 +343,13 @@ def run_ours(args, rank, world, dev_index):
         "vs_baseline": None,
         "dtype": "mxfp4 weights (e2m1 + e8m0), fp32 activations and accumulation",
         "data": "synthetic (seeded SplitMix64: uniform E2M1 codes, E8M0 in [120,130], x ~ N(0,1), W_r ~ N(0,0.02) bf16)",
-        "config": {"workload": "moe_layer_decode_b1: 896 experts d=7168 f=1536 resident (15.7 GB), "
-                               "router bf16 [896x7168], top-16, softmax combine",
+        "config": {"workload": "moe_layer_decode_b1: %d experts d=7168 f=1536 resident (%.1f GB), "
+                               "router bf16 [%dx7168], top-16, softmax combine" % (E, E * EXPERT_BYTES / 1e9, E),
                    "global_batch": world, "seq_len": 1, "parallelism": "replicas" if world > 1 else "single",
                    "launch": "cuda graph of 32 steps, replayed" if graph is not None else "host launch per step",
-                   "l2": "inputs larger than L2: %d rotated router copies (%.0f MB) + 896 experts "
+                   "l2": "inputs larger than L2: %d rotated router copies (%.0f MB) + %d experts "
                          "(16 random per token, 281 MB/token) + %d distinct tokens"
-                         % (N_ROUTER_COPIES, N_ROUTER_COPIES * ROUTER_BYTES / 1e6, N_TOKENS)},
+                         % (N_ROUTER_COPIES, N_ROUTER_COPIES * ROUTER_BYTES / 1e6, E, N_TOKENS)},
         "layer_hbm": {"bytes_per_token": LAYER_BYTES, "gbs": round(layer_gbs, 1),
                       "frac_of_peak": round(layer_gbs / peak, 4), "frac_of_8tbs": round(layer_gbs / 8000, 4)},
         "kernels_ms": ({"fused_layer": round(k_ms, 5), "fused_layer_eager_events": round(eager_ms, 5),
@@ -637,9 +637,10 @@ def run_batched(args, rank, world, dev_index, T, bf16, use_bias):
     e2e = _e2e(step_host, min(steps, 200 if T <= 64 else 5), world, dev_index, xb, T * D * 4, T)
     e2e["unit"] = "tokens/s"
     name = "decode%d" % T if T <= 64 else "prefill%d" % T
-    desc = ("moe_layer_%s: 896 experts d=7168 f=1536 resident (15.7 GB), router bf16 [896x7168], "
+    desc = ("moe_layer_%s: %d experts d=7168 f=1536 resident (%.1f GB), router bf16 [%dx7168], "
             "top-16, X %s [%dx7168]%s, grouped by expert" %
-            (name, "bf16" if bf16 else "fp32", T, ", selection bias ~N(0,1)" if use_bias else ""))
+            (name, E, E * EXPERT_BYTES / 1e9, E, "bf16" if bf16 else "fp32", T,
+             ", selection bias ~N(0,1)" if use_bias else ""))
     line = _base_line("MoE-layer tokens/s (%d tokens per step, 896 experts, top-16, MXFP4)" % T,
                       round(steps * T * world / (ms * 1e-3), 2), "tokens/s", world, args, per,
                       "mxfp4 weights (e2m1 + e8m0), %s activations, fp32 accumulation" %
@@ -650,7 +651,8 @@ def run_batched(args, rank, world, dev_index, T, bf16, use_bias):
                        "l2": "inputs larger than L2: %d token batches, %d router copies, %.0f distinct "
                              "experts (%.2f GB) per batch" % (NB, n_r, Umean, w_bytes / 1e9)}, clocks)
     line.update({
-        "roofline": _roofline("k3_grouped_rows (gate/up + SwiGLU over the batch's experts)",
+        "roofline": _roofline("k3_tc_expert<0> (tcgen05 gate/up + SwiGLU over the batch's experts, "
+                              "with the token gather and tile plan)",
                               gu_bytes, statistics.mean(gu_ms)),
         "step_bytes": {"distinct_experts": Umean, "bytes": int(step_bytes),
                        "gbs": round(step_bytes / (per * 1e-3) / 1e9, 1)},
@@ -812,7 +814,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch every step from the host")
     ap.add_argument("--workload", default="decode1", choices=["decode1"] + sorted(WORKLOADS))
+    ap.add_argument("--experts", type=int, default=896,
+                    help="experts per layer (smaller pools for profiler captures; 896 is the workload)")
     args = ap.parse_args()
+    global E, ROUTER_BYTES, LAYER_BYTES
+    E = args.experts
+    ROUTER_BYTES = E * D * 2
+    LAYER_BYTES = K * EXPERT_BYTES + ROUTER_BYTES
     if args.warmup < 3:
         args.warmup = 3
     rank = int(os.environ.get("RANK", "0"))

@@ -238,12 +238,22 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int x_dtype, int32_t T, f
  *                      (two FMAs per weight, fp32-class products).  The
  *                      rounding adds a relative error of order 2^-12 per
  *                      activation; the router is fp32 either way.
+ *  K3MOE_OPT_TC        multi-token forwards (and bf16 batch-1 forwards) of a
+ *                      layer created with max_tokens > 1 run the expert
+ *                      products as grouped tcgen05 MMAs: weights decoded
+ *                      exactly to bf16 in shared memory, fp32 activations and
+ *                      the SwiGLU output split into bf16 hi + lo (16
+ *                      significant bits), fp32 accumulation, the weighted
+ *                      combine by fp32 atomic adds (summation order not
+ *                      fixed).  Needs d % 256 == 0 and f % 256 == 0; default 1.
+ *                      0 selects the CUDA-core grouped path.
  * k3moe_layer_fused_t1 returns 1 when a batch-1 fp32 forward of this layer
  * would run fused, else 0 (negative on error).  After a device-side timeout
  * (k3moe_device_error() == K3MOE_ETIMEOUT) a layer must be recreated.
  */
 #define K3MOE_OPT_FUSED_T1 1
 #define K3MOE_OPT_ACT_F16  2
+#define K3MOE_OPT_TC       4
 int k3moe_layer_set_option(k3moe_layer *L, int32_t option, int32_t value);
 int k3moe_layer_fused_t1(const k3moe_layer *L);
 

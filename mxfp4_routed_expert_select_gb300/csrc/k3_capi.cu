@@ -45,6 +45,18 @@ int launch_route_multi(const void *X, int xdt, int T, const uint16_t *Wr, int E,
 int launch_group(const int32_t *ids, int npairs, int E, int nt, int32_t *offsets, int32_t *perm,
                  int4 *items, int32_t *n_items, cudaStream_t s);
 int grouped_nt();
+bool tc_supported(int E, int k, int d, int f);
+int tc_max_tiles(int npairs, int E, int tn);
+size_t tc_max_rows(int npairs, int E);
+size_t tc_tile_bytes();
+size_t tc_map_bytes();
+int tc_make_maps(const DevExpert *host_table, int E, int d, int f, void *dev_maps);
+int launch_tc_gateup(const void *X, int xdt, int k, int E, int d, int f, const DevExpert *table,
+                     const void *maps, const int32_t *offsets, const int32_t *perm, void *tiles,
+                     int32_t *n_tiles, int max_tiles, uint8_t *Xg, uint8_t *Hg, int *err, cudaStream_t s);
+int launch_tc_down(int T, int k, int d, int f, const DevExpert *table, const void *maps, const int32_t *perm,
+                   const float *wsel, const void *tiles, const int32_t *n_tiles, const uint8_t *Hg, float *out,
+                   int *err, cudaStream_t s);
 int launch_grouped_gateup(const void *X, int xdt, const DevExpert *table, const int32_t *perm,
                           const int4 *items, const int32_t *n_items, int max_items, int k, int d,
                           int f, float *h, cudaStream_t s);
@@ -243,13 +255,23 @@ struct k3moe_layer {
     bool fused;          // K3MOE_OPT_FUSED_T1
     bool act16;          // K3MOE_OPT_ACT_F16
     unsigned long long *ctr;  // monotonic cross-CTA counters of the fused kernel
+    // tensor-core grouped path (T > 1)
+    bool tc;             // K3MOE_OPT_TC (default on where supported)
+    bool tc_ready;       // its buffers and tensor maps exist
+    void *tc_tiles;      // [tc_max_tiles] tiles
+    int32_t *tc_ntiles;  // [1]
+    int tc_max_tiles;
+    uint8_t *Xg;         // token rows, bf16, tile-major
+    uint8_t *Hg;         // SwiGLU rows (hi, lo), bf16, tile-major
+    void *tc_maps;       // [E][3] tensor maps of the packed planes
 };
 
 static void layer_free(k3moe_layer *L)
 {
     if (!L) return;
     void *ptrs[] = {L->table, L->logits, L->part,  L->ids,     L->w,      L->h,    L->Y,
-                    L->offsets, L->perm, L->items, L->n_items, L->ticket, L->ctr};
+                    L->offsets, L->perm, L->items, L->n_items, L->ticket, L->ctr,
+                    L->tc_tiles, L->tc_ntiles, L->Xg, L->Hg, L->tc_maps};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete L;
@@ -301,6 +323,17 @@ int k3moe_layer_create(k3moe_layer **out, const k3moe_layer_desc *D)
     alloc((void **)&L->n_items, sizeof(int32_t));
     alloc((void **)&L->ticket, sizeof(unsigned));
     alloc((void **)&L->ctr, sizeof(unsigned long long) * k3::fused_t1_counters());
+    if (L->maxT > 1 && D->host_experts && k3::tc_supported(L->E, L->k, L->d, L->f)) {
+        L->tc_max_tiles = k3::tc_max_tiles((int)pairs, L->E, 64);
+        const size_t rows = k3::tc_max_rows((int)pairs, L->E);
+        alloc(&L->tc_tiles, k3::tc_tile_bytes() * L->tc_max_tiles);
+        alloc((void **)&L->tc_ntiles, sizeof(int32_t));
+        alloc((void **)&L->Xg, rows * L->d * 2);
+        alloc((void **)&L->Hg, rows * L->f * 2);
+        alloc(&L->tc_maps, k3::tc_map_bytes() * 3 * L->E);
+        L->tc_ready = ok;
+        L->tc = true;
+    }
     L->fused = true;
     L->act16 = false;
     if (!ok) {
@@ -320,6 +353,8 @@ int k3moe_layer_create(k3moe_layer **out, const k3moe_layer_desc *D)
     }
     L->router_only = D->host_experts == nullptr;
     cudaError_t st = cudaMemcpy(L->table, tmp, sizeof(DevExpert) * L->E, cudaMemcpyHostToDevice);
+    if (st == cudaSuccess && L->tc_ready && k3::tc_make_maps(tmp, L->E, L->d, L->f, L->tc_maps) != K3MOE_OK)
+        L->tc_ready = false;  // the CUDA-core grouped path serves instead
     free(tmp);
     if (st == cudaSuccess) st = cudaMemset(L->ticket, 0, sizeof(unsigned));
     if (st == cudaSuccess)
@@ -400,6 +435,16 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int xdt, int32_t T, float
         K3_TRY(k3::launch_rows_t1(1, (const float *)X, src, L->k, L->d, L->f, L->h, st));
         if (L->nev) K3_CUDA(cudaEventRecord(L->ev[2], st));
         K3_TRY(k3::launch_down_t1(L->h, src, L->w, L->k, L->d, L->f, out, st));
+    } else if (L->tc && L->tc_ready) {
+        int *err = k3::device_error_word();
+        K3_TRY(k3::launch_group(L->ids, T * L->k, L->E, k3::grouped_nt(), L->offsets, L->perm,
+                                L->items, L->n_items, st));
+        K3_TRY(k3::launch_tc_gateup(X, xdt, L->k, L->E, L->d, L->f, L->table, L->tc_maps, L->offsets,
+                                    L->perm, L->tc_tiles, L->tc_ntiles, L->tc_max_tiles, L->Xg, L->Hg,
+                                    err, st));
+        if (L->nev) K3_CUDA(cudaEventRecord(L->ev[2], st));
+        K3_TRY(k3::launch_tc_down(T, L->k, L->d, L->f, L->table, L->tc_maps, L->perm, L->w,
+                                  L->tc_tiles, L->tc_ntiles, L->Hg, out, err, st));
     } else {
         const int npairs = T * L->k;
         K3_TRY(k3::launch_group(L->ids, npairs, L->E, k3::grouped_nt(), L->offsets, L->perm,
@@ -430,6 +475,10 @@ int k3moe_layer_set_option(k3moe_layer *L, int32_t option, int32_t value)
     }
     if (option == K3MOE_OPT_ACT_F16) {
         L->act16 = value != 0;
+        return K3MOE_OK;
+    }
+    if (option == K3MOE_OPT_TC) {
+        L->tc = value != 0;
         return K3MOE_OK;
     }
     return K3MOE_EINVAL;

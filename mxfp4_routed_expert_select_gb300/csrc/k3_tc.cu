@@ -1,0 +1,852 @@
+// k3_tc.cu -- grouped expert products on the tensor cores (tcgen05 + TMEM).
+//
+// Multi-token batches (decode batches, prefill) group the (token, slot) pairs
+// by expert, so every expert matrix meets a block of tokens and the work is a
+// dense grouped contraction.  The pages give the per-expert products
+// ("kimi-k3-in-c" explainer, "Reduction one": E2M1 codes, one E8M0 scale per
+// 32 weights); here they run as MMAs:
+//
+//   weights  E2M1 * 2^(e-127) is exact in bf16 (2 significant bits, bf16 has
+//            8 exponent bits), so decode warps turn the packed nibbles into
+//            bf16 in shared memory, exactly, in the 128-byte-swizzled K-major
+//            layout the MMA reads.  The packed bytes never exist as floats in
+//            global memory.
+//   tokens   fp32 activations are split x = hi + lo, hi = bf16(x),
+//            lo = bf16(x - hi) (16 significant bits, relative 2^-17); both
+//            halves are columns of the same MMA and are added in the
+//            epilogue.  bf16 activations need no split.
+//   h        the SwiGLU output is split the same way for the down product.
+//   products bf16 x bf16 -> fp32 accumulation in TMEM (tcgen05.mma
+//            kind::f16, M = 128 weight rows, N = the tile's token columns).
+//
+// Per step: k3_tc_plan cuts every expert's pairs into tiles of at most TN
+// tokens; k3_tc_gather writes each tile's token rows (bf16, pre-swizzled,
+// k-step-major so a k-step of a tile is one contiguous block); k3_tc_expert<0>
+// computes h for (tile, 128 rows of f) units; k3_tc_expert<1> computes the
+// down product for (tile, 128 rows of d) units and adds w * y into the output
+// (fp32 atomics: the order of the k additions of a token is not fixed).
+//
+// One persistent CTA per SM, 15 warps:
+//   warp 0      TMA of packed weight tiles (128 rows x 128 bytes per matrix,
+//               one tensor map per expert matrix) into a staging ring
+//   warp 1      bulk copies of token tiles, one per k-step, into a ring of
+//               2 KB slots (a k-step takes N/16 slots, so narrow tiles run
+//               up to 16 k-steps ahead and wide ones as far as space allows)
+//   warp 2      TMEM owner; lane 0 issues the MMAs and commits
+//   warps 3-10  decoders: staged nibbles -> bf16, two threads per weight row
+//   warps 11-14 epilogue: TMEM -> registers -> SwiGLU / weighted combine
+// Every wait is bounded (2 s); a timeout sets the device error word, the CTA
+// drains its copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "k3_device.cuh"
+
+namespace k3 {
+
+struct TcTile {
+    int32_t expert, pair_begin, n, nx, nh, xrow0, hrow0, pad;
+};
+
+namespace {
+
+constexpr int TC_M = 128;           // weight rows per unit (MMA M)
+constexpr int TC_KS = 64;           // K per k-step: one 128-byte bf16 row
+constexpr int TC_SS = 256;          // K per staging step: 128 packed bytes per row
+constexpr int TC_KPS = TC_SS / TC_KS;
+constexpr int W_PK = 0, W_B = 1, W_MMA = 2, W_DEC = 3;
+constexpr int TC_NB = 16;           // token k-steps in flight at most
+constexpr int TC_SLOT = 2048;       // token ring granularity: 16 rows x 128 bytes
+constexpr uint32_t TC_TMEM_COLS = 512;
+
+template <int PH>
+struct TcCfg {
+    static constexpr int NA = PH == 0 ? 2 : 1;                // matrices per unit
+    static constexpr int SA = PH == 0 ? 3 : 4;                // decoded-weight stages
+    static constexpr int SP = PH == 0 ? 2 : 3;                // packed staging stages
+    static constexpr int NSLOT = PH == 0 ? 32 : 56;           // token ring slots
+    static constexpr int BMAX = PH == 0 ? 128 : 256;          // token rows per k-step
+    static constexpr int A_BYTES = NA * TC_M * 128;
+    static constexpr int PK_BYTES = NA * TC_M * 128;          // swizzled like the operands
+    static constexpr int PK_OFF = SA * A_BYTES;
+    static constexpr int B_OFF = PK_OFF + SP * PK_BYTES;
+    static constexpr int BAR_OFF = B_OFF + NSLOT * TC_SLOT;
+    static constexpr int SMEM = BAR_OFF + 512 + 1024;         // + barriers + alignment slack
+    static constexpr int DEC = 8;                             // decoder warps
+    static constexpr int IPP = NA * 2 / (DEC / 4);            // 32-groups per thread per k-step
+    static constexpr int W_EPI = W_DEC + DEC;
+    static constexpr int THREADS = (W_EPI + 4) * 32;
+    static_assert(IPP == 1 || IPP == 2, "decoder split");
+    static_assert(BMAX / 16 <= NSLOT / 2, "token ring too small");
+};
+
+K3_DEV uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (stride byte offset), descriptor version 1.
+K3_DEV uint64_t sw128_desc(uint32_t saddr)
+{
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, M = 128, N = n (multiple of 16, <= 256).
+K3_DEV uint32_t bf16_idesc(int n)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TC_M >> 4) << 24);
+}
+K3_DEV void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+                 "l"(a), "l"(b), "r"(idesc), "r"(acc)
+                 : "memory");
+}
+K3_DEV void mma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+K3_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+K3_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+K3_DEV void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 2D tiled TMA load (x = byte column, a multiple of 16; y = row).
+K3_DEV void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+                 "%3}], [%4];" ::"r"(dst),
+                 "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+                 : "memory");
+}
+
+// 16 consecutive fp32 columns of TMEM for this warp's 32 lanes.
+K3_DEV void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+                 "%11, %12, %13, %14, %15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+                   "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+K3_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+K3_DEV uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// f16 bits of 2^(e-127) when that is a normal f16 (e in [113, 142]), else 0
+// with ok = false.  The NaN byte 255 gives 0 (the group is dropped), ok.
+K3_DEV uint16_t e8m0_f16(uint32_t e, bool &ok)
+{
+    ok = true;
+    if (e == 255u) return 0;
+    if (e >= 113u && e <= 142u) return (uint16_t)((e - 112u) << 10);
+    ok = false;
+    return 0;
+}
+
+// Eight codes (one word) times the group scale -> eight exact bf16 values.
+// Fast form: f16 code * f16 scale in fp32 (exact), the bf16 is the high half.
+K3_DEV uint4 decode8_bf16(uint32_t w, uint16_t sc)
+{
+    uint32_t h0, h1, h2, h3;
+    e2m1x8_to_half2x4(w, h0, h1, h2, h3);
+    uint4 o;
+    o.x = prmt(__float_as_uint(mfma(lo16(h0), sc, 0.f)), __float_as_uint(mfma(hi16(h0), sc, 0.f)), 0x7632u);
+    o.y = prmt(__float_as_uint(mfma(lo16(h1), sc, 0.f)), __float_as_uint(mfma(hi16(h1), sc, 0.f)), 0x7632u);
+    o.z = prmt(__float_as_uint(mfma(lo16(h2), sc, 0.f)), __float_as_uint(mfma(hi16(h2), sc, 0.f)), 0x7632u);
+    o.w = prmt(__float_as_uint(mfma(lo16(h3), sc, 0.f)), __float_as_uint(mfma(hi16(h3), sc, 0.f)), 0x7632u);
+    return o;
+}
+// General form for any scale byte: fp32 multiply by 2^(e-127).
+K3_DEV uint4 decode8_bf16_any(uint32_t w, float s)
+{
+    uint32_t h[4];
+    e2m1x8_to_half2x4(w, h[0], h[1], h[2], h[3]);
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const float2 f = h2f2(h[i]);
+        o[i] = prmt(__float_as_uint(f.x * s), __float_as_uint(f.y * s), 0x7632u);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+K3_DEV bool tc_wait(uint32_t bar, uint32_t parity, int *err, volatile int *abort_flag)
+{
+    if (*abort_flag) return false;
+    if (!mbar_wait(bar, parity, err)) {
+        *abort_flag = 1;
+        return false;
+    }
+    return true;
+}
+
+K3_DEV uint32_t bf16_rn_bits(float v) { return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+
+struct TcArgs {
+    const TcTile *tiles;
+    const int32_t *n_tiles;
+    const DevExpert *table;
+    const CUtensorMap *maps;  // [E][3]: gate, up, down packed planes
+    const uint8_t *Bsrc;      // token rows (phase 0) or h rows (phase 1)
+    uint8_t *Hg;              // phase 0 output
+    float *out;               // phase 1 output [T x d]
+    const int32_t *perm;
+    const float *wsel;
+    int k, d, f;
+    int *err;
+};
+
+}  // namespace
+
+template <int PH>
+__global__ void __launch_bounds__(TcCfg<PH>::THREADS, 1) k3_tc_expert(const TcArgs a)
+{
+    using C = TcCfg<PH>;
+    constexpr int W_EPI = C::W_EPI;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sbase = smem_addr(sm);
+    uint64_t *bars = (uint64_t *)(sm + C::BAR_OFF);
+    const int B_PKF = 0, B_PKE = B_PKF + C::SP, B_AF = B_PKE + C::SP, B_AE = B_AF + C::SA, B_BF = B_AE + C::SA,
+              B_BE = B_BF + TC_NB, B_ACCF = B_BE + TC_NB, B_ACCE = B_ACCF + 2, B_FIN = B_ACCE + 2,
+              NBARS = B_FIN + 1;
+    volatile uint32_t *boff = (volatile uint32_t *)(bars + NBARS);  // [TC_NB] token ring offsets
+    uint32_t *tmem_slot = (uint32_t *)(boff + TC_NB);
+    volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+    auto bar = [&](int i) { return smem_addr(bars + i); };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int K = PH == 0 ? a.d : a.f;     // reduction length
+    const int ROWS = PH == 0 ? a.f : a.d;  // weight rows per matrix
+    const int nrb = ROWS / TC_M;
+    const int nss = K / TC_SS;
+    const int nks = K / TC_KS;
+    const int n_units = *a.n_tiles * nrb;
+    // Every role walks the same units (u = blockIdx.x, += gridDim.x) and
+    // fetches the next unit's tile record one unit ahead.
+    auto tile_at = [&](int v) -> TcTile {
+        TcTile t = {};
+        if (v < n_units) t = a.tiles[v / nrb];
+        return t;
+    };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::SP; i++) {
+            mbar_init(bar(B_PKF + i), 1);
+            mbar_init(bar(B_PKE + i), C::DEC);
+        }
+        for (int i = 0; i < C::SA; i++) {
+            mbar_init(bar(B_AF + i), C::DEC);
+            mbar_init(bar(B_AE + i), 1);
+        }
+        for (int i = 0; i < TC_NB; i++) {
+            mbar_init(bar(B_BF + i), 1);
+            mbar_init(bar(B_BE + i), 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(bar(B_ACCF + i), 1);
+            mbar_init(bar(B_ACCE + i), 4);
+        }
+        mbar_init(bar(B_FIN), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == W_MMA) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(TC_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *(volatile uint32_t *)tmem_slot;
+
+    auto a_stage = [&](int s) { return sbase + (uint32_t)(s * C::A_BYTES); };
+    auto pk_stage = [&](int s) { return sbase + (uint32_t)(C::PK_OFF + s * C::PK_BYTES); };
+    const uint32_t b_ring = sbase + (uint32_t)C::B_OFF;
+
+    if (warp == W_PK) {
+        // ------------------------------------------------ packed weight tiles
+        uint32_t it = 0;
+        uint32_t issued[C::SP];
+#pragma unroll
+        for (int i = 0; i < C::SP; i++) issued[i] = 0;
+        if (lane == 0) {
+            TcTile tl_next = tile_at(blockIdx.x);
+            for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
+                const TcTile tl = tl_next;
+                tl_next = tile_at(u + (int)gridDim.x);
+                const int rb = u % nrb;
+                const CUtensorMap *mp = a.maps + 3 * tl.expert + (PH == 0 ? 0 : 2);
+                bool ok = true;
+                for (int ss = 0; ss < nss; ss++, it++) {
+                    const int slot = it % C::SP;
+                    if (it >= (uint32_t)C::SP &&
+                        !tc_wait(bar(B_PKE + slot), ((it / C::SP) - 1) & 1, a.err, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(B_PKF + slot), C::PK_BYTES);
+                    issued[slot]++;
+#pragma unroll
+                    for (int m = 0; m < C::NA; m++)
+                        tma_load_2d(pk_stage(slot) + (uint32_t)(m * TC_M * 128), mp + m, ss * 128, rb * TC_M,
+                                    bar(B_PKF + slot));
+                }
+                if (!ok) break;
+            }
+            // drain: every fill issued here has landed before the CTA exits
+            for (int s = 0; s < C::SP; s++)
+                if (issued[s]) mbar_wait(bar(B_PKF + s), (issued[s] - 1) & 1, a.err);
+        }
+        __syncwarp();
+    } else if (warp == W_B) {
+        // --------------------------------------------------- token tiles
+        // Slots are counted with free-running counters: a k-step of c slots
+        // starts at `head` (skipping to the ring start when it would not fit
+        // before the end) and the slots up to the end of the oldest k-step
+        // the MMAs have finished are free again.
+        if (lane == 0) {
+            uint32_t kt = 0, done = 0, head = 0, tail = 0;
+            uint32_t endv[TC_NB];
+            TcTile tl_next = tile_at(blockIdx.x);
+            for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
+                const TcTile tl = tl_next;
+                tl_next = tile_at(u + (int)gridDim.x);
+                const int nb = PH == 0 ? tl.nx : tl.nh;
+                if (nb < 16 || nb % 16 || nb > C::BMAX) {
+                    set_device_error(a.err, K3MOE_EINVAL);
+                    *abort_flag = 1;
+                    break;
+                }
+                const uint8_t *src = a.Bsrc + (size_t)(PH == 0 ? tl.xrow0 : tl.hrow0) * K * 2;
+                const uint32_t bytes = (uint32_t)nb * 128u;
+                const uint32_t c = (uint32_t)nb / 16u;
+                bool ok = true;
+                for (int ks = 0; ks < nks && ok; ks++, kt++) {
+                    uint32_t start = head;
+                    if (start % C::NSLOT + c > (uint32_t)C::NSLOT) start += C::NSLOT - start % C::NSLOT;
+                    while (kt - done >= (uint32_t)TC_NB || start + c - tail > (uint32_t)C::NSLOT) {
+                        if (done == kt ||
+                            !tc_wait(bar(B_BE + done % TC_NB), (done / TC_NB) & 1, a.err, abort_flag)) {
+                            if (done == kt) set_device_error(a.err, K3MOE_EINVAL);
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        tail = endv[done % TC_NB];
+                        done++;
+                    }
+                    if (!ok) break;
+                    head = start + c;
+                    endv[kt % TC_NB] = head;
+                    const uint32_t off = (start % C::NSLOT) * TC_SLOT;
+                    boff[kt % TC_NB] = off;
+                    mbar_arrive_expect_tx(bar(B_BF + kt % TC_NB), bytes);
+                    bulk_g2s(b_ring + off, src + (size_t)ks * bytes, bytes, bar(B_BF + kt % TC_NB));
+                }
+                if (!ok) break;
+            }
+            // drain: every copy issued here has landed before the CTA exits
+            for (uint32_t q = done; q < kt; q++) mbar_wait(bar(B_BF + q % TC_NB), (q / TC_NB) & 1, a.err);
+        }
+        __syncwarp();
+    } else if (warp == W_MMA) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            uint32_t kt = 0, ut = 0;
+            TcTile tl_next = tile_at(blockIdx.x);
+            for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x, ut++) {
+                const TcTile tl = tl_next;
+                tl_next = tile_at(u + (int)gridDim.x);
+                const int nb = PH == 0 ? tl.nx : tl.nh;
+                if (nb < 16 || nb % 16 || nb > C::BMAX) {
+                    set_device_error(a.err, K3MOE_EINVAL);
+                    *abort_flag = 1;
+                    break;
+                }
+                const uint32_t idesc = bf16_idesc(nb);
+                const int buf = ut & 1;
+                if (ut >= 2 && !tc_wait(bar(B_ACCE + buf), ((ut / 2) - 1) & 1, a.err, abort_flag)) break;
+                tc_fence_after();
+                bool ok = true;
+                for (int ks = 0; ks < nks; ks++, kt++) {
+                    const int sa = kt % C::SA, sb = kt % TC_NB;
+                    if (!tc_wait(bar(B_AF + sa), (kt / C::SA) & 1, a.err, abort_flag) ||
+                        !tc_wait(bar(B_BF + sb), (kt / TC_NB) & 1, a.err, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t bs = b_ring + boff[sb];
+#pragma unroll
+                    for (int m = 0; m < C::NA; m++) {
+                        const uint32_t as = a_stage(sa) + (uint32_t)(m * TC_M * 128);
+                        const uint32_t td = tmem + (uint32_t)(buf * 256 + m * 128);
+#pragma unroll
+                        for (int kk = 0; kk < TC_KS / 16; kk++)
+                            mma_bf16(td, sw128_desc(as + kk * 32), sw128_desc(bs + kk * 32), idesc,
+                                     (ks | kk) != 0);
+                    }
+                    mma_commit(bar(B_AE + sa));
+                    mma_commit(bar(B_BE + sb));
+                }
+                if (!ok) break;
+                mma_commit(bar(B_ACCF + buf));
+            }
+            // every MMA issued above has completed before TMEM is freed
+            mma_commit(bar(B_FIN));
+            mbar_wait(bar(B_FIN), 0, a.err);
+        }
+        __syncwarp();
+    } else if (warp < W_EPI) {
+        // ------------------------------------------------------- decoders
+        // Thread (row r, part p) decodes IPP of the row's NA x 2 32-groups
+        // of every k-step (items p*IPP .. p*IPP+IPP-1; item = 2 * matrix +
+        // group); the items of a part share one matrix.
+        const int dw = warp - W_DEC;
+        const int r = (dw & 3) * 32 + lane;  // weight row within the unit
+        const int part = dw >> 2;
+        const int mat = (part * C::IPP) >> 1;
+        uint32_t it = 0, kt = 0;
+        const int g_per_ss = TC_SS / 32;  // 8 scale bytes per row per staging step
+        const int G = gridDim.x;
+        auto scale_plane = [&](int e) -> const uint8_t * {
+            return PH == 1 ? a.table[e].ds : (mat == 0 ? a.table[e].gs : a.table[e].us);
+        };
+        // The scale row of the next unit is found in three steps spread over
+        // the current unit (its expert at the first staging step, the plane at
+        // the middle one, the first 8 bytes at the last one), so no load in the
+        // loop waits on another.
+        int u = blockIdx.x;
+        const uint8_t *scl = nullptr, *nplane = nullptr, *nscl = nullptr;
+        int nexp = 0;
+        if (u < n_units)
+            scl = scale_plane(a.tiles[u / nrb].expert) + (size_t)((u % nrb) * TC_M + r) * (K / 32);
+        uint2 sc_next = scl ? __ldg((const uint2 *)scl) : make_uint2(0, 0);
+        int ss = 0;
+        while (u < n_units && !*abort_flag) {
+            const int un = u + G;
+            if (ss == 0 && un < n_units) nexp = a.tiles[un / nrb].expert;
+            if (ss == nss / 2 && un < n_units) nplane = scale_plane(nexp);
+            const uint2 sc = sc_next;
+            if (ss + 1 < nss) {
+                sc_next = __ldg((const uint2 *)(scl + (ss + 1) * g_per_ss));
+            } else if (un < n_units) {
+                nscl = nplane + (size_t)((un % nrb) * TC_M + r) * (K / 32);
+                sc_next = __ldg((const uint2 *)nscl);
+            }
+            int ss2 = ss + 1, u2 = u;
+            if (ss2 == nss) {
+                ss2 = 0;
+                u2 = un;
+            }
+            const int pslot = it % C::SP;
+            if (!__all_sync(0xffffffffu, tc_wait(bar(B_PKF + pslot), (it / C::SP) & 1, a.err, abort_flag))) break;
+            bool ok = true;
+            for (int kk = 0; kk < TC_KPS; kk++, kt++) {
+                const int slot = kt % C::SA;
+                if (kt >= (uint32_t)C::SA &&
+                    !__all_sync(0xffffffffu, tc_wait(bar(B_AE + slot), ((kt / C::SA) - 1) & 1, a.err, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t src = pk_stage(pslot) + (uint32_t)(mat * TC_M * 128 + r * 128);
+                const uint32_t dst = a_stage(slot) + (uint32_t)(mat * TC_M * 128 + r * 128);
+                const uint32_t scw = kk < 2 ? sc.x : sc.y;
+#pragma unroll
+                for (int gg = 0; gg < C::IPP; gg++) {
+                    const int g = (part * C::IPP + gg) & 1;  // 32-group within the k-step
+                    // the group's 16 packed bytes are chunk 2 kk + g of the staged row
+                    const int pc = 2 * kk + g;
+                    const uint4 q = lds128(src + (uint32_t)((pc ^ (r & 7)) << 4));
+                    const uint32_t e = (scw >> (16 * (kk & 1) + 8 * g)) & 0xffu;
+                    bool fast;
+                    const uint16_t sh = e8m0_f16(e, fast);
+                    uint4 o[4];
+                    if (__all_sync(0xffffffffu, fast)) {
+                        o[0] = decode8_bf16(q.x, sh);
+                        o[1] = decode8_bf16(q.y, sh);
+                        o[2] = decode8_bf16(q.z, sh);
+                        o[3] = decode8_bf16(q.w, sh);
+                    } else {
+                        const float sf = e8m0_scale(e);
+                        o[0] = decode8_bf16_any(q.x, sf);
+                        o[1] = decode8_bf16_any(q.y, sf);
+                        o[2] = decode8_bf16_any(q.z, sf);
+                        o[3] = decode8_bf16_any(q.w, sf);
+                    }
+#pragma unroll
+                    for (int w = 0; w < 4; w++) {
+                        const int c = g * 4 + w;  // 16-byte chunk of the k-step's 128-byte bf16 row
+                        const uint32_t ad = dst + (uint32_t)(((c ^ (r & 7)) << 4));
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(ad), "r"(o[w].x), "r"(o[w].y),
+                                     "r"(o[w].z), "r"(o[w].w)
+                                     : "memory");
+                    }
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_AF + slot));
+            }
+            if (!ok) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_PKE + pslot));
+            it++;
+            if (u2 != u) scl = nscl;
+            u = u2;
+            ss = ss2;
+        }
+    } else {
+        // ------------------------------------------------------- epilogue
+        const int q = warp & 3;       // TMEM lane quadrant of this warp
+        const int r = q * 32 + lane;  // weight row within the unit
+        uint32_t ut = 0;
+        TcTile tl_next = tile_at(blockIdx.x);
+        for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x, ut++) {
+            const TcTile tl = tl_next;
+            tl_next = tile_at(u + (int)gridDim.x);
+            const int buf = ut & 1;
+            if (!__all_sync(0xffffffffu, tc_wait(bar(B_ACCF + buf), (ut / 2) & 1, a.err, abort_flag))) break;
+            tc_fence_after();
+            const int rb = u % nrb;
+            const int P = (tl.n + 15) & ~15;
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 256);
+            const bool xsplit = PH == 0 && tl.nx > P;
+            for (int j0 = 0; j0 < tl.n; j0 += 16) {
+                if (PH == 0) {
+                    float g[16], v[16], t[16];
+                    tmem_ld16(tbase + j0, g);
+                    if (xsplit) {
+                        tmem_ld16(tbase + P + j0, t);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; i++) g[i] += t[i];
+                    }
+                    tmem_ld16(tbase + 128 + j0, v);
+                    if (xsplit) {
+                        tmem_ld16(tbase + 128 + P + j0, t);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; i++) v[i] += t[i];
+                    }
+                    tmem_wait_ld();
+                    const int col = rb * TC_M + r;  // index into f
+                    const int s = col >> 6, c = (col & 63) >> 3, byte = (col & 7) * 2;
+                    uint8_t *hb = a.Hg + (size_t)tl.hrow0 * a.f * 2 + (size_t)s * tl.nh * 128 + byte;
+#pragma unroll
+                    for (int jj = 0; jj < 16; jj++) {
+                        const int j = j0 + jj;
+                        if (j < tl.n) {
+                            const float h = silu(g[jj]) * v[jj];
+                            const uint32_t hi = bf16_rn_bits(h);
+                            const uint32_t lo = bf16_rn_bits(h - __uint_as_float(hi << 16));
+                            const int jh = j, jl = P + j;
+                            *(uint16_t *)(hb + jh * 128 + ((c ^ (jh & 7)) << 4)) = (uint16_t)hi;
+                            *(uint16_t *)(hb + jl * 128 + ((c ^ (jl & 7)) << 4)) = (uint16_t)lo;
+                        }
+                    }
+                } else {
+                    float yh[16], yl[16];
+                    tmem_ld16(tbase + j0, yh);
+                    tmem_ld16(tbase + P + j0, yl);
+                    tmem_wait_ld();
+                    const int row = rb * TC_M + r;  // index into d
+#pragma unroll
+                    for (int jj = 0; jj < 16; jj++) {
+                        const int j = j0 + jj;
+                        if (j < tl.n) {
+                            const int pair = a.perm[tl.pair_begin + j];
+                            const float w = a.wsel[pair];
+                            atomicAdd(a.out + (size_t)(pair / a.k) * a.d + row, w * (yh[jj] + yl[jj]));
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_ACCE + buf));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == W_MMA) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- planning
+
+// Tiles of at most tn tokens per expert, with the row offsets of each tile in
+// the token array (nx rows) and in the h array (nh rows).  One CTA.
+__global__ void __launch_bounds__(1024) k3_tc_plan(const int32_t *__restrict__ offsets, int E, int tn,
+                                                   int xsplit, int max_tiles, TcTile *tiles,
+                                                   int32_t *n_tiles, int *err)
+{
+    __shared__ int wsum[3][32];
+    __shared__ int base[3];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if (threadIdx.x == 0) base[0] = base[1] = base[2] = 0;
+    __syncthreads();
+    for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+        const int e = e0 + threadIdx.x;
+        const int c = e < E ? offsets[e + 1] - offsets[e] : 0;
+        const int nt = (c + tn - 1) / tn;
+        int rx = 0, rh = 0;
+        for (int j = 0; j < nt; j++) {
+            const int n = min(tn, c - j * tn), p = (n + 15) & ~15;
+            rx += xsplit ? 2 * p : p;
+            rh += 2 * p;
+        }
+        int v[3] = {nt, rx, rh}, inc[3];
+#pragma unroll
+        for (int i = 0; i < 3; i++) {
+            int x = v[i];
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            inc[i] = x;
+            if (lane == 31) wsum[i][warp] = x;
+        }
+        __syncthreads();
+        if (warp == 0) {
+#pragma unroll
+            for (int i = 0; i < 3; i++) {
+                int x = lane < nw ? wsum[i][lane] : 0;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += y;
+                }
+                if (lane < nw) wsum[i][lane] = x - wsum[i][lane];  // exclusive
+            }
+        }
+        __syncthreads();
+        int t = base[0] + wsum[0][warp] + inc[0] - v[0];
+        int xr = base[1] + wsum[1][warp] + inc[1] - v[1];
+        int hr = base[2] + wsum[2][warp] + inc[2] - v[2];
+        for (int j = 0; j < nt; j++, t++) {
+            const int n = min(tn, c - j * tn), p = (n + 15) & ~15;
+            const int nx = xsplit ? 2 * p : p, nh = 2 * p;
+            if (t < max_tiles) {
+                TcTile tl;
+                tl.expert = e;
+                tl.pair_begin = offsets[e] + j * tn;
+                tl.n = n;
+                tl.nx = nx;
+                tl.nh = nh;
+                tl.xrow0 = xr;
+                tl.hrow0 = hr;
+                tl.pad = 0;
+                tiles[t] = tl;
+            }
+            xr += nx;
+            hr += nh;
+        }
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) {
+            base[0] = t;
+            base[1] = xr;
+            base[2] = hr;
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        if (base[0] > max_tiles) {
+            set_device_error(err, K3MOE_EINVAL);
+            *n_tiles = 0;
+        } else {
+            *n_tiles = base[0];
+        }
+    }
+}
+
+// Token rows of every tile, bf16, k-step-major and pre-swizzled: the 8
+// 16-byte chunks of a row's 64-element slice sit at chunk ^ (row & 7).
+template <typename XT>
+__global__ void __launch_bounds__(256) k3_tc_gather(const XT *__restrict__ X, const int32_t *__restrict__ perm,
+                                                    int k, int d, const TcTile *__restrict__ tiles,
+                                                    const int32_t *n_tiles, uint8_t *Xg)
+{
+    const int nt = *n_tiles;
+    const int c8 = d / 8;
+    for (int t = blockIdx.x; t < nt; t += gridDim.x) {
+        const TcTile tl = tiles[t];
+        const int P = (tl.n + 15) & ~15;
+        const bool xsplit = tl.nx > P;
+        uint8_t *base = Xg + (size_t)tl.xrow0 * d * 2;
+        const int total = tl.nx * c8;
+        for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+            const int row = idx / c8, ch = idx - row * c8;
+            const int s = ch >> 3, c = ch & 7;
+            int j = row;
+            bool lo = false;
+            if (xsplit && row >= P) {
+                j = row - P;
+                lo = true;
+            }
+            uint4 o = make_uint4(0, 0, 0, 0);
+            if (j < tl.n) {
+                const int tok = perm[tl.pair_begin + j] / k;
+                if constexpr (sizeof(XT) == 2) {
+                    if (!lo) o = *(const uint4 *)((const uint16_t *)X + (size_t)tok * d + ch * 8);
+                } else {
+                    const float4 *src = (const float4 *)((const float *)X + (size_t)tok * d + ch * 8);
+                    const float4 v0 = src[0], v1 = src[1];
+                    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                    uint32_t h[8];
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        const uint32_t hi = bf16_rn_bits(v[i]);
+                        h[i] = lo ? bf16_rn_bits(v[i] - __uint_as_float(hi << 16)) : hi;
+                    }
+                    o = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+                }
+            }
+            *(uint4 *)(base + (size_t)s * tl.nx * 128 + row * 128 + ((c ^ (row & 7)) << 4)) = o;
+        }
+    }
+}
+
+// --------------------------------------------------------------- launchers
+
+int num_sms();
+
+bool tc_supported(int E, int k, int d, int f)
+{
+    return E >= 1 && k >= 1 && d % TC_SS == 0 && f % TC_SS == 0 && d >= TC_SS && f >= TC_SS &&
+           d <= 16384 && f <= 16384;
+}
+int tc_tile_tokens(int xdt) { return xdt == K3MOE_BF16 ? 128 : 64; }
+int tc_max_tiles(int npairs, int E, int tn) { return (npairs + tn - 1) / tn + E; }
+// Rows of the token and h arrays for the worst case of either activation type.
+size_t tc_max_rows(int npairs, int E) { return 2 * ((size_t)npairs + 15 * (size_t)tc_max_tiles(npairs, E, 64)); }
+size_t tc_tile_bytes() { return sizeof(TcTile); }
+size_t tc_map_bytes() { return sizeof(CUtensorMap); }
+
+// Tensor maps of the packed planes of E experts (host table of device plane
+// pointers): [E][gate, up, down], 2D u8 tensors of rows x in/2 bytes, boxes
+// of 128 rows x 128 bytes with the 128-byte swizzle, written to dev_maps.
+int tc_make_maps(const DevExpert *host_table, int E, int d, int f, void *dev_maps)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn) {
+            cudaGetLastError();
+            return K3MOE_ECUDA;
+        }
+        encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    }
+    CUtensorMap *maps = (CUtensorMap *)malloc(sizeof(CUtensorMap) * 3 * (size_t)E);
+    if (!maps) return K3MOE_ENOMEM;
+    int rc = K3MOE_OK;
+    for (int e = 0; e < E && rc == K3MOE_OK; e++) {
+        const uint8_t *planes[3] = {host_table[e].gp, host_table[e].up, host_table[e].dp};
+        for (int m = 0; m < 3; m++) {
+            const int rows = m < 2 ? f : d, in = m < 2 ? d : f;
+            const cuuint64_t dims[2] = {(cuuint64_t)(in / 2), (cuuint64_t)rows};
+            const cuuint64_t strides[1] = {(cuuint64_t)(in / 2)};
+            const cuuint32_t box[2] = {128, (cuuint32_t)TC_M};
+            const cuuint32_t estr[2] = {1, 1};
+            if (encode(&maps[3 * e + m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void *)planes[m], dims, strides, box,
+                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+                rc = K3MOE_EINVAL;
+                break;
+            }
+        }
+    }
+    if (rc == K3MOE_OK &&
+        cudaMemcpy(dev_maps, maps, sizeof(CUtensorMap) * 3 * (size_t)E, cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        rc = K3MOE_ECUDA;
+    }
+    free(maps);
+    return rc;
+}
+
+template <int PH>
+static int launch_expert(const TcArgs &a, cudaStream_t s)
+{
+    static bool ready = false;
+    if (!ready) {
+        if (cudaFuncSetAttribute(k3_tc_expert<PH>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<PH>::SMEM) !=
+            cudaSuccess)
+            return K3MOE_ECUDA;
+        ready = true;
+    }
+    k3_tc_expert<PH><<<num_sms(), TcCfg<PH>::THREADS, TcCfg<PH>::SMEM, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
+}
+
+// Plan, token gather and the gate/up + SwiGLU phase (h into Hg).
+int launch_tc_gateup(const void *X, int xdt, int k, int E, int d, int f, const DevExpert *table,
+                     const void *maps, const int32_t *offsets, const int32_t *perm, void *tiles,
+                     int32_t *n_tiles, int max_tiles, uint8_t *Xg, uint8_t *Hg, int *err, cudaStream_t s)
+{
+    const int tn = tc_tile_tokens(xdt);
+    k3_tc_plan<<<1, 1024, 0, s>>>(offsets, E, tn, xdt == K3MOE_F32, max_tiles, (TcTile *)tiles, n_tiles, err);
+    if (cudaGetLastError() != cudaSuccess) return K3MOE_ECUDA;
+    const int g = 2 * num_sms();
+    if (xdt == K3MOE_BF16)
+        k3_tc_gather<uint16_t><<<g, 256, 0, s>>>((const uint16_t *)X, perm, k, d, (const TcTile *)tiles, n_tiles, Xg);
+    else
+        k3_tc_gather<float><<<g, 256, 0, s>>>((const float *)X, perm, k, d, (const TcTile *)tiles, n_tiles, Xg);
+    if (cudaGetLastError() != cudaSuccess) return K3MOE_ECUDA;
+    TcArgs a = {};
+    a.tiles = (const TcTile *)tiles;
+    a.n_tiles = n_tiles;
+    a.table = table;
+    a.maps = (const CUtensorMap *)maps;
+    a.Bsrc = Xg;
+    a.Hg = Hg;
+    a.k = k;
+    a.d = d;
+    a.f = f;
+    a.err = err;
+    return launch_expert<0>(a, s);
+}
+
+// Down phase and the weighted combine: out = sum_j w_j y_j (out is zeroed first).
+int launch_tc_down(int T, int k, int d, int f, const DevExpert *table, const void *maps, const int32_t *perm,
+                   const float *wsel, const void *tiles, const int32_t *n_tiles, const uint8_t *Hg, float *out,
+                   int *err, cudaStream_t s)
+{
+    if (cudaMemsetAsync(out, 0, sizeof(float) * (size_t)T * d, s) != cudaSuccess) return K3MOE_ECUDA;
+    TcArgs a = {};
+    a.tiles = (const TcTile *)tiles;
+    a.n_tiles = n_tiles;
+    a.table = table;
+    a.maps = (const CUtensorMap *)maps;
+    a.Bsrc = Hg;
+    a.out = out;
+    a.perm = perm;
+    a.wsel = wsel;
+    a.k = k;
+    a.d = d;
+    a.f = f;
+    a.err = err;
+    return launch_expert<1>(a, s);
+}
+
+}  // namespace k3
