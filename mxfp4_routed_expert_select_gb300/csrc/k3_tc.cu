@@ -45,8 +45,11 @@
 
 namespace k3 {
 
+// One tile: up to TN tokens of one expert.  Token rows (nx of them, from
+// xrow0) and h rows (nh, from hrow0) keep hi rows at [0, n) and, when split,
+// lo rows at [P, P + n) with P = n rounded up to 8.
 struct TcTile {
-    int32_t expert, pair_begin, n, nx, nh, xrow0, hrow0, pad;
+    int32_t expert, pair_begin, n, nx, nh, xrow0, hrow0, split;
 };
 
 namespace {
@@ -83,29 +86,59 @@ struct TcCfg {
 
 K3_DEV uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart (stride byte offset), descriptor version 1.
-K3_DEV uint64_t sw128_desc(uint32_t saddr)
-{
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
 // K-major, M = 128, N = n (multiple of 16, <= 256).
 K3_DEV uint32_t bf16_idesc(int n)
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TC_M >> 4) << 24);
 }
-K3_DEV void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+// Shared-memory matrix descriptor of a K-major operand with the 128-byte
+// swizzle, split in its two 32-bit halves.  Low half: start address >> 4
+// (bits 0-13) and leading byte offset 1 (bits 16-29, unused with this
+// swizzle); it is the only half that changes, and +32 bytes of K is +2.
+// High half: stride byte offset 1024 >> 4 (8-row groups 1024 bytes apart),
+// descriptor version 1 (bit 46 of the whole), swizzle mode 2 (bits 61-63).
+K3_DEV uint32_t sw128_lo(uint32_t saddr) { return ((saddr & 0x3FFFFu) >> 4) | (1u << 16); }
+constexpr uint32_t SW128_HI = (1024u >> 4) | (1u << 14) | (2u << 29);
+// One k-step (64 of K) of D (+)= A * B^T: four K = 16 MMAs on consecutive
+// 32-byte slices of A and B, A and B given by the low halves of their
+// descriptors.  Executed by the whole warp; elect.sync picks the one lane
+// that issues.  The per-MMA offsets are added inside one asm block, so the
+// operands that vary from one k-step to the next are moved once per block
+// (an MMA whose descriptor is recomputed outside costs about 90 cycles more).
+#define K3_MMA4(TD, AL, BL)                                                                                  \
+    "mov.b64 da, {" AL ", %5};\n\tmov.b64 db, {" BL ", %5};\n\t"                                          \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [" TD "], da, db, %3, p;\n\t"                                    \
+    "add.u32 a, " AL ", 2;\n\tadd.u32 b, " BL ", 2;\n\tmov.b64 da, {a, %5};\n\tmov.b64 db, {b, %5};\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [" TD "], da, db, %3, 1;\n\t"                                    \
+    "add.u32 a, " AL ", 4;\n\tadd.u32 b, " BL ", 4;\n\tmov.b64 da, {a, %5};\n\tmov.b64 db, {b, %5};\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [" TD "], da, db, %3, 1;\n\t"                                    \
+    "add.u32 a, " AL ", 6;\n\tadd.u32 b, " BL ", 6;\n\tmov.b64 da, {a, %5};\n\tmov.b64 db, {b, %5};\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [" TD "], da, db, %3, 1;\n\t"
+K3_DEV void mma_kstep1(uint32_t td, uint32_t alo, uint32_t blo, uint32_t idesc, uint32_t acc)
 {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-                 "l"(a), "l"(b), "r"(idesc), "r"(acc)
+    asm volatile("{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t.reg .b32 a, b;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t" K3_MMA4("%0", "%1", "%2") "}" ::"r"(td),
+                 "r"(alo), "r"(blo), "r"(idesc), "r"(acc), "r"(SW128_HI)
                  : "memory");
 }
+// Two matrices (gate, up) against the same B: A of the second matrix is
+// 16 KB further (+1024 in the descriptor), its accumulator 128 columns on.
+K3_DEV void mma_kstep2(uint32_t td, uint32_t alo, uint32_t blo, uint32_t idesc, uint32_t acc)
+{
+    asm volatile("{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t.reg .b32 a, b, a1, t1;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "add.u32 a1, %1, 1024;\n\tadd.u32 t1, %0, 128;\n\t" K3_MMA4("%0", "%1", "%2")
+                     K3_MMA4("t1", "a1", "%2") "}" ::"r"(td),
+                 "r"(alo), "r"(blo), "r"(idesc), "r"(acc), "r"(SW128_HI)
+                 : "memory");
+}
+#undef K3_MMA4
+// Commit by the lane elect.sync picks (the lane that issued the MMAs).
 K3_DEV void mma_commit(uint32_t bar)
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
                  : "memory");
 }
 K3_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -121,18 +154,16 @@ K3_DEV void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint
                  : "memory");
 }
 
-// 16 consecutive fp32 columns of TMEM for this warp's 32 lanes.
-K3_DEV void tmem_ld16(uint32_t taddr, float (&v)[16])
+// 8 consecutive fp32 columns (column address a multiple of 8).
+K3_DEV void tmem_ld8(uint32_t taddr, float (&v)[8])
 {
-    uint32_t r[16];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-                 "%11, %12, %13, %14, %15}, [%16];"
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-                   "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                   "=r"(r[7])
                  : "r"(taddr));
 #pragma unroll
-    for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 8; i++) v[i] = __uint_as_float(r[i]);
 }
 K3_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
@@ -192,6 +223,13 @@ K3_DEV bool tc_wait(uint32_t bar, uint32_t parity, int *err, volatile int *abort
 }
 
 K3_DEV uint32_t bf16_rn_bits(float v) { return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+
+// Rows of a tile of n tokens.  A split operand keeps its hi rows at
+// [0, n) and its lo rows at [P, P + n), P = n rounded up to 8; every MMA
+// width is a multiple of 16.
+K3_DEV int tile_p(int n) { return (n + 7) & ~7; }
+K3_DEV int tile_nx(int n, bool xsplit) { return xsplit ? 2 * tile_p(n) : (n + 15) & ~15; }
+K3_DEV int tile_nh(int n) { return 2 * tile_p(n); }
 
 struct TcArgs {
     const TcTile *tiles;
@@ -366,51 +404,49 @@ __global__ void __launch_bounds__(TcCfg<PH>::THREADS, 1) k3_tc_expert(const TcAr
         __syncwarp();
     } else if (warp == W_MMA) {
         // ------------------------------------------------------------ MMA
-        if (lane == 0) {
-            uint32_t kt = 0, ut = 0;
-            TcTile tl_next = tile_at(blockIdx.x);
-            for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x, ut++) {
-                const TcTile tl = tl_next;
-                tl_next = tile_at(u + (int)gridDim.x);
-                const int nb = PH == 0 ? tl.nx : tl.nh;
-                if (nb < 16 || nb % 16 || nb > C::BMAX) {
-                    set_device_error(a.err, K3MOE_EINVAL);
-                    *abort_flag = 1;
+        // The whole warp walks the loop (the MMAs need a converged warp for
+        // elect.sync); every lane takes the same branches.
+        uint32_t kt = 0, ut = 0;
+        TcTile tl_next = tile_at(blockIdx.x);
+        for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x, ut++) {
+            const TcTile tl = tl_next;
+            tl_next = tile_at(u + (int)gridDim.x);
+            const int nb = PH == 0 ? tl.nx : tl.nh;
+            if (nb < 16 || nb % 16 || nb > C::BMAX) {
+                if (lane == 0) set_device_error(a.err, K3MOE_EINVAL);
+                *abort_flag = 1;
+                break;
+            }
+            const uint32_t idesc = bf16_idesc(nb);
+            const int buf = ut & 1;
+            if (ut >= 2 && !__all_sync(0xffffffffu, tc_wait(bar(B_ACCE + buf), ((ut / 2) - 1) & 1, a.err, abort_flag)))
+                break;
+            tc_fence_after();
+            const uint32_t td = tmem + (uint32_t)(buf * 256);
+            bool ok = true;
+            for (int ks = 0; ks < nks; ks++, kt++) {
+                const int sa = kt % C::SA, sb = kt % TC_NB;
+                if (!__all_sync(0xffffffffu, tc_wait(bar(B_AF + sa), (kt / C::SA) & 1, a.err, abort_flag) &&
+                                                 tc_wait(bar(B_BF + sb), (kt / TC_NB) & 1, a.err, abort_flag))) {
+                    ok = false;
                     break;
                 }
-                const uint32_t idesc = bf16_idesc(nb);
-                const int buf = ut & 1;
-                if (ut >= 2 && !tc_wait(bar(B_ACCE + buf), ((ut / 2) - 1) & 1, a.err, abort_flag)) break;
                 tc_fence_after();
-                bool ok = true;
-                for (int ks = 0; ks < nks; ks++, kt++) {
-                    const int sa = kt % C::SA, sb = kt % TC_NB;
-                    if (!tc_wait(bar(B_AF + sa), (kt / C::SA) & 1, a.err, abort_flag) ||
-                        !tc_wait(bar(B_BF + sb), (kt / TC_NB) & 1, a.err, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t bs = b_ring + boff[sb];
-#pragma unroll
-                    for (int m = 0; m < C::NA; m++) {
-                        const uint32_t as = a_stage(sa) + (uint32_t)(m * TC_M * 128);
-                        const uint32_t td = tmem + (uint32_t)(buf * 256 + m * 128);
-#pragma unroll
-                        for (int kk = 0; kk < TC_KS / 16; kk++)
-                            mma_bf16(td, sw128_desc(as + kk * 32), sw128_desc(bs + kk * 32), idesc,
-                                     (ks | kk) != 0);
-                    }
-                    mma_commit(bar(B_AE + sa));
-                    mma_commit(bar(B_BE + sb));
-                }
-                if (!ok) break;
-                mma_commit(bar(B_ACCF + buf));
+                const uint32_t blo = sw128_lo(b_ring + boff[sb]);
+                const uint32_t alo = sw128_lo(a_stage(sa));
+                if (C::NA == 2)
+                    mma_kstep2(td, alo, blo, idesc, ks != 0);
+                else
+                    mma_kstep1(td, alo, blo, idesc, ks != 0);
+                mma_commit(bar(B_AE + sa));
+                mma_commit(bar(B_BE + sb));
             }
-            // every MMA issued above has completed before TMEM is freed
-            mma_commit(bar(B_FIN));
-            mbar_wait(bar(B_FIN), 0, a.err);
+            if (!ok) break;
+            mma_commit(bar(B_ACCF + buf));
         }
+        // every MMA issued above has completed before TMEM is freed
+        mma_commit(bar(B_FIN));
+        mbar_wait(bar(B_FIN), 0, a.err);
         __syncwarp();
     } else if (warp < W_EPI) {
         // ------------------------------------------------------- decoders
@@ -523,32 +559,32 @@ __global__ void __launch_bounds__(TcCfg<PH>::THREADS, 1) k3_tc_expert(const TcAr
             if (!__all_sync(0xffffffffu, tc_wait(bar(B_ACCF + buf), (ut / 2) & 1, a.err, abort_flag))) break;
             tc_fence_after();
             const int rb = u % nrb;
-            const int P = (tl.n + 15) & ~15;
+            const int P = tile_p(tl.n);
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 256);
-            const bool xsplit = PH == 0 && tl.nx > P;
-            for (int j0 = 0; j0 < tl.n; j0 += 16) {
+            const bool xsplit = PH == 0 && tl.split;
+            for (int j0 = 0; j0 < tl.n; j0 += 8) {
                 if (PH == 0) {
-                    float g[16], v[16], t[16];
-                    tmem_ld16(tbase + j0, g);
+                    float g[8], v[8], t[8];
+                    tmem_ld8(tbase + j0, g);
                     if (xsplit) {
-                        tmem_ld16(tbase + P + j0, t);
+                        tmem_ld8(tbase + P + j0, t);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 16; i++) g[i] += t[i];
+                        for (int i = 0; i < 8; i++) g[i] += t[i];
                     }
-                    tmem_ld16(tbase + 128 + j0, v);
+                    tmem_ld8(tbase + 128 + j0, v);
                     if (xsplit) {
-                        tmem_ld16(tbase + 128 + P + j0, t);
+                        tmem_ld8(tbase + 128 + P + j0, t);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 16; i++) v[i] += t[i];
+                        for (int i = 0; i < 8; i++) v[i] += t[i];
                     }
                     tmem_wait_ld();
                     const int col = rb * TC_M + r;  // index into f
                     const int s = col >> 6, c = (col & 63) >> 3, byte = (col & 7) * 2;
                     uint8_t *hb = a.Hg + (size_t)tl.hrow0 * a.f * 2 + (size_t)s * tl.nh * 128 + byte;
 #pragma unroll
-                    for (int jj = 0; jj < 16; jj++) {
+                    for (int jj = 0; jj < 8; jj++) {
                         const int j = j0 + jj;
                         if (j < tl.n) {
                             const float h = silu(g[jj]) * v[jj];
@@ -560,13 +596,13 @@ __global__ void __launch_bounds__(TcCfg<PH>::THREADS, 1) k3_tc_expert(const TcAr
                         }
                     }
                 } else {
-                    float yh[16], yl[16];
-                    tmem_ld16(tbase + j0, yh);
-                    tmem_ld16(tbase + P + j0, yl);
+                    float yh[8], yl[8];
+                    tmem_ld8(tbase + j0, yh);
+                    tmem_ld8(tbase + P + j0, yl);
                     tmem_wait_ld();
                     const int row = rb * TC_M + r;  // index into d
 #pragma unroll
-                    for (int jj = 0; jj < 16; jj++) {
+                    for (int jj = 0; jj < 8; jj++) {
                         const int j = j0 + jj;
                         if (j < tl.n) {
                             const int pair = a.perm[tl.pair_begin + j];
@@ -610,9 +646,9 @@ __global__ void __launch_bounds__(1024) k3_tc_plan(const int32_t *__restrict__ o
         const int nt = (c + tn - 1) / tn;
         int rx = 0, rh = 0;
         for (int j = 0; j < nt; j++) {
-            const int n = min(tn, c - j * tn), p = (n + 15) & ~15;
-            rx += xsplit ? 2 * p : p;
-            rh += 2 * p;
+            const int n = min(tn, c - j * tn);
+            rx += tile_nx(n, xsplit);
+            rh += tile_nh(n);
         }
         int v[3] = {nt, rx, rh}, inc[3];
 #pragma unroll
@@ -642,8 +678,8 @@ __global__ void __launch_bounds__(1024) k3_tc_plan(const int32_t *__restrict__ o
         int xr = base[1] + wsum[1][warp] + inc[1] - v[1];
         int hr = base[2] + wsum[2][warp] + inc[2] - v[2];
         for (int j = 0; j < nt; j++, t++) {
-            const int n = min(tn, c - j * tn), p = (n + 15) & ~15;
-            const int nx = xsplit ? 2 * p : p, nh = 2 * p;
+            const int n = min(tn, c - j * tn);
+            const int nx = tile_nx(n, xsplit), nh = tile_nh(n);
             if (t < max_tiles) {
                 TcTile tl;
                 tl.expert = e;
@@ -653,7 +689,7 @@ __global__ void __launch_bounds__(1024) k3_tc_plan(const int32_t *__restrict__ o
                 tl.nh = nh;
                 tl.xrow0 = xr;
                 tl.hrow0 = hr;
-                tl.pad = 0;
+                tl.split = xsplit;
                 tiles[t] = tl;
             }
             xr += nx;
@@ -688,8 +724,8 @@ __global__ void __launch_bounds__(256) k3_tc_gather(const XT *__restrict__ X, co
     const int c8 = d / 8;
     for (int t = blockIdx.x; t < nt; t += gridDim.x) {
         const TcTile tl = tiles[t];
-        const int P = (tl.n + 15) & ~15;
-        const bool xsplit = tl.nx > P;
+        const int P = tile_p(tl.n);
+        const bool xsplit = tl.split != 0;
         uint8_t *base = Xg + (size_t)tl.xrow0 * d * 2;
         const int total = tl.nx * c8;
         for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
