@@ -38,6 +38,10 @@ GATEUP_BYTES = K * 2 * (F * D // 2 + F * D // 32)   # 187,170,816
 DOWN_BYTES = K * (D * F // 2 + D * F // 32)          # 93,585,408
 LAYER_BYTES = K * EXPERT_BYTES + ROUTER_BYTES        # 293,601,280
 N_ROUTER_COPIES = 16
+# DRAM read + write bytes of one launch of the fused batch-1 kernel at the
+# 896-expert workload, from a one-pass ncu capture of this bench (median of
+# three launches); the algorithmic bytes are LAYER_BYTES = 293,601,280.
+FUSED_TRAFFIC = 294038272
 N_TOKENS = 1024
 
 
@@ -359,7 +363,10 @@ def run_ours(args, rank, world, dev_index):
                         "down_combine": round(statistics.mean(dn_ms), 5), "steps_sampled": n_ev}),
         "roofline": {"kernel": k_name, "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_src, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": FUSED_TRAFFIC if (fused and E == 896) else None,
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of "
+                                       "k3_moe_t1_fused<0> at this workload (median of 3 launches)",
                      "algorithmic_bytes": k_bytes},
         "e2e": {"value": round(n_e2e * world / (e2e_ms * 1e-3), 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": D * 4, "d2h_bytes_per_step": D * 4, "steps": n_e2e},
