@@ -49,6 +49,32 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
+# ------------------------------------------------------------ ranks
+# N > 1: every rank runs the same workload on its own GPU over its own
+# tokens (weak scaling, no collective on the data path).  The only
+# cross-rank steps are a barrier around the timed region and the maximum of
+# the ranks' times, which sets the whole job's rate.
+
+def max_over_ranks(v, world, device=None):
+    """Largest value of `v` over all ranks (v itself when world == 1)."""
+    if world <= 1:
+        return v
+    import torch
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_first_token(rank, n_per_rank):
+    """Index of the first synthetic token of this rank's disjoint shard."""
+    return rank * n_per_rank
+
+
+def job_rate(units_per_rank, world, ms_max):
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    return units_per_rank * world / (ms_max * 1e-3)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -174,7 +200,7 @@ def run_ours(args, rank, world, dev_index):
     Wr0 = torch.from_numpy(Wr_bits.view(np.int16)).to(dev)
     routers = [Wr0] + [Wr0.clone() for _ in range(N_ROUTER_COPIES - 1)]
     layers = [k.Layer(E, K, D, F, r, views, max_tokens=1) for r in routers]
-    X = torch.from_numpy(np.stack([synth.token_f32(1, rank * N_TOKENS + t, D)
+    X = torch.from_numpy(np.stack([synth.token_f32(1, rank_first_token(rank, N_TOKENS) + t, D)
                                    for t in range(N_TOKENS)])).to(dev)
     out = torch.empty(D, dtype=torch.float32, device=dev)
     s = torch.cuda.current_stream()
@@ -239,11 +265,7 @@ def run_ours(args, rank, world, dev_index):
         l.set_events(None)
     if world > 1:
         torch.distributed.barrier()
-    ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     if graph is not None:
         # the fused kernel's own duration, events on its stream around each launch
         for i in range(n_ev):
@@ -316,11 +338,7 @@ def run_ours(args, rank, world, dev_index):
         oh.copy_(out, non_blocking=True)
     e1.record(s)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
 
     peak, peak_src = measured_peaks()
     gu_avg = statistics.mean(gu_ms)
@@ -336,7 +354,7 @@ def run_ours(args, rank, world, dev_index):
     layer_gbs = LAYER_BYTES / (ms / args.steps * 1e-3) / 1e9
     result = {
         "metric": "MoE-layer decode tokens/s (batch 1, 896 experts, top-16, MXFP4)",
-        "value": round(args.steps * world / (ms * 1e-3), 2),
+        "value": round(job_rate(args.steps, world, ms), 2),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -368,7 +386,7 @@ def run_ours(args, rank, world, dev_index):
                      "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of "
                                        "k3_moe_t1_fused<0> at this workload (median of 3 launches)",
                      "algorithmic_bytes": k_bytes},
-        "e2e": {"value": round(n_e2e * world / (e2e_ms * 1e-3), 2), "unit": "tokens/s",
+        "e2e": {"value": round(job_rate(n_e2e, world, e2e_ms), 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": D * 4, "d2h_bytes_per_step": D * 4, "steps": n_e2e},
         "gpu_launches": (1 if fused else 3) * args.steps,
         "act_f16_mode": act16,
@@ -468,12 +486,9 @@ def _timed(steps, warmup, step, dev_index, world, graph_steps=0):
     t1.record(s)
     torch.cuda.synchronize()
     clocks = clock.stop()
-    ms = t0.elapsed_time(t1)
     if world > 1:
         torch.distributed.barrier()
-        tt = torch.tensor([ms], device=torch.device("cuda", dev_index))
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), world, torch.device("cuda", dev_index))
     return ms, steps, clocks
 
 
@@ -526,12 +541,8 @@ def _e2e(step_host, n, world, dev_index, h2d, d2h, unit_per_step=1):
         step_host(i)
     e1.record(s)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([ms], device=torch.device("cuda", dev_index))
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
-    return {"value": round(n * unit_per_step * world / (ms * 1e-3), 2), "h2d_bytes_per_step": h2d,
+    ms = max_over_ranks(e0.elapsed_time(e1), world, torch.device("cuda", dev_index))
+    return {"value": round(job_rate(n * unit_per_step, world, ms), 2), "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": n}
 
 

@@ -71,6 +71,14 @@ int k3moe_version(void);
  * (0 = none, else a K3MOE_E* code).  Synchronises the device. */
 int k3moe_device_error(void);
 
+/* Self-check of the bounded waits (the pages have no counterpart; every
+ * wait in this library's kernels is bounded so that a lost producer ends in
+ * an error status instead of a hung GPU).  Enqueues one CTA that waits on a
+ * barrier nothing completes; after the 2 s limit it records K3MOE_ETIMEOUT
+ * in the device error word and exits normally.  Returns K3MOE_OK when the
+ * launch was enqueued; read the outcome with k3moe_device_error(). */
+int k3moe_check_wait_timeout(k3moe_stream s);
+
 /* ---------------------------------------------------------- packed format */
 
 /*

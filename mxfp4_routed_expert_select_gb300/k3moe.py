@@ -86,6 +86,7 @@ SIGNATURES = {
     "k3moe_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "k3moe_version": (ctypes.c_int, []),
     "k3moe_device_error": (ctypes.c_int, []),
+    "k3moe_check_wait_timeout": (ctypes.c_int, [ctypes.c_void_p]),
     "k3moe_matrix_bytes": (_I64, [_I, _I]),
     "k3moe_expert_bytes": (_I64, [_I, _I]),
     "k3moe_expert_view": (ctypes.c_int, [_P, _P, _I, _I]),
@@ -378,3 +379,8 @@ def stream_decode(layers, cache, X, T, out, eps=1e-6, stream=None, want_trace=Tr
                                     None if hits is None else hits.ctypes.data, _stream(stream)),
           "k3moe_stream_decode")
     return ids, hits
+
+
+def check_wait_timeout(stream=None):
+    """k3moe_check_wait_timeout: enqueue the bounded-wait self-check."""
+    check(lib().k3moe_check_wait_timeout(_stream(stream)), "k3moe_check_wait_timeout")
