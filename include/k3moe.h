@@ -255,6 +255,17 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int x_dtype, int32_t T, f
  *                      combine by fp32 atomic adds (summation order not
  *                      fixed).  Needs d % 256 == 0 and f % 256 == 0; default 1.
  *                      0 selects the CUDA-core grouped path.
+ *  K3MOE_OPT_TC_E4M3   on the K3MOE_OPT_TC path, run gate/up with e4m3
+ *                      operands (kind::f8f6f4): weights decoded exactly to
+ *                      e4m3 (possible when every gate/up scale byte of the
+ *                      layer is in [119, 133] or 255, checked at layer
+ *                      creation; otherwise the option has no effect) and
+ *                      activations as e4m3 pieces with power-of-two scales
+ *                      (4 pieces for fp32 tokens, each element then within
+ *                      2^-15 of the token's largest magnitude; 2 for bf16
+ *                      tokens, exact but for elements below about 2^-10 of
+ *                      that magnitude); the down product stays bf16.
+ *                      Default 1.
  * k3moe_layer_fused_t1 returns 1 when a batch-1 fp32 forward of this layer
  * would run fused, else 0 (negative on error).  After a device-side timeout
  * (k3moe_device_error() == K3MOE_ETIMEOUT) a layer must be recreated.
@@ -262,6 +273,7 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int x_dtype, int32_t T, f
 #define K3MOE_OPT_FUSED_T1 1
 #define K3MOE_OPT_ACT_F16  2
 #define K3MOE_OPT_TC       4
+#define K3MOE_OPT_TC_E4M3  8
 int k3moe_layer_set_option(k3moe_layer *L, int32_t option, int32_t value);
 int k3moe_layer_fused_t1(const k3moe_layer *L);
 

@@ -46,14 +46,16 @@ int launch_group(const int32_t *ids, int npairs, int E, int nt, int32_t *offsets
                  int4 *items, int32_t *n_items, cudaStream_t s);
 int grouped_nt();
 bool tc_supported(int E, int k, int d, int f);
-int tc_max_tiles(int npairs, int E, int tn);
-size_t tc_max_rows(int npairs, int E);
+int tc_max_tiles(int npairs, int E);
+size_t tc_xg_bytes(int npairs, int E, int d);
+size_t tc_hg_bytes(int npairs, int E, int f);
 size_t tc_tile_bytes();
 size_t tc_map_bytes();
 int tc_make_maps(const DevExpert *host_table, int E, int d, int f, void *dev_maps);
-int launch_tc_gateup(const void *X, int xdt, int k, int E, int d, int f, const DevExpert *table,
-                     const void *maps, const int32_t *offsets, const int32_t *perm, void *tiles,
-                     int32_t *n_tiles, int max_tiles, uint8_t *Xg, uint8_t *Hg, int *err, cudaStream_t s);
+int tc_e4m3_eligible(const DevExpert *dev_table, int E, int d, int f, cudaStream_t s);
+int launch_tc_gateup(const void *X, int xdt, int T, int kd, int k, int E, int d, int f, const DevExpert *table,
+                     const void *maps, const int32_t *offsets, const int32_t *perm, void *tiles, int32_t *n_tiles,
+                     int max_tiles, float *tscale, uint8_t *Xg, uint8_t *Hg, int *err, cudaStream_t s);
 int launch_tc_down(int T, int k, int d, int f, const DevExpert *table, const void *maps, const int32_t *perm,
                    const float *wsel, const void *tiles, const int32_t *n_tiles, const uint8_t *Hg, float *out,
                    int *err, cudaStream_t s);
@@ -264,6 +266,9 @@ struct k3moe_layer {
     uint8_t *Xg;         // token rows, bf16, tile-major
     uint8_t *Hg;         // SwiGLU rows (hi, lo), bf16, tile-major
     void *tc_maps;       // [E][3] tensor maps of the packed planes
+    bool e4m3_ok;        // every gate/up scale byte allows the exact e4m3 decode
+    bool e4m3;           // K3MOE_OPT_TC_E4M3 (default on where e4m3_ok)
+    float *tscale;       // [maxT] token scales of the e4m3 pieces
 };
 
 static void layer_free(k3moe_layer *L)
@@ -271,7 +276,7 @@ static void layer_free(k3moe_layer *L)
     if (!L) return;
     void *ptrs[] = {L->table, L->logits, L->part,  L->ids,     L->w,      L->h,    L->Y,
                     L->offsets, L->perm, L->items, L->n_items, L->ticket, L->ctr,
-                    L->tc_tiles, L->tc_ntiles, L->Xg, L->Hg, L->tc_maps};
+                    L->tc_tiles, L->tc_ntiles, L->Xg, L->Hg, L->tc_maps, L->tscale};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete L;
@@ -324,12 +329,12 @@ int k3moe_layer_create(k3moe_layer **out, const k3moe_layer_desc *D)
     alloc((void **)&L->ticket, sizeof(unsigned));
     alloc((void **)&L->ctr, sizeof(unsigned long long) * k3::fused_t1_counters());
     if (L->maxT > 1 && D->host_experts && k3::tc_supported(L->E, L->k, L->d, L->f)) {
-        L->tc_max_tiles = k3::tc_max_tiles((int)pairs, L->E, 64);
-        const size_t rows = k3::tc_max_rows((int)pairs, L->E);
+        L->tc_max_tiles = k3::tc_max_tiles((int)pairs, L->E);
         alloc(&L->tc_tiles, k3::tc_tile_bytes() * L->tc_max_tiles);
         alloc((void **)&L->tc_ntiles, sizeof(int32_t));
-        alloc((void **)&L->Xg, rows * L->d * 2);
-        alloc((void **)&L->Hg, rows * L->f * 2);
+        alloc((void **)&L->Xg, k3::tc_xg_bytes((int)pairs, L->E, L->d));
+        alloc((void **)&L->Hg, k3::tc_hg_bytes((int)pairs, L->E, L->f));
+        alloc((void **)&L->tscale, sizeof(float) * L->maxT);
         alloc(&L->tc_maps, k3::tc_map_bytes() * 3 * L->E);
         L->tc_ready = ok;
         L->tc = true;
@@ -355,6 +360,10 @@ int k3moe_layer_create(k3moe_layer **out, const k3moe_layer_desc *D)
     cudaError_t st = cudaMemcpy(L->table, tmp, sizeof(DevExpert) * L->E, cudaMemcpyHostToDevice);
     if (st == cudaSuccess && L->tc_ready && k3::tc_make_maps(tmp, L->E, L->d, L->f, L->tc_maps) != K3MOE_OK)
         L->tc_ready = false;  // the CUDA-core grouped path serves instead
+    if (st == cudaSuccess && L->tc_ready) {
+        L->e4m3_ok = k3::tc_e4m3_eligible(L->table, L->E, L->d, L->f, 0) == 1;
+        L->e4m3 = L->e4m3_ok;
+    }
     free(tmp);
     if (st == cudaSuccess) st = cudaMemset(L->ticket, 0, sizeof(unsigned));
     if (st == cudaSuccess)
@@ -439,9 +448,9 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int xdt, int32_t T, float
         int *err = k3::device_error_word();
         K3_TRY(k3::launch_group(L->ids, T * L->k, L->E, k3::grouped_nt(), L->offsets, L->perm,
                                 L->items, L->n_items, st));
-        K3_TRY(k3::launch_tc_gateup(X, xdt, L->k, L->E, L->d, L->f, L->table, L->tc_maps, L->offsets,
-                                    L->perm, L->tc_tiles, L->tc_ntiles, L->tc_max_tiles, L->Xg, L->Hg,
-                                    err, st));
+        K3_TRY(k3::launch_tc_gateup(X, xdt, T, (L->e4m3 && L->e4m3_ok) ? 1 : 0, L->k, L->E, L->d, L->f,
+                                    L->table, L->tc_maps, L->offsets, L->perm, L->tc_tiles, L->tc_ntiles,
+                                    L->tc_max_tiles, L->tscale, L->Xg, L->Hg, err, st));
         if (L->nev) K3_CUDA(cudaEventRecord(L->ev[2], st));
         K3_TRY(k3::launch_tc_down(T, L->k, L->d, L->f, L->table, L->tc_maps, L->perm, L->w,
                                   L->tc_tiles, L->tc_ntiles, L->Hg, out, err, st));
@@ -479,6 +488,10 @@ int k3moe_layer_set_option(k3moe_layer *L, int32_t option, int32_t value)
     }
     if (option == K3MOE_OPT_TC) {
         L->tc = value != 0;
+        return K3MOE_OK;
+    }
+    if (option == K3MOE_OPT_TC_E4M3) {
+        L->e4m3 = value != 0;
         return K3MOE_OK;
     }
     return K3MOE_EINVAL;

@@ -39,6 +39,7 @@
 // drains its copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "k3_device.cuh"
@@ -46,8 +47,9 @@
 namespace k3 {
 
 // One tile: up to TN tokens of one expert.  Token rows (nx of them, from
-// xrow0) and h rows (nh, from hrow0) keep hi rows at [0, n) and, when split,
-// lo rows at [P, P + n) with P = n rounded up to 8.
+// xrow0; `split` pieces of P = n rounded up to 8 rows each, or one block of
+// n rows rounded up to 16 when split is 1) and h rows (nh = 2P from hrow0,
+// bf16 hi then lo).
 struct TcTile {
     int32_t expert, pair_begin, n, nx, nh, xrow0, hrow0, split;
 };
@@ -55,33 +57,38 @@ struct TcTile {
 namespace {
 
 constexpr int TC_M = 128;           // weight rows per unit (MMA M)
-constexpr int TC_KS = 64;           // K per k-step: one 128-byte bf16 row
 constexpr int TC_SS = 256;          // K per staging step: 128 packed bytes per row
-constexpr int TC_KPS = TC_SS / TC_KS;
 constexpr int W_PK = 0, W_B = 1, W_MMA = 2, W_DEC = 3;
 constexpr int TC_NB = 16;           // token k-steps in flight at most
 constexpr int TC_SLOT = 2048;       // token ring granularity: 16 rows x 128 bytes
 constexpr uint32_t TC_TMEM_COLS = 512;
 
-template <int PH>
+// PH: 0 = gate/up + SwiGLU, 1 = down + combine.  KD: operand kind, 0 = bf16
+// (kind::f16, a k-step is 64 of K), 1 = e4m3 (kind::f8f6f4, 128 of K).
+template <int PH, int KD>
 struct TcCfg {
     static constexpr int NA = PH == 0 ? 2 : 1;                // matrices per unit
     static constexpr int SA = PH == 0 ? 3 : 4;                // decoded-weight stages
     static constexpr int SP = PH == 0 ? 2 : 3;                // packed staging stages
-    static constexpr int NSLOT = PH == 0 ? 32 : 56;           // token ring slots
+    static constexpr int KSK = KD ? 128 : 64;                 // K per k-step (one 128-byte row)
+    static constexpr int KPS = TC_SS / KSK;                   // k-steps per staging step
+    static constexpr int GPK = KSK / 32;                      // 32-groups per k-step
+    static constexpr int NSLOT = PH == 0 ? (KD ? 30 : 32) : 56;  // token ring slots
     static constexpr int BMAX = PH == 0 ? 128 : 256;          // token rows per k-step
     static constexpr int A_BYTES = NA * TC_M * 128;
     static constexpr int PK_BYTES = NA * TC_M * 128;          // swizzled like the operands
     static constexpr int PK_OFF = SA * A_BYTES;
     static constexpr int B_OFF = PK_OFF + SP * PK_BYTES;
-    static constexpr int BAR_OFF = B_OFF + NSLOT * TC_SLOT;
+    static constexpr int LUT_OFF = B_OFF + NSLOT * TC_SLOT;   // e4m3 decode tables (KD = 1)
+    static constexpr int BAR_OFF = LUT_OFF + (KD ? 256 * 8 : 0);
     static constexpr int SMEM = BAR_OFF + 512 + 1024;         // + barriers + alignment slack
     static constexpr int DEC = 8;                             // decoder warps
-    static constexpr int IPP = NA * 2 / (DEC / 4);            // 32-groups per thread per k-step
+    static constexpr int IPP = NA * GPK / (DEC / 4);          // 32-groups per thread per k-step
     static constexpr int W_EPI = W_DEC + DEC;
     static constexpr int THREADS = (W_EPI + 4) * 32;
-    static_assert(IPP == 1 || IPP == 2, "decoder split");
+    static_assert(IPP >= 1 && GPK % IPP == 0, "decoder split");
     static_assert(BMAX / 16 <= NSLOT / 2, "token ring too small");
+    static_assert(SMEM <= 232448, "shared memory");
 };
 
 K3_DEV uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -92,6 +99,8 @@ K3_DEV uint32_t bf16_idesc(int n)
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TC_M >> 4) << 24);
 }
+// kind::f8f6f4 with e4m3 A and B (format code 0), otherwise the same fields.
+K3_DEV uint32_t e4m3_idesc(int n) { return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TC_M >> 4) << 24); }
 // Shared-memory matrix descriptor of a K-major operand with the 128-byte
 // swizzle, split in its two 32-bit halves.  Low half: start address >> 4
 // (bits 0-13) and leading byte offset 1 (bits 16-29, unused with this
@@ -106,33 +115,40 @@ constexpr uint32_t SW128_HI = (1024u >> 4) | (1u << 14) | (2u << 29);
 // that issues.  The per-MMA offsets are added inside one asm block, so the
 // operands that vary from one k-step to the next are moved once per block
 // (an MMA whose descriptor is recomputed outside costs about 90 cycles more).
-#define K3_MMA4(TD, AL, BL)                                                                                  \
+// Both kinds read 32 bytes of K per MMA (16 bf16 or 32 e4m3 values).
+#define K3_MMA4(KIND, TD, AL, BL)                                                                            \
     "mov.b64 da, {" AL ", %5};\n\tmov.b64 db, {" BL ", %5};\n\t"                                          \
-    "@e tcgen05.mma.cta_group::1.kind::f16 [" TD "], da, db, %3, p;\n\t"                                    \
+    "@e tcgen05.mma.cta_group::1." KIND " [" TD "], da, db, %3, p;\n\t"                                     \
     "add.u32 a, " AL ", 2;\n\tadd.u32 b, " BL ", 2;\n\tmov.b64 da, {a, %5};\n\tmov.b64 db, {b, %5};\n\t" \
-    "@e tcgen05.mma.cta_group::1.kind::f16 [" TD "], da, db, %3, 1;\n\t"                                    \
+    "@e tcgen05.mma.cta_group::1." KIND " [" TD "], da, db, %3, 1;\n\t"                                     \
     "add.u32 a, " AL ", 4;\n\tadd.u32 b, " BL ", 4;\n\tmov.b64 da, {a, %5};\n\tmov.b64 db, {b, %5};\n\t" \
-    "@e tcgen05.mma.cta_group::1.kind::f16 [" TD "], da, db, %3, 1;\n\t"                                    \
+    "@e tcgen05.mma.cta_group::1." KIND " [" TD "], da, db, %3, 1;\n\t"                                     \
     "add.u32 a, " AL ", 6;\n\tadd.u32 b, " BL ", 6;\n\tmov.b64 da, {a, %5};\n\tmov.b64 db, {b, %5};\n\t" \
-    "@e tcgen05.mma.cta_group::1.kind::f16 [" TD "], da, db, %3, 1;\n\t"
-K3_DEV void mma_kstep1(uint32_t td, uint32_t alo, uint32_t blo, uint32_t idesc, uint32_t acc)
-{
-    asm volatile("{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t.reg .b32 a, b;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t" K3_MMA4("%0", "%1", "%2") "}" ::"r"(td),
-                 "r"(alo), "r"(blo), "r"(idesc), "r"(acc), "r"(SW128_HI)
-                 : "memory");
-}
+    "@e tcgen05.mma.cta_group::1." KIND " [" TD "], da, db, %3, 1;\n\t"
+#define K3_KSTEP1(KIND)                                                                                      \
+    asm volatile("{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t.reg .b32 a, b;\n\t"                      \
+                 "setp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t" K3_MMA4(KIND, "%0", "%1", "%2") "}" \
+                 ::"r"(td), "r"(alo), "r"(blo), "r"(idesc), "r"(acc), "r"(SW128_HI)                           \
+                 : "memory")
 // Two matrices (gate, up) against the same B: A of the second matrix is
 // 16 KB further (+1024 in the descriptor), its accumulator 128 columns on.
-K3_DEV void mma_kstep2(uint32_t td, uint32_t alo, uint32_t blo, uint32_t idesc, uint32_t acc)
+#define K3_KSTEP2(KIND)                                                                                      \
+    asm volatile("{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t.reg .b32 a, b, a1, t1;\n\t"              \
+                 "setp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"                                   \
+                 "add.u32 a1, %1, 1024;\n\tadd.u32 t1, %0, 128;\n\t" K3_MMA4(KIND, "%0", "%1", "%2")           \
+                     K3_MMA4(KIND, "t1", "a1", "%2") "}" ::"r"(td),                                           \
+                 "r"(alo), "r"(blo), "r"(idesc), "r"(acc), "r"(SW128_HI)                                      \
+                 : "memory")
+template <int NA, int KD>
+K3_DEV void mma_kstep(uint32_t td, uint32_t alo, uint32_t blo, uint32_t idesc, uint32_t acc)
 {
-    asm volatile("{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t.reg .b32 a, b, a1, t1;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
-                 "add.u32 a1, %1, 1024;\n\tadd.u32 t1, %0, 128;\n\t" K3_MMA4("%0", "%1", "%2")
-                     K3_MMA4("t1", "a1", "%2") "}" ::"r"(td),
-                 "r"(alo), "r"(blo), "r"(idesc), "r"(acc), "r"(SW128_HI)
-                 : "memory");
+    if constexpr (NA == 2 && KD == 0) K3_KSTEP2("kind::f16");
+    if constexpr (NA == 2 && KD == 1) K3_KSTEP2("kind::f8f6f4");
+    if constexpr (NA == 1 && KD == 0) K3_KSTEP1("kind::f16");
+    if constexpr (NA == 1 && KD == 1) K3_KSTEP1("kind::f8f6f4");
 }
+#undef K3_KSTEP1
+#undef K3_KSTEP2
 #undef K3_MMA4
 // Commit by the lane elect.sync picks (the lane that issued the MMAs).
 K3_DEV void mma_commit(uint32_t bar)
@@ -212,6 +228,21 @@ K3_DEV uint4 decode8_bf16_any(uint32_t w, float s)
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Eight codes (one word) -> eight e4m3 bytes through a per-scale table of
+// the eight magnitudes (t[m] = e4m3 of E2M1 magnitude m times 2^(e-127),
+// bytes 0-3 in tlo, 4-7 in thi): the magnitudes are byte lookups with the
+// nibbles as selectors, and each nibble's sign (bit 3) lands on bit 7 of its
+// byte by interleaving the bytes of w << 4 (even nibbles) and w (odd ones).
+K3_DEV uint2 decode8_e4m3(uint32_t w, uint32_t tlo, uint32_t thi)
+{
+    const uint32_t mag = w & 0x77777777u;
+    const uint32_t w4 = w << 4;
+    uint2 o;
+    o.x = prmt(tlo, thi, mag) | (prmt(w4, w, 0x5140u) & 0x80808080u);
+    o.y = prmt(tlo, thi, mag >> 16) | (prmt(w4, w, 0x7362u) & 0x80808080u);
+    return o;
+}
+
 K3_DEV bool tc_wait(uint32_t bar, uint32_t parity, int *err, volatile int *abort_flag)
 {
     if (*abort_flag) return false;
@@ -224,11 +255,11 @@ K3_DEV bool tc_wait(uint32_t bar, uint32_t parity, int *err, volatile int *abort
 
 K3_DEV uint32_t bf16_rn_bits(float v) { return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
-// Rows of a tile of n tokens.  A split operand keeps its hi rows at
-// [0, n) and its lo rows at [P, P + n), P = n rounded up to 8; every MMA
-// width is a multiple of 16.
+// Rows of a tile of n tokens.  An operand split in np pieces keeps piece c
+// in rows [c P, c P + n), P = n rounded up to 8 (bf16 hi/lo: np = 2; e4m3
+// pieces: np = 2 or 4); every MMA width is a multiple of 16.
 K3_DEV int tile_p(int n) { return (n + 7) & ~7; }
-K3_DEV int tile_nx(int n, bool xsplit) { return xsplit ? 2 * tile_p(n) : (n + 15) & ~15; }
+K3_DEV int tile_nx(int n, int np) { return np > 1 ? np * tile_p(n) : (n + 15) & ~15; }
 K3_DEV int tile_nh(int n) { return 2 * tile_p(n); }
 
 struct TcArgs {
@@ -241,16 +272,17 @@ struct TcArgs {
     float *out;               // phase 1 output [T x d]
     const int32_t *perm;
     const float *wsel;
+    const float *tscale;      // e4m3 token pieces: per-token scale of piece 0
     int k, d, f;
     int *err;
 };
 
 }  // namespace
 
-template <int PH>
-__global__ void __launch_bounds__(TcCfg<PH>::THREADS, 1) k3_tc_expert(const TcArgs a)
+template <int PH, int KD>
+__global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const TcArgs a)
 {
-    using C = TcCfg<PH>;
+    using C = TcCfg<PH, KD>;
     constexpr int W_EPI = C::W_EPI;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -269,7 +301,7 @@ __global__ void __launch_bounds__(TcCfg<PH>::THREADS, 1) k3_tc_expert(const TcAr
     const int ROWS = PH == 0 ? a.f : a.d;  // weight rows per matrix
     const int nrb = ROWS / TC_M;
     const int nss = K / TC_SS;
-    const int nks = K / TC_KS;
+    const int nks = K / C::KSK;
     const int n_units = *a.n_tiles * nrb;
     // Every role walks the same units (u = blockIdx.x, += gridDim.x) and
     // fetches the next unit's tile record one unit ahead.
@@ -299,6 +331,23 @@ __global__ void __launch_bounds__(TcCfg<PH>::THREADS, 1) k3_tc_expert(const TcAr
         mbar_init(bar(B_FIN), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if constexpr (KD == 1) {
+        // e4m3 of E2M1 magnitude m times 2^(e-127), for every scale byte e:
+        // exact for e in [119, 133]; 255 (a dropped group) and the bytes a
+        // layer on this path never holds get zeros.
+        uint2 *lut = (uint2 *)(sm + C::LUT_OFF);
+        for (int e = threadIdx.x; e < 256; e += blockDim.x) {
+            uint32_t t[2] = {0u, 0u};
+            if (e >= 119 && e <= 133) {
+                const float mag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+#pragma unroll
+                for (int m = 1; m < 8; m++)
+                    t[m >> 2] |= (uint32_t)__nv_cvt_float_to_fp8(ldexpf(mag[m], e - 127), __NV_SATFINITE, __NV_E4M3)
+                                 << (8 * (m & 3));
+            }
+            lut[e] = make_uint2(t[0], t[1]);
+        }
     }
     if (warp == W_MMA) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -370,7 +419,8 @@ __global__ void __launch_bounds__(TcCfg<PH>::THREADS, 1) k3_tc_expert(const TcAr
                     *abort_flag = 1;
                     break;
                 }
-                const uint8_t *src = a.Bsrc + (size_t)(PH == 0 ? tl.xrow0 : tl.hrow0) * K * 2;
+                // a row holds K elements: e4m3 token rows 1 byte each, bf16 rows 2
+                const uint8_t *src = a.Bsrc + (size_t)(PH == 0 ? tl.xrow0 : tl.hrow0) * K * (KD ? 1 : 2);
                 const uint32_t bytes = (uint32_t)nb * 128u;
                 const uint32_t c = (uint32_t)nb / 16u;
                 bool ok = true;
@@ -417,7 +467,7 @@ __global__ void __launch_bounds__(TcCfg<PH>::THREADS, 1) k3_tc_expert(const TcAr
                 *abort_flag = 1;
                 break;
             }
-            const uint32_t idesc = bf16_idesc(nb);
+            const uint32_t idesc = KD ? e4m3_idesc(nb) : bf16_idesc(nb);
             const int buf = ut & 1;
             if (ut >= 2 && !__all_sync(0xffffffffu, tc_wait(bar(B_ACCE + buf), ((ut / 2) - 1) & 1, a.err, abort_flag)))
                 break;
@@ -434,10 +484,7 @@ __global__ void __launch_bounds__(TcCfg<PH>::THREADS, 1) k3_tc_expert(const TcAr
                 tc_fence_after();
                 const uint32_t blo = sw128_lo(b_ring + boff[sb]);
                 const uint32_t alo = sw128_lo(a_stage(sa));
-                if (C::NA == 2)
-                    mma_kstep2(td, alo, blo, idesc, ks != 0);
-                else
-                    mma_kstep1(td, alo, blo, idesc, ks != 0);
+                mma_kstep<C::NA, KD>(td, alo, blo, idesc, ks != 0);
                 mma_commit(bar(B_AE + sa));
                 mma_commit(bar(B_BE + sb));
             }
@@ -450,13 +497,14 @@ __global__ void __launch_bounds__(TcCfg<PH>::THREADS, 1) k3_tc_expert(const TcAr
         __syncwarp();
     } else if (warp < W_EPI) {
         // ------------------------------------------------------- decoders
-        // Thread (row r, part p) decodes IPP of the row's NA x 2 32-groups
-        // of every k-step (items p*IPP .. p*IPP+IPP-1; item = 2 * matrix +
+        // Thread (row r, part p) decodes IPP of the row's NA x GPK 32-groups
+        // of every k-step (items p*IPP .. p*IPP+IPP-1; item = GPK * matrix +
         // group); the items of a part share one matrix.
         const int dw = warp - W_DEC;
         const int r = (dw & 3) * 32 + lane;  // weight row within the unit
         const int part = dw >> 2;
-        const int mat = (part * C::IPP) >> 1;
+        const int mat = (part * C::IPP) / C::GPK;
+        const uint32_t lut = sbase + (uint32_t)C::LUT_OFF;
         uint32_t it = 0, kt = 0;
         const int g_per_ss = TC_SS / 32;  // 8 scale bytes per row per staging step
         const int G = gridDim.x;
@@ -493,7 +541,7 @@ __global__ void __launch_bounds__(TcCfg<PH>::THREADS, 1) k3_tc_expert(const TcAr
             const int pslot = it % C::SP;
             if (!__all_sync(0xffffffffu, tc_wait(bar(B_PKF + pslot), (it / C::SP) & 1, a.err, abort_flag))) break;
             bool ok = true;
-            for (int kk = 0; kk < TC_KPS; kk++, kt++) {
+            for (int kk = 0; kk < C::KPS; kk++, kt++) {
                 const int slot = kt % C::SA;
                 if (kt >= (uint32_t)C::SA &&
                     !__all_sync(0xffffffffu, tc_wait(bar(B_AE + slot), ((kt / C::SA) - 1) & 1, a.err, abort_flag))) {
@@ -502,14 +550,29 @@ __global__ void __launch_bounds__(TcCfg<PH>::THREADS, 1) k3_tc_expert(const TcAr
                 }
                 const uint32_t src = pk_stage(pslot) + (uint32_t)(mat * TC_M * 128 + r * 128);
                 const uint32_t dst = a_stage(slot) + (uint32_t)(mat * TC_M * 128 + r * 128);
-                const uint32_t scw = kk < 2 ? sc.x : sc.y;
 #pragma unroll
                 for (int gg = 0; gg < C::IPP; gg++) {
-                    const int g = (part * C::IPP + gg) & 1;  // 32-group within the k-step
-                    // the group's 16 packed bytes are chunk 2 kk + g of the staged row
-                    const int pc = 2 * kk + g;
+                    const int g = (part * C::IPP + gg) % C::GPK;  // 32-group within the k-step
+                    // the group's 16 packed bytes are chunk pc of the staged row, its
+                    // scale byte pc of the staging step's 8
+                    const int pc = kk * C::GPK + g;
                     const uint4 q = lds128(src + (uint32_t)((pc ^ (r & 7)) << 4));
-                    const uint32_t e = (scw >> (16 * (kk & 1) + 8 * g)) & 0xffu;
+                    const uint32_t e = ((pc < 4 ? sc.x : sc.y) >> (8 * (pc & 3))) & 0xffu;
+                    if constexpr (KD == 1) {
+                        const uint2 t = lds64(lut + e * 8);
+                        const uint2 o0 = decode8_e4m3(q.x, t.x, t.y), o1 = decode8_e4m3(q.y, t.x, t.y);
+                        const uint2 o2 = decode8_e4m3(q.z, t.x, t.y), o3 = decode8_e4m3(q.w, t.x, t.y);
+                        // 32 e4m3 bytes = chunks 2g and 2g + 1 of the k-step's 128-byte row
+                        const uint32_t a0 = dst + (uint32_t)((((2 * g) ^ (r & 7))) << 4);
+                        const uint32_t a1 = dst + (uint32_t)((((2 * g + 1) ^ (r & 7))) << 4);
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(o0.x), "r"(o0.y),
+                                     "r"(o1.x), "r"(o1.y)
+                                     : "memory");
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(o2.x), "r"(o2.y),
+                                     "r"(o3.x), "r"(o3.y)
+                                     : "memory");
+                        continue;
+                    }
                     bool fast;
                     const uint16_t sh = e8m0_f16(e, fast);
                     uint4 o[4];
@@ -561,25 +624,36 @@ __global__ void __launch_bounds__(TcCfg<PH>::THREADS, 1) k3_tc_expert(const TcAr
             const int rb = u % nrb;
             const int P = tile_p(tl.n);
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 256);
-            const bool xsplit = PH == 0 && tl.split;
+            // token pieces: columns c P + j, piece c weighing rho^c (rho = 1 for
+            // bf16 hi/lo, 1/16 for e4m3 pieces, which also carry the token's
+            // scale); summed from the smallest piece up
+            const int np = PH == 0 ? (tl.split > 1 ? tl.split : 1) : 2;
+            const float rho = KD ? 0.0625f : 1.0f;
             for (int j0 = 0; j0 < tl.n; j0 += 8) {
                 if (PH == 0) {
                     float g[8], v[8], t[8];
-                    tmem_ld8(tbase + j0, g);
-                    if (xsplit) {
-                        tmem_ld8(tbase + P + j0, t);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 8; i++) g[i] += t[i];
-                    }
-                    tmem_ld8(tbase + 128 + j0, v);
-                    if (xsplit) {
-                        tmem_ld8(tbase + 128 + P + j0, t);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 8; i++) v[i] += t[i];
-                    }
+                    tmem_ld8(tbase + (np - 1) * P + j0, g);
+                    tmem_ld8(tbase + 128 + (np - 1) * P + j0, v);
                     tmem_wait_ld();
+                    for (int c = np - 2; c >= 0; c--) {
+                        tmem_ld8(tbase + c * P + j0, t);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 8; i++) g[i] = fmaf(g[i], rho, t[i]);
+                        tmem_ld8(tbase + 128 + c * P + j0, t);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 8; i++) v[i] = fmaf(v[i], rho, t[i]);
+                    }
+                    if (KD == 1) {
+#pragma unroll
+                        for (int i = 0; i < 8; i++) {
+                            const int j = min(j0 + i, tl.n - 1);
+                            const float sx = a.tscale[a.perm[tl.pair_begin + j] / a.k];
+                            g[i] *= sx;
+                            v[i] *= sx;
+                        }
+                    }
                     const int col = rb * TC_M + r;  // index into f
                     const int s = col >> 6, c = (col & 63) >> 3, byte = (col & 7) * 2;
                     uint8_t *hb = a.Hg + (size_t)tl.hrow0 * a.f * 2 + (size_t)s * tl.nh * 128 + byte;
@@ -632,7 +706,7 @@ __global__ void __launch_bounds__(TcCfg<PH>::THREADS, 1) k3_tc_expert(const TcAr
 // Tiles of at most tn tokens per expert, with the row offsets of each tile in
 // the token array (nx rows) and in the h array (nh rows).  One CTA.
 __global__ void __launch_bounds__(1024) k3_tc_plan(const int32_t *__restrict__ offsets, int E, int tn,
-                                                   int xsplit, int max_tiles, TcTile *tiles,
+                                                   int np, int max_tiles, TcTile *tiles,
                                                    int32_t *n_tiles, int *err)
 {
     __shared__ int wsum[3][32];
@@ -647,7 +721,7 @@ __global__ void __launch_bounds__(1024) k3_tc_plan(const int32_t *__restrict__ o
         int rx = 0, rh = 0;
         for (int j = 0; j < nt; j++) {
             const int n = min(tn, c - j * tn);
-            rx += tile_nx(n, xsplit);
+            rx += tile_nx(n, np);
             rh += tile_nh(n);
         }
         int v[3] = {nt, rx, rh}, inc[3];
@@ -679,7 +753,7 @@ __global__ void __launch_bounds__(1024) k3_tc_plan(const int32_t *__restrict__ o
         int hr = base[2] + wsum[2][warp] + inc[2] - v[2];
         for (int j = 0; j < nt; j++, t++) {
             const int n = min(tn, c - j * tn);
-            const int nx = tile_nx(n, xsplit), nh = tile_nh(n);
+            const int nx = tile_nx(n, np), nh = tile_nh(n);
             if (t < max_tiles) {
                 TcTile tl;
                 tl.expert = e;
@@ -689,7 +763,7 @@ __global__ void __launch_bounds__(1024) k3_tc_plan(const int32_t *__restrict__ o
                 tl.nh = nh;
                 tl.xrow0 = xr;
                 tl.hrow0 = hr;
-                tl.split = xsplit;
+                tl.split = np;
                 tiles[t] = tl;
             }
             xr += nx;
@@ -713,51 +787,143 @@ __global__ void __launch_bounds__(1024) k3_tc_plan(const int32_t *__restrict__ o
     }
 }
 
-// Token rows of every tile, bf16, k-step-major and pre-swizzled: the 8
-// 16-byte chunks of a row's 64-element slice sit at chunk ^ (row & 7).
-template <typename XT>
+// Token rows of every tile, k-step-major and pre-swizzled: the 8 16-byte
+// chunks of a row's 128-byte k-step slice sit at chunk ^ (row & 7).
+// KD = 0: bf16 rows (fp32 tokens as hi, lo pieces).  KD = 1: e4m3 pieces,
+// piece c = RN(r_c / s_c) with r_0 = x, r_{c+1} = r_c - s_c * piece c and
+// s_c = s_0 16^-c (s_0 = the token's scale, a power of two): every step is
+// exact in fp32, so the pieces sum to x within s_0 16^-np.
+template <typename XT, int KD>
 __global__ void __launch_bounds__(256) k3_tc_gather(const XT *__restrict__ X, const int32_t *__restrict__ perm,
                                                     int k, int d, const TcTile *__restrict__ tiles,
-                                                    const int32_t *n_tiles, uint8_t *Xg)
+                                                    const int32_t *n_tiles, const float *__restrict__ tscale,
+                                                    uint8_t *Xg)
 {
     const int nt = *n_tiles;
-    const int c8 = d / 8;
+    const int EPC = KD ? 16 : 8;  // elements per 16-byte chunk
+    const int cpr = d / EPC;      // chunks per row
+    const size_t rowb = KD ? (size_t)d : (size_t)d * 2;
     for (int t = blockIdx.x; t < nt; t += gridDim.x) {
         const TcTile tl = tiles[t];
         const int P = tile_p(tl.n);
-        const bool xsplit = tl.split != 0;
-        uint8_t *base = Xg + (size_t)tl.xrow0 * d * 2;
-        const int total = tl.nx * c8;
+        const int np = tl.split;
+        uint8_t *base = Xg + (size_t)tl.xrow0 * rowb;
+        const int total = tl.nx * cpr;
         for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
-            const int row = idx / c8, ch = idx - row * c8;
+            const int row = idx / cpr, ch = idx - row * cpr;
             const int s = ch >> 3, c = ch & 7;
-            int j = row;
-            bool lo = false;
-            if (xsplit && row >= P) {
-                j = row - P;
-                lo = true;
+            int j = row, piece = 0;
+            if (np > 1) {
+                piece = row / P;
+                j = row - piece * P;
             }
             uint4 o = make_uint4(0, 0, 0, 0);
-            if (j < tl.n) {
+            if (j < tl.n && piece < (np > 1 ? np : 1)) {
                 const int tok = perm[tl.pair_begin + j] / k;
+                float v[16];
                 if constexpr (sizeof(XT) == 2) {
-                    if (!lo) o = *(const uint4 *)((const uint16_t *)X + (size_t)tok * d + ch * 8);
+                    const uint4 *src = (const uint4 *)((const uint16_t *)X + (size_t)tok * d + ch * EPC);
+#pragma unroll
+                    for (int q = 0; q < EPC / 8; q++) {
+                        const uint4 u = src[q];
+                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int i = 0; i < 4; i++) {
+                            v[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
+                            v[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+                        }
+                    }
                 } else {
-                    const float4 *src = (const float4 *)((const float *)X + (size_t)tok * d + ch * 8);
-                    const float4 v0 = src[0], v1 = src[1];
-                    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                    const float4 *src = (const float4 *)((const float *)X + (size_t)tok * d + ch * EPC);
+#pragma unroll
+                    for (int q = 0; q < EPC / 4; q++) {
+                        const float4 f4 = src[q];
+                        v[4 * q] = f4.x;
+                        v[4 * q + 1] = f4.y;
+                        v[4 * q + 2] = f4.z;
+                        v[4 * q + 3] = f4.w;
+                    }
+                }
+                if constexpr (KD == 0) {
                     uint32_t h[8];
 #pragma unroll
                     for (int i = 0; i < 8; i++) {
                         const uint32_t hi = bf16_rn_bits(v[i]);
-                        h[i] = lo ? bf16_rn_bits(v[i] - __uint_as_float(hi << 16)) : hi;
+                        h[i] = piece ? bf16_rn_bits(v[i] - __uint_as_float(hi << 16)) : hi;
                     }
                     o = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+                } else {
+                    const float inv0 = 1.0f / tscale[tok];  // a power of two: exact
+                    uint32_t b[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                    for (int i = 0; i < 16; i += 2) {
+                        float r0 = v[i] * inv0, r1 = v[i + 1] * inv0;  // in units of s_0
+                        uint32_t q2 = 0;
+                        for (int cc = 0; cc <= piece; cc++) {
+                            q2 = __nv_cvt_float2_to_fp8x2(make_float2(r0, r1), __NV_SATFINITE, __NV_E4M3);
+                            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)q2, __NV_E4M3);
+                            const float2 back = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+                            r0 = (r0 - back.x) * 16.0f;
+                            r1 = (r1 - back.y) * 16.0f;
+                        }
+                        b[i >> 2] |= (q2 & 0xffffu) << (8 * (i & 3));  // elements i, i + 1 -> bytes i, i + 1
+                    }
+                    o = make_uint4(b[0], b[1], b[2], b[3]);
                 }
             }
             *(uint4 *)(base + (size_t)s * tl.nx * 128 + row * 128 + ((c ^ (row & 7)) << 4)) = o;
         }
     }
+}
+
+// s_0 of every token for e4m3 pieces: 2^(x - 8) where the token's largest
+// magnitude is m 2^x, m in [0.5, 1), so that |x| / s_0 < 256 < 448 (the e4m3
+// maximum); 1 for an all-zero token.  One warp per token.
+template <typename XT>
+__global__ void __launch_bounds__(256) k3_tc_token_scale(const XT *__restrict__ X, int T, int d, float *tscale)
+{
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (t >= T) return;
+    float m = 0.f;
+    for (int i = lane; i < d; i += 32) {
+        float v;
+        if constexpr (sizeof(XT) == 2)
+            v = __uint_as_float((uint32_t)((const uint16_t *)X)[(size_t)t * d + i] << 16);
+        else
+            v = ((const float *)X)[(size_t)t * d + i];
+        m = fmaxf(m, fabsf(v));
+    }
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    if (lane == 0) {
+        int ex = 0;
+        frexpf(m, &ex);
+        tscale[t] = m > 0.f ? ldexpf(1.f, ex - 8) : 1.f;
+    }
+}
+
+// Counts the gate and up scale bytes of every expert outside [119, 133] and
+// other than 255 (the bytes the e4m3 decode cannot represent exactly).
+__global__ void __launch_bounds__(256) k3_tc_scale_range(const DevExpert *__restrict__ table, int E, int d, int f,
+                                                        unsigned *bad)
+{
+    const int e = blockIdx.x, m = blockIdx.y;
+    const uint8_t *p = m == 0 ? table[e].gs : table[e].us;
+    const size_t n = (size_t)f * (d / 32);
+    unsigned cnt = 0;
+    for (size_t i = threadIdx.x * 16; i < n; i += blockDim.x * 16) {
+        const uint4 q = *(const uint4 *)(p + i);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            const uint32_t b = (w[j >> 2] >> (8 * (j & 3))) & 0xffu;
+            cnt += (b != 255u && (b < 119u || b > 133u));
+        }
+    }
+    if (cnt) atomicAdd(bad, cnt);
 }
 
 // --------------------------------------------------------------- launchers
@@ -769,12 +935,40 @@ bool tc_supported(int E, int k, int d, int f)
     return E >= 1 && k >= 1 && d % TC_SS == 0 && f % TC_SS == 0 && d >= TC_SS && f >= TC_SS &&
            d <= 16384 && f <= 16384;
 }
-int tc_tile_tokens(int xdt) { return xdt == K3MOE_BF16 ? 128 : 64; }
-int tc_max_tiles(int npairs, int E, int tn) { return (npairs + tn - 1) / tn + E; }
-// Rows of the token and h arrays for the worst case of either activation type.
-size_t tc_max_rows(int npairs, int E) { return 2 * ((size_t)npairs + 15 * (size_t)tc_max_tiles(npairs, E, 64)); }
+// Tokens per tile and pieces per token row for each operand kind: every
+// gate/up MMA is at most 128 columns wide.
+int tc_tile_tokens(int xdt, int kd) { return kd ? (xdt == K3MOE_BF16 ? 64 : 32) : (xdt == K3MOE_BF16 ? 128 : 64); }
+static int tc_pieces(int xdt, int kd) { return kd ? (xdt == K3MOE_BF16 ? 2 : 4) : (xdt == K3MOE_BF16 ? 1 : 2); }
+int tc_max_tiles(int npairs, int E) { return (npairs + 31) / 32 + E; }
+// Bytes of the token and h row arrays, the worst case over kinds and types.
+size_t tc_xg_bytes(int npairs, int E, int d) { return 4 * ((size_t)npairs + 7 * (size_t)tc_max_tiles(npairs, E)) * d; }
+size_t tc_hg_bytes(int npairs, int E, int f) { return 2 * ((size_t)npairs + 7 * (size_t)tc_max_tiles(npairs, E)) * f * 2; }
 size_t tc_tile_bytes() { return sizeof(TcTile); }
 size_t tc_map_bytes() { return sizeof(CUtensorMap); }
+
+// 1 when every gate and up scale byte of the E experts is in [119, 133] or
+// 255 (the e4m3 gate/up path is exact), 0 otherwise, negative on error.
+int tc_e4m3_eligible(const DevExpert *dev_table, int E, int d, int f, cudaStream_t s)
+{
+    unsigned *bad = nullptr;
+    unsigned h = 1;
+    if (cudaMalloc(&bad, sizeof(unsigned)) != cudaSuccess) {
+        cudaGetLastError();
+        return K3MOE_ENOMEM;
+    }
+    int rc = K3MOE_OK;
+    if (cudaMemsetAsync(bad, 0, sizeof(unsigned), s) != cudaSuccess) rc = K3MOE_ECUDA;
+    if (rc == K3MOE_OK) {
+        k3_tc_scale_range<<<dim3(E, 2), 256, 0, s>>>(dev_table, E, d, f, bad);
+        if (cudaGetLastError() != cudaSuccess ||
+            cudaMemcpyAsync(&h, bad, sizeof(unsigned), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            rc = K3MOE_ECUDA;
+    }
+    cudaGetLastError();
+    cudaFree(bad);
+    return rc == K3MOE_OK ? (h == 0 ? 1 : 0) : rc;
+}
 
 // Tensor maps of the packed planes of E experts (host table of device plane
 // pointers): [E][gate, up, down], 2D u8 tensors of rows x in/2 bytes, boxes
@@ -821,46 +1015,65 @@ int tc_make_maps(const DevExpert *host_table, int E, int d, int f, void *dev_map
     return rc;
 }
 
-template <int PH>
+template <int PH, int KD>
 static int launch_expert(const TcArgs &a, cudaStream_t s)
 {
+    using C = TcCfg<PH, KD>;
     static bool ready = false;
     if (!ready) {
-        if (cudaFuncSetAttribute(k3_tc_expert<PH>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<PH>::SMEM) !=
+        if (cudaFuncSetAttribute(k3_tc_expert<PH, KD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
             cudaSuccess)
             return K3MOE_ECUDA;
         ready = true;
     }
-    k3_tc_expert<PH><<<num_sms(), TcCfg<PH>::THREADS, TcCfg<PH>::SMEM, s>>>(a);
+    k3_tc_expert<PH, KD><<<num_sms(), C::THREADS, C::SMEM, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
 }
 
-// Plan, token gather and the gate/up + SwiGLU phase (h into Hg).
-int launch_tc_gateup(const void *X, int xdt, int k, int E, int d, int f, const DevExpert *table,
-                     const void *maps, const int32_t *offsets, const int32_t *perm, void *tiles,
-                     int32_t *n_tiles, int max_tiles, uint8_t *Xg, uint8_t *Hg, int *err, cudaStream_t s)
+// Plan, token rows and the gate/up + SwiGLU phase (h into Hg); kd = 1 runs
+// gate/up on e4m3 operands (only for layers whose scale bytes allow it).
+int launch_tc_gateup(const void *X, int xdt, int T, int kd, int k, int E, int d, int f, const DevExpert *table,
+                     const void *maps, const int32_t *offsets, const int32_t *perm, void *tiles, int32_t *n_tiles,
+                     int max_tiles, float *tscale, uint8_t *Xg, uint8_t *Hg, int *err, cudaStream_t s)
 {
-    const int tn = tc_tile_tokens(xdt);
-    k3_tc_plan<<<1, 1024, 0, s>>>(offsets, E, tn, xdt == K3MOE_F32, max_tiles, (TcTile *)tiles, n_tiles, err);
+    const int tn = tc_tile_tokens(xdt, kd), np = tc_pieces(xdt, kd);
+    k3_tc_plan<<<1, 1024, 0, s>>>(offsets, E, tn, np, max_tiles, (TcTile *)tiles, n_tiles, err);
     if (cudaGetLastError() != cudaSuccess) return K3MOE_ECUDA;
+    if (kd) {
+        if (xdt == K3MOE_BF16)
+            k3_tc_token_scale<uint16_t><<<(T + 7) / 8, 256, 0, s>>>((const uint16_t *)X, T, d, tscale);
+        else
+            k3_tc_token_scale<float><<<(T + 7) / 8, 256, 0, s>>>((const float *)X, T, d, tscale);
+        if (cudaGetLastError() != cudaSuccess) return K3MOE_ECUDA;
+    }
     const int g = 2 * num_sms();
-    if (xdt == K3MOE_BF16)
-        k3_tc_gather<uint16_t><<<g, 256, 0, s>>>((const uint16_t *)X, perm, k, d, (const TcTile *)tiles, n_tiles, Xg);
-    else
-        k3_tc_gather<float><<<g, 256, 0, s>>>((const float *)X, perm, k, d, (const TcTile *)tiles, n_tiles, Xg);
+    const TcTile *tl = (const TcTile *)tiles;
+    if (xdt == K3MOE_BF16) {
+        if (kd)
+            k3_tc_gather<uint16_t, 1><<<g, 256, 0, s>>>((const uint16_t *)X, perm, k, d, tl, n_tiles, tscale, Xg);
+        else
+            k3_tc_gather<uint16_t, 0><<<g, 256, 0, s>>>((const uint16_t *)X, perm, k, d, tl, n_tiles, tscale, Xg);
+    } else {
+        if (kd)
+            k3_tc_gather<float, 1><<<g, 256, 0, s>>>((const float *)X, perm, k, d, tl, n_tiles, tscale, Xg);
+        else
+            k3_tc_gather<float, 0><<<g, 256, 0, s>>>((const float *)X, perm, k, d, tl, n_tiles, tscale, Xg);
+    }
     if (cudaGetLastError() != cudaSuccess) return K3MOE_ECUDA;
     TcArgs a = {};
-    a.tiles = (const TcTile *)tiles;
+    a.tiles = tl;
     a.n_tiles = n_tiles;
     a.table = table;
     a.maps = (const CUtensorMap *)maps;
     a.Bsrc = Xg;
     a.Hg = Hg;
+    a.perm = perm;
+    a.tscale = tscale;
     a.k = k;
     a.d = d;
     a.f = f;
     a.err = err;
-    return launch_expert<0>(a, s);
+    return kd ? launch_expert<0, 1>(a, s) : launch_expert<0, 0>(a, s);
 }
 
 // Down phase and the weighted combine: out = sum_j w_j y_j (out is zeroed first).
@@ -882,7 +1095,7 @@ int launch_tc_down(int T, int k, int d, int f, const DevExpert *table, const voi
     a.d = d;
     a.f = f;
     a.err = err;
-    return launch_expert<1>(a, s);
+    return launch_expert<1, 0>(a, s);
 }
 
 }  // namespace k3

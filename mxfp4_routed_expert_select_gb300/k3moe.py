@@ -26,6 +26,7 @@ K3MOE_BF16 = 1
 K3MOE_OPT_FUSED_T1 = 1
 K3MOE_OPT_ACT_F16 = 2
 K3MOE_OPT_TC = 4
+K3MOE_OPT_TC_E4M3 = 8
 K3MOE_NOALLOC_MAX_F = 2048
 
 

@@ -14,8 +14,9 @@ from mxfp4_routed_expert_select_gb300 import k3moe as k
 pytestmark = pytest.mark.gpu
 
 
-def _forward(L, X, T, K, tc=True):
+def _forward(L, X, T, K, tc=True, e4m3=True):
     L.set_option(k.K3MOE_OPT_TC, 1 if tc else 0)
+    L.set_option(k.K3MOE_OPT_TC_E4M3, 1 if e4m3 else 0)
     out = torch.empty((T, L.d), dtype=torch.float32, device="cuda")
     ids = torch.empty((T, K), dtype=torch.int32, device="cuda")
     w = torch.empty((T, K), dtype=torch.float32, device="cuda")
@@ -25,14 +26,14 @@ def _forward(L, X, T, K, tc=True):
     return out.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
 
 
-def _case(pool, Wr_bits, bias, K, T, bf16, sample=None, witness=True):
+def _case(pool, Wr_bits, bias, K, T, bf16, sample=None, witness=True, e4m3=True):
     d, f, E = pool.d, pool.f, pool.E
     subs = margin_subs(pool.pool, T, d, Wr_bits, K, bias, bf16=bf16)
     Xd = tokens(pool.pool, np.arange(T), d, subs, bf16)
     X = tokens_device(pool.pool, T, d, subs, bf16)
     bt = None if bias is None else torch.from_numpy(np.asarray(bias, np.float32)).cuda()
     L = k.Layer(E, K, d, f, router_tensor(Wr_bits), pool.views, bt, max_tokens=T)
-    out, ids, w = _forward(L, X, T, K, tc=True)
+    out, ids, w = _forward(L, X, T, K, tc=True, e4m3=e4m3)
     lg = oracle.router_logits(Xd, Wr_bits)
     rids, rw, m = oracle.topk(lg, K, None if bias is None else np.asarray(bias, np.float64))
     assert np.all(m >= 1e-3)
@@ -57,11 +58,12 @@ def small():
     return pool, synth.router_bf16(5, 0, E, d), synth.bias_normal(5, 0, E), K
 
 
+@pytest.mark.parametrize("e4m3", [True, False])
 @pytest.mark.parametrize("T,bf16,use_bias", [(2, False, False), (37, False, True), (37, True, False),
                                              (200, True, True), (200, False, False)])
-def test_tc_small_layer(small, T, bf16, use_bias):
+def test_tc_small_layer(small, T, bf16, use_bias, e4m3):
     pool, Wr_bits, bias, K = small
-    _case(pool, Wr_bits, bias if use_bias else None, K, T, bf16)
+    _case(pool, Wr_bits, bias if use_bias else None, K, T, bf16, e4m3=e4m3)
 
 
 @pytest.fixture(scope="module")
@@ -73,10 +75,11 @@ def few_experts():
     return pool, synth.router_bf16(12, 0, E, d), K
 
 
+@pytest.mark.parametrize("e4m3", [True, False])
 @pytest.mark.parametrize("bf16", [False, True])
-def test_tc_several_tiles_per_expert(few_experts, bf16):
+def test_tc_several_tiles_per_expert(few_experts, bf16, e4m3):
     pool, Wr_bits, K = few_experts
-    out, ids = _case(pool, Wr_bits, None, K, 600, bf16, sample=[0, 1, 299, 598, 599])
+    out, ids = _case(pool, Wr_bits, None, K, 600, bf16, sample=[0, 1, 299, 598, 599], e4m3=e4m3)
     counts = np.bincount(ids.ravel(), minlength=pool.E)
     assert counts.max() > 128
 
@@ -123,4 +126,20 @@ def test_tc_layer_forward_twice_is_repeatable(small):
     assert np.array_equal(ia, ib)
     for t in range(T):
         assert rel_err(a[t], b[t]) <= 1e-6
+    L.close()
+
+
+def test_e4m3_path_agrees_with_the_bf16_path_and_is_chosen_only_where_exact(small):
+    """The two operand kinds of the tensor path give the same outputs to
+    fp32-class error on an eligible layer (scale bytes in [120, 130])."""
+    pool, Wr_bits, bias, K = small
+    T, d = 96, pool.d
+    subs = margin_subs(5, T, d, Wr_bits, K)
+    X = tokens_device(5, T, d, subs)
+    L = k.Layer(pool.E, K, d, pool.f, router_tensor(Wr_bits), pool.views, max_tokens=T)
+    a, ia, _ = _forward(L, X, T, K, e4m3=True)
+    b, ib, _ = _forward(L, X, T, K, e4m3=False)
+    assert np.array_equal(ia, ib)
+    for t in range(T):
+        assert rel_err(a[t], b[t]) <= 2e-4, t
     L.close()
