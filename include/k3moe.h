@@ -255,16 +255,16 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int x_dtype, int32_t T, f
  *                      combine by fp32 atomic adds (summation order not
  *                      fixed).  Needs d % 256 == 0 and f % 256 == 0; default 1.
  *                      0 selects the CUDA-core grouped path.
- *  K3MOE_OPT_TC_E4M3   on the K3MOE_OPT_TC path, run gate/up with e4m3
- *                      operands (kind::f8f6f4): weights decoded exactly to
- *                      e4m3 (possible when every gate/up scale byte of the
- *                      layer is in [119, 133] or 255, checked at layer
- *                      creation; otherwise the option has no effect) and
- *                      activations as e4m3 pieces with power-of-two scales
- *                      (4 pieces for fp32 tokens, each element then within
- *                      2^-15 of the token's largest magnitude; 2 for bf16
- *                      tokens, exact but for elements below about 2^-10 of
- *                      that magnitude); the down product stays bf16.
+ *  K3MOE_OPT_TC_E4M3   on the K3MOE_OPT_TC path, run the expert products
+ *                      with e4m3 operands (kind::f8f6f4): weights decoded
+ *                      exactly to e4m3 (possible when every scale byte of
+ *                      the layer is in [119, 133] or 255, checked at layer
+ *                      creation; otherwise the option has no effect),
+ *                      activations and h as e4m3 pieces with power-of-two
+ *                      scales (4 pieces for fp32 tokens and for h, each
+ *                      element then within 2^-15 of its token's or pair's
+ *                      largest magnitude; 2 for bf16 tokens, exact but for
+ *                      elements below about 2^-10 of that magnitude).
  *                      Default 1.
  * k3moe_layer_fused_t1 returns 1 when a batch-1 fp32 forward of this layer
  * would run fused, else 0 (negative on error).  After a device-side timeout

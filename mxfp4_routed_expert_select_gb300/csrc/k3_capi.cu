@@ -55,10 +55,11 @@ int tc_make_maps(const DevExpert *host_table, int E, int d, int f, void *dev_map
 int tc_e4m3_eligible(const DevExpert *dev_table, int E, int d, int f, cudaStream_t s);
 int launch_tc_gateup(const void *X, int xdt, int T, int kd, int k, int E, int d, int f, const DevExpert *table,
                      const void *maps, const int32_t *offsets, const int32_t *perm, void *tiles, int32_t *n_tiles,
-                     int max_tiles, float *tscale, uint8_t *Xg, uint8_t *Hg, int *err, cudaStream_t s);
-int launch_tc_down(int T, int k, int d, int f, const DevExpert *table, const void *maps, const int32_t *perm,
-                   const float *wsel, const void *tiles, const int32_t *n_tiles, const uint8_t *Hg, float *out,
-                   int *err, cudaStream_t s);
+                     int max_tiles, float *tscale, uint8_t *Xg, uint8_t *Hg, float *hf, unsigned *hmax, int *err,
+                     cudaStream_t s);
+int launch_tc_down(int T, int kd, int k, int d, int f, const DevExpert *table, const void *maps, const int32_t *perm,
+                   const float *wsel, const void *tiles, const int32_t *n_tiles, uint8_t *Hg, const float *hf,
+                   unsigned *hmax, float *out, int *err, cudaStream_t s);
 int launch_grouped_gateup(const void *X, int xdt, const DevExpert *table, const int32_t *perm,
                           const int4 *items, const int32_t *n_items, int max_items, int k, int d,
                           int f, float *h, cudaStream_t s);
@@ -269,6 +270,8 @@ struct k3moe_layer {
     bool e4m3_ok;        // every gate/up scale byte allows the exact e4m3 decode
     bool e4m3;           // K3MOE_OPT_TC_E4M3 (default on where e4m3_ok)
     float *tscale;       // [maxT] token scales of the e4m3 pieces
+    float *hf;           // [maxT * k * f] h in fp32 (e4m3 down)
+    unsigned *hmax;      // [maxT * k] per-pair max |h| bits (e4m3 down)
 };
 
 static void layer_free(k3moe_layer *L)
@@ -276,7 +279,7 @@ static void layer_free(k3moe_layer *L)
     if (!L) return;
     void *ptrs[] = {L->table, L->logits, L->part,  L->ids,     L->w,      L->h,    L->Y,
                     L->offsets, L->perm, L->items, L->n_items, L->ticket, L->ctr,
-                    L->tc_tiles, L->tc_ntiles, L->Xg, L->Hg, L->tc_maps, L->tscale};
+                    L->tc_tiles, L->tc_ntiles, L->Xg, L->Hg, L->tc_maps, L->tscale, L->hf, L->hmax};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete L;
@@ -335,6 +338,8 @@ int k3moe_layer_create(k3moe_layer **out, const k3moe_layer_desc *D)
         alloc((void **)&L->Xg, k3::tc_xg_bytes((int)pairs, L->E, L->d));
         alloc((void **)&L->Hg, k3::tc_hg_bytes((int)pairs, L->E, L->f));
         alloc((void **)&L->tscale, sizeof(float) * L->maxT);
+        alloc((void **)&L->hf, sizeof(float) * pairs * L->f);
+        alloc((void **)&L->hmax, sizeof(unsigned) * pairs);
         alloc(&L->tc_maps, k3::tc_map_bytes() * 3 * L->E);
         L->tc_ready = ok;
         L->tc = true;
@@ -448,12 +453,13 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int xdt, int32_t T, float
         int *err = k3::device_error_word();
         K3_TRY(k3::launch_group(L->ids, T * L->k, L->E, k3::grouped_nt(), L->offsets, L->perm,
                                 L->items, L->n_items, st));
-        K3_TRY(k3::launch_tc_gateup(X, xdt, T, (L->e4m3 && L->e4m3_ok) ? 1 : 0, L->k, L->E, L->d, L->f,
-                                    L->table, L->tc_maps, L->offsets, L->perm, L->tc_tiles, L->tc_ntiles,
-                                    L->tc_max_tiles, L->tscale, L->Xg, L->Hg, err, st));
+        const int kd = (L->e4m3 && L->e4m3_ok) ? 1 : 0;
+        K3_TRY(k3::launch_tc_gateup(X, xdt, T, kd, L->k, L->E, L->d, L->f, L->table, L->tc_maps, L->offsets,
+                                    L->perm, L->tc_tiles, L->tc_ntiles, L->tc_max_tiles, L->tscale, L->Xg,
+                                    L->Hg, L->hf, L->hmax, err, st));
         if (L->nev) K3_CUDA(cudaEventRecord(L->ev[2], st));
-        K3_TRY(k3::launch_tc_down(T, L->k, L->d, L->f, L->table, L->tc_maps, L->perm, L->w,
-                                  L->tc_tiles, L->tc_ntiles, L->Hg, out, err, st));
+        K3_TRY(k3::launch_tc_down(T, kd, L->k, L->d, L->f, L->table, L->tc_maps, L->perm, L->w,
+                                  L->tc_tiles, L->tc_ntiles, L->Hg, L->hf, L->hmax, out, err, st));
     } else {
         const int npairs = T * L->k;
         K3_TRY(k3::launch_group(L->ids, npairs, L->E, k3::grouped_nt(), L->offsets, L->perm,

@@ -48,8 +48,8 @@ namespace k3 {
 
 // One tile: up to TN tokens of one expert.  Token rows (nx of them, from
 // xrow0; `split` pieces of P = n rounded up to 8 rows each, or one block of
-// n rows rounded up to 16 when split is 1) and h rows (nh = 2P from hrow0,
-// bf16 hi then lo).
+// n rows rounded up to 16 when split is 1) and h rows (nh from hrow0: bf16
+// hi and lo, nh = 2P, or four e4m3 pieces, nh = 4P).
 struct TcTile {
     int32_t expert, pair_begin, n, nx, nh, xrow0, hrow0, split;
 };
@@ -73,7 +73,7 @@ struct TcCfg {
     static constexpr int KSK = KD ? 128 : 64;                 // K per k-step (one 128-byte row)
     static constexpr int KPS = TC_SS / KSK;                   // k-steps per staging step
     static constexpr int GPK = KSK / 32;                      // 32-groups per k-step
-    static constexpr int NSLOT = PH == 0 ? (KD ? 30 : 32) : 56;  // token ring slots
+    static constexpr int NSLOT = PH == 0 ? (KD ? 30 : 32) : (KD ? 54 : 56);  // token ring slots
     static constexpr int BMAX = PH == 0 ? 128 : 256;          // token rows per k-step
     static constexpr int A_BYTES = NA * TC_M * 128;
     static constexpr int PK_BYTES = NA * TC_M * 128;          // swizzled like the operands
@@ -81,7 +81,10 @@ struct TcCfg {
     static constexpr int B_OFF = PK_OFF + SP * PK_BYTES;
     static constexpr int LUT_OFF = B_OFF + NSLOT * TC_SLOT;   // e4m3 decode tables (KD = 1)
     static constexpr int BAR_OFF = LUT_OFF + (KD ? 256 * 8 : 0);
-    static constexpr int SMEM = BAR_OFF + 512 + 1024;         // + barriers + alignment slack
+    static constexpr int NBARS = 2 * SP + 2 * SA + 3 * 16 + 5;  // mbarriers (see the kernel)
+    static constexpr int BAR_BYTES = 768;                     // mbarriers, token ring offsets, TMEM slot, flag
+    static constexpr int SMEM = BAR_OFF + BAR_BYTES + 1024;   // + alignment slack
+    static_assert(NBARS * 8 + 16 * 4 + 8 <= BAR_BYTES, "barrier block");
     static constexpr int DEC = 8;                             // decoder warps
     static constexpr int IPP = NA * GPK / (DEC / 4);          // 32-groups per thread per k-step
     static constexpr int W_EPI = W_DEC + DEC;
@@ -160,6 +163,35 @@ K3_DEV void mma_commit(uint32_t bar)
 K3_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 K3_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 K3_DEV void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Thread-block clusters: this CTA's rank, the cluster's size and index, the
+// number of clusters; a cluster-wide barrier (every thread of every CTA).
+K3_DEV uint32_t cluster_rank() { uint32_t r; asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r)); return r; }
+K3_DEV uint32_t cluster_size() { uint32_t r; asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r)); return r; }
+K3_DEV uint32_t cluster_id() { uint32_t r; asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r)); return r; }
+K3_DEV uint32_t cluster_count() { uint32_t r; asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r)); return r; }
+K3_DEV void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Bulk copy global -> the same shared offset of every CTA in `mask`, each
+// CTA's barrier at `bar` counting the bytes that land in it.
+K3_DEV void bulk_g2s_multicast(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar, uint16_t mask)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, "
+                 "[%3], %4;" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar), "h"(mask)
+                 : "memory");
+}
+// Commit (by the elected lane) arriving on the barrier at `bar` in every CTA
+// of `mask` once this thread's MMAs so far have completed.
+K3_DEV void mma_commit_multicast(uint32_t bar, uint16_t mask)
+{
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}"
+                 ::"r"(bar), "h"(mask)
+                 : "memory");
+}
 
 // 2D tiled TMA load (x = byte column, a multiple of 16; y = row).
 K3_DEV void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
@@ -253,14 +285,53 @@ K3_DEV bool tc_wait(uint32_t bar, uint32_t parity, int *err, volatile int *abort
     return true;
 }
 
+// out[0..3] += v0..v3 with one vector reduction (16-byte aligned address).
+K3_DEV void red_add_v4(float *out, float v0, float v1, float v2, float v3)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(out), "f"(v0), "f"(v1), "f"(v2), "f"(v3)
+                 : "memory");
+}
+// Transposes an 8 x 8 block held by groups of 8 lanes: before, lane g holds
+// v[i] = A[g][i]; after, v[i] = A[i][g] (three butterfly exchange stages).
+K3_DEV void transpose8(float (&v)[8], int lane)
+{
+    const int g = lane & 7;
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            if ((i & m) == 0) {
+                const bool upper = (g & m) != 0;
+                const float send = upper ? v[i] : v[i | m];
+                const float recv = __shfl_xor_sync(0xffffffffu, send, m);
+                if (upper)
+                    v[i] = recv;
+                else
+                    v[i | m] = recv;
+            }
+        }
+    }
+}
+
 K3_DEV uint32_t bf16_rn_bits(float v) { return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+
+// Scale of piece 0 of e4m3 pieces for values of largest magnitude m:
+// 2^(x - 8) for m = mant 2^x, mant in [0.5, 1) (so |v| / scale < 256, below
+// the e4m3 maximum 448); 1 for m = 0.
+K3_DEV float piece_scale(float m)
+{
+    int ex = 0;
+    frexpf(m, &ex);
+    return m > 0.f ? ldexpf(1.f, ex - 8) : 1.f;
+}
+K3_DEV float h_scale(unsigned mbits) { return piece_scale(__uint_as_float(mbits)); }
 
 // Rows of a tile of n tokens.  An operand split in np pieces keeps piece c
 // in rows [c P, c P + n), P = n rounded up to 8 (bf16 hi/lo: np = 2; e4m3
 // pieces: np = 2 or 4); every MMA width is a multiple of 16.
 K3_DEV int tile_p(int n) { return (n + 7) & ~7; }
 K3_DEV int tile_nx(int n, int np) { return np > 1 ? np * tile_p(n) : (n + 15) & ~15; }
-K3_DEV int tile_nh(int n) { return 2 * tile_p(n); }
+K3_DEV int tile_nh(int n, int nph) { return nph * tile_p(n); }
 
 struct TcArgs {
     const TcTile *tiles;
@@ -273,6 +344,8 @@ struct TcArgs {
     const int32_t *perm;
     const float *wsel;
     const float *tscale;      // e4m3 token pieces: per-token scale of piece 0
+    float *hf;                // e4m3 down: h in fp32, [pair][f] in tile order
+    unsigned *hmax;           // e4m3 down: per pair, bits of max |h| (non-negative floats order as ints)
     int k, d, f;
     int *err;
 };
@@ -289,8 +362,9 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
     const uint32_t sbase = smem_addr(sm);
     uint64_t *bars = (uint64_t *)(sm + C::BAR_OFF);
     const int B_PKF = 0, B_PKE = B_PKF + C::SP, B_AF = B_PKE + C::SP, B_AE = B_AF + C::SA, B_BF = B_AE + C::SA,
-              B_BE = B_BF + TC_NB, B_ACCF = B_BE + TC_NB, B_ACCE = B_ACCF + 2, B_FIN = B_ACCE + 2,
-              NBARS = B_FIN + 1;
+              B_BE = B_BF + TC_NB, B_BEC = B_BE + TC_NB, B_ACCF = B_BEC + TC_NB, B_ACCE = B_ACCF + 2,
+              B_FIN = B_ACCE + 2, NBARS = B_FIN + 1;
+    static_assert(2 * C::SP + 2 * C::SA + 3 * TC_NB + 5 == C::NBARS, "barrier count");
     volatile uint32_t *boff = (volatile uint32_t *)(bars + NBARS);  // [TC_NB] token ring offsets
     uint32_t *tmem_slot = (uint32_t *)(boff + TC_NB);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
@@ -302,12 +376,21 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
     const int nrb = ROWS / TC_M;
     const int nss = K / TC_SS;
     const int nks = K / C::KSK;
-    const int n_units = *a.n_tiles * nrb;
-    // Every role walks the same units (u = blockIdx.x, += gridDim.x) and
-    // fetches the next unit's tile record one unit ahead.
-    auto tile_at = [&](int v) -> TcTile {
+    // Clusters of CS CTAs take groups of CS consecutive row blocks of one
+    // tile (CTA rank r the r-th); the cluster's leader copies each k-step of
+    // the tile's token (or h) rows once, to every CTA of the cluster.  Every
+    // role walks the same groups (cluster index, += number of clusters) and
+    // fetches the next group's tile record one group ahead.
+    const int CS = (int)cluster_size(), crank = (int)cluster_rank();
+    const int ncl = (int)cluster_count(), cid = (int)cluster_id();
+    const bool leader = crank == 0;
+    const uint16_t cmask = (uint16_t)((1u << CS) - 1u);
+    const int gpt = nrb / CS;                   // groups per tile
+    const int n_groups = *a.n_tiles * gpt;
+    auto unit_of = [&](int ug) { return (ug / gpt) * nrb + (ug % gpt) * CS + crank; };
+    auto tile_at = [&](int ug) -> TcTile {
         TcTile t = {};
-        if (v < n_units) t = a.tiles[v / nrb];
+        if (ug < n_groups) t = a.tiles[ug / gpt];
         return t;
     };
 
@@ -323,6 +406,7 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
         for (int i = 0; i < TC_NB; i++) {
             mbar_init(bar(B_BF + i), 1);
             mbar_init(bar(B_BE + i), 1);
+            mbar_init(bar(B_BEC + i), CS);  // the leader's: one commit per CTA of the cluster
         }
         for (int i = 0; i < 2; i++) {
             mbar_init(bar(B_ACCF + i), 1);
@@ -358,6 +442,7 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // every CTA's barriers exist before any copy or commit reaches them
     tc_fence_after();
     const uint32_t tmem = *(volatile uint32_t *)tmem_slot;
 
@@ -372,10 +457,11 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
 #pragma unroll
         for (int i = 0; i < C::SP; i++) issued[i] = 0;
         if (lane == 0) {
-            TcTile tl_next = tile_at(blockIdx.x);
-            for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
+            TcTile tl_next = tile_at(cid);
+            for (int ug = cid; ug < n_groups && !*abort_flag; ug += ncl) {
+                const int u = unit_of(ug);
                 const TcTile tl = tl_next;
-                tl_next = tile_at(u + (int)gridDim.x);
+                tl_next = tile_at(ug + ncl);
                 const int rb = u % nrb;
                 const CUtensorMap *mp = a.maps + 3 * tl.expert + (PH == 0 ? 0 : 2);
                 bool ok = true;
@@ -406,13 +492,19 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
         // starts at `head` (skipping to the ring start when it would not fit
         // before the end) and the slots up to the end of the oldest k-step
         // the MMAs have finished are free again.
+        // Every CTA runs the same allocation (the offsets depend only on the
+        // tiles' widths); the leader waits until every CTA of the cluster is
+        // done with the slots (its cluster-wide barriers) and issues the copy
+        // to all of them, the others only announce the bytes to expect once
+        // their own MMAs are done with the k-step the barrier last served.
         if (lane == 0) {
             uint32_t kt = 0, done = 0, head = 0, tail = 0;
             uint32_t endv[TC_NB];
-            TcTile tl_next = tile_at(blockIdx.x);
-            for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
+            const int B_FREE = (leader && CS > 1) ? B_BEC : B_BE;
+            TcTile tl_next = tile_at(cid);
+            for (int ug = cid; ug < n_groups && !*abort_flag; ug += ncl) {
                 const TcTile tl = tl_next;
-                tl_next = tile_at(u + (int)gridDim.x);
+                tl_next = tile_at(ug + ncl);
                 const int nb = PH == 0 ? tl.nx : tl.nh;
                 if (nb < 16 || nb % 16 || nb > C::BMAX) {
                     set_device_error(a.err, K3MOE_EINVAL);
@@ -429,7 +521,7 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
                     if (start % C::NSLOT + c > (uint32_t)C::NSLOT) start += C::NSLOT - start % C::NSLOT;
                     while (kt - done >= (uint32_t)TC_NB || start + c - tail > (uint32_t)C::NSLOT) {
                         if (done == kt ||
-                            !tc_wait(bar(B_BE + done % TC_NB), (done / TC_NB) & 1, a.err, abort_flag)) {
+                            !tc_wait(bar(B_FREE + done % TC_NB), (done / TC_NB) & 1, a.err, abort_flag)) {
                             if (done == kt) set_device_error(a.err, K3MOE_EINVAL);
                             *abort_flag = 1;
                             ok = false;
@@ -444,7 +536,11 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
                     const uint32_t off = (start % C::NSLOT) * TC_SLOT;
                     boff[kt % TC_NB] = off;
                     mbar_arrive_expect_tx(bar(B_BF + kt % TC_NB), bytes);
-                    bulk_g2s(b_ring + off, src + (size_t)ks * bytes, bytes, bar(B_BF + kt % TC_NB));
+                    if (CS == 1)
+                        bulk_g2s(b_ring + off, src + (size_t)ks * bytes, bytes, bar(B_BF + kt % TC_NB));
+                    else if (leader)
+                        bulk_g2s_multicast(b_ring + off, src + (size_t)ks * bytes, bytes, bar(B_BF + kt % TC_NB),
+                                           cmask);
                 }
                 if (!ok) break;
             }
@@ -457,10 +553,10 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
         // The whole warp walks the loop (the MMAs need a converged warp for
         // elect.sync); every lane takes the same branches.
         uint32_t kt = 0, ut = 0;
-        TcTile tl_next = tile_at(blockIdx.x);
-        for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x, ut++) {
+        TcTile tl_next = tile_at(cid);
+        for (int ug = cid; ug < n_groups && !*abort_flag; ug += ncl, ut++) {
             const TcTile tl = tl_next;
-            tl_next = tile_at(u + (int)gridDim.x);
+            tl_next = tile_at(ug + ncl);
             const int nb = PH == 0 ? tl.nx : tl.nh;
             if (nb < 16 || nb % 16 || nb > C::BMAX) {
                 if (lane == 0) set_device_error(a.err, K3MOE_EINVAL);
@@ -487,6 +583,7 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
                 mma_kstep<C::NA, KD>(td, alo, blo, idesc, ks != 0);
                 mma_commit(bar(B_AE + sa));
                 mma_commit(bar(B_BE + sb));
+                if (CS > 1) mma_commit_multicast(bar(B_BEC + sb), 1);  // the leader's slot barrier
             }
             if (!ok) break;
             mma_commit(bar(B_ACCF + buf));
@@ -507,7 +604,6 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
         const uint32_t lut = sbase + (uint32_t)C::LUT_OFF;
         uint32_t it = 0, kt = 0;
         const int g_per_ss = TC_SS / 32;  // 8 scale bytes per row per staging step
-        const int G = gridDim.x;
         auto scale_plane = [&](int e) -> const uint8_t * {
             return PH == 1 ? a.table[e].ds : (mat == 0 ? a.table[e].gs : a.table[e].us);
         };
@@ -515,28 +611,28 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
         // the current unit (its expert at the first staging step, the plane at
         // the middle one, the first 8 bytes at the last one), so no load in the
         // loop waits on another.
-        int u = blockIdx.x;
+        int ug = cid;
         const uint8_t *scl = nullptr, *nplane = nullptr, *nscl = nullptr;
         int nexp = 0;
-        if (u < n_units)
-            scl = scale_plane(a.tiles[u / nrb].expert) + (size_t)((u % nrb) * TC_M + r) * (K / 32);
+        if (ug < n_groups)
+            scl = scale_plane(a.tiles[ug / gpt].expert) + (size_t)((unit_of(ug) % nrb) * TC_M + r) * (K / 32);
         uint2 sc_next = scl ? __ldg((const uint2 *)scl) : make_uint2(0, 0);
         int ss = 0;
-        while (u < n_units && !*abort_flag) {
-            const int un = u + G;
-            if (ss == 0 && un < n_units) nexp = a.tiles[un / nrb].expert;
-            if (ss == nss / 2 && un < n_units) nplane = scale_plane(nexp);
+        while (ug < n_groups && !*abort_flag) {
+            const int ugn = ug + ncl;
+            if (ss == 0 && ugn < n_groups) nexp = a.tiles[ugn / gpt].expert;
+            if (ss == nss / 2 && ugn < n_groups) nplane = scale_plane(nexp);
             const uint2 sc = sc_next;
             if (ss + 1 < nss) {
                 sc_next = __ldg((const uint2 *)(scl + (ss + 1) * g_per_ss));
-            } else if (un < n_units) {
-                nscl = nplane + (size_t)((un % nrb) * TC_M + r) * (K / 32);
+            } else if (ugn < n_groups) {
+                nscl = nplane + (size_t)((unit_of(ugn) % nrb) * TC_M + r) * (K / 32);
                 sc_next = __ldg((const uint2 *)nscl);
             }
-            int ss2 = ss + 1, u2 = u;
+            int ss2 = ss + 1, ug2 = ug;
             if (ss2 == nss) {
                 ss2 = 0;
-                u2 = un;
+                ug2 = ugn;
             }
             const int pslot = it % C::SP;
             if (!__all_sync(0xffffffffu, tc_wait(bar(B_PKF + pslot), (it / C::SP) & 1, a.err, abort_flag))) break;
@@ -605,8 +701,8 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_PKE + pslot));
             it++;
-            if (u2 != u) scl = nscl;
-            u = u2;
+            if (ug2 != ug) scl = nscl;
+            ug = ug2;
             ss = ss2;
         }
     } else {
@@ -614,10 +710,11 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
         const int q = warp & 3;       // TMEM lane quadrant of this warp
         const int r = q * 32 + lane;  // weight row within the unit
         uint32_t ut = 0;
-        TcTile tl_next = tile_at(blockIdx.x);
-        for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x, ut++) {
+        TcTile tl_next = tile_at(cid);
+        for (int ug = cid; ug < n_groups && !*abort_flag; ug += ncl, ut++) {
+            const int u = unit_of(ug);
             const TcTile tl = tl_next;
-            tl_next = tile_at(u + (int)gridDim.x);
+            tl_next = tile_at(ug + ncl);
             const int buf = ut & 1;
             if (!__all_sync(0xffffffffu, tc_wait(bar(B_ACCF + buf), (ut / 2) & 1, a.err, abort_flag))) break;
             tc_fence_after();
@@ -627,7 +724,7 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
             // token pieces: columns c P + j, piece c weighing rho^c (rho = 1 for
             // bf16 hi/lo, 1/16 for e4m3 pieces, which also carry the token's
             // scale); summed from the smallest piece up
-            const int np = PH == 0 ? (tl.split > 1 ? tl.split : 1) : 2;
+            const int np = tl.split > 1 ? tl.split : 1;
             const float rho = KD ? 0.0625f : 1.0f;
             for (int j0 = 0; j0 < tl.n; j0 += 8) {
                 if (PH == 0) {
@@ -655,6 +752,22 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
                         }
                     }
                     const int col = rb * TC_M + r;  // index into f
+                    if (a.hf) {
+                        // e4m3 down: h in fp32 and its per-pair maximum magnitude
+#pragma unroll
+                        for (int jj = 0; jj < 8; jj++) {
+                            const int j = j0 + jj;
+                            if (j < tl.n) {
+                                const float h = silu(g[jj]) * v[jj];
+                                a.hf[(size_t)(tl.pair_begin + j) * a.f + col] = h;
+                                float m = fabsf(h);
+#pragma unroll
+                                for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                                if (lane == 0) atomicMax(a.hmax + tl.pair_begin + j, __float_as_uint(m));
+                            }
+                        }
+                        continue;
+                    }
                     const int s = col >> 6, c = (col & 63) >> 3, byte = (col & 7) * 2;
                     uint8_t *hb = a.Hg + (size_t)tl.hrow0 * a.f * 2 + (size_t)s * tl.nh * 128 + byte;
 #pragma unroll
@@ -670,19 +783,30 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
                         }
                     }
                 } else {
-                    float yh[8], yl[8];
-                    tmem_ld8(tbase + j0, yh);
-                    tmem_ld8(tbase + P + j0, yl);
+                    // h pieces: bf16 hi, lo (rho = 1) or four e4m3 pieces (rho =
+                    // 1/16, times the pair's h scale)
+                    const int nph = KD ? 4 : 2;
+                    float y[8], t[8];
+                    tmem_ld8(tbase + (nph - 1) * P + j0, y);
                     tmem_wait_ld();
-                    const int row = rb * TC_M + r;  // index into d
+                    for (int c = nph - 2; c >= 0; c--) {
+                        tmem_ld8(tbase + c * P + j0, t);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int jj = 0; jj < 8; jj++) {
-                        const int j = j0 + jj;
-                        if (j < tl.n) {
-                            const int pair = a.perm[tl.pair_begin + j];
-                            const float w = a.wsel[pair];
-                            atomicAdd(a.out + (size_t)(pair / a.k) * a.d + row, w * (yh[jj] + yl[jj]));
-                        }
+                        for (int i = 0; i < 8; i++) y[i] = fmaf(y[i], rho, t[i]);
+                    }
+                    // lane l of group q (rows 8q..8q+7 of this warp's 32) now takes
+                    // token j0 + (l & 7) of the eight and adds its eight rows with
+                    // two vector reductions instead of eight scalar atomics
+                    transpose8(y, lane);
+                    const int j = j0 + (lane & 7);
+                    if (j < tl.n) {
+                        const int pair = a.perm[tl.pair_begin + j];
+                        float w = a.wsel[pair];
+                        if (KD == 1) w *= h_scale(a.hmax[tl.pair_begin + j]);
+                        float *o = a.out + (size_t)(pair / a.k) * a.d + rb * TC_M + q * 32 + (lane & ~7);
+                        red_add_v4(o, w * y[0], w * y[1], w * y[2], w * y[3]);
+                        red_add_v4(o + 4, w * y[4], w * y[5], w * y[6], w * y[7]);
                     }
                 }
             }
@@ -699,6 +823,7 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_TMEM_COLS)
                      : "memory");
     }
+    cluster_sync();  // no CTA leaves while a copy or commit of another may still reach it
 }
 
 // ---------------------------------------------------------------- planning
@@ -706,7 +831,7 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
 // Tiles of at most tn tokens per expert, with the row offsets of each tile in
 // the token array (nx rows) and in the h array (nh rows).  One CTA.
 __global__ void __launch_bounds__(1024) k3_tc_plan(const int32_t *__restrict__ offsets, int E, int tn,
-                                                   int np, int max_tiles, TcTile *tiles,
+                                                   int np, int nph, int max_tiles, TcTile *tiles,
                                                    int32_t *n_tiles, int *err)
 {
     __shared__ int wsum[3][32];
@@ -722,7 +847,7 @@ __global__ void __launch_bounds__(1024) k3_tc_plan(const int32_t *__restrict__ o
         for (int j = 0; j < nt; j++) {
             const int n = min(tn, c - j * tn);
             rx += tile_nx(n, np);
-            rh += tile_nh(n);
+            rh += tile_nh(n, nph);
         }
         int v[3] = {nt, rx, rh}, inc[3];
 #pragma unroll
@@ -753,7 +878,7 @@ __global__ void __launch_bounds__(1024) k3_tc_plan(const int32_t *__restrict__ o
         int hr = base[2] + wsum[2][warp] + inc[2] - v[2];
         for (int j = 0; j < nt; j++, t++) {
             const int n = min(tn, c - j * tn);
-            const int nx = tile_nx(n, np), nh = tile_nh(n);
+            const int nx = tile_nx(n, np), nh = tile_nh(n, nph);
             if (t < max_tiles) {
                 TcTile tl;
                 tl.expert = e;
@@ -876,6 +1001,53 @@ __global__ void __launch_bounds__(256) k3_tc_gather(const XT *__restrict__ X, co
     }
 }
 
+// h rows of every tile as four e4m3 pieces (rows c P + j, k-step-major,
+// pre-swizzled like the token rows), from h in fp32 and the pair's scale.
+__global__ void __launch_bounds__(256) k3_tc_hpieces(const float *__restrict__ hf, const unsigned *__restrict__ hmax,
+                                                    int f, const TcTile *__restrict__ tiles, const int32_t *n_tiles,
+                                                    uint8_t *Hg)
+{
+    const int nt = *n_tiles;
+    const int cpr = f / 16;  // 16-element chunks per row
+    for (int t = blockIdx.x; t < nt; t += gridDim.x) {
+        const TcTile tl = tiles[t];
+        const int P = tile_p(tl.n);
+        uint8_t *base = Hg + (size_t)tl.hrow0 * f;
+        for (int idx = threadIdx.x; idx < tl.n * cpr; idx += blockDim.x) {
+            const int j = idx / cpr, ch = idx - j * cpr;
+            const int s = ch >> 3, c = ch & 7;
+            const float inv0 = 1.0f / h_scale(hmax[tl.pair_begin + j]);  // a power of two: exact
+            const float4 *src = (const float4 *)(hf + (size_t)(tl.pair_begin + j) * f + ch * 16);
+            float r[16];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const float4 v = src[q];
+                r[4 * q] = v.x * inv0;
+                r[4 * q + 1] = v.y * inv0;
+                r[4 * q + 2] = v.z * inv0;
+                r[4 * q + 3] = v.w * inv0;
+            }
+#pragma unroll
+            for (int piece = 0; piece < 4; piece++) {
+                uint32_t b[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                for (int i = 0; i < 16; i += 2) {
+                    const uint32_t q2 =
+                        __nv_cvt_float2_to_fp8x2(make_float2(r[i], r[i + 1]), __NV_SATFINITE, __NV_E4M3);
+                    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)q2, __NV_E4M3);
+                    const float2 back = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+                    r[i] = (r[i] - back.x) * 16.0f;
+                    r[i + 1] = (r[i + 1] - back.y) * 16.0f;
+                    b[i >> 2] |= (q2 & 0xffffu) << (8 * (i & 3));
+                }
+                const int row = piece * P + j;
+                *(uint4 *)(base + (size_t)s * tl.nh * 128 + row * 128 + ((c ^ (row & 7)) << 4)) =
+                    make_uint4(b[0], b[1], b[2], b[3]);
+            }
+        }
+    }
+}
+
 // s_0 of every token for e4m3 pieces: 2^(x - 8) where the token's largest
 // magnitude is m 2^x, m in [0.5, 1), so that |x| / s_0 < 256 < 448 (the e4m3
 // maximum); 1 for an all-zero token.  One warp per token.
@@ -898,21 +1070,17 @@ __global__ void __launch_bounds__(256) k3_tc_token_scale(const XT *__restrict__ 
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-    if (lane == 0) {
-        int ex = 0;
-        frexpf(m, &ex);
-        tscale[t] = m > 0.f ? ldexpf(1.f, ex - 8) : 1.f;
-    }
+    if (lane == 0) tscale[t] = piece_scale(m);
 }
 
-// Counts the gate and up scale bytes of every expert outside [119, 133] and
+// Counts the scale bytes of every expert (gate, up, down) outside [119, 133] and
 // other than 255 (the bytes the e4m3 decode cannot represent exactly).
 __global__ void __launch_bounds__(256) k3_tc_scale_range(const DevExpert *__restrict__ table, int E, int d, int f,
                                                         unsigned *bad)
 {
     const int e = blockIdx.x, m = blockIdx.y;
-    const uint8_t *p = m == 0 ? table[e].gs : table[e].us;
-    const size_t n = (size_t)f * (d / 32);
+    const uint8_t *p = m == 0 ? table[e].gs : m == 1 ? table[e].us : table[e].ds;
+    const size_t n = m < 2 ? (size_t)f * (d / 32) : (size_t)d * (f / 32);
     unsigned cnt = 0;
     for (size_t i = threadIdx.x * 16; i < n; i += blockDim.x * 16) {
         const uint4 q = *(const uint4 *)(p + i);
@@ -946,8 +1114,8 @@ size_t tc_hg_bytes(int npairs, int E, int f) { return 2 * ((size_t)npairs + 7 * 
 size_t tc_tile_bytes() { return sizeof(TcTile); }
 size_t tc_map_bytes() { return sizeof(CUtensorMap); }
 
-// 1 when every gate and up scale byte of the E experts is in [119, 133] or
-// 255 (the e4m3 gate/up path is exact), 0 otherwise, negative on error.
+// 1 when every scale byte of the E experts is in [119, 133] or 255 (the e4m3
+// decode is exact), 0 otherwise, negative on error.
 int tc_e4m3_eligible(const DevExpert *dev_table, int E, int d, int f, cudaStream_t s)
 {
     unsigned *bad = nullptr;
@@ -959,7 +1127,7 @@ int tc_e4m3_eligible(const DevExpert *dev_table, int E, int d, int f, cudaStream
     int rc = K3MOE_OK;
     if (cudaMemsetAsync(bad, 0, sizeof(unsigned), s) != cudaSuccess) rc = K3MOE_ECUDA;
     if (rc == K3MOE_OK) {
-        k3_tc_scale_range<<<dim3(E, 2), 256, 0, s>>>(dev_table, E, d, f, bad);
+        k3_tc_scale_range<<<dim3(E, 3), 256, 0, s>>>(dev_table, E, d, f, bad);
         if (cudaGetLastError() != cudaSuccess ||
             cudaMemcpyAsync(&h, bad, sizeof(unsigned), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
             cudaStreamSynchronize(s) != cudaSuccess)
@@ -1015,31 +1183,77 @@ int tc_make_maps(const DevExpert *host_table, int E, int d, int f, void *dev_map
     return rc;
 }
 
+// Launches one phase on persistent CTAs in clusters of CS (4 when the row
+// blocks divide by 4, else 2, else 1), as many clusters as fit at once.
 template <int PH, int KD>
 static int launch_expert(const TcArgs &a, cudaStream_t s)
 {
     using C = TcCfg<PH, KD>;
     static bool ready = false;
+    static int grid[5] = {0, 0, 0, 0, 0};
     if (!ready) {
         if (cudaFuncSetAttribute(k3_tc_expert<PH, KD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
             cudaSuccess)
             return K3MOE_ECUDA;
+        for (int cs : {1, 2, 4}) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = cs;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.gridDim = dim3(num_sms() / cs * cs);
+            cfg.blockDim = dim3(C::THREADS);
+            cfg.dynamicSmemBytes = C::SMEM;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, k3_tc_expert<PH, KD>, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                n = 0;
+            }
+            grid[cs] = n * cs;
+        }
+        if (grid[1] <= 0) grid[1] = num_sms();
         ready = true;
     }
-    k3_tc_expert<PH, KD><<<num_sms(), C::THREADS, C::SMEM, s>>>(a);
-    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
+    // the cluster size that keeps the most CTAs resident (clusters must fit
+    // in a GPC, so larger ones can leave SMs idle); larger on a tie
+    const int nrb = (PH == 0 ? a.f : a.d) / TC_M;
+    int cs = 1;
+    for (int c : {2, 4})
+        if (nrb % c == 0 && grid[c] >= grid[cs]) cs = c;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = cs;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.gridDim = dim3(grid[cs]);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k3_tc_expert<PH, KD>, a) != cudaSuccess) {
+        cudaGetLastError();
+        return K3MOE_ECUDA;
+    }
+    return K3MOE_OK;
 }
 
 // Plan, token rows and the gate/up + SwiGLU phase (h into Hg); kd = 1 runs
 // gate/up on e4m3 operands (only for layers whose scale bytes allow it).
 int launch_tc_gateup(const void *X, int xdt, int T, int kd, int k, int E, int d, int f, const DevExpert *table,
                      const void *maps, const int32_t *offsets, const int32_t *perm, void *tiles, int32_t *n_tiles,
-                     int max_tiles, float *tscale, uint8_t *Xg, uint8_t *Hg, int *err, cudaStream_t s)
+                     int max_tiles, float *tscale, uint8_t *Xg, uint8_t *Hg, float *hf, unsigned *hmax, int *err,
+                     cudaStream_t s)
 {
     const int tn = tc_tile_tokens(xdt, kd), np = tc_pieces(xdt, kd);
-    k3_tc_plan<<<1, 1024, 0, s>>>(offsets, E, tn, np, max_tiles, (TcTile *)tiles, n_tiles, err);
+    k3_tc_plan<<<1, 1024, 0, s>>>(offsets, E, tn, np, kd ? 4 : 2, max_tiles, (TcTile *)tiles, n_tiles, err);
     if (cudaGetLastError() != cudaSuccess) return K3MOE_ECUDA;
     if (kd) {
+        if (cudaMemsetAsync(hmax, 0, sizeof(unsigned) * (size_t)T * k, s) != cudaSuccess) return K3MOE_ECUDA;
         if (xdt == K3MOE_BF16)
             k3_tc_token_scale<uint16_t><<<(T + 7) / 8, 256, 0, s>>>((const uint16_t *)X, T, d, tscale);
         else
@@ -1069,6 +1283,8 @@ int launch_tc_gateup(const void *X, int xdt, int T, int kd, int k, int E, int d,
     a.Hg = Hg;
     a.perm = perm;
     a.tscale = tscale;
+    a.hf = kd ? hf : nullptr;
+    a.hmax = hmax;
     a.k = k;
     a.d = d;
     a.f = f;
@@ -1077,10 +1293,14 @@ int launch_tc_gateup(const void *X, int xdt, int T, int kd, int k, int E, int d,
 }
 
 // Down phase and the weighted combine: out = sum_j w_j y_j (out is zeroed first).
-int launch_tc_down(int T, int k, int d, int f, const DevExpert *table, const void *maps, const int32_t *perm,
-                   const float *wsel, const void *tiles, const int32_t *n_tiles, const uint8_t *Hg, float *out,
-                   int *err, cudaStream_t s)
+int launch_tc_down(int T, int kd, int k, int d, int f, const DevExpert *table, const void *maps, const int32_t *perm,
+                   const float *wsel, const void *tiles, const int32_t *n_tiles, uint8_t *Hg, const float *hf,
+                   unsigned *hmax, float *out, int *err, cudaStream_t s)
 {
+    if (kd) {
+        k3_tc_hpieces<<<2 * num_sms(), 256, 0, s>>>(hf, hmax, f, (const TcTile *)tiles, n_tiles, Hg);
+        if (cudaGetLastError() != cudaSuccess) return K3MOE_ECUDA;
+    }
     if (cudaMemsetAsync(out, 0, sizeof(float) * (size_t)T * d, s) != cudaSuccess) return K3MOE_ECUDA;
     TcArgs a = {};
     a.tiles = (const TcTile *)tiles;
@@ -1091,11 +1311,12 @@ int launch_tc_down(int T, int k, int d, int f, const DevExpert *table, const voi
     a.out = out;
     a.perm = perm;
     a.wsel = wsel;
+    a.hmax = hmax;
     a.k = k;
     a.d = d;
     a.f = f;
     a.err = err;
-    return launch_expert<1, 0>(a, s);
+    return kd ? launch_expert<1, 1>(a, s) : launch_expert<1, 0>(a, s);
 }
 
 }  // namespace k3
