@@ -246,18 +246,46 @@ __global__ void __launch_bounds__(1024) k3_group(const int32_t *__restrict__ ids
     __syncthreads();
     for (int p = threadIdx.x; p < npairs; p += blockDim.x) atomicAdd(&cnt[ids[p]], 1);
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0, it = 0;
-        for (int e = 0; e < E; e++) {
-            off[e] = run;
-            for (int b = 0; b < cnt[e]; b += nt) {
-                items[it] = make_int4(e, run + b, min(nt, cnt[e] - b), 0);
-                it++;
+    // offsets and work items by a block-wide exclusive scan over experts
+    // (one thread per expert; the layer has at most blockDim experts)
+    {
+        __shared__ int wsum[2][32];
+        const int e = threadIdx.x, lane = e & 31, warp = e >> 5, nw = blockDim.x >> 5;
+        const int c = e < E ? cnt[e] : 0, ni = (c + nt - 1) / nt;
+        int v[2] = {c, ni}, inc[2];
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            int x = v[i];
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
             }
-            run += cnt[e];
+            inc[i] = x;
+            if (lane == 31) wsum[i][warp] = x;
         }
-        off[E] = run;
-        *n_items = it;
+        __syncthreads();
+        if (warp == 0) {
+#pragma unroll
+            for (int i = 0; i < 2; i++) {
+                int x = lane < nw ? wsum[i][lane] : 0;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += y;
+                }
+                if (lane < nw) wsum[i][lane] = x - wsum[i][lane];
+            }
+        }
+        __syncthreads();
+        const int first = wsum[0][warp] + inc[0] - v[0];   // exclusive prefix of the counts
+        const int item0 = wsum[1][warp] + inc[1] - v[1];   // exclusive prefix of the item counts
+        if (e < E) {
+            off[e] = first;
+            for (int b = 0; b < ni; b++) items[item0 + b] = make_int4(e, first + b * nt, min(nt, c - b * nt), 0);
+        }
+        if (e == blockDim.x - 1) {
+            off[E] = first + c;
+            *n_items = item0 + ni;
+        }
     }
     __syncthreads();
     for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = off[e];
@@ -296,10 +324,20 @@ int route_multi_nsplit(int T, int E, int d)
     return (int)want;
 }
 
+int launch_router_tc(const uint16_t *X, int T, const uint16_t *Wr, int E, int d, float *logits, int *err,
+                     cudaStream_t s);
+int *device_error_word();
+
 int launch_route_multi(const void *X, int xdt, int T, const uint16_t *Wr, int E, int d,
                        float *part, int nsplit, float *logits, const float *bias, int k,
                        int32_t *ids, float *w, cudaStream_t s)
 {
+    // bf16 tokens in numbers: the logits as a tensor-core GEMM
+    if (xdt == K3MOE_BF16 && T >= 128 && d % 64 == 0 &&
+        launch_router_tc((const uint16_t *)X, T, Wr, E, d, part, device_error_word(), s) == K3MOE_OK) {
+        k3_topk_multi<<<(T + 7) / 8, 256, 0, s>>>(part, 1, T, E, bias, k, logits, ids, w);
+        return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
+    }
     int klen = (d + nsplit - 1) / nsplit;
     klen = (klen + RT_K - 1) / RT_K * RT_K;
     const int ns = (d + klen - 1) / klen;

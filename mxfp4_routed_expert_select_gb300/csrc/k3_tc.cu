@@ -924,6 +924,10 @@ __global__ void __launch_bounds__(256) k3_tc_gather(const XT *__restrict__ X, co
                                                     const int32_t *n_tiles, const float *__restrict__ tscale,
                                                     uint8_t *Xg)
 {
+    // One thread per (token of the tile, 16-byte output chunk): the token's
+    // elements are read once and all its pieces written.  Rows past n (the
+    // padding of each piece) are left as they are: they only feed MMA
+    // columns that no epilogue reads.
     const int nt = *n_tiles;
     const int EPC = KD ? 16 : 8;  // elements per 16-byte chunk
     const int cpr = d / EPC;      // chunks per row
@@ -931,72 +935,71 @@ __global__ void __launch_bounds__(256) k3_tc_gather(const XT *__restrict__ X, co
     for (int t = blockIdx.x; t < nt; t += gridDim.x) {
         const TcTile tl = tiles[t];
         const int P = tile_p(tl.n);
-        const int np = tl.split;
+        const int np = tl.split > 1 ? tl.split : 1;
         uint8_t *base = Xg + (size_t)tl.xrow0 * rowb;
-        const int total = tl.nx * cpr;
-        for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
-            const int row = idx / cpr, ch = idx - row * cpr;
+        for (int idx = threadIdx.x; idx < tl.n * cpr; idx += blockDim.x) {
+            const int j = idx / cpr, ch = idx - j * cpr;
             const int s = ch >> 3, c = ch & 7;
-            int j = row, piece = 0;
-            if (np > 1) {
-                piece = row / P;
-                j = row - piece * P;
-            }
-            uint4 o = make_uint4(0, 0, 0, 0);
-            if (j < tl.n && piece < (np > 1 ? np : 1)) {
-                const int tok = perm[tl.pair_begin + j] / k;
-                float v[16];
-                if constexpr (sizeof(XT) == 2) {
-                    const uint4 *src = (const uint4 *)((const uint16_t *)X + (size_t)tok * d + ch * EPC);
+            const int tok = perm[tl.pair_begin + j] / k;
+            float v[16];
+            if constexpr (sizeof(XT) == 2) {
+                const uint4 *src = (const uint4 *)((const uint16_t *)X + (size_t)tok * d + ch * EPC);
 #pragma unroll
-                    for (int q = 0; q < EPC / 8; q++) {
-                        const uint4 u = src[q];
-                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                for (int q = 0; q < EPC / 8; q++) {
+                    const uint4 u = src[q];
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                        for (int i = 0; i < 4; i++) {
-                            v[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
-                            v[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-                        }
-                    }
-                } else {
-                    const float4 *src = (const float4 *)((const float *)X + (size_t)tok * d + ch * EPC);
-#pragma unroll
-                    for (int q = 0; q < EPC / 4; q++) {
-                        const float4 f4 = src[q];
-                        v[4 * q] = f4.x;
-                        v[4 * q + 1] = f4.y;
-                        v[4 * q + 2] = f4.z;
-                        v[4 * q + 3] = f4.w;
+                    for (int i = 0; i < 4; i++) {
+                        v[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
+                        v[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
                     }
                 }
-                if constexpr (KD == 0) {
-                    uint32_t h[8];
+            } else {
+                const float4 *src = (const float4 *)((const float *)X + (size_t)tok * d + ch * EPC);
 #pragma unroll
-                    for (int i = 0; i < 8; i++) {
-                        const uint32_t hi = bf16_rn_bits(v[i]);
-                        h[i] = piece ? bf16_rn_bits(v[i] - __uint_as_float(hi << 16)) : hi;
-                    }
-                    o = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
-                } else {
-                    const float inv0 = 1.0f / tscale[tok];  // a power of two: exact
+                for (int q = 0; q < EPC / 4; q++) {
+                    const float4 f4 = src[q];
+                    v[4 * q] = f4.x;
+                    v[4 * q + 1] = f4.y;
+                    v[4 * q + 2] = f4.z;
+                    v[4 * q + 3] = f4.w;
+                }
+            }
+            auto put = [&](int piece, uint4 o) {
+                const int row = piece * P + j;
+                *(uint4 *)(base + (size_t)s * tl.nx * 128 + row * 128 + ((c ^ (row & 7)) << 4)) = o;
+            };
+            if constexpr (KD == 0) {
+                uint32_t hi[8], lo[8];
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    hi[i] = bf16_rn_bits(v[i]);
+                    lo[i] = bf16_rn_bits(v[i] - __uint_as_float(hi[i] << 16));
+                }
+                put(0, make_uint4(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16), hi[4] | (hi[5] << 16),
+                                  hi[6] | (hi[7] << 16)));
+                if (np > 1)
+                    put(1, make_uint4(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16), lo[4] | (lo[5] << 16),
+                                      lo[6] | (lo[7] << 16)));
+            } else {
+                const float inv0 = 1.0f / tscale[tok];  // a power of two: exact
+#pragma unroll
+                for (int i = 0; i < 16; i++) v[i] *= inv0;  // in units of s_0
+                for (int piece = 0; piece < np; piece++) {
                     uint32_t b[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
                     for (int i = 0; i < 16; i += 2) {
-                        float r0 = v[i] * inv0, r1 = v[i + 1] * inv0;  // in units of s_0
-                        uint32_t q2 = 0;
-                        for (int cc = 0; cc <= piece; cc++) {
-                            q2 = __nv_cvt_float2_to_fp8x2(make_float2(r0, r1), __NV_SATFINITE, __NV_E4M3);
-                            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)q2, __NV_E4M3);
-                            const float2 back = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
-                            r0 = (r0 - back.x) * 16.0f;
-                            r1 = (r1 - back.y) * 16.0f;
-                        }
+                        const uint32_t q2 =
+                            __nv_cvt_float2_to_fp8x2(make_float2(v[i], v[i + 1]), __NV_SATFINITE, __NV_E4M3);
+                        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)q2, __NV_E4M3);
+                        const float2 back = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+                        v[i] = (v[i] - back.x) * 16.0f;
+                        v[i + 1] = (v[i + 1] - back.y) * 16.0f;
                         b[i >> 2] |= (q2 & 0xffffu) << (8 * (i & 3));  // elements i, i + 1 -> bytes i, i + 1
                     }
-                    o = make_uint4(b[0], b[1], b[2], b[3]);
+                    put(piece, make_uint4(b[0], b[1], b[2], b[3]));
                 }
             }
-            *(uint4 *)(base + (size_t)s * tl.nx * 128 + row * 128 + ((c ^ (row & 7)) << 4)) = o;
         }
     }
 }
@@ -1094,6 +1097,113 @@ __global__ void __launch_bounds__(256) k3_tc_scale_range(const DevExpert *__rest
     if (cnt) atomicAdd(bad, cnt);
 }
 
+// ------------------------------------------------------------------ router
+
+// logits[t][e] = sum_i X[t][i] W_r[e][i] for bf16 tokens on the tensor cores:
+// one CTA per (128 experts x 256 tokens) tile, both operands by TMA (128-byte
+// swizzle, out-of-range rows read as zeros), fp32 accumulation in TMEM.
+// bf16 x bf16 products are exact in fp32.  Warp 0: TMA; warp 1: MMA; warps
+// 2-5: epilogue.
+constexpr int RT_S = 4, RT_N = 256, RT_A = TC_M * 128, RT_B = RT_N * 128;
+constexpr int RT_SMEM = RT_S * (RT_A + RT_B) + 256 + 1024;
+
+__global__ void __launch_bounds__(192, 1) k3_router_tc(const __grid_constant__ CUtensorMap wmap,
+                                                      const __grid_constant__ CUtensorMap xmap, int T, int E, int d,
+                                                      float *logits, int *err)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sbase = smem_addr(sm);
+    uint64_t *bars = (uint64_t *)(sm + RT_S * (RT_A + RT_B));
+    const int B_F = 0, B_E = RT_S, B_ACC = 2 * RT_S, B_FIN = 2 * RT_S + 1;
+    uint32_t *tmem_slot = (uint32_t *)(bars + B_FIN + 1);
+    volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+    auto bar = [&](int i) { return smem_addr(bars + i); };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * TC_M, n0 = blockIdx.y * RT_N, nks = d / 64;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < RT_S; i++) {
+            mbar_init(bar(B_F + i), 1);
+            mbar_init(bar(B_E + i), 1);
+        }
+        mbar_init(bar(B_ACC), 1);
+        mbar_init(bar(B_FIN), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(RT_N)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *(volatile uint32_t *)tmem_slot;
+    auto stage = [&](int s) { return sbase + (uint32_t)(s * (RT_A + RT_B)); };
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int ks = 0; ks < nks && !*abort_flag; ks++, issued++) {
+                const int s = ks % RT_S;
+                if (ks >= RT_S && !tc_wait(bar(B_E + s), ((ks / RT_S) - 1) & 1, err, abort_flag)) break;
+                mbar_arrive_expect_tx(bar(B_F + s), RT_A + RT_B);
+                asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+                             "[%1, {%2, %3}], [%4];" ::"r"(stage(s)),
+                             "l"((uint64_t)&wmap), "r"(ks * 64), "r"(m0), "r"(bar(B_F + s))
+                             : "memory");
+                asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+                             "[%1, {%2, %3}], [%4];" ::"r"(stage(s) + RT_A),
+                             "l"((uint64_t)&xmap), "r"(ks * 64), "r"(n0), "r"(bar(B_F + s))
+                             : "memory");
+            }
+            for (int q = issued > RT_S ? issued - RT_S : 0; q < issued; q++)  // drain
+                mbar_wait(bar(B_F + q % RT_S), (q / RT_S) & 1, err);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        const uint32_t idesc = bf16_idesc(RT_N);
+        bool ok = true;
+        for (int ks = 0; ks < nks && !*abort_flag; ks++) {
+            const int s = ks % RT_S;
+            if (!__all_sync(0xffffffffu, tc_wait(bar(B_F + s), (ks / RT_S) & 1, err, abort_flag))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            mma_kstep<1, 0>(tmem, sw128_lo(stage(s)), sw128_lo(stage(s) + RT_A), idesc, ks != 0);
+            mma_commit(bar(B_E + s));
+        }
+        if (ok) mma_commit(bar(B_ACC));
+        mma_commit(bar(B_FIN));
+        mbar_wait(bar(B_FIN), 0, err);
+        __syncwarp();
+    } else {
+        const int q = warp & 3;
+        if (__all_sync(0xffffffffu, tc_wait(bar(B_ACC), 0, err, abort_flag))) {
+            tc_fence_after();
+            const int e = m0 + q * 32 + lane;
+            for (int c0 = 0; c0 < RT_N; c0 += 8) {
+                float v[8];
+                tmem_ld8(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    const int t = n0 + c0 + i;
+                    if (e < E && t < T) logits[(size_t)t * E + e] = v[i];
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(RT_N) : "memory");
+    }
+}
+
 // --------------------------------------------------------------- launchers
 
 int num_sms();
@@ -1181,6 +1291,52 @@ int tc_make_maps(const DevExpert *host_table, int E, int d, int f, void *dev_map
     }
     free(maps);
     return rc;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    }
+    return encode;
+}
+
+// Router logits of bf16 tokens on the tensor cores (see k3_router_tc):
+// logits [T x E] fp32.  Needs d % 64 == 0.
+int launch_router_tc(const uint16_t *X, int T, const uint16_t *Wr, int E, int d, float *logits, int *err,
+                     cudaStream_t s)
+{
+    auto encode = tensor_map_encoder();
+    if (!encode || d % 64) return K3MOE_ECUDA;
+    CUtensorMap wmap, xmap;
+    const cuuint64_t wdims[2] = {(cuuint64_t)d, (cuuint64_t)E}, xdims[2] = {(cuuint64_t)d, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+    const cuuint32_t wbox[2] = {64, (cuuint32_t)TC_M}, xbox[2] = {64, (cuuint32_t)RT_N}, es[2] = {1, 1};
+    if (encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)Wr, wdims, strides, wbox, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void *)X, xdims, strides, xbox, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return K3MOE_EINVAL;
+    static bool ready = false;
+    if (!ready) {
+        if (cudaFuncSetAttribute(k3_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, RT_SMEM) != cudaSuccess)
+            return K3MOE_ECUDA;
+        ready = true;
+    }
+    const dim3 grid((E + TC_M - 1) / TC_M, (T + RT_N - 1) / RT_N);
+    k3_router_tc<<<grid, 192, RT_SMEM, s>>>(wmap, xmap, T, E, d, logits, err);
+    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
 }
 
 // Launches one phase on persistent CTAs in clusters of CS (4 when the row
