@@ -669,8 +669,8 @@ def run_batched(args, rank, world, dev_index, T, bf16, use_bias):
                        "l2": "inputs larger than L2: %d token batches, %d router copies, %.0f distinct "
                              "experts (%.2f GB) per batch" % (NB, n_r, Umean, w_bytes / 1e9)}, clocks)
     line.update({
-        "roofline": _roofline("k3_tc_expert<0> (tcgen05 gate/up + SwiGLU over the batch's experts, "
-                              "with the token gather and tile plan)",
+        "roofline": _roofline("k3_tc_expert<0,1> (tcgen05 kind::f8f6f4 gate/up + SwiGLU over the batch's "
+                              "experts; the timed span also holds grouping, tile plan, token scales and gather)",
                               gu_bytes, statistics.mean(gu_ms)),
         "step_bytes": {"distinct_experts": Umean, "bytes": int(step_bytes),
                        "gbs": round(step_bytes / (per * 1e-3) / 1e9, 1)},
@@ -678,7 +678,9 @@ def run_batched(args, rank, world, dev_index, T, bf16, use_bias):
         "kernels_ms": {"route_topk": round(statistics.mean(r_ms), 4),
                        "group_gate_up_swiglu": round(statistics.mean(gu_ms), 4),
                        "down_combine": round(statistics.mean(dn_ms), 4)},
-        "e2e": e2e, "gpu_launches": 6 * steps})
+        # router GEMM + top-k, grouping, tile plan, token scales, token gather,
+        # gate/up, h pieces, down + combine
+        "e2e": e2e, "gpu_launches": 9 * steps})
     for l in layers:
         l.close()
     return line
