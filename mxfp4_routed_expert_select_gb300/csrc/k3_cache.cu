@@ -4,8 +4,10 @@
 // explainer, "The cache the project exists for" and "The bug the code
 // confesses to"; "How kimi-k3-in-c Runs...", "The LRU cache"), rebuilt for
 // one GPU: the arena is one cudaMalloc of `slots` expert blobs in HBM; a miss
-// is one cudaMemcpyAsync of the expert's blob on a side stream; the caller's
-// compute stream waits on per-slot events, so the host never blocks.
+// is one cudaMemcpyAsync of the expert's blob on one of a few side streams
+// (taken in turn, so that the copies of a batch run on several copy engines
+// at once); the caller's compute stream waits on per-slot events, so the host
+// never blocks.
 //
 // Slot states: a key (>= 0), EMPTY, or INFLIGHT.  INFLIGHT marks a slot that
 // a batch has reserved for a copy and not yet published.  Victim selection
@@ -31,9 +33,11 @@ namespace {
 constexpr int64_t kEmpty = -1;
 constexpr int64_t kInflight = -2;
 
-// Default copier: device arena, side stream, per-slot copy/release events.
+// Default copier: device arena, side streams, per-slot copy/release events.
+constexpr int kSideStreams = 4;
 struct CudaCopier {
-    cudaStream_t side = nullptr;
+    cudaStream_t side[kSideStreams] = {};
+    unsigned next = 0;               // side stream of the next copy
     cudaStream_t compute = nullptr;  // set per call
     std::vector<cudaEvent_t> copied, released;
     std::vector<char> has_release;
@@ -56,11 +60,11 @@ int cuda_free(void *ctx, void *p)
 int cuda_copy(void *ctx, int32_t slot, void *dst, const void *src, size_t bytes)
 {
     CudaCopier *c = (CudaCopier *)ctx;
-    if (c->has_release[slot] && cudaStreamWaitEvent(c->side, c->released[slot], 0) != cudaSuccess)
+    cudaStream_t side = c->side[c->next++ % kSideStreams];
+    if (c->has_release[slot] && cudaStreamWaitEvent(side, c->released[slot], 0) != cudaSuccess)
         return K3MOE_ECUDA;
-    if (cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, c->side) != cudaSuccess)
-        return K3MOE_ECUDA;
-    if (cudaEventRecord(c->copied[slot], c->side) != cudaSuccess) return K3MOE_ECUDA;
+    if (cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, side) != cudaSuccess) return K3MOE_ECUDA;
+    if (cudaEventRecord(c->copied[slot], side) != cudaSuccess) return K3MOE_ECUDA;
     return K3MOE_OK;
 }
 int cuda_wait(void *ctx, int32_t slot)
@@ -106,7 +110,8 @@ static void cache_free(k3moe_cache *C)
     if (C->cuda) {
         for (auto e : C->cuda->copied) cudaEventDestroy(e);
         for (auto e : C->cuda->released) cudaEventDestroy(e);
-        if (C->cuda->side) cudaStreamDestroy(C->cuda->side);
+        for (cudaStream_t st : C->cuda->side)
+            if (st) cudaStreamDestroy(st);
         delete C->cuda;
     }
     delete C;
@@ -148,11 +153,12 @@ static int cache_init(k3moe_cache **out, size_t capacity_bytes, size_t expert_by
             return K3MOE_ENOMEM;
         }
         C->cp = {C->cuda, cuda_alloc, cuda_free, cuda_copy, cuda_wait, cuda_release};
-        if (cudaStreamCreateWithFlags(&C->cuda->side, cudaStreamNonBlocking) != cudaSuccess) {
-            cudaGetLastError();
-            cache_free(C);
-            return K3MOE_ECUDA;
-        }
+        for (cudaStream_t &st : C->cuda->side)
+            if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) {
+                cudaGetLastError();
+                cache_free(C);
+                return K3MOE_ECUDA;
+            }
         C->cuda->copied.resize(slots);
         C->cuda->released.resize(slots);
         C->cuda->has_release.assign(slots, 0);
@@ -217,7 +223,9 @@ int k3moe_cache_create_with_copier(k3moe_cache **out, size_t capacity_bytes,
 int k3moe_cache_destroy(k3moe_cache *C)
 {
     if (!C) return K3MOE_EINVAL;
-    if (C->cuda && C->cuda->side) cudaStreamSynchronize(C->cuda->side);
+    if (C->cuda)
+        for (cudaStream_t st : C->cuda->side)
+            if (st) cudaStreamSynchronize(st);
     cache_free(C);
     return K3MOE_OK;
 }
