@@ -356,6 +356,30 @@ int k3moe_cache_destroy(k3moe_cache *C);
 int k3moe_cache_acquire(k3moe_cache *C, const int64_t *host_keys, int32_t n,
                         void **host_blobs_out, uint8_t *host_hit_out, k3moe_stream compute);
 
+/*
+ * Split form of k3moe_cache_acquire, so that the hits can be computed while
+ * the misses copy: the same plan, the same copies and the same outputs, but
+ * `compute` is NOT made to wait for the copies and the misses' slots stay
+ * INFLIGHT.  Hit pointers may be used on `compute` at once; miss pointers
+ * only after k3moe_cache_wait_copies(C, compute).  A later acquire (either
+ * form) and k3moe_cache_release wait for the pending copies themselves first.
+ */
+int k3moe_cache_acquire_split(k3moe_cache *C, const int64_t *host_keys, int32_t n,
+                              void **host_blobs_out, uint8_t *host_hit_out,
+                              k3moe_stream compute);
+
+/* Makes `compute` wait for every copy issued by an acquire and not yet waited
+ * for, and publishes those keys.  Returns the copier's code of the first
+ * failed wait (that slot becomes EMPTY and its key uncached). */
+int k3moe_cache_wait_copies(k3moe_cache *C, k3moe_stream compute);
+
+/* The same for one blob pointer handed out by an acquire: `compute` waits
+ * for that slot's copy only (no-op for a hit or a copy already waited for).
+ * The copies of one acquire land in the order of their keys, so a caller can
+ * compute on the first misses while the later ones are still copying.
+ * K3MOE_EINVAL if blob is not a slot of this cache. */
+int k3moe_cache_wait_copy(k3moe_cache *C, const void *blob, k3moe_stream compute);
+
 /* Ends the use of every slot handed out since the previous release: records
  * on `compute` the point after which those slots may be overwritten (a later
  * miss that evicts one of them makes its copy wait for that point).  Slots
@@ -410,8 +434,10 @@ int32_t k3moe_cache_slot_of(const k3moe_cache *C, int64_t key);
  *   u   = x / sqrt(mean(x^2) + eps)                 (RMSNorm, unit gain)
  *   ids, w = top-k routing of u by layer l's router (+ selection bias)
  *   the k ids go to the host (one small D2H copy; the stream is synchronised)
- *   slots = k3moe_cache_acquire(keys l * n_experts + ids)   (misses copied)
- *   x  += sum_j w_j * expert_{ids_j}(u)              (experts read from slots)
+ *   slots = k3moe_cache_acquire_split(keys l * n_experts + ids)
+ *   x  += sum over hits of w_j * expert_{ids_j}(u)   (while the misses copy)
+ *   for each miss j, in copy order:
+ *       k3moe_cache_wait_copy(slot j);  x += w_j * expert_{ids_j}(u)
  *   k3moe_cache_release
  *  desc.host_layers  host array of n_layers layers (router-only layers are
  *                    fine: created with host_experts = NULL); all with the

@@ -4,10 +4,12 @@
 // explainer, "The cache the project exists for" and "The bug the code
 // confesses to"; "How kimi-k3-in-c Runs...", "The LRU cache"), rebuilt for
 // one GPU: the arena is one cudaMalloc of `slots` expert blobs in HBM; a miss
-// is one cudaMemcpyAsync of the expert's blob on one of a few side streams
-// (taken in turn, so that the copies of a batch run on several copy engines
-// at once); the caller's compute stream waits on per-slot events, so the host
-// never blocks.
+// is one cudaMemcpyAsync of the expert's blob on a side stream; the caller's
+// compute stream waits on per-slot events, so the host never blocks.  The
+// copies of one batch go to one side stream, in the batch's order, so that
+// they land one after the other and a caller can compute on each as soon as
+// it is in (a measured host link gives the same ~200 GB/s to one stream as
+// to several); successive batches take the side streams in turn.
 //
 // Slot states: a key (>= 0), EMPTY, or INFLIGHT.  INFLIGHT marks a slot that
 // a batch has reserved for a copy and not yet published.  Victim selection
@@ -24,6 +26,7 @@
 
 #include <cstring>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include "k3moe.h"
@@ -37,7 +40,8 @@ constexpr int64_t kInflight = -2;
 constexpr int kSideStreams = 4;
 struct CudaCopier {
     cudaStream_t side[kSideStreams] = {};
-    unsigned next = 0;               // side stream of the next copy
+    unsigned next = 0;               // side stream of the next batch
+    unsigned cur = 0;                // side stream of this batch
     cudaStream_t compute = nullptr;  // set per call
     std::vector<cudaEvent_t> copied, released;
     std::vector<char> has_release;
@@ -60,7 +64,7 @@ int cuda_free(void *ctx, void *p)
 int cuda_copy(void *ctx, int32_t slot, void *dst, const void *src, size_t bytes)
 {
     CudaCopier *c = (CudaCopier *)ctx;
-    cudaStream_t side = c->side[c->next++ % kSideStreams];
+    cudaStream_t side = c->side[c->cur];
     if (c->has_release[slot] && cudaStreamWaitEvent(side, c->released[slot], 0) != cudaSuccess)
         return K3MOE_ECUDA;
     if (cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, side) != cudaSuccess) return K3MOE_ECUDA;
@@ -101,6 +105,7 @@ struct k3moe_cache {
     k3moe_copier cp;
     CudaCopier *cuda = nullptr;     // when the default copier is used
     std::vector<int32_t> used;      // slots handed out since the last release
+    std::vector<std::pair<int32_t, int64_t>> pending;  // (slot, key) copied, not waited for
 };
 
 static void cache_free(k3moe_cache *C)
@@ -230,13 +235,44 @@ int k3moe_cache_destroy(k3moe_cache *C)
     return K3MOE_OK;
 }
 
-int k3moe_cache_acquire(k3moe_cache *C, const int64_t *keys, int32_t n, void **blobs_out,
-                        uint8_t *hit_out, k3moe_stream compute)
+// Makes `compute` wait for the copy into slot s (an INFLIGHT slot) and
+// publishes its key.
+static int wait_one(k3moe_cache *C, int32_t s, int64_t key)
+{
+    if (C->key[s] != kInflight) return K3MOE_OK;
+    const int r = C->cp.wait(C->cp.ctx, s);
+    if (r != K3MOE_OK) {
+        C->key[s] = kEmpty;
+        return r;
+    }
+    C->key[s] = key;
+    C->where[key] = s;
+    return K3MOE_OK;
+}
+
+// Makes `compute` wait for every copy issued and not yet waited for, and
+// publishes those slots' keys (INFLIGHT -> key).
+static int wait_pending(k3moe_cache *C, k3moe_stream compute)
+{
+    if (C->cuda) C->cuda->compute = reinterpret_cast<cudaStream_t>(compute);
+    int rc = K3MOE_OK;
+    for (const auto &pk : C->pending) {
+        const int r = wait_one(C, pk.first, pk.second);
+        if (r != K3MOE_OK && rc == K3MOE_OK) rc = r;
+    }
+    C->pending.clear();
+    return rc;
+}
+
+static int acquire(k3moe_cache *C, const int64_t *keys, int32_t n, void **blobs_out,
+                   uint8_t *hit_out, k3moe_stream compute, bool wait)
 {
     if (!C || !keys || !blobs_out || n <= 0) return K3MOE_EINVAL;
     for (int32_t i = 0; i < n; i++)
         if (keys[i] < 0 || keys[i] >= C->nkeys) return K3MOE_EINVAL;
-    if (C->cuda) C->cuda->compute = reinterpret_cast<cudaStream_t>(compute);
+    // copies of an earlier split acquire are published first, so that their
+    // keys are found as hits and not copied a second time
+    int rc = wait_pending(C, compute);
 
     // plan: hits, then one distinct victim per distinct missing key
     std::vector<char> taken(C->slots, 0);
@@ -284,7 +320,7 @@ int k3moe_cache_acquire(k3moe_cache *C, const int64_t *keys, int32_t n, void **b
         }
         C->key[s] = kInflight;
     }
-    int rc = K3MOE_OK;
+    if (C->cuda && !victims.empty()) C->cuda->cur = C->cuda->next++ % kSideStreams;
     for (int32_t i : victims) {
         const int32_t s = slot_of[i];
         int r = C->cp.copy(C->cp.ctx, s, C->arena + (size_t)s * C->expert_bytes, C->host[keys[i]],
@@ -295,18 +331,11 @@ int k3moe_cache_acquire(k3moe_cache *C, const int64_t *keys, int32_t n, void **b
             continue;
         }
         C->st.h2d_bytes += (int64_t)C->expert_bytes;
+        C->pending.emplace_back(s, keys[i]);
     }
-    for (int32_t i : victims) {
-        const int32_t s = slot_of[i];
-        if (C->key[s] != kInflight) continue;
-        int r = C->cp.wait(C->cp.ctx, s);
-        if (r != K3MOE_OK) {
-            C->key[s] = kEmpty;
-            if (rc == K3MOE_OK) rc = r;
-            continue;
-        }
-        C->key[s] = keys[i];
-        C->where[keys[i]] = s;
+    if (wait) {
+        const int r = wait_pending(C, compute);
+        if (rc == K3MOE_OK) rc = r;
     }
     for (int32_t i = 0; i < n; i++) {
         blobs_out[i] = C->arena + (size_t)slot_of[i] * C->expert_bytes;
@@ -322,11 +351,48 @@ int k3moe_cache_acquire(k3moe_cache *C, const int64_t *keys, int32_t n, void **b
     return rc;
 }
 
+int k3moe_cache_acquire(k3moe_cache *C, const int64_t *keys, int32_t n, void **blobs_out,
+                        uint8_t *hit_out, k3moe_stream compute)
+{
+    return acquire(C, keys, n, blobs_out, hit_out, compute, true);
+}
+
+int k3moe_cache_acquire_split(k3moe_cache *C, const int64_t *keys, int32_t n, void **blobs_out,
+                              uint8_t *hit_out, k3moe_stream compute)
+{
+    return acquire(C, keys, n, blobs_out, hit_out, compute, false);
+}
+
+int k3moe_cache_wait_copies(k3moe_cache *C, k3moe_stream compute)
+{
+    if (!C) return K3MOE_EINVAL;
+    return wait_pending(C, compute);
+}
+
+int k3moe_cache_wait_copy(k3moe_cache *C, const void *blob, k3moe_stream compute)
+{
+    if (!C || !blob) return K3MOE_EINVAL;
+    const uint8_t *b = (const uint8_t *)blob;
+    if (b < C->arena) return K3MOE_EINVAL;
+    const size_t off = (size_t)(b - C->arena);
+    if (off % C->expert_bytes || off / C->expert_bytes >= (size_t)C->slots) return K3MOE_EINVAL;
+    const int32_t s = (int32_t)(off / C->expert_bytes);
+    for (size_t q = 0; q < C->pending.size(); q++) {
+        if (C->pending[q].first != s) continue;
+        if (C->cuda) C->cuda->compute = reinterpret_cast<cudaStream_t>(compute);
+        const int r = wait_one(C, s, C->pending[q].second);
+        C->pending.erase(C->pending.begin() + (long)q);
+        return r;
+    }
+    return K3MOE_OK;  // a hit, or a copy already waited for
+}
+
 int k3moe_cache_release(k3moe_cache *C, k3moe_stream compute)
 {
     if (!C) return K3MOE_EINVAL;
-    if (C->cuda) C->cuda->compute = reinterpret_cast<cudaStream_t>(compute);
-    int rc = K3MOE_OK;
+    // a slot whose copy `compute` has not waited for must not be marked free
+    // on `compute`: the next copy into it could overtake the running one
+    int rc = wait_pending(C, compute);
     for (int32_t s : C->used) {
         int r = C->cp.release(C->cp.ctx, s);
         if (r != K3MOE_OK && rc == K3MOE_OK) rc = r;

@@ -2,6 +2,8 @@
 // library-owned layer scratch, and the launch sequence of each call.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -34,10 +36,11 @@ int *device_error_word()
 int launch_rows_t1(int mode, const float *x, const ExpertSrc &src, int k, int in, int rows,
                    float *out, cudaStream_t s);
 int launch_down_t1(const float *h, const ExpertSrc &src, const float *w, int k, int d, int f,
-                   float *out, cudaStream_t s);
-int launch_route_t1(const void *x, int xdt, const uint16_t *Wr, int E, int d, float *logits,
-                    const float *bias, int k, int32_t *ids, float *w, unsigned *ticket,
-                    cudaStream_t s);
+                   float *out, cudaStream_t s, bool acc = false);
+int route_t1_splits(int d);
+int launch_route_t1(const void *x, int xdt, const uint16_t *Wr, int E, int d, float *part,
+                    float *logits, const float *bias, int k, int32_t *ids, float *w,
+                    unsigned *ticket, float eps, float *u, cudaStream_t s);
 int route_multi_nsplit(int T, int E, int d);
 int launch_route_multi(const void *X, int xdt, int T, const uint16_t *Wr, int E, int d,
                        float *part, int nsplit, float *logits, const float *bias, int k,
@@ -320,7 +323,9 @@ int k3moe_layer_create(k3moe_layer **out, const k3moe_layer_desc *D)
     };
     alloc((void **)&L->table, sizeof(DevExpert) * L->E);
     alloc((void **)&L->logits, sizeof(float) * L->maxT * L->E);
-    alloc((void **)&L->part, sizeof(float) * L->nsplit * (size_t)L->maxT * L->E);
+    // multi-token split-K partials, or the batch-1 router's [S][E] partials + S sums of x^2
+    const size_t t1part = (size_t)k3::route_t1_splits(L->d) * (L->E + 1);
+    alloc((void **)&L->part, sizeof(float) * std::max((size_t)L->nsplit * L->maxT * L->E, t1part));
     alloc((void **)&L->ids, sizeof(int32_t) * pairs);
     alloc((void **)&L->w, sizeof(float) * pairs);
     alloc((void **)&L->h, sizeof(float) * pairs * L->f);
@@ -392,8 +397,8 @@ int k3moe_layer_destroy(k3moe_layer *L)
 static int route_into(k3moe_layer *L, const void *X, int xdt, int32_t T, cudaStream_t s)
 {
     if (T == 1)
-        return k3::launch_route_t1(X, xdt, L->Wr, L->E, L->d, L->logits, L->bias, L->k, L->ids,
-                                   L->w, L->ticket, s);
+        return k3::launch_route_t1(X, xdt, L->Wr, L->E, L->d, L->part, L->logits, L->bias, L->k,
+                                   L->ids, L->w, L->ticket, 0.f, nullptr, s);
     return k3::launch_route_multi(X, xdt, T, L->Wr, L->E, L->d, L->part, L->nsplit, L->logits,
                                   L->bias, L->k, L->ids, L->w, s);
 }
@@ -571,25 +576,25 @@ extern "C" int k3moe_stream_decode(const k3moe_stream_desc *D, const float *X, i
         if (!L || L->E != E || L->k != k || L->d != d || L->f != f) return K3MOE_EINVAL;
     }
     cudaStream_t st = cs(s);
-    float *xcur = nullptr, *u = nullptr, *delta = nullptr, *wdev = nullptr;
-    int32_t *iddev = nullptr, *idhost = nullptr;
+    float *xcur = nullptr, *u = nullptr, *wsub = nullptr;
+    float *whost = nullptr;  // pinned: [k] routing weights, then [k] reordered hits-first
+    int32_t *idhost = nullptr;
     int rc = K3MOE_OK;
     auto fail = [&](int code) {
         if (rc == K3MOE_OK) rc = code;
     };
     if (cudaMalloc(&xcur, sizeof(float) * d) != cudaSuccess ||
         cudaMalloc(&u, sizeof(float) * d) != cudaSuccess ||
-        cudaMalloc(&delta, sizeof(float) * d) != cudaSuccess ||
-        cudaMalloc(&wdev, sizeof(float) * k) != cudaSuccess ||
-        cudaMalloc(&iddev, sizeof(int32_t) * k) != cudaSuccess ||
-        cudaMallocHost(&idhost, sizeof(int32_t) * k) != cudaSuccess) {
+        cudaMalloc(&wsub, sizeof(float) * k) != cudaSuccess ||
+        cudaMallocHost(&idhost, sizeof(int32_t) * k) != cudaSuccess ||
+        cudaMallocHost(&whost, sizeof(float) * 2 * k) != cudaSuccess) {
         cudaGetLastError();
         fail(K3MOE_ENOMEM);
     }
     std::vector<int64_t> keys(k);
     std::vector<void *> blobs(k);
     std::vector<uint8_t> hits(k);
-    std::vector<k3moe_expert> views(k);
+    std::vector<int> order(k);
     for (int t = 0; t < T && rc == K3MOE_OK; t++) {
         if (cudaMemcpyAsync(xcur, X + (size_t)t * d, sizeof(float) * d, cudaMemcpyDeviceToDevice,
                             st) != cudaSuccess) {
@@ -598,13 +603,16 @@ extern "C" int k3moe_stream_decode(const k3moe_stream_desc *D, const float *X, i
         }
         for (int l = 0; l < D->n_layers && rc == K3MOE_OK; l++) {
             k3moe_layer *L = D->host_layers[l];
-            int r = k3moe_rmsnorm(u, xcur, d, D->eps, s);
-            if (r == K3MOE_OK) r = k3moe_layer_route(L, u, K3MOE_F32, 1, iddev, wdev, s);
+            // RMSNorm folded into the router: u = x / sqrt(mean(x^2) + eps)
+            int r = k3::launch_route_t1(xcur, K3MOE_F32, L->Wr, E, d, L->part, L->logits, L->bias,
+                                        k, L->ids, L->w, L->ticket, D->eps, u, st);
             if (r != K3MOE_OK) {
                 fail(r);
                 break;
             }
-            if (cudaMemcpyAsync(idhost, iddev, sizeof(int32_t) * k, cudaMemcpyDeviceToHost, st) !=
+            if (cudaMemcpyAsync(idhost, L->ids, sizeof(int32_t) * k, cudaMemcpyDeviceToHost, st) !=
+                    cudaSuccess ||
+                cudaMemcpyAsync(whost, L->w, sizeof(float) * k, cudaMemcpyDeviceToHost, st) !=
                     cudaSuccess ||
                 cudaStreamSynchronize(st) != cudaSuccess) {
                 cudaGetLastError();
@@ -612,14 +620,45 @@ extern "C" int k3moe_stream_decode(const k3moe_stream_desc *D, const float *X, i
                 break;
             }
             for (int j = 0; j < k; j++) keys[j] = (int64_t)l * E + idhost[j];
-            r = k3moe_cache_acquire(D->cache, keys.data(), k, blobs.data(), hits.data(), s);
+            // The misses' copies run on a side stream while the hits are
+            // computed; each miss is then computed as soon as its own copy is
+            // in, so that only the last miss's compute follows the copies.
+            r = k3moe_cache_acquire_split(D->cache, keys.data(), k, blobs.data(), hits.data(), s);
             if (r != K3MOE_OK) {
                 fail(r);
                 break;
             }
-            for (int j = 0; j < k && r == K3MOE_OK; j++) r = k3moe_expert_view(&views[j], blobs[j], d, f);
-            if (r == K3MOE_OK) r = k3moe_layer_experts_t1(L, u, views.data(), wdev, k, delta, s);
-            if (r == K3MOE_OK) r = k3moe_residual_add(xcur, delta, d, s);
+            int nh = 0;
+            for (int j = 0; j < k; j++)
+                if (hits[j]) order[nh++] = j;
+            for (int j = 0, q = nh; j < k; j++)  // misses in key order = copy order
+                if (!hits[j]) order[q++] = j;
+            ExpertSrc src;
+            memset(&src, 0, sizeof(src));
+            for (int q = 0; q < k && r == K3MOE_OK; q++) {
+                whost[k + q] = whost[order[q]];
+                k3moe_expert v;
+                r = k3moe_expert_view(&v, blobs[order[q]], d, f);
+                if (r == K3MOE_OK) src.inl[q] = to_dev(v);
+            }
+            // whost[k..] is rewritten only after the next layer's synchronise,
+            // when this copy has long completed
+            if (r == K3MOE_OK && cudaMemcpyAsync(wsub, whost + k, sizeof(float) * k,
+                                                 cudaMemcpyHostToDevice, st) != cudaSuccess)
+                r = K3MOE_ECUDA;
+            // x += sum_j w_j expert_j(u): the down kernel adds into x
+            if (r == K3MOE_OK && nh > 0) {
+                r = k3::launch_rows_t1(1, u, src, nh, d, f, L->h, st);
+                if (r == K3MOE_OK) r = k3::launch_down_t1(L->h, src, wsub, nh, d, f, xcur, st, true);
+            }
+            for (int q = nh; q < k && r == K3MOE_OK; q++) {
+                r = k3moe_cache_wait_copy(D->cache, blobs[order[q]], s);
+                ExpertSrc one;
+                memset(&one, 0, sizeof(one));
+                one.inl[0] = src.inl[q];
+                if (r == K3MOE_OK) r = k3::launch_rows_t1(1, u, one, 1, d, f, L->h, st);
+                if (r == K3MOE_OK) r = k3::launch_down_t1(L->h, one, wsub + q, 1, d, f, xcur, st, true);
+            }
             const int rr = k3moe_cache_release(D->cache, s);
             if (r == K3MOE_OK) r = rr;
             if (r != K3MOE_OK) {
@@ -639,9 +678,8 @@ extern "C" int k3moe_stream_decode(const k3moe_stream_desc *D, const float *X, i
     cudaGetLastError();
     cudaFree(xcur);
     cudaFree(u);
-    cudaFree(delta);
-    cudaFree(wdev);
-    cudaFree(iddev);
+    cudaFree(wsub);
     cudaFreeHost(idhost);
+    cudaFreeHost(whost);
     return rc;
 }

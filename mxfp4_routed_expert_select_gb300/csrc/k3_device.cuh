@@ -363,5 +363,218 @@ K3_DEV float warp_sum(float v)
 
 K3_DEV float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// Ticket of a "last CTA finishes the work" pattern: called by one thread
+// after a __syncthreads that follows the CTA's global writes.  The acq_rel
+// atomic publishes those writes at GPU scope (cumulatively, through the
+// barrier) and, for the last CTA, makes every other CTA's writes visible;
+// a fence.sc by every thread (a __threadfence) is much slower.
+K3_DEV unsigned ticket_arrive(unsigned *ticket)
+{
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(ticket) : "memory");
+    return old;
+}
+
+// Order-preserving map of an fp32 score to uint32 (larger score -> larger key).
+K3_DEV uint32_t okey(float v)
+{
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// 256 threads (threadIdx.x 0..255, synchronised by sync()) select the top k (k <= 32) of E <= 1024
+// scores logit[e] + bias[e] (bias may be null), ties to the lower id, with the
+// same result as warp_topk below: the k-th largest key is found one byte at a
+// time (4 rounds of a 256-bin shared-memory histogram over the keys that
+// match the prefix so far, warp-aggregated atomics, and a descending scan by
+// one warp), then every key above it and the lowest-id ties at it are
+// compacted in id order.  ids_out[0..k) / w_out as in warp_topk.
+struct CtaTopkSmem {
+    unsigned hist[256];
+    unsigned cnt[2][4][8];  // per (pass, m, warp) selection counts
+    int ids[32];
+    unsigned prefix, need;
+};
+template <typename Sync>
+K3_DEV void cta_topk(const float *logit, const float *bias, int E, int k, int32_t *ids_out,
+                     float *w_out, CtaTopkSmem &sm, Sync sync)
+{
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    uint32_t key[4];
+#pragma unroll
+    for (int m = 0; m < 4; m++) {
+        const int e = t + 256 * m;
+        key[m] = 0u;  // below every real key
+        if (e < E) key[m] = okey(__ldcg(logit + e) + (bias ? __ldg(bias + e) : 0.f));
+    }
+    uint32_t prefix = 0u, mask = 0u;
+    unsigned need = (unsigned)k;
+#pragma unroll 1
+    for (int r = 0; r < 4; r++) {
+        const int shift = 24 - 8 * r;
+        sm.hist[t] = 0u;
+        sync();
+#pragma unroll
+        for (int m = 0; m < 4; m++) {
+            const bool in = (t + 256 * m < E) && (key[m] & mask) == prefix;
+            const unsigned act = __ballot_sync(0xffffffffu, in);
+            if (in) {
+                const unsigned dg = (key[m] >> shift) & 255u;
+                const unsigned peers = __match_any_sync(act, dg);
+                if (lane == __ffs(peers) - 1) atomicAdd(&sm.hist[dg], (unsigned)__popc(peers));
+            }
+        }
+        sync();
+        if (warp == 0) {
+            // lane l owns bins 255-8l .. 248-8l (descending)
+            unsigned hb[8], own = 0;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                hb[i] = sm.hist[255 - 8 * lane - i];
+                own += hb[i];
+            }
+            unsigned incl = own;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const unsigned o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            const unsigned excl = incl - own;
+            if (excl < need && incl >= need) {
+                unsigned cum = excl;
+                for (int i = 0; i < 8; i++) {
+                    if (cum + hb[i] >= need) {
+                        sm.prefix = prefix | ((uint32_t)(255 - 8 * lane - i) << shift);
+                        sm.need = need - cum;
+                        break;
+                    }
+                    cum += hb[i];
+                }
+            }
+        }
+        sync();
+        prefix = sm.prefix;
+        need = sm.need;
+        mask |= 255u << shift;
+    }
+    // prefix = the k-th largest key; take the `need` lowest-id ties at it
+    const uint32_t T = prefix;
+    const unsigned lt = (1u << lane) - 1u;
+    unsigned eqb[4], rank_eq[4];
+#pragma unroll
+    for (int m = 0; m < 4; m++) {
+        eqb[m] = __ballot_sync(0xffffffffu, (t + 256 * m < E) && key[m] == T);
+        if (lane == 0) sm.cnt[0][m][warp] = __popc(eqb[m]);
+    }
+    sync();
+    if (warp == 0) {  // exclusive prefix over (m, warp) = id order
+        const unsigned c = sm.cnt[0][lane >> 3][lane & 7];
+        unsigned incl = c;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const unsigned o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        sm.cnt[0][lane >> 3][lane & 7] = incl - c;
+    }
+    sync();
+    unsigned selb[4];
+#pragma unroll
+    for (int m = 0; m < 4; m++) {
+        rank_eq[m] = sm.cnt[0][m][warp] + __popc(eqb[m] & lt);
+        const bool sel = (t + 256 * m < E) &&
+                         (key[m] > T || (((eqb[m] >> lane) & 1u) && rank_eq[m] < need));
+        selb[m] = __ballot_sync(0xffffffffu, sel);
+        if (lane == 0) sm.cnt[1][m][warp] = __popc(selb[m]);
+    }
+    sync();
+    if (warp == 0) {
+        const unsigned c = sm.cnt[1][lane >> 3][lane & 7];
+        unsigned incl = c;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const unsigned o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        sm.cnt[1][lane >> 3][lane & 7] = incl - c;
+    }
+    sync();
+#pragma unroll
+    for (int m = 0; m < 4; m++)
+        if ((selb[m] >> lane) & 1u) sm.ids[sm.cnt[1][m][warp] + __popc(selb[m] & lt)] = t + 256 * m;
+    sync();
+    if (warp == 0) {
+        const int my_id = (lane < k) ? sm.ids[lane] : 0;
+        const float l = (lane < k) ? __ldcg(logit + my_id) : -INFINITY;
+        float mx = l;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float ex = (lane < k) ? expf(l - mx) : 0.f;
+        const float sum = warp_sum(ex);
+        if (lane < k) {
+            ids_out[lane] = my_id;
+            w_out[lane] = ex / sum;
+        }
+    }
+}
+
+// One warp selects the top k (k <= 32) of E <= 1024 scores logit[e] + bias[e]
+// (bias may be null), ties to the lower id: a radix search for the k-th
+// largest key (32 rounds of one count and one warp reduction), then every
+// key above it and the lowest-id ties at it.  ids_out[0..k) receives the ids
+// in ascending order and w_out the softmax of the UNBIASED logits over the
+// chosen set ("Running Kimi K3 locally", invariant 3).  logit is read with
+// ld.cg (other CTAs may have written it); ids_out is read back by the warp.
+K3_DEV void warp_topk(const float *logit, const float *bias, int E, int k, int32_t *ids_out,
+                      float *w_out, int lane)
+{
+    uint32_t key[32];
+#pragma unroll
+    for (int q = 0; q < 32; q++) {
+        const int e = lane + 32 * q;
+        key[q] = 0u;  // below every real key (okey(-inf) = 0x007fffff)
+        if (e < E) key[q] = okey(__ldcg(logit + e) + (bias ? __ldg(bias + e) : 0.f));
+    }
+    uint32_t T = 0u;  // largest T with count(key >= T) >= k
+    for (int b = 31; b >= 0; b--) {
+        const uint32_t cand = T | (1u << b);
+        uint32_t c0 = 0, c1 = 0;
+#pragma unroll
+        for (int q = 0; q < 32; q += 2) {
+            c0 += key[q] >= cand;
+            c1 += key[q + 1] >= cand;
+        }
+        if (__reduce_add_sync(0xffffffffu, c0 + c1) >= (unsigned)k) T = cand;
+    }
+    uint32_t cgt = 0;
+#pragma unroll
+    for (int q = 0; q < 32; q++) cgt += key[q] > T;
+    const int need = k - (int)__reduce_add_sync(0xffffffffu, cgt);
+    const uint32_t lt = (1u << lane) - 1u;
+    int eq_before = 0, sel_before = 0;
+#pragma unroll
+    for (int q = 0; q < 32; q++) {
+        const int e = lane + 32 * q;
+        const bool eq = (e < E) && key[q] == T;
+        const unsigned beq = __ballot_sync(0xffffffffu, eq);
+        const bool pick_eq = eq && (eq_before + __popc(beq & lt)) < need;
+        const bool sel = ((e < E) && key[q] > T) || pick_eq;
+        const unsigned bsel = __ballot_sync(0xffffffffu, sel);
+        if (sel) ids_out[sel_before + __popc(bsel & lt)] = e;
+        eq_before += __popc(beq);
+        sel_before += __popc(bsel);
+    }
+    __syncwarp();
+    const int my_id = (lane < k) ? ids_out[lane] : 0;
+    const float l = (lane < k) ? __ldcg(logit + my_id) : -INFINITY;
+    float mx = l;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float ex = (lane < k) ? expf(l - mx) : 0.f;
+    const float sum = warp_sum(ex);
+    if (lane < k) w_out[lane] = ex / sum;
+    __syncwarp();
+}
+
 
 }  // namespace k3

@@ -125,71 +125,20 @@ K3_DEV float bf16x8_dotf(uint4 wv, const float *xv, float acc)
     return acc;
 }
 
-// order-preserving map of an fp32 score to uint32 (larger score -> larger key)
-K3_DEV uint32_t okey(float v)
+// Compute warps 0..7 (named barrier 2): the top k of the scores into sel_ids
+// / sel_w (shared memory); CTA 0 also writes them to the layer's ids / w.
+K3_DEV void topk_phase(const FusedArgs &a, int *sel_ids, float *sel_w, CtaTopkSmem &tk)
 {
-    const uint32_t u = __float_as_uint(v);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// One warp: the top k of E scores (logit + bias), ties to the lower id, by a
-// radix search for the k-th largest key; ids ascending and softmax weights of
-// the unbiased logits over the chosen set into sel_ids / sel_w.
-K3_DEV void warp_topk_radix(const FusedArgs &a, int *sel_ids, float *sel_w, int lane)
-{
-    const int E = a.E, k = a.k;
-    uint32_t key[32];
-#pragma unroll
-    for (int q = 0; q < 32; q++) {
-        const int e = lane + 32 * q;
-        key[q] = 0u;  // below every real key (okey of -inf is 0x007fffff)
-        if (e < E) key[q] = okey(__ldcg(a.logits + e) + (a.bias ? __ldg(a.bias + e) : 0.f));
-    }
-    // largest T with count(key >= T) >= k
-    uint32_t T = 0u;
-    for (int b = 31; b >= 0; b--) {
-        const uint32_t cand = T | (1u << b);
-        uint32_t c0 = 0, c1 = 0;
-#pragma unroll
-        for (int q = 0; q < 32; q += 2) {
-            c0 += key[q] >= cand;
-            c1 += key[q + 1] >= cand;
+    cta_topk(a.logits, a.bias, a.E, a.k, sel_ids, sel_w, tk, [] { named_sync(2, 256); });
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x < 32) {
+        __syncwarp();
+        if (lane < a.k && blockIdx.x == 0) {
+            a.ids[lane] = sel_ids[lane];
+            a.w[lane] = sel_w[lane];
         }
-        if (__reduce_add_sync(0xffffffffu, c0 + c1) >= (unsigned)k) T = cand;
+        __syncwarp();
     }
-    // everything above T is in; ties at T fill the rest in id order
-    uint32_t cgt = 0;
-#pragma unroll
-    for (int q = 0; q < 32; q++) cgt += key[q] > T;
-    const int need = k - (int)__reduce_add_sync(0xffffffffu, cgt);
-    const uint32_t lt = (1u << lane) - 1u;
-    int eq_before = 0, sel_before = 0;
-#pragma unroll
-    for (int q = 0; q < 32; q++) {
-        const int e = lane + 32 * q;
-        const bool eq = (e < E) && key[q] == T;
-        const unsigned beq = __ballot_sync(0xffffffffu, eq);
-        const bool pick_eq = eq && (eq_before + __popc(beq & lt)) < need;
-        const bool sel = ((e < E) && key[q] > T) || pick_eq;
-        const unsigned bsel = __ballot_sync(0xffffffffu, sel);
-        if (sel) sel_ids[sel_before + __popc(bsel & lt)] = e;
-        eq_before += __popc(beq);
-        sel_before += __popc(bsel);
-    }
-    __syncwarp();
-    const int my_id = (lane < k) ? sel_ids[lane] : 0;
-    const float l = (lane < k) ? __ldcg(a.logits + my_id) : -INFINITY;
-    float mx = l;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    const float ex = (lane < k) ? expf(l - mx) : 0.f;
-    const float sum = warp_sum(ex);
-    if (lane < k) sel_w[lane] = ex / sum;
-    if (lane < k && blockIdx.x == 0) {
-        a.ids[lane] = my_id;
-        a.w[lane] = ex / sum;
-    }
-    __syncwarp();
 }
 
 template <bool ACT16>
@@ -379,9 +328,10 @@ __global__ void __launch_bounds__(FU_THREADS, 1) k3_moe_t1_fused(FusedArgs a)
     if (!grid_barrier(a, abort_flag)) return;
 
     // ------------------------------------------------------ phase T: top-k
-    if (warp == 0) {
-        warp_topk_radix(a, sel_ids, sel_w, lane);
-        if (lane == 0) {
+    if (warp < 8) {
+        __shared__ CtaTopkSmem tk;
+        topk_phase(a, sel_ids, sel_w, tk);
+        if (threadIdx.x == 0) {
             __threadfence_block();
             mbar_arrive(topk_bar);  // the producer may now stream expert rows
         }

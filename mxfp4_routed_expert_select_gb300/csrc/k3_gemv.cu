@@ -290,13 +290,15 @@ __global__ void __launch_bounds__(512, 1) k3_rows_pipe(const float *__restrict__
 }
 
 // -------------------------------------------------------------------- down
-// out[i] = sum_j w[j] * (down_j[i] . h[j])  over the k selected experts.
+// out[i] = sum_j w[j] * (down_j[i] . h[j])  over the k selected experts
+// (added to out[i] when acc is set).
 // CTA: k * nsub warps; warp (j, s) handles expert j and rows i0+s, i0+s+nsub..
 // Lane owns HPL half-groups (16 columns each) of the f-long input.
 template <int HPL, int U>
 __global__ void __launch_bounds__(512) k3_down_t1(const float *__restrict__ h, ExpertSrc src,
                                                   const float *__restrict__ w, int k, int d, int f,
-                                                  float *__restrict__ out, int rows_per_cta)
+                                                  float *__restrict__ out, int rows_per_cta,
+                                                  int acc)
 {
     extern __shared__ float red[];  // [k][rows_per_cta]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -378,7 +380,7 @@ __global__ void __launch_bounds__(512) k3_down_t1(const float *__restrict__ h, E
     for (int t = threadIdx.x; t < i1 - i0; t += blockDim.x) {
         float a = 0.f;
         for (int jj = 0; jj < k; jj++) a += red[(size_t)jj * rows_per_cta + t];
-        out[i0 + t] = a;
+        out[i0 + t] = acc ? out[i0 + t] + a : a;
     }
 }
 
@@ -501,7 +503,7 @@ int launch_rows_t1(int mode, const float *x, const ExpertSrc &src, int k, int in
 
 template <int HPL>
 static int launch_down_hpl(const float *h, const ExpertSrc &src, const float *w, int k, int d,
-                           int f, float *out, cudaStream_t s)
+                           int f, float *out, cudaStream_t s, bool acc)
 {
     const int nsub = 16 / k;
     const int threads = k * nsub * 32;
@@ -515,20 +517,20 @@ static int launch_down_hpl(const float *h, const ExpertSrc &src, const float *w,
         cudaFuncSetAttribute(k3_down_t1<HPL, kUdown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     const int grid = (d + rpc - 1) / rpc;
-    k3_down_t1<HPL, kUdown><<<grid, threads, smem, s>>>(h, src, w, k, d, f, out, rpc);
+    k3_down_t1<HPL, kUdown><<<grid, threads, smem, s>>>(h, src, w, k, d, f, out, rpc, acc ? 1 : 0);
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
 }
 
 int launch_down_t1(const float *h, const ExpertSrc &src, const float *w, int k, int d, int f,
-                   float *out, cudaStream_t s)
+                   float *out, cudaStream_t s, bool acc)
 {
     if (k < 1 || k > 16) return K3MOE_EINVAL;
     const int hpl = (f / 16 + 31) / 32;
     switch (hpl) {
-    case 1: return launch_down_hpl<1>(h, src, w, k, d, f, out, s);
-    case 2: return launch_down_hpl<2>(h, src, w, k, d, f, out, s);
-    case 3: return launch_down_hpl<3>(h, src, w, k, d, f, out, s);
-    case 4: return launch_down_hpl<4>(h, src, w, k, d, f, out, s);
+    case 1: return launch_down_hpl<1>(h, src, w, k, d, f, out, s, acc);
+    case 2: return launch_down_hpl<2>(h, src, w, k, d, f, out, s, acc);
+    case 3: return launch_down_hpl<3>(h, src, w, k, d, f, out, s, acc);
+    case 4: return launch_down_hpl<4>(h, src, w, k, d, f, out, s, acc);
     default: return K3MOE_EINVAL;
     }
 }

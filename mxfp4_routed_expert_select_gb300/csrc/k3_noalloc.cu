@@ -29,7 +29,7 @@ namespace k3 {
 int launch_rows_t1_err(int mode, const float *x, const ExpertSrc &src, int k, int in, int rows,
                        float *out, int *err, cudaStream_t s);
 int launch_down_t1(const float *h, const ExpertSrc &src, const float *w, int k, int d, int f,
-                   float *out, cudaStream_t s);
+                   float *out, cudaStream_t s, bool acc = false);
 }  // namespace k3
 
 // Largest expert intermediate size f the static scratch holds (8 KB of fp32).

@@ -12,65 +12,15 @@ namespace k3 {
 
 int num_sms();
 
-// Selection key: larger is better; ties broken toward the lower id.
-K3_DEV bool better(float a, int ia, float b, int ib) { return a > b || (a == b && ia < ib); }
-
-// One warp selects the top k (k <= 32) of E scores for one token.
-// logit: unbiased logits [E] (read with ld.cg: they may have been written by
-// other CTAs of the same kernel), bias: [E] or null.  The scores are loaded
-// once into registers (E <= 32 * TK_MAXPL); k rounds of a warp argmax follow.
-// Writes ids ascending and the softmax weights of the unbiased logits.
-constexpr int TK_MAXPL = 32;  // E <= 1024
-K3_DEV void warp_topk(const float *logit, const float *bias, int E, int k, int32_t *ids_out,
-                      float *w_out, int lane)
-{
-    float sc[TK_MAXPL];
-#pragma unroll
-    for (int q = 0; q < TK_MAXPL; q++) {
-        const int e = lane + 32 * q;
-        sc[q] = -INFINITY;
-        if (e < E) sc[q] = __ldcg(logit + e) + (bias ? __ldg(bias + e) : 0.f);
-    }
-    unsigned taken = 0;  // bit q: my element q already chosen
-    int my_id = -1;
-    for (int r = 0; r < k; r++) {
-        float bs = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int q = 0; q < TK_MAXPL; q++) {
-            const int e = lane + 32 * q;
-            if (e < E && !((taken >> q) & 1u) && better(sc[q], e, bs, bi)) { bs = sc[q]; bi = e; }
-        }
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-            float os = __shfl_xor_sync(0xffffffffu, bs, off);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (better(os, oi, bs, bi)) { bs = os; bi = oi; }
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == r) my_id = bi;
-    }
-    // ascending ids: rank of my id among the k chosen
-    int pos = 0;
-    for (int q = 0; q < k; q++) {
-        int other = __shfl_sync(0xffffffffu, my_id, q);
-        if (lane < k && other < my_id) pos++;
-    }
-    float l = (lane < k) ? __ldcg(logit + my_id) : -INFINITY;
-    float mx = l;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    float ex = (lane < k) ? expf(l - mx) : 0.f;
-    float sum = warp_sum(ex);
-    if (lane < k) {
-        ids_out[pos] = my_id;
-        w_out[pos] = ex / sum;
-    }
-}
 
 // ------------------------------------------------------- batch-1 router
-// One warp per expert row: 16-byte loads of 8 bf16 weights, x read through
-// L1.  The last CTA to finish (ticket counter, no waiting) runs the top-k.
+// The 12.8 MB of W_r for one token are only read at full HBM speed when
+// nearly all of them are in flight at once: every expert row is split into S
+// column ranges of RT1_CHUNKS 16-byte chunks (S = 4 at d = 7168), one warp
+// per (row, range), each lane issuing all its loads (<= RT1_LPL) before the
+// first multiply.  Partial dot products go to part[S][E]; the last CTA to
+// finish (ticket counter, no waiting) sums them in a fixed order, applies the
+// optional RMSNorm factor and runs the top-k.
 template <typename XT>
 K3_DEV void load_x8(const XT *x, int i, float (&xv)[8]);
 template <>
@@ -104,46 +54,110 @@ K3_DEV float bf16x8_dot(uint4 wv, const float (&xv)[8], float acc)
     return acc;
 }
 
+constexpr int RT1_LPL = 8;                 // 16-byte loads per lane per range
+constexpr int RT1_CHUNKS = 32 * RT1_LPL;   // 8-column chunks per range
+constexpr int RT1_SMAX = 16;               // ranges per row: d <= 16384
+
+int route_t1_splits(int d) { return ((d >> 3) + RT1_CHUNKS - 1) / RT1_CHUNKS; }
+
+// part: [S][E] partial dot products, then S partial sums of x^2 (RMSNorm
+// mode).  RMSNorm mode (u != null, x fp32): r = 1/sqrt(mean(x^2) + eps); the
+// logits are r * (W_r . x), equal to W_r . (r x) up to rounding, and u = r x
+// is written for the expert kernels.  Otherwise r = 1 and u is not written.
+// The last CTA's loads are all issued before their first use (fixed-size
+// unrolled loops): a dependent chain of L2 round trips there would cost more
+// than the whole matrix read.
 template <typename XT>
 __global__ void __launch_bounds__(256) k3_router_t1(const XT *__restrict__ x,
                                                     const uint16_t *__restrict__ Wr, int E, int d,
-                                                    float *logits, const float *bias, int k,
-                                                    int32_t *ids, float *w, unsigned *ticket)
+                                                    int S, float *part, float *logits,
+                                                    const float *bias, int k, int32_t *ids,
+                                                    float *w, unsigned *ticket, float eps,
+                                                    float *u)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int e = blockIdx.x * (blockDim.x >> 5) + warp;
+    const int lane = threadIdx.x & 31;
+    const int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int e = g / S, sp = g - e * S;
     if (e < E) {
         const uint16_t *row = Wr + (size_t)e * d;
-        float acc0 = 0.f, acc1 = 0.f;
-        const int nchunk = d >> 3;
-        int c = lane;
-        for (; c + 32 < nchunk; c += 64) {
-            uint4 w0 = ld_stream16(row + 8 * c);
-            uint4 w1 = ld_stream16(row + 8 * (c + 32));
-            float x0[8], x1[8];
-            load_x8<XT>(x, 8 * c, x0);
-            load_x8<XT>(x, 8 * (c + 32), x1);
-            acc0 = bf16x8_dot(w0, x0, acc0);
-            acc1 = bf16x8_dot(w1, x1, acc1);
+        const int c0 = sp * RT1_CHUNKS, c1 = min(c0 + RT1_CHUNKS, d >> 3);
+        uint4 wv[RT1_LPL];
+#pragma unroll
+        for (int q = 0; q < RT1_LPL; q++) {
+            const int c = c0 + lane + 32 * q;
+            wv[q] = c < c1 ? ld_stream16(row + 8 * c) : make_uint4(0, 0, 0, 0);
         }
-        for (; c < nchunk; c += 32) {
-            uint4 w0 = ld_stream16(row + 8 * c);
-            float x0[8];
-            load_x8<XT>(x, 8 * c, x0);
-            acc0 = bf16x8_dot(w0, x0, acc0);
+        float acc = 0.f, xx = 0.f;
+#pragma unroll
+        for (int q = 0; q < RT1_LPL; q++) {
+            const int c = c0 + lane + 32 * q;
+            if (c < c1) {
+                float xv[8];
+                load_x8<XT>(x, 8 * c, xv);
+                acc = bf16x8_dot(wv[q], xv, acc);
+#pragma unroll
+                for (int i = 0; i < 8; i++) xx = fmaf(xv[i], xv[i], xx);
+            }
         }
-        float acc = warp_sum(acc0 + acc1);
-        if (lane == 0) logits[e] = acc;
+        acc = warp_sum(acc);
+        if (lane == 0) part[(size_t)sp * E + e] = acc;
+        if (u && e == 0) {  // row 0's S warps cover x once
+            xx = warp_sum(xx);
+            if (lane == 0) part[(size_t)S * E + sp] = xx;
+        }
     }
-    // last CTA does the selection
     __shared__ unsigned s_last;
-    __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1u) == gridDim.x - 1);
+    if (threadIdx.x == 0) s_last = (ticket_arrive(ticket) == gridDim.x - 1);
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
-    if (warp == 0) warp_topk(logits, bias, E, k, ids, w, lane);
+    float r = 1.f;
+    if (u) {
+        float v[RT1_SMAX];
+#pragma unroll
+        for (int q = 0; q < RT1_SMAX; q++) v[q] = q < S ? __ldcg(part + (size_t)S * E + q) : 0.f;
+        float ss = 0.f;
+#pragma unroll
+        for (int q = 0; q < RT1_SMAX; q++) ss += v[q];
+        r = rsqrtf(ss / (float)d + eps);
+        const float4 *x4 = reinterpret_cast<const float4 *>(x);
+        float4 *u4 = reinterpret_cast<float4 *>(u);
+        const int n4 = d >> 2;
+        for (int i0 = threadIdx.x; i0 < n4; i0 += 8 * blockDim.x) {
+            float4 t[8];
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                const int i = i0 + q * blockDim.x;
+                if (i < n4) t[q] = x4[i];
+            }
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                const int i = i0 + q * blockDim.x;
+                if (i < n4) u4[i] = make_float4(t[q].x * r, t[q].y * r, t[q].z * r, t[q].w * r);
+            }
+        }
+    }
+    for (int i0 = threadIdx.x; i0 < E; i0 += 2 * blockDim.x) {
+        float v[2][RT1_SMAX];
+#pragma unroll
+        for (int m = 0; m < 2; m++) {
+            const int i = i0 + m * blockDim.x;
+#pragma unroll
+            for (int q = 0; q < RT1_SMAX; q++)
+                v[m][q] = (i < E && q < S) ? __ldcg(part + (size_t)q * E + i) : 0.f;
+        }
+#pragma unroll
+        for (int m = 0; m < 2; m++) {
+            const int i = i0 + m * blockDim.x;
+            float a = 0.f;
+#pragma unroll
+            for (int q = 0; q < RT1_SMAX; q++) a += v[m][q];
+            if (i < E) logits[i] = a * r;
+        }
+    }
+    __syncthreads();
+    __shared__ CtaTopkSmem tk;
+    cta_topk(logits, bias, E, k, ids, w, tk, [] { __syncthreads(); });
     if (threadIdx.x == 0) *ticket = 0;  // ready for the next launch on this stream
 }
 
@@ -298,18 +312,21 @@ __global__ void __launch_bounds__(1024) k3_group(const int32_t *__restrict__ ids
 
 // ------------------------------------------------------------- launchers
 
-int launch_route_t1(const void *x, int xdt, const uint16_t *Wr, int E, int d, float *logits,
-                    const float *bias, int k, int32_t *ids, float *w, unsigned *ticket,
-                    cudaStream_t s)
+int launch_route_t1(const void *x, int xdt, const uint16_t *Wr, int E, int d, float *part,
+                    float *logits, const float *bias, int k, int32_t *ids, float *w,
+                    unsigned *ticket, float eps, float *u, cudaStream_t s)
 {
+    const int S = route_t1_splits(d);
+    if ((u && xdt != K3MOE_F32) || S > RT1_SMAX) return K3MOE_EINVAL;
     const int threads = 256, wpb = threads / 32;
-    const int grid = (E + wpb - 1) / wpb;
+    const int grid = (int)(((long)E * S + wpb - 1) / wpb);
     if (xdt == K3MOE_F32)
-        k3_router_t1<float><<<grid, threads, 0, s>>>((const float *)x, Wr, E, d, logits, bias, k,
-                                                     ids, w, ticket);
+        k3_router_t1<float><<<grid, threads, 0, s>>>((const float *)x, Wr, E, d, S, part, logits,
+                                                     bias, k, ids, w, ticket, eps, u);
     else
         k3_router_t1<__nv_bfloat16><<<grid, threads, 0, s>>>((const __nv_bfloat16 *)x, Wr, E, d,
-                                                             logits, bias, k, ids, w, ticket);
+                                                             S, part, logits, bias, k, ids, w,
+                                                             ticket, eps, u);
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
 }
 

@@ -109,6 +109,9 @@ SIGNATURES = {
     "k3moe_cache_create": (ctypes.c_int, [_P, _SZ, _SZ, _P, _I, _I]),
     "k3moe_cache_destroy": (ctypes.c_int, [_P]),
     "k3moe_cache_acquire": (ctypes.c_int, [_P, _P, _I, _P, _P, _P]),
+    "k3moe_cache_acquire_split": (ctypes.c_int, [_P, _P, _I, _P, _P, _P]),
+    "k3moe_cache_wait_copies": (ctypes.c_int, [_P, _P]),
+    "k3moe_cache_wait_copy": (ctypes.c_int, [_P, _P, _P]),
     "k3moe_cache_release": (ctypes.c_int, [_P, _P]),
     "k3moe_cache_pin": (ctypes.c_int, [_P, _I64, _P]),
     "k3moe_cache_get_stats": (ctypes.c_int, [_P, _P]),
@@ -325,16 +328,25 @@ class Cache:
         self.h = h
         self.nkeys = n
 
-    def acquire(self, keys, stream=0, raise_on_error=True):
+    def acquire(self, keys, stream=0, raise_on_error=True, split=False):
+        """split=True: k3moe_cache_acquire_split (misses usable only after
+        wait_copies)."""
         keys = np.ascontiguousarray(keys, np.int64)
         n = keys.size
         out = (ctypes.c_void_p * n)()
         hit = np.zeros(n, np.uint8)
-        st = lib().k3moe_cache_acquire(self.h, keys.ctypes.data, n,
-                                       ctypes.cast(out, ctypes.c_void_p), hit.ctypes.data, stream)
+        name = "k3moe_cache_acquire_split" if split else "k3moe_cache_acquire"
+        st = getattr(lib(), name)(self.h, keys.ctypes.data, n,
+                                  ctypes.cast(out, ctypes.c_void_p), hit.ctypes.data, stream)
         if raise_on_error:
-            check(st, "k3moe_cache_acquire")
+            check(st, name)
         return [out[i] for i in range(n)], hit, st
+
+    def wait_copies(self, stream=0):
+        return lib().k3moe_cache_wait_copies(self.h, stream)
+
+    def wait_copy(self, blob_ptr, stream=0):
+        return lib().k3moe_cache_wait_copy(self.h, blob_ptr, stream)
 
     def release(self, stream=0):
         return check(lib().k3moe_cache_release(self.h, stream), "k3moe_cache_release")

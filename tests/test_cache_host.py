@@ -168,3 +168,66 @@ def test_refusals():
     _, _, st = c.acquire([4], raise_on_error=False)
     assert st == k.K3MOE_EINVAL
     assert c.pin(7) == k.K3MOE_EINVAL
+
+
+def test_split_acquire_defers_the_waits_and_keeps_the_plan():
+    """k3moe_cache_acquire_split: the same slots, copies and counters as the
+    plain acquire, but the misses' waits come only with wait_copies (or with
+    the next acquire / release), and until then their keys are INFLIGHT."""
+    ca, cpa = make_cache(1, 64, 8)
+    cb, cpb = make_cache(1, 64, 8)
+    batches = [[0, 1, 2, 3], [2, 3, 4, 5], [6, 7, 8, 9], [0, 9, 10, 11]]
+    for b in batches:
+        pa, ha, _ = ca.acquire(b)
+        nw = len(cpb.waits)
+        pb, hb, _ = cb.acquire(b, split=True)
+        misses = int((hb == 0).sum())
+        assert len(cpb.waits) == nw  # no wait yet
+        assert cb.stats()["inflight"] == misses
+        for key, h in zip(b, hb):
+            assert (cb.slot_of(key) >= 0) == bool(h)
+        assert cb.wait_copies() == 0
+        assert len(cpb.waits) == nw + misses
+        assert cb.stats()["inflight"] == 0
+        assert list(ha) == list(hb)
+        assert [ca.slot_of(x) for x in b] == [cb.slot_of(x) for x in b]
+        for key, p in zip(b, pb):
+            assert ctypes.string_at(p, 1)[0] == key % 251
+        ca.release()
+        cb.release()
+    assert [s for s, _, _ in cpa.copies] == [s for s, _, _ in cpb.copies]
+    assert cpa.waits == cpb.waits
+    assert ca.stats() == cb.stats()
+
+
+def test_release_and_the_next_acquire_wait_for_pending_copies():
+    c, cp = make_cache(1, 64, 8)
+    _, hit, _ = c.acquire([0, 1, 2], split=True)
+    assert cp.waits == [] and c.stats()["inflight"] == 3
+    c.release()  # publishes before marking the slots free
+    assert sorted(cp.waits) == sorted(s for s, _, _ in cp.copies)
+    assert len(cp.releases) == 3 and c.stats()["inflight"] == 0
+    _, _, _ = c.acquire([3], split=True)
+    # a second split acquire of the pending key finds it as a hit, not a miss
+    _, hit, _ = c.acquire([3, 0], split=True)
+    assert list(hit) == [1, 1] and len(cp.copies) == 4
+    assert c.stats()["inflight"] == 0
+    c.release()
+
+
+def test_wait_copy_waits_for_one_slot():
+    c, cp = make_cache(1, 64, 8)
+    c.acquire([0, 1])
+    c.release()
+    ptrs, hit, _ = c.acquire([0, 5, 6], split=True)
+    assert list(hit) == [1, 0, 0] and cp.waits == [cp.copies[0][0], cp.copies[1][0]]
+    n0 = len(cp.waits)
+    assert c.wait_copy(ptrs[0]) == 0 and len(cp.waits) == n0  # a hit: nothing to wait for
+    assert c.wait_copy(ptrs[2]) == 0
+    assert cp.waits[n0:] == [c.slot_of(6)] and c.slot_of(5) == -1
+    assert c.stats()["inflight"] == 1
+    assert c.wait_copy(ptrs[2]) == 0 and len(cp.waits) == n0 + 1  # already waited for
+    assert c.wait_copy(ptrs[1] + 1) == k.K3MOE_EINVAL  # not a slot start
+    assert c.wait_copy(ptrs[1]) == 0 and c.slot_of(5) >= 0
+    assert c.stats()["inflight"] == 0
+    c.release()
