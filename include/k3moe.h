@@ -266,16 +266,33 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int x_dtype, int32_t T, f
  *                      largest magnitude; 2 for bf16 tokens, exact but for
  *                      elements below about 2^-10 of that magnitude).
  *                      Default 1.
+ *  K3MOE_OPT_MX        batch-1 forwards of a layer with a resident expert
+ *                      table run the expert products on the block-scaled
+ *                      tensor cores (tcgen05.mma kind::mxf4): the packed
+ *                      E2M1 planes and their E8M0 scales are the A operand
+ *                      as stored, with no decode; the activations (and h)
+ *                      are the B operand as 16 E2M1 pieces per 32-block
+ *                      with one E8M0 scale each, exact in fp32 to below
+ *                      2e-8 of the block's largest magnitude; fp32
+ *                      accumulation; the weighted combine in a fixed order.
+ *                      Needs d % 512 == 0, f % 512 == 0, d <= 8192,
+ *                      f <= 2048, top_k <= 16.  Takes precedence over
+ *                      K3MOE_OPT_FUSED_T1.  Default 1.
  * k3moe_layer_fused_t1 returns 1 when a batch-1 fp32 forward of this layer
- * would run fused, else 0 (negative on error).  After a device-side timeout
+ * would run fused (the block-scaled path is off or unsupported), else 0
+ * (negative on error).  After a device-side timeout
  * (k3moe_device_error() == K3MOE_ETIMEOUT) a layer must be recreated.
  */
 #define K3MOE_OPT_FUSED_T1 1
 #define K3MOE_OPT_ACT_F16  2
 #define K3MOE_OPT_TC       4
 #define K3MOE_OPT_TC_E4M3  8
+#define K3MOE_OPT_MX       16
 int k3moe_layer_set_option(k3moe_layer *L, int32_t option, int32_t value);
 int k3moe_layer_fused_t1(const k3moe_layer *L);
+/* 1 when a batch-1 forward of this layer runs on the block-scaled tensor
+ * cores (K3MOE_OPT_MX set and the layer supports it), else 0. */
+int k3moe_layer_mx_t1(const k3moe_layer *L);
 
 /*
  * Timing hook: when set, every later k3moe_layer_forward records

@@ -40,7 +40,17 @@ int launch_down_t1(const float *h, const ExpertSrc &src, const float *w, int k, 
 int route_t1_splits(int d);
 int launch_route_t1(const void *x, int xdt, const uint16_t *Wr, int E, int d, float *part,
                     float *logits, const float *bias, int k, int32_t *ids, float *w,
-                    unsigned *ticket, float eps, float *u, cudaStream_t s);
+                    unsigned *ticket, float eps, float *u, uint8_t *ximg, float *r_out,
+                    float *zero_out, cudaStream_t s);
+bool mx_supported(int E, int k, int d, int f);
+size_t mx_part_floats(int k, int d, int f);
+size_t mx_ximg_bytes(int d);
+size_t mx_himg_bytes(int k, int f);
+size_t mx_cnt_words(int k, int d, int f);
+int mx_make_maps(const DevExpert *host_table, int E, int d, int f, void *dev_maps);
+int launch_mx_t1(const void *maps, const int32_t *ids, const float *w, const uint8_t *ximg, const float *rscale,
+                 uint8_t *himg, float *part, unsigned *cnt, int k, int d, int f, float *out, int *err,
+                 cudaStream_t s);
 int route_multi_nsplit(int T, int E, int d);
 int launch_route_multi(const void *X, int xdt, int T, const uint16_t *Wr, int E, int d,
                        float *part, int nsplit, float *logits, const float *bias, int k,
@@ -275,6 +285,14 @@ struct k3moe_layer {
     float *tscale;       // [maxT] token scales of the e4m3 pieces
     float *hf;           // [maxT * k * f] h in fp32 (e4m3 down)
     unsigned *hmax;      // [maxT * k] per-pair max |h| bits (e4m3 down)
+    // block-scaled tensor-core path of one token (kind::mxf4)
+    bool mx;             // K3MOE_OPT_MX (default on where supported)
+    bool mx_ready;       // its buffers and tensor maps exist
+    void *mx_maps;       // [E][6] tensor maps: packed and scale planes
+    uint8_t *mx_ximg;    // pieces of x: B image + scale atoms
+    uint8_t *mx_himg;    // pieces of h per selected expert
+    float *mx_part;      // split-tile partial sums
+    unsigned *mx_cnt;    // tile tickets (zero between launches)
 };
 
 static void layer_free(k3moe_layer *L)
@@ -282,7 +300,8 @@ static void layer_free(k3moe_layer *L)
     if (!L) return;
     void *ptrs[] = {L->table, L->logits, L->part,  L->ids,     L->w,      L->h,    L->Y,
                     L->offsets, L->perm, L->items, L->n_items, L->ticket, L->ctr,
-                    L->tc_tiles, L->tc_ntiles, L->Xg, L->Hg, L->tc_maps, L->tscale, L->hf, L->hmax};
+                    L->tc_tiles, L->tc_ntiles, L->Xg, L->Hg, L->tc_maps, L->tscale, L->hf, L->hmax,
+                    L->mx_maps, L->mx_ximg, L->mx_himg, L->mx_part, L->mx_cnt};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete L;
@@ -349,6 +368,15 @@ int k3moe_layer_create(k3moe_layer **out, const k3moe_layer_desc *D)
         L->tc_ready = ok;
         L->tc = true;
     }
+    if (D->host_experts && k3::mx_supported(L->E, L->k, L->d, L->f)) {
+        alloc(&L->mx_maps, k3::tc_map_bytes() * 6 * L->E);
+        alloc((void **)&L->mx_ximg, k3::mx_ximg_bytes(L->d));
+        alloc((void **)&L->mx_himg, k3::mx_himg_bytes(L->k, L->f));
+        alloc((void **)&L->mx_part, sizeof(float) * k3::mx_part_floats(L->k, L->d, L->f));
+        alloc((void **)&L->mx_cnt, sizeof(unsigned) * k3::mx_cnt_words(L->k, L->d, L->f));
+        L->mx_ready = ok;
+        L->mx = true;
+    }
     L->fused = true;
     L->act16 = false;
     if (!ok) {
@@ -374,6 +402,15 @@ int k3moe_layer_create(k3moe_layer **out, const k3moe_layer_desc *D)
         L->e4m3_ok = k3::tc_e4m3_eligible(L->table, L->E, L->d, L->f, 0) == 1;
         L->e4m3 = L->e4m3_ok;
     }
+    if (st == cudaSuccess && L->mx_ready) {
+        if (k3::mx_make_maps(tmp, L->E, L->d, L->f, L->mx_maps) != K3MOE_OK) {
+            L->mx_ready = false;  // the fused CUDA-core kernel serves instead
+        } else {
+            st = cudaMemset(L->mx_cnt, 0, sizeof(unsigned) * k3::mx_cnt_words(L->k, L->d, L->f));
+            if (st == cudaSuccess) st = cudaMemset(L->mx_ximg, 0, k3::mx_ximg_bytes(L->d));
+            if (st == cudaSuccess) st = cudaMemset(L->mx_himg, 0, k3::mx_himg_bytes(L->k, L->f));
+        }
+    }
     free(tmp);
     if (st == cudaSuccess) st = cudaMemset(L->ticket, 0, sizeof(unsigned));
     if (st == cudaSuccess)
@@ -398,7 +435,7 @@ static int route_into(k3moe_layer *L, const void *X, int xdt, int32_t T, cudaStr
 {
     if (T == 1)
         return k3::launch_route_t1(X, xdt, L->Wr, L->E, L->d, L->part, L->logits, L->bias, L->k,
-                                   L->ids, L->w, L->ticket, 0.f, nullptr, s);
+                                   L->ids, L->w, L->ticket, 0.f, nullptr, nullptr, nullptr, nullptr, s);
     return k3::launch_route_multi(X, xdt, T, L->Wr, L->E, L->d, L->part, L->nsplit, L->logits,
                                   L->bias, L->k, L->ids, L->w, s);
 }
@@ -427,6 +464,22 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int xdt, int32_t T, float
         return K3MOE_EINVAL;
     cudaStream_t st = cs(s);
     if (L->nev) K3_CUDA(cudaEventRecord(L->ev[0], st));
+    if (T == 1 && L->mx && L->mx_ready) {
+        // router + pieces of x, then the block-scaled gate/up and down phases
+        K3_TRY(k3::launch_route_t1(X, xdt, L->Wr, L->E, L->d, L->part, L->logits, L->bias, L->k, L->ids, L->w,
+                                   L->ticket, 0.f, nullptr, L->mx_ximg, nullptr, out, st));
+        if (L->nev) K3_CUDA(cudaEventRecord(L->ev[1], st));
+        K3_TRY(k3::launch_mx_t1(L->mx_maps, L->ids, L->w, L->mx_ximg, nullptr, L->mx_himg, L->mx_part, L->mx_cnt,
+                                L->k, L->d, L->f, out, k3::device_error_word(), st));
+        if (L->nev) {
+            K3_CUDA(cudaEventRecord(L->ev[2], st));
+            K3_CUDA(cudaEventRecord(L->ev[3], st));
+        }
+        if (ids_out)
+            K3_CUDA(cudaMemcpyAsync(ids_out, L->ids, sizeof(int32_t) * L->k, cudaMemcpyDeviceToDevice, st));
+        if (w_out) K3_CUDA(cudaMemcpyAsync(w_out, L->w, sizeof(float) * L->k, cudaMemcpyDeviceToDevice, st));
+        return K3MOE_OK;
+    }
     if (T == 1 && xdt == K3MOE_F32 && k3moe_layer_fused_t1(L) == 1) {
         K3_TRY(k3::launch_fused_t1((const float *)X, L->Wr, L->bias, L->table, L->E, L->k, L->d,
                                    L->f, L->logits, L->ids, L->w, L->h, L->Y, out, L->ctr,
@@ -505,13 +558,24 @@ int k3moe_layer_set_option(k3moe_layer *L, int32_t option, int32_t value)
         L->e4m3 = value != 0;
         return K3MOE_OK;
     }
+    if (option == K3MOE_OPT_MX) {
+        L->mx = value != 0;
+        return K3MOE_OK;
+    }
     return K3MOE_EINVAL;
 }
 
 int k3moe_layer_fused_t1(const k3moe_layer *L)
 {
     if (!L) return K3MOE_EINVAL;
+    if (L->mx && L->mx_ready) return 0;  // the block-scaled path takes precedence
     return (L->fused && !L->router_only && k3::fused_t1_supported(L->E, L->k, L->d, L->f)) ? 1 : 0;
+}
+
+int k3moe_layer_mx_t1(const k3moe_layer *L)
+{
+    if (!L) return K3MOE_EINVAL;
+    return (L->mx && L->mx_ready) ? 1 : 0;
 }
 
 int k3moe_layer_set_events(k3moe_layer *L, void *const *host_events, int32_t n)
@@ -605,7 +669,7 @@ extern "C" int k3moe_stream_decode(const k3moe_stream_desc *D, const float *X, i
             k3moe_layer *L = D->host_layers[l];
             // RMSNorm folded into the router: u = x / sqrt(mean(x^2) + eps)
             int r = k3::launch_route_t1(xcur, K3MOE_F32, L->Wr, E, d, L->part, L->logits, L->bias,
-                                        k, L->ids, L->w, L->ticket, D->eps, u, st);
+                                        k, L->ids, L->w, L->ticket, D->eps, u, nullptr, nullptr, nullptr, st);
             if (r != K3MOE_OK) {
                 fail(r);
                 break;

@@ -1,0 +1,703 @@
+// k3_mx.cu -- batch-1 expert products on the block-scaled tensor cores.
+//
+// The pages' expert weights are E2M1 codes with one E8M0 scale per 32
+// ("kimi-k3-in-c" explainer, "Reduction one"), which is exactly the operand
+// format of tcgen05.mma kind::mxf4 (block_scale, scale_vec::2X): packed
+// E2M1 A and B in shared memory, one E8M0 scale per row and 32 of K in TMEM.
+// So the packed planes go from HBM to the tensor core by TMA with no decode
+// at all, and the fp32 activations become the B operand as a sum of E2M1
+// pieces:
+//
+//   v = sum_p q_p * 2^(s_p)      per 32-block of v, p = 0..15
+//
+// where piece p rounds the residual r_p = v - (pieces so far) to the E2M1
+// grid after scaling by 2^-s_p, s_p the smallest exponent with
+// 6 * 2^s_p >= max |r_p| over the block.  Every residual is exact in fp32
+// and shrinks by at least 3x per piece, so 16 pieces leave less than
+// 3^-16 (2e-8) of the block maximum.  The 16 pieces are the 16 columns of
+// one M = 128, N = 16 MMA; the epilogue adds the columns.
+//
+// Per token (one launch each, stream-ordered):
+//   router   (k3_route.cu) logits, top-k, and the pieces of x: a B image
+//            [K/256][16 rows][128 bytes], 128-byte swizzled, plus E8M0 scale
+//            atoms [K/128][512 bytes] in the layout tcgen05.cp copies to TMEM
+//   phase 0  gate and up rows of the k experts (tiles of 128 rows, K = d):
+//            g, u -> h = silu(r g) * (r u) (r = the RMSNorm factor or 1) ->
+//            the pieces of h per expert (B images of phase 1)
+//   phase 1  down rows (tiles of 128 rows, K = f): y_j -> out = sum_j w_j y_j
+// Both phases split the k * rows/128 tiles' K steps evenly over one CTA per
+// SM (a tile may be split between CTAs); a split tile's partial sums meet in
+// a workspace and the CTA that completes the tile (an acq_rel ticket) adds
+// them in a fixed order, so results do not depend on timing.
+//
+// A weight group whose scale byte is 255 is dropped, as on the other paths:
+// its scale becomes 0 (2^-127), so it adds at most 6 * 2^-127 * sum |v| of
+// its block, far below the fp32 resolution of any nonzero output.
+//
+// CTA: 8 warps.  warp 0 TMA producer (weight tiles 128 rows x 128 bytes,
+// scale boxes 128 rows x 16 bytes), warp 1 MMA issuer and TMEM owner, warp
+// 2 turns scale boxes into tcgen05.cp atoms, warps 4-7 epilogue (TMEM lane
+// quadrants 0-3).  Every wait is bounded; a timeout sets the device error
+// word and the CTA drains and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdlib>
+
+#include "k3_mx.cuh"
+#include "k3_tcgen05.cuh"
+
+namespace k3 {
+
+constexpr int MX_M = 128;       // weight rows per tile
+constexpr int MX_UK = 256;      // K per unit: 128 packed bytes per row, 4 MMAs
+constexpr int MX_THREADS = 256;
+constexpr int MX_W_PROD = 0, MX_W_MMA = 1, MX_W_PERM = 2, MX_W_BLD = 3, MX_W_EPI = 4;
+constexpr int MX_TMEM_COLS = 512;
+
+// Instruction descriptor of kind::mxf4 block_scale: E2M1 A and B (format 1,
+// bits 7-9 and 10-12), K-major, N = 16 (bits 17-22: N >> 3), UE8M0 scales
+// (bit 23), M = 128 (bits 24-28: M >> 4), the byte of the A and B scale
+// words that holds this MMA's first scale (bits 29-30 and 4-5).
+K3_DEV uint32_t mx_idesc(uint32_t ida, uint32_t idb)
+{
+    return (idb << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(MX_N >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(MX_M >> 4) << 24) | (ida << 29);
+}
+// One MMA, issued by the elected lane of a converged warp.
+K3_DEV void mx_mma(uint32_t td, uint32_t alo, uint32_t blo, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                   uint32_t acc)
+{
+    asm volatile("{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "mov.b64 da, {%1, %7};\n\tmov.b64 db, {%2, %7};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], da, db, %3, [%5], [%6], p;\n\t}"
+                 ::"r"(td), "r"(alo), "r"(blo), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb), "r"(SW128_HI)
+                 : "memory");
+}
+// Copies one 512-byte scale atom (32 rows x 16 bytes, no swizzle) from shared
+// memory to TMEM columns taddr .. taddr+3 of lanes 0-31, repeated in the
+// other three lane quadrants.
+K3_DEV void mx_cp_atom(uint32_t taddr, uint32_t saddr)
+{
+    const uint32_t lo = ((saddr & 0x3FFFFu) >> 4) | (1u << 16), hi = (128u >> 4) | (1u << 14);
+    asm volatile("{\n\t.reg .pred e;\n\t.reg .b64 d;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "mov.b64 d, {%1, %2};\n\t@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], d;\n\t}" ::"r"(taddr),
+                 "r"(lo), "r"(hi)
+                 : "memory");
+}
+K3_DEV uint32_t lds32(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+K3_DEV void sts32(uint32_t a, uint32_t v) { asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory"); }
+// Named barrier of the four epilogue warps.  The non-aligned form: a lane
+// that arrives after the others of its warp (the leader after its ticket)
+// is counted as itself, not as another arrival of the whole warp.
+K3_DEV void red_add_f32(float *p, float v) { asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory"); }
+K3_DEV void mx_bar_epi() { asm volatile("barrier.sync 2, 128;" ::: "memory"); }
+K3_DEV unsigned ticket_add(unsigned *p, unsigned v)
+{
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+struct MxArgs {
+    const CUtensorMap *maps;  // [E][6]: gate, up, down packed planes; gate, up, down scale planes
+    const int32_t *ids;       // [k]
+    const float *w;           // [k] combine weights (phase 1)
+    const uint8_t *bimg;      // phase 0: x pieces [d/256][16][128]; phase 1: h pieces, per slot j
+    const uint8_t *bsf;       // phase 0: x scale atoms [d/128][512]; phase 1: per slot j
+    const float *rscale;      // phase 0: RMSNorm factor, or null for 1
+    uint8_t *himg, *hsf;      // phase 0 output: h pieces per slot j (f * 8 and f / 128 * 512 bytes)
+    float *part;              // split-tile partials [tiles][units per tile][128][NMAT]
+    float *out;               // phase 1: [d], added into
+    unsigned *cnt;            // phase 0: [tiles] tickets; phase 1: [d / 128] row-tile tickets
+    int k, d, f;
+    int *err;
+};
+
+template <int PH>
+struct MxCfg {
+    static constexpr int NMAT = PH == 0 ? 2 : 1;
+    static constexpr int A_BYTES = MX_M * 128;           // one matrix, one unit
+    static constexpr int SC_BYTES = MX_M * 16;           // scale box
+    static constexpr int AT_BYTES = 2 * 512;             // two atoms per matrix per unit
+    static constexpr int STAGE = NMAT * (A_BYTES + SC_BYTES + AT_BYTES);
+    static constexpr int NS = PH == 0 ? 4 : 9;
+    // TMEM columns: accumulators from 0, A scale slots from TSA, B scales from TSB
+    static constexpr int TSA = PH == 0 ? 64 : 32, TSB = PH == 0 ? 128 : 112;
+    static constexpr int TMEM_COLS = 512;
+    static_assert(NMAT * 2 * MX_N <= TSA && NS * NMAT * 8 <= TSB - TSA, "TMEM layout");
+};
+
+// Shared memory of one phase: [stages][B images][scale atom staging (phase 1)].
+// The phases overlap; the barriers of both follow the larger layout.
+template <int PH>
+static size_t mx_layout_bytes(int K)
+{
+    using C = MxCfg<PH>;
+    const size_t b = PH == 0 ? (size_t)K * 8 : 2 * (size_t)K * 8;
+    const size_t sf = PH == 0 ? 0 : 2 * (size_t)(K / 128) * 512;
+    return (size_t)C::NS * C::STAGE + b + sf;
+}
+static size_t mx_bar_off(int d, int f) { return std::max(mx_layout_bytes<0>(d), mx_layout_bytes<1>(f)); }
+static size_t mx_smem(int d, int f) { return 1024 + mx_bar_off(d, f) + 1024; }
+
+// Barriers of one phase: full, atoms-full, empty per stage; accumulator
+// full / empty per TMEM buffer; B image loaded (two experts at most);
+// B scales in TMEM; all MMAs done.
+template <int PH>
+struct MxBars {
+    static constexpr int NS = MxCfg<PH>::NS;
+    static constexpr int FULL = 0, AFULL = NS, EMPTY = 2 * NS, ACCF = 3 * NS, ACCE = ACCF + 2, BLOAD = ACCE + 2,
+                         BSCL = BLOAD + 2, FIN = BSCL + 1, N = FIN + 1;
+};
+template <int PH>
+K3_DEV void mx_init_bars(uint64_t *bars)
+{
+    using Bs = MxBars<PH>;
+    for (int i = 0; i < Bs::NS; i++) {
+        mbar_init(smem_addr(bars + Bs::FULL + i), 1);
+        mbar_init(smem_addr(bars + Bs::AFULL + i), 1);
+        mbar_init(smem_addr(bars + Bs::EMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; i++) {
+        mbar_init(smem_addr(bars + Bs::ACCF + i), 1);
+        mbar_init(smem_addr(bars + Bs::ACCE + i), 4);
+        mbar_init(smem_addr(bars + Bs::BLOAD + i), 1);
+    }
+    mbar_init(smem_addr(bars + Bs::BSCL), 1);
+    mbar_init(smem_addr(bars + Bs::FIN), 1);
+}
+
+// Bounded wait until *p >= target (acquire); false after the time limit.
+K3_DEV bool mx_wait_count(const unsigned *p, unsigned target, int *err)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        __nanosleep(64);
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        if (v >= target) return true;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            set_device_error(err, K3MOE_ETIMEOUT);
+            return false;
+        }
+    }
+}
+
+// One phase on this CTA's share of the units.  sm: the 1024-aligned shared
+// memory (phase layouts overlap: the phases run one after the other),
+// bars: this phase's barriers, hready[j]: h tiles of expert slot j done.
+template <int PH>
+K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem, volatile int *abort_flag,
+                    unsigned *s_last, unsigned *s_stop, unsigned *hready)
+{
+    using C = MxCfg<PH>;
+    using Bs = MxBars<PH>;
+    constexpr int NMAT = C::NMAT, NS = C::NS;
+    const uint32_t sbase = smem_addr(sm);
+    const int K = PH == 0 ? a.d : a.f, ROWS = PH == 0 ? a.f : a.d;
+    const uint32_t b_off = (uint32_t)(NS * C::STAGE);
+    const uint32_t bimg_bytes = (uint32_t)K * 8u, bsf_bytes = (uint32_t)(K / 128) * 512u;
+    const uint32_t sf_off = b_off + (PH == 0 ? bimg_bytes : 2 * bimg_bytes);
+    const int B_FULL = Bs::FULL, B_AFULL = Bs::AFULL, B_EMPTY = Bs::EMPTY, B_ACCF = Bs::ACCF, B_ACCE = Bs::ACCE,
+              B_BLOAD = Bs::BLOAD, B_BSCL = Bs::BSCL, B_FIN = Bs::FIN;
+    auto bar = [&](int i) { return smem_addr(bars + i); };
+    auto a_at = [&](int s, int m) { return sbase + (uint32_t)(s * C::STAGE + m * C::A_BYTES); };
+    auto sc_at = [&](int s, int m) { return sbase + (uint32_t)(s * C::STAGE + NMAT * C::A_BYTES + m * C::SC_BYTES); };
+    auto at_at = [&](int s, int m) {
+        return sbase + (uint32_t)(s * C::STAGE + NMAT * (C::A_BYTES + C::SC_BYTES) + m * C::AT_BYTES);
+    };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tpe = ROWS / MX_M;  // tiles per expert
+    const int upt = K / MX_UK;    // units per tile
+    const int ntiles = a.k * tpe;
+    const long U = (long)ntiles * upt, G = gridDim.x;
+    const long ulo = U * blockIdx.x / G, uhi = U * (blockIdx.x + 1) / G;
+    auto cta_of = [&](long u) { return (long)(((u + 1) * G - 1) / U); };
+
+    // the experts of this CTA's range (phase 1 loads one B image per expert;
+    // a range spans at most two experts, checked at launch)
+    const int j_first = ulo < uhi ? (int)((ulo / upt) / tpe) : 0;
+    const int j_last = ulo < uhi ? (int)(((uhi - 1) / upt) / tpe) : -1;
+
+    if (ulo < uhi && warp == MX_W_PROD) {
+        // ---------------------------------------------------- TMA producer
+        uint32_t issued[NS];
+#pragma unroll
+        for (int i = 0; i < NS; i++) issued[i] = 0;
+        if (lane == 0) {
+            bool ok = true;
+            // B operand images
+            if (PH == 0) {
+                mbar_arrive_expect_tx(bar(B_BLOAD), bimg_bytes + bsf_bytes);
+                for (uint32_t o = 0; o < bimg_bytes; o += 16384)
+                    bulk_g2s(sbase + b_off + o, a.bimg + o, min(16384u, bimg_bytes - o), bar(B_BLOAD));
+                for (uint32_t o = 0; o < bsf_bytes; o += 16384)  // staged in the last stage
+                    bulk_g2s(sbase + (uint32_t)((NS - 1) * C::STAGE) + o, a.bsf + o, min(16384u, bsf_bytes - o),
+                             bar(B_BLOAD));
+            }
+            uint32_t it = 0;
+            int cur_tile = -1;
+            const CUtensorMap *mp = nullptr;
+            int t = 0;
+            for (long u = ulo; u < uhi && ok && !*abort_flag; u++, it++) {
+                const int tile = (int)(u / upt), uu = (int)(u % upt);
+                if (tile != cur_tile) {
+                    cur_tile = tile;
+                    const int e = __ldg(a.ids + tile / tpe);
+                    mp = a.maps + 6 * (size_t)e;
+                    t = tile % tpe;
+                }
+                const int s = it % NS;
+                if (it >= (uint32_t)NS && !tc_wait(bar(B_EMPTY + s), ((it / NS) - 1) & 1, a.err, abort_flag)) break;
+                // phase 0: the last stage holds the B scale atoms until they are in TMEM
+                if (PH == 0 && it == (uint32_t)(NS - 1) && !tc_wait(bar(B_BSCL), 0, a.err, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(bar(B_FULL + s), NMAT * (C::A_BYTES + C::SC_BYTES));
+                issued[s]++;
+#pragma unroll
+                for (int m = 0; m < NMAT; m++) {
+                    const int pm = PH == 0 ? m : 2;
+                    tma_load_2d(a_at(s, m), mp + pm, uu * 128, t * MX_M, bar(B_FULL + s));
+                    tma_load_2d(sc_at(s, m), mp + 3 + pm, 16 * (uu >> 1), t * MX_M, bar(B_FULL + s));
+                }
+            }
+            // drain: every copy issued here has landed before the CTA exits
+            for (int s = 0; s < NS; s++)
+                if (issued[s]) mbar_wait(bar(B_FULL + s), (issued[s] - 1) & 1, a.err);
+            if (PH == 0) mbar_wait(bar(B_BLOAD), 0, a.err);
+        }
+        __syncwarp();
+    } else if (PH == 1 && ulo < uhi && warp == MX_W_BLD) {
+        // ------------------------------- h pieces of this CTA's experts (phase 1)
+        // once every h tile of expert slot j is written (acquire), copied with
+        // plain loads (they were written by plain stores of other CTAs) into
+        // the B buffer, then made visible to the tensor core's proxy
+        for (int x = 0; x <= j_last - j_first && !*abort_flag; x++) {
+            const int j = j_first + x;
+            bool ok = true;
+            if (lane == 0) ok = mx_wait_count(hready + j, (unsigned)(a.f / MX_M), a.err);  // h tiles of one expert
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+                *abort_flag = 1;
+                break;
+            }
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.bimg + (size_t)j * bimg_bytes);
+            for (uint32_t i = lane; i < bimg_bytes / 16; i += 32) {
+                const uint4 v = __ldcg(src + i);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + b_off + x * bimg_bytes + 16 * i),
+                             "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                             : "memory");
+            }
+            const uint4 *ssrc = reinterpret_cast<const uint4 *>(a.bsf + (size_t)j * bsf_bytes);
+            for (uint32_t i = lane; i < bsf_bytes / 16; i += 32) {
+                const uint4 v = __ldcg(ssrc + i);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + sf_off + x * bsf_bytes + 16 * i),
+                             "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                             : "memory");
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_BLOAD + x));
+        }
+    } else if (ulo < uhi && warp == MX_W_PERM) {
+        // ------------------------------------- scale boxes -> tcgen05.cp atoms
+        // atom byte 16 r0 + 4 r1 + kb = scale of row r0 + 32 r1, k-block kb
+        uint32_t it = 0;
+        for (long u = ulo; u < uhi && !*abort_flag; u++, it++) {
+            const int uu = (int)(u % upt), s = it % NS;
+            if (!__all_sync(0xffffffffu, tc_wait(bar(B_FULL + s), (it / NS) & 1, a.err, abort_flag))) break;
+#pragma unroll
+            for (int m = 0; m < NMAT; m++)
+#pragma unroll
+                for (int at = 0; at < 2; at++)
+#pragma unroll
+                    for (int r1 = 0; r1 < 4; r1++) {
+                        uint32_t v = lds32(sc_at(s, m) + (uint32_t)((lane + 32 * r1) * 16 + 8 * (uu & 1) + 4 * at));
+                        v &= ~__vcmpeq4(v, 0xffffffffu);  // 255 (a dropped group) -> 2^-127
+                        sts32(at_at(s, m) + (uint32_t)(at * 512 + 16 * lane + 4 * r1), v);
+                    }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_AFULL + s));
+        }
+    } else if (ulo < uhi && warp == MX_W_MMA) {
+        // ------------------------------------------------------ MMA issuer
+        bool ok = true;
+        if (PH == 0) {
+            ok = __all_sync(0xffffffffu, tc_wait(bar(B_BLOAD), 0, a.err, abort_flag));
+            if (ok) {
+                tc_fence_after();
+                for (int at = 0; at < K / 128; at++)
+                    mx_cp_atom(tmem + C::TSB + 4 * at, sbase + (uint32_t)((NS - 1) * C::STAGE + 512 * at));
+                mma_commit(bar(B_BSCL));
+            }
+        }
+        uint32_t it = 0, sg = 0;
+        int bx = -1;  // phase 1: B buffer of the current expert
+        for (long u = ulo; u < uhi && ok && !*abort_flag; u++, it++) {
+            const int tile = (int)(u / upt), uu = (int)(u % upt);
+            const bool first = (u == ulo) || uu == 0, last = (u + 1 == uhi) || uu == upt - 1;
+            if (PH == 1 && tile / tpe - j_first != bx) {
+                bx = tile / tpe - j_first;
+                if (!__all_sync(0xffffffffu, tc_wait(bar(B_BLOAD + bx), 0, a.err, abort_flag))) break;
+                tc_fence_after();
+                for (int at = 0; at < K / 128; at++)
+                    mx_cp_atom(tmem + C::TSB + (uint32_t)(bx * (K / 32) + 4 * at),
+                               sbase + sf_off + (uint32_t)(bx * bsf_bytes + 512 * at));
+            }
+            const int buf = sg & 1;
+            if (first && sg >= 2 &&
+                !__all_sync(0xffffffffu, tc_wait(bar(B_ACCE + buf), ((sg / 2) - 1) & 1, a.err, abort_flag)))
+                break;
+            const int s = it % NS;
+            if (!__all_sync(0xffffffffu, tc_wait(bar(B_AFULL + s), (it / NS) & 1, a.err, abort_flag))) break;
+            tc_fence_after();
+            const uint32_t tsa = tmem + C::TSA + (uint32_t)(s * NMAT * 8);
+#pragma unroll
+            for (int m = 0; m < NMAT; m++) {
+                mx_cp_atom(tsa + m * 8, at_at(s, m));
+                mx_cp_atom(tsa + m * 8 + 4, at_at(s, m) + 512);
+            }
+            const uint32_t bimg = sbase + b_off + (uint32_t)((PH == 1 ? bx : 0) * bimg_bytes);
+            const uint32_t tsb = tmem + C::TSB + (uint32_t)((PH == 1 ? bx : 0) * (K / 32));
+#pragma unroll
+            for (int q4 = 0; q4 < 4; q4++) {
+                const int q = uu * 4 + q4;  // K step of 64 within the tile's K
+                const uint32_t blo = sw128_lo(bimg + (uint32_t)((q >> 2) * (MX_N * 128))) + 2u * (uint32_t)(q & 3);
+                const uint32_t idesc = mx_idesc(2u * (q4 & 1), 2u * (q & 1));
+                const uint32_t sfb = tsb + 4u * (uint32_t)(q >> 1);
+#pragma unroll
+                for (int m = 0; m < NMAT; m++)
+                    mx_mma(tmem + (uint32_t)(buf * NMAT * MX_N + m * MX_N), sw128_lo(a_at(s, m)) + 2u * q4, blo, idesc,
+                           tsa + m * 8 + 4 * (q4 >> 1), sfb, (first && q4 == 0) ? 0u : 1u);
+            }
+            mma_commit(bar(B_EMPTY + s));
+            if (last) {
+                mma_commit(bar(B_ACCF + buf));
+                sg++;
+            }
+        }
+        // every MMA and copy issued above has completed before TMEM is freed
+        mma_commit(bar(B_FIN));
+        mbar_wait(bar(B_FIN), 0, a.err);
+        __syncwarp();
+    } else if (ulo < uhi && warp >= MX_W_EPI) {
+        // --------------------------------------------------------- epilogue
+        // The four warps run the same segments and meet at the same named
+        // barriers (bar 2): whether to go on is decided by one thread and
+        // read by all between two barriers, so no warp can leave while the
+        // others wait.
+        const int qd = warp & 3, row = qd * 32 + lane;
+        const bool leader = threadIdx.x == MX_W_EPI * 32;
+        uint32_t sg = 0;
+        long u = ulo;
+        const float rr = (PH == 0 && a.rscale) ? __ldg(a.rscale) : 1.f;
+        int done_j[2] = {-1, -1}, done_n[2] = {0, 0};  // leader: h tiles finished per expert slot
+        for (;;) {
+            if (leader) *s_stop = (u >= uhi || *abort_flag) ? 1u : 0u;
+            mx_bar_epi();
+            const bool stop = *s_stop != 0u;
+            mx_bar_epi();
+            if (stop) break;
+            const int tile = (int)(u / upt);
+            const long t0 = (long)tile * upt, t1 = t0 + upt;
+            const long ua = u, ub = t1 < uhi ? t1 : uhi;
+            u = ub;
+            const int buf = sg & 1;
+            const bool ok = __all_sync(0xffffffffu, tc_wait(bar(B_ACCF + buf), (sg / 2) & 1, a.err, abort_flag));
+            float v[NMAT];
+#pragma unroll
+            for (int m = 0; m < NMAT; m++) v[m] = 0.f;
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int m = 0; m < NMAT; m++) {
+                    float c0[8], c1[8];
+                    const uint32_t ta = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(buf * NMAT * MX_N + m * MX_N);
+                    tmem_ld8(ta, c0);
+                    tmem_ld8(ta + 8, c1);
+                    tmem_wait_ld();
+                    float acc = c1[7];  // the smallest pieces first
+#pragma unroll
+                    for (int i = 6; i >= 0; i--) acc += c1[i];
+#pragma unroll
+                    for (int i = 7; i >= 0; i--) acc += c0[i];
+                    v[m] = acc;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_ACCE + buf));
+            }
+            sg++;
+            // a split tile's partial sums sit in slots indexed by the first
+            // unit of their segment
+            const bool whole = ua == t0 && ub == t1;
+            const int seg = (int)(ua - t0);
+            const int j = tile / tpe, t = tile % tpe;
+            if (PH == 0) {
+                float *pp = a.part + ((size_t)tile * upt) * MX_M * NMAT;
+                if (!whole && ua != t0) {
+                    // a later segment: the CTA holding the tile's first units
+                    // (at the end of its range, so it gets there last) finishes
+                    // the tile; publish this part for it
+#pragma unroll
+                    for (int m = 0; m < NMAT; m++) pp[((size_t)seg * MX_M + row) * NMAT + m] = v[m];
+                    __syncwarp();
+                    mx_bar_epi();
+                    if (leader) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.cnt + tile) : "memory");
+                    continue;
+                }
+                if (!whole) {
+                    // the first segment: wait for the others' parts (usually
+                    // published long before), add them in unit order
+                    int nother = 0;
+                    for (long us = ub; us < t1;) {
+                        const long ub2 = U * (cta_of(us) + 1) / G;
+                        us = ub2 < t1 ? ub2 : t1;
+                        nother++;
+                    }
+                    if (leader) *s_last = mx_wait_count(a.cnt + tile, (unsigned)nother, a.err) ? 1u : 0u;
+                    __syncwarp();
+                    mx_bar_epi();
+                    if (*s_last != 1u) *abort_flag = 1;
+                    for (long us = ub; us < t1;) {
+                        const long ub2 = U * (cta_of(us) + 1) / G, ue = ub2 < t1 ? ub2 : t1;
+#pragma unroll
+                        for (int m = 0; m < NMAT; m++) v[m] += __ldcg(pp + ((size_t)(us - t0) * MX_M + row) * NMAT + m);
+                        us = ue;
+                    }
+                    if (leader) a.cnt[tile] = 0;  // for the next launch
+                }
+                const float h = silu(rr * v[0]) * (rr * v[1]);
+                mx_encode_block(h, lane, (t * MX_M + qd * 32) / 32, a.himg + (size_t)j * a.f * 8,
+                                a.hsf + (size_t)j * (a.f / 128) * 512);
+                // h tiles done per expert slot, published together at the end
+                if (leader) {
+                    int q = 0;
+                    while (q < 2 && done_j[q] >= 0 && done_j[q] != j) q++;
+                    if (done_j[q] >= 0 && done_j[q] != j) {
+                        set_device_error(a.err, K3MOE_EINVAL);  // a range spans at most two experts
+                        *abort_flag = 1;
+                    } else {
+                        done_j[q] = j;
+                        done_n[q]++;
+                    }
+                }
+            } else {
+                // w_j * (this segment's part of y_j) straight into out: the
+                // down product is linear, so split tiles need no exchange
+                red_add_f32(a.out + (size_t)t * MX_M + row, __ldg(a.w + j) * v[0]);
+            }
+        }
+        if (PH == 0) {
+            // every h piece this CTA wrote is in memory before the counts
+            __syncwarp();
+            mx_bar_epi();
+            if (leader)
+                for (int q = 0; q < 2; q++)
+                    if (done_n[q])
+                        asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(hready + done_j[q]),
+                                     "r"((unsigned)done_n[q])
+                                     : "memory");
+        }
+    }
+}
+
+// Both phases of one token in one persistent kernel (cooperative launch:
+// phase-1 CTAs wait for the h tiles that other CTAs finish in phase 0).
+__global__ void __launch_bounds__(MX_THREADS, 1)
+    k3_mx_layer(const MxArgs a0, const MxArgs a1, unsigned *hready, unsigned *exit_cnt, uint32_t bar_off)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars0 = (uint64_t *)(sm + bar_off);
+    uint64_t *bars1 = bars0 + MxBars<0>::N;
+    uint32_t *tmem_slot = (uint32_t *)(bars1 + MxBars<1>::N);
+    volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+    unsigned *s_last = (unsigned *)(tmem_slot + 2);  // epilogue: this CTA completes the tile
+    unsigned *s_stop = (unsigned *)(tmem_slot + 3);  // epilogue: no further segment
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        mx_init_bars<0>(bars0);
+        mx_init_bars<1>(bars1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == MX_W_MMA) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(MX_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *(volatile uint32_t *)tmem_slot;
+
+    mx_body<0>(a0, sm, bars0, tmem, abort_flag, s_last, s_stop, hready);
+    // every role of phase 0 is done here (its MMAs completed, its copies
+    // landed): the shared memory and TMEM are phase 1's
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    mx_body<1>(a1, sm, bars1, tmem, abort_flag, s_last, s_stop, hready);
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == MX_W_MMA) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(MX_TMEM_COLS)
+                     : "memory");
+    }
+    // the last CTA out clears the h counters (no CTA reads them any more)
+    if (threadIdx.x == 0 && ticket_add(exit_cnt, 1) == gridDim.x - 1) {
+        for (int j = 0; j < a0.k; j++) hready[j] = 0;
+        *exit_cnt = 0;
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+int num_sms();
+
+bool mx_supported(int E, int k, int d, int f)
+{
+    // phase 0 stages the B scale atoms of x in one stage; TMEM holds d / 32
+    // (phase 0) and 2 f / 32 (phase 1) columns of B scales
+    return E >= 1 && k >= 1 && k <= 16 && d % 512 == 0 && f % 512 == 0 && d <= 8192 && f <= 2048 &&
+           (d / 128) * 512 <= MxCfg<0>::STAGE && MxCfg<0>::TSB + d / 32 <= MxCfg<0>::TMEM_COLS &&
+           MxCfg<1>::TSB + 2 * (f / 32) <= MxCfg<1>::TMEM_COLS && mx_smem(d, f) <= 232448;
+}
+
+// partial-sum slots: one per unit of a tile (a segment writes the slot of
+// its first unit)
+size_t mx_part_floats(int k, int d, int f) { return (size_t)k * (f / MX_M) * (d / MX_UK) * MX_M * 2; }
+size_t mx_ximg_bytes(int d) { return (size_t)d * 8 + (size_t)(d / 128) * 512; }
+size_t mx_himg_bytes(int k, int f) { return (size_t)k * ((size_t)f * 8 + (size_t)(f / 128) * 512); }
+// counters: split phase-0 tiles' published parts, h tiles per expert slot, CTA exits
+size_t mx_cnt_words(int k, int d, int f) { (void)d; return (size_t)k * (f / MX_M) + k + 1; }
+
+// Tensor maps of E experts: [E][gate, up, down packed; gate, up, down scales]
+// (packed: rows x in/2 bytes, boxes 128 rows x 128 bytes, 128-byte swizzle;
+// scales: rows x in/32 bytes, boxes 128 rows x 16 bytes, no swizzle).
+int mx_make_maps(const DevExpert *host_table, int E, int d, int f, void *dev_maps)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn) {
+            cudaGetLastError();
+            return K3MOE_ECUDA;
+        }
+        encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    }
+    CUtensorMap *maps = (CUtensorMap *)malloc(sizeof(CUtensorMap) * 6 * (size_t)E);
+    if (!maps) return K3MOE_ENOMEM;
+    int rc = K3MOE_OK;
+    for (int e = 0; e < E && rc == K3MOE_OK; e++) {
+        const uint8_t *planes[6] = {host_table[e].gp, host_table[e].up, host_table[e].dp,
+                                    host_table[e].gs, host_table[e].us, host_table[e].ds};
+        for (int m = 0; m < 6; m++) {
+            const bool sc = m >= 3;
+            const int rows = (m % 3) < 2 ? f : d, in = (m % 3) < 2 ? d : f;
+            const cuuint64_t width = sc ? (cuuint64_t)(in / 32) : (cuuint64_t)(in / 2);
+            const cuuint64_t dims[2] = {width, (cuuint64_t)rows};
+            const cuuint64_t strides[1] = {width};
+            const cuuint32_t box[2] = {sc ? 16u : 128u, (cuuint32_t)MX_M};
+            const cuuint32_t estr[2] = {1, 1};
+            if (encode(&maps[6 * e + m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void *)planes[m], dims, strides, box,
+                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                       sc ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+                rc = K3MOE_EINVAL;
+                break;
+            }
+        }
+    }
+    if (rc == K3MOE_OK &&
+        cudaMemcpy(dev_maps, maps, sizeof(CUtensorMap) * 6 * (size_t)E, cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        rc = K3MOE_ECUDA;
+    }
+    free(maps);
+    return rc;
+}
+
+// Both phases for one token whose pieces (ximg: image then scale atoms) the
+// router has written.  out += sum_j w_j y_j (the caller zeroes out first for
+// a plain forward); the order of the additions is not fixed.
+int launch_mx_t1(const void *maps, const int32_t *ids, const float *w, const uint8_t *ximg, const float *rscale,
+                 uint8_t *himg, float *part, unsigned *cnt, int k, int d, int f, float *out, int *err,
+                 cudaStream_t s)
+{
+    const int G = num_sms();
+    // phase 1 holds the B images of two experts: a CTA's range must not
+    // span more than two
+    const long u1 = (long)k * (d / MX_M) * (f / MX_UK);
+    if ((u1 + G - 1) / G > (long)(d / MX_M) * (f / MX_UK)) return K3MOE_EINVAL;
+    MxArgs a0 = {};
+    a0.maps = (const CUtensorMap *)maps;
+    a0.ids = ids;
+    a0.w = w;
+    a0.k = k;
+    a0.d = d;
+    a0.f = f;
+    a0.err = err;
+    MxArgs a1 = a0;
+    a0.bimg = ximg;
+    a0.bsf = ximg + (size_t)d * 8;
+    a0.rscale = rscale;
+    a0.himg = himg;
+    a0.hsf = himg + (size_t)k * f * 8;
+    a0.part = part;
+    a0.cnt = cnt;
+    a1.bimg = himg;
+    a1.bsf = himg + (size_t)k * f * 8;
+    a1.out = out;
+    unsigned *hready = cnt + (size_t)k * (f / MX_M);
+    unsigned *exit_cnt = hready + k;
+    uint32_t bar_off = (uint32_t)mx_bar_off(d, f);
+    const size_t smem = mx_smem(d, f);
+    static size_t configured = 0;
+    if (smem > configured) {
+        if (cudaFuncSetAttribute(k3_mx_layer, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return K3MOE_ECUDA;
+        }
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k3_mx_layer, MX_THREADS, smem) != cudaSuccess ||
+            per_sm < 1) {
+            cudaGetLastError();
+            return K3MOE_ECUDA;
+        }
+        configured = smem;
+    }
+    void *args[] = {(void *)&a0, (void *)&a1, (void *)&hready, (void *)&exit_cnt, (void *)&bar_off};
+    if (cudaLaunchCooperativeKernel((const void *)k3_mx_layer, dim3(G), dim3(MX_THREADS), args, smem, s) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return K3MOE_ECUDA;
+    }
+    return K3MOE_OK;
+}
+
+}  // namespace k3

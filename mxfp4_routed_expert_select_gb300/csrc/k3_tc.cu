@@ -42,7 +42,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
-#include "k3_device.cuh"
+#include "k3_tcgen05.cuh"
 
 namespace k3 {
 
@@ -94,8 +94,6 @@ struct TcCfg {
     static_assert(SMEM <= 232448, "shared memory");
 };
 
-K3_DEV uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
 // K-major, M = 128, N = n (multiple of 16, <= 256).
 K3_DEV uint32_t bf16_idesc(int n)
@@ -104,14 +102,6 @@ K3_DEV uint32_t bf16_idesc(int n)
 }
 // kind::f8f6f4 with e4m3 A and B (format code 0), otherwise the same fields.
 K3_DEV uint32_t e4m3_idesc(int n) { return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TC_M >> 4) << 24); }
-// Shared-memory matrix descriptor of a K-major operand with the 128-byte
-// swizzle, split in its two 32-bit halves.  Low half: start address >> 4
-// (bits 0-13) and leading byte offset 1 (bits 16-29, unused with this
-// swizzle); it is the only half that changes, and +32 bytes of K is +2.
-// High half: stride byte offset 1024 >> 4 (8-row groups 1024 bytes apart),
-// descriptor version 1 (bit 46 of the whole), swizzle mode 2 (bits 61-63).
-K3_DEV uint32_t sw128_lo(uint32_t saddr) { return ((saddr & 0x3FFFFu) >> 4) | (1u << 16); }
-constexpr uint32_t SW128_HI = (1024u >> 4) | (1u << 14) | (2u << 29);
 // One k-step (64 of K) of D (+)= A * B^T: four K = 16 MMAs on consecutive
 // 32-byte slices of A and B, A and B given by the low halves of their
 // descriptors.  Executed by the whole warp; elect.sync picks the one lane
@@ -153,17 +143,6 @@ K3_DEV void mma_kstep(uint32_t td, uint32_t alo, uint32_t blo, uint32_t idesc, u
 #undef K3_KSTEP1
 #undef K3_KSTEP2
 #undef K3_MMA4
-// Commit by the lane elect.sync picks (the lane that issued the MMAs).
-K3_DEV void mma_commit(uint32_t bar)
-{
-    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
-                 : "memory");
-}
-K3_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-K3_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-K3_DEV void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
 // Thread-block clusters: this CTA's rank, the cluster's size and index, the
 // number of clusters; a cluster-wide barrier (every thread of every CTA).
 K3_DEV uint32_t cluster_rank() { uint32_t r; asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r)); return r; }
@@ -192,28 +171,6 @@ K3_DEV void mma_commit_multicast(uint32_t bar, uint16_t mask)
                  ::"r"(bar), "h"(mask)
                  : "memory");
 }
-
-// 2D tiled TMA load (x = byte column, a multiple of 16; y = row).
-K3_DEV void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-                 "%3}], [%4];" ::"r"(dst),
-                 "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
-                 : "memory");
-}
-
-// 8 consecutive fp32 columns (column address a multiple of 8).
-K3_DEV void tmem_ld8(uint32_t taddr, float (&v)[8])
-{
-    uint32_t r[8];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                   "=r"(r[7])
-                 : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 8; i++) v[i] = __uint_as_float(r[i]);
-}
-K3_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 K3_DEV uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 {
@@ -273,16 +230,6 @@ K3_DEV uint2 decode8_e4m3(uint32_t w, uint32_t tlo, uint32_t thi)
     o.x = prmt(tlo, thi, mag) | (prmt(w4, w, 0x5140u) & 0x80808080u);
     o.y = prmt(tlo, thi, mag >> 16) | (prmt(w4, w, 0x7362u) & 0x80808080u);
     return o;
-}
-
-K3_DEV bool tc_wait(uint32_t bar, uint32_t parity, int *err, volatile int *abort_flag)
-{
-    if (*abort_flag) return false;
-    if (!mbar_wait(bar, parity, err)) {
-        *abort_flag = 1;
-        return false;
-    }
-    return true;
 }
 
 // out[0..3] += v0..v3 with one vector reduction (16-byte aligned address).

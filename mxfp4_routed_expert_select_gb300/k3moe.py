@@ -27,6 +27,7 @@ K3MOE_OPT_FUSED_T1 = 1
 K3MOE_OPT_ACT_F16 = 2
 K3MOE_OPT_TC = 4
 K3MOE_OPT_TC_E4M3 = 8
+K3MOE_OPT_MX = 16
 K3MOE_NOALLOC_MAX_F = 2048
 
 
@@ -104,6 +105,7 @@ SIGNATURES = {
     "k3moe_layer_set_events": (ctypes.c_int, [_P, _P, _I]),
     "k3moe_layer_set_option": (ctypes.c_int, [_P, _I, _I]),
     "k3moe_layer_fused_t1": (ctypes.c_int, [_P]),
+    "k3moe_layer_mx_t1": (ctypes.c_int, [_P]),
     "k3moe_rmsnorm": (ctypes.c_int, [_P, _P, _I, _F, _P]),
     "k3moe_residual_add": (ctypes.c_int, [_P, _P, _I, _P]),
     "k3moe_cache_create": (ctypes.c_int, [_P, _SZ, _SZ, _P, _I, _I]),
@@ -277,6 +279,9 @@ class Layer:
 
     def fused_t1(self):
         return lib().k3moe_layer_fused_t1(self.h) == 1
+
+    def mx_t1(self):
+        return lib().k3moe_layer_mx_t1(self.h) == 1
 
     def set_events(self, events):
         """events: 4 torch.cuda.Event (or None to clear); each must have been

@@ -84,6 +84,35 @@ def test_ties_go_to_lower_ids_and_bias_only_selects(small):
     L2.close()
 
 
+@pytest.mark.parametrize("path,T", [("mx", 1), ("fused", 1), ("unfused", 1), ("unfused", 5)])
+def test_ties_at_the_selection_boundary(fusable, path, T):
+    """W_r = 0 and a bias with K-2 distinct high values, then four equal ones
+    for the last two slots: the two lowest ids of the tied four are chosen,
+    on the block-scaled and the fused batch-1 paths, the batch-1 router and
+    the multi-token one.  The expected ids come from the oracle's rule."""
+    pool, _, _, E, d, f = fusable
+    K = 8
+    b = np.zeros(E, np.float32)
+    hi = [40, 3, 17, 29, 8, 44]          # K - 2 clear winners
+    tied = [11, 5, 33, 20]               # equal scores at the boundary
+    b[hi] = np.arange(10, 10 + len(hi), dtype=np.float32)
+    b[tied] = 5.0
+    zero = torch.zeros((E, d), dtype=torch.int16, device="cuda")
+    L = k.Layer(E, K, d, f, zero, pool.views, torch.from_numpy(b).cuda(), max_tokens=max(T, 1))
+    L.set_option(k.K3MOE_OPT_MX, 1 if path == "mx" else 0)
+    L.set_option(k.K3MOE_OPT_FUSED_T1, 1 if path == "fused" else 0)
+    assert L.mx_t1() == (path == "mx")
+    assert L.fused_t1() == (path == "fused")
+    X = tokens_device(6, T, d, list(range(T)))
+    out, ids, w = _run(L, X, T, K)
+    rids, rw, _ = oracle.topk(np.zeros((T, E)), K, b.astype(np.float64))
+    assert sorted(hi + [5, 11]) == list(rids[0])
+    assert np.array_equal(ids, rids)
+    assert np.allclose(w, 1.0 / K)  # the unbiased logits are all 0
+    assert k.device_error() == 0
+    L.close()
+
+
 def test_degenerate_top_k(small):
     pool, Wr_bits, bias, E, K, d, f = small
     for kk in (1, 16):
@@ -187,12 +216,14 @@ def test_fused_batch1_matches_oracle_and_unfused(fusable, K, use_bias, act16):
     Xd = tokens(6, np.arange(T), d, subs)
     X = tokens_device(6, T, d, subs)
     L = k.Layer(E, K, d, f, router_tensor(Wr_bits), pool.views, bt, max_tokens=1)
+    L.set_option(k.K3MOE_OPT_MX, 0)
     assert L.fused_t1()
     if act16:
         L.set_option(k.K3MOE_OPT_ACT_F16, 1)
     L2 = k.Layer(E, K, d, f, router_tensor(Wr_bits), pool.views, bt, max_tokens=1)
+    L2.set_option(k.K3MOE_OPT_MX, 0)
     L2.set_option(k.K3MOE_OPT_FUSED_T1, 0)
-    assert not L2.fused_t1()
+    assert not L2.fused_t1() and not L2.mx_t1()
     for t in range(T):
         out, ids, w = _run(L, X[t:t + 1].contiguous(), 1, K)
         _check(pool, Wr_bits, b, K, Xd[t:t + 1], out, ids, w)
@@ -210,20 +241,26 @@ def test_fused_batch1_matches_oracle_and_unfused(fusable, K, use_bias, act16):
     L2.close()
 
 
-def test_full_decode_batch1_unfused_path(full):
+@pytest.mark.parametrize("path", ["fused", "unfused"])
+def test_full_decode_batch1_cuda_core_paths(full, path):
+    """The two CUDA-core batch-1 paths on the full layer (the default there is
+    the block-scaled tensor-core path, covered by test_full_decode_batch1)."""
     pool, Wr_bits, bias, L, Lb = full
-    assert L.fused_t1()
+    assert L.mx_t1()
     T = 2
     subs = margin_subs(1, T, D, Wr_bits, K16)
     Xd = tokens(1, np.arange(T), D, subs)
     X = tokens_device(1, T, D, subs)
-    L.set_option(k.K3MOE_OPT_FUSED_T1, 0)
+    L.set_option(k.K3MOE_OPT_MX, 0)
+    L.set_option(k.K3MOE_OPT_FUSED_T1, 1 if path == "fused" else 0)
     try:
+        assert L.fused_t1() == (path == "fused")
         for t in range(T):
             out, ids, w = _run(L, X[t:t + 1].contiguous(), 1, K16)
             _check(pool, Wr_bits, None, K16, Xd[t:t + 1], out, ids, w)
     finally:
         L.set_option(k.K3MOE_OPT_FUSED_T1, 1)
+        L.set_option(k.K3MOE_OPT_MX, 1)
 
 
 def test_full_decode_batch1_f16_activations(full):
@@ -235,7 +272,9 @@ def test_full_decode_batch1_f16_activations(full):
     Xd = tokens(1, np.arange(T), D, subs)
     X = tokens_device(1, T, D, subs)
     L.set_option(k.K3MOE_OPT_ACT_F16, 1)
+    L.set_option(k.K3MOE_OPT_MX, 0)
     try:
+        assert L.fused_t1()
         errs = []
         for t in range(T):
             out, ids, w = _run(L, X[t:t + 1].contiguous(), 1, K16)
@@ -247,3 +286,4 @@ def test_full_decode_batch1_f16_activations(full):
         print("f16-activation max rel err per token:", ["%.2e" % e for e in errs])
     finally:
         L.set_option(k.K3MOE_OPT_ACT_F16, 0)
+        L.set_option(k.K3MOE_OPT_MX, 1)
