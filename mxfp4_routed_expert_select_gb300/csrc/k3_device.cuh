@@ -375,6 +375,42 @@ K3_DEV unsigned ticket_arrive(unsigned *ticket)
     return old;
 }
 
+// Eight consecutive activations as fp32 (fp32 or bf16 input) and their dot
+// product with eight bf16 weights (fp32 accumulation), for the router.
+template <typename XT>
+K3_DEV void load_x8(const XT *x, int i, float (&xv)[8]);
+template <>
+K3_DEV void load_x8<float>(const float *x, int i, float (&xv)[8])
+{
+    float4 a = __ldg(reinterpret_cast<const float4 *>(x + i));
+    float4 b = __ldg(reinterpret_cast<const float4 *>(x + i + 4));
+    xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
+    xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
+}
+template <>
+K3_DEV void load_x8<__nv_bfloat16>(const __nv_bfloat16 *x, int i, float (&xv)[8])
+{
+    uint4 a = __ldg(reinterpret_cast<const uint4 *>(x + i));
+    uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        xv[2 * q] = __uint_as_float(w[q] << 16);
+        xv[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+    }
+}
+
+K3_DEV float bf16x8_dot(uint4 wv, const float (&xv)[8], float acc)
+{
+    uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        acc = fmaf(__uint_as_float(w[q] << 16), xv[2 * q], acc);
+        acc = fmaf(__uint_as_float(w[q] & 0xffff0000u), xv[2 * q + 1], acc);
+    }
+    return acc;
+}
+
+
 // Order-preserving map of an fp32 score to uint32 (larger score -> larger key).
 K3_DEV uint32_t okey(float v)
 {
@@ -395,9 +431,9 @@ struct CtaTopkSmem {
     int ids[32];
     unsigned prefix, need;
 };
-template <typename Sync>
-K3_DEV void cta_topk(const float *logit, const float *bias, int E, int k, int32_t *ids_out,
-                     float *w_out, CtaTopkSmem &sm, Sync sync)
+template <typename Sync, typename Logit>
+K3_DEV void cta_topk_by(Logit logit_of, const float *bias, int E, int k, int32_t *ids_out, float *w_out,
+                        CtaTopkSmem &sm, Sync sync)
 {
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     uint32_t key[4];
@@ -405,7 +441,7 @@ K3_DEV void cta_topk(const float *logit, const float *bias, int E, int k, int32_
     for (int m = 0; m < 4; m++) {
         const int e = t + 256 * m;
         key[m] = 0u;  // below every real key
-        if (e < E) key[m] = okey(__ldcg(logit + e) + (bias ? __ldg(bias + e) : 0.f));
+        if (e < E) key[m] = okey(logit_of(e) + (bias ? __ldg(bias + e) : 0.f));
     }
     uint32_t prefix = 0u, mask = 0u;
     unsigned need = (unsigned)k;
@@ -505,7 +541,7 @@ K3_DEV void cta_topk(const float *logit, const float *bias, int E, int k, int32_
     sync();
     if (warp == 0) {
         const int my_id = (lane < k) ? sm.ids[lane] : 0;
-        const float l = (lane < k) ? __ldcg(logit + my_id) : -INFINITY;
+        const float l = (lane < k) ? logit_of(my_id) : -INFINITY;
         float mx = l;
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -516,6 +552,13 @@ K3_DEV void cta_topk(const float *logit, const float *bias, int E, int k, int32_
             w_out[lane] = ex / sum;
         }
     }
+}
+// logits in global memory (ld.cg: other CTAs may have written them)
+template <typename Sync>
+K3_DEV void cta_topk(const float *logit, const float *bias, int E, int k, int32_t *ids_out, float *w_out,
+                     CtaTopkSmem &sm, Sync sync)
+{
+    cta_topk_by([&](int e) { return __ldcg(logit + e); }, bias, E, k, ids_out, w_out, sm, sync);
 }
 
 // One warp selects the top k (k <= 32) of E <= 1024 scores logit[e] + bias[e]

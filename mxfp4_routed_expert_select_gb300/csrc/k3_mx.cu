@@ -98,6 +98,11 @@ K3_DEV void sts32(uint32_t a, uint32_t v) { asm volatile("st.shared.u32 [%0], %1
 // Named barrier of the four epilogue warps.  The non-aligned form: a lane
 // that arrives after the others of its warp (the leader after its ticket)
 // is counted as itself, not as another arrival of the whole warp.
+// CTA-wide barrier in its non-aligned form: every thread is counted as
+// itself, so a warp whose lanes come from different role code (lane 0 of the
+// producer after its loop, the epilogue leader after its counts) cannot be
+// counted twice and let the barrier open before another warp arrives.
+K3_DEV void cta_sync_threads() { asm volatile("barrier.sync 0;" ::: "memory"); }
 K3_DEV void red_add_f32(float *p, float v) { asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory"); }
 K3_DEV void mx_bar_epi() { asm volatile("barrier.sync 2, 128;" ::: "memory"); }
 K3_DEV unsigned ticket_add(unsigned *p, unsigned v)
@@ -109,8 +114,6 @@ K3_DEV unsigned ticket_add(unsigned *p, unsigned v)
 
 struct MxArgs {
     const CUtensorMap *maps;  // [E][6]: gate, up, down packed planes; gate, up, down scale planes
-    const int32_t *ids;       // [k]
-    const float *w;           // [k] combine weights (phase 1)
     const uint8_t *bimg;      // phase 0: x pieces [d/256][16][128]; phase 1: h pieces, per slot j
     const uint8_t *bsf;       // phase 0: x scale atoms [d/128][512]; phase 1: per slot j
     const float *rscale;      // phase 0: RMSNorm factor, or null for 1
@@ -130,10 +133,14 @@ struct MxCfg {
     static constexpr int AT_BYTES = 2 * 512;             // two atoms per matrix per unit
     static constexpr int STAGE = NMAT * (A_BYTES + SC_BYTES + AT_BYTES);
     static constexpr int NS = PH == 0 ? 4 : 9;
-    // TMEM columns: accumulators from 0, A scale slots from TSA, B scales from TSB
-    static constexpr int TSA = PH == 0 ? 64 : 32, TSB = PH == 0 ? 128 : 112;
+    // TMEM columns: accumulators from TACC, A scale slots from TSA, B scales
+    // from TSB.  Phase 1 uses the columns of phase 0's B scales (free once
+    // phase 0's MMAs are done), so its MMAs can start while the phase-0
+    // epilogue still reads phase 0's accumulators (columns 0-63).
+    static constexpr int TACC = PH == 0 ? 0 : 128;
+    static constexpr int TSA = PH == 0 ? 64 : 160, TSB = PH == 0 ? 128 : 232;
     static constexpr int TMEM_COLS = 512;
-    static_assert(NMAT * 2 * MX_N <= TSA && NS * NMAT * 8 <= TSB - TSA, "TMEM layout");
+    static_assert(TACC + NMAT * 2 * MX_N <= TSA && NS * NMAT * 8 <= TSB - TSA, "TMEM layout");
 };
 
 // Shared memory of one phase: [stages][B images][scale atom staging (phase 1)].
@@ -199,7 +206,8 @@ K3_DEV bool mx_wait_count(const unsigned *p, unsigned target, int *err)
 // bars: this phase's barriers, hready[j]: h tiles of expert slot j done.
 template <int PH>
 K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem, volatile int *abort_flag,
-                    unsigned *s_last, unsigned *s_stop, unsigned *hready)
+                    unsigned *s_last, unsigned *s_stop, unsigned *hready, const int32_t *sel_ids,
+                    const float *sel_w, uint32_t prev_fin)
 {
     using C = MxCfg<PH>;
     using Bs = MxBars<PH>;
@@ -240,6 +248,8 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
             bool ok = true;
             // B operand images
             if (PH == 0) {
+                // the x image was written by other CTAs' plain stores (phase R)
+                asm volatile("fence.proxy.async.global;" ::: "memory");
                 mbar_arrive_expect_tx(bar(B_BLOAD), bimg_bytes + bsf_bytes);
                 for (uint32_t o = 0; o < bimg_bytes; o += 16384)
                     bulk_g2s(sbase + b_off + o, a.bimg + o, min(16384u, bimg_bytes - o), bar(B_BLOAD));
@@ -247,6 +257,8 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                     bulk_g2s(sbase + (uint32_t)((NS - 1) * C::STAGE) + o, a.bsf + o, min(16384u, bsf_bytes - o),
                              bar(B_BLOAD));
             }
+            // phase 1 reuses phase 0's shared memory: its MMAs must be done
+            if (PH == 1 && ok) ok = tc_wait(prev_fin, 0, a.err, abort_flag);
             uint32_t it = 0;
             int cur_tile = -1;
             const CUtensorMap *mp = nullptr;
@@ -255,7 +267,7 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                 const int tile = (int)(u / upt), uu = (int)(u % upt);
                 if (tile != cur_tile) {
                     cur_tile = tile;
-                    const int e = __ldg(a.ids + tile / tpe);
+                    const int e = sel_ids[tile / tpe];
                     mp = a.maps + 6 * (size_t)e;
                     t = tile % tpe;
                 }
@@ -286,6 +298,7 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
         // once every h tile of expert slot j is written (acquire), copied with
         // plain loads (they were written by plain stores of other CTAs) into
         // the B buffer, then made visible to the tensor core's proxy
+        if (!__all_sync(0xffffffffu, tc_wait(prev_fin, 0, a.err, abort_flag))) return;  // phase 0's smem
         for (int x = 0; x <= j_last - j_first && !*abort_flag; x++) {
             const int j = j_first + x;
             bool ok = true;
@@ -381,7 +394,7 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                 const uint32_t sfb = tsb + 4u * (uint32_t)(q >> 1);
 #pragma unroll
                 for (int m = 0; m < NMAT; m++)
-                    mx_mma(tmem + (uint32_t)(buf * NMAT * MX_N + m * MX_N), sw128_lo(a_at(s, m)) + 2u * q4, blo, idesc,
+                    mx_mma(tmem + (uint32_t)(C::TACC + buf * NMAT * MX_N + m * MX_N), sw128_lo(a_at(s, m)) + 2u * q4, blo, idesc,
                            tsa + m * 8 + 4 * (q4 >> 1), sfb, (first && q4 == 0) ? 0u : 1u);
             }
             mma_commit(bar(B_EMPTY + s));
@@ -426,7 +439,8 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
 #pragma unroll
                 for (int m = 0; m < NMAT; m++) {
                     float c0[8], c1[8];
-                    const uint32_t ta = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(buf * NMAT * MX_N + m * MX_N);
+                    const uint32_t ta =
+                        tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(C::TACC + buf * NMAT * MX_N + m * MX_N);
                     tmem_ld8(ta, c0);
                     tmem_ld8(ta + 8, c1);
                     tmem_wait_ld();
@@ -499,7 +513,7 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
             } else {
                 // w_j * (this segment's part of y_j) straight into out: the
                 // down product is linear, so split tiles need no exchange
-                red_add_f32(a.out + (size_t)t * MX_M + row, __ldg(a.w + j) * v[0]);
+                red_add_f32(a.out + (size_t)t * MX_M + row, sel_w[j] * v[0]);
             }
         }
         if (PH == 0) {
@@ -516,11 +530,110 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
     }
 }
 
-// Both phases of one token in one persistent kernel (cooperative launch:
-// phase-1 CTAs wait for the h tiles that other CTAs finish in phase 0).
-__global__ void __launch_bounds__(MX_THREADS, 1)
-    k3_mx_layer(const MxArgs a0, const MxArgs a1, unsigned *hready, unsigned *exit_cnt, uint32_t bar_off)
+// Router of one token (phase R), spread over every CTA.
+struct MxRoute {
+    const void *x;          // [d] fp32 or bf16
+    const uint16_t *Wr;     // [E][d] bf16
+    const float *bias;      // [E] selection bias or null
+    float *rpart;           // [S][E] partial logits
+    uint8_t *ximg;          // pieces of x: B image, then scale atoms
+    int32_t *ids_out;       // [k] selection (ascending ids), written by CTA 0
+    float *w_out;           // [k] combine weights
+    unsigned *gbar;         // grid barrier counter (zero between launches)
+    int E;
+};
+constexpr int MX_RCH = 256;  // 16-byte chunks of a router row range (8 per lane)
+
+// Phase R: partial logits of (row, range) units by every warp of the grid,
+// the E2M1 pieces of x (warp g: 32-block g), out zeroed; a grid barrier; then
+// every CTA sums the logits and selects the top k itself.  False on timeout.
+template <typename XT>
+K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, int32_t *sel_ids, float *sel_w,
+                     float *s_logit, CtaTopkSmem &tk, unsigned *s_flag)
 {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int d = a0.d, E = r.E, S = ((d >> 3) + MX_RCH - 1) / MX_RCH;
+    const long NW = (long)gridDim.x * (MX_THREADS / 32), gw = (long)blockIdx.x * (MX_THREADS / 32) + warp;
+    const XT *x = reinterpret_cast<const XT *>(r.x);
+    for (long u = gw; u < (long)E * S; u += NW) {
+        const int e = (int)(u / S), sp = (int)(u - (long)e * S);
+        const uint16_t *row = r.Wr + (size_t)e * d;
+        const int c0 = sp * MX_RCH, c1 = min(c0 + MX_RCH, d >> 3);
+        uint4 wv[8];
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+            const int c = c0 + lane + 32 * q;
+            wv[q] = c < c1 ? ld_stream16(row + 8 * c) : make_uint4(0, 0, 0, 0);
+        }
+        float acc = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+            const int c = c0 + lane + 32 * q;
+            if (c < c1) {
+                float xv[8];
+                load_x8<XT>(x, 8 * c, xv);
+                acc = bf16x8_dot(wv[q], xv, acc);
+            }
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) r.rpart[(size_t)sp * E + e] = acc;
+    }
+    for (long b = gw; b < (d >> 5); b += NW) {
+        float xv;
+        if constexpr (sizeof(XT) == 4) xv = __ldg(reinterpret_cast<const float *>(x) + 32 * b + lane);
+        else xv = __uint_as_float((uint32_t)__ldg(reinterpret_cast<const uint16_t *>(x) + 32 * b + lane) << 16);
+        mx_encode_block(xv, lane, (int)b, r.ximg, r.ximg + (size_t)d * 8);
+    }
+    for (long i = (long)blockIdx.x * MX_THREADS + threadIdx.x; i < d; i += (long)gridDim.x * MX_THREADS) out[i] = 0.f;
+    // the x image is read by other CTAs' bulk copies (async proxy)
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    cta_sync_threads();
+    if (threadIdx.x == 0) {
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(r.gbar) : "memory");
+        *s_flag = mx_wait_count(r.gbar, gridDim.x, a0.err) ? 1u : 0u;
+    }
+    cta_sync_threads();
+    if (*s_flag != 1u) return false;
+    // logits: the S partials of each row, summed in range order
+    for (int e0 = threadIdx.x; e0 < E; e0 += 4 * MX_THREADS) {
+        float v[4][4];
+#pragma unroll
+        for (int m = 0; m < 4; m++)
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const int e = e0 + m * MX_THREADS;
+                v[m][q] = (e < E && q < S) ? __ldcg(r.rpart + (size_t)q * E + e) : 0.f;
+            }
+#pragma unroll
+        for (int m = 0; m < 4; m++) {
+            const int e = e0 + m * MX_THREADS;
+            if (e < E) s_logit[e] = ((v[m][0] + v[m][1]) + v[m][2]) + v[m][3];
+        }
+    }
+    cta_sync_threads();
+    cta_topk_by([&](int e) { return s_logit[e]; }, r.bias, E, a0.k, sel_ids, sel_w, tk,
+                [] { cta_sync_threads(); });
+    cta_sync_threads();
+    if (blockIdx.x == 0 && threadIdx.x < a0.k) {
+        r.ids_out[threadIdx.x] = sel_ids[threadIdx.x];
+        r.w_out[threadIdx.x] = sel_w[threadIdx.x];
+    }
+    return true;
+}
+
+// The whole layer for one token in one persistent kernel (cooperative
+// launch: CTAs wait for each other at the router's grid barrier and for the
+// h tiles that other CTAs finish in phase 0).
+template <typename XT>
+__global__ void __launch_bounds__(MX_THREADS, 1)
+    k3_mx_layer(const MxRoute r, const MxArgs a0, const MxArgs a1, unsigned *hready, unsigned *exit_cnt,
+                uint32_t bar_off)
+{
+    __shared__ int32_t sel_ids[32];
+    __shared__ float sel_w[32];
+    __shared__ float s_logit[1024];
+    __shared__ CtaTopkSmem tk;
+    __shared__ unsigned s_flag;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bars0 = (uint64_t *)(sm + bar_off);
@@ -547,18 +660,18 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *(volatile uint32_t *)tmem_slot;
 
-    mx_body<0>(a0, sm, bars0, tmem, abort_flag, s_last, s_stop, hready);
-    // every role of phase 0 is done here (its MMAs completed, its copies
-    // landed): the shared memory and TMEM are phase 1's
-    __syncwarp();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    mx_body<1>(a1, sm, bars1, tmem, abort_flag, s_last, s_stop, hready);
+    if (!mx_route<XT>(r, a0, a1.out, sel_ids, sel_w, s_logit, tk, &s_flag)) *abort_flag = 1;
+    cta_sync_threads();
+    // Each role goes on to phase 1 when it is done with phase 0; the roles
+    // that write phase 1's shared memory (producer, h loader) first wait for
+    // phase 0's MMAs to complete (its FIN barrier); phase 1's TMEM columns
+    // are not phase 0's accumulators, which the epilogue may still read.
+    const uint32_t fin0 = smem_addr(bars0 + MxBars<0>::FIN);
+    mx_body<0>(a0, sm, bars0, tmem, abort_flag, s_last, s_stop, hready, sel_ids, sel_w, 0u);
+    mx_body<1>(a1, sm, bars1, tmem, abort_flag, s_last, s_stop, hready, sel_ids, sel_w, fin0);
 
-    __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    cta_sync_threads();
     if (warp == MX_W_MMA) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(MX_TMEM_COLS)
@@ -567,6 +680,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     // the last CTA out clears the h counters (no CTA reads them any more)
     if (threadIdx.x == 0 && ticket_add(exit_cnt, 1) == gridDim.x - 1) {
         for (int j = 0; j < a0.k; j++) hready[j] = 0;
+        *r.gbar = 0;
         *exit_cnt = 0;
     }
 }
@@ -580,8 +694,8 @@ bool mx_supported(int E, int k, int d, int f)
     // phase 0 stages the B scale atoms of x in one stage; TMEM holds d / 32
     // (phase 0) and 2 f / 32 (phase 1) columns of B scales
     return E >= 1 && k >= 1 && k <= 16 && d % 512 == 0 && f % 512 == 0 && d <= 8192 && f <= 2048 &&
-           (d / 128) * 512 <= MxCfg<0>::STAGE && MxCfg<0>::TSB + d / 32 <= MxCfg<0>::TMEM_COLS &&
-           MxCfg<1>::TSB + 2 * (f / 32) <= MxCfg<1>::TMEM_COLS && mx_smem(d, f) <= 232448;
+           (d / 128) * 512 <= MxCfg<0>::STAGE && MxCfg<0>::TSB + d / 32 <= MX_TMEM_COLS &&
+           MxCfg<1>::TSB + 2 * (f / 32) <= MX_TMEM_COLS && mx_smem(d, f) <= 232448;
 }
 
 // partial-sum slots: one per unit of a tile (a segment writes the slot of
@@ -589,8 +703,8 @@ bool mx_supported(int E, int k, int d, int f)
 size_t mx_part_floats(int k, int d, int f) { return (size_t)k * (f / MX_M) * (d / MX_UK) * MX_M * 2; }
 size_t mx_ximg_bytes(int d) { return (size_t)d * 8 + (size_t)(d / 128) * 512; }
 size_t mx_himg_bytes(int k, int f) { return (size_t)k * ((size_t)f * 8 + (size_t)(f / 128) * 512); }
-// counters: split phase-0 tiles' published parts, h tiles per expert slot, CTA exits
-size_t mx_cnt_words(int k, int d, int f) { (void)d; return (size_t)k * (f / MX_M) + k + 1; }
+// counters: split phase-0 tiles' published parts, h tiles per expert slot, CTA exits, grid barrier
+size_t mx_cnt_words(int k, int d, int f) { (void)d; return (size_t)k * (f / MX_M) + k + 2; }
 
 // Tensor maps of E experts: [E][gate, up, down packed; gate, up, down scales]
 // (packed: rows x in/2 bytes, boxes 128 rows x 128 bytes, 128-byte swizzle;
@@ -641,22 +755,58 @@ int mx_make_maps(const DevExpert *host_table, int E, int d, int f, void *dev_map
     return rc;
 }
 
-// Both phases for one token whose pieces (ximg: image then scale atoms) the
-// router has written.  out += sum_j w_j y_j (the caller zeroes out first for
-// a plain forward); the order of the additions is not fixed.
-int launch_mx_t1(const void *maps, const int32_t *ids, const float *w, const uint8_t *ximg, const float *rscale,
-                 uint8_t *himg, float *part, unsigned *cnt, int k, int d, int f, float *out, int *err,
-                 cudaStream_t s)
+// The whole batch-1 layer for one token: router and top-k (ids_out, w_out),
+// gate/up + SwiGLU, down + weighted combine into out (overwritten).  x is
+// fp32 or bf16 (xdt), rpart / ximg / himg / part / cnt are the layer's
+// workspace (cnt zero between launches).
+template <typename XT>
+static int launch_layer(const MxRoute &r, const MxArgs &a0, const MxArgs &a1, unsigned *hready, unsigned *exit_cnt,
+                        uint32_t bar_off, size_t smem, cudaStream_t s)
+{
+    static size_t configured = 0;
+    if (smem > configured) {
+        if (cudaFuncSetAttribute(k3_mx_layer<XT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return K3MOE_ECUDA;
+        }
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k3_mx_layer<XT>, MX_THREADS, smem) != cudaSuccess ||
+            per_sm < 1) {
+            cudaGetLastError();
+            return K3MOE_ECUDA;
+        }
+        configured = smem;
+    }
+    void *args[] = {(void *)&r, (void *)&a0, (void *)&a1, (void *)&hready, (void *)&exit_cnt, (void *)&bar_off};
+    if (cudaLaunchCooperativeKernel((const void *)k3_mx_layer<XT>, dim3(num_sms()), dim3(MX_THREADS), args, smem, s) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return K3MOE_ECUDA;
+    }
+    return K3MOE_OK;
+}
+
+int launch_mx_t1(const void *x, int xdt, const uint16_t *Wr, int E, const float *bias, const void *maps,
+                 float *rpart, uint8_t *ximg, uint8_t *himg, float *part, unsigned *cnt, int k, int d, int f,
+                 int32_t *ids_out, float *w_out, float *out, int *err, cudaStream_t s)
 {
     const int G = num_sms();
     // phase 1 holds the B images of two experts: a CTA's range must not
-    // span more than two
+    // span more than two; the in-kernel top-k takes E <= 1024
     const long u1 = (long)k * (d / MX_M) * (f / MX_UK);
-    if ((u1 + G - 1) / G > (long)(d / MX_M) * (f / MX_UK)) return K3MOE_EINVAL;
+    if ((u1 + G - 1) / G > (long)(d / MX_M) * (f / MX_UK) || E > 1024) return K3MOE_EINVAL;
+    MxRoute r = {};
+    r.x = x;
+    r.Wr = Wr;
+    r.bias = bias;
+    r.rpart = rpart;
+    r.ximg = ximg;
+    r.ids_out = ids_out;
+    r.w_out = w_out;
+    r.E = E;
     MxArgs a0 = {};
     a0.maps = (const CUtensorMap *)maps;
-    a0.ids = ids;
-    a0.w = w;
     a0.k = k;
     a0.d = d;
     a0.f = f;
@@ -664,7 +814,7 @@ int launch_mx_t1(const void *maps, const int32_t *ids, const float *w, const uin
     MxArgs a1 = a0;
     a0.bimg = ximg;
     a0.bsf = ximg + (size_t)d * 8;
-    a0.rscale = rscale;
+    a0.rscale = nullptr;
     a0.himg = himg;
     a0.hsf = himg + (size_t)k * f * 8;
     a0.part = part;
@@ -674,30 +824,12 @@ int launch_mx_t1(const void *maps, const int32_t *ids, const float *w, const uin
     a1.out = out;
     unsigned *hready = cnt + (size_t)k * (f / MX_M);
     unsigned *exit_cnt = hready + k;
-    uint32_t bar_off = (uint32_t)mx_bar_off(d, f);
+    r.gbar = exit_cnt + 1;
+    const uint32_t bar_off = (uint32_t)mx_bar_off(d, f);
     const size_t smem = mx_smem(d, f);
-    static size_t configured = 0;
-    if (smem > configured) {
-        if (cudaFuncSetAttribute(k3_mx_layer, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            return K3MOE_ECUDA;
-        }
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k3_mx_layer, MX_THREADS, smem) != cudaSuccess ||
-            per_sm < 1) {
-            cudaGetLastError();
-            return K3MOE_ECUDA;
-        }
-        configured = smem;
-    }
-    void *args[] = {(void *)&a0, (void *)&a1, (void *)&hready, (void *)&exit_cnt, (void *)&bar_off};
-    if (cudaLaunchCooperativeKernel((const void *)k3_mx_layer, dim3(G), dim3(MX_THREADS), args, smem, s) !=
-        cudaSuccess) {
-        cudaGetLastError();
-        return K3MOE_ECUDA;
-    }
-    return K3MOE_OK;
+    if (xdt == K3MOE_F32) return launch_layer<float>(r, a0, a1, hready, exit_cnt, bar_off, smem, s);
+    if (xdt == K3MOE_BF16) return launch_layer<__nv_bfloat16>(r, a0, a1, hready, exit_cnt, bar_off, smem, s);
+    return K3MOE_EINVAL;
 }
 
 }  // namespace k3

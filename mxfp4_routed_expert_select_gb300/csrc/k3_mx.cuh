@@ -23,16 +23,15 @@ K3_DEV void mx_encode_block(float r, int lane, int b, uint8_t *img, uint8_t *sf)
     const bool bad = __any_sync(0xffffffffu, !(fabsf(r) <= 3.4028235e38f));
 #pragma unroll 1
     for (int p = 0; p < MX_N; p++) {
-        float m = fabsf(r);
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        // block maximum of |r|: non-negative floats order like their bits
+        const uint32_t mb = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(r)));
+        const float m = __uint_as_float(mb);
         uint32_t sbyte = 127u, code = 0u;
         if (bad) {
             sbyte = 255u;
         } else if (m > 0.f) {
-            int ex;
-            frexpf(m, &ex);  // 2^(ex-1) <= m < 2^ex
-            int s = (m <= 0.75f * __int_as_float((127 + min(max(ex, -126), 127)) << 23)) ? ex - 3 : ex - 2;
+            const int ex = (int)max(mb >> 23, 1u) - 126;  // 2^(ex-1) <= m < 2^ex (m normal)
+            int s = (m <= 0.75f * __int_as_float((127 + min(ex, 127)) << 23)) ? ex - 3 : ex - 2;
             s = min(max(s, -126), 126);
             sbyte = (uint32_t)(s + 127);
             const float a = fabsf(r) * __int_as_float((127 - s) << 23);  // |r| / 2^s, exact

@@ -24,39 +24,6 @@ int num_sms();
 // first multiply.  Partial dot products go to part[S][E]; the last CTA to
 // finish (ticket counter, no waiting) sums them in a fixed order, applies the
 // optional RMSNorm factor and runs the top-k.
-template <typename XT>
-K3_DEV void load_x8(const XT *x, int i, float (&xv)[8]);
-template <>
-K3_DEV void load_x8<float>(const float *x, int i, float (&xv)[8])
-{
-    float4 a = __ldg(reinterpret_cast<const float4 *>(x + i));
-    float4 b = __ldg(reinterpret_cast<const float4 *>(x + i + 4));
-    xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
-    xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
-}
-template <>
-K3_DEV void load_x8<__nv_bfloat16>(const __nv_bfloat16 *x, int i, float (&xv)[8])
-{
-    uint4 a = __ldg(reinterpret_cast<const uint4 *>(x + i));
-    uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-    for (int q = 0; q < 4; q++) {
-        xv[2 * q] = __uint_as_float(w[q] << 16);
-        xv[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
-    }
-}
-
-K3_DEV float bf16x8_dot(uint4 wv, const float (&xv)[8], float acc)
-{
-    uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-    for (int q = 0; q < 4; q++) {
-        acc = fmaf(__uint_as_float(w[q] << 16), xv[2 * q], acc);
-        acc = fmaf(__uint_as_float(w[q] & 0xffff0000u), xv[2 * q + 1], acc);
-    }
-    return acc;
-}
-
 constexpr int RT1_LPL = 8;                 // 16-byte loads per lane per range
 constexpr int RT1_CHUNKS = 32 * RT1_LPL;   // 8-column chunks per range
 constexpr int RT1_SMAX = 16;               // ranges per row: d <= 16384
