@@ -118,29 +118,37 @@ struct MxArgs {
     const uint8_t *bsf;       // phase 0: x scale atoms [d/128][512]; phase 1: per slot j
     const float *rscale;      // phase 0: RMSNorm factor, or null for 1
     uint8_t *himg, *hsf;      // phase 0 output: h pieces per slot j (f * 8 and f / 128 * 512 bytes)
-    float *part;              // split-tile partials [tiles][units per tile][128][NMAT]
+    float *part;              // split-tile partials of phase 0 [tiles][units per tile][128][2]
     float *out;               // phase 1: [d], added into
     unsigned *cnt;            // phase 0: [tiles] tickets; phase 1: [d / 128] row-tile tickets
     int k, d, f;
     int *err;
 };
 
+// A stage holds two 128-row x 128-byte A tiles: phase 0 the gate and the up
+// tile of one 256-long K step (two accumulators), phase 1 two consecutive
+// 256-long K steps of the down rows (one accumulator, a 512-long unit).
+// Scale boxes (128 rows x 16 bytes = 16 k-blocks): phase 0 one per matrix,
+// of which a unit uses half; phase 1 one, all of it.
 template <int PH>
 struct MxCfg {
-    static constexpr int NMAT = PH == 0 ? 2 : 1;
-    static constexpr int A_BYTES = MX_M * 128;           // one matrix, one unit
+    static constexpr int NMAT = 2;                       // A tiles per stage
+    static constexpr int NOUT = PH == 0 ? 2 : 1;         // accumulators
+    static constexpr int NSC = PH == 0 ? 2 : 1;          // scale boxes per stage
+    static constexpr int UK = PH == 0 ? 256 : 512;       // K per unit
+    static constexpr int A_BYTES = MX_M * 128;           // one A tile
     static constexpr int SC_BYTES = MX_M * 16;           // scale box
-    static constexpr int AT_BYTES = 2 * 512;             // two atoms per matrix per unit
-    static constexpr int STAGE = NMAT * (A_BYTES + SC_BYTES + AT_BYTES);
-    static constexpr int NS = PH == 0 ? 4 : 9;
+    static constexpr int AT_BYTES = 2 * 512;             // two atoms per A tile
+    static constexpr int STAGE = NMAT * (A_BYTES + AT_BYTES) + NSC * SC_BYTES;
+    static constexpr int NS = PH == 0 ? 4 : 5;
     // TMEM columns: accumulators from TACC, A scale slots from TSA, B scales
     // from TSB.  Phase 1 uses the columns of phase 0's B scales (free once
     // phase 0's MMAs are done), so its MMAs can start while the phase-0
     // epilogue still reads phase 0's accumulators (columns 0-63).
     static constexpr int TACC = PH == 0 ? 0 : 128;
-    static constexpr int TSA = PH == 0 ? 64 : 160, TSB = PH == 0 ? 128 : 232;
+    static constexpr int TSA = PH == 0 ? 64 : 160, TSB = PH == 0 ? 128 : 240;
     static constexpr int TMEM_COLS = 512;
-    static_assert(TACC + NMAT * 2 * MX_N <= TSA && NS * NMAT * 8 <= TSB - TSA, "TMEM layout");
+    static_assert(TACC + NOUT * 2 * MX_N <= TSA && NS * NMAT * 8 <= TSB - TSA, "TMEM layout");
 };
 
 // Shared memory of one phase: [stages][B images][scale atom staging (phase 1)].
@@ -223,12 +231,13 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
     auto a_at = [&](int s, int m) { return sbase + (uint32_t)(s * C::STAGE + m * C::A_BYTES); };
     auto sc_at = [&](int s, int m) { return sbase + (uint32_t)(s * C::STAGE + NMAT * C::A_BYTES + m * C::SC_BYTES); };
     auto at_at = [&](int s, int m) {
-        return sbase + (uint32_t)(s * C::STAGE + NMAT * (C::A_BYTES + C::SC_BYTES) + m * C::AT_BYTES);
+        return sbase + (uint32_t)(s * C::STAGE + NMAT * C::A_BYTES + C::NSC * C::SC_BYTES + m * C::AT_BYTES);
     };
+    constexpr int NOUT = C::NOUT;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tpe = ROWS / MX_M;  // tiles per expert
-    const int upt = K / MX_UK;    // units per tile
+    const int upt = K / C::UK;    // units per tile
     const int ntiles = a.k * tpe;
     const long U = (long)ntiles * upt, G = gridDim.x;
     const long ulo = U * blockIdx.x / G, uhi = U * (blockIdx.x + 1) / G;
@@ -278,13 +287,19 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(bar(B_FULL + s), NMAT * (C::A_BYTES + C::SC_BYTES));
+                mbar_arrive_expect_tx(bar(B_FULL + s), NMAT * C::A_BYTES + C::NSC * C::SC_BYTES);
                 issued[s]++;
+                if (PH == 0) {
 #pragma unroll
-                for (int m = 0; m < NMAT; m++) {
-                    const int pm = PH == 0 ? m : 2;
-                    tma_load_2d(a_at(s, m), mp + pm, uu * 128, t * MX_M, bar(B_FULL + s));
-                    tma_load_2d(sc_at(s, m), mp + 3 + pm, 16 * (uu >> 1), t * MX_M, bar(B_FULL + s));
+                    for (int m = 0; m < 2; m++) {  // gate, up
+                        tma_load_2d(a_at(s, m), mp + m, uu * 128, t * MX_M, bar(B_FULL + s));
+                        tma_load_2d(sc_at(s, m), mp + 3 + m, 16 * (uu >> 1), t * MX_M, bar(B_FULL + s));
+                    }
+                } else {
+#pragma unroll
+                    for (int m = 0; m < 2; m++)  // two K steps of the down rows
+                        tma_load_2d(a_at(s, m), mp + 2, (2 * uu + m) * 128, t * MX_M, bar(B_FULL + s));
+                    tma_load_2d(sc_at(s, 0), mp + 5, 16 * uu, t * MX_M, bar(B_FULL + s));
                 }
             }
             // drain: every copy issued here has landed before the CTA exits
@@ -338,7 +353,11 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                 for (int at = 0; at < 2; at++)
 #pragma unroll
                     for (int r1 = 0; r1 < 4; r1++) {
-                        uint32_t v = lds32(sc_at(s, m) + (uint32_t)((lane + 32 * r1) * 16 + 8 * (uu & 1) + 4 * at));
+                        // phase 0: A tile m's own box, the unit's half; phase 1: the
+                        // one box, tile m's half
+                        const uint32_t box = PH == 0 ? sc_at(s, m) : sc_at(s, 0);
+                        const int byte = PH == 0 ? 8 * (uu & 1) + 4 * at : 8 * m + 4 * at;
+                        uint32_t v = lds32(box + (uint32_t)((lane + 32 * r1) * 16 + byte));
                         v &= ~__vcmpeq4(v, 0xffffffffu);  // 255 (a dropped group) -> 2^-127
                         sts32(at_at(s, m) + (uint32_t)(at * 512 + 16 * lane + 4 * r1), v);
                     }
@@ -386,16 +405,31 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
             }
             const uint32_t bimg = sbase + b_off + (uint32_t)((PH == 1 ? bx : 0) * bimg_bytes);
             const uint32_t tsb = tmem + C::TSB + (uint32_t)((PH == 1 ? bx : 0) * (K / 32));
+            if (PH == 0) {
 #pragma unroll
-            for (int q4 = 0; q4 < 4; q4++) {
-                const int q = uu * 4 + q4;  // K step of 64 within the tile's K
-                const uint32_t blo = sw128_lo(bimg + (uint32_t)((q >> 2) * (MX_N * 128))) + 2u * (uint32_t)(q & 3);
-                const uint32_t idesc = mx_idesc(2u * (q4 & 1), 2u * (q & 1));
-                const uint32_t sfb = tsb + 4u * (uint32_t)(q >> 1);
+                for (int q4 = 0; q4 < 4; q4++) {
+                    const int q = uu * 4 + q4;  // K step of 64 within the tile's K
+                    const uint32_t blo = sw128_lo(bimg + (uint32_t)((q >> 2) * (MX_N * 128))) + 2u * (uint32_t)(q & 3);
+                    const uint32_t idesc = mx_idesc(2u * (q4 & 1), 2u * (q & 1));
+                    const uint32_t sfb = tsb + 4u * (uint32_t)(q >> 1);
 #pragma unroll
-                for (int m = 0; m < NMAT; m++)
-                    mx_mma(tmem + (uint32_t)(C::TACC + buf * NMAT * MX_N + m * MX_N), sw128_lo(a_at(s, m)) + 2u * q4, blo, idesc,
-                           tsa + m * 8 + 4 * (q4 >> 1), sfb, (first && q4 == 0) ? 0u : 1u);
+                    for (int m = 0; m < 2; m++)  // gate, up: their own accumulators
+                        mx_mma(tmem + (uint32_t)(C::TACC + buf * NOUT * MX_N + m * MX_N), sw128_lo(a_at(s, m)) + 2u * q4,
+                               blo, idesc, tsa + m * 8 + 4 * (q4 >> 1), sfb, (first && q4 == 0) ? 0u : 1u);
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < 2; m++)  // the unit's two 256-long K steps, one accumulator
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; q4++) {
+                        const int q = uu * 8 + m * 4 + q4;
+                        const uint32_t blo =
+                            sw128_lo(bimg + (uint32_t)((q >> 2) * (MX_N * 128))) + 2u * (uint32_t)(q & 3);
+                        const uint32_t idesc = mx_idesc(2u * (q4 & 1), 2u * (q & 1));
+                        const uint32_t sfb = tsb + 4u * (uint32_t)(q >> 1);
+                        mx_mma(tmem + (uint32_t)(C::TACC + buf * MX_N), sw128_lo(a_at(s, m)) + 2u * q4, blo, idesc,
+                               tsa + m * 8 + 4 * (q4 >> 1), sfb, (first && m == 0 && q4 == 0) ? 0u : 1u);
+                    }
             }
             mma_commit(bar(B_EMPTY + s));
             if (last) {
@@ -431,16 +465,16 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
             u = ub;
             const int buf = sg & 1;
             const bool ok = __all_sync(0xffffffffu, tc_wait(bar(B_ACCF + buf), (sg / 2) & 1, a.err, abort_flag));
-            float v[NMAT];
+            float v[NOUT];
 #pragma unroll
-            for (int m = 0; m < NMAT; m++) v[m] = 0.f;
+            for (int m = 0; m < NOUT; m++) v[m] = 0.f;
             if (ok) {
                 tc_fence_after();
 #pragma unroll
-                for (int m = 0; m < NMAT; m++) {
+                for (int m = 0; m < NOUT; m++) {
                     float c0[8], c1[8];
                     const uint32_t ta =
-                        tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(C::TACC + buf * NMAT * MX_N + m * MX_N);
+                        tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(C::TACC + buf * NOUT * MX_N + m * MX_N);
                     tmem_ld8(ta, c0);
                     tmem_ld8(ta + 8, c1);
                     tmem_wait_ld();
@@ -462,13 +496,13 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
             const int seg = (int)(ua - t0);
             const int j = tile / tpe, t = tile % tpe;
             if (PH == 0) {
-                float *pp = a.part + ((size_t)tile * upt) * MX_M * NMAT;
+                float *pp = a.part + ((size_t)tile * upt) * MX_M * NOUT;
                 if (!whole && ua != t0) {
                     // a later segment: the CTA holding the tile's first units
                     // (at the end of its range, so it gets there last) finishes
                     // the tile; publish this part for it
 #pragma unroll
-                    for (int m = 0; m < NMAT; m++) pp[((size_t)seg * MX_M + row) * NMAT + m] = v[m];
+                    for (int m = 0; m < NOUT; m++) pp[((size_t)seg * MX_M + row) * NOUT + m] = v[m];
                     __syncwarp();
                     mx_bar_epi();
                     if (leader) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.cnt + tile) : "memory");
@@ -490,7 +524,7 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                     for (long us = ub; us < t1;) {
                         const long ub2 = U * (cta_of(us) + 1) / G, ue = ub2 < t1 ? ub2 : t1;
 #pragma unroll
-                        for (int m = 0; m < NMAT; m++) v[m] += __ldcg(pp + ((size_t)(us - t0) * MX_M + row) * NMAT + m);
+                        for (int m = 0; m < NOUT; m++) v[m] += __ldcg(pp + ((size_t)(us - t0) * MX_M + row) * NOUT + m);
                         us = ue;
                     }
                     if (leader) a.cnt[tile] = 0;  // for the next launch
@@ -794,8 +828,8 @@ int launch_mx_t1(const void *x, int xdt, const uint16_t *Wr, int E, const float 
     const int G = num_sms();
     // phase 1 holds the B images of two experts: a CTA's range must not
     // span more than two; the in-kernel top-k takes E <= 1024
-    const long u1 = (long)k * (d / MX_M) * (f / MX_UK);
-    if ((u1 + G - 1) / G > (long)(d / MX_M) * (f / MX_UK) || E > 1024) return K3MOE_EINVAL;
+    const long upe1 = (long)(d / MX_M) * (f / MxCfg<1>::UK), u1 = (long)k * upe1;
+    if ((u1 + G - 1) / G > upe1 || E > 1024) return K3MOE_EINVAL;
     MxRoute r = {};
     r.x = x;
     r.Wr = Wr;
