@@ -42,6 +42,9 @@ N_ROUTER_COPIES = 16
 # 896-expert workload, from a one-pass ncu capture of this bench (median of
 # three launches); the algorithmic bytes are LAYER_BYTES = 293,601,280.
 FUSED_TRAFFIC = 294038272
+# The same for the block-scaled batch-1 kernel (k3_mx_layer), or None until
+# a capture of the current kernel exists.
+MX_TRAFFIC = None
 N_TOKENS = 1024
 
 
@@ -283,6 +286,7 @@ def run_ours(args, rank, world, dev_index):
     dn_ms = [e[2].elapsed_time(e[3]) for e in evs]
 
     fused = layers[0].fused_t1()
+    mx = layers[0].mx_t1()
     # the opt-in f16-activation mode, same workload, for the record
     act16 = None
     if fused:
@@ -345,12 +349,25 @@ def run_ours(args, rank, world, dev_index):
 
     peak, peak_src = measured_peaks()
     gu_avg = statistics.mean(gu_ms)
-    if fused:
+    traffic, traffic_src = None, None
+    if mx:
+        # one kernel per step: router, top-k, gate/up, down and combine
+        eager_ms = statistics.mean([a + b + c for a, b, c in zip(route_ms, gu_ms, dn_ms)])
+        k_ms = ms / args.steps if graph is not None else eager_ms
+        k_name, k_bytes = ("k3_mx_layer<float> (router + top-k + 16 experts on tcgen05 kind::mxf4 + combine)",
+                           LAYER_BYTES)
+        if E == 896 and MX_TRAFFIC:
+            traffic, traffic_src = MX_TRAFFIC, ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of "
+                                                "k3_mx_layer<float> at this workload (median of 3 launches)")
+    elif fused:
         # one kernel per step: its average duration over the timed region is at
         # most the step time (graph replay gaps count against it)
         eager_ms = statistics.mean([a + b + c for a, b, c in zip(route_ms, gu_ms, dn_ms)])
         k_ms = ms / args.steps if graph is not None else eager_ms
         k_name, k_bytes = "k3_moe_t1_fused (router + top-k + 16 experts + combine)", LAYER_BYTES
+        if E == 896:
+            traffic, traffic_src = FUSED_TRAFFIC, ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch "
+                                                   "of k3_moe_t1_fused<0> at this workload (median of 3 launches)")
     else:
         k_ms, k_name, k_bytes = gu_avg, "k3_rows_pipe (gate/up + SwiGLU, 16 experts)", GATEUP_BYTES
     achieved = k_bytes / (k_ms * 1e-3) / 1e9
@@ -377,21 +394,19 @@ def run_ours(args, rank, world, dev_index):
                          % (N_ROUTER_COPIES, N_ROUTER_COPIES * ROUTER_BYTES / 1e6, E, N_TOKENS)},
         "layer_hbm": {"bytes_per_token": LAYER_BYTES, "gbs": round(layer_gbs, 1),
                       "frac_of_peak": round(layer_gbs / peak, 4), "frac_of_8tbs": round(layer_gbs / 8000, 4)},
-        "kernels_ms": ({"fused_layer": round(k_ms, 5), "fused_layer_eager_events": round(eager_ms, 5),
-                        "steps_sampled": n_ev} if fused else
+        "kernels_ms": ({"layer_kernel": round(k_ms, 5), "layer_kernel_eager_events": round(eager_ms, 5),
+                        "steps_sampled": n_ev} if (fused or mx) else
                        {"route_topk": round(statistics.mean(route_ms), 5),
                         "gate_up_swiglu": round(gu_avg, 5),
                         "down_combine": round(statistics.mean(dn_ms), 5), "steps_sampled": n_ev}),
         "roofline": {"kernel": k_name, "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": FUSED_TRAFFIC if (fused and E == 896) else None,
-                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of "
-                                       "k3_moe_t1_fused<0> at this workload (median of 3 launches)",
+                     "traffic": traffic, "traffic_source": traffic_src,
                      "algorithmic_bytes": k_bytes},
         "e2e": {"value": round(job_rate(n_e2e, world, e2e_ms), 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": D * 4, "d2h_bytes_per_step": D * 4, "steps": n_e2e},
-        "gpu_launches": (1 if fused else 3) * args.steps,
+        "gpu_launches": (1 if (fused or mx) else 3) * args.steps,
         "act_f16_mode": act16,
         "clocks": clocks,
     }

@@ -49,7 +49,7 @@ size_t mx_himg_bytes(int k, int f);
 size_t mx_cnt_words(int k, int d, int f);
 int mx_make_maps(const DevExpert *host_table, int E, int d, int f, void *dev_maps);
 int launch_mx_t1(const void *x, int xdt, const uint16_t *Wr, int E, const float *bias, const void *maps,
-                 float *rpart, uint8_t *ximg, uint8_t *himg, float *part, unsigned *cnt, int k, int d, int f,
+                 float *logits, uint8_t *ximg, uint8_t *himg, float *part, unsigned *cnt, int k, int d, int f,
                  int32_t *ids_out, float *w_out, float *out, int *err, cudaStream_t s);
 int route_multi_nsplit(int T, int E, int d);
 int launch_route_multi(const void *X, int xdt, int T, const uint16_t *Wr, int E, int d,
@@ -467,7 +467,7 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int xdt, int32_t T, float
     if (T == 1 && L->mx && L->mx_ready) {
         // one persistent kernel: router and top-k, then the block-scaled
         // gate/up and down phases
-        K3_TRY(k3::launch_mx_t1(X, xdt, L->Wr, L->E, L->bias, L->mx_maps, L->part, L->mx_ximg, L->mx_himg,
+        K3_TRY(k3::launch_mx_t1(X, xdt, L->Wr, L->E, L->bias, L->mx_maps, L->logits, L->mx_ximg, L->mx_himg,
                                 L->mx_part, L->mx_cnt, L->k, L->d, L->f, L->ids, L->w, out,
                                 k3::device_error_word(), st));
         if (L->nev) {

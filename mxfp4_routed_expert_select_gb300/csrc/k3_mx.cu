@@ -215,7 +215,7 @@ K3_DEV bool mx_wait_count(const unsigned *p, unsigned target, int *err)
 template <int PH>
 K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem, volatile int *abort_flag,
                     unsigned *s_last, unsigned *s_stop, unsigned *hready, const int32_t *sel_ids,
-                    const float *sel_w, uint32_t prev_fin)
+                    const float *sel_w, uint32_t prev_fin, const volatile unsigned *x_issued)
 {
     using C = MxCfg<PH>;
     using Bs = MxBars<PH>;
@@ -256,16 +256,7 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
         if (lane == 0) {
             bool ok = true;
             // B operand images
-            if (PH == 0) {
-                // the x image was written by other CTAs' plain stores (phase R)
-                asm volatile("fence.proxy.async.global;" ::: "memory");
-                mbar_arrive_expect_tx(bar(B_BLOAD), bimg_bytes + bsf_bytes);
-                for (uint32_t o = 0; o < bimg_bytes; o += 16384)
-                    bulk_g2s(sbase + b_off + o, a.bimg + o, min(16384u, bimg_bytes - o), bar(B_BLOAD));
-                for (uint32_t o = 0; o < bsf_bytes; o += 16384)  // staged in the last stage
-                    bulk_g2s(sbase + (uint32_t)((NS - 1) * C::STAGE) + o, a.bsf + o, min(16384u, bsf_bytes - o),
-                             bar(B_BLOAD));
-            }
+            // phase 0: the x image copies were issued at the router's grid barrier
             // phase 1 reuses phase 0's shared memory: its MMAs must be done
             if (PH == 1 && ok) ok = tc_wait(prev_fin, 0, a.err, abort_flag);
             uint32_t it = 0;
@@ -305,41 +296,35 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
             // drain: every copy issued here has landed before the CTA exits
             for (int s = 0; s < NS; s++)
                 if (issued[s]) mbar_wait(bar(B_FULL + s), (issued[s] - 1) & 1, a.err);
-            if (PH == 0) mbar_wait(bar(B_BLOAD), 0, a.err);
+            if (PH == 0 && *x_issued == 1u) mbar_wait(bar(B_BLOAD), 0, a.err);  // x image copies
         }
         __syncwarp();
     } else if (PH == 1 && ulo < uhi && warp == MX_W_BLD) {
         // ------------------------------- h pieces of this CTA's experts (phase 1)
-        // once every h tile of expert slot j is written (acquire), copied with
-        // plain loads (they were written by plain stores of other CTAs) into
-        // the B buffer, then made visible to the tensor core's proxy
-        if (!__all_sync(0xffffffffu, tc_wait(prev_fin, 0, a.err, abort_flag))) return;  // phase 0's smem
-        for (int x = 0; x <= j_last - j_first && !*abort_flag; x++) {
-            const int j = j_first + x;
-            bool ok = true;
-            if (lane == 0) ok = mx_wait_count(hready + j, (unsigned)(a.f / MX_M), a.err);  // h tiles of one expert
-            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
-                *abort_flag = 1;
-                break;
+        // once every h tile of expert slot j is written (acquire), bulk
+        // copies into the B buffer; the writers fenced their plain stores
+        // towards the async proxy before publishing, the copy side does too
+        int loaded = 0;
+        if (lane == 0) {
+            bool ok = tc_wait(prev_fin, 0, a.err, abort_flag);  // phase 0's smem
+            for (int x = 0; x <= j_last - j_first && ok && !*abort_flag; x++) {
+                const int j = j_first + x;
+                if (!mx_wait_count(hready + j, (unsigned)(a.f / MX_M), a.err)) {  // h tiles of one expert
+                    *abort_flag = 1;
+                    break;
+                }
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                mbar_arrive_expect_tx(bar(B_BLOAD + x), bimg_bytes + bsf_bytes);
+                for (uint32_t o = 0; o < bimg_bytes; o += 16384)
+                    bulk_g2s(sbase + b_off + x * bimg_bytes + o, a.bimg + (size_t)j * bimg_bytes + o,
+                             min(16384u, bimg_bytes - o), bar(B_BLOAD + x));
+                bulk_g2s(sbase + sf_off + x * bsf_bytes, a.bsf + (size_t)j * bsf_bytes, bsf_bytes, bar(B_BLOAD + x));
+                loaded++;
             }
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.bimg + (size_t)j * bimg_bytes);
-            for (uint32_t i = lane; i < bimg_bytes / 16; i += 32) {
-                const uint4 v = __ldcg(src + i);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + b_off + x * bimg_bytes + 16 * i),
-                             "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                             : "memory");
-            }
-            const uint4 *ssrc = reinterpret_cast<const uint4 *>(a.bsf + (size_t)j * bsf_bytes);
-            for (uint32_t i = lane; i < bsf_bytes / 16; i += 32) {
-                const uint4 v = __ldcg(ssrc + i);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + sf_off + x * bsf_bytes + 16 * i),
-                             "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                             : "memory");
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_BLOAD + x));
+            // drain: the copies land before the CTA exits
+            for (int x = 0; x < loaded; x++) mbar_wait(bar(B_BLOAD + x), 0, a.err);
         }
+        __syncwarp();
     } else if (ulo < uhi && warp == MX_W_PERM) {
         // ------------------------------------- scale boxes -> tcgen05.cp atoms
         // atom byte 16 r0 + 4 r1 + kb = scale of row r0 + 32 r1, k-block kb
@@ -551,7 +536,9 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
             }
         }
         if (PH == 0) {
-            // every h piece this CTA wrote is in memory before the counts
+            // every h piece this CTA wrote is in memory (and ordered towards
+            // the async proxy that copies it) before the counts
+            asm volatile("fence.proxy.async.global;" ::: "memory");
             __syncwarp();
             mx_bar_epi();
             if (leader)
@@ -569,79 +556,95 @@ struct MxRoute {
     const void *x;          // [d] fp32 or bf16
     const uint16_t *Wr;     // [E][d] bf16
     const float *bias;      // [E] selection bias or null
-    float *rpart;           // [S][E] partial logits
+    float *logits;          // [E]
     uint8_t *ximg;          // pieces of x: B image, then scale atoms
     int32_t *ids_out;       // [k] selection (ascending ids), written by CTA 0
     float *w_out;           // [k] combine weights
     unsigned *gbar;         // grid barrier counter (zero between launches)
     int E;
 };
-constexpr int MX_RCH = 256;  // 16-byte chunks of a router row range (8 per lane)
 
-// Phase R: partial logits of (row, range) units by every warp of the grid,
-// the E2M1 pieces of x (warp g: 32-block g), out zeroed; a grid barrier; then
-// every CTA sums the logits and selects the top k itself.  False on timeout.
+// Phase R.  Each CTA copies its block of router rows (E / G rows, one
+// contiguous piece of W_r) into its still unused stage memory with bulk
+// copies, one warp per row computes the logits from there; meanwhile warp g
+// of the grid encodes 32-block g of x and the CTAs zero out.  A grid barrier,
+// then every CTA reads the E logits and selects the top k itself.  False on
+// a timeout.
 template <typename XT>
-K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, int32_t *sel_ids, float *sel_w,
-                     float *s_logit, CtaTopkSmem &tk, unsigned *s_flag)
+K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, uint8_t *sm, uint32_t bar_r, uint32_t bload0,
+                     int32_t *sel_ids, float *sel_w, float *s_logit, CtaTopkSmem &tk, unsigned *s_flag)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int d = a0.d, E = r.E, S = ((d >> 3) + MX_RCH - 1) / MX_RCH;
-    const long NW = (long)gridDim.x * (MX_THREADS / 32), gw = (long)blockIdx.x * (MX_THREADS / 32) + warp;
-    const XT *x = reinterpret_cast<const XT *>(r.x);
-    for (long u = gw; u < (long)E * S; u += NW) {
-        const int e = (int)(u / S), sp = (int)(u - (long)e * S);
-        const uint16_t *row = r.Wr + (size_t)e * d;
-        const int c0 = sp * MX_RCH, c1 = min(c0 + MX_RCH, d >> 3);
-        uint4 wv[8];
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            const int c = c0 + lane + 32 * q;
-            wv[q] = c < c1 ? ld_stream16(row + 8 * c) : make_uint4(0, 0, 0, 0);
-        }
-        float acc = 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            const int c = c0 + lane + 32 * q;
-            if (c < c1) {
-                float xv[8];
-                load_x8<XT>(x, 8 * c, xv);
-                acc = bf16x8_dot(wv[q], xv, acc);
-            }
-        }
-        acc = warp_sum(acc);
-        if (lane == 0) r.rpart[(size_t)sp * E + e] = acc;
+    const int d = a0.d, E = r.E, G = gridDim.x;
+    const int e0 = (int)((long)E * blockIdx.x / G), e1 = (int)((long)E * (blockIdx.x + 1) / G);
+    const uint32_t rbytes = (uint32_t)(e1 - e0) * (uint32_t)d * 2u;
+    const uint32_t sbase = smem_addr(sm);
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(bar_r, rbytes);
+        const uint8_t *src = reinterpret_cast<const uint8_t *>(r.Wr + (size_t)e0 * d);
+        for (uint32_t o = 0; o < rbytes; o += 16384) bulk_g2s(sbase + o, src + o, min(16384u, rbytes - o), bar_r);
     }
+    const XT *x = reinterpret_cast<const XT *>(r.x);
+    const long NW = (long)G * (MX_THREADS / 32), gw = (long)blockIdx.x * (MX_THREADS / 32) + warp;
     for (long b = gw; b < (d >> 5); b += NW) {
         float xv;
         if constexpr (sizeof(XT) == 4) xv = __ldg(reinterpret_cast<const float *>(x) + 32 * b + lane);
         else xv = __uint_as_float((uint32_t)__ldg(reinterpret_cast<const uint16_t *>(x) + 32 * b + lane) << 16);
         mx_encode_block(xv, lane, (int)b, r.ximg, r.ximg + (size_t)d * 8);
     }
-    for (long i = (long)blockIdx.x * MX_THREADS + threadIdx.x; i < d; i += (long)gridDim.x * MX_THREADS) out[i] = 0.f;
+    for (long i = (long)blockIdx.x * MX_THREADS + threadIdx.x; i < d; i += (long)G * MX_THREADS) out[i] = 0.f;
+    bool ok = mbar_wait(bar_r, 0, a0.err);
+    for (int e = e0 + warp; e < e1 && ok; e += MX_THREADS / 32) {
+        const uint32_t row = sbase + (uint32_t)(e - e0) * (uint32_t)d * 2u;
+        float acc0 = 0.f, acc1 = 0.f;
+        for (int c = lane; c < (d >> 3); c += 64) {
+            float xa[8], xb[8];
+            load_x8<XT>(x, 8 * c, xa);
+            const uint4 wa = lds128(row + 16u * (uint32_t)c);
+            acc0 = bf16x8_dot(wa, xa, acc0);
+            if (c + 32 < (d >> 3)) {
+                load_x8<XT>(x, 8 * (c + 32), xb);
+                acc1 = bf16x8_dot(lds128(row + 16u * (uint32_t)(c + 32)), xb, acc1);
+            }
+        }
+        const float acc = warp_sum(acc0 + acc1);
+        if (lane == 0) r.logits[e] = acc;
+    }
     // the x image is read by other CTAs' bulk copies (async proxy)
     asm volatile("fence.proxy.async.global;" ::: "memory");
     cta_sync_threads();
     if (threadIdx.x == 0) {
+        bool good = ok;
         asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(r.gbar) : "memory");
-        *s_flag = mx_wait_count(r.gbar, gridDim.x, a0.err) ? 1u : 0u;
+        good = mx_wait_count(r.gbar, G, a0.err) && good;
+        *s_flag = good ? 1u : 0u;
+        if (good) {
+            // phase 0's B operand, the pieces of x, while the top-k runs: the
+            // image to its buffer, the scale atoms staged in the last stage
+            using C0 = MxCfg<0>;
+            const uint32_t bimg = (uint32_t)d * 8u, bsf = (uint32_t)(d / 128) * 512u;
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            mbar_arrive_expect_tx(bload0, bimg + bsf);
+            for (uint32_t o = 0; o < bimg; o += 16384)
+                bulk_g2s(sbase + (uint32_t)(C0::NS * C0::STAGE) + o, r.ximg + o, min(16384u, bimg - o), bload0);
+            for (uint32_t o = 0; o < bsf; o += 16384)
+                bulk_g2s(sbase + (uint32_t)((C0::NS - 1) * C0::STAGE) + o, r.ximg + bimg + o, min(16384u, bsf - o),
+                         bload0);
+        }
     }
     cta_sync_threads();
     if (*s_flag != 1u) return false;
-    // logits: the S partials of each row, summed in range order
-    for (int e0 = threadIdx.x; e0 < E; e0 += 4 * MX_THREADS) {
-        float v[4][4];
-#pragma unroll
-        for (int m = 0; m < 4; m++)
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                const int e = e0 + m * MX_THREADS;
-                v[m][q] = (e < E && q < S) ? __ldcg(r.rpart + (size_t)q * E + e) : 0.f;
-            }
+    for (int e0b = threadIdx.x; e0b < E; e0b += 4 * MX_THREADS) {
+        float v[4];
 #pragma unroll
         for (int m = 0; m < 4; m++) {
-            const int e = e0 + m * MX_THREADS;
-            if (e < E) s_logit[e] = ((v[m][0] + v[m][1]) + v[m][2]) + v[m][3];
+            const int e = e0b + m * MX_THREADS;
+            v[m] = e < E ? __ldcg(r.logits + e) : 0.f;
+        }
+#pragma unroll
+        for (int m = 0; m < 4; m++) {
+            const int e = e0b + m * MX_THREADS;
+            if (e < E) s_logit[e] = v[m];
         }
     }
     cta_sync_threads();
@@ -667,19 +670,22 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     __shared__ float sel_w[32];
     __shared__ float s_logit[1024];
     __shared__ CtaTopkSmem tk;
-    __shared__ unsigned s_flag;
+    __shared__ unsigned s_flag;  // 1: the router's grid barrier passed, x image copies issued
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bars0 = (uint64_t *)(sm + bar_off);
     uint64_t *bars1 = bars0 + MxBars<0>::N;
-    uint32_t *tmem_slot = (uint32_t *)(bars1 + MxBars<1>::N);
+    uint64_t *bar_r = bars1 + MxBars<1>::N;  // router rows landed
+    uint32_t *tmem_slot = (uint32_t *)(bar_r + 1);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
     unsigned *s_last = (unsigned *)(tmem_slot + 2);  // epilogue: this CTA completes the tile
     unsigned *s_stop = (unsigned *)(tmem_slot + 3);  // epilogue: no further segment
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
+        s_flag = 0;
         mx_init_bars<0>(bars0);
         mx_init_bars<1>(bars1);
+        mbar_init(smem_addr(bar_r), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -694,15 +700,17 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *(volatile uint32_t *)tmem_slot;
 
-    if (!mx_route<XT>(r, a0, a1.out, sel_ids, sel_w, s_logit, tk, &s_flag)) *abort_flag = 1;
+    if (!mx_route<XT>(r, a0, a1.out, sm, smem_addr(bar_r), smem_addr(bars0 + MxBars<0>::BLOAD), sel_ids, sel_w, s_logit,
+                      tk, &s_flag))
+        *abort_flag = 1;
     cta_sync_threads();
     // Each role goes on to phase 1 when it is done with phase 0; the roles
     // that write phase 1's shared memory (producer, h loader) first wait for
     // phase 0's MMAs to complete (its FIN barrier); phase 1's TMEM columns
     // are not phase 0's accumulators, which the epilogue may still read.
     const uint32_t fin0 = smem_addr(bars0 + MxBars<0>::FIN);
-    mx_body<0>(a0, sm, bars0, tmem, abort_flag, s_last, s_stop, hready, sel_ids, sel_w, 0u);
-    mx_body<1>(a1, sm, bars1, tmem, abort_flag, s_last, s_stop, hready, sel_ids, sel_w, fin0);
+    mx_body<0>(a0, sm, bars0, tmem, abort_flag, s_last, s_stop, hready, sel_ids, sel_w, 0u, &s_flag);
+    mx_body<1>(a1, sm, bars1, tmem, abort_flag, s_last, s_stop, hready, sel_ids, sel_w, fin0, &s_flag);
 
     tc_fence_before();
     cta_sync_threads();
@@ -791,7 +799,7 @@ int mx_make_maps(const DevExpert *host_table, int E, int d, int f, void *dev_map
 
 // The whole batch-1 layer for one token: router and top-k (ids_out, w_out),
 // gate/up + SwiGLU, down + weighted combine into out (overwritten).  x is
-// fp32 or bf16 (xdt), rpart / ximg / himg / part / cnt are the layer's
+// fp32 or bf16 (xdt), logits / ximg / himg / part / cnt are the layer's
 // workspace (cnt zero between launches).
 template <typename XT>
 static int launch_layer(const MxRoute &r, const MxArgs &a0, const MxArgs &a1, unsigned *hready, unsigned *exit_cnt,
@@ -822,7 +830,7 @@ static int launch_layer(const MxRoute &r, const MxArgs &a0, const MxArgs &a1, un
 }
 
 int launch_mx_t1(const void *x, int xdt, const uint16_t *Wr, int E, const float *bias, const void *maps,
-                 float *rpart, uint8_t *ximg, uint8_t *himg, float *part, unsigned *cnt, int k, int d, int f,
+                 float *logits, uint8_t *ximg, uint8_t *himg, float *part, unsigned *cnt, int k, int d, int f,
                  int32_t *ids_out, float *w_out, float *out, int *err, cudaStream_t s)
 {
     const int G = num_sms();
@@ -830,11 +838,13 @@ int launch_mx_t1(const void *x, int xdt, const uint16_t *Wr, int E, const float 
     // span more than two; the in-kernel top-k takes E <= 1024
     const long upe1 = (long)(d / MX_M) * (f / MxCfg<1>::UK), u1 = (long)k * upe1;
     if ((u1 + G - 1) / G > upe1 || E > 1024) return K3MOE_EINVAL;
+    // router rows below the stage holding the x scale atoms
+    if ((size_t)((E + G - 1) / G) * d * 2 > (size_t)(MxCfg<0>::NS - 1) * MxCfg<0>::STAGE) return K3MOE_EINVAL;
     MxRoute r = {};
     r.x = x;
     r.Wr = Wr;
     r.bias = bias;
-    r.rpart = rpart;
+    r.logits = logits;
     r.ximg = ximg;
     r.ids_out = ids_out;
     r.w_out = w_out;
