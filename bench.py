@@ -42,9 +42,9 @@ N_ROUTER_COPIES = 16
 # 896-expert workload, from a one-pass ncu capture of this bench (median of
 # three launches); the algorithmic bytes are LAYER_BYTES = 293,601,280.
 FUSED_TRAFFIC = 294038272
-# The same for the block-scaled batch-1 kernel (k3_mx_layer), or None until
-# a capture of the current kernel exists.
-MX_TRAFFIC = None
+# The same for the block-scaled batch-1 kernel (k3_mx_layer<float>, median of
+# three launches); None whenever the kernel changed since the capture.
+MX_TRAFFIC = 301050624
 N_TOKENS = 1024
 
 
