@@ -40,8 +40,7 @@ int launch_down_t1(const float *h, const ExpertSrc &src, const float *w, int k, 
 int route_t1_splits(int d);
 int launch_route_t1(const void *x, int xdt, const uint16_t *Wr, int E, int d, float *part,
                     float *logits, const float *bias, int k, int32_t *ids, float *w,
-                    unsigned *ticket, float eps, float *u, uint8_t *ximg, float *r_out,
-                    float *zero_out, cudaStream_t s);
+                    unsigned *ticket, float eps, float *u, cudaStream_t s);
 bool mx_supported(int E, int k, int d, int f);
 size_t mx_part_floats(int k, int d, int f);
 size_t mx_ximg_bytes(int d);
@@ -435,7 +434,7 @@ static int route_into(k3moe_layer *L, const void *X, int xdt, int32_t T, cudaStr
 {
     if (T == 1)
         return k3::launch_route_t1(X, xdt, L->Wr, L->E, L->d, L->part, L->logits, L->bias, L->k,
-                                   L->ids, L->w, L->ticket, 0.f, nullptr, nullptr, nullptr, nullptr, s);
+                                   L->ids, L->w, L->ticket, 0.f, nullptr, s);
     return k3::launch_route_multi(X, xdt, T, L->Wr, L->E, L->d, L->part, L->nsplit, L->logits,
                                   L->bias, L->k, L->ids, L->w, s);
 }
@@ -669,7 +668,7 @@ extern "C" int k3moe_stream_decode(const k3moe_stream_desc *D, const float *X, i
             k3moe_layer *L = D->host_layers[l];
             // RMSNorm folded into the router: u = x / sqrt(mean(x^2) + eps)
             int r = k3::launch_route_t1(xcur, K3MOE_F32, L->Wr, E, d, L->part, L->logits, L->bias,
-                                        k, L->ids, L->w, L->ticket, D->eps, u, nullptr, nullptr, nullptr, st);
+                                        k, L->ids, L->w, L->ticket, D->eps, u, st);
             if (r != K3MOE_OK) {
                 fail(r);
                 break;

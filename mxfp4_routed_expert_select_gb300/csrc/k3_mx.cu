@@ -116,7 +116,6 @@ struct MxArgs {
     const CUtensorMap *maps;  // [E][6]: gate, up, down packed planes; gate, up, down scale planes
     const uint8_t *bimg;      // phase 0: x pieces [d/256][16][128]; phase 1: h pieces, per slot j
     const uint8_t *bsf;       // phase 0: x scale atoms [d/128][512]; phase 1: per slot j
-    const float *rscale;      // phase 0: RMSNorm factor, or null for 1
     uint8_t *himg, *hsf;      // phase 0 output: h pieces per slot j (f * 8 and f / 128 * 512 bytes)
     float *part;              // split-tile partials of phase 0 [tiles][units per tile][128][2]
     float *out;               // phase 1: [d], added into
@@ -436,7 +435,6 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
         const bool leader = threadIdx.x == MX_W_EPI * 32;
         uint32_t sg = 0;
         long u = ulo;
-        const float rr = (PH == 0 && a.rscale) ? __ldg(a.rscale) : 1.f;
         int done_j[2] = {-1, -1}, done_n[2] = {0, 0};  // leader: h tiles finished per expert slot
         for (;;) {
             if (leader) *s_stop = (u >= uhi || *abort_flag) ? 1u : 0u;
@@ -514,7 +512,7 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                     }
                     if (leader) a.cnt[tile] = 0;  // for the next launch
                 }
-                const float h = silu(rr * v[0]) * (rr * v[1]);
+                const float h = silu(v[0]) * v[1];
                 mx_encode_block(h, lane, (t * MX_M + qd * 32) / 32, a.himg + (size_t)j * a.f * 8,
                                 a.hsf + (size_t)j * (a.f / 128) * 512);
                 // h tiles done per expert slot, published together at the end
@@ -858,7 +856,6 @@ int launch_mx_t1(const void *x, int xdt, const uint16_t *Wr, int E, const float 
     MxArgs a1 = a0;
     a0.bimg = ximg;
     a0.bsf = ximg + (size_t)d * 8;
-    a0.rscale = nullptr;
     a0.himg = himg;
     a0.hsf = himg + (size_t)k * f * 8;
     a0.part = part;

@@ -6,10 +6,8 @@
 // combine weights are the softmax of the UNBIASED logits over the chosen set
 // ("Running Kimi K3 locally", "How is the C engine actually built?",
 // invariant 3).  ids are written in ascending order.
-#include <algorithm>
 
 #include "k3_device.cuh"
-#include "k3_mx.cuh"
 
 namespace k3 {
 
@@ -43,8 +41,7 @@ __global__ void __launch_bounds__(256) k3_router_t1(const XT *__restrict__ x,
                                                     int S, float *part, float *logits,
                                                     const float *bias, int k, int32_t *ids,
                                                     float *w, unsigned *ticket, float eps,
-                                                    float *u, uint8_t *ximg, float *r_out,
-                                                    float *zero_out)
+                                                    float *u)
 {
     const int lane = threadIdx.x & 31;
     const int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -77,17 +74,6 @@ __global__ void __launch_bounds__(256) k3_router_t1(const XT *__restrict__ x,
             if (lane == 0) part[(size_t)S * E + sp] = xx;
         }
     }
-    // the block-scaled expert products add into their output: zero it here
-    if (zero_out)
-        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d; i += gridDim.x * blockDim.x) zero_out[i] = 0.f;
-    // E2M1 pieces of x for the block-scaled expert products: warp g encodes
-    // 32-block g (the grid has at least d / 32 warps)
-    if (ximg && g < (d >> 5)) {
-        float xv;
-        if constexpr (sizeof(XT) == 4) xv = __ldg(reinterpret_cast<const float *>(x) + 32 * g + lane);
-        else xv = __uint_as_float((uint32_t)__ldg(reinterpret_cast<const uint16_t *>(x) + 32 * g + lane) << 16);
-        mx_encode_block(xv, lane, g, ximg, ximg + (size_t)d * 8);
-    }
     __shared__ unsigned s_last;
     __syncthreads();
     if (threadIdx.x == 0) s_last = (ticket_arrive(ticket) == gridDim.x - 1);
@@ -102,7 +88,6 @@ __global__ void __launch_bounds__(256) k3_router_t1(const XT *__restrict__ x,
 #pragma unroll
         for (int q = 0; q < RT1_SMAX; q++) ss += v[q];
         r = rsqrtf(ss / (float)d + eps);
-        if (r_out && threadIdx.x == 0) *r_out = r;
         const float4 *x4 = reinterpret_cast<const float4 *>(x);
         float4 *u4 = reinterpret_cast<float4 *>(u);
         const int n4 = d >> 2;
@@ -297,21 +282,19 @@ __global__ void __launch_bounds__(1024) k3_group(const int32_t *__restrict__ ids
 
 int launch_route_t1(const void *x, int xdt, const uint16_t *Wr, int E, int d, float *part,
                     float *logits, const float *bias, int k, int32_t *ids, float *w,
-                    unsigned *ticket, float eps, float *u, uint8_t *ximg, float *r_out,
-                    float *zero_out, cudaStream_t s)
+                    unsigned *ticket, float eps, float *u, cudaStream_t s)
 {
     const int S = route_t1_splits(d);
     if ((u && xdt != K3MOE_F32) || S > RT1_SMAX) return K3MOE_EINVAL;
     const int threads = 256, wpb = threads / 32;
-    const long warps = std::max((long)E * S, (long)(d / 32));
-    const int grid = (int)((warps + wpb - 1) / wpb);
+    const int grid = (int)(((long)E * S + wpb - 1) / wpb);
     if (xdt == K3MOE_F32)
         k3_router_t1<float><<<grid, threads, 0, s>>>((const float *)x, Wr, E, d, S, part, logits,
-                                                     bias, k, ids, w, ticket, eps, u, ximg, r_out, zero_out);
+                                                     bias, k, ids, w, ticket, eps, u);
     else
         k3_router_t1<__nv_bfloat16><<<grid, threads, 0, s>>>((const __nv_bfloat16 *)x, Wr, E, d,
                                                              S, part, logits, bias, k, ids, w,
-                                                             ticket, eps, u, ximg, r_out, zero_out);
+                                                             ticket, eps, u);
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
 }
 
