@@ -15,7 +15,10 @@ Other workloads of the same layer, one JSON line each (not the headline):
   --workload prefill4096  4096 bf16 tokens, selection bias ~N(0,1)
   --workload stream       4 layers x 896 experts in pinned host memory behind
                           an 8 GB HBM LRU cache, 256 tokens, RMSNorm +
-                          residual, Zipf(1.1) selection bias
+                          residual, Zipf(1.1) selection bias; the recorded
+                          trace is replayed offline (LRU, Belady, sizes);
+                          --pin-hot N pins the N most requested experts of
+                          256 untimed history tokens first
 """
 import argparse
 import json
@@ -725,6 +728,27 @@ def stream_launches(hits):
     return int((2 + 2 * (nh > 0) + 2 * nm).sum())
 
 
+def _stream_policy(k, cache, slots, n_w, n_tok, n_layers, hits, plain_lru):
+    """Offline replays of the recorded trace (warm-up + timed tokens): the
+    live hit flags reproduced by the LRU replay (plain LRU runs only), LRU
+    against Belady's optimum at this cache's size, and a sizing sweep."""
+    keys, bl = cache.trace()
+    timed = slice(keys.size - hits.size, keys.size)
+    out = {"trace_keys": int(keys.size), "timed_keys": int(hits.size)}
+    if plain_lru:
+        _, flags = k.trace_replay(keys, bl, slots, "lru")
+        out["lru_replay_reproduces_live"] = bool(np.array_equal(flags[timed], hits.reshape(-1)))
+    _, bel = k.trace_replay(keys, bl, slots, "belady")
+    out["belady_hit_rate_timed"] = round(float(bel[timed].mean()), 4)
+    caps = [16 * n_layers, 128, 256, slots, 2 * slots, 4 * slots, E * n_layers]
+    lru = k.trace_sweep(keys, bl, caps, "lru")
+    best = k.trace_sweep(keys, bl, caps, "belady")
+    out["sizing"] = {"slots": caps, "lru_hit_rate": [round(int(h) / keys.size, 4) for h in lru],
+                     "belady_hit_rate": [round(int(h) / keys.size, 4) for h in best],
+                     "note": "whole recorded trace from an empty cache"}
+    return out
+
+
 def run_stream(args, rank, world, dev_index, n_layers=4, cache_bytes=8_000_000_000, n_tok=256):
     """Host-streamed pool: n_layers x 896 experts in pinned host memory, an
     HBM LRU cache of `cache_bytes`, batch-1 tokens through all layers with
@@ -757,7 +781,8 @@ def run_stream(args, rank, world, dev_index, n_layers=4, cache_bytes=8_000_000_0
     base = host.data_ptr()
     cache = k.Cache(cache_bytes, eb, [base + q * eb for q in range(n_layers * E)], n_layers, E)
     n_w = max(args.warmup, 3)
-    X = torch.from_numpy(synth.tokens_f32(2, n_w + n_tok + 64, D, t0=rank * 100000)).to(dev)
+    n_h = 256 if args.pin_hot > 0 else 0  # history tokens before the hot set is pinned
+    X = torch.from_numpy(synth.tokens_f32(2, n_h + n_w + n_tok + 64, D, t0=rank * 100000)).to(dev)
     out = torch.empty_like(X)
     # the host link, measured in this run: pinned host -> HBM copies of one expert
     probe = torch.empty(eb, dtype=torch.uint8, device=dev)
@@ -782,6 +807,11 @@ def run_stream(args, rank, world, dev_index, n_layers=4, cache_bytes=8_000_000_0
         rates.append(16 * eb / (p0.elapsed_time(p1) * 1e-3) / 1e9)
     h2d_gbs = max(rates)
     del probe
+    if n_h:
+        k.stream_decode(layers, cache, X[:n_h], n_h, out[:n_h], 1e-6, want_trace=False)
+        k.check(cache.pin_hot(args.pin_hot), "k3moe_cache_pin_hot")
+        X, out = X[n_h:], out[n_h:]
+    cache.record_trace(True)
     k.stream_decode(layers, cache, X[:n_w], n_w, out[:n_w], 1e-6, want_trace=False)
     st0 = cache.stats()
     clock = ClockSampler(dev_index)
@@ -799,6 +829,7 @@ def run_stream(args, rank, world, dev_index, n_layers=4, cache_bytes=8_000_000_0
     clocks = clock.stop()
     ms = e0.elapsed_time(e1)
     st1 = cache.stats()
+    policy = _stream_policy(k, cache, st1["slots"], n_w, n_tok, n_layers, hits, args.pin_hot == 0)
     look = st1["lookups"] - st0["lookups"]
     nh = st1["hits"] - st0["hits"]
     h2d = st1["h2d_bytes"] - st0["h2d_bytes"]
@@ -835,7 +866,9 @@ def run_stream(args, rank, world, dev_index, n_layers=4, cache_bytes=8_000_000_0
                                  "as its copy lands, release)",
                        "l2": "inputs larger than L2 (expert slots 17.5 MB each, 64 per token)",
                        "host_pool": "every blob copied to HBM once before timing (pool warmed)",
-                       "warmup_tokens": n_w}, clocks)
+                       "warmup_tokens": n_w,
+                       "policy": ("LRU with the %d most requested experts of %d history tokens "
+                                  "pinned" % (args.pin_hot, n_h)) if n_h else "LRU"}, clocks)
     line.update({
         "cache": {"lookups": look, "hits": nh, "hit_rate": round(nh / max(look, 1), 4),
                   "h2d_bytes": h2d, "hbm_expert_bytes": hbm,
@@ -848,7 +881,8 @@ def run_stream(args, rank, world, dev_index, n_layers=4, cache_bytes=8_000_000_0
                      "peak": 1.0, "peak_source": "ideal time = hits and misses at %s HBM %.0f GB/s and "
                      "measured host link %.1f GB/s" % (src, peak, h2d_gbs), "unit": "ideal/measured",
                      "frac": round(ideal_s / (ms * 1e-3), 4), "traffic": None},
-        "wall_s": round(wall, 3), "e2e": e2e, "gpu_launches": stream_launches(hits)})
+        "wall_s": round(wall, 3), "e2e": e2e, "gpu_launches": stream_launches(hits),
+        "cache_policy": policy})
     cache.close()
     for l in layers:
         l.close()
@@ -872,6 +906,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch every step from the host")
     ap.add_argument("--workload", default="decode1", choices=["decode1"] + sorted(WORKLOADS))
+    ap.add_argument("--pin-hot", type=int, default=0,
+                    help="stream workload: run 256 untimed history tokens, then pin the N most "
+                         "requested experts of the cache's histogram before timing")
     ap.add_argument("--experts", type=int, default=896,
                     help="experts per layer (smaller pools for profiler captures; 896 is the workload)")
     args = ap.parse_args()

@@ -5,8 +5,9 @@
  * decoder straight from packed MXFP4 weights: router logits, top-k selection
  * with softmax combine weights, and for every selected expert the gate/up
  * products, SwiGLU, the down product and the weighted combine.  The 4-bit
- * codes are decoded in registers; no weight is ever expanded to float in
- * memory.
+ * codes feed block-scaled tensor-core products as stored (batch 1) or are
+ * decoded on chip, in registers or shared memory; no weight is ever expanded
+ * in device memory.
  *
  * Sources of the operations (page title, section):
  *  [EXPL]  "kimi-k3-in-c" explainer, ai.thesatyajit.com
@@ -54,6 +55,7 @@ extern "C" {
 #define K3MOE_ETIMEOUT (-4)  /* a bounded device or host wait ran out          */
 #define K3MOE_EBUSY    (-5)  /* cache: no evictable slot for a batch          */
 #define K3MOE_ENODEV   (-6)  /* no usable sm_103 device                       */
+#define K3MOE_EIO      (-7)  /* a file could not be opened, read or written   */
 
 /* Input activation types for k3moe_layer_forward. */
 #define K3MOE_F32  0
@@ -440,6 +442,81 @@ int k3moe_cache_create_with_copier(k3moe_cache **host_out, size_t capacity_bytes
 
 /* Slot index that holds `key`, or -1 (for tests). */
 int32_t k3moe_cache_slot_of(const k3moe_cache *C, int64_t key);
+
+/* ------------------------------------------------- cache policy tooling */
+
+/*
+ * Tools for choosing what the cache keeps: the pages keep a request
+ * histogram so that a hot set can be measured and pinned rather than
+ * guessed [EXPL, "The cache the project exists for"], size the expert cache
+ * from a recorded trace replayed offline [LOCAL, "the four reductions"], and
+ * compare LRU with Belady's offline optimum over capacities [ENG, "The
+ * interesting design decisions"].  All host-side: no CUDA call.
+ *
+ * A trace is n_batches batches of keys (one batch = the keys one acquire
+ * asked for, e.g. one token's experts at one layer): batch_len[b] >= 1 keys
+ * each, concatenated in keys[] (sum of batch_len keys, each >= 0).
+ */
+#define K3MOE_POLICY_LRU    0  /* the live cache's policy, decision for decision  */
+#define K3MOE_POLICY_BELADY 1  /* offline optimum: evict the farthest next use    */
+
+/* Starts (on != 0; the record is cleared) or stops recording the keys of
+ * every acquire that is placed (a refused batch is not recorded; pins are
+ * not requests and are not recorded). */
+int k3moe_cache_trace_record(k3moe_cache *C, int32_t on);
+
+/* The record so far: *host_n_keys / *host_n_batches receive its sizes; the
+ * keys and batch lengths are copied out when the host arrays are non-null
+ * and large enough (cap_keys, cap_batches), else K3MOE_EINVAL. */
+int k3moe_cache_trace_get(const k3moe_cache *C, int64_t *host_keys, int64_t cap_keys,
+                          int32_t *host_batch_len, int32_t cap_batches, int64_t *host_n_keys,
+                          int32_t *host_n_batches);
+
+/*
+ * Replays a trace through a cache of `capacity` slots.  K3MOE_POLICY_LRU
+ * makes exactly the live cache's decisions (hits first, then each miss takes
+ * the lowest EMPTY slot, else the least recently used slot, lowest index on
+ * ties, that is neither pinned nor used by the same batch; a key repeated in
+ * a batch is a hit the second time); the npinned keys of host_pinned are
+ * loaded first, into slots 0..npinned-1, and never evicted.
+ * K3MOE_POLICY_BELADY evicts the resident key, not used by the same batch,
+ * whose next use is farthest away (npinned must be 0).
+ *  host_hit_out  optional uint8 per trace key: 1 hit, 0 miss
+ *  host_hits_out receives the hit count
+ * K3MOE_EBUSY if a batch finds no evictable slot, K3MOE_EINVAL on bad
+ * arguments (a negative key, batch_len < 1, npinned > capacity).
+ */
+int k3moe_trace_replay(const int64_t *host_keys, const int32_t *host_batch_len, int32_t n_batches,
+                       int32_t capacity, int32_t policy, const int64_t *host_pinned,
+                       int32_t npinned, uint8_t *host_hit_out, int64_t *host_hits_out);
+
+/* Cache sizing: the hit count at each of ncap capacities (replays run on
+ * host threads); host_hits_out[c] is -1 where a batch does not fit. */
+int k3moe_trace_sweep(const int64_t *host_keys, const int32_t *host_batch_len, int32_t n_batches,
+                      const int32_t *host_capacities, int32_t ncap, int32_t policy,
+                      int64_t *host_hits_out);
+
+/* Hot set: the n keys with the largest counts in hist[0..nkeys), in order of
+ * decreasing count, ties to the lower key.  K3MOE_EINVAL if n > nkeys. */
+int k3moe_hot_set(const uint32_t *host_hist, int64_t nkeys, int32_t n, int64_t *host_keys_out);
+
+/* Pins the n most requested keys of the cache's own histogram (hottest
+ * first; K3MOE_EBUSY from the first that finds no slot). */
+int k3moe_cache_pin_hot(k3moe_cache *C, int32_t n, k3moe_stream compute);
+
+/* Ends a pin: the key stays cached and becomes evictable again (no-op for a
+ * key that is not pinned). */
+int k3moe_cache_unpin(k3moe_cache *C, int64_t key);
+
+/* Trace file: "K3TRACE1", int64 n_batches, int64 n_keys, int32
+ * batch_len[n_batches], int64 keys[n_keys], little-endian.  load with null
+ * arrays reports the sizes only; K3MOE_EINVAL for a file that is not such a
+ * trace (or arrays too small), K3MOE_EIO if it cannot be opened or written. */
+int k3moe_trace_save(const char *path, const int64_t *host_keys, const int32_t *host_batch_len,
+                     int32_t n_batches);
+int k3moe_trace_load(const char *path, int64_t *host_keys, int64_t cap_keys,
+                     int32_t *host_batch_len, int32_t cap_batches, int64_t *host_n_keys,
+                     int32_t *host_n_batches);
 
 /* --------------------------------------------------- streamed decode loop */
 

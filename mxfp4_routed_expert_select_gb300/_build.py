@@ -1,5 +1,6 @@
 """Builds libk3moe.so in-tree with nvcc for sm_103a (one -gencode, the
-translation units compiled in parallel, cudart linked statically)."""
+translation units -- CUDA sources and host-only C++ -- compiled in parallel,
+cudart linked statically)."""
 import os
 import subprocess
 import sys
@@ -16,7 +17,7 @@ FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", os.p
 
 
 def sources():
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
 
 
 def _stale(outputs_mtime):
@@ -32,7 +33,7 @@ def build(force=False, verbose=False, extra=()):
     procs = []
     objs = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
         objs.append(obj)
         cmd = [NVCC] + ARCH + FLAGS + list(extra) + ["-c", src, "-o", obj]
         if verbose:
@@ -48,8 +49,7 @@ def build(force=False, verbose=False, extra=()):
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(failed))
     tmp = SO + ".%d.tmp" % os.getpid()
-    subprocess.check_call([NVCC] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcuda"] if False else
-                          [NVCC] + ARCH + ["-shared", "-o", tmp] + objs)
+    subprocess.check_call([NVCC] + ARCH + ["-shared", "-o", tmp] + objs)
     os.replace(tmp, SO)
     return SO
 

@@ -106,6 +106,9 @@ struct k3moe_cache {
     CudaCopier *cuda = nullptr;     // when the default copier is used
     std::vector<int32_t> used;      // slots handed out since the last release
     std::vector<std::pair<int32_t, int64_t>> pending;  // (slot, key) copied, not waited for
+    bool tracing = false;           // record the keys of every placed batch
+    std::vector<int64_t> trace_keys;
+    std::vector<int32_t> trace_len;
 };
 
 static void cache_free(k3moe_cache *C)
@@ -305,6 +308,10 @@ static int acquire(k3moe_cache *C, const int64_t *keys, int32_t n, void **blobs_
     }
 
     // commit: recency and use marks for every slot of the batch
+    if (C->tracing) {
+        C->trace_keys.insert(C->trace_keys.end(), keys, keys + n);
+        C->trace_len.push_back(n);
+    }
     for (int32_t i = 0; i < n; i++) {
         C->hist[keys[i]]++;
         const int32_t s = slot_of[i];
@@ -409,7 +416,10 @@ int k3moe_cache_pin(k3moe_cache *C, int64_t key, k3moe_stream compute)
     // pinning is not a request: keep the request counters as they were
     const k3moe_cache_stats before = C->st;
     const uint32_t h = C->hist[key];
+    const bool tracing = C->tracing;
+    C->tracing = false;
     int rc = k3moe_cache_acquire(C, &key, 1, &blob, nullptr, compute);
+    C->tracing = tracing;
     C->st.lookups = before.lookups;
     C->st.hits = before.hits;
     C->st.misses = before.misses;
@@ -422,6 +432,56 @@ int k3moe_cache_pin(k3moe_cache *C, int64_t key, k3moe_stream compute)
         C->st.pinned++;
     }
     return k3moe_cache_release(C, compute);
+}
+
+int k3moe_cache_pin_hot(k3moe_cache *C, int32_t n, k3moe_stream compute)
+{
+    if (!C || n < 0 || n > C->nkeys) return K3MOE_EINVAL;
+    std::vector<int64_t> hot((size_t)n);
+    int rc = k3moe_hot_set(C->hist.data(), C->nkeys, n, hot.data());
+    for (int32_t i = 0; i < n && rc == K3MOE_OK; i++) rc = k3moe_cache_pin(C, hot[(size_t)i], compute);
+    return rc;
+}
+
+int k3moe_cache_unpin(k3moe_cache *C, int64_t key)
+{
+    if (!C || key < 0 || key >= C->nkeys) return K3MOE_EINVAL;
+    const int32_t s = C->where[key];
+    if (s >= 0 && C->pin[s]) {
+        C->pin[s] = 0;
+        C->st.pinned--;
+    }
+    return K3MOE_OK;
+}
+
+int k3moe_cache_trace_record(k3moe_cache *C, int32_t on)
+{
+    if (!C) return K3MOE_EINVAL;
+    if (on) {
+        C->trace_keys.clear();
+        C->trace_len.clear();
+    }
+    C->tracing = on != 0;
+    return K3MOE_OK;
+}
+
+int k3moe_cache_trace_get(const k3moe_cache *C, int64_t *keys, int64_t cap_keys, int32_t *batch_len,
+                          int32_t cap_batches, int64_t *n_keys, int32_t *n_batches)
+{
+    if (!C || !n_keys || !n_batches) return K3MOE_EINVAL;
+    const int64_t nk = (int64_t)C->trace_keys.size();
+    const int32_t nb = (int32_t)C->trace_len.size();
+    *n_keys = nk;
+    *n_batches = nb;
+    if (keys) {
+        if (cap_keys < nk) return K3MOE_EINVAL;
+        if (nk) memcpy(keys, C->trace_keys.data(), sizeof(int64_t) * (size_t)nk);
+    }
+    if (batch_len) {
+        if (cap_batches < nb) return K3MOE_EINVAL;
+        if (nb) memcpy(batch_len, C->trace_len.data(), sizeof(int32_t) * (size_t)nb);
+    }
+    return K3MOE_OK;
 }
 
 int k3moe_cache_get_stats(k3moe_cache *C, k3moe_cache_stats *out)

@@ -148,6 +148,7 @@ const char *k3moe_strerror(int st)
     case K3MOE_ETIMEOUT: return "bounded wait timed out";
     case K3MOE_EBUSY: return "no evictable cache slot";
     case K3MOE_ENODEV: return "no usable device";
+    case K3MOE_EIO: return "file input/output error";
     default: return "unknown status";
     }
 }

@@ -21,6 +21,9 @@ K3MOE_ECUDA = -3
 K3MOE_ETIMEOUT = -4
 K3MOE_EBUSY = -5
 K3MOE_ENODEV = -6
+K3MOE_EIO = -7
+K3MOE_POLICY_LRU = 0
+K3MOE_POLICY_BELADY = 1
 K3MOE_F32 = 0
 K3MOE_BF16 = 1
 K3MOE_OPT_FUSED_T1 = 1
@@ -120,6 +123,15 @@ SIGNATURES = {
     "k3moe_cache_histogram": (ctypes.POINTER(ctypes.c_uint32), [_P]),
     "k3moe_cache_create_with_copier": (ctypes.c_int, [_P, _SZ, _SZ, _P, _I, _I, _P]),
     "k3moe_cache_slot_of": (_I, [_P, _I64]),
+    "k3moe_cache_trace_record": (ctypes.c_int, [_P, _I]),
+    "k3moe_cache_trace_get": (ctypes.c_int, [_P, _P, _I64, _P, _I, _P, _P]),
+    "k3moe_cache_pin_hot": (ctypes.c_int, [_P, _I, _P]),
+    "k3moe_cache_unpin": (ctypes.c_int, [_P, _I64]),
+    "k3moe_trace_replay": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _I, _P, _P]),
+    "k3moe_trace_sweep": (ctypes.c_int, [_P, _P, _I, _P, _I, _I, _P]),
+    "k3moe_hot_set": (ctypes.c_int, [_P, _I64, _I, _P]),
+    "k3moe_trace_save": (ctypes.c_int, [ctypes.c_char_p, _P, _P, _I]),
+    "k3moe_trace_load": (ctypes.c_int, [ctypes.c_char_p, _P, _I64, _P, _I, _P, _P]),
     "k3moe_stream_decode": (ctypes.c_int, [_P, _P, _I, _P, _P, _P, _P]),
 }
 
@@ -371,6 +383,29 @@ class Cache:
     def slot_of(self, key):
         return lib().k3moe_cache_slot_of(self.h, int(key))
 
+    def record_trace(self, on=True):
+        """k3moe_cache_trace_record: start (clearing the record) or stop."""
+        check(lib().k3moe_cache_trace_record(self.h, 1 if on else 0), "k3moe_cache_trace_record")
+
+    def trace(self):
+        """k3moe_cache_trace_get: (keys int64, batch_len int32) recorded so far."""
+        nk, nb = ctypes.c_int64(), ctypes.c_int32()
+        check(lib().k3moe_cache_trace_get(self.h, None, 0, None, 0, ctypes.byref(nk),
+                                          ctypes.byref(nb)), "k3moe_cache_trace_get")
+        keys = np.zeros(nk.value, np.int64)
+        bl = np.zeros(nb.value, np.int32)
+        check(lib().k3moe_cache_trace_get(self.h, keys.ctypes.data, keys.size, bl.ctypes.data,
+                                          bl.size, ctypes.byref(nk), ctypes.byref(nb)),
+              "k3moe_cache_trace_get")
+        return keys, bl
+
+    def pin_hot(self, n, stream=0):
+        """k3moe_cache_pin_hot: pin the n most requested keys."""
+        return lib().k3moe_cache_pin_hot(self.h, int(n), stream)
+
+    def unpin(self, key):
+        return check(lib().k3moe_cache_unpin(self.h, int(key)), "k3moe_cache_unpin")
+
     def close(self):
         if self.h:
             lib().k3moe_cache_destroy(self.h)
@@ -381,6 +416,68 @@ class Cache:
             self.close()
         except Exception:
             pass
+
+
+_POLICIES = {"lru": K3MOE_POLICY_LRU, "belady": K3MOE_POLICY_BELADY}
+
+
+def _trace_arrays(keys, batch_len):
+    return np.ascontiguousarray(keys, np.int64), np.ascontiguousarray(batch_len, np.int32)
+
+
+def trace_replay(keys, batch_len, capacity, policy="lru", pinned=()):
+    """k3moe_trace_replay: (hit count, uint8 hit flag per key); the status
+    K3MOE_EBUSY is returned as a hit count of -1."""
+    keys, bl = _trace_arrays(keys, batch_len)
+    pin = np.ascontiguousarray(pinned, np.int64)
+    hit = np.zeros(keys.size, np.uint8)
+    hits = ctypes.c_int64(-1)
+    st = lib().k3moe_trace_replay(keys.ctypes.data, bl.ctypes.data, bl.size, int(capacity),
+                                  _POLICIES[policy], pin.ctypes.data if pin.size else None,
+                                  pin.size, hit.ctypes.data, ctypes.byref(hits))
+    if st == K3MOE_EBUSY:
+        return -1, hit
+    check(st, "k3moe_trace_replay")
+    return hits.value, hit
+
+
+def trace_sweep(keys, batch_len, capacities, policy="lru"):
+    """k3moe_trace_sweep: hit counts per capacity (-1 where a batch does not fit)."""
+    keys, bl = _trace_arrays(keys, batch_len)
+    caps = np.ascontiguousarray(capacities, np.int32)
+    out = np.zeros(caps.size, np.int64)
+    check(lib().k3moe_trace_sweep(keys.ctypes.data, bl.ctypes.data, bl.size, caps.ctypes.data,
+                                  caps.size, _POLICIES[policy], out.ctypes.data),
+          "k3moe_trace_sweep")
+    return out
+
+
+def hot_set(hist, n):
+    """k3moe_hot_set: the n most frequent keys, hottest first, ties to the lower key."""
+    h = np.ascontiguousarray(hist, np.uint32)
+    out = np.zeros(int(n), np.int64)
+    check(lib().k3moe_hot_set(h.ctypes.data, h.size, int(n), out.ctypes.data if n else None),
+          "k3moe_hot_set")
+    return out
+
+
+def trace_save(path, keys, batch_len):
+    keys, bl = _trace_arrays(keys, batch_len)
+    check(lib().k3moe_trace_save(os.fsencode(path), keys.ctypes.data, bl.ctypes.data, bl.size),
+          "k3moe_trace_save")
+
+
+def trace_load(path):
+    """k3moe_trace_load: (keys int64, batch_len int32)."""
+    nk, nb = ctypes.c_int64(), ctypes.c_int32()
+    p = os.fsencode(path)
+    check(lib().k3moe_trace_load(p, None, 0, None, 0, ctypes.byref(nk), ctypes.byref(nb)),
+          "k3moe_trace_load")
+    keys = np.zeros(nk.value, np.int64)
+    bl = np.zeros(nb.value, np.int32)
+    check(lib().k3moe_trace_load(p, keys.ctypes.data, keys.size, bl.ctypes.data, bl.size,
+                                 ctypes.byref(nk), ctypes.byref(nb)), "k3moe_trace_load")
+    return keys, bl
 
 
 def stream_decode(layers, cache, X, T, out, eps=1e-6, stream=None, want_trace=True):
