@@ -72,6 +72,7 @@ def lib():
         L.orc_router_logits.argtypes = [p, p, p, i, i, i]
         L.orc_topk_one.restype = d
         L.orc_topk.argtypes = [p, p, p, p, p, i, i, i]
+        L.orc_topk_sigmoid.argtypes = [p, p, p, p, p, i, i, i, i]
         L.orc_combine.argtypes = [p, p, i, i, p, p, i, p, i]
         L.orc_layer_forward.argtypes = [p, p, p, p, p, i, i, i, i, p, p, p, i]
         L.orc_rmsnorm.argtypes = [p, p, i, d]
@@ -205,15 +206,29 @@ def router_logits(x, Wr_bits):
     return out
 
 
-def topk(logits, k, bias=None):
-    """(ids ascending int32 [T,k], softmax weights [T,k], margins [T])."""
+ROUTERS = ("softmax", "sigmoid", "sigmoid_norm")
+
+
+def topk(logits, k, bias=None, router="softmax"):
+    """(ids ascending int32 [T,k], weights [T,k], margins [T]).
+
+    router "softmax": select on logit + bias, weights = softmax of the
+    unbiased selected logits.  "sigmoid" / "sigmoid_norm": select on
+    sigmoid(logit) + bias, weights = the unbiased sigmoid scores, as they are
+    or renormalised over the chosen set."""
     logits = _c(np.atleast_2d(logits), np.float64)
     T, E = logits.shape
     b = None if bias is None else _c(bias, np.float64)
     ids = np.empty((T, k), np.int32)
     w = np.empty((T, k), np.float64)
     m = np.empty(T, np.float64)
-    lib().orc_topk(_p(ids), _p(w), _p(m), _p(logits), _p(b), T, E, k)
+    if router == "softmax":
+        lib().orc_topk(_p(ids), _p(w), _p(m), _p(logits), _p(b), T, E, k)
+    elif router in ("sigmoid", "sigmoid_norm"):
+        lib().orc_topk_sigmoid(_p(ids), _p(w), _p(m), _p(logits), _p(b), T, E, k,
+                               1 if router == "sigmoid_norm" else 0)
+    else:
+        raise ValueError(router)
     return ids, w, m
 
 

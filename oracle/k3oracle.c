@@ -275,6 +275,55 @@ void orc_topk(int32_t *ids, double *w, double *margin, const double *logits, con
     }
 }
 
+/* Sigmoid router variant ("Running Kimi K3 locally", "How is the C engine
+ * actually built?", invariant 3: top-k is taken on the biased score and the
+ * combine weights are the UNBIASED sigmoid scores).  Per expert the score is
+ * s_e = 1 / (1 + e^-logit_e); the k largest s_e + bias_e are chosen, ties to
+ * the lower id, ids ascending.  w[j] = s_{ids[j]} when normalize == 0; the
+ * pages do not say whether the weights are renormalised over the chosen set,
+ * so normalize == 1 gives w[j] = s_{ids[j]} / sum_j s_{ids[j]} as the other
+ * reading.  Returns the margin on s + bias (rank k minus rank k+1). */
+double orc_topk_sigmoid_one(int32_t *ids, double *w, const double *logit, const double *bias, int E,
+                            int k, int normalize)
+{
+    double *score = (double *)malloc(sizeof(double) * (size_t)E);
+    unsigned char *taken = (unsigned char *)calloc((size_t)E, 1);
+    for (int e = 0; e < E; e++) score[e] = 1.0 / (1.0 + exp(-logit[e]));
+    double kth = 0.0, next = INFINITY;
+    for (int r = 0; r < k + 1 && r < E; r++) {
+        int best = -1;
+        double bs = 0.0;
+        for (int e = 0; e < E; e++) {
+            if (taken[e]) continue;
+            double s = score[e] + (bias ? bias[e] : 0.0);
+            if (best < 0 || s > bs) { best = e; bs = s; }
+        }
+        if (r < k) { taken[best] = 1; kth = bs; }
+        else next = bs;
+    }
+    int n = 0;
+    for (int e = 0; e < E; e++)
+        if (taken[e]) ids[n++] = e;
+    double sum = 0.0;
+    for (int j = 0; j < k; j++) { w[j] = score[ids[j]]; sum += w[j]; }
+    if (normalize)
+        for (int j = 0; j < k; j++) w[j] /= sum;
+    free(score);
+    free(taken);
+    return (k < E) ? kth - next : INFINITY;
+}
+
+void orc_topk_sigmoid(int32_t *ids, double *w, double *margin, const double *logits,
+                      const double *bias, int T, int E, int k, int normalize)
+{
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; t++) {
+        double m = orc_topk_sigmoid_one(ids + (size_t)t * k, w + (size_t)t * k,
+                                        logits + (size_t)t * E, bias, E, k, normalize);
+        if (margin) margin[t] = m;
+    }
+}
+
 /* ------------------------------------------------------------------- layer */
 
 /* out[t] = sum_j w[t][j] * expert_{ids[t][j]}(x[t]) for given routing (j in

@@ -157,6 +157,82 @@ def test_softmax_invariants():
         assert np.all(np.diff(w[t, order]) >= 0)
 
 
+# --------------------------------------------------------- sigmoid router
+
+def _logistic(z):
+    """The logistic function through tanh, an identity independent of the
+    oracle's 1 / (1 + e^-z): sigma(z) = (1 + tanh(z / 2)) / 2."""
+    return 0.5 * (1.0 + np.tanh(np.asarray(z, np.float64) / 2.0))
+
+
+def test_sigmoid_router_selects_on_sigmoid_plus_bias():
+    """Selection on sigmoid(logit) + bias, weights the unbiased sigmoid
+    scores ("Running Kimi K3 locally", 'How is the C engine actually built?',
+    invariant 3).  logits [3, 0, -1], bias [0, 0.6, 0], k = 1: sigmoid(3) =
+    0.9526 < sigmoid(0) + 0.6 = 1.1, so expert 1 is chosen, with weight
+    sigmoid(0) = 1/2 (not the biased 1.1).  Selection on logit + bias, or on
+    sigmoid(logit + bias), would choose expert 0."""
+    lg = np.array([3.0, 0.0, -1.0])
+    b = np.array([0.0, 0.6, 0.0])
+    for router in ("sigmoid", "sigmoid_norm"):
+        ids, w, m = oracle.topk(lg, 1, b, router)
+        assert list(ids[0]) == [1]
+        assert w[0, 0] == (0.5 if router == "sigmoid" else 1.0)
+        assert abs(m[0] - (1.1 - _logistic(3.0))) < 1e-15
+    assert list(oracle.topk(lg, 1, b)[0][0]) == [0]  # the softmax router's choice
+    # k = 2: experts 0 and 1, weights sigmoid(3) and 1/2
+    ids, w, _ = oracle.topk(lg, 2, b, "sigmoid")
+    assert list(ids[0]) == [0, 1]
+    assert abs(w[0, 0] - _logistic(3.0)) < 1e-15 and w[0, 1] == 0.5
+
+
+@pytest.mark.parametrize("E,k", [(8, 3), (64, 16), (896, 16)])
+def test_sigmoid_router_against_full_sort(E, k):
+    rng = np.random.default_rng(100 + E)
+    for trial in range(10):
+        lg = rng.standard_normal(E) * 2
+        if trial % 3 == 1:
+            lg = np.round(lg * 2) / 2  # many exact ties
+        bias = rng.standard_normal(E) * 0.1 if trial % 2 else None
+        ids, w, m = oracle.topk(lg, k, bias, "sigmoid")
+        s = _logistic(lg) + (bias if bias is not None else 0)
+        if trial % 3 != 1:  # no near-ties: the tanh form orders exactly alike
+            assert list(ids[0]) == _brute_topk(list(s), k)
+            srt = sorted(s, reverse=True)
+            assert abs(m[0] - (srt[k - 1] - srt[k])) < 1e-14
+        # weights: the unbiased scores of the chosen experts
+        assert np.allclose(w[0], _logistic(lg[ids[0]]), rtol=1e-14, atol=0)
+        _, wn, _ = oracle.topk(lg, k, bias, "sigmoid_norm")
+        assert abs(wn[0].sum() - 1.0) < 1e-15
+        assert np.allclose(wn[0], w[0] / w[0].sum(), rtol=1e-14, atol=0)
+
+
+def test_sigmoid_router_without_bias_selects_like_the_softmax_router():
+    """The logistic function is increasing: with no bias the chosen set is
+    that of the (pinned) softmax router, ties included."""
+    rng = np.random.default_rng(31)
+    lg = rng.standard_normal((40, 896)) * 1.7
+    lg[::5] = np.round(lg[::5] * 4) / 4
+    assert np.array_equal(oracle.topk(lg, 16, None, "sigmoid")[0], oracle.topk(lg, 16)[0])
+
+
+def test_sigmoid_router_bias_steers_selection_only():
+    """Two biases that choose the same experts give the same weights; the
+    weights never depend on the bias.  A router that took its weights from
+    the biased scores fails these checks (planted below)."""
+    rng = np.random.default_rng(32)
+    lg = rng.standard_normal((30, 896)) * 1.7
+    b1 = rng.standard_normal(896) * 0.05
+    ids1, w1, _ = oracle.topk(lg, 16, b1, "sigmoid")
+    ids2, w2, _ = oracle.topk(lg, 16, b1 + 0.37, "sigmoid")  # a constant shift keeps the choice
+    assert np.array_equal(ids1, ids2) and np.array_equal(w1, w2)
+    for t in range(30):
+        assert np.allclose(w1[t], _logistic(lg[t, ids1[t]]), rtol=1e-14, atol=0)
+    collapsed = w1 + b1[ids1]  # weights from the biased score: the mistake
+    assert not np.allclose(collapsed, _logistic(np.take_along_axis(lg, ids1.astype(np.int64), 1)),
+                           rtol=1e-6, atol=0)
+
+
 # ------------------------------------------------------------------ layer
 
 def _rand_expert(rng, d, f):
