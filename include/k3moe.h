@@ -276,10 +276,21 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int x_dtype, int32_t T, f
  *                      are the B operand as 16 E2M1 pieces per 32-block
  *                      with one E8M0 scale each, exact in fp32 to below
  *                      2e-8 of the block's largest magnitude; fp32
- *                      accumulation; the weighted combine in a fixed order.
+ *                      accumulation; the weighted combine by fp32
+ *                      reductions (summation order not fixed).
  *                      Needs d % 512 == 0, f % 512 == 0, d <= 8192,
  *                      f <= 2048, top_k <= 16.  Takes precedence over
  *                      K3MOE_OPT_FUSED_T1.  Default 1.
+ *  K3MOE_OPT_SIGMOID_ROUTER  the router scores each expert with
+ *                      s = 1 / (1 + e^-logit), selects the top_k largest
+ *                      s + sel_bias and weights the chosen experts with their
+ *                      UNBIASED scores s ("Running Kimi K3 locally", "How is
+ *                      the C engine actually built?", invariant 3).  Default
+ *                      0: selection on logit + sel_bias, weights the softmax
+ *                      of the chosen logits.  Applies to every path.
+ *  K3MOE_OPT_SIGMOID_NORM  with K3MOE_OPT_SIGMOID_ROUTER, the weights are
+ *                      divided by their sum over the chosen set (the pages do
+ *                      not say whether they are renormalised).  Default 0.
  * k3moe_layer_fused_t1 returns 1 when a batch-1 fp32 forward of this layer
  * would run fused (the block-scaled path is off or unsupported), else 0
  * (negative on error).  After a device-side timeout
@@ -290,6 +301,8 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int x_dtype, int32_t T, f
 #define K3MOE_OPT_TC       4
 #define K3MOE_OPT_TC_E4M3  8
 #define K3MOE_OPT_MX       16
+#define K3MOE_OPT_SIGMOID_ROUTER 32
+#define K3MOE_OPT_SIGMOID_NORM   64
 int k3moe_layer_set_option(k3moe_layer *L, int32_t option, int32_t value);
 int k3moe_layer_fused_t1(const k3moe_layer *L);
 /* 1 when a batch-1 forward of this layer runs on the block-scaled tensor

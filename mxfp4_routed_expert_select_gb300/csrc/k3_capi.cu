@@ -39,7 +39,7 @@ int launch_down_t1(const float *h, const ExpertSrc &src, const float *w, int k, 
                    float *out, cudaStream_t s, bool acc = false);
 int route_t1_splits(int d);
 int launch_route_t1(const void *x, int xdt, const uint16_t *Wr, int E, int d, float *part,
-                    float *logits, const float *bias, int k, int32_t *ids, float *w,
+                    float *logits, Router rt, int k, int32_t *ids, float *w,
                     unsigned *ticket, float eps, float *u, cudaStream_t s);
 bool mx_supported(int E, int k, int d, int f);
 size_t mx_part_floats(int k, int d, int f);
@@ -47,12 +47,12 @@ size_t mx_ximg_bytes(int d);
 size_t mx_himg_bytes(int k, int f);
 size_t mx_cnt_words(int k, int d, int f);
 int mx_make_maps(const DevExpert *host_table, int E, int d, int f, void *dev_maps);
-int launch_mx_t1(const void *x, int xdt, const uint16_t *Wr, int E, const float *bias, const void *maps,
+int launch_mx_t1(const void *x, int xdt, const uint16_t *Wr, int E, Router rt, const void *maps,
                  float *logits, uint8_t *ximg, uint8_t *himg, float *part, unsigned *cnt, int k, int d, int f,
                  int32_t *ids_out, float *w_out, float *out, int *err, cudaStream_t s);
 int route_multi_nsplit(int T, int E, int d);
 int launch_route_multi(const void *X, int xdt, int T, const uint16_t *Wr, int E, int d,
-                       float *part, int nsplit, float *logits, const float *bias, int k,
+                       float *part, int nsplit, float *logits, Router rt, int k,
                        int32_t *ids, float *w, cudaStream_t s);
 int launch_group(const int32_t *ids, int npairs, int E, int nt, int32_t *offsets, int32_t *perm,
                  int4 *items, int32_t *n_items, cudaStream_t s);
@@ -82,7 +82,7 @@ int launch_combine(const float *Y, int T, int k, int d, float *out, cudaStream_t
 int launch_rmsnorm(float *u, const float *x, int n, float eps, cudaStream_t s);
 int launch_residual(float *x, const float *dlt, int n, cudaStream_t s);
 bool fused_t1_supported(int E, int k, int d, int f);
-int launch_fused_t1(const float *x, const uint16_t *Wr, const float *bias, const DevExpert *table,
+int launch_fused_t1(const float *x, const uint16_t *Wr, Router rt, const DevExpert *table,
                     int E, int k, int d, int f, float *logits, int32_t *ids, float *w, float *h,
                     float *Y, float *out, unsigned long long *ctr, bool act16, cudaStream_t s);
 int fused_t1_counters();
@@ -270,6 +270,8 @@ struct k3moe_layer {
     bool router_only;    // created without a resident expert table
     bool fused;          // K3MOE_OPT_FUSED_T1
     bool act16;          // K3MOE_OPT_ACT_F16
+    bool sigmoid;        // K3MOE_OPT_SIGMOID_ROUTER
+    bool sig_norm;       // K3MOE_OPT_SIGMOID_NORM
     unsigned long long *ctr;  // monotonic cross-CTA counters of the fused kernel
     // tensor-core grouped path (T > 1)
     bool tc;             // K3MOE_OPT_TC (default on where supported)
@@ -294,6 +296,13 @@ struct k3moe_layer {
     float *mx_part;      // split-tile partial sums
     unsigned *mx_cnt;    // tile tickets (zero between launches)
 };
+
+// The layer's selection rule: its bias and score rule (K3MOE_OPT_SIGMOID_*).
+static k3::Router router_of(const k3moe_layer *L)
+{
+    return k3::Router{L->bias, L->sigmoid ? (L->sig_norm ? k3::K3_ROUTER_SIGMOID_NORM : k3::K3_ROUTER_SIGMOID)
+                                         : k3::K3_ROUTER_SOFTMAX};
+}
 
 static void layer_free(k3moe_layer *L)
 {
@@ -434,10 +443,10 @@ int k3moe_layer_destroy(k3moe_layer *L)
 static int route_into(k3moe_layer *L, const void *X, int xdt, int32_t T, cudaStream_t s)
 {
     if (T == 1)
-        return k3::launch_route_t1(X, xdt, L->Wr, L->E, L->d, L->part, L->logits, L->bias, L->k,
+        return k3::launch_route_t1(X, xdt, L->Wr, L->E, L->d, L->part, L->logits, router_of(L), L->k,
                                    L->ids, L->w, L->ticket, 0.f, nullptr, s);
     return k3::launch_route_multi(X, xdt, T, L->Wr, L->E, L->d, L->part, L->nsplit, L->logits,
-                                  L->bias, L->k, L->ids, L->w, s);
+                                  router_of(L), L->k, L->ids, L->w, s);
 }
 
 static bool valid_call(k3moe_layer *L, const void *X, int xdt, int32_t T)
@@ -467,7 +476,7 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int xdt, int32_t T, float
     if (T == 1 && L->mx && L->mx_ready) {
         // one persistent kernel: router and top-k, then the block-scaled
         // gate/up and down phases
-        K3_TRY(k3::launch_mx_t1(X, xdt, L->Wr, L->E, L->bias, L->mx_maps, L->logits, L->mx_ximg, L->mx_himg,
+        K3_TRY(k3::launch_mx_t1(X, xdt, L->Wr, L->E, router_of(L), L->mx_maps, L->logits, L->mx_ximg, L->mx_himg,
                                 L->mx_part, L->mx_cnt, L->k, L->d, L->f, L->ids, L->w, out,
                                 k3::device_error_word(), st));
         if (L->nev) {
@@ -481,7 +490,7 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int xdt, int32_t T, float
         return K3MOE_OK;
     }
     if (T == 1 && xdt == K3MOE_F32 && k3moe_layer_fused_t1(L) == 1) {
-        K3_TRY(k3::launch_fused_t1((const float *)X, L->Wr, L->bias, L->table, L->E, L->k, L->d,
+        K3_TRY(k3::launch_fused_t1((const float *)X, L->Wr, router_of(L), L->table, L->E, L->k, L->d,
                                    L->f, L->logits, L->ids, L->w, L->h, L->Y, out, L->ctr,
                                    L->act16, st));
         if (L->nev) {
@@ -560,6 +569,14 @@ int k3moe_layer_set_option(k3moe_layer *L, int32_t option, int32_t value)
     }
     if (option == K3MOE_OPT_MX) {
         L->mx = value != 0;
+        return K3MOE_OK;
+    }
+    if (option == K3MOE_OPT_SIGMOID_ROUTER) {
+        L->sigmoid = value != 0;
+        return K3MOE_OK;
+    }
+    if (option == K3MOE_OPT_SIGMOID_NORM) {
+        L->sig_norm = value != 0;
         return K3MOE_OK;
     }
     return K3MOE_EINVAL;
@@ -668,7 +685,7 @@ extern "C" int k3moe_stream_decode(const k3moe_stream_desc *D, const float *X, i
         for (int l = 0; l < D->n_layers && rc == K3MOE_OK; l++) {
             k3moe_layer *L = D->host_layers[l];
             // RMSNorm folded into the router: u = x / sqrt(mean(x^2) + eps)
-            int r = k3::launch_route_t1(xcur, K3MOE_F32, L->Wr, E, d, L->part, L->logits, L->bias,
+            int r = k3::launch_route_t1(xcur, K3MOE_F32, L->Wr, E, d, L->part, L->logits, router_of(L),
                                         k, L->ids, L->w, L->ticket, D->eps, u, st);
             if (r != K3MOE_OK) {
                 fail(r);

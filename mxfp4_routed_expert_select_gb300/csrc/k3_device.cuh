@@ -418,8 +418,43 @@ K3_DEV uint32_t okey(float v)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The router's rule ("Running Kimi K3 locally", "How is the C engine actually
+// built?", invariant 3: the bias steers the selection only, the combine
+// weights come from the unbiased scores):
+//  K3_ROUTER_SOFTMAX       select on logit + bias; weights = softmax of the
+//                          chosen experts' logits
+//  K3_ROUTER_SIGMOID       score = 1 / (1 + e^-logit); select on score + bias;
+//                          weights = the chosen experts' scores
+//  K3_ROUTER_SIGMOID_NORM  as K3_ROUTER_SIGMOID, weights divided by their sum
+enum : int { K3_ROUTER_SOFTMAX = 0, K3_ROUTER_SIGMOID = 1, K3_ROUTER_SIGMOID_NORM = 2 };
+struct Router {
+    const float *bias;  // [E] selection bias, or null
+    int mode;           // K3_ROUTER_*
+};
+K3_DEV float router_sigmoid(float l) { return 1.f / (1.f + expf(-l)); }
+// selection key of expert e with logit l
+K3_DEV float router_select(const Router &r, float l, int e)
+{
+    const float s = r.mode == K3_ROUTER_SOFTMAX ? l : router_sigmoid(l);
+    return r.bias ? s + __ldg(r.bias + e) : s;
+}
+// combine weight of the chosen expert held by this lane (on = lane < k, l its
+// logit); every lane of the warp calls it
+K3_DEV float router_weight(int mode, float l, bool on)
+{
+    if (mode == K3_ROUTER_SOFTMAX) {
+        float mx = on ? l : -INFINITY;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float ex = on ? expf(l - mx) : 0.f;
+        return ex / warp_sum(ex);
+    }
+    const float sg = on ? router_sigmoid(l) : 0.f;
+    return mode == K3_ROUTER_SIGMOID ? sg : sg / warp_sum(sg);
+}
+
 // 256 threads (threadIdx.x 0..255, synchronised by sync()) select the top k (k <= 32) of E <= 1024
-// scores logit[e] + bias[e] (bias may be null), ties to the lower id, with the
+// selection keys router_select(rt, logit[e], e), ties to the lower id, with the
 // same result as warp_topk below: the k-th largest key is found one byte at a
 // time (4 rounds of a 256-bin shared-memory histogram over the keys that
 // match the prefix so far, warp-aggregated atomics, and a descending scan by
@@ -432,7 +467,7 @@ struct CtaTopkSmem {
     unsigned prefix, need;
 };
 template <typename Sync, typename Logit>
-K3_DEV void cta_topk_by(Logit logit_of, const float *bias, int E, int k, int32_t *ids_out, float *w_out,
+K3_DEV void cta_topk_by(Logit logit_of, const Router &rt, int E, int k, int32_t *ids_out, float *w_out,
                         CtaTopkSmem &sm, Sync sync)
 {
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -441,7 +476,7 @@ K3_DEV void cta_topk_by(Logit logit_of, const float *bias, int E, int k, int32_t
     for (int m = 0; m < 4; m++) {
         const int e = t + 256 * m;
         key[m] = 0u;  // below every real key
-        if (e < E) key[m] = okey(logit_of(e) + (bias ? __ldg(bias + e) : 0.f));
+        if (e < E) key[m] = okey(router_select(rt, logit_of(e), e));
     }
     uint32_t prefix = 0u, mask = 0u;
     unsigned need = (unsigned)k;
@@ -541,34 +576,30 @@ K3_DEV void cta_topk_by(Logit logit_of, const float *bias, int E, int k, int32_t
     sync();
     if (warp == 0) {
         const int my_id = (lane < k) ? sm.ids[lane] : 0;
-        const float l = (lane < k) ? logit_of(my_id) : -INFINITY;
-        float mx = l;
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        const float ex = (lane < k) ? expf(l - mx) : 0.f;
-        const float sum = warp_sum(ex);
+        const float wv = router_weight(rt.mode, (lane < k) ? logit_of(my_id) : 0.f, lane < k);
         if (lane < k) {
             ids_out[lane] = my_id;
-            w_out[lane] = ex / sum;
+            w_out[lane] = wv;
         }
     }
 }
 // logits in global memory (ld.cg: other CTAs may have written them)
 template <typename Sync>
-K3_DEV void cta_topk(const float *logit, const float *bias, int E, int k, int32_t *ids_out, float *w_out,
+K3_DEV void cta_topk(const float *logit, const Router &rt, int E, int k, int32_t *ids_out, float *w_out,
                      CtaTopkSmem &sm, Sync sync)
 {
-    cta_topk_by([&](int e) { return __ldcg(logit + e); }, bias, E, k, ids_out, w_out, sm, sync);
+    cta_topk_by([&](int e) { return __ldcg(logit + e); }, rt, E, k, ids_out, w_out, sm, sync);
 }
 
-// One warp selects the top k (k <= 32) of E <= 1024 scores logit[e] + bias[e]
-// (bias may be null), ties to the lower id: a radix search for the k-th
-// largest key (32 rounds of one count and one warp reduction), then every
-// key above it and the lowest-id ties at it.  ids_out[0..k) receives the ids
-// in ascending order and w_out the softmax of the UNBIASED logits over the
-// chosen set ("Running Kimi K3 locally", invariant 3).  logit is read with
-// ld.cg (other CTAs may have written it); ids_out is read back by the warp.
-K3_DEV void warp_topk(const float *logit, const float *bias, int E, int k, int32_t *ids_out,
+// One warp selects the top k (k <= 32) of E <= 1024 selection keys
+// router_select(rt, logit[e], e), ties to the lower id: a radix search for
+// the k-th largest key (32 rounds of one count and one warp reduction), then
+// every key above it and the lowest-id ties at it.  ids_out[0..k) receives
+// the ids in ascending order and w_out the router's weights from the
+// UNBIASED scores ("Running Kimi K3 locally", invariant 3).  logit is read
+// with ld.cg (other CTAs may have written it); ids_out is read back by the
+// warp.
+K3_DEV void warp_topk(const float *logit, const Router &rt, int E, int k, int32_t *ids_out,
                       float *w_out, int lane)
 {
     uint32_t key[32];
@@ -576,7 +607,7 @@ K3_DEV void warp_topk(const float *logit, const float *bias, int E, int k, int32
     for (int q = 0; q < 32; q++) {
         const int e = lane + 32 * q;
         key[q] = 0u;  // below every real key (okey(-inf) = 0x007fffff)
-        if (e < E) key[q] = okey(__ldcg(logit + e) + (bias ? __ldg(bias + e) : 0.f));
+        if (e < E) key[q] = okey(router_select(rt, __ldcg(logit + e), e));
     }
     uint32_t T = 0u;  // largest T with count(key >= T) >= k
     for (int b = 31; b >= 0; b--) {
@@ -609,13 +640,8 @@ K3_DEV void warp_topk(const float *logit, const float *bias, int E, int k, int32
     }
     __syncwarp();
     const int my_id = (lane < k) ? ids_out[lane] : 0;
-    const float l = (lane < k) ? __ldcg(logit + my_id) : -INFINITY;
-    float mx = l;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    const float ex = (lane < k) ? expf(l - mx) : 0.f;
-    const float sum = warp_sum(ex);
-    if (lane < k) w_out[lane] = ex / sum;
+    const float wv = router_weight(rt.mode, (lane < k) ? __ldcg(logit + my_id) : 0.f, lane < k);
+    if (lane < k) w_out[lane] = wv;
     __syncwarp();
 }
 

@@ -49,7 +49,7 @@ constexpr int FU_NCTR = FU_CTR_GEN + 1;
 struct FusedArgs {
     const float *x;          // [d]
     const uint16_t *Wr;      // [E][d] bf16
-    const float *bias;       // [E] or null
+    Router rt;               // selection bias ([E] or null) and score rule
     const DevExpert *table;  // [E]
     int E, k, d, f;
     float *logits;           // [E]
@@ -129,7 +129,7 @@ K3_DEV float bf16x8_dotf(uint4 wv, const float *xv, float acc)
 // / sel_w (shared memory); CTA 0 also writes them to the layer's ids / w.
 K3_DEV void topk_phase(const FusedArgs &a, int *sel_ids, float *sel_w, CtaTopkSmem &tk)
 {
-    cta_topk(a.logits, a.bias, a.E, a.k, sel_ids, sel_w, tk, [] { named_sync(2, 256); });
+    cta_topk(a.logits, a.rt, a.E, a.k, sel_ids, sel_w, tk, [] { named_sync(2, 256); });
     const int lane = threadIdx.x & 31;
     if (threadIdx.x < 32) {
         __syncwarp();
@@ -522,14 +522,14 @@ size_t fused_t1_smem(int d, int f, int *S_out, uint32_t *slot_out)
     return total(S);
 }
 
-int launch_fused_t1(const float *x, const uint16_t *Wr, const float *bias, const DevExpert *table,
+int launch_fused_t1(const float *x, const uint16_t *Wr, Router rt, const DevExpert *table,
                     int E, int k, int d, int f, float *logits, int32_t *ids, float *w, float *h,
                     float *Y, float *out, unsigned long long *ctr, bool act16, cudaStream_t s)
 {
     FusedArgs a;
     a.x = x;
     a.Wr = Wr;
-    a.bias = bias;
+    a.rt = rt;
     a.table = table;
     a.E = E;
     a.k = k;

@@ -553,7 +553,7 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
 struct MxRoute {
     const void *x;          // [d] fp32 or bf16
     const uint16_t *Wr;     // [E][d] bf16
-    const float *bias;      // [E] selection bias or null
+    Router rt;              // selection bias ([E] or null) and score rule
     float *logits;          // [E]
     uint8_t *ximg;          // pieces of x: B image, then scale atoms
     int32_t *ids_out;       // [k] selection (ascending ids), written by CTA 0
@@ -646,7 +646,7 @@ K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, uint8_t *sm
         }
     }
     cta_sync_threads();
-    cta_topk_by([&](int e) { return s_logit[e]; }, r.bias, E, a0.k, sel_ids, sel_w, tk,
+    cta_topk_by([&](int e) { return s_logit[e]; }, r.rt, E, a0.k, sel_ids, sel_w, tk,
                 [] { cta_sync_threads(); });
     cta_sync_threads();
     if (blockIdx.x == 0 && threadIdx.x < a0.k) {
@@ -827,7 +827,7 @@ static int launch_layer(const MxRoute &r, const MxArgs &a0, const MxArgs &a1, un
     return K3MOE_OK;
 }
 
-int launch_mx_t1(const void *x, int xdt, const uint16_t *Wr, int E, const float *bias, const void *maps,
+int launch_mx_t1(const void *x, int xdt, const uint16_t *Wr, int E, Router rt, const void *maps,
                  float *logits, uint8_t *ximg, uint8_t *himg, float *part, unsigned *cnt, int k, int d, int f,
                  int32_t *ids_out, float *w_out, float *out, int *err, cudaStream_t s)
 {
@@ -841,7 +841,7 @@ int launch_mx_t1(const void *x, int xdt, const uint16_t *Wr, int E, const float 
     MxRoute r = {};
     r.x = x;
     r.Wr = Wr;
-    r.bias = bias;
+    r.rt = rt;
     r.logits = logits;
     r.ximg = ximg;
     r.ids_out = ids_out;

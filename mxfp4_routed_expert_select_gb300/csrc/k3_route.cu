@@ -2,10 +2,11 @@
 // and grouping of (token, slot) pairs by expert (sm_103a).
 //
 // Router: logits[t][e] = sum_i W_r[e][i] x[t][i], W_r bf16, fp32 accumulate.
-// Selection: the top_k largest (logit + sel_bias), ties to the lower id; the
-// combine weights are the softmax of the UNBIASED logits over the chosen set
-// ("Running Kimi K3 locally", "How is the C engine actually built?",
-// invariant 3).  ids are written in ascending order.
+// Selection: the top_k largest selection keys (logit + sel_bias, or
+// sigmoid(logit) + sel_bias for the sigmoid router), ties to the lower id; the
+// combine weights come from the UNBIASED scores of the chosen set ("Running
+// Kimi K3 locally", "How is the C engine actually built?", invariant 3).  ids
+// are written in ascending order.
 
 #include "k3_device.cuh"
 
@@ -39,7 +40,7 @@ template <typename XT>
 __global__ void __launch_bounds__(256) k3_router_t1(const XT *__restrict__ x,
                                                     const uint16_t *__restrict__ Wr, int E, int d,
                                                     int S, float *part, float *logits,
-                                                    const float *bias, int k, int32_t *ids,
+                                                    Router rt, int k, int32_t *ids,
                                                     float *w, unsigned *ticket, float eps,
                                                     float *u)
 {
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(256) k3_router_t1(const XT *__restrict__ x,
     }
     __syncthreads();
     __shared__ CtaTopkSmem tk;
-    cta_topk(logits, bias, E, k, ids, w, tk, [] { __syncthreads(); });
+    cta_topk(logits, rt, E, k, ids, w, tk, [] { __syncthreads(); });
     if (threadIdx.x == 0) *ticket = 0;  // ready for the next launch on this stream
 }
 
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(256) k3_router_tiled(const XT *__restrict__ X,
 
 // Sums split-K partials in fixed order, then selects per token (warp/token).
 __global__ void __launch_bounds__(256) k3_topk_multi(const float *__restrict__ part, int nsplit,
-                                                     int T, int E, const float *bias, int k,
+                                                     int T, int E, Router rt, int k,
                                                      float *logits, int32_t *ids, float *w)
 {
     const int lane = threadIdx.x & 31;
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(256) k3_topk_multi(const float *__restrict__ p
         lg[e] = s;
     }
     __syncwarp();
-    warp_topk(lg, bias, E, k, ids + (size_t)t * k, w + (size_t)t * k, lane);
+    warp_topk(lg, rt, E, k, ids + (size_t)t * k, w + (size_t)t * k, lane);
 }
 
 // ---------------------------------------------------------------- grouping
@@ -281,7 +282,7 @@ __global__ void __launch_bounds__(1024) k3_group(const int32_t *__restrict__ ids
 // ------------------------------------------------------------- launchers
 
 int launch_route_t1(const void *x, int xdt, const uint16_t *Wr, int E, int d, float *part,
-                    float *logits, const float *bias, int k, int32_t *ids, float *w,
+                    float *logits, Router rt, int k, int32_t *ids, float *w,
                     unsigned *ticket, float eps, float *u, cudaStream_t s)
 {
     const int S = route_t1_splits(d);
@@ -290,10 +291,10 @@ int launch_route_t1(const void *x, int xdt, const uint16_t *Wr, int E, int d, fl
     const int grid = (int)(((long)E * S + wpb - 1) / wpb);
     if (xdt == K3MOE_F32)
         k3_router_t1<float><<<grid, threads, 0, s>>>((const float *)x, Wr, E, d, S, part, logits,
-                                                     bias, k, ids, w, ticket, eps, u);
+                                                     rt, k, ids, w, ticket, eps, u);
     else
         k3_router_t1<__nv_bfloat16><<<grid, threads, 0, s>>>((const __nv_bfloat16 *)x, Wr, E, d,
-                                                             S, part, logits, bias, k, ids, w,
+                                                             S, part, logits, rt, k, ids, w,
                                                              ticket, eps, u);
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
 }
@@ -314,13 +315,13 @@ int launch_router_tc(const uint16_t *X, int T, const uint16_t *Wr, int E, int d,
 int *device_error_word();
 
 int launch_route_multi(const void *X, int xdt, int T, const uint16_t *Wr, int E, int d,
-                       float *part, int nsplit, float *logits, const float *bias, int k,
+                       float *part, int nsplit, float *logits, Router rt, int k,
                        int32_t *ids, float *w, cudaStream_t s)
 {
     // bf16 tokens in numbers: the logits as a tensor-core GEMM
     if (xdt == K3MOE_BF16 && T >= 128 && d % 64 == 0 &&
         launch_router_tc((const uint16_t *)X, T, Wr, E, d, part, device_error_word(), s) == K3MOE_OK) {
-        k3_topk_multi<<<(T + 7) / 8, 256, 0, s>>>(part, 1, T, E, bias, k, logits, ids, w);
+        k3_topk_multi<<<(T + 7) / 8, 256, 0, s>>>(part, 1, T, E, rt, k, logits, ids, w);
         return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
     }
     int klen = (d + nsplit - 1) / nsplit;
@@ -332,7 +333,7 @@ int launch_route_multi(const void *X, int xdt, int T, const uint16_t *Wr, int E,
     else
         k3_router_tiled<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16 *)X, T, Wr, E,
                                                             d, klen, part);
-    k3_topk_multi<<<(T + 7) / 8, 256, 0, s>>>(part, ns, T, E, bias, k, logits, ids, w);
+    k3_topk_multi<<<(T + 7) / 8, 256, 0, s>>>(part, ns, T, E, rt, k, logits, ids, w);
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
 }
 

@@ -31,6 +31,8 @@ K3MOE_OPT_ACT_F16 = 2
 K3MOE_OPT_TC = 4
 K3MOE_OPT_TC_E4M3 = 8
 K3MOE_OPT_MX = 16
+K3MOE_OPT_SIGMOID_ROUTER = 32
+K3MOE_OPT_SIGMOID_NORM = 64
 K3MOE_NOALLOC_MAX_F = 2048
 
 

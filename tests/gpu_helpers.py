@@ -52,9 +52,11 @@ def router_tensor(bits, dev="cuda"):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev)
 
 
-def margin_subs(pool, T, d, Wr_bits, k_, bias=None, gap=1e-3, bf16=False, max_tries=50):
+def margin_subs(pool, T, d, Wr_bits, k_, bias=None, gap=1e-3, bf16=False, max_tries=50,
+                router="softmax"):
     """Per-token substream indices such that the oracle's rank-k / rank-k+1
-    gap (on logit + bias) is at least `gap`."""
+    gap (on the router's selection key: logit + bias, or sigmoid(logit) +
+    bias) is at least `gap`."""
     subs = np.zeros(T, np.int64)
     todo = np.arange(T)
     b = None if bias is None else np.asarray(bias, np.float64)
@@ -63,7 +65,7 @@ def margin_subs(pool, T, d, Wr_bits, k_, bias=None, gap=1e-3, bf16=False, max_tr
             return subs
         X = tokens(pool, todo, d, subs[todo], bf16)
         lg = oracle.router_logits(X, Wr_bits)
-        _, _, m = oracle.topk(lg, k_, b)
+        _, _, m = oracle.topk(lg, k_, b, router)
         bad = m < gap
         subs[todo[bad]] += 1
         todo = todo[bad]
