@@ -22,7 +22,8 @@
  *  - Pointers are DEVICE pointers unless the parameter name starts with
  *    `host_`.  Device buffers must be 16-byte aligned.
  *  - The caller owns every buffer it passes; the library owns only the objects
- *    it creates (layer, cache) and frees them in the matching destroy call.
+ *    it creates (layer, cache, trunk) and frees them in the matching destroy
+ *    call.
  *  - Work is enqueued on the caller's stream `s` (a cudaStream_t; NULL is the
  *    legacy default stream) and returns before the GPU finishes.  Outputs are
  *    valid once the stream has reached that point.
@@ -53,7 +54,7 @@ extern "C" {
 #define K3MOE_ENOMEM   (-2)  /* an allocation the call needs failed           */
 #define K3MOE_ECUDA    (-3)  /* a CUDA runtime call failed                    */
 #define K3MOE_ETIMEOUT (-4)  /* a bounded device or host wait ran out          */
-#define K3MOE_EBUSY    (-5)  /* cache: no evictable slot for a batch          */
+#define K3MOE_EBUSY    (-5)  /* cache or trunk: no free slot for the request  */
 #define K3MOE_ENODEV   (-6)  /* no usable sm_103 device                       */
 #define K3MOE_EIO      (-7)  /* a file could not be opened, read or written   */
 
@@ -530,6 +531,70 @@ int k3moe_trace_save(const char *path, const int64_t *host_keys, const int32_t *
 int k3moe_trace_load(const char *path, int64_t *host_keys, int64_t cap_keys,
                      int32_t *host_batch_len, int32_t cap_batches, int64_t *host_n_keys,
                      int32_t *host_n_batches);
+
+/* ------------------------------------------------ dense trunk streaming */
+
+/*
+ * Per-layer weights that every token reads in the same order (the pages'
+ * dense trunk: layer 0, 1, ..., M-1 on every token) kept as a pinned prefix
+ * plus a ring of streaming slots [LOCAL, "the four reductions", reduction
+ * three; ENG, "The interesting design decisions"]: a cyclic scan defeats
+ * LRU (an LRU of C < M slots hits nothing), while a resident prefix of P
+ * layers hits exactly P/M.
+ *
+ *  host_layers[M]       host pointers to each layer's bytes (pinned by the
+ *                       caller for full speed), host_layer_bytes[M] sizes
+ *                       (each > 0, a multiple of 16)
+ *  pinned_bytes         HBM budget of the prefix: layers 0..P-1 are resident,
+ *                       P the largest count whose sizes (rounded up to 256 B)
+ *                       fit; they are copied once, stream-ordered
+ *  ring_slots           R streaming slots of the largest streamed layer's
+ *                       size; R >= 1 when P < M (R >= 2 lets the next layer
+ *                       copy while the current one computes)
+ *
+ * The streamed layers P..M-1 are expected in cyclic order (after M-1 comes
+ * P of the next token).  The n-th streamed request uses ring slot n mod R;
+ * after each acquire and release the copies of the next layers are issued
+ * into free slots (at most R - 1 ahead), each after the release of the
+ * slot's previous layer.  A request out of that order is served too, with
+ * its copy issued on demand.  A failed prefetch copy is not an error of the
+ * call that issued it: the layer is copied again when it is requested, and
+ * that request returns the copier's code if the copy fails again.
+ */
+typedef struct k3moe_trunk k3moe_trunk;
+
+typedef struct {
+    int64_t requests;       /* acquires                                       */
+    int64_t resident;       /* acquires of prefix layers                      */
+    int64_t prefetched;     /* streamed acquires whose copy was already issued */
+    int64_t h2d_bytes;      /* bytes copied host -> HBM (prefix included)     */
+    int32_t n_layers;
+    int32_t pinned_layers;  /* P */
+    int32_t ring_slots;     /* R */
+    int32_t reserved;
+} k3moe_trunk_stats;
+
+int k3moe_trunk_create(k3moe_trunk **host_out, const void *const *host_layers,
+                       const size_t *host_layer_bytes, int32_t n_layers, size_t pinned_bytes,
+                       int32_t ring_slots);
+/* The same over a copier (k3moe_copier below the cache): copier slots
+ * 0..P-1 are the prefix layers, P..P+R-1 the ring.  No CUDA call. */
+int k3moe_trunk_create_with_copier(k3moe_trunk **host_out, const void *const *host_layers,
+                                   const size_t *host_layer_bytes, int32_t n_layers,
+                                   size_t pinned_bytes, int32_t ring_slots,
+                                   const k3moe_copier *host_copier);
+int k3moe_trunk_destroy(k3moe_trunk *T);
+
+/* Device pointer of `layer`'s bytes, usable on `compute` (which is made to
+ * wait for its copy).  host_resident_out (optional) receives 1 for a prefix
+ * layer.  The layer stays valid until k3moe_trunk_release.  K3MOE_EBUSY if
+ * its ring slot still holds a layer that has not been released. */
+int k3moe_trunk_acquire(k3moe_trunk *T, int32_t layer, void **host_dev_out,
+                        uint8_t *host_resident_out, k3moe_stream compute);
+/* Ends the use of an acquired layer: records on `compute` the point after
+ * which its ring slot may be overwritten (no-op for a prefix layer). */
+int k3moe_trunk_release(k3moe_trunk *T, int32_t layer, k3moe_stream compute);
+int k3moe_trunk_get_stats(const k3moe_trunk *T, k3moe_trunk_stats *host_out);
 
 /* --------------------------------------------------- streamed decode loop */
 

@@ -69,6 +69,16 @@ class CacheStats(ctypes.Structure):
         return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
 
 
+class TrunkStats(ctypes.Structure):
+    _fields_ = [("requests", ctypes.c_int64), ("resident", ctypes.c_int64),
+                ("prefetched", ctypes.c_int64), ("h2d_bytes", ctypes.c_int64),
+                ("n_layers", ctypes.c_int32), ("pinned_layers", ctypes.c_int32),
+                ("ring_slots", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
+
+
 class StreamDesc(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("host_layers", ctypes.c_void_p),
                 ("cache", ctypes.c_void_p), ("eps", ctypes.c_float)]
@@ -135,6 +145,12 @@ SIGNATURES = {
     "k3moe_trace_save": (ctypes.c_int, [ctypes.c_char_p, _P, _P, _I]),
     "k3moe_trace_load": (ctypes.c_int, [ctypes.c_char_p, _P, _I64, _P, _I, _P, _P]),
     "k3moe_stream_decode": (ctypes.c_int, [_P, _P, _I, _P, _P, _P, _P]),
+    "k3moe_trunk_create": (ctypes.c_int, [_P, _P, _P, _I, _SZ, _I]),
+    "k3moe_trunk_create_with_copier": (ctypes.c_int, [_P, _P, _P, _I, _SZ, _I, _P]),
+    "k3moe_trunk_destroy": (ctypes.c_int, [_P]),
+    "k3moe_trunk_acquire": (ctypes.c_int, [_P, _I, _P, _P, _P]),
+    "k3moe_trunk_release": (ctypes.c_int, [_P, _I, _P]),
+    "k3moe_trunk_get_stats": (ctypes.c_int, [_P, _P]),
 }
 
 _lib = None
@@ -411,6 +427,57 @@ class Cache:
     def close(self):
         if self.h:
             lib().k3moe_cache_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Trunk:
+    """k3moe_trunk_* : per-layer weights as a resident prefix plus a ring of
+    streaming slots."""
+
+    def __init__(self, host_layer_ptrs, layer_bytes, pinned_bytes, ring_slots, copier=None):
+        n = len(host_layer_ptrs)
+        self._ptrs = (ctypes.c_void_p * n)(*host_layer_ptrs)
+        self._bytes = (ctypes.c_size_t * n)(*layer_bytes)
+        h = ctypes.c_void_p()
+        if copier is None:
+            st = lib().k3moe_trunk_create(ctypes.byref(h), ctypes.cast(self._ptrs, ctypes.c_void_p),
+                                          ctypes.cast(self._bytes, ctypes.c_void_p), n,
+                                          int(pinned_bytes), int(ring_slots))
+        else:
+            self._copier = copier
+            st = lib().k3moe_trunk_create_with_copier(
+                ctypes.byref(h), ctypes.cast(self._ptrs, ctypes.c_void_p),
+                ctypes.cast(self._bytes, ctypes.c_void_p), n, int(pinned_bytes), int(ring_slots),
+                ctypes.byref(copier))
+        check(st, "k3moe_trunk_create")
+        self.h = h
+
+    def acquire(self, layer, stream=0, raise_on_error=True):
+        """(device pointer, resident flag, status)."""
+        p = ctypes.c_void_p()
+        res = ctypes.c_uint8()
+        st = lib().k3moe_trunk_acquire(self.h, int(layer), ctypes.byref(p), ctypes.byref(res), stream)
+        if raise_on_error:
+            check(st, "k3moe_trunk_acquire")
+        return p.value, res.value, st
+
+    def release(self, layer, stream=0):
+        return lib().k3moe_trunk_release(self.h, int(layer), stream)
+
+    def stats(self):
+        s = TrunkStats()
+        check(lib().k3moe_trunk_get_stats(self.h, ctypes.byref(s)), "k3moe_trunk_get_stats")
+        return s.as_dict()
+
+    def close(self):
+        if self.h:
+            lib().k3moe_trunk_destroy(self.h)
             self.h = None
 
     def __del__(self):
