@@ -3,8 +3,9 @@
  *
  * The library computes the routed-expert layer of a mixture-of-experts
  * decoder straight from packed MXFP4 weights: router logits, top-k selection
- * with softmax combine weights, and for every selected expert the gate/up
- * products, SwiGLU, the down product and the weighted combine.  The 4-bit
+ * with combine weights from the unbiased scores, and for every selected
+ * expert the gate/up products, SwiGLU, the down product and the weighted
+ * combine.  The 4-bit
  * codes feed block-scaled tensor-core products as stored (batch 1) or are
  * decoded on chip, in registers or shared memory; no weight is ever expanded
  * in device memory.
@@ -217,7 +218,8 @@ int k3moe_layer_destroy(k3moe_layer *L);
 /*
  * Routing only: logits = X W_r^T (fp32 accumulation), the top_k experts by
  * logit + sel_bias (ties to the lower id), ids ascending, and w = softmax of
- * the unbiased logits over the chosen set.
+ * the unbiased logits over the chosen set (or the sigmoid rule of
+ * K3MOE_OPT_SIGMOID_ROUTER below).
  *  X    [T x d], x_dtype K3MOE_F32 or K3MOE_BF16
  *  ids  int32 [T x top_k] (out), w fp32 [T x top_k] (out)
  */

@@ -3,7 +3,7 @@
 //
 //   phase R  router logits  (bf16 W_r rows streamed, fp32 x)
 //   -- grid barrier (the only one) --
-//   phase T  top-k + softmax (every CTA computes the same selection)
+//   phase T  top-k + combine weights (every CTA computes the same selection)
 //   phase G  gate/up products + SwiGLU of the k experts -> h   (MXFP4)
 //            each finished stage bumps its expert's "h rows done" counter
 //   phase D  down products -> w_j * y_j, once its expert's h is complete

@@ -1,4 +1,4 @@
-// k3_route.cu -- router logits, top-k selection with softmax combine weights,
+// k3_route.cu -- router logits, top-k selection with its combine weights,
 // and grouping of (token, slot) pairs by expert (sm_103a).
 //
 // Router: logits[t][e] = sum_i W_r[e][i] x[t][i], W_r bf16, fp32 accumulate.
