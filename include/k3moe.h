@@ -5,10 +5,9 @@
  * decoder straight from packed MXFP4 weights: router logits, top-k selection
  * with combine weights from the unbiased scores, and for every selected
  * expert the gate/up products, SwiGLU, the down product and the weighted
- * combine.  The 4-bit
- * codes feed block-scaled tensor-core products as stored (batch 1) or are
- * decoded on chip, in registers or shared memory; no weight is ever expanded
- * in device memory.
+ * combine.  The 4-bit codes feed block-scaled tensor-core products as stored
+ * (batch 1) or are decoded on chip, in registers or shared memory; no weight
+ * is ever expanded in device memory.
  *
  * Sources of the operations (page title, section):
  *  [EXPL]  "kimi-k3-in-c" explainer, ai.thesatyajit.com
