@@ -73,6 +73,10 @@ def lib():
         L.orc_topk_one.restype = d
         L.orc_topk.argtypes = [p, p, p, p, p, i, i, i]
         L.orc_topk_sigmoid.argtypes = [p, p, p, p, p, i, i, i, i]
+        L.orc_mx_quant_block.restype = i
+        L.orc_mx_quant_block.argtypes = [p, p]
+        L.orc_mx_quantize.argtypes = [p, p, p, p, i]
+        L.orc_expert_forward_mxq.argtypes = [p, p, p]
         L.orc_combine.argtypes = [p, p, i, i, p, p, i, p, i]
         L.orc_layer_forward.argtypes = [p, p, p, p, p, i, i, i, i, p, p, p, i]
         L.orc_rmsnorm.argtypes = [p, p, i, d]
@@ -187,6 +191,27 @@ def expert_forward(ex, x, h_bf16=False, want_h=False):
     h = np.empty(f, np.float64) if want_h else None
     lib().orc_expert_forward_ex(_p(y), ctypes.byref(e), _p(x), int(bool(h_bf16)), _p(h))
     return (y, h) if want_h else y
+
+
+def mx_quantize(x):
+    """MXFP4 quantisation of fp32 activations (OCP rule): (values float64 [n],
+    codes uint8 [n], scale bytes uint8 [n/32]); n a multiple of 32."""
+    x = _c(x, np.float32).ravel()
+    assert x.size % 32 == 0
+    xq = np.empty(x.size, np.float64)
+    codes = np.empty(x.size, np.uint8)
+    sc = np.empty(x.size // 32, np.uint8)
+    lib().orc_mx_quantize(_p(xq), _p(codes), _p(sc), _p(x), x.size)
+    return xq, codes, sc
+
+
+def expert_forward_mxq(ex, x):
+    """One expert with MXFP4-quantised activations x (fp32 [d]) and h."""
+    e = make_expert(ex)
+    x = _c(x, np.float32)
+    y = np.empty(e.gate.in_, np.float64)
+    lib().orc_expert_forward_mxq(_p(y), ctypes.byref(e), _p(x))
+    return y
 
 
 # ------------------------------------------------------------------ router

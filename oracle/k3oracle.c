@@ -209,6 +209,89 @@ void orc_expert_forward(double *y, const orc_expert *E, const double *x)
     orc_expert_forward_ex(y, E, x, 0, NULL);
 }
 
+/* ------------------------------------------- MXFP4 activations (mode B) */
+
+/* Quantisation of activations to MXFP4 for a block-scaled product whose B
+ * operand is E2M1 too.  The pages store only weights this way; the rule for
+ * activations is the OCP Microscaling v1.0 conversion (a reading, not the
+ * pages'): per 32-block the shared exponent is floor(log2(amax)) minus the
+ * largest E2M1 exponent (2), as an E8M0 byte clamped to [0, 254]; each value
+ * divided by 2^(e-127) is rounded to the nearest E2M1 magnitude, ties to the
+ * even code, values above 6 saturating to 6.  A block holding a non-finite
+ * value gets scale byte 255 and decodes to NaN.  codes[i] carries the sign in
+ * bit 3 (a negative value that rounds to 0 gets code 8, -0).  Returns the
+ * scale byte. */
+int orc_mx_quant_block(uint8_t *codes, const float *x)
+{
+    double amax = 0.0;
+    int bad = 0;
+    for (int i = 0; i < 32; i++) {
+        if (!isfinite(x[i])) bad = 1;
+        else amax = fmax(amax, fabs((double)x[i]));
+    }
+    if (bad) {
+        for (int i = 0; i < 32; i++) codes[i] = 0;
+        return 255;
+    }
+    int e = 0;
+    if (amax > 0.0) {
+        int E;
+        frexp(amax, &E);        /* amax = m 2^E, m in [0.5, 1): floor(log2 amax) = E - 1 */
+        e = (E - 1) - 2 + 127;
+        if (e < 0) e = 0;
+        if (e > 254) e = 254;
+    }
+    const double inv = ldexp(1.0, 127 - e);
+    for (int i = 0; i < 32; i++) {
+        const double v = fabs((double)x[i]) * inv;  /* exact: a power-of-two scaling */
+        /* midpoints of the magnitudes 0 .5 1 1.5 2 3 4 6; at a midpoint the
+         * even code wins: 0.25 -> 0, 0.75 -> 1, 1.25 -> 1, 1.75 -> 2,
+         * 2.5 -> 2, 3.5 -> 4, 5 -> 4 */
+        int c = (v > 0.25) + (v >= 0.75) + (v > 1.25) + (v >= 1.75) + (v > 2.5) + (v >= 3.5) +
+                (v > 5.0);
+        if (signbit(x[i])) c |= 8;
+        codes[i] = (uint8_t)c;
+    }
+    return e;
+}
+
+/* xq[i] = the value of x[i]'s MXFP4 code, n a multiple of 32.  codes and
+ * scales (n and n/32 bytes) may be null. */
+void orc_mx_quantize(double *xq, uint8_t *codes, uint8_t *scales, const float *x, int n)
+{
+    uint8_t c[32];
+    for (int b = 0; b < n / 32; b++) {
+        const int e = orc_mx_quant_block(c, x + 32 * b);
+        for (int i = 0; i < 32; i++) {
+            xq[32 * b + i] = (e == 255) ? NAN : ORC_E2M1[c[i]] * ldexp(1.0, e - 127);
+            if (codes) codes[32 * b + i] = c[i];
+        }
+        if (scales) scales[b] = (uint8_t)e;
+    }
+}
+
+/* One expert with MXFP4 activations: x is quantised, g and u are computed
+ * from it in fp64, h = silu(g) u is rounded to fp32 (the precision in which a
+ * kernel holds h before it quantises it) and quantised, and y = W_down h. */
+void orc_expert_forward_mxq(double *y, const orc_expert *E, const float *x)
+{
+    const int d = E->gate.in, f = E->gate.rows;
+    double *xq = (double *)malloc(sizeof(double) * (size_t)d);
+    double *g = (double *)malloc(sizeof(double) * (size_t)f);
+    double *u = (double *)malloc(sizeof(double) * (size_t)f);
+    float *h = (float *)malloc(sizeof(float) * (size_t)f);
+    orc_mx_quantize(xq, NULL, NULL, x, d);
+    orc_matvec(g, &E->gate, xq);
+    orc_matvec(u, &E->up, xq);
+    for (int i = 0; i < f; i++) h[i] = (float)(orc_silu(g[i]) * u[i]);
+    orc_mx_quantize(g, NULL, NULL, h, f);
+    orc_matvec(y, &E->down, g);
+    free(xq);
+    free(g);
+    free(u);
+    free(h);
+}
+
 /* ------------------------------------------------------------------ router */
 
 /* bf16 bit pattern -> its exact value (bf16 is the top half of an fp32). */
