@@ -27,6 +27,23 @@ def test_library_exports_every_declared_symbol():
     assert names <= set(k.SIGNATURES), sorted(names - set(k.SIGNATURES))
 
 
+def test_header_is_plain_c():
+    """include/k3moe.h is a C header: it compiles as strict C99 and C11 with
+    every warning on, no C++ or CUDA types in it (checked by gcc reading the
+    source from stdin, nothing written)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    src = '#include "k3moe.h"\nint main(void) { return (int)k3moe_expert_bytes(7168, 1536) & 0; }\n'
+    for std in ("c99", "c11"):
+        r = subprocess.run([gcc, "-std=" + std, "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                            "-I", os.path.join(ROOT, "include"), "-x", "c", "-"],
+                           input=src, capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+
+
 def test_byte_arithmetic_host():
     assert k.expert_bytes(7168, 1536) == 17547264
     assert k.matrix_bytes(1536, 7168) == 5849088
