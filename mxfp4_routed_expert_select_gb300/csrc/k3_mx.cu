@@ -646,8 +646,15 @@ K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, uint8_t *sm
         }
     }
     cta_sync_threads();
-    cta_topk_by([&](int e) { return s_logit[e]; }, r.rt, E, a0.k, sel_ids, sel_w, tk,
-                [] { cta_sync_threads(); });
+    // the rule is a kernel parameter, the same in every thread: the default
+    // softmax rule is passed as a constant so that its selection compiles
+    // with the rule folded away
+    auto logit_of = [&](int e) { return s_logit[e]; };
+    if (r.rt.mode == K3_ROUTER_SOFTMAX)
+        cta_topk_by(logit_of, Router{r.rt.bias, K3_ROUTER_SOFTMAX}, E, a0.k, sel_ids, sel_w, tk,
+                    [] { cta_sync_threads(); });
+    else
+        cta_topk_by(logit_of, r.rt, E, a0.k, sel_ids, sel_w, tk, [] { cta_sync_threads(); });
     cta_sync_threads();
     if (blockIdx.x == 0 && threadIdx.x < a0.k) {
         r.ids_out[threadIdx.x] = sel_ids[threadIdx.x];
