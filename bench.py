@@ -44,10 +44,16 @@ N_ROUTER_COPIES = 16
 # DRAM read + write bytes of one launch of the fused batch-1 kernel at the
 # 896-expert workload, from a one-pass ncu capture of this bench (median of
 # three launches); the algorithmic bytes are LAYER_BYTES = 293,601,280.
-FUSED_TRAFFIC = 294038272
-# The same for the block-scaled batch-1 kernel (k3_mx_layer<float>, median of
-# three launches); None whenever the kernel changed since the capture.
-MX_TRAFFIC = 301050624
+# None whenever the kernel changed since the capture; the last capture is
+# kept beside it, labelled.
+FUSED_TRAFFIC = None
+FUSED_TRAFFIC_LAST = 294038272
+# The same for the block-scaled batch-1 kernel (k3_mx_layer<float>).
+MX_TRAFFIC = None
+MX_TRAFFIC_LAST = 301050624
+TRAFFIC_LAST_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch at this workload "
+                     "(median of 3 launches), taken before the router rule became selectable; the "
+                     "kernel has changed since, its memory accesses have not")
 N_TOKENS = 1024
 
 
@@ -352,7 +358,7 @@ def run_ours(args, rank, world, dev_index):
 
     peak, peak_src = measured_peaks()
     gu_avg = statistics.mean(gu_ms)
-    traffic, traffic_src = None, None
+    traffic, traffic_src, traffic_last = None, None, None
     if mx:
         # one kernel per step: router, top-k, gate/up, down and combine
         eager_ms = statistics.mean([a + b + c for a, b, c in zip(route_ms, gu_ms, dn_ms)])
@@ -362,15 +368,19 @@ def run_ours(args, rank, world, dev_index):
         if E == 896 and MX_TRAFFIC:
             traffic, traffic_src = MX_TRAFFIC, ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of "
                                                 "k3_mx_layer<float> at this workload (median of 3 launches)")
+        elif E == 896:
+            traffic_last = {"bytes": MX_TRAFFIC_LAST, "source": TRAFFIC_LAST_NOTE}
     elif fused:
         # one kernel per step: its average duration over the timed region is at
         # most the step time (graph replay gaps count against it)
         eager_ms = statistics.mean([a + b + c for a, b, c in zip(route_ms, gu_ms, dn_ms)])
         k_ms = ms / args.steps if graph is not None else eager_ms
         k_name, k_bytes = "k3_moe_t1_fused (router + top-k + 16 experts + combine)", LAYER_BYTES
-        if E == 896:
+        if E == 896 and FUSED_TRAFFIC:
             traffic, traffic_src = FUSED_TRAFFIC, ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch "
                                                    "of k3_moe_t1_fused<0> at this workload (median of 3 launches)")
+        elif E == 896:
+            traffic_last = {"bytes": FUSED_TRAFFIC_LAST, "source": TRAFFIC_LAST_NOTE}
     else:
         k_ms, k_name, k_bytes = gu_avg, "k3_rows_pipe (gate/up + SwiGLU, 16 experts)", GATEUP_BYTES
     achieved = k_bytes / (k_ms * 1e-3) / 1e9
@@ -406,6 +416,7 @@ def run_ours(args, rank, world, dev_index):
                      "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": traffic, "traffic_source": traffic_src,
+                     "traffic_last_capture": traffic_last,
                      "algorithmic_bytes": k_bytes},
         "e2e": {"value": round(job_rate(n_e2e, world, e2e_ms), 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": D * 4, "d2h_bytes_per_step": D * 4, "steps": n_e2e},
