@@ -757,6 +757,16 @@ def _stream_policy(k, cache, slots, n_w, n_tok, n_layers, hits, plain_lru):
     out["sizing"] = {"slots": caps, "lru_hit_rate": [round(int(h) / keys.size, 4) for h in lru],
                      "belady_hit_rate": [round(int(h) / keys.size, 4) for h in best],
                      "note": "whole recorded trace from an empty cache"}
+    # the pinned hot set sized offline: hot keys of the first half's
+    # histogram, hit rate on the second half, per number pinned
+    half = keys.size // 2
+    hot = k.hot_set(np.bincount(keys[:half], minlength=E * n_layers).astype(np.uint32), slots)
+    counts = [0, slots // 4, slots // 2, 3 * slots // 4, slots - 16]
+    pin = k.trace_pin_sweep(keys, bl, slots, hot, counts, count_from=half)
+    out["pin_sweep"] = {"pinned": counts,
+                        "hit_rate_second_half": [round(int(h) / (keys.size - half), 4) if h >= 0 else None
+                                                 for h in pin],
+                        "note": "hot set from the first half's request histogram, LRU in the other slots"}
     return out
 
 

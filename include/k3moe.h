@@ -511,6 +511,17 @@ int k3moe_trace_sweep(const int64_t *host_keys, const int32_t *host_batch_len, i
                       const int32_t *host_capacities, int32_t ncap, int32_t policy,
                       int64_t *host_hits_out);
 
+/* Sizing the pinned hot set: for each c < ncounts, the LRU replay of the
+ * trace through `capacity` slots with hot_keys[0..pin_counts[c]) pinned (as
+ * in k3moe_trace_replay), counting only the hits at trace positions >=
+ * count_from (e.g. a hot set measured on the first part of a trace and judged
+ * on the rest).  host_hits_out[c] is -1 where a batch does not fit.  Replays
+ * run on host threads. */
+int k3moe_trace_pin_sweep(const int64_t *host_keys, const int32_t *host_batch_len, int32_t n_batches,
+                          int32_t capacity, const int64_t *host_hot_keys,
+                          const int32_t *host_pin_counts, int32_t ncounts, int64_t count_from,
+                          int64_t *host_hits_out);
+
 /* Hot set: the n keys with the largest counts in hist[0..nkeys), in order of
  * decreasing count, ties to the lower key.  K3MOE_EINVAL if n > nkeys. */
 int k3moe_hot_set(const uint32_t *host_hist, int64_t nkeys, int32_t n, int64_t *host_keys_out);

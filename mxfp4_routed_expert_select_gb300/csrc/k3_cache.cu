@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <exception>
 #include <new>
 #include <utility>
 #include <vector>
@@ -116,8 +117,10 @@ static void cache_free(k3moe_cache *C)
     if (!C) return;
     if (C->arena) C->cp.free_arena(C->cp.ctx, C->arena);
     if (C->cuda) {
-        for (auto e : C->cuda->copied) cudaEventDestroy(e);
-        for (auto e : C->cuda->released) cudaEventDestroy(e);
+        for (auto e : C->cuda->copied)
+            if (e) cudaEventDestroy(e);
+        for (auto e : C->cuda->released)
+            if (e) cudaEventDestroy(e);
         for (cudaStream_t st : C->cuda->side)
             if (st) cudaStreamDestroy(st);
         delete C->cuda;
@@ -144,14 +147,21 @@ static int cache_init(k3moe_cache **out, size_t capacity_bytes, size_t expert_by
     C->n_layers = n_layers;
     C->n_experts = n_experts;
     C->nkeys = nkeys;
-    C->host.assign(host_blobs, host_blobs + nkeys);
     C->slots = (int32_t)slots;
-    C->key.assign(slots, kEmpty);
-    C->last.assign(slots, -1);
-    C->pin.assign(slots, 0);
-    C->in_use.assign(slots, 0);
-    C->where.assign(nkeys, -1);
-    C->hist.assign(nkeys, 0);
+    try {
+        C->host.assign(host_blobs, host_blobs + nkeys);
+        C->key.assign(slots, kEmpty);
+        C->last.assign(slots, -1);
+        C->pin.assign(slots, 0);
+        C->in_use.assign(slots, 0);
+        C->where.assign(nkeys, -1);
+        C->hist.assign(nkeys, 0);
+        C->used.reserve(slots);     // at most one entry per slot
+        C->pending.reserve(slots);  // an INFLIGHT slot is never a victim
+    } catch (const std::exception &) {
+        delete C;
+        return K3MOE_ENOMEM;
+    }
     memset(&C->st, 0, sizeof(C->st));
     C->st.slots = C->slots;
     if (use_cuda) {
@@ -167,9 +177,14 @@ static int cache_init(k3moe_cache **out, size_t capacity_bytes, size_t expert_by
                 cache_free(C);
                 return K3MOE_ECUDA;
             }
-        C->cuda->copied.resize(slots);
-        C->cuda->released.resize(slots);
-        C->cuda->has_release.assign(slots, 0);
+        try {
+            C->cuda->copied.assign(slots, nullptr);
+            C->cuda->released.assign(slots, nullptr);
+            C->cuda->has_release.assign(slots, 0);
+        } catch (const std::exception &) {
+            cache_free(C);
+            return K3MOE_ENOMEM;
+        }
         for (size_t s = 0; s < slots; s++) {
             if (cudaEventCreateWithFlags(&C->cuda->copied[s], cudaEventDisableTiming) !=
                     cudaSuccess ||
@@ -307,11 +322,21 @@ static int acquire(k3moe_cache *C, const int64_t *keys, int32_t n, void **blobs_
         victims.push_back(i);
     }
 
-    // commit: recency and use marks for every slot of the batch
+    // the record of the trace grows before anything is committed, so that a
+    // failed allocation leaves the cache as it was
     if (C->tracing) {
-        C->trace_keys.insert(C->trace_keys.end(), keys, keys + n);
-        C->trace_len.push_back(n);
+        const size_t nk = C->trace_keys.size();
+        try {
+            C->trace_keys.insert(C->trace_keys.end(), keys, keys + n);
+            C->trace_len.push_back(n);
+        } catch (const std::exception &) {
+            C->trace_keys.resize(nk);
+            return K3MOE_ENOMEM;
+        }
     }
+    // commit (no allocation below: used and pending hold at most one entry
+    // per slot and were reserved at create): recency and use marks for every
+    // slot of the batch
     for (int32_t i = 0; i < n; i++) {
         C->hist[keys[i]]++;
         const int32_t s = slot_of[i];
@@ -358,16 +383,28 @@ static int acquire(k3moe_cache *C, const int64_t *keys, int32_t n, void **blobs_
     return rc;
 }
 
+// The plan's scratch vectors are allocated before anything is committed: a
+// failed allocation changes nothing.
+static int acquire_guarded(k3moe_cache *C, const int64_t *keys, int32_t n, void **blobs_out,
+                           uint8_t *hit_out, k3moe_stream compute, bool wait)
+{
+    try {
+        return acquire(C, keys, n, blobs_out, hit_out, compute, wait);
+    } catch (const std::exception &) {
+        return K3MOE_ENOMEM;
+    }
+}
+
 int k3moe_cache_acquire(k3moe_cache *C, const int64_t *keys, int32_t n, void **blobs_out,
                         uint8_t *hit_out, k3moe_stream compute)
 {
-    return acquire(C, keys, n, blobs_out, hit_out, compute, true);
+    return acquire_guarded(C, keys, n, blobs_out, hit_out, compute, true);
 }
 
 int k3moe_cache_acquire_split(k3moe_cache *C, const int64_t *keys, int32_t n, void **blobs_out,
                               uint8_t *hit_out, k3moe_stream compute)
 {
-    return acquire(C, keys, n, blobs_out, hit_out, compute, false);
+    return acquire_guarded(C, keys, n, blobs_out, hit_out, compute, false);
 }
 
 int k3moe_cache_wait_copies(k3moe_cache *C, k3moe_stream compute)

@@ -214,6 +214,29 @@ int replay(const Trace &t, int32_t capacity, int32_t policy, const int64_t *pinn
     }
 }
 
+// Runs fn(0..n-1) spread over the host's threads (fn must not throw).  A
+// thread that cannot be started leaves its share to the calling thread.
+template <typename Fn>
+void for_each_on_threads(int32_t n, Fn &fn)
+{
+    const unsigned hw = std::max(1u, std::thread::hardware_concurrency());
+    const int32_t nthreads = (int32_t)std::min<unsigned>(hw, (unsigned)n);
+    std::vector<std::thread> pool;
+    int32_t started = 1;  // share 0 is the calling thread's
+    try {
+        pool.reserve((size_t)nthreads);
+        for (; started < nthreads; started++)
+            pool.emplace_back([&fn, w = started, n, nthreads] {
+                for (int32_t c = w; c < n; c += nthreads) fn(c);
+            });
+    } catch (const std::exception &) {
+    }
+    for (int32_t c = 0; c < n; c += nthreads) fn(c);
+    for (int32_t w = started; w < nthreads; w++)
+        for (int32_t c = w; c < n; c += nthreads) fn(c);
+    for (auto &th : pool) th.join();
+}
+
 void put_le(unsigned char *p, uint64_t v, int bytes)
 {
     for (int i = 0; i < bytes; i++) p[i] = (unsigned char)(v >> (8 * i));
@@ -254,26 +277,63 @@ int k3moe_trace_sweep(const int64_t *keys, const int32_t *batch_len, int32_t n_b
     for (int32_t c = 0; c < ncap; c++)
         if (capacities[c] < 1) return K3MOE_EINVAL;
     const Trace t{keys, batch_len, n_batches, total};
-    std::vector<int> rc((size_t)ncap, K3MOE_OK);
+    std::vector<int> rc;
+    try {
+        rc.assign((size_t)ncap, K3MOE_OK);
+    } catch (const std::exception &) {
+        return K3MOE_ENOMEM;
+    }
     auto run = [&](int32_t c) {
         int64_t h = -1;
         const int r = replay(t, capacities[c], policy, nullptr, 0, nullptr, &h);
         hits_out[c] = r == K3MOE_OK ? h : -1;
         rc[(size_t)c] = r == K3MOE_EBUSY ? K3MOE_OK : r;
     };
-    const unsigned hw = std::max(1u, std::thread::hardware_concurrency());
-    const int32_t nthreads = (int32_t)std::min<unsigned>(hw, (unsigned)ncap);
+    for_each_on_threads(ncap, run);
+    for (int r : rc)
+        if (r != K3MOE_OK) return r;
+    return K3MOE_OK;
+}
+
+int k3moe_trace_pin_sweep(const int64_t *keys, const int32_t *batch_len, int32_t n_batches,
+                          int32_t capacity, const int64_t *hot_keys, const int32_t *pin_counts,
+                          int32_t ncounts, int64_t count_from, int64_t *hits_out)
+{
+    const int64_t total = trace_total(keys, batch_len, n_batches);
+    if (total < 0 || capacity < 1 || ncounts < 1 || !pin_counts || !hits_out || count_from < 0)
+        return K3MOE_EINVAL;
+    int32_t most = 0;
+    for (int32_t c = 0; c < ncounts; c++) {
+        if (pin_counts[c] < 0 || pin_counts[c] > capacity) return K3MOE_EINVAL;
+        most = std::max(most, pin_counts[c]);
+    }
+    if (most > 0 && !hot_keys) return K3MOE_EINVAL;
+    for (int32_t p = 0; p < most; p++)
+        if (hot_keys[p] < 0) return K3MOE_EINVAL;
+    const Trace t{keys, batch_len, n_batches, total};
+    std::vector<int> rc;
     try {
-        std::vector<std::thread> pool;
-        for (int32_t w = 1; w < nthreads; w++)
-            pool.emplace_back([&, w] {
-                for (int32_t c = w; c < ncap; c += nthreads) run(c);
-            });
-        for (int32_t c = 0; c < ncap; c += nthreads) run(c);
-        for (auto &th : pool) th.join();
+        rc.assign((size_t)ncounts, K3MOE_OK);
     } catch (const std::exception &) {
         return K3MOE_ENOMEM;
     }
+    auto run = [&](int32_t c) {
+        int64_t h = -1;
+        int r = K3MOE_ENOMEM;
+        try {
+            std::vector<uint8_t> hit((size_t)total);
+            r = replay(t, capacity, K3MOE_POLICY_LRU, hot_keys, pin_counts[c], hit.data(), &h);
+            if (r == K3MOE_OK) {
+                h = 0;
+                for (int64_t i = count_from; i < total; i++) h += hit[(size_t)i];
+            }
+        } catch (const std::exception &) {
+            r = K3MOE_ENOMEM;
+        }
+        hits_out[c] = r == K3MOE_OK ? h : -1;
+        rc[(size_t)c] = r == K3MOE_EBUSY ? K3MOE_OK : r;
+    };
+    for_each_on_threads(ncounts, run);
     for (int r : rc)
         if (r != K3MOE_OK) return r;
     return K3MOE_OK;

@@ -20,6 +20,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <exception>
 #include <new>
 #include <vector>
 
@@ -160,14 +161,20 @@ static int trunk_init(k3moe_trunk **out, const void *const *host, const size_t *
     T->M = M;
     T->P = P;
     T->R = R;
-    T->host.assign(host, host + M);
-    T->bytes.assign(bytes, bytes + M);
     T->ring_off = used;
     T->ring_bytes = ring_bytes;
-    T->prefix_pending.assign((size_t)P, 0);
-    T->slot_seq.assign((size_t)R, -1);
-    T->slot_pending.assign((size_t)R, 0);
-    T->slot_in_use.assign((size_t)R, 0);
+    try {
+        T->host.assign(host, host + M);
+        T->bytes.assign(bytes, bytes + M);
+        T->off.reserve((size_t)P);
+        T->prefix_pending.assign((size_t)P, 0);
+        T->slot_seq.assign((size_t)R, -1);
+        T->slot_pending.assign((size_t)R, 0);
+        T->slot_in_use.assign((size_t)R, 0);
+    } catch (const std::exception &) {
+        delete T;
+        return K3MOE_ENOMEM;
+    }
     memset(&T->st, 0, sizeof(T->st));
     T->st.n_layers = M;
     T->st.pinned_layers = P;
@@ -182,9 +189,14 @@ static int trunk_init(k3moe_trunk **out, const void *const *host, const size_t *
         }
         T->cp = {T->cuda, tc_alloc, tc_free, tc_copy, tc_wait, tc_release};
         const size_t ns = (size_t)P + (size_t)R;
-        T->cuda->copied.assign(ns, nullptr);
-        T->cuda->released.assign(ns, nullptr);
-        T->cuda->has_release.assign(ns, 0);
+        try {
+            T->cuda->copied.assign(ns, nullptr);
+            T->cuda->released.assign(ns, nullptr);
+            T->cuda->has_release.assign(ns, 0);
+        } catch (const std::exception &) {
+            trunk_free(T);
+            return K3MOE_ENOMEM;
+        }
         bool ok = cudaStreamCreateWithFlags(&T->cuda->side, cudaStreamNonBlocking) == cudaSuccess;
         for (size_t s = 0; ok && s < ns; s++)
             ok = cudaEventCreateWithFlags(&T->cuda->copied[s], cudaEventDisableTiming) == cudaSuccess &&

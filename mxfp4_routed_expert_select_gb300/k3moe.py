@@ -141,6 +141,7 @@ SIGNATURES = {
     "k3moe_cache_unpin": (ctypes.c_int, [_P, _I64]),
     "k3moe_trace_replay": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _I, _P, _P]),
     "k3moe_trace_sweep": (ctypes.c_int, [_P, _P, _I, _P, _I, _I, _P]),
+    "k3moe_trace_pin_sweep": (ctypes.c_int, [_P, _P, _I, _I, _P, _P, _I, _I64, _P]),
     "k3moe_hot_set": (ctypes.c_int, [_P, _I64, _I, _P]),
     "k3moe_trace_save": (ctypes.c_int, [ctypes.c_char_p, _P, _P, _I]),
     "k3moe_trace_load": (ctypes.c_int, [ctypes.c_char_p, _P, _I64, _P, _I, _P, _P]),
@@ -518,6 +519,19 @@ def trace_sweep(keys, batch_len, capacities, policy="lru"):
     check(lib().k3moe_trace_sweep(keys.ctypes.data, bl.ctypes.data, bl.size, caps.ctypes.data,
                                   caps.size, _POLICIES[policy], out.ctypes.data),
           "k3moe_trace_sweep")
+    return out
+
+
+def trace_pin_sweep(keys, batch_len, capacity, hot_keys, pin_counts, count_from=0):
+    """k3moe_trace_pin_sweep: LRU hits at positions >= count_from with the
+    first pin_counts[c] hot keys pinned, per c (-1 where a batch does not fit)."""
+    keys, bl = _trace_arrays(keys, batch_len)
+    hot = np.ascontiguousarray(hot_keys, np.int64)
+    pc = np.ascontiguousarray(pin_counts, np.int32)
+    out = np.zeros(pc.size, np.int64)
+    check(lib().k3moe_trace_pin_sweep(keys.ctypes.data, bl.ctypes.data, bl.size, int(capacity),
+                                      hot.ctypes.data if hot.size else None, pc.ctypes.data, pc.size,
+                                      int(count_from), out.ctypes.data), "k3moe_trace_pin_sweep")
     return out
 
 

@@ -205,6 +205,24 @@ def test_pinning_the_measured_hot_set_beats_plain_lru_on_a_zipf_trace():
     c.close()
 
 
+def test_pin_sweep_equals_replays_and_finds_a_better_hot_set():
+    """Each pin count's hits (counted from the second half) equal those of a
+    replay with that many hot keys pinned; on the Zipf trace some pinned hot
+    set beats plain LRU (0 pinned) on the held-out half."""
+    keys, bl = _routing_trace(256)
+    C, half = 455, keys.size // 2
+    hot = k.hot_set(np.bincount(keys[:half], minlength=4 * 896).astype(np.uint32), C)
+    counts = [0, 64, 200, 350, C - 16, C - 15, C]
+    sw = k.trace_pin_sweep(keys, bl, C, hot, counts, count_from=half)
+    for n, h in zip(counts, sw):
+        hits, flags = k.trace_replay(keys, bl, C, "lru", hot[:n])
+        assert h == (-1 if hits < 0 else int(flags[half:].sum()))
+    assert sw[-1] == -1  # every slot pinned: the first unpinned request finds no slot
+    assert max(sw[1:5]) > sw[0]
+    with pytest.raises(k.K3Error):
+        k.trace_pin_sweep(keys, bl, C, hot, [C + 1])
+
+
 def test_trace_file_round_trip_and_refusals(tmp_path):
     keys, bl = _routing_trace(8)
     path = str(tmp_path / "t.k3trace")
