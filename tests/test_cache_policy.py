@@ -17,7 +17,7 @@ import pytest
 import oracle
 import synth
 from mxfp4_routed_expert_select_gb300 import k3moe as k
-from test_cache_host import make_cache, run_trace
+from test_cache_host import FakeCopier, make_cache, run_trace
 
 
 def _random_trace(rng, dup):
@@ -109,6 +109,26 @@ def test_trace_record_skips_pins_and_refused_batches_and_restarts_clean():
     assert c.trace()[0].tolist() == [1, 2, 3]
     c.record_trace(True)
     assert c.trace()[0].size == 0
+    c.close()
+
+
+def test_request_histogram_has_the_pages_size(golden):
+    """One counter per (MoE layer, expert) key: 92 x 896 = 82,432 counters of
+    4 bytes, 330 KB (the explainer page, 'The cache the project exists
+    for'), counting every request."""
+    g = golden["request_histogram"]
+    buf = ctypes.create_string_buffer(64)
+    n = g["layers"] * g["experts_per_layer"]
+    cp = FakeCopier()
+    c = k.Cache(4 * 64, 64, [ctypes.addressof(buf)] * n, g["layers"], g["experts_per_layer"],
+                copier=cp.struct)
+    h = c.histogram()
+    assert h.size == g["counters"] and round(h.nbytes / 1000) == g["kb"]
+    for keys in ([5, 82431], [5], [7, 5]):
+        c.acquire(keys)
+        c.release()
+    h = c.histogram()
+    assert (h[5], h[7], h[82431], int(h.sum())) == (3, 1, 1, 5)
     c.close()
 
 
