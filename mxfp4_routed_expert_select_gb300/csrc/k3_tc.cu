@@ -81,7 +81,7 @@ struct TcCfg {
     static constexpr int B_OFF = PK_OFF + SP * PK_BYTES;
     static constexpr int LUT_OFF = B_OFF + NSLOT * TC_SLOT;   // e4m3 decode tables (KD = 1)
     static constexpr int BAR_OFF = LUT_OFF + (KD ? 256 * 8 : 0);
-    static constexpr int NBARS = 2 * SP + 2 * SA + 3 * 16 + 5;  // mbarriers (see the kernel)
+    static constexpr int NBARS = 2 * SP + 2 * SA + 2 * 16 + 5;  // mbarriers (see the kernel)
     static constexpr int BAR_BYTES = 768;                     // mbarriers, token ring offsets, TMEM slot, flag
     static constexpr int SMEM = BAR_OFF + BAR_BYTES + 1024;   // + alignment slack
     static_assert(NBARS * 8 + 16 * 4 + 8 <= BAR_BYTES, "barrier block");
@@ -143,35 +143,6 @@ K3_DEV void mma_kstep(uint32_t td, uint32_t alo, uint32_t blo, uint32_t idesc, u
 #undef K3_KSTEP1
 #undef K3_KSTEP2
 #undef K3_MMA4
-// Thread-block clusters: this CTA's rank, the cluster's size and index, the
-// number of clusters; a cluster-wide barrier (every thread of every CTA).
-K3_DEV uint32_t cluster_rank() { uint32_t r; asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r)); return r; }
-K3_DEV uint32_t cluster_size() { uint32_t r; asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r)); return r; }
-K3_DEV uint32_t cluster_id() { uint32_t r; asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r)); return r; }
-K3_DEV uint32_t cluster_count() { uint32_t r; asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r)); return r; }
-K3_DEV void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Bulk copy global -> the same shared offset of every CTA in `mask`, each
-// CTA's barrier at `bar` counting the bytes that land in it.
-K3_DEV void bulk_g2s_multicast(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar, uint16_t mask)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, "
-                 "[%3], %4;" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar), "h"(mask)
-                 : "memory");
-}
-// Commit (by the elected lane) arriving on the barrier at `bar` in every CTA
-// of `mask` once this thread's MMAs so far have completed.
-K3_DEV void mma_commit_multicast(uint32_t bar, uint16_t mask)
-{
-    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}"
-                 ::"r"(bar), "h"(mask)
-                 : "memory");
-}
-
 K3_DEV uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 {
     uint32_t d;
@@ -309,9 +280,9 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
     const uint32_t sbase = smem_addr(sm);
     uint64_t *bars = (uint64_t *)(sm + C::BAR_OFF);
     const int B_PKF = 0, B_PKE = B_PKF + C::SP, B_AF = B_PKE + C::SP, B_AE = B_AF + C::SA, B_BF = B_AE + C::SA,
-              B_BE = B_BF + TC_NB, B_BEC = B_BE + TC_NB, B_ACCF = B_BEC + TC_NB, B_ACCE = B_ACCF + 2,
-              B_FIN = B_ACCE + 2, NBARS = B_FIN + 1;
-    static_assert(2 * C::SP + 2 * C::SA + 3 * TC_NB + 5 == C::NBARS, "barrier count");
+              B_BE = B_BF + TC_NB, B_ACCF = B_BE + TC_NB, B_ACCE = B_ACCF + 2, B_FIN = B_ACCE + 2,
+              NBARS = B_FIN + 1;
+    static_assert(2 * C::SP + 2 * C::SA + 2 * TC_NB + 5 == C::NBARS, "barrier count");
     volatile uint32_t *boff = (volatile uint32_t *)(bars + NBARS);  // [TC_NB] token ring offsets
     uint32_t *tmem_slot = (uint32_t *)(boff + TC_NB);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
@@ -323,18 +294,14 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
     const int nrb = ROWS / TC_M;
     const int nss = K / TC_SS;
     const int nks = K / C::KSK;
-    // Clusters of CS CTAs take groups of CS consecutive row blocks of one
-    // tile (CTA rank r the r-th); the cluster's leader copies each k-step of
-    // the tile's token (or h) rows once, to every CTA of the cluster.  Every
-    // role walks the same groups (cluster index, += number of clusters) and
-    // fetches the next group's tile record one group ahead.
-    const int CS = (int)cluster_size(), crank = (int)cluster_rank();
-    const int ncl = (int)cluster_count(), cid = (int)cluster_id();
-    const bool leader = crank == 0;
-    const uint16_t cmask = (uint16_t)((1u << CS) - 1u);
-    const int gpt = nrb / CS;                   // groups per tile
+    // Units are (tile, 128-row block) pairs, unit u = tile u / nrb, row
+    // block u % nrb.  Every role walks the same units (CTA index, += number
+    // of CTAs) and fetches the next unit's tile record one unit ahead; every
+    // CTA copies its own token (or h) rows.
+    const int ncl = (int)gridDim.x, cid = (int)blockIdx.x;
+    const int gpt = nrb;                        // units per tile
     const int n_groups = *a.n_tiles * gpt;
-    auto unit_of = [&](int ug) { return (ug / gpt) * nrb + (ug % gpt) * CS + crank; };
+    auto unit_of = [&](int ug) { return ug; };
     auto tile_at = [&](int ug) -> TcTile {
         TcTile t = {};
         if (ug < n_groups) t = a.tiles[ug / gpt];
@@ -353,7 +320,6 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
         for (int i = 0; i < TC_NB; i++) {
             mbar_init(bar(B_BF + i), 1);
             mbar_init(bar(B_BE + i), 1);
-            mbar_init(bar(B_BEC + i), CS);  // the leader's: one commit per CTA of the cluster
         }
         for (int i = 0; i < 2; i++) {
             mbar_init(bar(B_ACCF + i), 1);
@@ -389,7 +355,6 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
     }
     tc_fence_before();
     __syncthreads();
-    cluster_sync();  // every CTA's barriers exist before any copy or commit reaches them
     tc_fence_after();
     const uint32_t tmem = *(volatile uint32_t *)tmem_slot;
 
@@ -439,15 +404,10 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
         // starts at `head` (skipping to the ring start when it would not fit
         // before the end) and the slots up to the end of the oldest k-step
         // the MMAs have finished are free again.
-        // Every CTA runs the same allocation (the offsets depend only on the
-        // tiles' widths); the leader waits until every CTA of the cluster is
-        // done with the slots (its cluster-wide barriers) and issues the copy
-        // to all of them, the others only announce the bytes to expect once
-        // their own MMAs are done with the k-step the barrier last served.
         if (lane == 0) {
             uint32_t kt = 0, done = 0, head = 0, tail = 0;
             uint32_t endv[TC_NB];
-            const int B_FREE = (leader && CS > 1) ? B_BEC : B_BE;
+            const int B_FREE = B_BE;
             TcTile tl_next = tile_at(cid);
             for (int ug = cid; ug < n_groups && !*abort_flag; ug += ncl) {
                 const TcTile tl = tl_next;
@@ -483,11 +443,7 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
                     const uint32_t off = (start % C::NSLOT) * TC_SLOT;
                     boff[kt % TC_NB] = off;
                     mbar_arrive_expect_tx(bar(B_BF + kt % TC_NB), bytes);
-                    if (CS == 1)
-                        bulk_g2s(b_ring + off, src + (size_t)ks * bytes, bytes, bar(B_BF + kt % TC_NB));
-                    else if (leader)
-                        bulk_g2s_multicast(b_ring + off, src + (size_t)ks * bytes, bytes, bar(B_BF + kt % TC_NB),
-                                           cmask);
+                    bulk_g2s(b_ring + off, src + (size_t)ks * bytes, bytes, bar(B_BF + kt % TC_NB));
                 }
                 if (!ok) break;
             }
@@ -530,7 +486,6 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
                 mma_kstep<C::NA, KD>(td, alo, blo, idesc, ks != 0);
                 mma_commit(bar(B_AE + sa));
                 mma_commit(bar(B_BE + sb));
-                if (CS > 1) mma_commit_multicast(bar(B_BEC + sb), 1);  // the leader's slot barrier
             }
             if (!ok) break;
             mma_commit(bar(B_ACCF + buf));
@@ -770,7 +725,6 @@ __global__ void __launch_bounds__(TcCfg<PH, KD>::THREADS, 1) k3_tc_expert(const 
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_TMEM_COLS)
                      : "memory");
     }
-    cluster_sync();  // no CTA leaves while a copy or commit of another may still reach it
 }
 
 // ---------------------------------------------------------------- planning
@@ -1275,73 +1229,20 @@ int launch_router_tc(const uint16_t *X, int T, const uint16_t *Wr, int E, int d,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return K3MOE_EINVAL;
-    static bool ready = false;
-    if (!ready) {
-        if (cudaFuncSetAttribute(k3_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, RT_SMEM) != cudaSuccess)
-            return K3MOE_ECUDA;
-        ready = true;
-    }
+    if (ensure_smem((const void *)k3_router_tc, RT_SMEM) != K3MOE_OK) return K3MOE_ECUDA;
     const dim3 grid((E + TC_M - 1) / TC_M, (T + RT_N - 1) / RT_N);
     k3_router_tc<<<grid, 192, RT_SMEM, s>>>(wmap, xmap, T, E, d, logits, err);
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
 }
 
-// Launches one phase on persistent CTAs in clusters of CS (4 when the row
-// blocks divide by 4, else 2, else 1), as many clusters as fit at once.
+// Launches one phase on persistent CTAs, one per SM.
 template <int PH, int KD>
 static int launch_expert(const TcArgs &a, cudaStream_t s)
 {
     using C = TcCfg<PH, KD>;
-    static bool ready = false;
-    static int grid[5] = {0, 0, 0, 0, 0};
-    if (!ready) {
-        if (cudaFuncSetAttribute(k3_tc_expert<PH, KD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-            cudaSuccess)
-            return K3MOE_ECUDA;
-        for (int cs : {1, 2, 4}) {
-            cudaLaunchConfig_t cfg = {};
-            cudaLaunchAttribute attr;
-            attr.id = cudaLaunchAttributeClusterDimension;
-            attr.val.clusterDim.x = cs;
-            attr.val.clusterDim.y = 1;
-            attr.val.clusterDim.z = 1;
-            cfg.gridDim = dim3(num_sms() / cs * cs);
-            cfg.blockDim = dim3(C::THREADS);
-            cfg.dynamicSmemBytes = C::SMEM;
-            cfg.attrs = &attr;
-            cfg.numAttrs = 1;
-            int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, k3_tc_expert<PH, KD>, &cfg) != cudaSuccess) {
-                cudaGetLastError();
-                n = 0;
-            }
-            grid[cs] = n * cs;
-        }
-        if (grid[1] <= 0) grid[1] = num_sms();
-        ready = true;
-    }
-    // the cluster size that keeps the most CTAs resident (clusters must fit
-    // in a GPC, so larger ones can leave SMs idle); larger on a tie
-    const int nrb = (PH == 0 ? a.f : a.d) / TC_M;
-    int cs = 1;
-    for (int c : {2, 4})
-        if (nrb % c == 0 && grid[c] >= grid[cs]) cs = c;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = cs;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.gridDim = dim3(grid[cs]);
-    cfg.blockDim = dim3(C::THREADS);
-    cfg.dynamicSmemBytes = C::SMEM;
-    cfg.stream = s;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, k3_tc_expert<PH, KD>, a) != cudaSuccess) {
-        cudaGetLastError();
-        return K3MOE_ECUDA;
-    }
+    if (ensure_smem((const void *)k3_tc_expert<PH, KD>, C::SMEM) != K3MOE_OK) return K3MOE_ECUDA;
+    k3_tc_expert<PH, KD><<<num_sms(), C::THREADS, C::SMEM, s>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return K3MOE_ECUDA;
     return K3MOE_OK;
 }
 
