@@ -35,7 +35,10 @@
  *    [ENG, "What byte-identical actually costs"].
  *  - Device kernels never trap.  Errors detected on the device (a bounded
  *    wait that ran out) are recorded in a device error word that
- *    k3moe_device_error() reads and clears.
+ *    k3moe_device_error() reads and clears.  The word is a file-scope device
+ *    variable (one int per device, zero at load), so no path allocates for
+ *    it; every entry point, k3moe_expert_gemv_noalloc included, reports
+ *    through it.
  */
 #ifndef K3MOE_H
 #define K3MOE_H
@@ -171,6 +174,9 @@ int k3moe_expert_gemv(float *y, const float *x, const k3moe_expert *host_e, int3
  *  - Allocates nothing: no cudaMalloc/cudaFree or allocating library call.
  *  - The first call on a device (with that device current) looks up the
  *    array's device address; make that first call before any stream capture.
+ *  - A bounded wait that runs out in its kernels is recorded in the device
+ *    error word: the call itself returns K3MOE_OK once the kernels are
+ *    enqueued; read the outcome with k3moe_device_error().
  *  - All calls on a device share the array: calls whose kernels overlap on the
  *    GPU race, so serialise them.  Each call overwrites the array fully before
  *    reading it.

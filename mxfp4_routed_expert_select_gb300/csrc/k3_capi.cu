@@ -14,25 +14,6 @@
 namespace k3 {
 int num_sms();
 
-// One zero-initialised int per device for errors found on the device.
-int *device_error_word()
-{
-    static int *words[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-        cudaGetLastError();
-        return nullptr;
-    }
-    if (!words[dev]) {
-        int *p = nullptr;
-        if (cudaMalloc(&p, sizeof(int)) != cudaSuccess || cudaMemset(p, 0, sizeof(int)) != cudaSuccess) {
-            cudaGetLastError();
-            return nullptr;
-        }
-        words[dev] = p;
-    }
-    return words[dev];
-}
 int launch_rows_t1(int mode, const float *x, const ExpertSrc &src, int k, int in, int rows,
                    float *out, cudaStream_t s);
 int launch_down_t1(const float *h, const ExpertSrc &src, const float *w, int k, int d, int f,
@@ -329,7 +310,7 @@ int k3moe_layer_create(k3moe_layer **out, const k3moe_layer_desc *D)
     if (D->host_experts)
         for (int e = 0; e < D->n_experts; e++)
             if (!valid_expert(D->host_experts[e], D->d, D->f)) return K3MOE_EINVAL;
-    if (!k3::device_error_word()) return K3MOE_ECUDA;  // allocate before any capture
+    if (!k3::device_error_word()) return K3MOE_ECUDA;  // look the word up before any capture
     k3moe_layer *L = new (std::nothrow) k3moe_layer;
     if (!L) return K3MOE_ENOMEM;
     memset(L, 0, sizeof(*L));

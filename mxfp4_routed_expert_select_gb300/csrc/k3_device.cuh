@@ -18,8 +18,14 @@
 
 namespace k3 {
 
-// Device error word (bounded waits that ran out write K3MOE_ETIMEOUT here);
-// one int per device, allocated by the host side (k3::device_error_word()).
+// Per-device host state (k3_runtime.cu): the device error word's address,
+// the SM count, and a kernel's dynamic shared-memory limit raised to `bytes`.
+int *device_error_word();
+int num_sms();
+int ensure_smem(const void *fn, size_t bytes);
+
+// Device error word (bounded waits that ran out write K3MOE_ETIMEOUT here):
+// one int per device, a file-scope device variable (k3::device_error_word()).
 K3_DEV void set_device_error(int *err, int code)
 {
     if (err) atomicCAS(err, 0, code);

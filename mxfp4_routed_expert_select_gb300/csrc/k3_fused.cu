@@ -550,20 +550,9 @@ int launch_fused_t1(const float *x, const uint16_t *Wr, Router rt, const DevExpe
     a.S = S;
     a.slotB = slot;
     auto kern = act16 ? k3_moe_t1_fused<true> : k3_moe_t1_fused<false>;
-    // one-time set-up per instantiation: shared-memory limit and a residency
-    // check (one CTA per SM is required for the grid barrier)
-    static size_t configured[2] = {0, 0};
-    if (smem > configured[act16]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return K3MOE_ECUDA;
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, FU_THREADS, smem) !=
-                cudaSuccess ||
-            per_sm < 1)
-            return K3MOE_ECUDA;
-        configured[act16] = smem;
-    }
+    // one CTA per SM must fit (the grid barrier needs every CTA resident;
+    // the cooperative launch refuses a grid that does not)
+    if (ensure_smem((const void *)kern, smem) != K3MOE_OK) return K3MOE_ECUDA;
     const int grid = num_sms();  // one CTA per SM, all co-resident
     void *args[] = {&a};
     if (cudaLaunchCooperativeKernel((const void *)kern, dim3(grid), dim3(FU_THREADS), args, smem, s) !=

@@ -386,18 +386,6 @@ __global__ void __launch_bounds__(512) k3_down_t1(const float *__restrict__ h, E
 
 // ------------------------------------------------------------- host launch
 
-static int g_num_sms = 0;
-
-int num_sms()
-{
-    if (g_num_sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (g_num_sms <= 0) g_num_sms = 1;
-    }
-    return g_num_sms;
-}
 
 template <typename K>
 static int blocks_per_sm(K kernel, int threads, size_t smem)
@@ -438,13 +426,7 @@ static int launch_rows_pipe(const float *x, const ExpertSrc &src, int k, int in,
     const size_t smem = (size_t)S * stageB + extra(S);
     if (smem > budget) return K3MOE_EINVAL;
     auto kern = k3_rows_pipe<NM, kPipeR, RS>;
-    static size_t configured = 0;
-    if (smem > configured) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return K3MOE_ECUDA;
-        configured = smem;
-    }
+    if (ensure_smem((const void *)kern, smem) != K3MOE_OK) return K3MOE_ECUDA;
     const long total = (long)k * rows;
     const int nstage = (int)((total + kPipeR - 1) / kPipeR);
     int grid = num_sms();
@@ -482,14 +464,10 @@ int launch_rows_t1_err(int mode, const float *x, const ExpertSrc &src, int k, in
     }
     const int grid = (int)((total + rpc - 1) / rpc);
     if (mode) {
-        if (smem > 48 * 1024)
-            cudaFuncSetAttribute(k3_rows_t1<1, kUrows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+        if (ensure_smem((const void *)k3_rows_t1<1, kUrows>, smem) != K3MOE_OK) return K3MOE_ECUDA;
         k3_rows_t1<1, kUrows><<<grid, threads, smem, s>>>(x, src, k, in, rows, out, rpc);
     } else {
-        if (smem > 48 * 1024)
-            cudaFuncSetAttribute(k3_rows_t1<0, kUrows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+        if (ensure_smem((const void *)k3_rows_t1<0, kUrows>, smem) != K3MOE_OK) return K3MOE_ECUDA;
         k3_rows_t1<0, kUrows><<<grid, threads, smem, s>>>(x, src, k, in, rows, out, rpc);
     }
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
@@ -513,9 +491,7 @@ static int launch_down_hpl(const float *h, const ExpertSrc &src, const float *w,
     int rpc = (int)((d + target - 1) / target);
     if (rpc < 1) rpc = 1;
     const size_t smem = (size_t)k * rpc * sizeof(float);
-    if (smem > 48 * 1024)
-        cudaFuncSetAttribute(k3_down_t1<HPL, kUdown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
+    if (ensure_smem((const void *)k3_down_t1<HPL, kUdown>, smem) != K3MOE_OK) return K3MOE_ECUDA;
     const int grid = (d + rpc - 1) / rpc;
     k3_down_t1<HPL, kUdown><<<grid, threads, smem, s>>>(h, src, w, k, d, f, out, rpc, acc ? 1 : 0);
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;

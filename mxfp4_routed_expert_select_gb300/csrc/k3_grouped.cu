@@ -187,8 +187,7 @@ static int launch_one(const XT *xin, const DevExpert *table, const int32_t *perm
     const int threads = nwarps * 32;
     const size_t smem = (size_t)nwarps * RB * NT * 2 * sizeof(float);
     auto kern = k3_grouped_rows<NT, U, MODE, XT>;
-    if (smem > 48 * 1024)
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (ensure_smem((const void *)kern, smem) != K3MOE_OK) return K3MOE_ECUDA;
     int bps = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, threads, smem);
     if (bps < 1) bps = 1;

@@ -810,21 +810,7 @@ template <typename XT>
 static int launch_layer(const MxRoute &r, const MxArgs &a0, const MxArgs &a1, unsigned *hready, unsigned *exit_cnt,
                         uint32_t bar_off, size_t smem, cudaStream_t s)
 {
-    static size_t configured = 0;
-    if (smem > configured) {
-        if (cudaFuncSetAttribute(k3_mx_layer<XT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            return K3MOE_ECUDA;
-        }
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k3_mx_layer<XT>, MX_THREADS, smem) != cudaSuccess ||
-            per_sm < 1) {
-            cudaGetLastError();
-            return K3MOE_ECUDA;
-        }
-        configured = smem;
-    }
+    if (ensure_smem((const void *)k3_mx_layer<XT>, smem) != K3MOE_OK) return K3MOE_ECUDA;
     void *args[] = {(void *)&r, (void *)&a0, (void *)&a1, (void *)&hready, (void *)&exit_cnt, (void *)&bar_off};
     if (cudaLaunchCooperativeKernel((const void *)k3_mx_layer<XT>, dim3(num_sms()), dim3(MX_THREADS), args, smem, s) !=
         cudaSuccess) {

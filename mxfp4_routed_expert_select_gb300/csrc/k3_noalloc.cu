@@ -7,21 +7,23 @@
 // not touch the host application's allocator, or systems whose device memory
 // is budgeted once at start-up.  This entry point gives them the same result
 // as k3moe_expert_gemv without a workspace argument: the SwiGLU intermediate h
-// lives in a fixed file-scope device array, and the kernels' timeout word in a
-// second one.
+// lives in a fixed file-scope device array.  Errors found on the device (a
+// bounded wait that ran out) go to the library's device error word, which is
+// itself a file-scope device variable, and k3moe_device_error() reads them.
 //
-// The arrays exist once per device that loads the library and stay allocated
-// until the process exits.  Host code cannot use their names as device
-// addresses (in host code the name denotes a host-side stand-in), so the
-// first call on each device, with that device current, looks the addresses up
-// with cudaGetSymbolAddress and remembers them; make that first call before
-// any stream capture.  Every call on a device shares the same arrays: two
-// calls whose kernels overlap on the GPU race on h, so serialise them (one
-// stream, or events).  h is overwritten completely by every call before it is
-// read, so nothing has to be cleared between calls.
+// The array exists once per device that loads the library and stays allocated
+// until the process exits.  Host code cannot use its name as a device address
+// (in host code the name denotes a host-side stand-in), so the first call on
+// each device, with that device current, looks the address up with
+// cudaGetSymbolAddress and remembers it; make that first call before any
+// stream capture.  Every call on a device shares the same array: two calls
+// whose kernels overlap on the GPU race on h, so serialise them (one stream,
+// or events).  h is overwritten completely by every call before it is read,
+// so nothing has to be cleared between calls.
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <mutex>
 
 #include "k3_device.cuh"
 
@@ -36,14 +38,14 @@ int launch_down_t1(const float *h, const ExpertSrc &src, const float *w, int k, 
 #define K3_NOALLOC_MAX_F K3MOE_NOALLOC_MAX_F
 
 static __device__ __align__(256) float g_noalloc_h[K3_NOALLOC_MAX_F];
-static __device__ __align__(256) int g_noalloc_err;
 
 namespace {
 constexpr int kMaxDevices = 64;
+std::once_flag g_h_once[kMaxDevices];
 float *g_h_addr[kMaxDevices];
-int *g_err_addr[kMaxDevices];
 
-// Device addresses of the two arrays on the current device (looked up once).
+// Device addresses of h and of the device error word on the current device
+// (looked up once per device; concurrent first calls are safe).
 int noalloc_setup(float **h, int **err)
 {
     int dev = 0;
@@ -51,19 +53,16 @@ int noalloc_setup(float **h, int **err)
         cudaGetLastError();
         return K3MOE_ENODEV;
     }
-    if (!g_h_addr[dev]) {
-        void *ph = nullptr, *pe = nullptr;
-        if (cudaGetSymbolAddress(&ph, g_noalloc_h) != cudaSuccess ||
-            cudaGetSymbolAddress(&pe, g_noalloc_err) != cudaSuccess || !ph || !pe) {
+    std::call_once(g_h_once[dev], [dev] {
+        void *ph = nullptr;
+        if (cudaGetSymbolAddress(&ph, g_noalloc_h) == cudaSuccess)
+            g_h_addr[dev] = (float *)ph;
+        else
             cudaGetLastError();
-            return K3MOE_ECUDA;
-        }
-        g_err_addr[dev] = (int *)pe;
-        g_h_addr[dev] = (float *)ph;
-    }
+    });
     *h = g_h_addr[dev];
-    *err = g_err_addr[dev];
-    return K3MOE_OK;
+    *err = k3::device_error_word();
+    return *h && *err ? K3MOE_OK : K3MOE_ECUDA;
 }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }

@@ -341,8 +341,7 @@ int launch_group(const int32_t *ids, int npairs, int E, int nt, int32_t *offsets
                  int4 *items, int32_t *n_items, cudaStream_t s)
 {
     const size_t smem = (size_t)(3 * E + 1) * sizeof(int32_t);
-    if (smem > 48 * 1024)
-        cudaFuncSetAttribute(k3_group, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (ensure_smem((const void *)k3_group, smem) != K3MOE_OK) return K3MOE_ECUDA;
     k3_group<<<1, 1024, smem, s>>>(ids, npairs, E, nt, offsets, perm, items, n_items);
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
 }

@@ -67,6 +67,7 @@ def lib():
         L.orc_round_bf16.restype = d
         L.orc_round_bf16.argtypes = [d]
         L.orc_expert_forward_ex.argtypes = [p, p, p, i, p]
+        L.orc_swiglu_n.argtypes = [p, p, ctypes.c_int64, i]
         L.orc_bf16_value.restype = d
         L.orc_bf16_value.argtypes = [ctypes.c_uint16]
         L.orc_router_logits.argtypes = [p, p, p, i, i, i]
@@ -281,6 +282,35 @@ def combine(x, ids, w, experts, E, h_bf16=False):
     out = np.empty((T, d), np.float64)
     lib().orc_combine(_p(out), _p(x), T, d, _p(ids), _p(w), k,
                       ctypes.cast(tab, ctypes.c_void_p), int(bool(h_bf16)))
+    return out
+
+
+def combine_grouped(x, ids, w, planes_of, h_bf16=False):
+    """The same weighted sum as ``combine``, grouped by expert: every selected
+    expert's three matrices are dequantised once (``dequant``, the pinned
+    definition) and applied to all of its tokens with a library matrix
+    product in fp64; SwiGLU is ``orc_silu`` (and ``orc_round_bf16``) element
+    by element.  ``planes_of(e)`` returns the expert's planes, so only one
+    expert is held at a time.  It differs from ``combine`` only in the order
+    of the fp64 sums (checked on the CPU), and makes whole-batch checks of
+    thousands of tokens affordable."""
+    x = _c(np.atleast_2d(x), np.float64)
+    T, d = x.shape
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float64)
+    out = np.zeros((T, d), np.float64)
+    for e in np.unique(ids):
+        ts, js = np.nonzero(ids == e)
+        ex = planes_of(int(e))
+        Xe = x[ts]
+        g = Xe @ dequant(ex["gate_packed"], ex["gate_scales"]).T
+        u = Xe @ dequant(ex["up_packed"], ex["up_scales"]).T
+        g = np.ascontiguousarray(g)
+        u = np.ascontiguousarray(u)
+        lib().orc_swiglu_n(_p(g), _p(u), g.size, int(bool(h_bf16)))
+        y = g @ dequant(ex["down_packed"], ex["down_scales"]).T
+        # a token selects an expert at most once, so ts has no repeats
+        out[ts] += w[ts, js][:, None] * y
     return out
 
 

@@ -108,9 +108,11 @@ double orc_weight(const orc_mat *W, int r, int j)
     return ORC_E2M1[orc_code(W, r, j)] * ldexp(1.0, e - 127);
 }
 
-/* Whole dense matrix in fp64, row-major [rows][in]. */
+/* Whole dense matrix in fp64, row-major [rows][in].  Rows are independent
+ * (OpenMP over rows only; every element is orc_weight's value). */
 void orc_dequant(double *Wd, const orc_mat *W)
 {
+#pragma omp parallel for schedule(static)
     for (int r = 0; r < W->rows; r++)
         for (int j = 0; j < W->in; j++)
             Wd[(size_t)r * W->in + j] = orc_weight(W, r, j);
@@ -182,6 +184,18 @@ double orc_round_bf16(double v)
         return qf * ldexp(1.0, -133);
     }
     return copysign(r, v);
+}
+
+/* orc_silu and orc_round_bf16 over an array, in place: v[i] = silu(v[i]) *
+ * u[i], rounded to bf16 if h_bf16 != 0 (the SwiGLU step of
+ * orc_expert_forward_ex for many rows at once). */
+void orc_swiglu_n(double *v, const double *u, int64_t n, int h_bf16)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; i++) {
+        const double h = orc_silu(v[i]) * u[i];
+        v[i] = h_bf16 ? orc_round_bf16(h) : h;
+    }
 }
 
 /* y = W_d (silu(W_g x) * (W_u x)).  If h_bf16 != 0, h is rounded to bf16

@@ -12,9 +12,36 @@ TOL = 2e-3  # max_i |y_i - r_i| / max_i |r_i| per token (fp32 accumulation)
 
 
 def rel_err(got, ref):
+    """Normwise error of one token (the gate): max_i |y_i - r_i| / max_i |r_i|."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     return float(np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-300))
+
+
+def elem_err(got, ref):
+    """Per-element relative error of one token, each denominator floored at
+    1e-2 * max_i |r_i| (elements near zero would make the plain ratio
+    meaningless): max_i |y_i - r_i| / max(|r_i|, 1e-2 max|r|).  Reported
+    beside the normwise gate."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    floor = max(1e-2 * np.max(np.abs(ref)), 1e-300)
+    return float(np.max(np.abs(got - ref) / np.maximum(np.abs(ref), floor)))
+
+
+def batch_errors(got, ref):
+    """(normwise, per-element) errors of every row of a [T, d] batch."""
+    got = np.atleast_2d(got)
+    ref = np.atleast_2d(ref)
+    return (np.array([rel_err(g, r) for g, r in zip(got, ref)]),
+            np.array([elem_err(g, r) for g, r in zip(got, ref)]))
+
+
+def report(name, norm, elem):
+    """One line of the errors a parity test measured (pytest -s shows it)."""
+    print("%s: %d tokens, normwise max %.3e median %.3e; per-element (floor 1e-2 max|r|) "
+          "max %.3e median %.3e" % (name, len(norm), np.max(norm), np.median(norm),
+                                     np.max(elem), np.median(elem)))
 
 
 class Pool:
@@ -32,8 +59,13 @@ class Pool:
         torch.cuda.synchronize()
         self.views = [k.expert_view(self.blobs[e].data_ptr(), d, f) for e in range(E)]
         self._cache = {}
+        self.override = {}
 
     def planes(self, e):
+        """Host planes of expert e (a test may replace an expert's planes by
+        putting them in `override` after packing them onto the device)."""
+        if e in self.override:
+            return self.override[e]
         return synth.expert(self.pool, self.layer, e, self.d, self.f, self.e_lo, self.e_hi)
 
     def experts(self, ids):

@@ -7,8 +7,8 @@ import torch
 
 import oracle
 import synth
-from gpu_helpers import (TOL, Pool, margin_subs, rel_err, router_tensor, tokens,
-                         tokens_device)
+from gpu_helpers import (TOL, Pool, batch_errors, margin_subs, rel_err, report, router_tensor,
+                         tokens, tokens_device)
 from mxfp4_routed_expert_select_gb300 import k3moe as k
 
 pytestmark = pytest.mark.gpu
@@ -23,7 +23,10 @@ def _run(layer, X, T, K):
     return out.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
 
 
-def _check(pool, Wr_bits, bias, K, Xd, out, ids, w, sample=None, h_bf16=False):
+def _check(pool, Wr_bits, bias, K, Xd, out, ids, w, h_bf16=False, name=None):
+    """Ids bit-exact and weights close for every token; every output vector
+    against the oracle (grouped by expert when the batch is large), gated on
+    the normwise error, the per-element error reported."""
     T = Xd.shape[0]
     lg = oracle.router_logits(Xd, Wr_bits)
     rids, rw, m = oracle.topk(lg, K, None if bias is None else bias.astype(np.float64))
@@ -31,12 +34,16 @@ def _check(pool, Wr_bits, bias, K, Xd, out, ids, w, sample=None, h_bf16=False):
     assert np.array_equal(ids, rids)
     # fp32 logits over d terms carry ~1e-5 absolute error; w inherits it
     assert np.allclose(w, rw, rtol=2e-4, atol=1e-7)
-    rows = range(T) if sample is None else sample
-    for t in rows:
-        ref = oracle.combine(Xd[t:t + 1], rids[t:t + 1], rw[t:t + 1], pool.experts(rids[t]),
-                             pool.E, h_bf16)[0]
-        e = rel_err(out[t], ref)
-        assert e <= TOL, (t, e)
+    if T * K <= 64:
+        ref = oracle.combine(Xd, rids, rw, pool.experts(rids), pool.E, h_bf16)
+    else:
+        ref = oracle.combine_grouped(Xd, rids, rw, pool.planes, h_bf16)
+    norm, elem = batch_errors(out, ref)
+    if name:
+        report(name, norm, elem)
+    bad = np.nonzero(norm > TOL)[0]
+    assert bad.size == 0, [(int(t), float(norm[t])) for t in bad[:10]]
+    return norm, elem
 
 
 # ------------------------------------------------------------ small layers
@@ -171,27 +178,30 @@ def test_full_decode_batch1(full):
 
 
 def test_full_batched_decode_64(full):
-    """64 fp32 tokens grouped by expert; ids of all, outputs sampled."""
+    """64 fp32 tokens grouped by expert; ids, weights and every output vector."""
     pool, Wr_bits, bias, L, Lb = full
     T = 64
     subs = margin_subs(1, T, D, Wr_bits, K16)
     Xd = tokens(1, np.arange(T), D, subs)
     X = tokens_device(1, T, D, subs)
     out, ids, w = _run(L, X, T, K16)
-    _check(pool, Wr_bits, None, K16, Xd, out, ids, w, sample=[0, 1, 31, 62, 63])
+    _check(pool, Wr_bits, None, K16, Xd, out, ids, w, name="decode T=64")
 
 
 def test_full_prefill_4096_bf16_biased(full):
-    """4096 bf16 tokens with a per-expert selection bias ~ N(0,1)."""
+    """4096 bf16 tokens with a per-expert selection bias ~ N(0,1); ids,
+    weights and all 4096 output vectors (the heavily loaded experts span
+    many tiles, so every tile edge and every scatter of the combine is
+    seen)."""
     pool, Wr_bits, bias, L, Lb = full
     T = 4096
     subs = margin_subs(1, T, D, Wr_bits, K16, bias, bf16=True)
     Xd = tokens(1, np.arange(T), D, subs, bf16=True)
     X = tokens_device(1, T, D, subs, bf16=True)
     out, ids, w = _run(Lb, X, T, K16)
-    _check(pool, Wr_bits, bias, K16, Xd, out, ids, w, sample=[0, 1777, 4095])
     counts = np.bincount(ids.ravel(), minlength=E896)
     assert counts.max() > 3 * counts.mean()  # the bias makes loads uneven
+    _check(pool, Wr_bits, bias, K16, Xd, out, ids, w, name="prefill T=4096")
 
 
 # ------------------------------------------- fused batch-1 kernel vs oracle

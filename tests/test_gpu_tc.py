@@ -8,7 +8,8 @@ import torch
 
 import oracle
 import synth
-from gpu_helpers import TOL, Pool, margin_subs, rel_err, router_tensor, tokens, tokens_device
+from gpu_helpers import (TOL, Pool, batch_errors, margin_subs, rel_err, report, router_tensor, tokens,
+                         tokens_device)
 from mxfp4_routed_expert_select_gb300 import k3moe as k
 
 pytestmark = pytest.mark.gpu
@@ -26,7 +27,7 @@ def _forward(L, X, T, K, tc=True, e4m3=True):
     return out.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
 
 
-def _case(pool, Wr_bits, bias, K, T, bf16, sample=None, witness=True, e4m3=True):
+def _case(pool, Wr_bits, bias, K, T, bf16, witness=True, e4m3=True):
     d, f, E = pool.d, pool.f, pool.E
     subs = margin_subs(pool.pool, T, d, Wr_bits, K, bias, bf16=bf16)
     Xd = tokens(pool.pool, np.arange(T), d, subs, bf16)
@@ -38,10 +39,12 @@ def _case(pool, Wr_bits, bias, K, T, bf16, sample=None, witness=True, e4m3=True)
     rids, rw, m = oracle.topk(lg, K, None if bias is None else np.asarray(bias, np.float64))
     assert np.all(m >= 1e-3)
     assert np.array_equal(ids, rids)
-    for t in (range(T) if sample is None else sample):
-        ref = oracle.combine(Xd[t:t + 1], rids[t:t + 1], rw[t:t + 1], pool.experts(rids[t]), E)[0]
-        e = rel_err(out[t], ref)
-        assert e <= TOL, (t, e)
+    ref = oracle.combine_grouped(Xd, rids, rw, pool.planes)
+    norm, elem = batch_errors(out, ref)
+    report("tensor path T=%d %s %s" % (T, "bf16" if bf16 else "fp32", "e4m3" if e4m3 else "bf16-kind"),
+           norm, elem)
+    bad = np.nonzero(norm > TOL)[0]
+    assert bad.size == 0, [(int(t), float(norm[t])) for t in bad[:10]]
     if witness:
         out2, ids2, _ = _forward(L, X, T, K, tc=False)
         assert np.array_equal(ids2, ids)
@@ -79,7 +82,7 @@ def few_experts():
 @pytest.mark.parametrize("bf16", [False, True])
 def test_tc_several_tiles_per_expert(few_experts, bf16, e4m3):
     pool, Wr_bits, K = few_experts
-    out, ids = _case(pool, Wr_bits, None, K, 600, bf16, sample=[0, 1, 299, 598, 599], e4m3=e4m3)
+    out, ids = _case(pool, Wr_bits, None, K, 600, bf16, e4m3=e4m3)
     counts = np.bincount(ids.ravel(), minlength=pool.E)
     assert counts.max() > 128
 
@@ -101,7 +104,7 @@ def test_tc_nan_scale_groups_are_dropped():
     planes["gate_scales"][:64, ::3] = 255
     k.pack_expert(pool.blobs[0], planes, d, f)
     torch.cuda.synchronize()
-    pool._cache[0] = planes
+    pool.override[0] = planes
     _case(pool, synth.router_bf16(14, 0, E, d), None, K, 40, False)
 
 
@@ -110,7 +113,7 @@ def test_tc_full_shape_small_batch():
     two tokens, N = 16 columns)."""
     E, K, d, f = 64, 16, 7168, 1536
     pool = Pool(15, 0, E, d, f)
-    _case(pool, synth.router_bf16(15, 0, E, d), None, K, 5, False, sample=[0, 4])
+    _case(pool, synth.router_bf16(15, 0, E, d), None, K, 5, False)
 
 
 def test_tc_layer_forward_twice_is_repeatable(small):

@@ -279,6 +279,28 @@ def test_layer_is_weighted_sum_of_selected_experts():
     assert np.allclose(out2[0] - out[0], w[0, j] * y, rtol=1e-9, atol=1e-9 * np.abs(y).max())
 
 
+@pytest.mark.parametrize("h_bf16", [False, True])
+def test_grouped_combine_equals_per_pair_combine(h_bf16):
+    """The grouped form (each expert dequantised once, all its tokens in one
+    fp64 matrix product) reaches the per-pair combine's result up to the
+    order of fp64 sums; a planted mistake (one pair's weight dropped) is
+    seen."""
+    rng = np.random.default_rng(11)
+    d, f, E, k, T = 96, 64, 7, 3, 9
+    exs = {e: _rand_expert(rng, d, f) for e in range(E)}
+    x = rng.standard_normal((T, d))
+    ids = np.stack([np.sort(rng.choice(E, k, replace=False)) for _ in range(T)]).astype(np.int32)
+    w = rng.random((T, k))
+    ref = oracle.combine(x, ids, w, exs, E, h_bf16)
+    got = oracle.combine_grouped(x, ids, w, lambda e: exs[e], h_bf16)
+    scale = np.abs(ref).max()
+    assert np.max(np.abs(got - ref)) <= 1e-12 * scale
+    w2 = w.copy()
+    w2[4, 1] = 0.0
+    bad = oracle.combine_grouped(x, ids, w2, lambda e: exs[e], h_bf16)
+    assert np.max(np.abs(bad - ref)) > 1e-3 * scale
+
+
 # ----------------------------------------------------------------- rmsnorm
 
 def test_rmsnorm_closed_forms_eps_inside_sqrt():
