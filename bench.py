@@ -1,6 +1,6 @@
 """Benchmark of the MXFP4 routed-expert MoE layer on one GB300 (or N ranks).
 
-Default workload: one MoE layer, batch-1 decode -- 896 experts of
+Headline workload: one MoE layer, batch-1 decode -- 896 experts of
 d=7168, f=1536 resident in HBM (15.7 GB), router W_r bf16 [896 x 7168],
 x fp32, top-16, softmax combine over the selected logits.  A step is one
 token through the whole layer (router + top-k + 16 experts + combine).
@@ -9,7 +9,14 @@ token through the whole layer (router + top-k + 16 experts + combine).
 
 Prints ONE JSON line (rank 0).  `value` is tokens/s of the whole job (every
 rank runs independent tokens: weak scaling, no collective on the data path).
-Other workloads of the same layer, one JSON line each (not the headline):
+Every timed region is exactly K steps between two events on the launching
+stream (a barrier and a device synchronisation on both sides); the region
+is repeated (at least 20 times, and for about a second in all) and the
+median is reported with its minimum and maximum.  The same line carries the
+other resident-pool configurations under "configs" (same pool, same rules):
+the single-expert GEMV, batched decode of 64 tokens and prefill of 4096.
+
+One configuration alone, one JSON line each:
   --workload expert       one expert GEMV (gate/up + SwiGLU + down), 1 token
   --workload decode64     batched decode, 64 tokens, grouped by expert
   --workload prefill4096  4096 bf16 tokens, selection bias ~N(0,1)
@@ -55,6 +62,14 @@ TRAFFIC_LAST_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launc
                      "(median of 3 launches), taken before the router rule became selectable; the "
                      "kernel has changed since, its memory accesses have not")
 N_TOKENS = 1024
+# Kernels of the secondary configurations (names for the roofline lines and
+# launches per step).  One expert: gate/up + SwiGLU, then down.
+EXPERT_GEMV_KERNEL = "k3_rows_t1 + k3_down_t1 (one expert: gate/up + SwiGLU, down)"
+EXPERT_GEMV_LAUNCHES = 2
+# Multi-token forwards: router GEMM + top-k, grouping, tile plan, token
+# scales, token gather, gate/up, h pieces, down + combine.
+GROUPED_GATEUP_KERNEL = "k3_tc_expert<0,1> (tcgen05 kind::f8f6f4)"
+GROUPED_LAUNCHES = 9
 
 
 def log(*a):
@@ -199,229 +214,260 @@ def cpu_baseline_sample(budget_s=12.0, pool_id=1):
     return done, t_oracle, oracle.max_threads()
 
 
+# ---------------------------------------------------------------- timing
+
+MIN_REPEATS = 20      # timed regions per measurement, at least
+REGION_SECONDS = 1.0  # ... and about this long in all
+
+
+def max_over_ranks_list(vals, world, device=None):
+    """Element-wise maximum over all ranks of a list of floats."""
+    if world <= 1:
+        return list(vals)
+    import torch
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def graph_plan(steps, n_inputs, chunk_max=32):
+    """How a timed region of exactly `steps` steps is replayed from CUDA
+    graphs: `full` replays of graphs holding `chunk` consecutive steps, then
+    one graph of the `rem` remaining steps (full * chunk + rem == steps).
+    `variants` graphs of `chunk` steps start at input offsets chunk * v, so
+    that successive replays walk up to `n_inputs` distinct inputs."""
+    steps = max(1, int(steps))
+    chunk = max(1, min(steps, chunk_max))
+    full, rem = divmod(steps, chunk)
+    variants = max(1, min(n_inputs // chunk, 64)) if full else 0
+    return {"chunk": chunk, "full": full, "rem": rem, "variants": variants}
+
+
+def spread(ms, steps):
+    """Median, minimum and maximum per-step time (ms) over the repeats."""
+    return {"repeats": len(ms), "ms_per_step_median": round(statistics.median(ms) / steps, 6),
+            "ms_per_step_min": round(min(ms) / steps, 6), "ms_per_step_max": round(max(ms) / steps, 6)}
+
+
+def timed_region(step, steps, warmup, dev_index, world, use_graph=True, n_inputs=1, chunk_max=32,
+                 min_repeats=MIN_REPEATS, seconds=REGION_SECONDS):
+    """Warm-up, then the timed region -- exactly `steps` steps between two
+    events on the current stream, a barrier (N > 1) and a device
+    synchronisation before it and a synchronisation after it -- repeated at
+    least `min_repeats` times and for about `seconds` in all, with the
+    clocks sampled meanwhile.  step(i) enqueues step i (its input i mod
+    n_inputs).  Returns (ms of each repeat, max over ranks; clocks; plan)."""
+    import torch
+    s = torch.cuda.current_stream()
+    dev = torch.device("cuda", dev_index)
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if use_graph:
+        plan = graph_plan(steps, n_inputs, chunk_max)
+        graphs = []
+        for v in range(plan["variants"]):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for j in range(plan["chunk"]):
+                    step(v * plan["chunk"] + j)
+            graphs.append(g)
+        g_rem = None
+        if plan["rem"]:
+            g_rem = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_rem):
+                for j in range(plan["rem"]):
+                    step(j)
+        for g in graphs + ([g_rem] if g_rem is not None else []):  # untimed first replays
+            g.replay()
+        torch.cuda.synchronize()
+        ctr = [0]
+
+        def region():
+            for _ in range(plan["full"]):
+                graphs[ctr[0] % len(graphs)].replay()
+                ctr[0] += 1
+            if g_rem is not None:
+                g_rem.replay()
+    else:
+        plan = {"graph": None}
+        base = [warmup]
+
+        def region():
+            for i in range(steps):
+                step(base[0] + i)
+            base[0] += steps
+    t0 = time.perf_counter()  # one untimed region sizes the repeats
+    region()
+    torch.cuda.synchronize()
+    one = max_over_ranks(max(time.perf_counter() - t0, 1e-6), world, dev)
+    repeats = max(min_repeats, min(5000, int(seconds / one)))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(repeats)]
+    clock = ClockSampler(dev_index)
+    clock.start()
+    time.sleep(0.3)
+    for r in range(repeats):
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        ev[r][0].record(s)
+        region()
+        ev[r][1].record(s)
+        torch.cuda.synchronize()
+    clocks = clock.stop()
+    ms = max_over_ranks_list([a.elapsed_time(b) for a, b in ev], world, dev)
+    return ms, clocks, plan
+
+
+def _kernel_events(layer, step, n):
+    """Per-phase durations (ms) of `n` eager forwards, from the layer's four
+    events recorded on its stream: [route, route->gate/up, gate/up->end]."""
+    import torch
+    s = torch.cuda.current_stream()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    for q in evs:  # torch creates the CUDA event at its first record
+        for e in q:
+            e.record(s)
+    torch.cuda.synchronize()
+    for i in range(n):
+        layer.set_events(evs[i])
+        step(i)
+    layer.set_events(None)
+    torch.cuda.synchronize()
+    return ([q[0].elapsed_time(q[1]) for q in evs], [q[1].elapsed_time(q[2]) for q in evs],
+            [q[2].elapsed_time(q[3]) for q in evs])
+
+
+DATA = ("synthetic (seeded SplitMix64: uniform E2M1 codes, E8M0 in [120,130], x ~ N(0,1), "
+        "W_r ~ N(0,0.02) bf16)")
+
+
+def _roofline(name, nbytes, k_ms, bound="hbm", traffic=None, traffic_src=None):
+    peak, src = measured_peaks()
+    ach = nbytes / (k_ms * 1e-3) / 1e9
+    return {"kernel": name, "bound": bound, "achieved": round(ach, 1), "peak": peak,
+            "peak_source": src, "unit": "GB/s", "frac": round(ach / peak, 4), "traffic": traffic,
+            "traffic_source": traffic_src, "algorithmic_bytes": int(nbytes)}
+
+
+def _e2e(step_host, steps, warmup, world, dev_index, h2d, d2h, units_per_step, unit):
+    """The metric end to end: every step copies its inputs from pinned host
+    memory and reads its result back (eager launches), same timing rules."""
+    ms, _, _ = timed_region(step_host, steps, warmup, dev_index, world, use_graph=False,
+                            seconds=REGION_SECONDS / 2)
+    med = statistics.median(ms)
+    return {"value": round(job_rate(steps * units_per_step, world, med), 2), "unit": unit,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "repeats": len(ms)}
+
+
+class Ctx:
+    """What every resident-pool configuration shares: the device, the 896
+    packed experts in HBM and the router weights."""
+
+    def __init__(self, dev_index):
+        import torch
+        import synth
+        self.dev_index = dev_index
+        self.dev = torch.device("cuda", dev_index)
+        torch.cuda.set_device(self.dev)
+        self.blobs, self.views = build_pool(self.dev)
+        self.Wr_bits = synth.router_bf16(1, 0, E, D)
+        self.Wr0 = torch.from_numpy(self.Wr_bits.view(np.int16)).to(self.dev)
+
+
 # ------------------------------------------------------------------ arms
 
-def run_ours(args, rank, world, dev_index):
+def run_decode1(args, ctx, rank, world):
+    """The headline: batch-1 decode through the whole layer, one token per
+    step, 1024 distinct tokens and 16 router copies walked by the replays."""
     import torch
     import synth
     from mxfp4_routed_expert_select_gb300 import k3moe as k
-    dev = torch.device("cuda", dev_index)
-    torch.cuda.set_device(dev)
-    blobs, views = build_pool(dev)
-    Wr_bits = synth.router_bf16(1, 0, E, D)
-    Wr0 = torch.from_numpy(Wr_bits.view(np.int16)).to(dev)
-    routers = [Wr0] + [Wr0.clone() for _ in range(N_ROUTER_COPIES - 1)]
-    layers = [k.Layer(E, K, D, F, r, views, max_tokens=1) for r in routers]
+    dev = ctx.dev
+    routers = [ctx.Wr0] + [ctx.Wr0.clone() for _ in range(N_ROUTER_COPIES - 1)]
+    layers = [k.Layer(E, K, D, F, r, ctx.views, max_tokens=1) for r in routers]
     X = torch.from_numpy(np.stack([synth.token_f32(1, rank_first_token(rank, N_TOKENS) + t, D)
                                    for t in range(N_TOKENS)])).to(dev)
     out = torch.empty(D, dtype=torch.float32, device=dev)
-    s = torch.cuda.current_stream()
 
     def step(i):
         layers[i % N_ROUTER_COPIES].forward(X[i % N_TOKENS], 1, out)
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-
-    # The timed steps replay a CUDA graph holding G_STEPS consecutive layer
-    # forwards (different tokens and router copies), as a decode loop would:
-    # no host launch overhead inside the step.
-    G_STEPS = 32
-    graph = None
-    if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            for i in range(G_STEPS):
-                step(i)
-        # untimed replays (about 30 ms) so that short runs are not timed on a
-        # cold start: clocks, address translation of the 15.7 GB pool
-        for _ in range(10):
-            graph.replay()
-        torch.cuda.synchronize()
-
-    # per-kernel events on the launching stream for the first steps of the
-    # timed region
-    n_ev = min(args.steps, 2000)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ev)]
-    for quad in evs:  # torch creates the CUDA event at its first record
-        for e in quad:
-            e.record(s)
-    clock = ClockSampler(dev_index)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    clock.start()
-    time.sleep(0.3)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    if graph is not None:
-        s = torch.cuda.current_stream()
-        n_rep = (args.steps + G_STEPS - 1) // G_STEPS
-        args.steps = n_rep * G_STEPS
-        t_start.record(s)
-        for _ in range(n_rep):
-            graph.replay()
-        t_end.record(s)
-    else:
-        t_start.record(s)
-        for i in range(args.steps):
-            L = layers[i % N_ROUTER_COPIES]
-            if i < n_ev:
-                L.set_events(evs[i])
-            elif i == n_ev:
-                for l in layers:
-                    l.set_events(None)
-            step(i)
-        t_end.record(s)
-    torch.cuda.synchronize()
-    clocks = clock.stop()
-    for l in layers:
-        l.set_events(None)
-    if world > 1:
-        torch.distributed.barrier()
-    ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
-    if graph is not None:
-        # the fused kernel's own duration, events on its stream around each launch
-        for i in range(n_ev):
-            L = layers[i % N_ROUTER_COPIES]
-            L.set_events(evs[i])
-            step(i)
-        for l in layers:
-            l.set_events(None)
-        torch.cuda.synchronize()
-    route_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    gu_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    dn_ms = [e[2].elapsed_time(e[3]) for e in evs]
-
-    fused = layers[0].fused_t1()
-    mx = layers[0].mx_t1()
-    # the opt-in f16-activation mode, same workload, for the record
-    act16 = None
-    if fused:
-        for l in layers:
-            l.set_option(k.K3MOE_OPT_ACT_F16, 1)
-        for i in range(args.warmup):
-            step(i)
-        torch.cuda.synchronize()
-        g16 = None
-        if not args.no_graph:
-            g16 = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g16):
-                for i in range(G_STEPS):
-                    step(i)
-            g16.replay()
-            torch.cuda.synchronize()
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        a0.record(s)
-        if g16 is not None:
-            for _ in range(args.steps // G_STEPS):
-                g16.replay()
-        else:
-            for i in range(args.steps):
-                step(i)
-        a1.record(s)
-        torch.cuda.synchronize()
-        ams = a0.elapsed_time(a1) / (args.steps if g16 is None else (args.steps // G_STEPS) * G_STEPS)
-        for l in layers:
-            l.set_option(k.K3MOE_OPT_ACT_F16, 0)
-        act16 = {"value": round(world * 1e3 / ams, 2), "unit": "tokens/s", "ms_per_step": round(ams, 5),
-                 "layer_gbs": round(LAYER_BYTES / (ams * 1e-3) / 1e9, 1),
-                 "note": "K3MOE_OPT_ACT_F16: activations rounded to f16 (16-element power-of-two blocks), "
-                         "fp32 accumulation; not the headline"}
+    ms, clocks, plan = timed_region(step, args.steps, args.warmup, ctx.dev_index, world,
+                                    use_graph=not args.no_graph, n_inputs=N_TOKENS)
+    per = statistics.median(ms) / args.steps
+    # each layer kernel's own duration, eager, events on its stream around it
+    n_ev = min(args.steps, 200)
+    r_ms, gu_ms, dn_ms = _kernel_events(layers[0], lambda i: layers[0].forward(X[i % N_TOKENS], 1, out), n_ev)
+    eager_ms = statistics.mean([a + b + c for a, b, c in zip(r_ms, gu_ms, dn_ms)])
 
     # e2e through the C ABI with host buffers: H2D of the token, the layer,
     # D2H of the output, every step
-    n_e2e = min(args.steps, 5000)
     xh = torch.empty((N_TOKENS, D), dtype=torch.float32, pin_memory=True)
     xh.copy_(X.cpu())
     oh = torch.empty(D, dtype=torch.float32, pin_memory=True)
     xd = torch.empty(D, dtype=torch.float32, device=dev)
-    for i in range(args.warmup):
-        xd.copy_(xh[i % N_TOKENS], non_blocking=True)
-        layers[i % N_ROUTER_COPIES].forward(xd, 1, out)
-        oh.copy_(out, non_blocking=True)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    e0.record(s)
-    for i in range(n_e2e):
-        xd.copy_(xh[i % N_TOKENS], non_blocking=True)
-        layers[i % N_ROUTER_COPIES].forward(xd, 1, out)
-        oh.copy_(out, non_blocking=True)
-    e1.record(s)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
 
-    peak, peak_src = measured_peaks()
-    gu_avg = statistics.mean(gu_ms)
-    traffic, traffic_src, traffic_last = None, None, None
+    def step_host(i):
+        xd.copy_(xh[i % N_TOKENS], non_blocking=True)
+        layers[i % N_ROUTER_COPIES].forward(xd, 1, out)
+        oh.copy_(out, non_blocking=True)
+
+    e2e = _e2e(step_host, args.steps, args.warmup, world, ctx.dev_index, D * 4, D * 4, 1, "tokens/s")
+
+    mx, fused = layers[0].mx_t1(), layers[0].fused_t1()
     if mx:
-        # one kernel per step: router, top-k, gate/up, down and combine
-        eager_ms = statistics.mean([a + b + c for a, b, c in zip(route_ms, gu_ms, dn_ms)])
-        k_ms = ms / args.steps if graph is not None else eager_ms
-        k_name, k_bytes = ("k3_mx_layer<float> (router + top-k + 16 experts on tcgen05 kind::mxf4 + combine)",
-                           LAYER_BYTES)
-        if E == 896 and MX_TRAFFIC:
-            traffic, traffic_src = MX_TRAFFIC, ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of "
-                                                "k3_mx_layer<float> at this workload (median of 3 launches)")
-        elif E == 896:
-            traffic_last = {"bytes": MX_TRAFFIC_LAST, "source": TRAFFIC_LAST_NOTE}
+        k_name = "k3_mx_layer<float> (router + top-k + 16 experts on tcgen05 kind::mxf4 + combine)"
+        traffic, traffic_last = (MX_TRAFFIC, None) if E == 896 and MX_TRAFFIC else \
+            (None, {"bytes": MX_TRAFFIC_LAST, "source": TRAFFIC_LAST_NOTE} if E == 896 else None)
     elif fused:
-        # one kernel per step: its average duration over the timed region is at
-        # most the step time (graph replay gaps count against it)
-        eager_ms = statistics.mean([a + b + c for a, b, c in zip(route_ms, gu_ms, dn_ms)])
-        k_ms = ms / args.steps if graph is not None else eager_ms
-        k_name, k_bytes = "k3_moe_t1_fused (router + top-k + 16 experts + combine)", LAYER_BYTES
-        if E == 896 and FUSED_TRAFFIC:
-            traffic, traffic_src = FUSED_TRAFFIC, ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch "
-                                                   "of k3_moe_t1_fused<0> at this workload (median of 3 launches)")
-        elif E == 896:
-            traffic_last = {"bytes": FUSED_TRAFFIC_LAST, "source": TRAFFIC_LAST_NOTE}
+        k_name = "k3_moe_t1_fused (router + top-k + 16 experts + combine)"
+        traffic, traffic_last = (FUSED_TRAFFIC, None) if E == 896 and FUSED_TRAFFIC else \
+            (None, {"bytes": FUSED_TRAFFIC_LAST, "source": TRAFFIC_LAST_NOTE} if E == 896 else None)
     else:
-        k_ms, k_name, k_bytes = gu_avg, "k3_rows_pipe (gate/up + SwiGLU, 16 experts)", GATEUP_BYTES
-    achieved = k_bytes / (k_ms * 1e-3) / 1e9
-    layer_gbs = LAYER_BYTES / (ms / args.steps * 1e-3) / 1e9
+        k_name, traffic, traffic_last = "k3_router_t1 + k3_rows_t1 + k3_down_t1", None, None
+    # one kernel per step (default path): its average duration over the timed
+    # region, replay gaps included, is at most the step time
+    k_ms = per if (mx or fused) and not args.no_graph else eager_ms
+    roof = _roofline(k_name, LAYER_BYTES, k_ms, traffic=traffic,
+                     traffic_src=("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch at this "
+                                  "workload (median of 3 launches)") if traffic else None)
+    if traffic_last:
+        roof["traffic_last_capture"] = traffic_last
+    peak = roof["peak"]
+    layer_gbs = LAYER_BYTES / (per * 1e-3) / 1e9
     result = {
         "metric": "MoE-layer decode tokens/s (batch 1, 896 experts, top-16, MXFP4)",
-        "value": round(job_rate(args.steps, world, ms), 2),
+        "value": round(job_rate(args.steps, world, statistics.median(ms)), 2),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms / args.steps, 5),
+        "ms_per_step": round(per, 6),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "mxfp4 weights (e2m1 + e8m0), fp32 activations and accumulation",
-        "data": "synthetic (seeded SplitMix64: uniform E2M1 codes, E8M0 in [120,130], x ~ N(0,1), W_r ~ N(0,0.02) bf16)",
+        "data": DATA,
         "config": {"workload": "moe_layer_decode_b1: %d experts d=7168 f=1536 resident (%.1f GB), "
                                "router bf16 [%dx7168], top-16, softmax combine" % (E, E * EXPERT_BYTES / 1e9, E),
                    "global_batch": world, "seq_len": 1, "parallelism": "replicas" if world > 1 else "single",
-                   "launch": "cuda graph of 32 steps, replayed" if graph is not None else "host launch per step",
-                   "l2": "inputs larger than L2: %d rotated router copies (%.0f MB) + %d experts "
-                         "(16 random per token, 281 MB/token) + %d distinct tokens"
-                         % (N_ROUTER_COPIES, N_ROUTER_COPIES * ROUTER_BYTES / 1e6, E, N_TOKENS)},
+                   "launch": ("cuda graphs of %d steps (%d offsets) + %d, replayed" %
+                              (plan["chunk"], plan["variants"], plan["rem"])) if plan.get("chunk")
+                   else "host launch per step",
+                   "l2": "inputs larger than L2: every step reads 16 experts (281 MB) and a router "
+                         "copy (12.8 MB); %d router copies and %d distinct tokens walked by the "
+                         "replays" % (N_ROUTER_COPIES, min(N_TOKENS, max(plan.get("variants", 1), 1) *
+                                                                 plan.get("chunk", args.steps)))},
+        "timing": spread(ms, args.steps),
         "layer_hbm": {"bytes_per_token": LAYER_BYTES, "gbs": round(layer_gbs, 1),
                       "frac_of_peak": round(layer_gbs / peak, 4), "frac_of_8tbs": round(layer_gbs / 8000, 4)},
-        "kernels_ms": ({"layer_kernel": round(k_ms, 5), "layer_kernel_eager_events": round(eager_ms, 5),
-                        "steps_sampled": n_ev} if (fused or mx) else
-                       {"route_topk": round(statistics.mean(route_ms), 5),
-                        "gate_up_swiglu": round(gu_avg, 5),
-                        "down_combine": round(statistics.mean(dn_ms), 5), "steps_sampled": n_ev}),
-        "roofline": {"kernel": k_name, "bound": "hbm",
-                     "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_src, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "traffic_source": traffic_src,
-                     "traffic_last_capture": traffic_last,
-                     "algorithmic_bytes": k_bytes},
-        "e2e": {"value": round(job_rate(n_e2e, world, e2e_ms), 2), "unit": "tokens/s",
-                "h2d_bytes_per_step": D * 4, "d2h_bytes_per_step": D * 4, "steps": n_e2e},
+        "kernels_ms": {"layer_kernel": round(k_ms, 6), "layer_kernel_eager_events": round(eager_ms, 6),
+                       "eager_launches_sampled": n_ev},
+        "roofline": roof,
+        "e2e": e2e,
         "gpu_launches": (1 if (fused or mx) else 3) * args.steps,
-        "act_f16_mode": act16,
         "clocks": clocks,
     }
     for l in layers:
@@ -482,111 +528,27 @@ def run_reference(args):
 
 # ------------------------------------------------------ other workloads
 
-def _timed(steps, warmup, step, dev_index, world, graph_steps=0):
-    """Warm-up, then `steps` steps between two events on the current stream
-    (optionally replaying a CUDA graph of `graph_steps` steps); clocks are
-    sampled meanwhile.  Returns (ms total, steps actually timed, clocks)."""
-    import torch
-    s = torch.cuda.current_stream()
-    for i in range(warmup):
-        step(i)
-    torch.cuda.synchronize()
-    graph = None
-    if graph_steps:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            for i in range(graph_steps):
-                step(i)
-        graph.replay()
-        torch.cuda.synchronize()
-        steps = max(1, (steps + graph_steps - 1) // graph_steps) * graph_steps
-    clock = ClockSampler(dev_index)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    clock.start()
-    time.sleep(0.3)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(s)
-    if graph is not None:
-        for _ in range(steps // graph_steps):
-            graph.replay()
-    else:
-        for i in range(steps):
-            step(i)
-    t1.record(s)
-    torch.cuda.synchronize()
-    clocks = clock.stop()
-    if world > 1:
-        torch.distributed.barrier()
-    ms = max_over_ranks(t0.elapsed_time(t1), world, torch.device("cuda", dev_index))
-    return ms, steps, clocks
-
-
-def _kernel_events(layer, step, n, sync=True):
-    """Per-phase durations (ms) of `n` eager forwards, from the layer's four
-    events recorded on its stream: [route, route->gate/up, gate/up->end]."""
-    import torch
-    s = torch.cuda.current_stream()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
-    for q in evs:
-        for e in q:
-            e.record(s)
-    torch.cuda.synchronize()
-    for i in range(n):
-        layer.set_events(evs[i])
-        step(i)
-    layer.set_events(None)
-    torch.cuda.synchronize()
-    return ([q[0].elapsed_time(q[1]) for q in evs], [q[1].elapsed_time(q[2]) for q in evs],
-            [q[2].elapsed_time(q[3]) for q in evs])
-
-
 def _base_line(metric, value, unit, world, args, ms_step, dtype, config, clocks):
     return {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": dtype,
-            "data": "synthetic (seeded SplitMix64: uniform E2M1 codes, E8M0 in [120,130], "
-                    "x ~ N(0,1), W_r ~ N(0,0.02) bf16)",
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": DATA,
             "config": config, "clocks": clocks}
 
 
-def _roofline(name, nbytes, k_ms, bound="hbm"):
-    peak, src = measured_peaks()
-    ach = nbytes / (k_ms * 1e-3) / 1e9
-    return {"kernel": name, "bound": bound, "achieved": round(ach, 1), "peak": peak,
-            "peak_source": src, "unit": "GB/s", "frac": round(ach / peak, 4), "traffic": None,
-            "algorithmic_bytes": int(nbytes)}
+def cfg_steps(args, cap):
+    """Steps of one timed region of a secondary configuration: --steps, at
+    most `cap` (so that the default line stays within about a minute)."""
+    return max(1, min(args.steps, cap))
 
 
-def _e2e(step_host, n, world, dev_index, h2d, d2h, unit_per_step=1):
-    import torch
-    s = torch.cuda.current_stream()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(s)
-    for i in range(n):
-        step_host(i)
-    e1.record(s)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(e0.elapsed_time(e1), world, torch.device("cuda", dev_index))
-    return {"value": round(job_rate(n * unit_per_step, world, ms), 2), "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": n}
-
-
-def run_expert(args, rank, world, dev_index):
+def run_expert(args, ctx, rank, world):
     """One expert GEMV per step, rotating over the 896 resident experts and
     1024 tokens (17.5 MB per expert: every step reads HBM, not L2)."""
     import torch
     import synth
     from mxfp4_routed_expert_select_gb300 import k3moe as k
-    dev = torch.device("cuda", dev_index)
-    torch.cuda.set_device(dev)
-    blobs, views = build_pool(dev)
+    dev = ctx.dev
+    steps = cfg_steps(args, 1024)
     X = torch.from_numpy(np.stack([synth.token_f32(1, rank * N_TOKENS + t, D)
                                    for t in range(N_TOKENS)])).to(dev)
     y = torch.empty(D, dtype=torch.float32, device=dev)
@@ -594,11 +556,10 @@ def run_expert(args, rank, world, dev_index):
     perm = synth.permutation(E, synth.tag(synth.K_MISC, 1, 0, 7))
 
     def step(i):
-        k.expert_gemv(y, X[i % N_TOKENS], views[int(perm[i % E])], D, F, ws)
+        k.expert_gemv(y, X[i % N_TOKENS], ctx.views[int(perm[i % E])], D, F, ws)
 
-    ms, steps, clocks = _timed(args.steps, args.warmup, step, dev_index, world, 32)
-    args.steps = steps
-    per = ms / steps
+    ms, clocks, plan = timed_region(step, steps, args.warmup, ctx.dev_index, world, True, n_inputs=E)
+    per = statistics.median(ms) / steps
     nbytes = EXPERT_BYTES + 2 * D * 4
     xh = torch.empty((N_TOKENS, D), dtype=torch.float32, pin_memory=True)
     xh.copy_(X.cpu())
@@ -607,43 +568,41 @@ def run_expert(args, rank, world, dev_index):
 
     def step_host(i):
         xd.copy_(xh[i % N_TOKENS], non_blocking=True)
-        k.expert_gemv(y, xd, views[int(perm[i % E])], D, F, ws)
+        k.expert_gemv(y, xd, ctx.views[int(perm[i % E])], D, F, ws)
         yh.copy_(y, non_blocking=True)
 
-    e2e = _e2e(step_host, min(steps, 5000), world, dev_index, D * 4, D * 4)
-    e2e["unit"] = "expert GEMVs/s"
-    line = _base_line("single MXFP4 expert GEMV (1 token, d=7168, f=1536) per second",
-                      round(steps * world / (ms * 1e-3), 2), "expert GEMVs/s", world, args, per,
-                      "mxfp4 weights (e2m1 + e8m0), fp32 activations and accumulation",
-                      {"workload": "expert_gemv_b1: one expert d=7168 f=1536 (17,547,264 B), "
-                                   "x fp32 [7168], y fp32 [7168]",
-                       "launch": "cuda graph of 32 steps, replayed",
-                       "l2": "inputs larger than L2: 896 distinct experts (15.7 GB) rotated"}, clocks)
-    line.update({"roofline": _roofline("k3_rows_t1 + k3_down_t1 (one expert, gate/up + SwiGLU, "
-                                       "down)", nbytes, per),
-                 "e2e": e2e, "gpu_launches": 2 * steps,
-                 "expert_hbm": {"bytes_per_gemv": nbytes, "gbs": round(nbytes / (per * 1e-3) / 1e9, 1)}})
-    return line
+    e2e = _e2e(step_host, steps, args.warmup, world, ctx.dev_index, D * 4, D * 4, 1, "expert GEMVs/s")
+    return {
+        "metric": "single MXFP4 expert GEMV (1 token, d=7168, f=1536) per second",
+        "value": round(job_rate(steps, world, statistics.median(ms)), 2), "unit": "expert GEMVs/s",
+        "steps": steps, "ms_per_step": round(per, 6), "higher_is_better": True,
+        "config": {"workload": "expert_gemv_b1: one expert d=7168 f=1536 (17,547,264 B), x fp32 [7168], "
+                               "y fp32 [7168]",
+                   "launch": "cuda graphs of %d steps (%d offsets) + %d, replayed" %
+                             (plan["chunk"], plan["variants"], plan["rem"]),
+                   "l2": "inputs larger than L2: 896 distinct experts (15.7 GB) rotated"},
+        "timing": spread(ms, steps),
+        "roofline": _roofline(EXPERT_GEMV_KERNEL, nbytes, per),
+        "tflops": round(2 * 3 * D * F / (per * 1e-3) / 1e12, 3),
+        "e2e": e2e, "gpu_launches": EXPERT_GEMV_LAUNCHES * steps, "clocks": clocks,
+        "expert_hbm": {"bytes_per_gemv": nbytes, "gbs": round(nbytes / (per * 1e-3) / 1e9, 1)}}
 
 
-def run_batched(args, rank, world, dev_index, T, bf16, use_bias):
+def run_batched(args, ctx, rank, world, T, bf16, use_bias):
     """The layer on T tokens per step: the grouped path (router, top-k,
     grouping by expert, grouped gate/up + SwiGLU, grouped down, combine)."""
     import torch
     import synth
     from mxfp4_routed_expert_select_gb300 import k3moe as k
-    dev = torch.device("cuda", dev_index)
-    torch.cuda.set_device(dev)
-    blobs, views = build_pool(dev)
-    Wr_bits = synth.router_bf16(1, 0, E, D)
-    Wr0 = torch.from_numpy(Wr_bits.view(np.int16)).to(dev)
+    dev = ctx.dev
+    steps = cfg_steps(args, 64 if T <= 64 else 20)
     bias = None
     if use_bias:
         bias = torch.from_numpy(synth.bias_normal(1, 0, E).astype(np.float32)).to(dev)
     NB = max(2, min(16, (1 << 28) // (T * D * (2 if bf16 else 4))))
     n_r = 4 if T >= 1024 else 16
-    routers = [Wr0] + [Wr0.clone() for _ in range(n_r - 1)]
-    layers = [k.Layer(E, K, D, F, r, views, bias, max_tokens=T) for r in routers]
+    routers = [ctx.Wr0] + [ctx.Wr0.clone() for _ in range(n_r - 1)]
+    layers = [k.Layer(E, K, D, F, r, ctx.views, bias, max_tokens=T) for r in routers]
     if bf16:
         Xs = [torch.from_numpy(synth.tokens_bf16(1, T, D, t0=rank * NB * T + b * T).view(np.int16))
               .to(dev).view(torch.bfloat16) for b in range(NB)]
@@ -663,12 +622,12 @@ def run_batched(args, rank, world, dev_index, T, bf16, use_bias):
         torch.cuda.synchronize()
         U.append(len(np.unique(ids.cpu().numpy())))
     Umean = statistics.mean(U)
-    graph_steps = 8 if T <= 64 else 0
-    ms, steps, clocks = _timed(args.steps, args.warmup, step, dev_index, world, graph_steps)
-    args.steps = steps
-    per = ms / steps
+    use_graph = T <= 64
+    ms, clocks, plan = timed_region(step, steps, args.warmup, ctx.dev_index, world, use_graph,
+                                    n_inputs=NB, chunk_max=8)
+    per = statistics.median(ms) / steps
     r_ms, gu_ms, dn_ms = _kernel_events(layers[0], lambda i: layers[0].forward(Xs[i % NB], T, out),
-                                        min(steps, 64 if T <= 64 else 8))
+                                        64 if T <= 64 else 8)
     xb = T * D * (2 if bf16 else 4)
     w_bytes = Umean * EXPERT_BYTES
     step_bytes = w_bytes + ROUTER_BYTES + xb + T * D * 4
@@ -684,35 +643,36 @@ def run_batched(args, rank, world, dev_index, T, bf16, use_bias):
         layers[i % n_r].forward(xd, T, out)
         oh.copy_(out, non_blocking=True)
 
-    e2e = _e2e(step_host, min(steps, 200 if T <= 64 else 5), world, dev_index, xb, T * D * 4, T)
-    e2e["unit"] = "tokens/s"
+    e2e = _e2e(step_host, steps, args.warmup, world, ctx.dev_index, xb, T * D * 4, T, "tokens/s")
     name = "decode%d" % T if T <= 64 else "prefill%d" % T
     desc = ("moe_layer_%s: %d experts d=7168 f=1536 resident (%.1f GB), router bf16 [%dx7168], "
             "top-16, X %s [%dx7168]%s, grouped by expert" %
             (name, E, E * EXPERT_BYTES / 1e9, E, "bf16" if bf16 else "fp32", T,
              ", selection bias ~N(0,1)" if use_bias else ""))
-    line = _base_line("MoE-layer tokens/s (%d tokens per step, 896 experts, top-16, MXFP4)" % T,
-                      round(steps * T * world / (ms * 1e-3), 2), "tokens/s", world, args, per,
-                      "mxfp4 weights (e2m1 + e8m0), %s activations, fp32 accumulation" %
-                      ("bf16" if bf16 else "fp32"),
-                      {"workload": desc, "global_batch": T * world, "seq_len": 1,
-                       "launch": ("cuda graph of %d steps, replayed" % graph_steps) if graph_steps
-                       else "host launch per step",
-                       "l2": "inputs larger than L2: %d token batches, %d router copies, %.0f distinct "
-                             "experts (%.2f GB) per batch" % (NB, n_r, Umean, w_bytes / 1e9)}, clocks)
-    line.update({
-        "roofline": _roofline("k3_tc_expert<0,1> (tcgen05 kind::f8f6f4 gate/up + SwiGLU over the batch's "
-                              "experts; the timed span also holds grouping, tile plan, token scales and gather)",
+    gu_kernel = GROUPED_GATEUP_KERNEL
+    line = {
+        "metric": "MoE-layer tokens/s (%d tokens per step, 896 experts, top-16, MXFP4)" % T,
+        "value": round(job_rate(steps * T, world, statistics.median(ms)), 2), "unit": "tokens/s",
+        "steps": steps, "ms_per_step": round(per, 6), "higher_is_better": True,
+        "dtype": "mxfp4 weights (e2m1 + e8m0), %s activations, fp32 accumulation" % ("bf16" if bf16 else "fp32"),
+        "config": {"workload": desc, "global_batch": T * world, "seq_len": 1,
+                   "launch": ("cuda graphs of %d steps (%d offsets) + %d, replayed" %
+                              (plan["chunk"], plan["variants"], plan["rem"])) if use_graph
+                   else "host launch per step",
+                   "l2": "inputs larger than L2: %d token batches, %d router copies, %.0f distinct "
+                         "experts (%.2f GB) per batch" % (NB, n_r, Umean, w_bytes / 1e9)},
+        "timing": spread(ms, steps),
+        "roofline": _roofline(gu_kernel + " (gate/up + SwiGLU over the batch's experts; the timed span "
+                              "also holds grouping, tile plan and token preparation)",
                               gu_bytes, statistics.mean(gu_ms)),
         "step_bytes": {"distinct_experts": Umean, "bytes": int(step_bytes),
-                       "gbs": round(step_bytes / (per * 1e-3) / 1e9, 1)},
+                       "gbs": round(step_bytes / (per * 1e-3) / 1e9, 1),
+                       "frac_of_peak": round(step_bytes / (per * 1e-3) / 1e9 / measured_peaks()[0], 4)},
         "tflops": round(flops / (per * 1e-3) / 1e12, 2),
         "kernels_ms": {"route_topk": round(statistics.mean(r_ms), 4),
                        "group_gate_up_swiglu": round(statistics.mean(gu_ms), 4),
                        "down_combine": round(statistics.mean(dn_ms), 4)},
-        # router GEMM + top-k, grouping, tile plan, token scales, token gather,
-        # gate/up, h pieces, down + combine
-        "e2e": e2e, "gpu_launches": 9 * steps})
+        "e2e": e2e, "gpu_launches": GROUPED_LAUNCHES * steps, "clocks": clocks}
     for l in layers:
         l.close()
     return line
@@ -865,13 +825,11 @@ def run_stream(args, rank, world, dev_index, n_layers=4, cache_bytes=8_000_000_0
     od = torch.empty(D, dtype=torch.float32, device=dev)
 
     def step_host(i):
-        xd.copy_(xh[i], non_blocking=True)
+        xd.copy_(xh[i % 64], non_blocking=True)
         k.stream_decode(layers, cache, xd, 1, od, 1e-6, want_trace=False)
-        oh[i].copy_(od, non_blocking=True)
+        oh[i % 64].copy_(od, non_blocking=True)
 
-    n_e = 32
-    e2e = _e2e(step_host, n_e, world, dev_index, D * 4, D * 4)
-    e2e["unit"] = "tokens/s"
+    e2e = _e2e(step_host, 32, 3, world, dev_index, D * 4, D * 4, 1, "tokens/s")
     args.steps = n_tok
     line = _base_line("host-streamed MoE decode tokens/s (4 layers x 896 experts in pinned host "
                       "memory, 8 GB HBM LRU cache)", round(n_tok * world / (ms * 1e-3), 3), "tokens/s",
@@ -910,21 +868,34 @@ def run_stream(args, rank, world, dev_index, n_layers=4, cache_bytes=8_000_000_0
     return line
 
 
-WORKLOADS = {
-    "expert": lambda a, r, w, d: run_expert(a, r, w, d),
-    "decode64": lambda a, r, w, d: run_batched(a, r, w, d, 64, False, False),
-    "prefill4096": lambda a, r, w, d: run_batched(a, r, w, d, 4096, True, True),
-    "stream": lambda a, r, w, d: run_stream(a, r, w, d),
+POOL_WORKLOADS = {
+    "expert": lambda a, c, r, w: run_expert(a, c, r, w),
+    "decode64": lambda a, c, r, w: run_batched(a, c, r, w, 64, False, False),
+    "prefill4096": lambda a, c, r, w: run_batched(a, c, r, w, 4096, True, True),
 }
+WORKLOADS = dict(POOL_WORKLOADS, stream=None)
+
+
+def as_line(sub, args, world):
+    """A secondary configuration's object as a JSON line of its own."""
+    line = {"metric": sub["metric"], "value": sub["value"], "unit": sub["unit"], "n_gpus": world,
+            "steps": sub["steps"], "warmup": args.warmup, "ms_per_step": sub["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": sub.get("dtype", "mxfp4 weights (e2m1 + e8m0), fp32 activations and accumulation"),
+            "data": DATA}
+    line.update({k_: v for k_, v in sub.items() if k_ not in line})
+    return line
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="headline only: leave out the secondary configurations")
     ap.add_argument("--no-graph", action="store_true", help="launch every step from the host")
     ap.add_argument("--workload", default="decode1", choices=["decode1"] + sorted(WORKLOADS))
     ap.add_argument("--pin-hot", type=int, default=0,
@@ -939,6 +910,7 @@ def main():
     LAYER_BYTES = K * EXPERT_BYTES + ROUTER_BYTES
     if args.warmup < 3:
         args.warmup = 3
+    args.steps = max(1, args.steps)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -958,21 +930,23 @@ def main():
     if world > 1:
         torch.distributed.barrier()
         __graft_entry__.build()
-    if args.workload != "decode1":
-        res = WORKLOADS[args.workload](args, rank, world, local)
-        if rank == 0:
-            print(json.dumps(res), flush=True)
-        if world > 1:
-            torch.distributed.destroy_process_group()
-        return
-    res = run_ours(args, rank, world, local)
+    if args.workload == "stream":
+        res = run_stream(args, rank, world, local)
+    else:
+        ctx = Ctx(local)
+        if args.workload != "decode1":
+            res = as_line(POOL_WORKLOADS[args.workload](args, ctx, rank, world), args, world)
+        else:
+            res = run_decode1(args, ctx, rank, world)
+            if not args.no_configs:
+                res["configs"] = {name: fn(args, ctx, rank, world) for name, fn in POOL_WORKLOADS.items()}
+            if rank == 0 and not args.no_cpu_baseline:
+                n, t, cores = cpu_baseline_sample()
+                res["cpu_baseline"] = {"value": round(n / t, 4), "unit": "tokens/s", "cores": cores,
+                                       "kind": "oracle",
+                                       "sample": "%d tokens of the same layer (router + top-16 + 16 experts + "
+                                                 "combine, fp64, OpenMP over all host cores) in %.1f s" % (n, t)}
     if rank == 0:
-        if not args.no_cpu_baseline:
-            n, t, cores = cpu_baseline_sample()
-            res["cpu_baseline"] = {"value": round(n / t, 4), "unit": "tokens/s", "cores": cores,
-                                   "kind": "oracle",
-                                   "sample": "%d tokens of the same layer (router + top-16 + 16 experts + "
-                                             "combine, fp64) in %.1f s" % (n, t)}
         print(json.dumps(res), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

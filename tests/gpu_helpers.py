@@ -50,6 +50,8 @@ class Pool:
     def __init__(self, pool, layer, E, d, f, dev="cuda", e_lo=120, e_hi=130):
         self.pool, self.layer, self.E, self.d, self.f = pool, layer, E, d, f
         self.e_lo, self.e_hi = e_lo, e_hi
+        self._cache = {}
+        self.override = {}
         self.eb = k.expert_bytes(d, f)
         self.blobs = torch.empty((E, self.eb), dtype=torch.uint8, device=dev)
         for e in range(E):
@@ -58,8 +60,6 @@ class Pool:
                 torch.cuda.synchronize()
         torch.cuda.synchronize()
         self.views = [k.expert_view(self.blobs[e].data_ptr(), d, f) for e in range(E)]
-        self._cache = {}
-        self.override = {}
 
     def planes(self, e):
         """Host planes of expert e (a test may replace an expert's planes by

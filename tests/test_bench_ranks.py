@@ -54,3 +54,22 @@ def test_single_rank_needs_no_process_group():
 def test_job_rate_counts_every_rank():
     # 2 ranks x 100 steps in 50 ms (the slowest rank) -> 4000 steps/s
     assert bench.job_rate(100, 2, 50.0) == pytest.approx(4000.0)
+
+
+@pytest.mark.parametrize("steps,n_inputs,chunk_max", [(20, 1024, 32), (32, 1024, 32), (1000, 1024, 32),
+                                                     (1, 1, 32), (37, 896, 32), (64, 16, 8), (7, 4, 8)])
+def test_graph_plan_replays_exactly_the_requested_steps(steps, n_inputs, chunk_max):
+    """A timed region replays full * chunk + rem graph steps == --steps, and
+    the graph variants start at distinct input offsets within n_inputs."""
+    p = bench.graph_plan(steps, n_inputs, chunk_max)
+    assert p["full"] * p["chunk"] + p["rem"] == steps
+    assert 1 <= p["chunk"] <= chunk_max and p["rem"] < p["chunk"]
+    if p["full"]:
+        assert p["variants"] >= 1
+        offsets = [v * p["chunk"] for v in range(p["variants"])]
+        assert len(set(o % n_inputs for o in offsets)) == len(offsets) or p["variants"] == 1
+
+
+def test_spread_reports_median_min_max_per_step():
+    s = bench.spread([4.0, 2.0, 3.0, 10.0, 3.0], 2)
+    assert s == {"repeats": 5, "ms_per_step_median": 1.5, "ms_per_step_min": 1.0, "ms_per_step_max": 5.0}
