@@ -280,6 +280,17 @@ K3_DEV uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
                  : "memory");
     return ok;
 }
+// Non-blocking: has the phase of `parity` completed?
+K3_DEV bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
 K3_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int *err)
 {
     if (mbar_try_wait(bar, parity)) return true;
@@ -589,6 +600,117 @@ K3_DEV void cta_topk_by(Logit logit_of, const Router &rt, int E, int k, int32_t 
         }
     }
 }
+// 256 threads select the top k (k <= 16) of E <= 1024 selection keys
+// router_select(rt, logit_of(e), e), ties to the lower id, with the same
+// result as cta_topk_by and warp_topk.  Warp w holds keys 128 w .. 128 w +
+// 127, four per lane (lane l the ids 128 w + 4 l .. + 3), each lane's four
+// sorted (key descending, id ascending on ties).  k rounds of a warp maximum
+// (redux.sync) take the warp's k largest in order: the lowest lane whose
+// head equals the maximum wins a tie, and lower lanes hold lower ids, so
+// equal keys leave in id order.  The 8 warps' k candidates meet in shared
+// memory, four per lane of warp 0 in the same order, and k more rounds take
+// the CTA's k largest.  One CTA barrier (the sync() call), no atomics.
+// ids_out[0..k) receives the ids in ascending order, w_out the weights from
+// the unbiased scores, as in warp_topk.
+struct CtaTopkRedSmem {
+    uint32_t key[128];
+    int32_t id[128];
+    int32_t ids[16];
+};
+// (key, id) pairs a, b in order: key descending, id ascending on ties
+K3_DEV void topk_cmpswap(uint32_t &ka, int &ia, uint32_t &kb, int &ib)
+{
+    if (kb > ka || (kb == ka && ib < ia)) {
+        const uint32_t tk = ka;
+        const int ti = ia;
+        ka = kb;
+        ia = ib;
+        kb = tk;
+        ib = ti;
+    }
+}
+// The warp's k largest (k <= 32) of the 128 pairs held four per lane (each
+// lane's sorted): lane i < k receives the i-th largest in (rk, rid).
+K3_DEV void warp_take_k(uint32_t (&key)[4], int (&id)[4], int k, int lane, uint32_t &rk, int &rid)
+{
+    rk = 0u;
+    rid = 0;
+    for (int i = 0; i < k; i++) {
+        const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
+        const int w = __ffs(__ballot_sync(0xffffffffu, key[0] == m)) - 1;
+        const int wid = __shfl_sync(0xffffffffu, id[0], w);
+        if (lane == i) {
+            rk = m;
+            rid = wid;
+        }
+        if (lane == w) {
+            key[0] = key[1];
+            key[1] = key[2];
+            key[2] = key[3];
+            key[3] = 0u;
+            id[0] = id[1];
+            id[1] = id[2];
+            id[2] = id[3];
+            id[3] = 0x7fffffff;
+        }
+    }
+}
+template <typename Sync, typename Logit>
+K3_DEV void cta_topk_red(Logit logit_of, const Router &rt, int E, int k, int32_t *ids_out, float *w_out,
+                         CtaTopkRedSmem &sm, Sync sync)
+{
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    uint32_t key[4];
+    int id[4];
+#pragma unroll
+    for (int r = 0; r < 4; r++) {
+        const int e = 128 * warp + 4 * lane + r;
+        key[r] = 0u;  // below every real key (okey(-inf) = 0x007fffff)
+        id[r] = 0x7fffffff;
+        if (e < E) {
+            key[r] = okey(router_select(rt, logit_of(e), e));
+            id[r] = e;
+        }
+    }
+    topk_cmpswap(key[0], id[0], key[1], id[1]);
+    topk_cmpswap(key[2], id[2], key[3], id[3]);
+    topk_cmpswap(key[0], id[0], key[2], id[2]);
+    topk_cmpswap(key[1], id[1], key[3], id[3]);
+    topk_cmpswap(key[1], id[1], key[2], id[2]);
+    uint32_t rk;
+    int rid;
+    warp_take_k(key, id, k, lane, rk, rid);
+    // candidate slot 16 w + i, i < k (the rest stay below every real key)
+    if (lane < 16) {
+        sm.key[16 * warp + lane] = lane < k ? rk : 0u;
+        sm.id[16 * warp + lane] = lane < k ? rid : 0x7fffffff;
+    }
+    sync();
+    if (warp == 0) {
+#pragma unroll
+        for (int r = 0; r < 4; r++) {
+            key[r] = sm.key[4 * lane + r];
+            id[r] = sm.id[4 * lane + r];
+        }
+        warp_take_k(key, id, k, lane, rk, rid);
+        // each winner's place in ascending id order
+        if (lane < k) sm.ids[lane] = rid;
+        __syncwarp();
+        int rank = 0;
+        if (lane < k)
+            for (int q = 0; q < k; q++) rank += sm.ids[q] < rid;
+        __syncwarp();
+        if (lane < k) sm.ids[rank] = rid;
+        __syncwarp();
+        const int my_id = (lane < k) ? sm.ids[lane] : 0;
+        const float wv = router_weight(rt.mode, (lane < k) ? logit_of(my_id) : 0.f, lane < k);
+        if (lane < k) {
+            ids_out[lane] = my_id;
+            w_out[lane] = wv;
+        }
+    }
+}
+
 // logits in global memory (ld.cg: other CTAs may have written them)
 template <typename Sync>
 K3_DEV void cta_topk(const float *logit, const Router &rt, int E, int k, int32_t *ids_out, float *w_out,

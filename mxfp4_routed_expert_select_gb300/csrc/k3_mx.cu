@@ -17,18 +17,25 @@
 // 3^-16 (2e-8) of the block maximum.  The 16 pieces are the 16 columns of
 // one M = 128, N = 16 MMA; the epilogue adds the columns.
 //
-// Per token (one launch each, stream-ordered):
-//   router   (k3_route.cu) logits, top-k, and the pieces of x: a B image
-//            [K/256][16 rows][128 bytes], 128-byte swizzled, plus E8M0 scale
-//            atoms [K/128][512 bytes] in the layout tcgen05.cp copies to TMEM
+// Per token, one cooperative launch (one CTA per SM):
+//   router   logits of this CTA's block of router rows, a grid barrier, then
+//            every CTA selects the top k itself (k rounds of a warp maximum
+//            per warp, then over the warps' candidates) and the pieces of x
+//            are copied in: a B image [K/256][16 rows][128 bytes], 128-byte
+//            swizzled, plus E8M0 scale atoms [K/128][512 bytes] in the layout
+//            tcgen05.cp copies to TMEM
 //   phase 0  gate and up rows of the k experts (tiles of 128 rows, K = d):
-//            g, u -> h = silu(r g) * (r u) (r = the RMSNorm factor or 1) ->
-//            the pieces of h per expert (B images of phase 1)
+//            g, u -> h = silu(g) * u -> the pieces of h per expert (B images
+//            of phase 1)
 //   phase 1  down rows (tiles of 128 rows, K = f): y_j -> out = sum_j w_j y_j
-// Both phases split the k * rows/128 tiles' K steps evenly over one CTA per
-// SM (a tile may be split between CTAs); a split tile's partial sums meet in
-// a workspace and the CTA that completes the tile (an acq_rel ticket) adds
-// them in a fixed order, so results do not depend on timing.
+// Both phases split the k * rows/128 tiles' K steps evenly over the CTAs (a
+// tile may be split between CTAs).  The CTA holding a split tile's first
+// units (at the end of its range) finishes the tile: it waits for the other
+// segments' partial sums, published early in the ranges of the CTAs after
+// it, while its own MMAs still run, and adds them in a fixed order, so the
+// result does not depend on timing.  The launch is a programmatic dependent
+// of the previous kernel on the stream: the router rows are requested before
+// that kernel has finished, everything else after it.
 //
 // A weight group whose scale byte is 255 is dropped, as on the other paths:
 // its scale becomes 0 (2^-127), so it adds at most 6 * 2^-127 * sum |v| of
@@ -44,6 +51,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 
 #include "k3_mx.cuh"
@@ -446,6 +454,39 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
             const long t0 = (long)tile * upt, t1 = t0 + upt;
             const long ua = u, ub = t1 < uhi ? t1 : uhi;
             u = ub;
+            // a split tile's partial sums sit in slots indexed by the first
+            // unit of their segment
+            const bool whole = ua == t0 && ub == t1;
+            const int seg = (int)(ua - t0);
+            const int j = tile / tpe, t = tile % tpe;
+            float pv[NOUT];
+#pragma unroll
+            for (int m = 0; m < NOUT; m++) pv[m] = 0.f;
+            if (PH == 0 && !whole && ua == t0) {
+                // the first segment: this CTA finishes the tile.  The other
+                // segments' parts (published at the start of the other CTAs'
+                // ranges) are waited for and read before this segment's own
+                // accumulator is, so that their round trips overlap its MMAs;
+                // they are added in unit order
+                const float *pp = a.part + ((size_t)tile * upt) * MX_M * NOUT;
+                int nother = 0;
+                for (long us = ub; us < t1;) {
+                    const long ub2 = U * (cta_of(us) + 1) / G;
+                    us = ub2 < t1 ? ub2 : t1;
+                    nother++;
+                }
+                if (leader) *s_last = mx_wait_count(a.cnt + tile, (unsigned)nother, a.err) ? 1u : 0u;
+                __syncwarp();
+                mx_bar_epi();
+                if (*s_last != 1u) *abort_flag = 1;
+                for (long us = ub; us < t1;) {
+                    const long ub2 = U * (cta_of(us) + 1) / G, ue = ub2 < t1 ? ub2 : t1;
+#pragma unroll
+                    for (int m = 0; m < NOUT; m++) pv[m] += __ldcg(pp + ((size_t)(us - t0) * MX_M + row) * NOUT + m);
+                    us = ue;
+                }
+                if (leader) a.cnt[tile] = 0;  // for the next launch
+            }
             const int buf = sg & 1;
             const bool ok = __all_sync(0xffffffffu, tc_wait(bar(B_ACCF + buf), (sg / 2) & 1, a.err, abort_flag));
             float v[NOUT];
@@ -473,11 +514,6 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                 if (lane == 0) mbar_arrive(bar(B_ACCE + buf));
             }
             sg++;
-            // a split tile's partial sums sit in slots indexed by the first
-            // unit of their segment
-            const bool whole = ua == t0 && ub == t1;
-            const int seg = (int)(ua - t0);
-            const int j = tile / tpe, t = tile % tpe;
             if (PH == 0) {
                 float *pp = a.part + ((size_t)tile * upt) * MX_M * NOUT;
                 if (!whole && ua != t0) {
@@ -491,27 +527,8 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                     if (leader) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.cnt + tile) : "memory");
                     continue;
                 }
-                if (!whole) {
-                    // the first segment: wait for the others' parts (usually
-                    // published long before), add them in unit order
-                    int nother = 0;
-                    for (long us = ub; us < t1;) {
-                        const long ub2 = U * (cta_of(us) + 1) / G;
-                        us = ub2 < t1 ? ub2 : t1;
-                        nother++;
-                    }
-                    if (leader) *s_last = mx_wait_count(a.cnt + tile, (unsigned)nother, a.err) ? 1u : 0u;
-                    __syncwarp();
-                    mx_bar_epi();
-                    if (*s_last != 1u) *abort_flag = 1;
-                    for (long us = ub; us < t1;) {
-                        const long ub2 = U * (cta_of(us) + 1) / G, ue = ub2 < t1 ? ub2 : t1;
 #pragma unroll
-                        for (int m = 0; m < NOUT; m++) v[m] += __ldcg(pp + ((size_t)(us - t0) * MX_M + row) * NOUT + m);
-                        us = ue;
-                    }
-                    if (leader) a.cnt[tile] = 0;  // for the next launch
-                }
+                for (int m = 0; m < NOUT; m++) v[m] += pv[m];
                 const float h = silu(v[0]) * v[1];
                 mx_encode_block(h, lane, (t * MX_M + qd * 32) / 32, a.himg + (size_t)j * a.f * 8,
                                 a.hsf + (size_t)j * (a.f / 128) * 512);
@@ -570,7 +587,7 @@ struct MxRoute {
 // a timeout.
 template <typename XT>
 K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, uint8_t *sm, uint32_t bar_r, uint32_t bload0,
-                     int32_t *sel_ids, float *sel_w, float *s_logit, CtaTopkSmem &tk, unsigned *s_flag)
+                     int32_t *sel_ids, float *sel_w, float *s_logit, CtaTopkRedSmem &tk, unsigned *s_flag)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int d = a0.d, E = r.E, G = gridDim.x;
@@ -582,6 +599,11 @@ K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, uint8_t *sm
         const uint8_t *src = reinterpret_cast<const uint8_t *>(r.Wr + (size_t)e0 * d);
         for (uint32_t o = 0; o < rbytes; o += 16384) bulk_g2s(sbase + o, src + o, min(16384u, rbytes - o), bar_r);
     }
+    // Launched as a programmatic dependent of the previous kernel on the
+    // stream: only the router rows (weights, never written by a kernel) are
+    // requested before it has completed; x, out and the workspace are touched
+    // after this wait.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const XT *x = reinterpret_cast<const XT *>(r.x);
     const long NW = (long)G * (MX_THREADS / 32), gw = (long)blockIdx.x * (MX_THREADS / 32) + warp;
     for (long b = gw; b < (d >> 5); b += NW) {
@@ -651,10 +673,10 @@ K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, uint8_t *sm
     // with the rule folded away
     auto logit_of = [&](int e) { return s_logit[e]; };
     if (r.rt.mode == K3_ROUTER_SOFTMAX)
-        cta_topk_by(logit_of, Router{r.rt.bias, K3_ROUTER_SOFTMAX}, E, a0.k, sel_ids, sel_w, tk,
-                    [] { cta_sync_threads(); });
+        cta_topk_red(logit_of, Router{r.rt.bias, K3_ROUTER_SOFTMAX}, E, a0.k, sel_ids, sel_w, tk,
+                      [] { cta_sync_threads(); });
     else
-        cta_topk_by(logit_of, r.rt, E, a0.k, sel_ids, sel_w, tk, [] { cta_sync_threads(); });
+        cta_topk_red(logit_of, r.rt, E, a0.k, sel_ids, sel_w, tk, [] { cta_sync_threads(); });
     cta_sync_threads();
     if (blockIdx.x == 0 && threadIdx.x < a0.k) {
         r.ids_out[threadIdx.x] = sel_ids[threadIdx.x];
@@ -674,7 +696,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     __shared__ int32_t sel_ids[32];
     __shared__ float sel_w[32];
     __shared__ float s_logit[1024];
-    __shared__ CtaTopkSmem tk;
+    __shared__ CtaTopkRedSmem tk;
     __shared__ unsigned s_flag;  // 1: the router's grid barrier passed, x image copies issued
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -714,6 +736,10 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     // phase 0's MMAs to complete (its FIN barrier); phase 1's TMEM columns
     // are not phase 0's accumulators, which the epilogue may still read.
     const uint32_t fin0 = smem_addr(bars0 + MxBars<0>::FIN);
+    // the next kernel on the stream may start its launch (its CTAs take
+    // the SMs this grid leaves and wait for its completion before reading
+    // anything it writes)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     mx_body<0>(a0, sm, bars0, tmem, abort_flag, s_last, s_stop, hready, sel_ids, sel_w, 0u, &s_flag);
     mx_body<1>(a1, sm, bars1, tmem, abort_flag, s_last, s_stop, hready, sel_ids, sel_w, fin0, &s_flag);
 
@@ -811,9 +837,31 @@ static int launch_layer(const MxRoute &r, const MxArgs &a0, const MxArgs &a1, un
                         uint32_t bar_off, size_t smem, cudaStream_t s)
 {
     if (ensure_smem((const void *)k3_mx_layer<XT>, smem) != K3MOE_OK) return K3MOE_ECUDA;
-    void *args[] = {(void *)&r, (void *)&a0, (void *)&a1, (void *)&hready, (void *)&exit_cnt, (void *)&bar_off};
-    if (cudaLaunchCooperativeKernel((const void *)k3_mx_layer<XT>, dim3(num_sms()), dim3(MX_THREADS), args, smem, s) !=
-        cudaSuccess) {
+    // cooperative (every CTA resident: the CTAs wait for each other) and, where
+    // the driver takes it, a programmatic dependent of the previous kernel on
+    // the stream, so that its launch and router-row copies overlap that
+    // kernel's tail
+    static std::atomic<int> pdl_refused{0};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms());
+    cfg.blockDim = dim3(MX_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_refused.load(std::memory_order_relaxed) ? 1 : 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k3_mx_layer<XT>, r, a0, a1, hready, exit_cnt, bar_off);
+    if (e != cudaSuccess && cfg.numAttrs == 2) {
+        cudaGetLastError();
+        pdl_refused.store(1, std::memory_order_relaxed);
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, k3_mx_layer<XT>, r, a0, a1, hready, exit_cnt, bar_off);
+    }
+    if (e != cudaSuccess) {
         cudaGetLastError();
         return K3MOE_ECUDA;
     }

@@ -39,6 +39,16 @@ K3_DEV void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint
                  : "memory");
 }
 
+// A hint: bring one TMA tile (x = byte column, y = row) of `map` into L2.
+// Nothing waits for it; a later load of the same tile hits L2 if the line is
+// still there.
+K3_DEV void tma_prefetch_l2_2d(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"((uint64_t)map), "r"(x),
+                 "r"(y)
+                 : "memory");
+}
+
 // 8 consecutive fp32 columns (column address a multiple of 8).
 K3_DEV void tmem_ld8(uint32_t taddr, float (&v)[8])
 {
