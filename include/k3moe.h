@@ -185,6 +185,26 @@ int k3moe_expert_gemv(float *y, const float *x, const k3moe_expert *host_e, int3
 int k3moe_expert_gemv_noalloc(float *y, const float *x, const k3moe_expert *host_e, int32_t d,
                               int32_t f, k3moe_stream s);
 
+/*
+ * MXFP4 quantisation of activations (the conversion K3MOE_OPT_MXQ applies;
+ * the pages quantise only the weights, so the rule is the OCP Microscaling
+ * v1.0 conversion to E2M1 with one E8M0 scale per 32): per 32-block of a row
+ * the scale byte is e = floor(log2 amax) - 2 + 127 clamped to [0, 254] (the
+ * block's largest magnitude amax; e = 0 for an all-zero block); each value
+ * divided by 2^(e-127) rounds to the nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6,
+ * ties to the even code, larger magnitudes saturating to 6; the sign is bit
+ * 3 of the code (a negative value that rounds to 0 gives code 8).  A block
+ * holding a non-finite value gets scale byte 255 and codes 0.
+ *  x       device, [rows][cols], x_dtype K3MOE_F32 or K3MOE_BF16, cols a
+ *          multiple of 32
+ *  codes   device, [rows][cols/2] bytes (out): two codes per byte, the even
+ *          element in the low nibble (the weights' packing)
+ *  scales  device, [rows][cols/32] bytes (out)
+ * Errors: K3MOE_EINVAL for null pointers, sizes <= 0, cols % 32 != 0.
+ */
+int k3moe_mx_quantize(uint8_t *codes, uint8_t *scales, const void *x, int x_dtype, int32_t rows,
+                      int32_t cols, k3moe_stream s);
+
 /* ----------------------------------------------------------------- layer */
 
 /*
@@ -299,6 +319,20 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int x_dtype, int32_t T, f
  *  K3MOE_OPT_SIGMOID_NORM  with K3MOE_OPT_SIGMOID_ROUTER, the weights are
  *                      divided by their sum over the chosen set (the pages do
  *                      not say whether they are renormalised).  Default 0.
+ *  K3MOE_OPT_MXQ       multi-token forwards (T > 1) of a layer created with
+ *                      max_tokens > 1 quantise the activations to MXFP4 and
+ *                      run the expert products as block-scaled E2M1 x E2M1
+ *                      GEMMs (tcgen05.mma kind::mxf4, weights as stored): x
+ *                      per 32-block along d and h = silu(g) * u (held in
+ *                      fp32) per 32-block along f, each by the conversion of
+ *                      k3moe_mx_quantize; fp32 accumulation; the weighted
+ *                      combine by fp32 reductions.  The pages quantise only
+ *                      the weights this way ["kimi-k3-in-c" explainer,
+ *                      "Reduction one"]; quantising the activations too is a
+ *                      different contract: the result is the layer of
+ *                      quantised activations (about 10% from the exact one
+ *                      per output vector), not the exact layer.  Needs
+ *                      d % 512 == 0, f % 512 == 0.  Default 0.
  * k3moe_layer_fused_t1 returns 1 when a batch-1 fp32 forward of this layer
  * would run fused (the block-scaled path is off or unsupported), else 0
  * (negative on error).  After a device-side timeout
@@ -311,11 +345,15 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int x_dtype, int32_t T, f
 #define K3MOE_OPT_MX       16
 #define K3MOE_OPT_SIGMOID_ROUTER 32
 #define K3MOE_OPT_SIGMOID_NORM   64
+#define K3MOE_OPT_MXQ            128
 int k3moe_layer_set_option(k3moe_layer *L, int32_t option, int32_t value);
 int k3moe_layer_fused_t1(const k3moe_layer *L);
 /* 1 when a batch-1 forward of this layer runs on the block-scaled tensor
  * cores (K3MOE_OPT_MX set and the layer supports it), else 0. */
 int k3moe_layer_mx_t1(const k3moe_layer *L);
+/* 1 when a multi-token forward of this layer runs with MXFP4 activations
+ * (K3MOE_OPT_MXQ set and the layer has its buffers and tensor maps), else 0. */
+int k3moe_layer_mxq(const k3moe_layer *L);
 
 /*
  * Timing hook: when set, every later k3moe_layer_forward records

@@ -39,6 +39,16 @@ int launch_group(const int32_t *ids, int npairs, int E, int nt, int32_t *offsets
                  int4 *items, int32_t *n_items, cudaStream_t s);
 int grouped_nt();
 bool tc_supported(int E, int k, int d, int f);
+bool mxq_supported(int E, int k, int d, int f);
+int mxq_max_tiles(int npairs, int E);
+size_t mxq_max_rows(int npairs, int E);
+size_t mxq_tile_bytes();
+int launch_mx_quantize(const void *x, int xdt, int rows, int cols, uint8_t *codes, uint8_t *scales,
+                       cudaStream_t s);
+int launch_mxq(const void *X, int xdt, int T, int k, int E, int d, int f, const void *maps,
+               const int32_t *offsets, const int32_t *perm, const float *wsel, void *tiles, int32_t *n_tiles,
+               int32_t *tbase, int32_t *slot, int max_tiles, uint8_t *Xg, uint8_t *Xsf, uint8_t *Hg, uint8_t *Hsf,
+               float *out, int *err, cudaStream_t s);
 int tc_max_tiles(int npairs, int E);
 size_t tc_xg_bytes(int npairs, int E, int d);
 size_t tc_hg_bytes(int npairs, int E, int f);
@@ -275,6 +285,16 @@ struct k3moe_layer {
     uint8_t *mx_ximg;    // pieces of x: B image + scale atoms
     uint8_t *mx_himg;    // pieces of h per selected expert
     float *mx_part;      // split-tile partial sums
+    // MXFP4-activation grouped path (T > 1, kind::mxf4)
+    bool mxq;            // K3MOE_OPT_MXQ (default off)
+    bool mxq_ready;      // its buffers exist (and the mx tensor maps)
+    void *mq_tiles;      // [mq_max_tiles] tiles
+    int32_t *mq_ntiles;  // [1]
+    int32_t *mq_tbase;   // [E] first tile of each expert
+    int32_t *mq_slot;    // [maxT * k] tile row of each pair
+    int mq_max_tiles;
+    uint8_t *mq_xg, *mq_xsf;  // token codes (rows) and scale atoms (per tile)
+    uint8_t *mq_hg, *mq_hsf;  // h codes and scale atoms
     unsigned *mx_cnt;    // tile tickets (zero between launches)
 };
 
@@ -291,7 +311,8 @@ static void layer_free(k3moe_layer *L)
     void *ptrs[] = {L->table, L->logits, L->part,  L->ids,     L->w,      L->h,    L->Y,
                     L->offsets, L->perm, L->items, L->n_items, L->ticket, L->ctr,
                     L->tc_tiles, L->tc_ntiles, L->Xg, L->Hg, L->tc_maps, L->tscale, L->hf, L->hmax,
-                    L->mx_maps, L->mx_ximg, L->mx_himg, L->mx_part, L->mx_cnt};
+                    L->mx_maps, L->mx_ximg, L->mx_himg, L->mx_part, L->mx_cnt,
+                    L->mq_tiles, L->mq_ntiles, L->mq_tbase, L->mq_slot, L->mq_xg, L->mq_xsf, L->mq_hg, L->mq_hsf};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     delete L;
@@ -366,6 +387,19 @@ int k3moe_layer_create(k3moe_layer **out, const k3moe_layer_desc *D)
         alloc((void **)&L->mx_cnt, sizeof(unsigned) * k3::mx_cnt_words(L->k, L->d, L->f));
         L->mx_ready = ok;
         L->mx = true;
+        if (L->maxT > 1 && k3::mxq_supported(L->E, L->k, L->d, L->f)) {
+            L->mq_max_tiles = k3::mxq_max_tiles((int)pairs, L->E);
+            const size_t rows = k3::mxq_max_rows((int)pairs, L->E);
+            alloc(&L->mq_tiles, k3::mxq_tile_bytes() * L->mq_max_tiles);
+            alloc((void **)&L->mq_ntiles, sizeof(int32_t));
+            alloc((void **)&L->mq_tbase, sizeof(int32_t) * L->E);
+            alloc((void **)&L->mq_slot, sizeof(int32_t) * pairs);
+            alloc((void **)&L->mq_xg, rows * (L->d / 2));
+            alloc((void **)&L->mq_xsf, (size_t)L->mq_max_tiles * (L->d / 128) * 512);
+            alloc((void **)&L->mq_hg, rows * (L->f / 2));
+            alloc((void **)&L->mq_hsf, (size_t)L->mq_max_tiles * (L->f / 128) * 512);
+            L->mxq_ready = ok;
+        }
     }
     L->fused = true;
     L->act16 = false;
@@ -395,6 +429,7 @@ int k3moe_layer_create(k3moe_layer **out, const k3moe_layer_desc *D)
     if (st == cudaSuccess && L->mx_ready) {
         if (k3::mx_make_maps(tmp, L->E, L->d, L->f, L->mx_maps) != K3MOE_OK) {
             L->mx_ready = false;  // the fused CUDA-core kernel serves instead
+            L->mxq_ready = false;
         } else {
             st = cudaMemset(L->mx_cnt, 0, sizeof(unsigned) * k3::mx_cnt_words(L->k, L->d, L->f));
             if (st == cudaSuccess) st = cudaMemset(L->mx_ximg, 0, k3::mx_ximg_bytes(L->d));
@@ -497,6 +532,14 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int xdt, int32_t T, float
         K3_TRY(k3::launch_rows_t1(1, (const float *)X, src, L->k, L->d, L->f, L->h, st));
         if (L->nev) K3_CUDA(cudaEventRecord(L->ev[2], st));
         K3_TRY(k3::launch_down_t1(L->h, src, L->w, L->k, L->d, L->f, out, st));
+    } else if (L->mxq && L->mxq_ready) {
+        int *err = k3::device_error_word();
+        K3_TRY(k3::launch_group(L->ids, T * L->k, L->E, k3::grouped_nt(), L->offsets, L->perm,
+                                L->items, L->n_items, st));
+        if (L->nev) K3_CUDA(cudaEventRecord(L->ev[2], st));
+        K3_TRY(k3::launch_mxq(X, xdt, T, L->k, L->E, L->d, L->f, L->mx_maps, L->offsets, L->perm, L->w,
+                              L->mq_tiles, L->mq_ntiles, L->mq_tbase, L->mq_slot, L->mq_max_tiles, L->mq_xg,
+                              L->mq_xsf, L->mq_hg, L->mq_hsf, out, err, st));
     } else if (L->tc && L->tc_ready) {
         int *err = k3::device_error_word();
         K3_TRY(k3::launch_group(L->ids, T * L->k, L->E, k3::grouped_nt(), L->offsets, L->perm,
@@ -560,6 +603,10 @@ int k3moe_layer_set_option(k3moe_layer *L, int32_t option, int32_t value)
         L->sig_norm = value != 0;
         return K3MOE_OK;
     }
+    if (option == K3MOE_OPT_MXQ) {
+        L->mxq = value != 0;
+        return K3MOE_OK;
+    }
     return K3MOE_EINVAL;
 }
 
@@ -574,6 +621,21 @@ int k3moe_layer_mx_t1(const k3moe_layer *L)
 {
     if (!L) return K3MOE_EINVAL;
     return (L->mx && L->mx_ready) ? 1 : 0;
+}
+
+int k3moe_layer_mxq(const k3moe_layer *L)
+{
+    if (!L) return K3MOE_EINVAL;
+    return (L->mxq && L->mxq_ready) ? 1 : 0;
+}
+
+int k3moe_mx_quantize(uint8_t *codes, uint8_t *scales, const void *x, int x_dtype, int32_t rows, int32_t cols,
+                      k3moe_stream s)
+{
+    if (!codes || !scales || !x || rows <= 0 || cols <= 0 || cols % 32 ||
+        (x_dtype != K3MOE_F32 && x_dtype != K3MOE_BF16))
+        return K3MOE_EINVAL;
+    return k3::launch_mx_quantize(x, x_dtype, rows, cols, codes, scales, cs(s));
 }
 
 int k3moe_layer_set_events(k3moe_layer *L, void *const *host_events, int32_t n)

@@ -33,6 +33,7 @@ K3MOE_OPT_TC_E4M3 = 8
 K3MOE_OPT_MX = 16
 K3MOE_OPT_SIGMOID_ROUTER = 32
 K3MOE_OPT_SIGMOID_NORM = 64
+K3MOE_OPT_MXQ = 128
 K3MOE_NOALLOC_MAX_F = 2048
 
 
@@ -121,6 +122,8 @@ SIGNATURES = {
     "k3moe_layer_set_option": (ctypes.c_int, [_P, _I, _I]),
     "k3moe_layer_fused_t1": (ctypes.c_int, [_P]),
     "k3moe_layer_mx_t1": (ctypes.c_int, [_P]),
+    "k3moe_layer_mxq": (ctypes.c_int, [_P]),
+    "k3moe_mx_quantize": (ctypes.c_int, [_P, _P, _P, _I, _I, _I, _P]),
     "k3moe_rmsnorm": (ctypes.c_int, [_P, _P, _I, _F, _P]),
     "k3moe_residual_add": (ctypes.c_int, [_P, _P, _I, _P]),
     "k3moe_cache_create": (ctypes.c_int, [_P, _SZ, _SZ, _P, _I, _I]),
@@ -255,6 +258,16 @@ def expert_gemv(y, x, expert, d, f, workspace, stream=None):
                                   nbytes, _stream(stream)), "k3moe_expert_gemv")
 
 
+def mx_quantize(codes, scales, x, rows, cols, stream=None):
+    """MXFP4 quantisation of activations (k3moe_mx_quantize): x [rows][cols]
+    (fp32 or bf16 tensor) -> codes uint8 [rows][cols/2], scales uint8
+    [rows][cols/32]."""
+    import torch
+    dt = K3MOE_BF16 if x.dtype == torch.bfloat16 else K3MOE_F32
+    check(lib().k3moe_mx_quantize(_ptr(codes), _ptr(scales), _ptr(x), dt, rows, cols, _stream(stream)),
+          "k3moe_mx_quantize")
+
+
 def expert_gemv_noalloc(y, x, expert, d, f, stream=None):
     """k3moe_expert_gemv without a workspace (static device scratch)."""
     check(lib().k3moe_expert_gemv_noalloc(_ptr(y), _ptr(x), ctypes.byref(expert), d, f,
@@ -313,6 +326,9 @@ class Layer:
 
     def mx_t1(self):
         return lib().k3moe_layer_mx_t1(self.h) == 1
+
+    def mxq(self):
+        return lib().k3moe_layer_mxq(self.h) == 1
 
     def set_events(self, events):
         """events: 4 torch.cuda.Event (or None to clear); each must have been

@@ -314,6 +314,39 @@ def combine_grouped(x, ids, w, planes_of, h_bf16=False):
     return out
 
 
+def combine_grouped_mxq(x, ids, w, planes_of, on_expert=None):
+    """The layer with MXFP4-quantised activations, grouped by expert: the
+    steps of ``expert_forward_mxq`` (x quantised per 32-block by
+    ``mx_quantize``; g and u in fp64 from the dequantised weights; h =
+    silu(g) u rounded to fp32 and quantised the same way; y = W_down h_q),
+    each expert's tokens in one library matrix product, weighted and summed
+    as in ``combine``.  ``on_expert(e, ts, js, h32, Wd)``, if given, sees
+    every expert's fp32 h rows and its dequantised down matrix (for a
+    test's tolerance of rounding decisions)."""
+    x = _c(np.atleast_2d(x), np.float64)
+    T, d = x.shape
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float64)
+    xq = mx_quantize(x.astype(np.float32).ravel())[0].reshape(T, d)
+    out = np.zeros((T, d), np.float64)
+    for e in np.unique(ids):
+        ts, js = np.nonzero(ids == e)
+        ex = planes_of(int(e))
+        Xe = xq[ts]
+        g = np.ascontiguousarray(Xe @ dequant(ex["gate_packed"], ex["gate_scales"]).T)
+        u = np.ascontiguousarray(Xe @ dequant(ex["up_packed"], ex["up_scales"]).T)
+        lib().orc_swiglu_n(_p(g), _p(u), g.size, 0)
+        h32 = g.astype(np.float32)
+        hq = mx_quantize(h32.ravel())[0].reshape(h32.shape)
+        Wd = dequant(ex["down_packed"], ex["down_scales"])
+        y = hq @ Wd.T
+        # a token selects an expert at most once, so ts has no repeats
+        out[ts] += w[ts, js][:, None] * y
+        if on_expert is not None:
+            on_expert(int(e), ts, js, h32, Wd)
+    return out
+
+
 def layer_forward(x, Wr_bits, k, experts, bias=None, h_bf16=False):
     """Full layer. `experts` must hold (at least) every expert selected."""
     x = _c(np.atleast_2d(x), np.float64)

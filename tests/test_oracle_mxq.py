@@ -140,3 +140,37 @@ def test_expert_forward_mxq_is_the_composition(d, f):
     exact = oracle.expert_forward(ex, x.astype(np.float64))
     rel = np.max(np.abs(got - exact)) / np.max(np.abs(exact))
     assert 1e-4 < rel < 0.5
+
+
+def test_grouped_mxq_combine_equals_the_per_pair_forward():
+    """The grouped form (each expert's tokens in one fp64 matrix product) is
+    the weighted sum of expert_forward_mxq over the chosen experts, up to the
+    order of fp64 sums; a planted mistake (a pair's weight dropped) is seen."""
+    rng = np.random.default_rng(21)
+    d, f, E, k, T = 128, 64, 6, 3, 7
+    exs = {}
+    for e in range(E):
+        exs[e] = dict(gate_packed=rng.integers(0, 256, (f, d // 2), dtype=np.uint8),
+                      gate_scales=rng.integers(120, 131, (f, d // 32), dtype=np.uint8),
+                      up_packed=rng.integers(0, 256, (f, d // 2), dtype=np.uint8),
+                      up_scales=rng.integers(120, 131, (f, d // 32), dtype=np.uint8),
+                      down_packed=rng.integers(0, 256, (d, f // 2), dtype=np.uint8),
+                      down_scales=rng.integers(120, 131, (d, f // 32), dtype=np.uint8))
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    ids = np.stack([np.sort(rng.choice(E, k, replace=False)) for _ in range(T)]).astype(np.int32)
+    w = rng.random((T, k))
+    ref = np.zeros((T, d))
+    for t in range(T):
+        for j in range(k):
+            ref[t] += w[t, j] * oracle.expert_forward_mxq(exs[int(ids[t, j])], x[t])
+    seen = []
+    got = oracle.combine_grouped_mxq(x, ids, w, lambda e: exs[e],
+                                     on_expert=lambda e, ts, js, h32, Wd: seen.append((e, len(ts), h32.shape)))
+    scale = np.abs(ref).max()
+    assert np.max(np.abs(got - ref)) <= 1e-12 * scale
+    assert sorted(s[0] for s in seen) == sorted(set(int(v) for v in ids.ravel()))
+    assert all(s[2] == (s[1], f) for s in seen)
+    w2 = w.copy()
+    w2[3, 2] = 0.0
+    bad = oracle.combine_grouped_mxq(x, ids, w2, lambda e: exs[e])
+    assert np.max(np.abs(bad - ref)) > 1e-3 * scale
