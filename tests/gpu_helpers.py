@@ -122,3 +122,77 @@ def tokens_device(pool, T, d, subs, bf16=False, dev="cuda"):
         return torch.from_numpy(X.view(np.int16)).to(dev).view(torch.bfloat16)
     X = np.stack([synth.token_f32(pool, t, d, int(subs[t])) for t in range(T)])
     return torch.from_numpy(X).to(dev)
+
+
+# ------------------------------------------- MXFP4-activation path parity
+
+MXQ_TAU = 3e-5  # reach of fp32 rounding, relative to a block's largest |h|
+_MIDS = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+_GAPS = np.array([0.5, 0.5, 0.5, 0.5, 1.0, 1.0, 2.0])
+
+
+def mxq_flip_bound(h32, Wd, wts):
+    """Allowance (per output row) for the h codes whose rounding decision is
+    within MXQ_TAU of the block maximum of a boundary: an element near an
+    E2M1 midpoint may move one step (the gap at that midpoint); a block whose
+    maximum is near a power of two may take the neighbouring scale, and its
+    elements may then move by the difference between the two quantisations,
+    both computed by the oracle's quantiser (the second on the block with its
+    largest element moved just across the power of two).  h32 [n, f] fp32
+    (the oracle's h rows of one expert), Wd [d, f] its dequantised down
+    matrix, wts [n] the pairs' combine weights.
+    Returns [n, d]: w * sum_i |Wd[r, i]| * delta_i."""
+    n, f = h32.shape
+    hb = np.abs(h32.astype(np.float64)).reshape(n, f // 32, 32)
+    amax = hb.max(axis=2)
+    _, E = np.frexp(amax)                       # amax = m 2^E, m in [0.5, 1)
+    s = np.where(amax > 0, np.ldexp(1.0, E - 3), 1.0)  # 2^(floor(log2 amax) - 2)
+    a = hb / s[..., None]
+    tau_a = (MXQ_TAU * amax / s)[..., None]
+    delta = np.zeros_like(hb)
+    for m, g in zip(_MIDS, _GAPS):
+        delta = np.maximum(delta, np.where(np.abs(a - m) <= tau_a, g, 0.0))
+    delta *= s[..., None]
+    p2 = np.exp2(np.round(np.log2(np.where(amax > 0, amax, 1.0))))
+    near = (amax > 0) & (np.abs(amax / p2 - 1.0) <= MXQ_TAU)
+    for r, b in zip(*np.nonzero(near)):
+        blk = h32[r, 32 * b:32 * b + 32].astype(np.float32)
+        i = int(np.argmax(np.abs(blk)))
+        alt = blk.copy()
+        # the largest element just across the power of two (same sign)
+        alt[i] = np.float32(np.copysign(p2[r, b] * (1.0 - 2 * MXQ_TAU) if amax[r, b] >= p2[r, b]
+                                        else p2[r, b], blk[i]))
+        q0 = oracle.mx_quantize(blk)[0]
+        q1 = oracle.mx_quantize(alt)[0]
+        delta[r, b] = np.maximum(delta[r, b], np.abs(q1 - q0))
+    delta = delta.reshape(n, f)
+    return (delta @ np.abs(Wd).T) * np.asarray(wts, np.float64)[:, None]
+
+
+def mxq_reference(Xd, rids, rw, planes_of):
+    """(mode-B oracle output, flip allowance) for a batch."""
+    T, d = Xd.shape
+    bound = np.zeros((T, d))
+
+    def acc(e, ts, js, h32, Wd):
+        bound[ts] += mxq_flip_bound(h32, Wd, rw[ts, js])
+
+    ref = oracle.combine_grouped_mxq(Xd, rids, rw, planes_of, on_expert=acc)
+    return ref, bound
+
+
+def mxq_check(out, ref, bound, name=None):
+    """Gate: |out - ref| <= TOL * max|ref_t| + bound elementwise, per token.
+    Returns (normwise errors, tokens with a non-zero allowance)."""
+    out = np.asarray(out, np.float64)
+    lim = TOL * np.max(np.abs(ref), axis=1, keepdims=True) + bound
+    excess = np.abs(out - ref) - lim
+    bad = np.nonzero(np.any(excess > 0, axis=1))[0]
+    norm, elem = batch_errors(out, ref)
+    if name:
+        report(name + " vs mode-B oracle", norm, elem)
+        print("%s: %d of %d tokens have a rounding-decision allowance (max %.3e of max|ref|)" %
+              (name, int(np.count_nonzero(bound.max(axis=1) > 0)), len(out),
+               float(np.max(bound.max(axis=1) / np.max(np.abs(ref), axis=1)))))
+    assert bad.size == 0, [(int(t), float(norm[t])) for t in bad[:10]]
+    return norm
