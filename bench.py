@@ -20,6 +20,8 @@ One configuration alone, one JSON line each:
   --workload expert       one expert GEMV (gate/up + SwiGLU + down), 1 token
   --workload decode64     batched decode, 64 tokens, grouped by expert
   --workload prefill4096  4096 bf16 tokens, selection bias ~N(0,1)
+  --workload prefill4096_mxq  the same with the activations quantised to
+                          MXFP4 (block-scaled E2M1 x E2M1 products)
   --workload stream       4 layers x 896 experts in pinned host memory behind
                           an 8 GB HBM LRU cache, 256 tokens, RMSNorm +
                           residual, Zipf(1.1) selection bias; the recorded
@@ -70,6 +72,11 @@ EXPERT_GEMV_LAUNCHES = 2
 # scales, token gather, gate/up, h pieces, down + combine.
 GROUPED_GATEUP_KERNEL = "k3_tc_expert<0,1> (tcgen05 kind::f8f6f4)"
 GROUPED_LAUNCHES = 9
+# With MXFP4 activations (K3MOE_OPT_MXQ): router GEMM + top-k, grouping,
+# tile plan, pair slots, token tiles, gate/up, down + combine.
+MXQ_GATEUP_KERNEL = "k3_mxq_expert<0> (tcgen05 kind::mxf4, E2M1 x E2M1, block-scaled)"
+MXQ_LAUNCHES = 8
+FP4_PER_BF16 = 6.0  # nominal dense FP4 : bf16 tensor throughput (13.5 : 2.25 PFLOP/s)
 
 
 def log(*a):
@@ -100,6 +107,14 @@ def rank_first_token(rank, n_per_rank):
 def job_rate(units_per_rank, world, ms_max):
     """Whole-job throughput: all ranks' units over the slowest rank's time."""
     return units_per_rank * world / (ms_max * 1e-3)
+
+
+def measured_bf16_tflops():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            return float(json.load(fh)["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
 
 
 def measured_peaks():
@@ -588,13 +603,16 @@ def run_expert(args, ctx, rank, world):
         "expert_hbm": {"bytes_per_gemv": nbytes, "gbs": round(nbytes / (per * 1e-3) / 1e9, 1)}}
 
 
-def run_batched(args, ctx, rank, world, T, bf16, use_bias):
+def run_batched(args, ctx, rank, world, T, bf16, use_bias, mxq=False):
     """The layer on T tokens per step: the grouped path (router, top-k,
-    grouping by expert, grouped gate/up + SwiGLU, grouped down, combine)."""
+    grouping by expert, grouped gate/up + SwiGLU, grouped down, combine);
+    mxq: with MXFP4-quantised activations on block-scaled MMAs."""
     import torch
     import synth
     from mxfp4_routed_expert_select_gb300 import k3moe as k
     dev = ctx.dev
+    if args.tokens:
+        T = args.tokens  # smaller batches for profiler captures
     steps = cfg_steps(args, 64 if T <= 64 else 20)
     bias = None
     if use_bias:
@@ -603,6 +621,10 @@ def run_batched(args, ctx, rank, world, T, bf16, use_bias):
     n_r = 4 if T >= 1024 else 16
     routers = [ctx.Wr0] + [ctx.Wr0.clone() for _ in range(n_r - 1)]
     layers = [k.Layer(E, K, D, F, r, ctx.views, bias, max_tokens=T) for r in routers]
+    if mxq:
+        for l in layers:
+            l.set_option(k.K3MOE_OPT_MXQ, 1)
+        assert layers[0].mxq(), "the MXFP4-activation path does not apply to this layer"
     if bf16:
         Xs = [torch.from_numpy(synth.tokens_bf16(1, T, D, t0=rank * NB * T + b * T).view(np.int16))
               .to(dev).view(torch.bfloat16) for b in range(NB)]
@@ -644,14 +666,16 @@ def run_batched(args, ctx, rank, world, T, bf16, use_bias):
         oh.copy_(out, non_blocking=True)
 
     e2e = _e2e(step_host, steps, args.warmup, world, ctx.dev_index, xb, T * D * 4, T, "tokens/s")
-    name = "decode%d" % T if T <= 64 else "prefill%d" % T
+    name = ("decode%d" % T if T <= 64 else "prefill%d" % T) + ("_mxq" if mxq else "")
     desc = ("moe_layer_%s: %d experts d=7168 f=1536 resident (%.1f GB), router bf16 [%dx7168], "
-            "top-16, X %s [%dx7168]%s, grouped by expert" %
+            "top-16, X %s [%dx7168]%s, grouped by expert%s" %
             (name, E, E * EXPERT_BYTES / 1e9, E, "bf16" if bf16 else "fp32", T,
-             ", selection bias ~N(0,1)" if use_bias else ""))
-    gu_kernel = GROUPED_GATEUP_KERNEL
+             ", selection bias ~N(0,1)" if use_bias else "",
+             "; activations and h quantised to MXFP4 (OCP rule), E2M1 x E2M1 block-scaled MMAs" if mxq else ""))
+    gu_kernel = MXQ_GATEUP_KERNEL if mxq else GROUPED_GATEUP_KERNEL
     line = {
-        "metric": "MoE-layer tokens/s (%d tokens per step, 896 experts, top-16, MXFP4)" % T,
+        "metric": "MoE-layer tokens/s (%d tokens per step, 896 experts, top-16, MXFP4%s)" %
+                  (T, " weights and activations" if mxq else ""),
         "value": round(job_rate(steps * T, world, statistics.median(ms)), 2), "unit": "tokens/s",
         "steps": steps, "ms_per_step": round(per, 6), "higher_is_better": True,
         "dtype": "mxfp4 weights (e2m1 + e8m0), %s activations, fp32 accumulation" % ("bf16" if bf16 else "fp32"),
@@ -672,7 +696,19 @@ def run_batched(args, ctx, rank, world, T, bf16, use_bias):
         "kernels_ms": {"route_topk": round(statistics.mean(r_ms), 4),
                        "group_gate_up_swiglu": round(statistics.mean(gu_ms), 4),
                        "down_combine": round(statistics.mean(dn_ms), 4)},
-        "e2e": e2e, "gpu_launches": GROUPED_LAUNCHES * steps, "clocks": clocks}
+        "e2e": e2e, "gpu_launches": (MXQ_LAUNCHES if mxq else GROUPED_LAUNCHES) * steps, "clocks": clocks}
+    if mxq:
+        # block-scaled FP4 products: the FP4 peak from the measured bf16 one
+        # and the nominal ratio; at this batch the weights' bytes cap it
+        bf, bsrc = measured_bf16_tflops()
+        fp4 = bf * FP4_PER_BF16
+        ach = flops / (per * 1e-3) / 1e12
+        cap = (flops / step_bytes) * measured_peaks()[0] * 1e9 / 1e12  # TFLOP/s at the HBM roofline
+        line["mxfp4"] = {"tflops": round(ach, 1), "peak_tflops": round(fp4, 1),
+                         "peak_source": "%s bf16 burst x %.0f (nominal FP4:bf16)" % (bsrc, FP4_PER_BF16),
+                         "frac_of_peak": round(ach / fp4, 4), "flop_per_byte": round(flops / step_bytes, 1),
+                         "hbm_bound_cap_tflops": round(cap, 1), "hbm_bound_cap_frac": round(cap / fp4, 4),
+                         "frac_of_cap": round(ach / cap, 4)}
     for l in layers:
         l.close()
     return line
@@ -872,6 +908,7 @@ POOL_WORKLOADS = {
     "expert": lambda a, c, r, w: run_expert(a, c, r, w),
     "decode64": lambda a, c, r, w: run_batched(a, c, r, w, 64, False, False),
     "prefill4096": lambda a, c, r, w: run_batched(a, c, r, w, 4096, True, True),
+    "prefill4096_mxq": lambda a, c, r, w: run_batched(a, c, r, w, 4096, True, True, mxq=True),
 }
 WORKLOADS = dict(POOL_WORKLOADS, stream=None)
 
@@ -901,6 +938,8 @@ def main():
     ap.add_argument("--pin-hot", type=int, default=0,
                     help="stream workload: run 256 untimed history tokens, then pin the N most "
                          "requested experts of the cache's histogram before timing")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="tokens per step of the decode64 / prefill workloads (profiler captures)")
     ap.add_argument("--experts", type=int, default=896,
                     help="experts per layer (smaller pools for profiler captures; 896 is the workload)")
     args = ap.parse_args()

@@ -45,10 +45,13 @@ size_t mxq_max_rows(int npairs, int E);
 size_t mxq_tile_bytes();
 int launch_mx_quantize(const void *x, int xdt, int rows, int cols, uint8_t *codes, uint8_t *scales,
                        cudaStream_t s);
-int launch_mxq(const void *X, int xdt, int T, int k, int E, int d, int f, const void *maps,
-               const int32_t *offsets, const int32_t *perm, const float *wsel, void *tiles, int32_t *n_tiles,
-               int32_t *tbase, int32_t *slot, int max_tiles, uint8_t *Xg, uint8_t *Xsf, uint8_t *Hg, uint8_t *Hsf,
-               float *out, int *err, cudaStream_t s);
+int launch_mxq_gateup(const void *X, int xdt, int T, int k, int E, int d, int f, const void *maps,
+                      const int32_t *offsets, const int32_t *perm, void *tiles, int32_t *n_tiles, int32_t *tbase,
+                      int32_t *slot, int max_tiles, uint8_t *Xg, uint8_t *Xsf, uint8_t *Hg, uint8_t *Hsf, int *err,
+                      cudaStream_t s);
+int launch_mxq_down(int T, int k, int d, int f, const void *maps, const int32_t *perm, const float *wsel,
+                    const void *tiles, const int32_t *n_tiles, const uint8_t *Hg, const uint8_t *Hsf, float *out,
+                    int *err, cudaStream_t s);
 int tc_max_tiles(int npairs, int E);
 size_t tc_xg_bytes(int npairs, int E, int d);
 size_t tc_hg_bytes(int npairs, int E, int f);
@@ -536,10 +539,12 @@ int k3moe_layer_forward(k3moe_layer *L, const void *X, int xdt, int32_t T, float
         int *err = k3::device_error_word();
         K3_TRY(k3::launch_group(L->ids, T * L->k, L->E, k3::grouped_nt(), L->offsets, L->perm,
                                 L->items, L->n_items, st));
+        K3_TRY(k3::launch_mxq_gateup(X, xdt, T, L->k, L->E, L->d, L->f, L->mx_maps, L->offsets, L->perm,
+                                     L->mq_tiles, L->mq_ntiles, L->mq_tbase, L->mq_slot, L->mq_max_tiles,
+                                     L->mq_xg, L->mq_xsf, L->mq_hg, L->mq_hsf, err, st));
         if (L->nev) K3_CUDA(cudaEventRecord(L->ev[2], st));
-        K3_TRY(k3::launch_mxq(X, xdt, T, L->k, L->E, L->d, L->f, L->mx_maps, L->offsets, L->perm, L->w,
-                              L->mq_tiles, L->mq_ntiles, L->mq_tbase, L->mq_slot, L->mq_max_tiles, L->mq_xg,
-                              L->mq_xsf, L->mq_hg, L->mq_hsf, out, err, st));
+        K3_TRY(k3::launch_mxq_down(T, L->k, L->d, L->f, L->mx_maps, L->perm, L->w, L->mq_tiles, L->mq_ntiles,
+                                   L->mq_hg, L->mq_hsf, out, err, st));
     } else if (L->tc && L->tc_ready) {
         int *err = k3::device_error_word();
         K3_TRY(k3::launch_group(L->ids, T * L->k, L->E, k3::grouped_nt(), L->offsets, L->perm,

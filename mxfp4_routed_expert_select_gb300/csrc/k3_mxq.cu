@@ -114,6 +114,35 @@ K3_DEV void mq_transpose8(float (&v)[8], int lane)
 
 }  // namespace
 
+// Code of |v| (bits ab, sign bit sg) in a block whose largest magnitude has
+// bits mb (the rule below); e receives the block's E8M0 byte.
+K3_DEV uint32_t mxq_rule(uint32_t ab, uint32_t sg, uint32_t mb, uint32_t &e)
+{
+    if (mb >= 0x7f800000u) {
+        e = 255u;
+        return 0u;
+    }
+    e = (uint32_t)min(max((int)(mb >> 23) - 2, 0), 254);     // floor(log2 amax) - 2 + 127
+    const float a = __uint_as_float(ab) * __uint_as_float((254u - e) << 23);  // |v| * 2^(127 - e) < 8, exact
+    uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
+    return sg ? (c | 8u) : c;
+}
+// 8 x 8 transpose of 4-bit values within groups of 8 lanes: before, lane r
+// of a group holds A[r][c] in nibble c; after, it holds A[c][r] in nibble c.
+K3_DEV uint32_t nib_transpose8(uint32_t w, int lane)
+{
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1) {
+        const uint32_t M = m == 1 ? 0x0F0F0F0Fu : (m == 2 ? 0x00FF00FFu : 0x0000FFFFu);
+        const int sh = 4 * m;
+        const bool upper = (lane & m) != 0;
+        const uint32_t send = upper ? (w & M) : ((w >> sh) & M);
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
+        w = upper ? ((w & (M << sh)) | recv) : ((w & M) | (recv << sh));
+    }
+    return w;
+}
+
 // The OCP MX conversion of one 32-block held one value per lane: returns this
 // lane's 4-bit code (bit 3 the sign; -0 is code 8) and, in *sbyte, the
 // block's E8M0 byte.  A block holding a non-finite value gets byte 255 and
@@ -125,15 +154,8 @@ K3_DEV uint32_t mxq_code(float v, uint32_t *sbyte)
 {
     const uint32_t ab = __float_as_uint(v) & 0x7fffffffu;
     const uint32_t mb = __reduce_max_sync(0xffffffffu, ab);  // non-negative floats order like their bits
-    if (mb >= 0x7f800000u) {
-        *sbyte = 255u;
-        return 0u;
-    }
-    const int eb = (int)(mb >> 23);                        // biased exponent of amax (0: subnormal or 0)
-    const uint32_t e = (uint32_t)min(max(eb - 2, 0), 254);  // floor(log2 amax) - 2 + 127
-    const float a = __uint_as_float(ab) * __uint_as_float((254u - e) << 23);  // |v| * 2^(127 - e) < 8
-    uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
-    if (__float_as_uint(v) >> 31) c |= 8u;
+    uint32_t e;
+    const uint32_t c = mxq_rule(ab, __float_as_uint(v) >> 31, mb, e);
     *sbyte = e;
     return c;
 }
@@ -570,15 +592,29 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k3_mxq_expert(const MqArgs a)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar(B_ACCE + buf));
                     }
+                    // eight tokens at once: their block maxima, this row's eight
+                    // codes as one word (nibble i = token j0 + i), then a nibble
+                    // transpose leaves word lane / 8 of token j0 + lane % 8's
+                    // 16-byte chunk in each lane
+                    uint32_t ab[8], mb[8], w = 0u, myscale = 0u;
 #pragma unroll
                     for (int i = 0; i < 8; i++) {
-                        const int j = j0 + i;
-                        uint32_t sb;
-                        const uint4 ch = mxq_chunk(mxq_pack(mxq_code(silu(g[i]) * v[i], &sb), lane));
-                        if (j < tl.n && lane == 0) {
-                            *(uint4 *)(hrows + mq_code_off(j, b, tl.np)) = ch;
-                            hsf[mq_sf_off(j, b)] = (uint8_t)sb;
-                        }
+                        const float h = silu(g[i]) * v[i];
+                        ab[i] = __float_as_uint(h);
+                        mb[i] = __reduce_max_sync(0xffffffffu, ab[i] & 0x7fffffffu);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        uint32_t e;
+                        const uint32_t c = mxq_rule(ab[i] & 0x7fffffffu, ab[i] >> 31, mb[i], e);
+                        w |= c << (4 * i);
+                        if (lane == i) myscale = e;
+                    }
+                    w = nib_transpose8(w, lane);
+                    const int j = j0 + (lane & 7);
+                    if (j < tl.n) {
+                        *(uint32_t *)(hrows + mq_code_off(j, b, tl.np) + 4 * (lane >> 3)) = w;
+                        if (lane < 8) hsf[mq_sf_off(j, b)] = (uint8_t)myscale;
                     }
                 }
             } else {
@@ -620,6 +656,224 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k3_mxq_expert(const MqArgs a)
     }
 }
 
+// ------------------------------------------------------- down (resident h)
+
+// Down products with each CTA on a contiguous range of (tile, 128 rows of d)
+// units: a tile's h codes (np x f/2 bytes) and scale atoms are copied into
+// shared memory once per run of its row blocks and stay there while the
+// down weight tiles stream through a ring of stages, so the h rows cross the
+// SM's load path once per run instead of once per row block.
+constexpr int MD_NS = 6;                        // weight stages
+constexpr int MD_STAGE = MQ_M * 128 + MQ_M * 16 + 1024;  // A tile, scale box, A atoms
+constexpr int MD_HMAX = MQ_TN * 768;            // h codes of a tile at most (f <= 1536)
+constexpr int MD_HSF = 12 * 512;                // its scale atoms (f / 128 <= 12)
+constexpr int MD_OFF_H = MD_NS * MD_STAGE;      // 1024-aligned: the stage is
+constexpr int MD_SMEM = 1024 + MD_OFF_H + MD_HMAX + MD_HSF + 1024;
+static_assert(MD_STAGE % 1024 == 0 && MD_SMEM <= 232448, "down smem");
+constexpr int MD_TACC = 0, MD_TSA = 2 * MQ_TN, MD_TSB = MD_TSA + 8 * MD_NS;  // + 2 x 48 B-scale columns
+static_assert(MD_TSB + 2 * 48 <= 512, "down TMEM");
+
+__global__ void __launch_bounds__(MQ_THREADS, 1) k3_mxq_down(const MqArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t sbase = smem_addr(sm);
+    uint64_t *bars = (uint64_t *)(sm + MD_OFF_H + MD_HMAX + MD_HSF);
+    const int B_FULL = 0, B_AFULL = MD_NS, B_EMPTY = 2 * MD_NS, B_ACCF = 3 * MD_NS, B_ACCE = B_ACCF + 2,
+              B_HFULL = B_ACCE + 2, B_HFREE = B_HFULL + 1, B_FIN = B_HFREE + 1, NB = B_FIN + 1;
+    uint32_t *tmem_slot = (uint32_t *)(bars + NB);
+    volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+    auto bar = [&](int i) { return smem_addr(bars + i); };
+    auto stage = [&](int s) { return sbase + (uint32_t)(s * MD_STAGE); };
+    const uint32_t hbuf = sbase + (uint32_t)MD_OFF_H, hsfbuf = hbuf + (uint32_t)MD_HMAX;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nrb = a.d / MQ_M, nks = a.f / 256;
+    const long n_units = (long)*a.n_tiles * nrb, G = gridDim.x;
+    const long ulo = n_units * blockIdx.x / G, uhi = n_units * (blockIdx.x + 1) / G;
+    const uint32_t hrow = (uint32_t)a.f / 2, hsfb = (uint32_t)(a.f / 128) * 512;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < MD_NS; i++) {
+            mbar_init(bar(B_FULL + i), 1);
+            mbar_init(bar(B_AFULL + i), 1);
+            mbar_init(bar(B_EMPTY + i), 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(bar(B_ACCF + i), 1);
+            mbar_init(bar(B_ACCE + i), 4);
+        }
+        mbar_init(bar(B_HFULL), 1);
+        mbar_init(bar(B_HFREE), 1);
+        mbar_init(bar(B_FIN), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == MQ_W_MMA) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(512)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *(volatile uint32_t *)tmem_slot;
+
+    if (warp == MQ_W_PROD) {
+        // ------------------------------------- weight tiles; h once per run
+        uint32_t issued[MD_NS];
+#pragma unroll
+        for (int i = 0; i < MD_NS; i++) issued[i] = 0;
+        uint32_t runs = 0;
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            int cur = -1;
+            for (long u = ulo; u < uhi && ok && !*abort_flag; u++) {
+                const int ti = (int)(u / nrb), rb = (int)(u % nrb);
+                const MqTile tl = a.tiles[ti];
+                if (tl.np < 16 || tl.np > MQ_TN || tl.np % 16 || a.f > 1536) {
+                    set_device_error(a.err, K3MOE_EINVAL);
+                    *abort_flag = 1;
+                    break;
+                }
+                if (ti != cur) {
+                    // the previous run's MMAs are done with the h buffer
+                    if (runs >= 1 && !tc_wait(bar(B_HFREE), (runs - 1) & 1, a.err, abort_flag)) break;
+                    cur = ti;
+                    const uint32_t hb = (uint32_t)tl.np * hrow;
+                    mbar_arrive_expect_tx(bar(B_HFULL), hb + hsfb);
+                    for (uint32_t o = 0; o < hb; o += 32768)
+                        bulk_g2s(hbuf + o, a.B + (size_t)tl.row0 * hrow + o, min(32768u, hb - o), bar(B_HFULL));
+                    bulk_g2s(hsfbuf, a.Bsf + (size_t)ti * hsfb, hsfb, bar(B_HFULL));
+                    runs++;
+                }
+                const CUtensorMap *mp = a.maps + 6 * (size_t)tl.expert;
+                for (int ks = 0; ks < nks; ks++, it++) {
+                    const int s = it % MD_NS;
+                    if (it >= (uint32_t)MD_NS &&
+                        !tc_wait(bar(B_EMPTY + s), ((it / MD_NS) - 1) & 1, a.err, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(B_FULL + s), MQ_M * 128 + MQ_M * 16);
+                    issued[s]++;
+                    tma_load_2d(stage(s), mp + 2, ks * 128, rb * MQ_M, bar(B_FULL + s));
+                    tma_load_2d(stage(s) + MQ_M * 128, mp + 5, 16 * (ks >> 1), rb * MQ_M, bar(B_FULL + s));
+                }
+            }
+            for (int s = 0; s < MD_NS; s++)
+                if (issued[s]) mbar_wait(bar(B_FULL + s), (issued[s] - 1) & 1, a.err);
+            if (runs) mbar_wait(bar(B_HFULL), (runs - 1) & 1, a.err);
+        }
+        __syncwarp();
+    } else if (warp == MQ_W_PERM) {
+        // ------------------------------------ scale boxes -> tcgen05.cp atoms
+        uint32_t it = 0;
+        for (long u = ulo; u < uhi && !*abort_flag; u++) {
+            for (int ks = 0; ks < nks; ks++, it++) {
+                const int s = it % MD_NS;
+                if (!__all_sync(0xffffffffu, tc_wait(bar(B_FULL + s), (it / MD_NS) & 1, a.err, abort_flag))) break;
+#pragma unroll
+                for (int at = 0; at < 2; at++)
+#pragma unroll
+                    for (int r1 = 0; r1 < 4; r1++) {
+                        uint32_t v = mq_lds32(stage(s) + MQ_M * 128 + (uint32_t)((lane + 32 * r1) * 16 + 8 * (ks & 1) + 4 * at));
+                        v &= ~__vcmpeq4(v, 0xffffffffu);  // 255 (a dropped weight group) -> 2^-127
+                        mq_sts32(stage(s) + MQ_M * 144 + (uint32_t)(at * 512 + 16 * lane + 4 * r1), v);
+                    }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_AFULL + s));
+            }
+            if (*abort_flag) break;
+        }
+    } else if (warp == MQ_W_MMA) {
+        // -------------------------------------------------------------- MMA
+        uint32_t it = 0, ut = 0, runs = 0;
+        int cur = -1;
+        bool ok = true;
+        for (long u = ulo; u < uhi && ok && !*abort_flag; u++, ut++) {
+            const int ti = (int)(u / nrb);
+            const MqTile tl = a.tiles[ti];
+            if (ti != cur) {
+                if (runs >= 1) mma_commit(bar(B_HFREE));  // the previous run's MMAs release the h buffer
+                cur = ti;
+                if (!__all_sync(0xffffffffu, tc_wait(bar(B_HFULL), runs & 1, a.err, abort_flag))) break;
+                tc_fence_after();
+                const uint32_t tsb = tmem + (uint32_t)(MD_TSB + 48 * (runs & 1));
+                for (int at = 0; at < a.f / 128; at++) mq_cp_atom(tsb + 4 * at, hsfbuf + (uint32_t)(512 * at));
+                runs++;
+            }
+            const int buf = (int)(ut & 1);
+            if (ut >= 2 && !__all_sync(0xffffffffu, tc_wait(bar(B_ACCE + buf), ((ut / 2) - 1) & 1, a.err, abort_flag)))
+                break;
+            tc_fence_after();
+            const uint32_t tacc = tmem + (uint32_t)(MD_TACC + buf * MQ_TN);
+            const uint32_t tsb = tmem + (uint32_t)(MD_TSB + 48 * ((runs - 1) & 1));
+            for (int ks = 0; ks < nks; ks++, it++) {
+                const int s = it % MD_NS;
+                if (!__all_sync(0xffffffffu, tc_wait(bar(B_AFULL + s), (it / MD_NS) & 1, a.err, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tsa = tmem + (uint32_t)(MD_TSA + 8 * s);
+                mq_cp_atom(tsa, stage(s) + MQ_M * 144);
+                mq_cp_atom(tsa + 4, stage(s) + MQ_M * 144 + 512);
+                const uint32_t blo = sw128_lo(hbuf + (uint32_t)(ks * tl.np * 128));
+#pragma unroll
+                for (int q4 = 0; q4 < 4; q4++)
+                    mq_mma(tacc, sw128_lo(stage(s)) + 2u * q4, blo + 2u * q4, mq_idesc(tl.np, 2u * (q4 & 1), 2u * (q4 & 1)),
+                           tsa + 4 * (q4 >> 1), tsb + 8 * ks + 4 * (q4 >> 1), (ks == 0 && q4 == 0) ? 0u : 1u);
+                mma_commit(bar(B_EMPTY + s));
+            }
+            if (!ok) break;
+            mma_commit(bar(B_ACCF + buf));
+        }
+        mma_commit(bar(B_FIN));
+        mbar_wait(bar(B_FIN), 0, a.err);
+        __syncwarp();
+    } else if (warp >= MQ_W_EPI) {
+        // --------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        uint32_t ut = 0;
+        for (long u = ulo; u < uhi && !*abort_flag; u++, ut++) {
+            const int ti = (int)(u / nrb), rb = (int)(u % nrb);
+            const MqTile tl = a.tiles[ti];
+            const int buf = (int)(ut & 1);
+            if (!__all_sync(0xffffffffu, tc_wait(bar(B_ACCF + buf), (ut / 2) & 1, a.err, abort_flag))) break;
+            tc_fence_after();
+            const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(MD_TACC + buf * MQ_TN);
+            for (int j0 = 0; j0 < tl.n; j0 += 8) {
+                float y[8];
+                tmem_ld8(tacc + (uint32_t)j0, y);
+                tmem_wait_ld();
+                mq_transpose8(y, lane);
+                const int j = j0 + (lane & 7);
+                if (j < tl.n) {
+                    const int pair = a.perm[tl.pair_begin + j];
+                    const float w = a.wsel[pair];
+                    float *o = a.out + (size_t)(pair / a.k) * a.d + rb * MQ_M + q * 32 + (lane & ~7);
+                    mq_red_v4(o, w * y[0], w * y[1], w * y[2], w * y[3]);
+                    mq_red_v4(o + 4, w * y[4], w * y[5], w * y[6], w * y[7]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_ACCE + buf));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == MQ_W_MMA) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
+    }
+}
+
 // --------------------------------------------------------------- launchers
 
 int num_sms();
@@ -656,14 +910,13 @@ static int launch_mxq_phase(const MqArgs &a, cudaStream_t s)
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
 }
 
-// The expert products of a grouped batch with MXFP4 activations: tile plan,
-// token tiles, gate/up + SwiGLU (h quantised), down + combine into out
-// (overwritten).  offsets / perm from the grouping; maps: the layer's six
-// tensor maps per expert.
-int launch_mxq(const void *X, int xdt, int T, int k, int E, int d, int f, const void *maps,
-               const int32_t *offsets, const int32_t *perm, const float *wsel, void *tiles, int32_t *n_tiles,
-               int32_t *tbase, int32_t *slot, int max_tiles, uint8_t *Xg, uint8_t *Xsf, uint8_t *Hg, uint8_t *Hsf,
-               float *out, int *err, cudaStream_t s)
+// The gate/up half of a grouped batch with MXFP4 activations: tile plan,
+// token tiles, gate/up + SwiGLU with h quantised into Hg / Hsf.  offsets /
+// perm from the grouping; maps: the layer's six tensor maps per expert.
+int launch_mxq_gateup(const void *X, int xdt, int T, int k, int E, int d, int f, const void *maps,
+                      const int32_t *offsets, const int32_t *perm, void *tiles, int32_t *n_tiles, int32_t *tbase,
+                      int32_t *slot, int max_tiles, uint8_t *Xg, uint8_t *Xsf, uint8_t *Hg, uint8_t *Hsf, int *err,
+                      cudaStream_t s)
 {
     const int npairs = T * k;
     k3_mxq_plan<<<1, 1024, 0, s>>>(offsets, E, max_tiles, (MqTile *)tiles, n_tiles, tbase, err);
@@ -682,24 +935,41 @@ int launch_mxq(const void *X, int xdt, int T, int k, int E, int d, int f, const 
     a.n_tiles = n_tiles;
     a.maps = (const CUtensorMap *)maps;
     a.perm = perm;
+    a.k = k;
+    a.d = d;
+    a.f = f;
+    a.err = err;
+    a.B = Xg;
+    a.Bsf = Xsf;
+    a.H = Hg;
+    a.Hsf = Hsf;
+    return launch_mxq_phase<0>(a, s);
+}
+
+// The down half: down products of the same tiles, w * y added into out
+// (zeroed first).
+int launch_mxq_down(int T, int k, int d, int f, const void *maps, const int32_t *perm, const float *wsel,
+                    const void *tiles, const int32_t *n_tiles, const uint8_t *Hg, const uint8_t *Hsf, float *out,
+                    int *err, cudaStream_t s)
+{
+    if (cudaMemsetAsync(out, 0, sizeof(float) * (size_t)T * d, s) != cudaSuccess) return K3MOE_ECUDA;
+    MqArgs a = {};
+    a.tiles = (const MqTile *)tiles;
+    a.n_tiles = n_tiles;
+    a.maps = (const CUtensorMap *)maps;
+    a.perm = perm;
     a.wsel = wsel;
     a.k = k;
     a.d = d;
     a.f = f;
     a.err = err;
-    MqArgs a0 = a;
-    a0.B = Xg;
-    a0.Bsf = Xsf;
-    a0.H = Hg;
-    a0.Hsf = Hsf;
-    const int r0 = launch_mxq_phase<0>(a0, s);
-    if (r0 != K3MOE_OK) return r0;
-    if (cudaMemsetAsync(out, 0, sizeof(float) * (size_t)T * d, s) != cudaSuccess) return K3MOE_ECUDA;
-    MqArgs a1 = a;
-    a1.B = Hg;
-    a1.Bsf = Hsf;
-    a1.out = out;
-    return launch_mxq_phase<1>(a1, s);
+    a.B = Hg;
+    a.Bsf = Hsf;
+    a.out = out;
+    if (f > 1536) return launch_mxq_phase<1>(a, s);
+    if (ensure_smem((const void *)k3_mxq_down, MD_SMEM) != K3MOE_OK) return K3MOE_ECUDA;
+    k3_mxq_down<<<num_sms(), MQ_THREADS, MD_SMEM, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
 }
 
 }  // namespace k3
