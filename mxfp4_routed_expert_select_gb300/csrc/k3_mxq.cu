@@ -363,7 +363,9 @@ struct MqArgs {
 template <int PH>
 struct MqCfg {
     static constexpr int NA = PH == 0 ? 2 : 1;             // weight matrices per unit
-    static constexpr int NS = PH == 0 ? 3 : 4;             // pipeline stages
+    static constexpr int NS = 4;                           // pipeline stages
+    static constexpr int NEPI = PH == 0 ? 8 : 4;           // epilogue warps (two per TMEM lane quadrant at PH 0)
+    static constexpr int THREADS = (MQ_W_EPI + NEPI) * 32;
     static constexpr int A_BYTES = MQ_M * 128;             // one weight tile (256 of K)
     static constexpr int SC_BYTES = MQ_M * 16;             // scale box (16 k-blocks)
     static constexpr int AT_BYTES = 2 * 512;               // two A atoms per matrix per k-step
@@ -387,7 +389,7 @@ struct MqCfg {
 };
 
 template <int PH>
-__global__ void __launch_bounds__(MQ_THREADS, 1) k3_mxq_expert(const MqArgs a)
+__global__ void __launch_bounds__(MqCfg<PH>::THREADS, 1) k3_mxq_expert(const MqArgs a)
 {
     using C = MqCfg<PH>;
     constexpr int NA = C::NA, NS = C::NS;
@@ -419,7 +421,7 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k3_mxq_expert(const MqArgs a)
         }
         for (int i = 0; i < 2; i++) {
             mbar_init(bar(B_ACCF + i), 1);
-            mbar_init(bar(B_ACCE + i), 4);
+            mbar_init(bar(B_ACCE + i), C::NEPI);
         }
         mbar_init(bar(B_FIN), 1);
         *abort_flag = 0;
@@ -564,6 +566,7 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k3_mxq_expert(const MqArgs a)
     } else if (warp >= MQ_W_EPI) {
         // --------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quadrant: weight rows 32 q .. 32 q + 31 of the unit
+        const int half = (warp - MQ_W_EPI) >> 2;  // PH 0: the two warps of a quadrant take alternate chunks
         uint32_t ut = 0;
         for (int u = cid; u < n_units && !*abort_flag; u += G, ut++) {
             const int ti = u / nrb, rb = u % nrb;
@@ -581,16 +584,19 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k3_mxq_expert(const MqArgs a)
                 uint8_t *hrows = a.H + (size_t)tl.row0 * (a.f / 2);
                 uint8_t *hsf = a.Hsf + (size_t)ti * (size_t)(a.f / 128) * 512;
                 const int b = 4 * rb + q;  // 32-block of f
-                for (int j0 = 0; j0 < tl.n; j0 += 8) {
+                bool released = false;
+                for (int j0 = 8 * half; j0 < tl.n; j0 += 16) {
                     float g[8], v[8];
                     tmem_ld8(tacc + (uint32_t)j0, g);
                     tmem_ld8(tacc + (uint32_t)(MQ_TN + j0), v);
                     tmem_wait_ld();
-                    if (j0 + 8 >= tl.n) {
-                        // the accumulator is read: the next unit's MMAs may start
+                    if (j0 + 16 >= tl.n) {
+                        // this warp's columns are read: once every epilogue warp
+                        // has done so, the next unit's MMAs may start
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar(B_ACCE + buf));
+                        released = true;
                     }
                     // eight tokens at once: their block maxima, this row's eight
                     // codes as one word (nibble i = token j0 + i), then a nibble
@@ -617,6 +623,11 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k3_mxq_expert(const MqArgs a)
                         if (lane < 8) hsf[mq_sf_off(j, b)] = (uint8_t)myscale;
                     }
                 }
+                if (!released) {  // no chunk of this unit fell to this warp
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_ACCE + buf));
+                }
             } else {
                 // lane l of group g (rows 8 g .. 8 g + 7 of this warp's 32) takes
                 // token j0 + (l mod 8) of the eight and adds its eight rows with
@@ -639,11 +650,6 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k3_mxq_expert(const MqArgs a)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_ACCE + buf));
             }
-            if (PH == 0 && tl.n <= 0) {  // no column was read: free the accumulator
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_ACCE + buf));
-            }
         }
     }
 
@@ -658,12 +664,15 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k3_mxq_expert(const MqArgs a)
 
 // ------------------------------------------------------- down (resident h)
 
-// Down products with each CTA on a contiguous range of (tile, 128 rows of d)
-// units: a tile's h codes (np x f/2 bytes) and scale atoms are copied into
-// shared memory once per run of its row blocks and stay there while the
-// down weight tiles stream through a ring of stages, so the h rows cross the
-// SM's load path once per run instead of once per row block.
+// Down products, units (tile, 128 rows of d) taken group by group (8 row
+// blocks of d per group, every group split evenly over the CTAs, tile-major
+// within it): the weighted reductions of all CTAs then land in the same
+// 8 x 128 columns of out at any time, which stay in L2.  A tile's h codes
+// (np x f/2 bytes) and scale atoms are copied into shared memory once per
+// run of its row blocks and stay there while the down weight tiles stream
+// through a ring of stages.
 constexpr int MD_NS = 6;                        // weight stages
+constexpr int MD_RG = 8;                        // row blocks of d per group (locality of the reductions)
 constexpr int MD_STAGE = MQ_M * 128 + MQ_M * 16 + 1024;  // A tile, scale box, A atoms
 constexpr int MD_HMAX = MQ_TN * 768;            // h codes of a tile at most (f <= 1536)
 constexpr int MD_HSF = 12 * 512;                // its scale atoms (f / 128 <= 12)
@@ -689,8 +698,49 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k3_mxq_down(const MqArgs a)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nrb = a.d / MQ_M, nks = a.f / 256;
-    const long n_units = (long)*a.n_tiles * nrb, G = gridDim.x;
-    const long ulo = n_units * blockIdx.x / G, uhi = n_units * (blockIdx.x + 1) / G;
+    const int n_tiles = *a.n_tiles;
+    const int ngrp = (nrb + MD_RG - 1) / MD_RG;
+    const long G = gridDim.x;
+    // This CTA's units, group after group: in group g (row blocks MD_RG g ..
+    // MD_RG g + rg - 1) the n_tiles x rg units (tile-major) are split evenly
+    // over the CTAs, so that at any time the CTAs add into the same rg x 128
+    // columns of out (a few MB, kept in L2).  seq(i) gives the i-th unit of
+    // this CTA as (tile, row block).
+    auto grp_lo = [&](int g) {
+        const long ug = (long)n_tiles * min(MD_RG, nrb - MD_RG * g);
+        return ug * blockIdx.x / G;
+    };
+    auto grp_hi = [&](int g) {
+        const long ug = (long)n_tiles * min(MD_RG, nrb - MD_RG * g);
+        return ug * (blockIdx.x + 1) / G;
+    };
+    long my_units = 0;
+    for (int g = 0; g < ngrp; g++) my_units += grp_hi(g) - grp_lo(g);
+    const long ulo = 0, uhi = my_units;
+    // cursor over the sequence (each role keeps its own)
+    struct Cursor {
+        int g;
+        long v, hi;
+    };
+    auto cur_init = [&]() {
+        Cursor c{0, grp_lo(0), grp_hi(0)};
+        while (c.v >= c.hi && c.g + 1 < ngrp) {
+            c.g++;
+            c.v = grp_lo(c.g);
+            c.hi = grp_hi(c.g);
+        }
+        return c;
+    };
+    auto cur_next = [&](Cursor &c) {
+        c.v++;
+        while (c.v >= c.hi && c.g + 1 < ngrp) {
+            c.g++;
+            c.v = grp_lo(c.g);
+            c.hi = grp_hi(c.g);
+        }
+    };
+    auto cur_tile = [&](const Cursor &c) { return (int)(c.v / min(MD_RG, nrb - MD_RG * c.g)); };
+    auto cur_rb = [&](const Cursor &c) { return MD_RG * c.g + (int)(c.v % min(MD_RG, nrb - MD_RG * c.g)); };
     const uint32_t hrow = (uint32_t)a.f / 2, hsfb = (uint32_t)(a.f / 128) * 512;
 
     if (threadIdx.x == 0) {
@@ -730,8 +780,9 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k3_mxq_down(const MqArgs a)
             uint32_t it = 0;
             bool ok = true;
             int cur = -1;
-            for (long u = ulo; u < uhi && ok && !*abort_flag; u++) {
-                const int ti = (int)(u / nrb), rb = (int)(u % nrb);
+            Cursor cu = cur_init();
+            for (long u = ulo; u < uhi && ok && !*abort_flag; u++, cur_next(cu)) {
+                const int ti = cur_tile(cu), rb = cur_rb(cu);
                 const MqTile tl = a.tiles[ti];
                 if (tl.np < 16 || tl.np > MQ_TN || tl.np % 16 || a.f > 1536) {
                     set_device_error(a.err, K3MOE_EINVAL);
@@ -794,8 +845,9 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k3_mxq_down(const MqArgs a)
         uint32_t it = 0, ut = 0, runs = 0;
         int cur = -1;
         bool ok = true;
-        for (long u = ulo; u < uhi && ok && !*abort_flag; u++, ut++) {
-            const int ti = (int)(u / nrb);
+        Cursor cu = cur_init();
+        for (long u = ulo; u < uhi && ok && !*abort_flag; u++, ut++, cur_next(cu)) {
+            const int ti = cur_tile(cu);
             const MqTile tl = a.tiles[ti];
             if (ti != cur) {
                 if (runs >= 1) mma_commit(bar(B_HFREE));  // the previous run's MMAs release the h buffer
@@ -839,13 +891,17 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k3_mxq_down(const MqArgs a)
         // --------------------------------------------------------- epilogue
         const int q = warp & 3;
         uint32_t ut = 0;
-        for (long u = ulo; u < uhi && !*abort_flag; u++, ut++) {
-            const int ti = (int)(u / nrb), rb = (int)(u % nrb);
+        Cursor cu = cur_init();
+        for (long u = ulo; u < uhi && !*abort_flag; u++, ut++, cur_next(cu)) {
+            const int ti = cur_tile(cu), rb = cur_rb(cu);
             const MqTile tl = a.tiles[ti];
             const int buf = (int)(ut & 1);
             if (!__all_sync(0xffffffffu, tc_wait(bar(B_ACCF + buf), (ut / 2) & 1, a.err, abort_flag))) break;
             tc_fence_after();
             const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(MD_TACC + buf * MQ_TN);
+            // lane l of group g (rows 8 g .. 8 g + 7 of this warp's 32) takes
+            // token j0 + (l mod 8) of the eight and adds its eight rows with
+            // two vector reductions
             for (int j0 = 0; j0 < tl.n; j0 += 8) {
                 float y[8];
                 tmem_ld8(tacc + (uint32_t)j0, y);
@@ -906,7 +962,7 @@ static int launch_mxq_phase(const MqArgs &a, cudaStream_t s)
 {
     using C = MqCfg<PH>;
     if (ensure_smem((const void *)k3_mxq_expert<PH>, C::SMEM) != K3MOE_OK) return K3MOE_ECUDA;
-    k3_mxq_expert<PH><<<num_sms(), MQ_THREADS, C::SMEM, s>>>(a);
+    k3_mxq_expert<PH><<<num_sms(), C::THREADS, C::SMEM, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
 }
 
@@ -952,7 +1008,6 @@ int launch_mxq_down(int T, int k, int d, int f, const void *maps, const int32_t 
                     const void *tiles, const int32_t *n_tiles, const uint8_t *Hg, const uint8_t *Hsf, float *out,
                     int *err, cudaStream_t s)
 {
-    if (cudaMemsetAsync(out, 0, sizeof(float) * (size_t)T * d, s) != cudaSuccess) return K3MOE_ECUDA;
     MqArgs a = {};
     a.tiles = (const MqTile *)tiles;
     a.n_tiles = n_tiles;
@@ -966,6 +1021,7 @@ int launch_mxq_down(int T, int k, int d, int f, const void *maps, const int32_t 
     a.B = Hg;
     a.Bsf = Hsf;
     a.out = out;
+    if (cudaMemsetAsync(out, 0, sizeof(float) * (size_t)T * d, s) != cudaSuccess) return K3MOE_ECUDA;
     if (f > 1536) return launch_mxq_phase<1>(a, s);
     if (ensure_smem((const void *)k3_mxq_down, MD_SMEM) != K3MOE_OK) return K3MOE_ECUDA;
     k3_mxq_down<<<num_sms(), MQ_THREADS, MD_SMEM, s>>>(a);
