@@ -265,7 +265,7 @@ def spread(ms, steps):
 
 
 def timed_region(step, steps, warmup, dev_index, world, use_graph=True, n_inputs=1, chunk_max=32,
-                 min_repeats=MIN_REPEATS, seconds=REGION_SECONDS):
+                 min_repeats=None, seconds=None):
     """Warm-up, then the timed region -- exactly `steps` steps between two
     events on the current stream, a barrier (N > 1) and a device
     synchronisation before it and a synchronisation after it -- repeated at
@@ -273,6 +273,8 @@ def timed_region(step, steps, warmup, dev_index, world, use_graph=True, n_inputs
     clocks sampled meanwhile.  step(i) enqueues step i (its input i mod
     n_inputs).  Returns (ms of each repeat, max over ranks; clocks; plan)."""
     import torch
+    min_repeats = MIN_REPEATS if min_repeats is None else min_repeats
+    seconds = REGION_SECONDS if seconds is None else seconds
     s = torch.cuda.current_stream()
     dev = torch.device("cuda", dev_index)
     for i in range(warmup):
@@ -913,6 +915,12 @@ POOL_WORKLOADS = {
 WORKLOADS = dict(POOL_WORKLOADS, stream=None)
 
 
+def _set_timing(min_repeats, seconds):
+    global MIN_REPEATS, REGION_SECONDS
+    MIN_REPEATS = max(1, int(min_repeats))
+    REGION_SECONDS = max(0.0, float(seconds))
+
+
 def as_line(sub, args, world):
     """A secondary configuration's object as a JSON line of its own."""
     line = {"metric": sub["metric"], "value": sub["value"], "unit": sub["unit"], "n_gpus": world,
@@ -938,12 +946,17 @@ def main():
     ap.add_argument("--pin-hot", type=int, default=0,
                     help="stream workload: run 256 untimed history tokens, then pin the N most "
                          "requested experts of the cache's histogram before timing")
+    ap.add_argument("--min-repeats", type=int, default=MIN_REPEATS,
+                    help="timed regions per measurement at least (profiler captures: 1)")
+    ap.add_argument("--region-seconds", type=float, default=REGION_SECONDS,
+                    help="about how long the repeats of one measurement last (profiler captures: 0)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="tokens per step of the decode64 / prefill workloads (profiler captures)")
     ap.add_argument("--experts", type=int, default=896,
                     help="experts per layer (smaller pools for profiler captures; 896 is the workload)")
     args = ap.parse_args()
     global E, ROUTER_BYTES, LAYER_BYTES
+    _set_timing(args.min_repeats, args.region_seconds)
     E = args.experts
     ROUTER_BYTES = E * D * 2
     LAYER_BYTES = K * EXPERT_BYTES + ROUTER_BYTES

@@ -24,6 +24,14 @@ int *device_error_word();
 int num_sms();
 int ensure_smem(const void *fn, size_t bytes);
 
+// Programmatic dependent launch: a kernel launched as a dependent of the
+// previous one on its stream may start while that one still runs; before it
+// reads anything that kernel writes (or writes anything it reads) it waits
+// here until that kernel has completed and its memory is visible.  Both are
+// no-ops for a kernel launched without the attribute.
+K3_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+K3_DEV void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Device error word (bounded waits that ran out write K3MOE_ETIMEOUT here):
 // one int per device, a file-scope device variable (k3::device_error_word()).
 K3_DEV void set_device_error(int *err, int code)

@@ -17,6 +17,8 @@
 //     transpose reduction, then across warps in shared memory;
 //   - the grid is the SM count times the resident CTAs per SM, with an equal
 //     row range per CTA, so every SM streams the same number of bytes.
+#include <atomic>
+
 #include "k3_device.cuh"
 
 namespace k3 {
@@ -180,6 +182,7 @@ __global__ void __launch_bounds__(512, 1) k3_rows_pipe(const float *__restrict__
     const int nst = st1 - st0;
     const long total = (long)k * rows;
 
+    griddep_launch_dependents();
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; i++) {
             mbar_init(full0 + 8 * i, 1);
@@ -191,6 +194,9 @@ __global__ void __launch_bounds__(512, 1) k3_rows_pipe(const float *__restrict__
     __syncthreads();
 
     if (warp == ncw) {  // ------------------------------------------ producer
+        // weights of inline experts are requested before the previous
+        // kernel on the stream has finished; routed ids are its output
+        if (src.ids) griddep_wait();
         if (lane == 0) {
             int issued = 0;
             bool ok = true;
@@ -222,6 +228,7 @@ __global__ void __launch_bounds__(512, 1) k3_rows_pipe(const float *__restrict__
     }
 
     // -------------------------------------------------------------- compute
+    griddep_wait();  // x and out belong to the kernels around this one
     const int c = warp % ncol, rs = warp / ncol;
     const int g = c * 32 + lane;
     const bool active = g < G;
@@ -307,27 +314,20 @@ __global__ void __launch_bounds__(512) k3_down_t1(const float *__restrict__ h, E
     const int HG = f >> 4;
     const int i0 = blockIdx.x * rows_per_cta;
     const int i1 = min(i0 + rows_per_cta, d);
+    griddep_launch_dependents();
+    // routed ids and the combine weights are the previous kernels' output
+    if (src.ids) griddep_wait();
 
     if (s < nsub) {
         const DevExpert e = fetch_expert(src, j);
-        const float wj = w ? w[j] : 1.0f;
+        float wj = 1.0f;  // the combine weight, read after the wait below
         float2 hr[HPL][8];
         bool act[HPL];
 #pragma unroll
         for (int m = 0; m < HPL; m++) {
-            const int hg = lane + 32 * m;
-            act[m] = hg < HG;
+            act[m] = lane + 32 * m < HG;
 #pragma unroll
             for (int i = 0; i < 8; i++) hr[m][i] = make_float2(0.f, 0.f);
-            if (act[m]) {
-                const float4 *hp = reinterpret_cast<const float4 *>(h + (size_t)j * f + 16 * hg);
-#pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    float4 t = hp[i];
-                    hr[m][2 * i] = make_float2(t.x, t.y);
-                    hr[m][2 * i + 1] = make_float2(t.z, t.w);
-                }
-            }
         }
         const size_t rowB = (size_t)(f >> 1), rowS = (size_t)(f >> 5);
         uint2 qv[2][U][HPL];
@@ -368,7 +368,23 @@ __global__ void __launch_bounds__(512) k3_down_t1(const float *__restrict__ h, E
             }
         };
         const int step = U * nsub;
+        // the first weight rows are requested before h, the previous
+        // kernel's output, is read
         issue(0, i0 + s);
+        griddep_wait();
+        if (w) wj = w[j];
+#pragma unroll
+        for (int m = 0; m < HPL; m++) {
+            if (act[m]) {
+                const float4 *hp = reinterpret_cast<const float4 *>(h + (size_t)j * f + 16 * (lane + 32 * m));
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    float4 t = hp[i];
+                    hr[m][2 * i] = make_float2(t.x, t.y);
+                    hr[m][2 * i + 1] = make_float2(t.z, t.w);
+                }
+            }
+        }
         for (int c = i0 + s; c < i1; c += 2 * step) {
             if (c + step < i1) issue(1, c + step);
             consume(0, c);
@@ -376,6 +392,7 @@ __global__ void __launch_bounds__(512) k3_down_t1(const float *__restrict__ h, E
             if (c + step < i1) consume(1, c + step);
         }
     }
+    griddep_wait();  // out belongs to the kernels around this one
     __syncthreads();
     for (int t = threadIdx.x; t < i1 - i0; t += blockDim.x) {
         float a = 0.f;
@@ -395,6 +412,35 @@ static int blocks_per_sm(K kernel, int threads, size_t smem)
         b < 1)
         b = 1;
     return b;
+}
+
+// Launches kernel<<<grid, block, smem, s>>>(args...) as a programmatic
+// dependent of the previous kernel on s where the driver takes it (the
+// kernel then overlaps its prologue, and its weight loads, with that
+// kernel's tail), else as a plain launch.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args)
+{
+    static std::atomic<int> refused{0};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = refused.load(std::memory_order_relaxed) ? 0 : 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    if (e != cudaSuccess && cfg.numAttrs == 1) {
+        cudaGetLastError();
+        refused.store(1, std::memory_order_relaxed);
+        cfg.numAttrs = 0;
+        e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    }
+    return e;
 }
 
 constexpr int kUrows = 2;  // rows per pipeline stage in the gate/up kernel
@@ -431,8 +477,12 @@ static int launch_rows_pipe(const float *x, const ExpertSrc &src, int k, int in,
     const int nstage = (int)((total + kPipeR - 1) / kPipeR);
     int grid = num_sms();
     if (grid > nstage) grid = nstage;
-    kern<<<grid, threads, smem, s>>>(x, src, k, in, rows, out, nstage, S, err);
-    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
+    if (launch_pdl(kern, dim3(grid), dim3(threads), smem, s, x, src, k, in, rows, out, nstage, S, err) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return K3MOE_ECUDA;
+    }
+    return K3MOE_OK;
 }
 
 // rows kernel: MODE 0 (one matrix) or 1 (gate/up SwiGLU over k experts).
@@ -493,8 +543,12 @@ static int launch_down_hpl(const float *h, const ExpertSrc &src, const float *w,
     const size_t smem = (size_t)k * rpc * sizeof(float);
     if (ensure_smem((const void *)k3_down_t1<HPL, kUdown>, smem) != K3MOE_OK) return K3MOE_ECUDA;
     const int grid = (d + rpc - 1) / rpc;
-    k3_down_t1<HPL, kUdown><<<grid, threads, smem, s>>>(h, src, w, k, d, f, out, rpc, acc ? 1 : 0);
-    return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_ECUDA;
+    if (launch_pdl(k3_down_t1<HPL, kUdown>, dim3(grid), dim3(threads), smem, s, h, src, w, k, d, f, out, rpc,
+                   acc ? 1 : 0) != cudaSuccess) {
+        cudaGetLastError();
+        return K3MOE_ECUDA;
+    }
+    return K3MOE_OK;
 }
 
 int launch_down_t1(const float *h, const ExpertSrc &src, const float *w, int k, int d, int f,
