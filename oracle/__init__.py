@@ -81,6 +81,8 @@ def lib():
         L.orc_combine.argtypes = [p, p, i, i, p, p, i, p, i]
         L.orc_layer_forward.argtypes = [p, p, p, p, p, i, i, i, i, p, p, p, i]
         L.orc_rmsnorm.argtypes = [p, p, i, d]
+        L.orc_shared_expert.argtypes = [p, p, p, p, p, i, i]
+        L.orc_shared_forward.argtypes = [p, p, i, i, i, i, p, p, p]
         L.orc_cache_lru.restype = ctypes.c_longlong
         L.orc_cache_lru.argtypes = [p, p, p, i, i, p, i]
         L.orc_cache_belady.restype = ctypes.c_longlong
@@ -356,6 +358,38 @@ def layer_forward(x, Wr_bits, k, experts, bias=None, h_bf16=False):
     ids, w, m = topk(logits, k, bias)
     out = combine(x, ids, w, experts, E, h_bf16)
     return out, ids, w, m
+
+
+def shared_expert(ex, x):
+    """One bf16 shared expert: ex = dict(gate [f, d], up [f, d], down [d, f])
+    as bf16 bit patterns (uint16); x [d].  Returns y [d] in fp64."""
+    g = _c(ex["gate"], np.uint16)
+    u = _c(ex["up"], np.uint16)
+    dn = _c(ex["down"], np.uint16)
+    f, d = g.shape
+    assert u.shape == (f, d) and dn.shape == (d, f)
+    x = _c(x, np.float64)
+    assert x.shape == (d,)
+    y = np.empty(d, np.float64)
+    lib().orc_shared_expert(_p(y), _p(g), _p(u), _p(dn), _p(x), d, f)
+    return y
+
+
+def shared_forward(x, experts):
+    """out[t] = sum_s shared_expert(experts[s], x[t]); x [T, d] fp64."""
+    x = _c(np.atleast_2d(x), np.float64)
+    T, d = x.shape
+    arrs = [(_c(e["gate"], np.uint16), _c(e["up"], np.uint16), _c(e["down"], np.uint16)) for e in experts]
+    f = arrs[0][0].shape[0]
+    n = len(arrs)
+    P = ctypes.c_void_p * n
+    gates = P(*[a[0].ctypes.data for a in arrs])
+    ups = P(*[a[1].ctypes.data for a in arrs])
+    downs = P(*[a[2].ctypes.data for a in arrs])
+    out = np.empty((T, d), np.float64)
+    lib().orc_shared_forward(_p(out), _p(x), T, d, f, n, ctypes.cast(gates, ctypes.c_void_p),
+                             ctypes.cast(ups, ctypes.c_void_p), ctypes.cast(downs, ctypes.c_void_p))
+    return out
 
 
 def rmsnorm(x, eps):

@@ -455,6 +455,58 @@ void orc_layer_forward(double *out, int32_t *ids, double *w, double *margin, con
     free(logits);
 }
 
+/* ------------------------------------------- shared (always-on) experts */
+
+/* One shared expert of the dense trunk, kept in bf16 (the pages keep the
+ * trunk at 16 bits on purpose, "kimi-k3-in-c" explainer, "Why the trunk stays
+ * at 16 bits"; each MoE layer has two shared experts that run on every token,
+ * "Running Kimi K3 locally", "What are the four reductions, and why is the
+ * answer unchanged?").  The same SwiGLU form as a routed expert:
+ * y = W_down (silu(W_gate x) * (W_up x)), every bf16 weight exact in fp64,
+ * each row sum in fp64 with j ascending.  gate, up: [f][d]; down: [d][f],
+ * row-major bf16 bit patterns. */
+void orc_shared_expert(double *y, const uint16_t *gate, const uint16_t *up, const uint16_t *down,
+                       const double *x, int d, int f)
+{
+    double *h = (double *)malloc(sizeof(double) * (size_t)f);
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < f; r++) {
+        double g = 0.0, u = 0.0;
+        for (int j = 0; j < d; j++) {
+            g += orc_bf16_value(gate[(size_t)r * d + j]) * x[j];
+            u += orc_bf16_value(up[(size_t)r * d + j]) * x[j];
+        }
+        h[r] = orc_silu(g) * u;
+    }
+#pragma omp parallel for schedule(static)
+    for (int c = 0; c < d; c++) {
+        double acc = 0.0;
+        for (int r = 0; r < f; r++) acc += orc_bf16_value(down[(size_t)c * f + r]) * h[r];
+        y[c] = acc;
+    }
+    free(h);
+}
+
+/* out[t] = sum over the n shared experts of shared_expert_s(x[t]): the
+ * shared experts' outputs are added to the layer's output with weight 1 (a
+ * reading: the pages name the shared experts but not how they combine; an
+ * always-on expert has no router weight). */
+void orc_shared_forward(double *out, const double *x, int T, int d, int f, int n,
+                        const uint16_t *const *gates, const uint16_t *const *ups,
+                        const uint16_t *const *downs)
+{
+    double *y = (double *)malloc(sizeof(double) * (size_t)d);
+    for (int t = 0; t < T; t++) {
+        double *o = out + (size_t)t * d;
+        for (int i = 0; i < d; i++) o[i] = 0.0;
+        for (int s = 0; s < n; s++) {
+            orc_shared_expert(y, gates[s], ups[s], downs[s], x + (size_t)t * d, d, f);
+            for (int i = 0; i < d; i++) o[i] += y[i];
+        }
+    }
+    free(y);
+}
+
 /* ----------------------------------------------------------------- rmsnorm */
 
 void orc_rmsnorm(double *y, const double *x, int n, double eps)

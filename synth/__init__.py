@@ -14,7 +14,9 @@ distributions of the workloads:
   token so a single token can be redrawn on its own;
 * router weights ``W_r ~ N(0, 0.02)`` rounded to bf16;
 * a per-expert selection bias: ``N(0, 1)`` in fp32, or a Zipf(s) log-weight
-  ``-s * ln(rank)`` over a seeded permutation of ranks.
+  ``-s * ln(rank)`` over a seeded permutation of ranks;
+* bf16 shared experts with unit-variance products (gate/up ~ N(0, 1/sqrt(d)),
+  down ~ N(0, 1/sqrt(f))).
 
 Every tensor is addressed by a 64-bit tag (kind, pool, layer, index,
 substream) under the base seed, so any one expert can be regenerated without
@@ -37,6 +39,7 @@ K_ROUTER = 8
 K_BIAS_NORMAL = 9
 K_ZIPF_PERM = 10
 K_MISC = 11
+K_SHARED_GATE, K_SHARED_UP, K_SHARED_DOWN = 12, 13, 14
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "k3synth.c")
@@ -145,6 +148,15 @@ def expert(pool, layer, e, d=7168, f=1536, e_lo=120, e_hi=130, seed=BASE_SEED):
     dp, ds = matrix(K_DOWN_PACKED, K_DOWN_SCALES, d, f, pool, layer, e, e_lo, e_hi, seed)
     return dict(gate_packed=gp, gate_scales=gs, up_packed=up, up_scales=us,
                 down_packed=dp, down_scales=ds, d=d, f=f)
+
+
+def shared_expert(pool, layer, s, d=7168, f=1536, seed=BASE_SEED):
+    """One bf16 shared expert (bit patterns): gate, up [f x d] ~ N(0, 1/sqrt(d)),
+    down [d x f] ~ N(0, 1/sqrt(f)) (unit-variance products)."""
+    return dict(gate=normal_bf16((f, d), tag(K_SHARED_GATE, pool, layer, s), 0.0, d ** -0.5, seed),
+                up=normal_bf16((f, d), tag(K_SHARED_UP, pool, layer, s), 0.0, d ** -0.5, seed),
+                down=normal_bf16((d, f), tag(K_SHARED_DOWN, pool, layer, s), 0.0, f ** -0.5, seed),
+                d=d, f=f)
 
 
 def token_f32(pool, t, d=7168, sub=0, seed=BASE_SEED):
