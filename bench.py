@@ -22,6 +22,7 @@ One configuration alone, one JSON line each:
   --workload prefill4096  4096 bf16 tokens, selection bias ~N(0,1)
   --workload prefill4096_mxq  the same with the activations quantised to
                           MXFP4 (block-scaled E2M1 x E2M1 products)
+  --workload shared       the two bf16 shared experts of a layer, batch 1
   --workload stream       4 layers x 896 experts in pinned host memory behind
                           an 8 GB HBM LRU cache, 256 tokens, RMSNorm +
                           residual, Zipf(1.1) selection bias; the recorded
@@ -605,6 +606,50 @@ def run_expert(args, ctx, rank, world):
         "expert_hbm": {"bytes_per_gemv": nbytes, "gbs": round(nbytes / (per * 1e-3) / 1e9, 1)}}
 
 
+def run_shared(args, ctx, rank, world, n_layers=4, n_shared=2):
+    """The two bf16 shared experts of a layer at batch 1 (132 MB per token
+    at d = 7168, f = 1536), four layers' copies rotated so that every step
+    reads HBM."""
+    import torch
+    import synth
+    from mxfp4_routed_expert_select_gb300 import k3moe as k
+    dev = ctx.dev
+    steps = cfg_steps(args, 256)
+    sb = k.shared_expert_bytes(D, F)
+    blobs = torch.empty((n_layers * n_shared, sb), dtype=torch.uint8, device=dev)
+    for l in range(n_layers):
+        for s_ in range(n_shared):
+            ex = synth.shared_expert(3, l, s_, D, F)
+            raw = np.concatenate([ex["gate"].ravel(), ex["up"].ravel(), ex["down"].ravel()]).view(np.uint8)
+            blobs[l * n_shared + s_].copy_(torch.from_numpy(raw))
+    views = [[k.shared_expert_view(blobs[l * n_shared + s_].data_ptr(), D, F) for s_ in range(n_shared)]
+             for l in range(n_layers)]
+    X = torch.from_numpy(np.stack([synth.token_f32(3, rank * N_TOKENS + t, D) for t in range(N_TOKENS)])).to(dev)
+    y = torch.empty(D, dtype=torch.float32, device=dev)
+    ws = torch.empty(k.shared_workspace(n_shared, F) // 4, dtype=torch.float32, device=dev)
+
+    def step(i):
+        k.shared_forward(y, X[i % N_TOKENS], 1, views[i % n_layers], D, F, ws)
+
+    ms, clocks, plan = timed_region(step, steps, args.warmup, ctx.dev_index, world, True, n_inputs=N_TOKENS)
+    per = statistics.median(ms) / steps
+    nbytes = n_shared * sb + 2 * D * 4
+    return {
+        "metric": "shared-expert tokens/s (the two bf16 shared experts of a layer, batch 1)",
+        "value": round(job_rate(steps, world, statistics.median(ms)), 2), "unit": "tokens/s",
+        "steps": steps, "ms_per_step": round(per, 6), "higher_is_better": True,
+        "dtype": "bf16 weights, fp32 activations and accumulation",
+        "config": {"workload": "shared_experts_b1: 2 bf16 SwiGLU experts d=7168 f=1536 (%d B), x fp32 [7168]"
+                               % (n_shared * sb),
+                   "launch": "cuda graphs of %d steps (%d offsets) + %d, replayed" %
+                             (plan["chunk"], plan["variants"], plan["rem"]),
+                   "l2": "inputs larger than L2: %d layers' shared experts (%.0f MB) rotated" %
+                         (n_layers, n_layers * n_shared * sb / 1e6)},
+        "timing": spread(ms, steps),
+        "roofline": _roofline("k3_shared_gateup + k3_shared_down (bf16 rows, CUDA cores)", nbytes, per),
+        "gpu_launches": 2 * steps, "clocks": clocks}
+
+
 def run_batched(args, ctx, rank, world, T, bf16, use_bias, mxq=False):
     """The layer on T tokens per step: the grouped path (router, top-k,
     grouping by expert, grouped gate/up + SwiGLU, grouped down, combine);
@@ -911,6 +956,7 @@ POOL_WORKLOADS = {
     "decode64": lambda a, c, r, w: run_batched(a, c, r, w, 64, False, False),
     "prefill4096": lambda a, c, r, w: run_batched(a, c, r, w, 4096, True, True),
     "prefill4096_mxq": lambda a, c, r, w: run_batched(a, c, r, w, 4096, True, True, mxq=True),
+    "shared": lambda a, c, r, w: run_shared(a, c, r, w),
 }
 WORKLOADS = dict(POOL_WORKLOADS, stream=None)
 

@@ -588,6 +588,41 @@ int k3moe_trace_load(const char *path, int64_t *host_keys, int64_t cap_keys,
                      int32_t *host_batch_len, int32_t cap_batches, int64_t *host_n_keys,
                      int32_t *host_n_batches);
 
+/* ------------------------------------------ shared (always-on) experts */
+
+/*
+ * A shared expert of the dense trunk: each MoE layer of the pages' model has
+ * two that run on every token next to the routed ones ["Running Kimi K3
+ * locally", "What are the four reductions, and why is the answer
+ * unchanged?"], kept in bf16 like the rest of the trunk ["kimi-k3-in-c"
+ * explainer, "Why the trunk stays at 16 bits"].  Row-major bf16 bit
+ * patterns: gate, up [f][d], down [d][f]; each pointer 16-byte aligned.
+ * A blob of k3moe_shared_expert_bytes(d, f) = 6 d f bytes holds gate, up
+ * and down in that order (k3moe_shared_expert_view).
+ */
+typedef struct {
+    const uint16_t *gate, *up, *down;
+} k3moe_bf16_expert;
+
+#define K3MOE_MAX_SHARED 4
+int64_t k3moe_shared_expert_bytes(int32_t d, int32_t f);
+int k3moe_shared_expert_view(k3moe_bf16_expert *host_out, const void *blob, int32_t d, int32_t f);
+/* Workspace bytes of k3moe_shared_forward for n_shared experts of size f. */
+size_t k3moe_shared_workspace(int32_t n_shared, int32_t f);
+/*
+ * out[t] (+)= sum_s W_down^s (silu(W_gate^s x_t) * (W_up^s x_t)) for the
+ * n_shared (1..K3MOE_MAX_SHARED) experts: the shared experts' outputs are
+ * added with weight 1 (a reading: the pages do not say how they combine;
+ * an always-on expert has no router weight).  fp32 accumulation.
+ *  x, out     device fp32 [T][d]; accumulate != 0 adds into out
+ *  d, f       multiples of 256
+ *  workspace  device, k3moe_shared_workspace(n_shared, f) bytes
+ * Errors: K3MOE_EINVAL for null or misaligned pointers, bad sizes.
+ */
+int k3moe_shared_forward(float *out, const float *x, int32_t T, const k3moe_bf16_expert *host_experts,
+                         int32_t n_shared, int32_t d, int32_t f, int32_t accumulate, void *workspace,
+                         size_t workspace_bytes, k3moe_stream s);
+
 /* ------------------------------------------------ dense trunk streaming */
 
 /*
@@ -667,6 +702,9 @@ int k3moe_trunk_get_stats(const k3moe_trunk *T, k3moe_trunk_stats *host_out);
  *   for each miss j, in copy order:
  *       k3moe_cache_wait_copy(slot j);  x += w_j * expert_{ids_j}(u)
  *   k3moe_cache_release
+ *   with desc.trunk: x += sum_s shared_expert_s(u), the n_shared bf16 shared
+ *   experts of layer l read from trunk layer l (k3moe_trunk_acquire /
+ *   _release; n_shared consecutive blobs of k3moe_shared_expert_bytes(d, f))
  *  desc.host_layers  host array of n_layers layers (router-only layers are
  *                    fine: created with host_experts = NULL); all with the
  *                    same n_experts, top_k, d, f; top_k <= 16
@@ -682,6 +720,8 @@ typedef struct {
     k3moe_layer *const *host_layers;
     k3moe_cache *cache;
     float eps;
+    k3moe_trunk *trunk;  /* optional: layer l's trunk bytes hold its shared experts */
+    int32_t n_shared;    /* shared experts per layer (0 without a trunk)           */
 } k3moe_stream_desc;
 
 int k3moe_stream_decode(const k3moe_stream_desc *host_desc, const float *X, int32_t T, float *out,

@@ -40,6 +40,10 @@ int launch_group(const int32_t *ids, int npairs, int E, int nt, int32_t *offsets
 int grouped_nt();
 bool tc_supported(int E, int k, int d, int f);
 bool mxq_supported(int E, int k, int d, int f);
+bool shared_supported(int n, int d, int f);
+size_t shared_workspace_floats(int n, int f);
+int launch_shared(const uint16_t *const *gate, const uint16_t *const *up, const uint16_t *const *down, int n,
+                  const float *x, int T, int d, int f, float *h, float *out, int accumulate, cudaStream_t s);
 int mxq_max_tiles(int npairs, int E);
 size_t mxq_max_rows(int npairs, int E);
 size_t mxq_tile_bytes();
@@ -628,6 +632,46 @@ int k3moe_layer_mx_t1(const k3moe_layer *L)
     return (L->mx && L->mx_ready) ? 1 : 0;
 }
 
+int64_t k3moe_shared_expert_bytes(int32_t d, int32_t f)
+{
+    if (d <= 0 || f <= 0 || d % 8 || f % 8) return -1;
+    return 6 * (int64_t)d * f;
+}
+
+int k3moe_shared_expert_view(k3moe_bf16_expert *out, const void *blob, int32_t d, int32_t f)
+{
+    if (!out || !blob || k3moe_shared_expert_bytes(d, f) < 0 || !aligned16(blob)) return K3MOE_EINVAL;
+    const uint16_t *b = (const uint16_t *)blob;
+    out->gate = b;
+    out->up = b + (size_t)d * f;
+    out->down = b + 2 * (size_t)d * f;
+    return K3MOE_OK;
+}
+
+size_t k3moe_shared_workspace(int32_t n, int32_t f)
+{
+    if (n <= 0 || n > K3MOE_MAX_SHARED || f <= 0) return 0;
+    return sizeof(float) * k3::shared_workspace_floats(n, f);
+}
+
+int k3moe_shared_forward(float *out, const float *x, int32_t T, const k3moe_bf16_expert *ex, int32_t n,
+                         int32_t d, int32_t f, int32_t accumulate, void *ws, size_t ws_bytes, k3moe_stream s)
+{
+    if (!out || !x || !ex || !ws || T <= 0 || n <= 0 || n > K3MOE_MAX_SHARED || !k3::shared_supported(n, d, f) ||
+        !aligned16(out) || !aligned16(x) || !aligned16(ws) || ws_bytes < k3moe_shared_workspace(n, f))
+        return K3MOE_EINVAL;
+    const uint16_t *g[K3MOE_MAX_SHARED], *u[K3MOE_MAX_SHARED], *dn[K3MOE_MAX_SHARED];
+    for (int i = 0; i < n; i++) {
+        if (!ex[i].gate || !ex[i].up || !ex[i].down || !aligned16(ex[i].gate) || !aligned16(ex[i].up) ||
+            !aligned16(ex[i].down))
+            return K3MOE_EINVAL;
+        g[i] = ex[i].gate;
+        u[i] = ex[i].up;
+        dn[i] = ex[i].down;
+    }
+    return k3::launch_shared(g, u, dn, n, x, T, d, f, (float *)ws, out, accumulate ? 1 : 0, cs(s));
+}
+
 int k3moe_layer_mxq(const k3moe_layer *L)
 {
     if (!L) return K3MOE_EINVAL;
@@ -700,12 +744,14 @@ extern "C" int k3moe_stream_decode(const k3moe_stream_desc *D, const float *X, i
     if (!L0) return K3MOE_EINVAL;
     const int E = L0->E, k = L0->k, d = L0->d, f = L0->f;
     if (k > k3::kMaxInline) return K3MOE_EINVAL;
+    const int nsh = D->trunk ? D->n_shared : 0;
+    if (D->trunk && (nsh <= 0 || nsh > K3MOE_MAX_SHARED || !k3::shared_supported(nsh, d, f))) return K3MOE_EINVAL;
     for (int l = 0; l < D->n_layers; l++) {
         const k3moe_layer *L = D->host_layers[l];
         if (!L || L->E != E || L->k != k || L->d != d || L->f != f) return K3MOE_EINVAL;
     }
     cudaStream_t st = cs(s);
-    float *xcur = nullptr, *u = nullptr, *wsub = nullptr;
+    float *xcur = nullptr, *u = nullptr, *wsub = nullptr, *shws = nullptr;
     float *whost = nullptr;  // pinned: [k] routing weights, then [k] reordered hits-first
     int32_t *idhost = nullptr;
     int rc = K3MOE_OK;
@@ -716,7 +762,8 @@ extern "C" int k3moe_stream_decode(const k3moe_stream_desc *D, const float *X, i
         cudaMalloc(&u, sizeof(float) * d) != cudaSuccess ||
         cudaMalloc(&wsub, sizeof(float) * k) != cudaSuccess ||
         cudaMallocHost(&idhost, sizeof(int32_t) * k) != cudaSuccess ||
-        cudaMallocHost(&whost, sizeof(float) * 2 * k) != cudaSuccess) {
+        cudaMallocHost(&whost, sizeof(float) * 2 * k) != cudaSuccess ||
+        (nsh && cudaMalloc(&shws, k3moe_shared_workspace(nsh, f)) != cudaSuccess)) {
         cudaGetLastError();
         fail(K3MOE_ENOMEM);
     }
@@ -780,6 +827,26 @@ extern "C" int k3moe_stream_decode(const k3moe_stream_desc *D, const float *X, i
                 r = k3::launch_rows_t1(1, u, src, nh, d, f, L->h, st);
                 if (r == K3MOE_OK) r = k3::launch_down_t1(L->h, src, wsub, nh, d, f, xcur, st, true);
             }
+            // x += the layer's shared experts, from its trunk bytes (while the
+            // misses still copy)
+            if (r == K3MOE_OK && nsh) {
+                void *tb = nullptr;
+                r = k3moe_trunk_acquire(D->trunk, l, &tb, nullptr, s);
+                const uint16_t *g[K3MOE_MAX_SHARED], *uu[K3MOE_MAX_SHARED], *dn[K3MOE_MAX_SHARED];
+                for (int q = 0; q < nsh && r == K3MOE_OK; q++) {
+                    k3moe_bf16_expert se;
+                    r = k3moe_shared_expert_view(&se, (const uint8_t *)tb + (size_t)q * k3moe_shared_expert_bytes(d, f),
+                                                 d, f);
+                    g[q] = se.gate;
+                    uu[q] = se.up;
+                    dn[q] = se.down;
+                }
+                if (r == K3MOE_OK) r = k3::launch_shared(g, uu, dn, nsh, u, 1, d, f, shws, xcur, 1, st);
+                if (tb) {
+                    const int rt = k3moe_trunk_release(D->trunk, l, s);
+                    if (r == K3MOE_OK) r = rt;
+                }
+            }
             for (int q = nh; q < k && r == K3MOE_OK; q++) {
                 r = k3moe_cache_wait_copy(D->cache, blobs[order[q]], s);
                 ExpertSrc one;
@@ -808,6 +875,7 @@ extern "C" int k3moe_stream_decode(const k3moe_stream_desc *D, const float *X, i
     cudaFree(xcur);
     cudaFree(u);
     cudaFree(wsub);
+    if (shws) cudaFree(shws);
     cudaFreeHost(idhost);
     cudaFreeHost(whost);
     return rc;

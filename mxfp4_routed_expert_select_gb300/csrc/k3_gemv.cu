@@ -17,9 +17,8 @@
 //     transpose reduction, then across warps in shared memory;
 //   - the grid is the SM count times the resident CTAs per SM, with an equal
 //     row range per CTA, so every SM streams the same number of bytes.
-#include <atomic>
-
 #include "k3_device.cuh"
+#include "k3_launch.cuh"
 
 namespace k3 {
 
@@ -412,35 +411,6 @@ static int blocks_per_sm(K kernel, int threads, size_t smem)
         b < 1)
         b = 1;
     return b;
-}
-
-// Launches kernel<<<grid, block, smem, s>>>(args...) as a programmatic
-// dependent of the previous kernel on s where the driver takes it (the
-// kernel then overlaps its prologue, and its weight loads, with that
-// kernel's tail), else as a plain launch.
-template <typename... KArgs, typename... Args>
-static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                              Args... args)
-{
-    static std::atomic<int> refused{0};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = refused.load(std::memory_order_relaxed) ? 0 : 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
-    if (e != cudaSuccess && cfg.numAttrs == 1) {
-        cudaGetLastError();
-        refused.store(1, std::memory_order_relaxed);
-        cfg.numAttrs = 0;
-        e = cudaLaunchKernelEx(&cfg, kernel, args...);
-    }
-    return e;
 }
 
 constexpr int kUrows = 2;  // rows per pipeline stage in the gate/up kernel

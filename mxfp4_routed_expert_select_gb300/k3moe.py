@@ -82,7 +82,12 @@ class TrunkStats(ctypes.Structure):
 
 class StreamDesc(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("host_layers", ctypes.c_void_p),
-                ("cache", ctypes.c_void_p), ("eps", ctypes.c_float)]
+                ("cache", ctypes.c_void_p), ("eps", ctypes.c_float),
+                ("trunk", ctypes.c_void_p), ("n_shared", ctypes.c_int32)]
+
+
+class Bf16Expert(ctypes.Structure):
+    _fields_ = [("gate", ctypes.c_void_p), ("up", ctypes.c_void_p), ("down", ctypes.c_void_p)]
 
 
 ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
@@ -123,6 +128,10 @@ SIGNATURES = {
     "k3moe_layer_fused_t1": (ctypes.c_int, [_P]),
     "k3moe_layer_mx_t1": (ctypes.c_int, [_P]),
     "k3moe_layer_mxq": (ctypes.c_int, [_P]),
+    "k3moe_shared_expert_bytes": (_I64, [_I, _I]),
+    "k3moe_shared_expert_view": (ctypes.c_int, [_P, _P, _I, _I]),
+    "k3moe_shared_workspace": (_SZ, [_I, _I]),
+    "k3moe_shared_forward": (ctypes.c_int, [_P, _P, _I, _P, _I, _I, _I, _I, _P, _SZ, _P]),
     "k3moe_mx_quantize": (ctypes.c_int, [_P, _P, _P, _I, _I, _I, _P]),
     "k3moe_rmsnorm": (ctypes.c_int, [_P, _P, _I, _F, _P]),
     "k3moe_residual_add": (ctypes.c_int, [_P, _P, _I, _P]),
@@ -579,12 +588,40 @@ def trace_load(path):
     return keys, bl
 
 
-def stream_decode(layers, cache, X, T, out, eps=1e-6, stream=None, want_trace=True):
-    """k3moe_stream_decode: T tokens through len(layers) layers over `cache`.
+def shared_expert_bytes(d, f):
+    return lib().k3moe_shared_expert_bytes(d, f)
+
+
+def shared_expert_view(blob_ptr, d, f):
+    v = Bf16Expert()
+    check(lib().k3moe_shared_expert_view(ctypes.byref(v), ctypes.c_void_p(blob_ptr), d, f),
+          "k3moe_shared_expert_view")
+    return v
+
+
+def shared_workspace(n, f):
+    return lib().k3moe_shared_workspace(n, f)
+
+
+def shared_forward(out, x, T, views, d, f, workspace, accumulate=False, stream=None):
+    """k3moe_shared_forward: out (+)= the shared experts `views` of x [T, d]."""
+    n = len(views)
+    arr = (Bf16Expert * n)(*views)
+    nbytes = workspace.numel() * workspace.element_size()
+    check(lib().k3moe_shared_forward(_ptr(out), _ptr(x), T, ctypes.cast(arr, ctypes.c_void_p), n, d, f,
+                                     1 if accumulate else 0, _ptr(workspace), nbytes, _stream(stream)),
+          "k3moe_shared_forward")
+
+
+def stream_decode(layers, cache, X, T, out, eps=1e-6, stream=None, want_trace=True, trunk=None,
+                  n_shared=0):
+    """k3moe_stream_decode: T tokens through len(layers) layers over `cache`
+    (and, with `trunk`, each layer's n_shared bf16 shared experts from it).
     Returns (ids [T, L, k], hits [T, L, k]) as numpy arrays when want_trace."""
     nl = len(layers)
     arr = (ctypes.c_void_p * nl)(*[l.h.value for l in layers])
-    desc = StreamDesc(nl, ctypes.cast(arr, ctypes.c_void_p), cache.h.value, eps)
+    desc = StreamDesc(nl, ctypes.cast(arr, ctypes.c_void_p), cache.h.value, eps,
+                      None if trunk is None else trunk.h.value, n_shared if trunk is not None else 0)
     kk = layers[0].k
     ids = np.zeros((T, nl, kk), np.int32) if want_trace else None
     hits = np.zeros((T, nl, kk), np.uint8) if want_trace else None
