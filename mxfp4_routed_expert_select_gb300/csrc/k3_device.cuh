@@ -614,7 +614,8 @@ K3_DEV void cta_topk_by(Logit logit_of, const Router &rt, int E, int k, int32_t 
         }
     }
 }
-// 256 threads select the top k (k <= 16) of E <= 1024 selection keys
+// The first 256 threads of a CTA select the top k (k <= 16) of E <= 1024
+// selection keys
 // router_select(rt, logit_of(e), e), ties to the lower id, with the same
 // result as cta_topk_by and warp_topk.  Warp w holds keys 128 w .. 128 w +
 // 127, four per lane (lane l the ids 128 w + 4 l .. + 3), each lane's four
@@ -622,13 +623,15 @@ K3_DEV void cta_topk_by(Logit logit_of, const Router &rt, int E, int k, int32_t 
 // (redux.sync) take the warp's k largest in order: the lowest lane whose
 // head equals the maximum wins a tie, and lower lanes hold lower ids, so
 // equal keys leave in id order.  The 8 warps' k candidates meet in shared
-// memory, four per lane of warp 0 in the same order, and k more rounds take
-// the CTA's k largest.  One CTA barrier (the sync() call), no atomics.
-// ids_out[0..k) receives the ids in ascending order, w_out the weights from
-// the unbiased scores, as in warp_topk.
+// memory as 64-bit words key << 32 | (2^32 - 1 - id), which order exactly
+// like (key descending, id ascending), and every candidate's place is the
+// number of candidates with a larger word (two threads per candidate, half
+// of the 128 each): the k whose place is below k are the CTA's k largest.
+// Two CTA barriers (the sync() calls), no atomics.  ids_out[0..k) receives
+// the ids in ascending order, w_out the weights from the unbiased scores, as
+// in warp_topk.
 struct CtaTopkRedSmem {
-    uint32_t key[128];
-    int32_t id[128];
+    uint64_t cand[128];
     int32_t ids[16];
 };
 // (key, id) pairs a, b in order: key descending, id ascending on ties
@@ -676,39 +679,45 @@ K3_DEV void cta_topk_red(Logit logit_of, const Router &rt, int E, int k, int32_t
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     uint32_t key[4];
     int id[4];
-#pragma unroll
-    for (int r = 0; r < 4; r++) {
-        const int e = 128 * warp + 4 * lane + r;
-        key[r] = 0u;  // below every real key (okey(-inf) = 0x007fffff)
-        id[r] = 0x7fffffff;
-        if (e < E) {
-            key[r] = okey(router_select(rt, logit_of(e), e));
-            id[r] = e;
-        }
-    }
-    topk_cmpswap(key[0], id[0], key[1], id[1]);
-    topk_cmpswap(key[2], id[2], key[3], id[3]);
-    topk_cmpswap(key[0], id[0], key[2], id[2]);
-    topk_cmpswap(key[1], id[1], key[3], id[3]);
-    topk_cmpswap(key[1], id[1], key[2], id[2]);
     uint32_t rk;
     int rid;
-    warp_take_k(key, id, k, lane, rk, rid);
-    // candidate slot 16 w + i, i < k (the rest stay below every real key)
-    if (lane < 16) {
-        sm.key[16 * warp + lane] = lane < k ? rk : 0u;
-        sm.id[16 * warp + lane] = lane < k ? rid : 0x7fffffff;
+    if (warp < 8) {  // warps beyond the eighth (if any) only meet the barrier
+#pragma unroll
+        for (int r = 0; r < 4; r++) {
+            const int e = 128 * warp + 4 * lane + r;
+            key[r] = 0u;  // below every real key (okey(-inf) = 0x007fffff)
+            id[r] = 0x7fffffff;
+            if (e < E) {
+                key[r] = okey(router_select(rt, logit_of(e), e));
+                id[r] = e;
+            }
+        }
+        topk_cmpswap(key[0], id[0], key[1], id[1]);
+        topk_cmpswap(key[2], id[2], key[3], id[3]);
+        topk_cmpswap(key[0], id[0], key[2], id[2]);
+        topk_cmpswap(key[1], id[1], key[3], id[3]);
+        topk_cmpswap(key[1], id[1], key[2], id[2]);
+        warp_take_k(key, id, k, lane, rk, rid);
+        // candidate slot 16 w + i, i < k (the rest, word 0, stay below every
+        // real candidate: a real key is at least okey(-inf) = 0x007fffff)
+        if (lane < 16)
+            sm.cand[16 * warp + lane] =
+                lane < k ? ((uint64_t)rk << 32) | (uint64_t)(0xffffffffu - (uint32_t)rid) : 0ull;
+    }
+    sync();
+    if (warp < 8) {
+        const int c = t >> 1, h = t & 1;
+        const uint64_t vc = sm.cand[c];
+        int ahead = 0;
+#pragma unroll 8
+        for (int q = 64 * h; q < 64 * h + 64; q++) ahead += sm.cand[q] > vc;
+        ahead += __shfl_xor_sync(0xffffffffu, ahead, 1);
+        if (h == 0 && ahead < k && vc != 0ull) sm.ids[ahead] = (int)(0xffffffffu - (uint32_t)vc);
     }
     sync();
     if (warp == 0) {
-#pragma unroll
-        for (int r = 0; r < 4; r++) {
-            key[r] = sm.key[4 * lane + r];
-            id[r] = sm.id[4 * lane + r];
-        }
-        warp_take_k(key, id, k, lane, rk, rid);
         // each winner's place in ascending id order
-        if (lane < k) sm.ids[lane] = rid;
+        rid = lane < k ? sm.ids[lane] : 0;
         __syncwarp();
         int rank = 0;
         if (lane < k)

@@ -41,11 +41,19 @@
 // its scale becomes 0 (2^-127), so it adds at most 6 * 2^-127 * sum |v| of
 // its block, far below the fp32 resolution of any nonzero output.
 //
-// CTA: 8 warps.  warp 0 TMA producer (weight tiles 128 rows x 128 bytes,
+// Each phase runs as two waves, the first k * 3/4 expert slots and then the
+// rest (gate/up A, gate/up B, down A, down B), so that down A starts on an h
+// that was completed while gate/up B streamed, and h of B is completed while
+// down A streams: the copy engines never wait for an epilogue.
+//
+// CTA: 12 warps.  warp 0 TMA producer (weight tiles 128 rows x 128 bytes,
 // scale boxes 128 rows x 16 bytes), warp 1 MMA issuer and TMEM owner, warp
-// 2 turns scale boxes into tcgen05.cp atoms, warps 4-7 epilogue (TMEM lane
-// quadrants 0-3).  Every wait is bounded; a timeout sets the device error
-// word and the CTA drains and exits.
+// 2 turns scale boxes into tcgen05.cp atoms, warp 3 loads phase 1's h
+// pieces, warps 4-7 the phase-0 epilogue and warps 8-11 the phase-1
+// epilogue (TMEM lane quadrants 0-3 each), so that down products are taken
+// out of TMEM while the last gate/up tiles are still being finished.  Every
+// wait is bounded; a timeout sets the device error word and the CTA drains
+// and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -61,9 +69,10 @@ namespace k3 {
 
 constexpr int MX_M = 128;       // weight rows per tile
 constexpr int MX_UK = 256;      // K per unit: 128 packed bytes per row, 4 MMAs
-constexpr int MX_THREADS = 256;
-constexpr int MX_W_PROD = 0, MX_W_MMA = 1, MX_W_PERM = 2, MX_W_BLD = 3, MX_W_EPI = 4;
+constexpr int MX_THREADS = 384;
+constexpr int MX_W_PROD = 0, MX_W_MMA = 1, MX_W_PERM = 2, MX_W_BLD = 3, MX_W_EPI = 4, MX_W_EPI1 = 8;
 constexpr int MX_TMEM_COLS = 512;
+constexpr int MX_ROUTER_ROWS = 8;  // router rows per CTA at most (E <= 8 x the SM count)
 
 // Instruction descriptor of kind::mxf4 block_scale: E2M1 A and B (format 1,
 // bits 7-9 and 10-12), K-major, N = 16 (bits 17-22: N >> 3), UE8M0 scales
@@ -112,7 +121,14 @@ K3_DEV void sts32(uint32_t a, uint32_t v) { asm volatile("st.shared.u32 [%0], %1
 // counted twice and let the barrier open before another warp arrives.
 K3_DEV void cta_sync_threads() { asm volatile("barrier.sync 0;" ::: "memory"); }
 K3_DEV void red_add_f32(float *p, float v) { asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory"); }
-K3_DEV void mx_bar_epi() { asm volatile("barrier.sync 2, 128;" ::: "memory"); }
+// Named barrier of one phase's four epilogue warps (2: phase 0, 3: phase 1;
+// the two groups run at the same time).
+template <int PH>
+K3_DEV void mx_bar_epi()
+{
+    if (PH == 0) asm volatile("barrier.sync 2, 128;" ::: "memory");
+    else asm volatile("barrier.sync 3, 128;" ::: "memory");
+}
 K3_DEV unsigned ticket_add(unsigned *p, unsigned v)
 {
     unsigned old;
@@ -172,13 +188,14 @@ static size_t mx_bar_off(int d, int f) { return std::max(mx_layout_bytes<0>(d), 
 static size_t mx_smem(int d, int f) { return 1024 + mx_bar_off(d, f) + 1024; }
 
 // Barriers of one phase: full, atoms-full, empty per stage; accumulator
-// full / empty per TMEM buffer; B image loaded (two experts at most);
-// B scales in TMEM; all MMAs done.
+// full / empty per TMEM buffer; B image loaded per B buffer (phase 1: two
+// buffers, used by the experts of a CTA's ranges in turn); B scales in TMEM;
+// all MMAs done; B buffer free (phase 1: the MMAs reading it are done).
 template <int PH>
 struct MxBars {
     static constexpr int NS = MxCfg<PH>::NS;
     static constexpr int FULL = 0, AFULL = NS, EMPTY = 2 * NS, ACCF = 3 * NS, ACCE = ACCF + 2, BLOAD = ACCE + 2,
-                         BSCL = BLOAD + 2, FIN = BSCL + 1, N = FIN + 1;
+                         BSCL = BLOAD + 2, FIN = BSCL + 1, BFREE = FIN + 1, N = BFREE + 2;
 };
 template <int PH>
 K3_DEV void mx_init_bars(uint64_t *bars)
@@ -193,6 +210,7 @@ K3_DEV void mx_init_bars(uint64_t *bars)
         mbar_init(smem_addr(bars + Bs::ACCF + i), 1);
         mbar_init(smem_addr(bars + Bs::ACCE + i), 4);
         mbar_init(smem_addr(bars + Bs::BLOAD + i), 1);
+        mbar_init(smem_addr(bars + Bs::BFREE + i), 1);
     }
     mbar_init(smem_addr(bars + Bs::BSCL), 1);
     mbar_init(smem_addr(bars + Bs::FIN), 1);
@@ -216,13 +234,32 @@ K3_DEV bool mx_wait_count(const unsigned *p, unsigned target, int *err)
     }
 }
 
-// One phase on this CTA's share of the units.  sm: the 1024-aligned shared
-// memory (phase layouts overlap: the phases run one after the other),
-// bars: this phase's barriers, hready[j]: h tiles of expert slot j done.
+// A wave of one phase: the units [uw0, uw0 + Uw) (the tiles of a run of
+// expert slots), spread over the CTAs like a whole phase.  A phase runs as
+// one or two waves; first / last mark its first and last wave.
+struct MxWave {
+    long uw0, Uw;
+    bool first, last;
+};
+// What one thread's role has done in a phase so far (ring stages, finished
+// accumulators, phase 1's B buffers), carried from one wave to the next so
+// that every barrier's parity follows on.
+template <int PH>
+struct MxState {
+    uint32_t it = 0, sg = 0;
+    int nexp = 0, cur_j = -1;
+    uint32_t issued[MxCfg<PH>::NS] = {};
+};
+
+// One wave of a phase on this CTA's share of its units.  sm: the
+// 1024-aligned shared memory (phase layouts overlap: the phases run one after
+// the other), bars: this phase's barriers, hready[j]: h tiles of expert slot j
+// done.
 template <int PH>
 K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem, volatile int *abort_flag,
                     unsigned *s_last, unsigned *s_stop, unsigned *hready, const int32_t *sel_ids,
-                    const float *sel_w, uint32_t prev_fin, const volatile unsigned *x_issued)
+                    const float *sel_w, uint32_t prev_fin, const volatile unsigned *x_issued, const MxWave &w,
+                    MxState<PH> &st)
 {
     using C = MxCfg<PH>;
     using Bs = MxBars<PH>;
@@ -233,7 +270,7 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
     const uint32_t bimg_bytes = (uint32_t)K * 8u, bsf_bytes = (uint32_t)(K / 128) * 512u;
     const uint32_t sf_off = b_off + (PH == 0 ? bimg_bytes : 2 * bimg_bytes);
     const int B_FULL = Bs::FULL, B_AFULL = Bs::AFULL, B_EMPTY = Bs::EMPTY, B_ACCF = Bs::ACCF, B_ACCE = Bs::ACCE,
-              B_BLOAD = Bs::BLOAD, B_BSCL = Bs::BSCL, B_FIN = Bs::FIN;
+              B_BLOAD = Bs::BLOAD, B_BSCL = Bs::BSCL, B_FIN = Bs::FIN, B_BFREE = Bs::BFREE;
     auto bar = [&](int i) { return smem_addr(bars + i); };
     auto a_at = [&](int s, int m) { return sbase + (uint32_t)(s * C::STAGE + m * C::A_BYTES); };
     auto sc_at = [&](int s, int m) { return sbase + (uint32_t)(s * C::STAGE + NMAT * C::A_BYTES + m * C::SC_BYTES); };
@@ -241,32 +278,32 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
         return sbase + (uint32_t)(s * C::STAGE + NMAT * C::A_BYTES + C::NSC * C::SC_BYTES + m * C::AT_BYTES);
     };
     constexpr int NOUT = C::NOUT;
+    constexpr int EPI = PH == 0 ? MX_W_EPI : MX_W_EPI1;  // first of the phase's epilogue warps
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tpe = ROWS / MX_M;  // tiles per expert
     const int upt = K / C::UK;    // units per tile
-    const int ntiles = a.k * tpe;
-    const long U = (long)ntiles * upt, G = gridDim.x;
-    const long ulo = U * blockIdx.x / G, uhi = U * (blockIdx.x + 1) / G;
-    auto cta_of = [&](long u) { return (long)(((u + 1) * G - 1) / U); };
+    const long U = w.Uw, G = gridDim.x;
+    const long ulo = w.uw0 + U * blockIdx.x / G, uhi = w.uw0 + U * (blockIdx.x + 1) / G;
+    // the CTA whose range holds unit u, and the end of CTA c's range
+    auto cta_of = [&](long u) { return (long)(((u - w.uw0 + 1) * G - 1) / U); };
+    auto end_of = [&](long c) { return w.uw0 + U * (c + 1) / G; };
 
     // the experts of this CTA's range (phase 1 loads one B image per expert;
     // a range spans at most two experts, checked at launch)
     const int j_first = ulo < uhi ? (int)((ulo / upt) / tpe) : 0;
     const int j_last = ulo < uhi ? (int)(((uhi - 1) / upt) / tpe) : -1;
 
-    if (ulo < uhi && warp == MX_W_PROD) {
+    if (warp == MX_W_PROD) {
         // ---------------------------------------------------- TMA producer
-        uint32_t issued[NS];
-#pragma unroll
-        for (int i = 0; i < NS; i++) issued[i] = 0;
-        if (lane == 0) {
+        if (lane == 0 && ulo < uhi) {
             bool ok = true;
             // B operand images
             // phase 0: the x image copies were issued at the router's grid barrier
             // phase 1 reuses phase 0's shared memory: its MMAs must be done
-            if (PH == 1 && ok) ok = tc_wait(prev_fin, 0, a.err, abort_flag);
-            uint32_t it = 0;
+            if (PH == 1 && w.first && ok) ok = tc_wait(prev_fin, 0, a.err, abort_flag);
+            uint32_t it = st.it;
+            const uint64_t pol = l2_evict_first();  // weights: read once
             int cur_tile = -1;
             const CUtensorMap *mp = nullptr;
             int t = 0;
@@ -286,56 +323,65 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                     break;
                 }
                 mbar_arrive_expect_tx(bar(B_FULL + s), NMAT * C::A_BYTES + C::NSC * C::SC_BYTES);
-                issued[s]++;
+                st.issued[s]++;
                 if (PH == 0) {
 #pragma unroll
                     for (int m = 0; m < 2; m++) {  // gate, up
-                        tma_load_2d(a_at(s, m), mp + m, uu * 128, t * MX_M, bar(B_FULL + s));
-                        tma_load_2d(sc_at(s, m), mp + 3 + m, 16 * (uu >> 1), t * MX_M, bar(B_FULL + s));
+                        tma_load_2d_hint(a_at(s, m), mp + m, uu * 128, t * MX_M, bar(B_FULL + s), pol);
+                        tma_load_2d_hint(sc_at(s, m), mp + 3 + m, 16 * (uu >> 1), t * MX_M, bar(B_FULL + s), pol);
                     }
                 } else {
 #pragma unroll
                     for (int m = 0; m < 2; m++)  // two K steps of the down rows
-                        tma_load_2d(a_at(s, m), mp + 2, (2 * uu + m) * 128, t * MX_M, bar(B_FULL + s));
-                    tma_load_2d(sc_at(s, 0), mp + 5, 16 * uu, t * MX_M, bar(B_FULL + s));
+                        tma_load_2d_hint(a_at(s, m), mp + 2, (2 * uu + m) * 128, t * MX_M, bar(B_FULL + s), pol);
+                    tma_load_2d_hint(sc_at(s, 0), mp + 5, 16 * uu, t * MX_M, bar(B_FULL + s), pol);
                 }
             }
-            // drain: every copy issued here has landed before the CTA exits
+            st.it = it;
+        }
+        if (lane == 0 && w.last) {
+            // drain: every copy issued in this phase has landed before the CTA exits
             for (int s = 0; s < NS; s++)
-                if (issued[s]) mbar_wait(bar(B_FULL + s), (issued[s] - 1) & 1, a.err);
+                if (st.issued[s]) mbar_wait(bar(B_FULL + s), (st.issued[s] - 1) & 1, a.err);
             if (PH == 0 && *x_issued == 1u) mbar_wait(bar(B_BLOAD), 0, a.err);  // x image copies
         }
         __syncwarp();
-    } else if (PH == 1 && ulo < uhi && warp == MX_W_BLD) {
+    } else if (PH == 1 && warp == MX_W_BLD) {
         // ------------------------------- h pieces of this CTA's experts (phase 1)
         // once every h tile of expert slot j is written (acquire), bulk
-        // copies into the B buffer; the writers fenced their plain stores
+        // copies into the next B buffer (the two buffers take a CTA's experts
+        // in turn, across waves; a buffer is refilled once the MMAs of its
+        // previous expert are done); the writers fenced their plain stores
         // towards the async proxy before publishing, the copy side does too
-        int loaded = 0;
         if (lane == 0) {
-            bool ok = tc_wait(prev_fin, 0, a.err, abort_flag);  // phase 0's smem
-            for (int x = 0; x <= j_last - j_first && ok && !*abort_flag; x++) {
+            bool ok = !w.first || tc_wait(prev_fin, 0, a.err, abort_flag);  // phase 0's smem
+            for (int x = 0; ulo < uhi && x <= j_last - j_first && ok && !*abort_flag; x++) {
                 const int j = j_first + x;
+                const int b = st.nexp & 1, use = st.nexp >> 1;
+                if (use > 0 && !tc_wait(bar(B_BFREE + b), (use - 1) & 1, a.err, abort_flag)) break;
                 if (!mx_wait_count(hready + j, (unsigned)(a.f / MX_M), a.err)) {  // h tiles of one expert
                     *abort_flag = 1;
                     break;
                 }
                 asm volatile("fence.proxy.async.global;" ::: "memory");
-                mbar_arrive_expect_tx(bar(B_BLOAD + x), bimg_bytes + bsf_bytes);
+                mbar_arrive_expect_tx(bar(B_BLOAD + b), bimg_bytes + bsf_bytes);
                 for (uint32_t o = 0; o < bimg_bytes; o += 16384)
-                    bulk_g2s(sbase + b_off + x * bimg_bytes + o, a.bimg + (size_t)j * bimg_bytes + o,
-                             min(16384u, bimg_bytes - o), bar(B_BLOAD + x));
-                bulk_g2s(sbase + sf_off + x * bsf_bytes, a.bsf + (size_t)j * bsf_bytes, bsf_bytes, bar(B_BLOAD + x));
-                loaded++;
+                    bulk_g2s(sbase + b_off + b * bimg_bytes + o, a.bimg + (size_t)j * bimg_bytes + o,
+                             min(16384u, bimg_bytes - o), bar(B_BLOAD + b));
+                bulk_g2s(sbase + sf_off + b * bsf_bytes, a.bsf + (size_t)j * bsf_bytes, bsf_bytes, bar(B_BLOAD + b));
+                st.nexp++;
             }
-            // drain: the copies land before the CTA exits
-            for (int x = 0; x < loaded; x++) mbar_wait(bar(B_BLOAD + x), 0, a.err);
+            // drain: the copies land before the CTA exits (buffer b's last
+            // fill is its ((nexp - b + 1) / 2)-th)
+            if (w.last)
+                for (int b = 0; b < 2 && b < st.nexp; b++)
+                    mbar_wait(bar(B_BLOAD + b), (((st.nexp - b + 1) >> 1) - 1) & 1, a.err);
         }
         __syncwarp();
     } else if (ulo < uhi && warp == MX_W_PERM) {
         // ------------------------------------- scale boxes -> tcgen05.cp atoms
         // atom byte 16 r0 + 4 r1 + kb = scale of row r0 + 32 r1, k-block kb
-        uint32_t it = 0;
+        uint32_t it = st.it;
         for (long u = ulo; u < uhi && !*abort_flag; u++, it++) {
             const int uu = (int)(u % upt), s = it % NS;
             if (!__all_sync(0xffffffffu, tc_wait(bar(B_FULL + s), (it / NS) & 1, a.err, abort_flag))) break;
@@ -357,10 +403,11 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_AFULL + s));
         }
-    } else if (ulo < uhi && warp == MX_W_MMA) {
+        st.it = it;
+    } else if (warp == MX_W_MMA) {
         // ------------------------------------------------------ MMA issuer
         bool ok = true;
-        if (PH == 0) {
+        if (PH == 0 && w.first) {
             ok = __all_sync(0xffffffffu, tc_wait(bar(B_BLOAD), 0, a.err, abort_flag));
             if (ok) {
                 tc_fence_after();
@@ -369,14 +416,19 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                 mma_commit(bar(B_BSCL));
             }
         }
-        uint32_t it = 0, sg = 0;
-        int bx = -1;  // phase 1: B buffer of the current expert
+        uint32_t it = st.it, sg = st.sg;
+        int bx = (st.nexp - 1) & 1;  // phase 1: B buffer of the current expert
         for (long u = ulo; u < uhi && ok && !*abort_flag; u++, it++) {
             const int tile = (int)(u / upt), uu = (int)(u % upt);
             const bool first = (u == ulo) || uu == 0, last = (u + 1 == uhi) || uu == upt - 1;
-            if (PH == 1 && tile / tpe - j_first != bx) {
-                bx = tile / tpe - j_first;
-                if (!__all_sync(0xffffffffu, tc_wait(bar(B_BLOAD + bx), 0, a.err, abort_flag))) break;
+            if (PH == 1 && tile / tpe != st.cur_j) {
+                // the previous expert's buffer is free once the MMAs issued so far are done
+                if (st.cur_j >= 0) mma_commit(bar(B_BFREE + bx));
+                st.cur_j = tile / tpe;
+                bx = st.nexp & 1;
+                const int use = st.nexp >> 1;
+                st.nexp++;
+                if (!__all_sync(0xffffffffu, tc_wait(bar(B_BLOAD + bx), use & 1, a.err, abort_flag))) break;
                 tc_fence_after();
                 for (int at = 0; at < K / 128; at++)
                     mx_cp_atom(tmem + C::TSB + (uint32_t)(bx * (K / 32) + 4 * at),
@@ -429,26 +481,30 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                 sg++;
             }
         }
-        // every MMA and copy issued above has completed before TMEM is freed
-        mma_commit(bar(B_FIN));
-        mbar_wait(bar(B_FIN), 0, a.err);
+        st.it = it;
+        st.sg = sg;
+        // every MMA and copy issued in this phase has completed before TMEM is freed
+        if (w.last) {
+            mma_commit(bar(B_FIN));
+            mbar_wait(bar(B_FIN), 0, a.err);
+        }
         __syncwarp();
-    } else if (ulo < uhi && warp >= MX_W_EPI) {
+    } else if (ulo < uhi && warp >= EPI && warp < EPI + 4) {
         // --------------------------------------------------------- epilogue
         // The four warps run the same segments and meet at the same named
         // barriers (bar 2): whether to go on is decided by one thread and
         // read by all between two barriers, so no warp can leave while the
         // others wait.
         const int qd = warp & 3, row = qd * 32 + lane;
-        const bool leader = threadIdx.x == MX_W_EPI * 32;
-        uint32_t sg = 0;
+        const bool leader = threadIdx.x == EPI * 32;
+        uint32_t sg = st.sg;
         long u = ulo;
         int done_j[2] = {-1, -1}, done_n[2] = {0, 0};  // leader: h tiles finished per expert slot
         for (;;) {
             if (leader) *s_stop = (u >= uhi || *abort_flag) ? 1u : 0u;
-            mx_bar_epi();
+            mx_bar_epi<PH>();
             const bool stop = *s_stop != 0u;
-            mx_bar_epi();
+            mx_bar_epi<PH>();
             if (stop) break;
             const int tile = (int)(u / upt);
             const long t0 = (long)tile * upt, t1 = t0 + upt;
@@ -471,16 +527,16 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                 const float *pp = a.part + ((size_t)tile * upt) * MX_M * NOUT;
                 int nother = 0;
                 for (long us = ub; us < t1;) {
-                    const long ub2 = U * (cta_of(us) + 1) / G;
+                    const long ub2 = end_of(cta_of(us));
                     us = ub2 < t1 ? ub2 : t1;
                     nother++;
                 }
                 if (leader) *s_last = mx_wait_count(a.cnt + tile, (unsigned)nother, a.err) ? 1u : 0u;
                 __syncwarp();
-                mx_bar_epi();
+                mx_bar_epi<PH>();
                 if (*s_last != 1u) *abort_flag = 1;
                 for (long us = ub; us < t1;) {
-                    const long ub2 = U * (cta_of(us) + 1) / G, ue = ub2 < t1 ? ub2 : t1;
+                    const long ub2 = end_of(cta_of(us)), ue = ub2 < t1 ? ub2 : t1;
 #pragma unroll
                     for (int m = 0; m < NOUT; m++) pv[m] += __ldcg(pp + ((size_t)(us - t0) * MX_M + row) * NOUT + m);
                     us = ue;
@@ -523,7 +579,7 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
 #pragma unroll
                     for (int m = 0; m < NOUT; m++) pp[((size_t)seg * MX_M + row) * NOUT + m] = v[m];
                     __syncwarp();
-                    mx_bar_epi();
+                    mx_bar_epi<PH>();
                     if (leader) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.cnt + tile) : "memory");
                     continue;
                 }
@@ -550,12 +606,13 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                 red_add_f32(a.out + (size_t)t * MX_M + row, sel_w[j] * v[0]);
             }
         }
+        st.sg = sg;
         if (PH == 0) {
             // every h piece this CTA wrote is in memory (and ordered towards
             // the async proxy that copies it) before the counts
             asm volatile("fence.proxy.async.global;" ::: "memory");
             __syncwarp();
-            mx_bar_epi();
+            mx_bar_epi<PH>();
             if (leader)
                 for (int q = 0; q < 2; q++)
                     if (done_n[q])
@@ -565,6 +622,11 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
         }
     }
 }
+
+// Expert slots in a phase's first wave: three quarters of k (all of them for
+// k < 4).  The second wave's gate/up time must cover the first wave's h
+// epilogue, and the first wave's down time the second wave's.
+K3_DEV int wave_split(int k) { return k < 4 ? k : (3 * k + 3) / 4; }
 
 // Router of one token (phase R), spread over every CTA.
 struct MxRoute {
@@ -581,10 +643,11 @@ struct MxRoute {
 
 // Phase R.  Each CTA copies its block of router rows (E / G rows, one
 // contiguous piece of W_r) into its still unused stage memory with bulk
-// copies, one warp per row computes the logits from there; meanwhile warp g
-// of the grid encodes 32-block g of x and the CTAs zero out.  A grid barrier,
-// then every CTA reads the E logits and selects the top k itself.  False on
-// a timeout.
+// copies (read once: evict-first in L2), and all its warps compute their
+// logits from there, each over a slice of K; meanwhile warp g of the grid
+// encodes 32-block g of x and the CTAs zero out.  A grid barrier, then every
+// CTA reads the E logits and selects the top k itself while its last warp
+// copies in the pieces of x.  False on a timeout.
 template <typename XT>
 K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, uint8_t *sm, uint32_t bar_r, uint32_t bload0,
                      int32_t *sel_ids, float *sel_w, float *s_logit, CtaTopkRedSmem &tk, unsigned *s_flag)
@@ -597,7 +660,9 @@ K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, uint8_t *sm
     if (threadIdx.x == 0) {
         mbar_arrive_expect_tx(bar_r, rbytes);
         const uint8_t *src = reinterpret_cast<const uint8_t *>(r.Wr + (size_t)e0 * d);
-        for (uint32_t o = 0; o < rbytes; o += 16384) bulk_g2s(sbase + o, src + o, min(16384u, rbytes - o), bar_r);
+        const uint64_t pol = l2_evict_first();  // router rows: read once
+        for (uint32_t o = 0; o < rbytes; o += 16384)
+            bulk_g2s_hint(sbase + o, src + o, min(16384u, rbytes - o), bar_r, pol);
     }
     // Launched as a programmatic dependent of the previous kernel on the
     // stream: only the router rows (weights, never written by a kernel) are
@@ -613,22 +678,51 @@ K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, uint8_t *sm
         mx_encode_block(xv, lane, (int)b, r.ximg, r.ximg + (size_t)d * 8);
     }
     for (long i = (long)blockIdx.x * MX_THREADS + threadIdx.x; i < d; i += (long)G * MX_THREADS) out[i] = 0.f;
+    // Logits of the CTA's rows, K-sliced: warp w takes 8-element chunks
+    // [c0, c1) of every row (at most three per lane), so each lane reads its
+    // x chunks once and keeps them in registers, and all warps work however
+    // few rows the CTA holds; the warps' partial sums meet in shared memory
+    // (s_logit, not yet in use) and are added in warp order.
+    constexpr int NWR = MX_THREADS / 32;
+    const int nr = e1 - e0;  // <= MX_ROUTER_ROWS, checked at launch
+    const int nch = d >> 3, c0 = nch * warp / NWR, c1 = nch * (warp + 1) / NWR;
+    float xr[3][8];
+#pragma unroll
+    for (int i = 0; i < 3; i++) {
+        const int c = c0 + lane + 32 * i;
+        if (c < c1) {
+            load_x8<XT>(x, 8 * c, xr[i]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; j++) xr[i][j] = 0.f;
+        }
+    }
     bool ok = mbar_wait(bar_r, 0, a0.err);
-    for (int e = e0 + warp; e < e1 && ok; e += MX_THREADS / 32) {
-        const uint32_t row = sbase + (uint32_t)(e - e0) * (uint32_t)d * 2u;
-        float acc0 = 0.f, acc1 = 0.f;
-        for (int c = lane; c < (d >> 3); c += 64) {
-            float xa[8], xb[8];
-            load_x8<XT>(x, 8 * c, xa);
-            const uint4 wa = lds128(row + 16u * (uint32_t)c);
-            acc0 = bf16x8_dot(wa, xa, acc0);
-            if (c + 32 < (d >> 3)) {
-                load_x8<XT>(x, 8 * (c + 32), xb);
-                acc1 = bf16x8_dot(lds128(row + 16u * (uint32_t)(c + 32)), xb, acc1);
+    float acc[MX_ROUTER_ROWS];
+#pragma unroll
+    for (int q = 0; q < MX_ROUTER_ROWS; q++) {
+        acc[q] = 0.f;
+        if (q < nr && ok) {
+            const uint32_t row = sbase + (uint32_t)q * (uint32_t)d * 2u;
+#pragma unroll
+            for (int i = 0; i < 3; i++) {
+                const int c = c0 + lane + 32 * i;
+                if (c < c1) acc[q] = bf16x8_dot(lds128(row + 16u * (uint32_t)c), xr[i], acc[q]);
             }
         }
-        const float acc = warp_sum(acc0 + acc1);
-        if (lane == 0) r.logits[e] = acc;
+    }
+#pragma unroll
+    for (int q = 0; q < MX_ROUTER_ROWS; q++) {
+        if (q < nr) {
+            const float v = warp_sum(acc[q]);
+            if (lane == 0) s_logit[warp * MX_ROUTER_ROWS + q] = v;
+        }
+    }
+    cta_sync_threads();
+    if ((int)threadIdx.x < nr) {
+        float l = 0.f;
+        for (int w = 0; w < NWR; w++) l += s_logit[w * MX_ROUTER_ROWS + threadIdx.x];
+        r.logits[e0 + threadIdx.x] = l;
     }
     // the x image is read by other CTAs' bulk copies (async proxy)
     asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -638,22 +732,23 @@ K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, uint8_t *sm
         asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(r.gbar) : "memory");
         good = mx_wait_count(r.gbar, G, a0.err) && good;
         *s_flag = good ? 1u : 0u;
-        if (good) {
-            // phase 0's B operand, the pieces of x, while the top-k runs: the
-            // image to its buffer, the scale atoms staged in the last stage
-            using C0 = MxCfg<0>;
-            const uint32_t bimg = (uint32_t)d * 8u, bsf = (uint32_t)(d / 128) * 512u;
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            mbar_arrive_expect_tx(bload0, bimg + bsf);
-            for (uint32_t o = 0; o < bimg; o += 16384)
-                bulk_g2s(sbase + (uint32_t)(C0::NS * C0::STAGE) + o, r.ximg + o, min(16384u, bimg - o), bload0);
-            for (uint32_t o = 0; o < bsf; o += 16384)
-                bulk_g2s(sbase + (uint32_t)((C0::NS - 1) * C0::STAGE) + o, r.ximg + bimg + o, min(16384u, bsf - o),
-                         bload0);
-        }
     }
     cta_sync_threads();
     if (*s_flag != 1u) return false;
+    if (threadIdx.x == (NWR - 1) * 32) {
+        // phase 0's B operand, the pieces of x, while the top-k runs (in the
+        // first eight warps): the image to its buffer, the scale atoms staged
+        // in the last stage
+        using C0 = MxCfg<0>;
+        const uint32_t bimg = (uint32_t)d * 8u, bsf = (uint32_t)(d / 128) * 512u;
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        mbar_arrive_expect_tx(bload0, bimg + bsf);
+        for (uint32_t o = 0; o < bimg; o += 16384)
+            bulk_g2s(sbase + (uint32_t)(C0::NS * C0::STAGE) + o, r.ximg + o, min(16384u, bimg - o), bload0);
+        for (uint32_t o = 0; o < bsf; o += 16384)
+            bulk_g2s(sbase + (uint32_t)((C0::NS - 1) * C0::STAGE) + o, r.ximg + bimg + o, min(16384u, bsf - o),
+                     bload0);
+    }
     for (int e0b = threadIdx.x; e0b < E; e0b += 4 * MX_THREADS) {
         float v[4];
 #pragma unroll
@@ -707,6 +802,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
     unsigned *s_last = (unsigned *)(tmem_slot + 2);  // epilogue: this CTA completes the tile
     unsigned *s_stop = (unsigned *)(tmem_slot + 3);  // epilogue: no further segment
+    unsigned *s_stop1 = (unsigned *)(tmem_slot + 4);  // the same for phase 1's epilogue warps
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         s_flag = 0;
@@ -740,8 +836,25 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     // the SMs this grid leaves and wait for its completion before reading
     // anything it writes)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    mx_body<0>(a0, sm, bars0, tmem, abort_flag, s_last, s_stop, hready, sel_ids, sel_w, 0u, &s_flag);
-    mx_body<1>(a1, sm, bars1, tmem, abort_flag, s_last, s_stop, hready, sel_ids, sel_w, fin0, &s_flag);
+    // Two waves per phase: gate/up of the first kA expert slots, then of the
+    // rest; down of the first kA, then of the rest.  The first wave's h is
+    // complete while the second wave's gate/up rows still stream, so the down
+    // phase starts on h that is ready, and the second wave's h has the first
+    // wave's down products to be finished in.
+    const int kA = wave_split(a0.k), kB = a0.k - kA;
+    const long upe0 = (long)(a0.f / MX_M) * (a0.d / MxCfg<0>::UK), upe1 = (long)(a0.d / MX_M) * (a0.f / MxCfg<1>::UK);
+    MxState<0> st0;
+    MxState<1> st1;
+    mx_body<0>(a0, sm, bars0, tmem, abort_flag, s_last, s_stop, hready, sel_ids, sel_w, 0u, &s_flag,
+               MxWave{0, kA * upe0, true, kB == 0}, st0);
+    if (kB > 0)
+        mx_body<0>(a0, sm, bars0, tmem, abort_flag, s_last, s_stop, hready, sel_ids, sel_w, 0u, &s_flag,
+                   MxWave{kA * upe0, kB * upe0, false, true}, st0);
+    mx_body<1>(a1, sm, bars1, tmem, abort_flag, s_last, s_stop1, hready, sel_ids, sel_w, fin0, &s_flag,
+               MxWave{0, kA * upe1, true, kB == 0}, st1);
+    if (kB > 0)
+        mx_body<1>(a1, sm, bars1, tmem, abort_flag, s_last, s_stop1, hready, sel_ids, sel_w, fin0, &s_flag,
+                   MxWave{kA * upe1, kB * upe1, false, true}, st1);
 
     tc_fence_before();
     cta_sync_threads();
@@ -879,6 +992,7 @@ int launch_mx_t1(const void *x, int xdt, const uint16_t *Wr, int E, Router rt, c
     if ((u1 + G - 1) / G > upe1 || E > 1024) return K3MOE_EINVAL;
     // router rows below the stage holding the x scale atoms
     if ((size_t)((E + G - 1) / G) * d * 2 > (size_t)(MxCfg<0>::NS - 1) * MxCfg<0>::STAGE) return K3MOE_EINVAL;
+    if ((E + G - 1) / G > MX_ROUTER_ROWS) return K3MOE_EINVAL;
     MxRoute r = {};
     r.x = x;
     r.Wr = Wr;

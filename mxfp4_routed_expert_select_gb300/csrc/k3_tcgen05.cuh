@@ -39,6 +39,34 @@ K3_DEV void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint
                  : "memory");
 }
 
+// L2 policy for data a launch reads once (the expert weights and router
+// rows): evicted first, so that streaming them does not push out of L2 what
+// the launch reuses -- its own instructions, the activation and h images,
+// partial sums and counters -- which would otherwise come back from HBM at
+// every first use.
+K3_DEV uint64_t l2_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+// tma_load_2d with an L2 cache policy.
+K3_DEV void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+                 "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+                 "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar), "l"(policy)
+                 : "memory");
+}
+// bulk_g2s with an L2 cache policy.
+K3_DEV void bulk_g2s_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, "
+                 "[%3], %4;" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+                 : "memory");
+}
+
 // A hint: bring one TMA tile (x = byte column, y = row) of `map` into L2.
 // Nothing waits for it; a later load of the same tile hits L2 if the line is
 // still there.
