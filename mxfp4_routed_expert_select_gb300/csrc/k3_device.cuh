@@ -379,6 +379,22 @@ K3_DEV int sel_of(int lane)
     return idx;
 }
 
+// 8 x 8 transpose of 4-bit values within groups of 8 lanes: before, lane r
+// of a group holds A[r][c] in nibble c; after, it holds A[c][r] in nibble c.
+K3_DEV uint32_t nib_transpose8(uint32_t w, int lane)
+{
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1) {
+        const uint32_t M = m == 1 ? 0x0F0F0F0Fu : (m == 2 ? 0x00FF00FFu : 0x0000FFFFu);
+        const int sh = 4 * m;
+        const bool upper = (lane & m) != 0;
+        const uint32_t send = upper ? (w & M) : ((w >> sh) & M);
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
+        w = upper ? ((w & (M << sh)) | recv) : ((w & M) | (recv << sh));
+    }
+    return w;
+}
+
 K3_DEV float warp_sum(float v)
 {
 #pragma unroll

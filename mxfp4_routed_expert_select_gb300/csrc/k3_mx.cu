@@ -10,17 +10,18 @@
 //
 //   v = sum_p q_p * 2^(s_p)      per 32-block of v, p = 0..15
 //
-// where piece p rounds the residual r_p = v - (pieces so far) to the E2M1
-// grid after scaling by 2^-s_p, s_p the smallest exponent with
-// 6 * 2^s_p >= max |r_p| over the block.  Every residual is exact in fp32
-// and shrinks by at least 3x per piece, so 16 pieces leave less than
-// 3^-16 (2e-8) of the block maximum.  The 16 pieces are the 16 columns of
-// one M = 128, N = 16 MMA; the epilogue adds the columns.
+// where, E being the biased exponent of the block's largest magnitude, q_p
+// is the p-th base-4 digit (from the top) of the 32-bit fixed-point
+// magnitude |v| * 2^(158 - E), as an E2M1 value 0, .5, 1 or 1.5 with the sign
+// of v, and s_p = E - 127 - 2p (k3_mx.cuh, mx_encode_block).  Values down to
+// 2^-8 of the block's scale are represented exactly, smaller ones to 2^-32 of
+// it.  The 16 pieces are the 16 columns of one M = 128, N = 16 MMA; the
+// epilogue adds the columns, smallest first.
 //
 // Per token, one cooperative launch (one CTA per SM):
 //   router   logits of this CTA's block of router rows, a grid barrier, then
 //            every CTA selects the top k itself (k rounds of a warp maximum
-//            per warp, then over the warps' candidates) and the pieces of x
+//            per warp, then a rank over the warps' candidates) and the pieces of x
 //            are copied in: a B image [K/256][16 rows][128 bytes], 128-byte
 //            swizzled, plus E8M0 scale atoms [K/128][512 bytes] in the layout
 //            tcgen05.cp copies to TMEM

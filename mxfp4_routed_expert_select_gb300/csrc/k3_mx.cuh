@@ -15,40 +15,74 @@ K3_DEV size_t mx_img_off(int p, int b, int w)
 }
 K3_DEV size_t mx_sf_off(int p, int b) { return (size_t)(b >> 2) * 512 + 16 * p + (b & 3); }
 
-// One warp encodes one 32-block of v (lane i holds element i) as MX_N E2M1
-// pieces into img / sf.  A block holding a non-finite value gets scale byte
-// 255 (NaN) in every piece, so the products carry the NaN on.
-K3_DEV void mx_encode_block(float r, int lane, int b, uint8_t *img, uint8_t *sf)
+// Spread eight 2-bit digits (digit q at bits 2q + 1 .. 2q of x) into the
+// low two bits of eight nibbles (digit q to nibble q).
+K3_DEV uint32_t spread_digits(uint32_t x)
 {
-    const bool bad = __any_sync(0xffffffffu, !(fabsf(r) <= 3.4028235e38f));
-#pragma unroll 1
-    for (int p = 0; p < MX_N; p++) {
-        // block maximum of |r|: non-negative floats order like their bits
-        const uint32_t mb = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(r)));
-        const float m = __uint_as_float(mb);
-        uint32_t sbyte = 127u, code = 0u;
-        if (bad) {
-            sbyte = 255u;
-        } else if (m > 0.f) {
-            const int ex = (int)max(mb >> 23, 1u) - 126;  // 2^(ex-1) <= m < 2^ex (m normal)
-            int s = (m <= 0.75f * __int_as_float((127 + min(ex, 127)) << 23)) ? ex - 3 : ex - 2;
-            s = min(max(s, -126), 126);
-            sbyte = (uint32_t)(s + 127);
-            const float a = fabsf(r) * __int_as_float((127 - s) << 23);  // |r| / 2^s, exact
-            code = (a >= 0.25f) + (a >= 0.75f) + (a >= 1.25f) + (a >= 1.75f) + (a >= 2.5f) + (a >= 3.5f) +
-                   (a >= 5.0f);
-            const float qv = code < 4u ? 0.5f * (float)code : (code == 7u ? 6.f : (float)code - 2.f);
-            const float q = copysignf(qv, r) * __int_as_float((127 + s) << 23);
-            if (r < 0.f && code) code |= 8u;
-            r -= q;  // exact: q is r rounded on a grid no finer than r's own
+    x &= 0xFFFFu;
+    x = (x | (x << 8)) & 0x00FF00FFu;
+    x = (x | (x << 4)) & 0x0F0F0F0Fu;
+    x = (x | (x << 2)) & 0x33333333u;
+    return x;
+}
+
+// One warp encodes one 32-block of v (lane i holds element i) as MX_N E2M1
+// pieces into img / sf.  With E the biased exponent of the block's largest
+// magnitude (at least 1), every |v| becomes the 32-bit integer
+// M = |v| * 2^(158 - E) (exact for |v| >= 2^(E - 135), rounded to the
+// nearest integer below that, so the error is at most 2^(E - 159): 2^-32 of
+// the block's scale), and piece p is the p-th base-4 digit of M from the top,
+// d_p = (M >> (30 - 2p)) & 3, an E2M1 magnitude d_p / 2 (codes 0-3) with the
+// scale 2^(E - 127 - 2p) (E8M0 byte E - 2p; pieces whose byte would be
+// negative are left out, all their digits standing for less than 2^-126).
+// The sign goes into every nibble (a zero digit becomes -0).  So
+// sum_p piece_p = sign * M * 2^(E - 158), and piece 0 carries the largest
+// part, as the epilogues' order of summation expects.  A block holding a
+// non-finite value gets scale byte 255 (NaN) in every piece, so the products
+// carry the NaN on; an all-zero block gets codes 0.  No step depends on the
+// previous piece: one block maximum, then bit arithmetic per lane, an 8 x 8
+// nibble transpose within each group of eight lanes (lane j of group g: word
+// g of pieces j and 8 + j), two word stores per lane and one scale byte per
+// piece.
+K3_DEV void mx_encode_block(float v, int lane, int b, uint8_t *img, uint8_t *sf)
+{
+    const uint32_t bits = __float_as_uint(v), ab = bits & 0x7fffffffu;
+    const bool bad = __any_sync(0xffffffffu, ab >= 0x7f800000u);
+    const uint32_t mb = __reduce_max_sync(0xffffffffu, ab);
+    const int E = max((int)(mb >> 23), 1);
+    uint32_t c0 = 0u, c1 = 0u, sbyte = 127u;
+    if (bad) {
+        sbyte = 255u;
+    } else if (mb != 0u) {
+        const int ev = max((int)(ab >> 23), 1);
+        const uint32_t m24 = (ab & 0x7fffffu) | ((ab >> 23) ? 0x800000u : 0u);
+        const int sh = ev - E + 8;  // <= 8
+        uint32_t M;
+        if (sh >= 0) M = m24 << sh;
+        else M = -sh < 32 ? (m24 + (1u << (-sh - 1))) >> -sh : 0u;
+        // digit p of M (from the top) to nibble p: reverse the digit order
+        // (bit reversal, then swap the two bits of each digit), then spread
+        uint32_t R = __brev(M);
+        R = ((R >> 1) & 0x55555555u) | ((R & 0x55555555u) << 1);
+        c0 = spread_digits(R);        // digits 0-7
+        c1 = spread_digits(R >> 16);  // digits 8-15
+        if (E < 2 * (MX_N - 1)) {     // pieces whose scale byte E - 2p would be negative
+            const int pmax = E >> 1;  // last piece with E - 2p >= 0
+            const uint64_t keep = pmax >= 15 ? ~0ull : ((1ull << (4 * (pmax + 1))) - 1ull);
+            c0 &= (uint32_t)keep;
+            c1 &= (uint32_t)(keep >> 32);
         }
-        uint32_t word = code << (4 * (lane & 7));
-        word |= __shfl_xor_sync(0xffffffffu, word, 1);
-        word |= __shfl_xor_sync(0xffffffffu, word, 2);
-        word |= __shfl_xor_sync(0xffffffffu, word, 4);
-        if ((lane & 7) == 0) *(uint32_t *)(img + mx_img_off(p, b, lane >> 3)) = word;
-        if (lane == 0) sf[mx_sf_off(p, b)] = (uint8_t)sbyte;
+        if (bits >> 31) {
+            c0 |= 0x88888888u;
+            c1 |= 0x88888888u;
+        }
+        sbyte = (uint32_t)max(E - 2 * lane, 0);
     }
+    const int j = lane & 7, g = lane >> 3;
+    const uint32_t w0 = nib_transpose8(c0, lane), w1 = nib_transpose8(c1, lane);
+    *(uint32_t *)(img + mx_img_off(j, b, g)) = w0;
+    *(uint32_t *)(img + mx_img_off(8 + j, b, g)) = w1;
+    if (lane < MX_N) sf[mx_sf_off(lane, b)] = (uint8_t)sbyte;
 }
 
 }  // namespace k3

@@ -127,22 +127,6 @@ K3_DEV uint32_t mxq_rule(uint32_t ab, uint32_t sg, uint32_t mb, uint32_t &e)
     uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
     return sg ? (c | 8u) : c;
 }
-// 8 x 8 transpose of 4-bit values within groups of 8 lanes: before, lane r
-// of a group holds A[r][c] in nibble c; after, it holds A[c][r] in nibble c.
-K3_DEV uint32_t nib_transpose8(uint32_t w, int lane)
-{
-#pragma unroll
-    for (int m = 1; m < 8; m <<= 1) {
-        const uint32_t M = m == 1 ? 0x0F0F0F0Fu : (m == 2 ? 0x00FF00FFu : 0x0000FFFFu);
-        const int sh = 4 * m;
-        const bool upper = (lane & m) != 0;
-        const uint32_t send = upper ? (w & M) : ((w >> sh) & M);
-        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
-        w = upper ? ((w & (M << sh)) | recv) : ((w & M) | (recv << sh));
-    }
-    return w;
-}
-
 // The OCP MX conversion of one 32-block held one value per lane: returns this
 // lane's 4-bit code (bit 3 the sign; -0 is code 8) and, in *sbyte, the
 // block's E8M0 byte.  A block holding a non-finite value gets byte 255 and
