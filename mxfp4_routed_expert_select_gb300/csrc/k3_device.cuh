@@ -631,24 +631,31 @@ K3_DEV void cta_topk_by(Logit logit_of, const Router &rt, int E, int k, int32_t 
     }
 }
 // The first 256 threads of a CTA select the top k (k <= 16) of E <= 1024
-// selection keys
-// router_select(rt, logit_of(e), e), ties to the lower id, with the same
-// result as cta_topk_by and warp_topk.  Warp w holds keys 128 w .. 128 w +
-// 127, four per lane (lane l the ids 128 w + 4 l .. + 3), each lane's four
-// sorted (key descending, id ascending on ties).  k rounds of a warp maximum
-// (redux.sync) take the warp's k largest in order: the lowest lane whose
-// head equals the maximum wins a tie, and lower lanes hold lower ids, so
-// equal keys leave in id order.  The 8 warps' k candidates meet in shared
-// memory as 64-bit words key << 32 | (2^32 - 1 - id), which order exactly
-// like (key descending, id ascending), and every candidate's place is the
-// number of candidates with a larger word (two threads per candidate, half
-// of the 128 each): the k whose place is below k are the CTA's k largest.
-// Two CTA barriers (the sync() calls), no atomics.  ids_out[0..k) receives
-// the ids in ascending order, w_out the weights from the unbiased scores, as
-// in warp_topk.
+// selection keys router_select(rt, logit_of(e), e), ties to the lower id, with
+// the same result as cta_topk_by and warp_topk; ids_out[0..k) receives the
+// ids in ascending order (the combine weights are left to the caller, see
+// router_weight).  Keys are compared as 64-bit words
+// key << 32 | (2^32 - 1 - id), which order exactly like (key descending, id
+// ascending); ids >= E are padding (word 0).  Warp w holds the ids
+// w + 8 (4 l + r), r = 0..3, in lane l (interleaved, so that every warp holds
+// about E / 8 real keys; within a warp lower lanes still hold lower ids), each
+// lane's four sorted.
+//  1. Each warp takes its R = ceil(k / 8) largest words (R rounds of a warp
+//     maximum, redux.sync); T = the smallest of the eight warps' R-th largest.
+//     At least 8 R >= k words are >= T, so the k largest are all >= T.
+//  2. The words >= T (usually a few dozen) go to shared memory, and each one's
+//     place is the number of those words larger than it: the k whose place is
+//     below k are the result.
+//  3. If more than 128 words are >= T (keys with many ties at T, or fewer
+//     than R real keys in some warp), each warp takes its k largest instead
+//     (k rounds) and the 8 k candidates are ranked the same way.
+// Then warp 0 puts the k ids in ascending order.  sync() is a barrier over
+// all threads of the CTA; threads of warps 8 and up only take part in it.
 struct CtaTopkRedSmem {
     uint64_t cand[128];
+    uint64_t thr[8];
     int32_t ids[16];
+    int32_t cnt;
 };
 // (key, id) pairs a, b in order: key descending, id ascending on ties
 K3_DEV void topk_cmpswap(uint32_t &ka, int &ia, uint32_t &kb, int &ib)
@@ -688,65 +695,101 @@ K3_DEV void warp_take_k(uint32_t (&key)[4], int (&id)[4], int k, int lane, uint3
         }
     }
 }
+K3_DEV uint64_t topk_word(uint32_t key, int id, int E)
+{
+    return id < E ? ((uint64_t)key << 32) | (uint64_t)(0xffffffffu - (uint32_t)id) : 0ull;
+}
+K3_DEV int topk_word_id(uint64_t w) { return (int)(0xffffffffu - (uint32_t)w); }
+// the keys of warp w's four ids of this lane, sorted
+template <typename Logit>
+K3_DEV void topk_lane_keys(Logit logit_of, const Router &rt, int E, int warp, int lane, uint32_t (&key)[4],
+                           int (&id)[4])
+{
+#pragma unroll
+    for (int r = 0; r < 4; r++) {
+        const int e = warp + 8 * (4 * lane + r);
+        key[r] = 0u;  // below every real key (okey(-inf) = 0x007fffff)
+        id[r] = 0x7fffffff;
+        if (e < E) {
+            key[r] = okey(router_select(rt, logit_of(e), e));
+            id[r] = e;
+        }
+    }
+    topk_cmpswap(key[0], id[0], key[1], id[1]);
+    topk_cmpswap(key[2], id[2], key[3], id[3]);
+    topk_cmpswap(key[0], id[0], key[2], id[2]);
+    topk_cmpswap(key[1], id[1], key[3], id[3]);
+    topk_cmpswap(key[1], id[1], key[2], id[2]);
+}
+// places of the n (<= 128) candidate words: the k smallest places go to
+// sm.ids in descending word order
+K3_DEV void topk_rank(CtaTopkRedSmem &sm, int n, int k, int t)
+{
+    if (t < n) {
+        const uint64_t vc = sm.cand[t];
+        int ahead = 0;
+#pragma unroll 4
+        for (int q = 0; q < n; q++) ahead += sm.cand[q] > vc;
+        if (ahead < k) sm.ids[ahead] = topk_word_id(vc);
+    }
+}
 template <typename Sync, typename Logit>
-K3_DEV void cta_topk_red(Logit logit_of, const Router &rt, int E, int k, int32_t *ids_out, float *w_out,
-                         CtaTopkRedSmem &sm, Sync sync)
+K3_DEV void cta_topk_red(Logit logit_of, const Router &rt, int E, int k, int32_t *ids_out, CtaTopkRedSmem &sm,
+                         Sync sync)
 {
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int R = (k + 7) >> 3;
     uint32_t key[4];
     int id[4];
-    uint32_t rk;
-    int rid;
-    if (warp < 8) {  // warps beyond the eighth (if any) only meet the barrier
+    uint64_t own[4];
+    if (warp < 8) {
+        topk_lane_keys(logit_of, rt, E, warp, lane, key, id);
 #pragma unroll
-        for (int r = 0; r < 4; r++) {
-            const int e = 128 * warp + 4 * lane + r;
-            key[r] = 0u;  // below every real key (okey(-inf) = 0x007fffff)
-            id[r] = 0x7fffffff;
-            if (e < E) {
-                key[r] = okey(router_select(rt, logit_of(e), e));
-                id[r] = e;
-            }
-        }
-        topk_cmpswap(key[0], id[0], key[1], id[1]);
-        topk_cmpswap(key[2], id[2], key[3], id[3]);
-        topk_cmpswap(key[0], id[0], key[2], id[2]);
-        topk_cmpswap(key[1], id[1], key[3], id[3]);
-        topk_cmpswap(key[1], id[1], key[2], id[2]);
-        warp_take_k(key, id, k, lane, rk, rid);
-        // candidate slot 16 w + i, i < k (the rest, word 0, stay below every
-        // real candidate: a real key is at least okey(-inf) = 0x007fffff)
-        if (lane < 16)
-            sm.cand[16 * warp + lane] =
-                lane < k ? ((uint64_t)rk << 32) | (uint64_t)(0xffffffffu - (uint32_t)rid) : 0ull;
+        for (int r = 0; r < 4; r++) own[r] = topk_word(key[r], id[r], E);
+        uint32_t rk;
+        int rid;
+        warp_take_k(key, id, R, lane, rk, rid);
+        const uint64_t tw = __shfl_sync(0xffffffffu, topk_word(rk, rid, E), R - 1);
+        if (lane == 0) sm.thr[warp] = tw;
+        if (t == 0) sm.cnt = 0;
     }
     sync();
     if (warp < 8) {
-        const int c = t >> 1, h = t & 1;
-        const uint64_t vc = sm.cand[c];
-        int ahead = 0;
-#pragma unroll 8
-        for (int q = 64 * h; q < 64 * h + 64; q++) ahead += sm.cand[q] > vc;
-        ahead += __shfl_xor_sync(0xffffffffu, ahead, 1);
-        if (h == 0 && ahead < k && vc != 0ull) sm.ids[ahead] = (int)(0xffffffffu - (uint32_t)vc);
+        uint64_t T = sm.thr[0];
+#pragma unroll
+        for (int w = 1; w < 8; w++) T = sm.thr[w] < T ? sm.thr[w] : T;
+#pragma unroll
+        for (int r = 0; r < 4; r++)
+            if (own[r] != 0ull && own[r] >= T) {
+                const int pos = atomicAdd(&sm.cnt, 1);
+                if (pos < 128) sm.cand[pos] = own[r];
+            }
+    }
+    sync();
+    const int n = sm.cnt;
+    if (n <= 128) {
+        topk_rank(sm, n, k, t);
+    } else {
+        sync();  // every thread has read the count
+        if (warp < 8) {
+            topk_lane_keys(logit_of, rt, E, warp, lane, key, id);
+            uint32_t rk;
+            int rid;
+            warp_take_k(key, id, k, lane, rk, rid);
+            if (lane < 16) sm.cand[16 * warp + lane] = lane < k ? topk_word(rk, rid, E) : 0ull;
+        }
+        sync();
+        topk_rank(sm, 128, k, t);
     }
     sync();
     if (warp == 0) {
         // each winner's place in ascending id order
-        rid = lane < k ? sm.ids[lane] : 0;
+        const int rid = lane < k ? sm.ids[lane] : 0;
         __syncwarp();
         int rank = 0;
         if (lane < k)
             for (int q = 0; q < k; q++) rank += sm.ids[q] < rid;
-        __syncwarp();
-        if (lane < k) sm.ids[rank] = rid;
-        __syncwarp();
-        const int my_id = (lane < k) ? sm.ids[lane] : 0;
-        const float wv = router_weight(rt.mode, (lane < k) ? logit_of(my_id) : 0.f, lane < k);
-        if (lane < k) {
-            ids_out[lane] = my_id;
-            w_out[lane] = wv;
-        }
+        if (lane < k) ids_out[rank] = rid;
     }
 }
 

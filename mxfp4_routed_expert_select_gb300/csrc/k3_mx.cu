@@ -18,7 +18,7 @@
 // it.  The 16 pieces are the 16 columns of one M = 128, N = 16 MMA; the
 // epilogue adds the columns, smallest first.
 //
-// Per token, one cooperative launch (one CTA per SM):
+// Per token, one launch of one CTA per SM, all resident at once:
 //   router   logits of this CTA's block of router rows, a grid barrier, then
 //            every CTA selects the top k itself (k rounds of a warp maximum
 //            per warp, then a rank over the warps' candidates) and the pieces of x
@@ -217,6 +217,25 @@ K3_DEV void mx_init_bars(uint64_t *bars)
     mbar_init(smem_addr(bars + Bs::FIN), 1);
 }
 
+// Before the first fill of phase-1 stage s (bytes [s, s + 1) x STAGE of phase
+// 1): the phase-0 stages under it are read for the last time (the final phase
+// of their `empty` barriers, issued[q] fills ago), and if it reaches past
+// phase 0's stages, into the B image of x, all of phase 0's MMAs are done
+// (fin).  Only the producer thread calls it, with its own phase-0 counts.
+K3_DEV bool mx_phase1_slot_free(int s, const uint64_t *bars0, const uint32_t *issued0, uint32_t fin, int *err,
+                                volatile int *abort_flag)
+{
+    using C0 = MxCfg<0>;
+    using C1 = MxCfg<1>;
+    const int lo = s * C1::STAGE, hi = (s + 1) * C1::STAGE;  // bytes of phase-1 stage s
+    if (hi > C0::NS * C0::STAGE) return tc_wait(fin, 0, err, abort_flag);
+    for (int q = lo / C0::STAGE; q <= (hi - 1) / C0::STAGE; q++) {
+        if (issued0[q] == 0u) return tc_wait(fin, 0, err, abort_flag);  // never filled: be safe
+        if (!tc_wait(smem_addr(bars0 + MxBars<0>::EMPTY + q), (issued0[q] - 1u) & 1u, err, abort_flag)) return false;
+    }
+    return true;
+}
+
 // Bounded wait until *p >= target (acquire); false after the time limit.
 K3_DEV bool mx_wait_count(const unsigned *p, unsigned target, int *err)
 {
@@ -239,7 +258,7 @@ K3_DEV bool mx_wait_count(const unsigned *p, unsigned target, int *err)
 // expert slots), spread over the CTAs like a whole phase.  A phase runs as
 // one or two waves; first / last mark its first and last wave.
 struct MxWave {
-    long uw0, Uw;
+    int uw0, Uw;  // units fit in 32 bits (at most 16 x 12 x 28 per wave)
     bool first, last;
 };
 // What one thread's role has done in a phase so far (ring stages, finished
@@ -260,7 +279,7 @@ template <int PH>
 K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem, volatile int *abort_flag,
                     unsigned *s_last, unsigned *s_stop, unsigned *hready, const int32_t *sel_ids,
                     const float *sel_w, uint32_t prev_fin, const volatile unsigned *x_issued, const MxWave &w,
-                    MxState<PH> &st)
+                    MxState<PH> &st, const uint64_t *prev_bars = nullptr, const uint32_t *prev_issued = nullptr)
 {
     using C = MxCfg<PH>;
     using Bs = MxBars<PH>;
@@ -284,11 +303,11 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tpe = ROWS / MX_M;  // tiles per expert
     const int upt = K / C::UK;    // units per tile
-    const long U = w.Uw, G = gridDim.x;
-    const long ulo = w.uw0 + U * blockIdx.x / G, uhi = w.uw0 + U * (blockIdx.x + 1) / G;
+    const int U = w.Uw, G = (int)gridDim.x;
+    const int ulo = w.uw0 + U * (int)blockIdx.x / G, uhi = w.uw0 + U * ((int)blockIdx.x + 1) / G;
     // the CTA whose range holds unit u, and the end of CTA c's range
-    auto cta_of = [&](long u) { return (long)(((u - w.uw0 + 1) * G - 1) / U); };
-    auto end_of = [&](long c) { return w.uw0 + U * (c + 1) / G; };
+    auto cta_of = [&](int u) { return ((u - w.uw0 + 1) * G - 1) / U; };
+    auto end_of = [&](int c) { return w.uw0 + U * (c + 1) / G; };
 
     // the experts of this CTA's range (phase 1 loads one B image per expert;
     // a range spans at most two experts, checked at launch)
@@ -301,14 +320,12 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
             bool ok = true;
             // B operand images
             // phase 0: the x image copies were issued at the router's grid barrier
-            // phase 1 reuses phase 0's shared memory: its MMAs must be done
-            if (PH == 1 && w.first && ok) ok = tc_wait(prev_fin, 0, a.err, abort_flag);
             uint32_t it = st.it;
             const uint64_t pol = l2_evict_first();  // weights: read once
             int cur_tile = -1;
             const CUtensorMap *mp = nullptr;
             int t = 0;
-            for (long u = ulo; u < uhi && ok && !*abort_flag; u++, it++) {
+            for (int u = ulo; u < uhi && ok && !*abort_flag; u++, it++) {
                 const int tile = (int)(u / upt), uu = (int)(u % upt);
                 if (tile != cur_tile) {
                     cur_tile = tile;
@@ -318,6 +335,17 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                 }
                 const int s = it % NS;
                 if (it >= (uint32_t)NS && !tc_wait(bar(B_EMPTY + s), ((it / NS) - 1) & 1, a.err, abort_flag)) break;
+                // phase 1 reuses phase 0's shared memory: the first fill of a
+                // phase-1 stage waits until the MMAs of the phase-0 stages it
+                // overlaps have read them for the last time (their final
+                // `empty` phase), so the copies run on across the change of
+                // phase; a stage reaching into phase 0's B image waits for all
+                // of phase 0's MMAs
+                if (PH == 1 && it < (uint32_t)NS && !mx_phase1_slot_free(s, prev_bars, prev_issued, prev_fin, a.err,
+                                                                         abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 // phase 0: the last stage holds the B scale atoms until they are in TMEM
                 if (PH == 0 && it == (uint32_t)(NS - 1) && !tc_wait(bar(B_BSCL), 0, a.err, abort_flag)) {
                     ok = false;
@@ -383,7 +411,7 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
         // ------------------------------------- scale boxes -> tcgen05.cp atoms
         // atom byte 16 r0 + 4 r1 + kb = scale of row r0 + 32 r1, k-block kb
         uint32_t it = st.it;
-        for (long u = ulo; u < uhi && !*abort_flag; u++, it++) {
+        for (int u = ulo; u < uhi && !*abort_flag; u++, it++) {
             const int uu = (int)(u % upt), s = it % NS;
             if (!__all_sync(0xffffffffu, tc_wait(bar(B_FULL + s), (it / NS) & 1, a.err, abort_flag))) break;
 #pragma unroll
@@ -419,7 +447,7 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
         }
         uint32_t it = st.it, sg = st.sg;
         int bx = (st.nexp - 1) & 1;  // phase 1: B buffer of the current expert
-        for (long u = ulo; u < uhi && ok && !*abort_flag; u++, it++) {
+        for (int u = ulo; u < uhi && ok && !*abort_flag; u++, it++) {
             const int tile = (int)(u / upt), uu = (int)(u % upt);
             const bool first = (u == ulo) || uu == 0, last = (u + 1 == uhi) || uu == upt - 1;
             if (PH == 1 && tile / tpe != st.cur_j) {
@@ -499,7 +527,7 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
         const int qd = warp & 3, row = qd * 32 + lane;
         const bool leader = threadIdx.x == EPI * 32;
         uint32_t sg = st.sg;
-        long u = ulo;
+        int u = ulo;
         int done_j[2] = {-1, -1}, done_n[2] = {0, 0};  // leader: h tiles finished per expert slot
         for (;;) {
             if (leader) *s_stop = (u >= uhi || *abort_flag) ? 1u : 0u;
@@ -508,8 +536,8 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
             mx_bar_epi<PH>();
             if (stop) break;
             const int tile = (int)(u / upt);
-            const long t0 = (long)tile * upt, t1 = t0 + upt;
-            const long ua = u, ub = t1 < uhi ? t1 : uhi;
+            const int t0 = tile * upt, t1 = t0 + upt;
+            const int ua = u, ub = t1 < uhi ? t1 : uhi;
             u = ub;
             // a split tile's partial sums sit in slots indexed by the first
             // unit of their segment
@@ -527,8 +555,8 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                 // they are added in unit order
                 const float *pp = a.part + ((size_t)tile * upt) * MX_M * NOUT;
                 int nother = 0;
-                for (long us = ub; us < t1;) {
-                    const long ub2 = end_of(cta_of(us));
+                for (int us = ub; us < t1;) {
+                    const int ub2 = end_of(cta_of(us));
                     us = ub2 < t1 ? ub2 : t1;
                     nother++;
                 }
@@ -536,8 +564,8 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                 __syncwarp();
                 mx_bar_epi<PH>();
                 if (*s_last != 1u) *abort_flag = 1;
-                for (long us = ub; us < t1;) {
-                    const long ub2 = end_of(cta_of(us)), ue = ub2 < t1 ? ub2 : t1;
+                for (int us = ub; us < t1;) {
+                    const int ub2 = end_of(cta_of(us)), ue = ub2 < t1 ? ub2 : t1;
 #pragma unroll
                     for (int m = 0; m < NOUT; m++) pv[m] += __ldcg(pp + ((size_t)(us - t0) * MX_M + row) * NOUT + m);
                     us = ue;
@@ -651,7 +679,7 @@ struct MxRoute {
 // copies in the pieces of x.  False on a timeout.
 template <typename XT>
 K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, uint8_t *sm, uint32_t bar_r, uint32_t bload0,
-                     int32_t *sel_ids, float *sel_w, float *s_logit, CtaTopkRedSmem &tk, unsigned *s_flag)
+                     int32_t *sel_ids, float *s_logit, CtaTopkRedSmem &tk, unsigned *s_flag)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int d = a0.d, E = r.E, G = gridDim.x;
@@ -769,21 +797,30 @@ K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, uint8_t *sm
     // with the rule folded away
     auto logit_of = [&](int e) { return s_logit[e]; };
     if (r.rt.mode == K3_ROUTER_SOFTMAX)
-        cta_topk_red(logit_of, Router{r.rt.bias, K3_ROUTER_SOFTMAX}, E, a0.k, sel_ids, sel_w, tk,
-                      [] { cta_sync_threads(); });
+        cta_topk_red(logit_of, Router{r.rt.bias, K3_ROUTER_SOFTMAX}, E, a0.k, sel_ids, tk,
+                     [] { cta_sync_threads(); });
     else
-        cta_topk_red(logit_of, r.rt, E, a0.k, sel_ids, sel_w, tk, [] { cta_sync_threads(); });
+        cta_topk_red(logit_of, r.rt, E, a0.k, sel_ids, tk, [] { cta_sync_threads(); });
     cta_sync_threads();
-    if (blockIdx.x == 0 && threadIdx.x < a0.k) {
-        r.ids_out[threadIdx.x] = sel_ids[threadIdx.x];
-        r.w_out[threadIdx.x] = sel_w[threadIdx.x];
-    }
+    if (blockIdx.x == 0 && threadIdx.x < a0.k) r.ids_out[threadIdx.x] = sel_ids[threadIdx.x];
     return true;
 }
 
-// The whole layer for one token in one persistent kernel (cooperative
-// launch: CTAs wait for each other at the router's grid barrier and for the
-// h tiles that other CTAs finish in phase 0).
+// The combine weights of the selected experts from their unbiased logits,
+// by one warp (lane j < k: expert slot j), into sel_w and, from CTA 0, w_out.
+K3_DEV void mx_weights(const MxRoute &r, int k, const int32_t *sel_ids, const float *s_logit, float *sel_w, int lane)
+{
+    const bool on = lane < k;
+    const float w = router_weight(r.rt.mode, on ? s_logit[sel_ids[lane]] : 0.f, on);
+    if (on) {
+        sel_w[lane] = w;
+        if (blockIdx.x == 0) r.w_out[lane] = w;
+    }
+}
+
+// The whole layer for one token in one persistent kernel (one CTA per SM,
+// all resident: CTAs wait for each other at the router's grid barrier and for
+// the h tiles that other CTAs finish in phase 0).
 template <typename XT>
 __global__ void __launch_bounds__(MX_THREADS, 1)
     k3_mx_layer(const MxRoute r, const MxArgs a0, const MxArgs a1, unsigned *hready, unsigned *exit_cnt,
@@ -824,7 +861,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *(volatile uint32_t *)tmem_slot;
 
-    if (!mx_route<XT>(r, a0, a1.out, sm, smem_addr(bar_r), smem_addr(bars0 + MxBars<0>::BLOAD), sel_ids, sel_w, s_logit,
+    if (!mx_route<XT>(r, a0, a1.out, sm, smem_addr(bar_r), smem_addr(bars0 + MxBars<0>::BLOAD), sel_ids, s_logit,
                       tk, &s_flag))
         *abort_flag = 1;
     cta_sync_threads();
@@ -837,13 +874,16 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     // the SMs this grid leaves and wait for its completion before reading
     // anything it writes)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // the combine weights are needed only by the phase-1 epilogue warps, whose
+    // first named barrier orders them for the others of the four
+    if (warp == MX_W_EPI1 && *abort_flag == 0) mx_weights(r, a0.k, sel_ids, s_logit, sel_w, threadIdx.x & 31);
     // Two waves per phase: gate/up of the first kA expert slots, then of the
     // rest; down of the first kA, then of the rest.  The first wave's h is
     // complete while the second wave's gate/up rows still stream, so the down
     // phase starts on h that is ready, and the second wave's h has the first
     // wave's down products to be finished in.
     const int kA = wave_split(a0.k), kB = a0.k - kA;
-    const long upe0 = (long)(a0.f / MX_M) * (a0.d / MxCfg<0>::UK), upe1 = (long)(a0.d / MX_M) * (a0.f / MxCfg<1>::UK);
+    const int upe0 = (a0.f / MX_M) * (a0.d / MxCfg<0>::UK), upe1 = (a0.d / MX_M) * (a0.f / MxCfg<1>::UK);
     MxState<0> st0;
     MxState<1> st1;
     mx_body<0>(a0, sm, bars0, tmem, abort_flag, s_last, s_stop, hready, sel_ids, sel_w, 0u, &s_flag,
@@ -852,10 +892,10 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
         mx_body<0>(a0, sm, bars0, tmem, abort_flag, s_last, s_stop, hready, sel_ids, sel_w, 0u, &s_flag,
                    MxWave{kA * upe0, kB * upe0, false, true}, st0);
     mx_body<1>(a1, sm, bars1, tmem, abort_flag, s_last, s_stop1, hready, sel_ids, sel_w, fin0, &s_flag,
-               MxWave{0, kA * upe1, true, kB == 0}, st1);
+               MxWave{0, kA * upe1, true, kB == 0}, st1, bars0, st0.issued);
     if (kB > 0)
         mx_body<1>(a1, sm, bars1, tmem, abort_flag, s_last, s_stop1, hready, sel_ids, sel_w, fin0, &s_flag,
-                   MxWave{kA * upe1, kB * upe1, false, true}, st1);
+                   MxWave{kA * upe1, kB * upe1, false, true}, st1, bars0, st0.issued);
 
     tc_fence_before();
     cta_sync_threads();
@@ -951,28 +991,43 @@ static int launch_layer(const MxRoute &r, const MxArgs &a0, const MxArgs &a1, un
                         uint32_t bar_off, size_t smem, cudaStream_t s)
 {
     if (ensure_smem((const void *)k3_mx_layer<XT>, smem) != K3MOE_OK) return K3MOE_ECUDA;
-    // cooperative (every CTA resident: the CTAs wait for each other) and, where
-    // the driver takes it, a programmatic dependent of the previous kernel on
-    // the stream, so that its launch and router-row copies overlap that
-    // kernel's tail
+    // The CTAs wait for each other (the router's grid barrier, the h tiles),
+    // so all of them must be resident at once: one CTA per SM, and the SM
+    // must hold one (checked once).  The launch is not a cooperative one: a
+    // cooperative launch starts only when every SM is free at the same time,
+    // which would keep it from the SMs that the previous kernel on the stream
+    // leaves one by one.  Instead, where the driver takes it, it is a
+    // programmatic dependent of that kernel, whose CTAs start as its CTAs exit
+    // and request their router rows before it has completed.  Every wait
+    // between CTAs is bounded, so a grid that could not become resident (an
+    // SM held by other work for seconds) ends with K3MOE_ETIMEOUT in the
+    // device error word rather than hanging.
+    static std::atomic<int> resident{0};
+    if (!resident.load(std::memory_order_relaxed)) {
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k3_mx_layer<XT>, MX_THREADS, smem) != cudaSuccess ||
+            b < 1) {
+            cudaGetLastError();
+            return K3MOE_ECUDA;
+        }
+        resident.store(1, std::memory_order_relaxed);
+    }
     static std::atomic<int> pdl_refused{0};
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_sms());
     cfg.blockDim = dim3(MX_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl_refused.load(std::memory_order_relaxed) ? 1 : 2;
+    cfg.numAttrs = pdl_refused.load(std::memory_order_relaxed) ? 0 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, k3_mx_layer<XT>, r, a0, a1, hready, exit_cnt, bar_off);
-    if (e != cudaSuccess && cfg.numAttrs == 2) {
+    if (e != cudaSuccess && cfg.numAttrs == 1) {
         cudaGetLastError();
         pdl_refused.store(1, std::memory_order_relaxed);
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 0;
         e = cudaLaunchKernelEx(&cfg, k3_mx_layer<XT>, r, a0, a1, hready, exit_cnt, bar_off);
     }
     if (e != cudaSuccess) {
