@@ -570,7 +570,7 @@ def run_expert(args, ctx, rank, world):
     X = torch.from_numpy(np.stack([synth.token_f32(1, rank * N_TOKENS + t, D)
                                    for t in range(N_TOKENS)])).to(dev)
     y = torch.empty(D, dtype=torch.float32, device=dev)
-    ws = torch.empty(k.expert_gemv_workspace(D, F) // 4 + 4, dtype=torch.float32, device=dev)
+    ws = torch.zeros(k.expert_gemv_workspace(D, F) // 4 + 4, dtype=torch.float32, device=dev)
     perm = synth.permutation(E, synth.tag(synth.K_MISC, 1, 0, 7))
 
     def step(i):

@@ -684,14 +684,17 @@ K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, uint8_t *sm
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int d = a0.d, E = r.E, G = gridDim.x;
     const int e0 = (int)((long)E * blockIdx.x / G), e1 = (int)((long)E * (blockIdx.x + 1) / G);
-    const uint32_t rbytes = (uint32_t)(e1 - e0) * (uint32_t)d * 2u;
+    const uint32_t rowb = (uint32_t)d * 2u;  // one router row (<= 16 KB: d <= 8192)
     const uint32_t sbase = smem_addr(sm);
     if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(bar_r, rbytes);
+        // one copy and one barrier per row, so that a row's products start
+        // as soon as it has landed
         const uint8_t *src = reinterpret_cast<const uint8_t *>(r.Wr + (size_t)e0 * d);
         const uint64_t pol = l2_evict_first();  // router rows: read once
-        for (uint32_t o = 0; o < rbytes; o += 16384)
-            bulk_g2s_hint(sbase + o, src + o, min(16384u, rbytes - o), bar_r, pol);
+        for (int q = 0; q < e1 - e0; q++) {
+            mbar_arrive_expect_tx(bar_r + 8u * q, rowb);
+            bulk_g2s_hint(sbase + rowb * q, src + (size_t)rowb * q, rowb, bar_r + 8u * q, pol);
+        }
     }
     // Launched as a programmatic dependent of the previous kernel on the
     // stream: only the router rows (weights, never written by a kernel) are
@@ -700,6 +703,7 @@ K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, uint8_t *sm
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const XT *x = reinterpret_cast<const XT *>(r.x);
     const long NW = (long)G * (MX_THREADS / 32), gw = (long)blockIdx.x * (MX_THREADS / 32) + warp;
+    const bool encodes = gw < (d >> 5);  // this warp writes pieces of x
     for (long b = gw; b < (d >> 5); b += NW) {
         float xv;
         if constexpr (sizeof(XT) == 4) xv = __ldg(reinterpret_cast<const float *>(x) + 32 * b + lane);
@@ -726,13 +730,14 @@ K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, uint8_t *sm
             for (int j = 0; j < 8; j++) xr[i][j] = 0.f;
         }
     }
-    bool ok = mbar_wait(bar_r, 0, a0.err);
+    bool ok = true;
     float acc[MX_ROUTER_ROWS];
 #pragma unroll
     for (int q = 0; q < MX_ROUTER_ROWS; q++) {
         acc[q] = 0.f;
+        if (q < nr && ok) ok = mbar_wait(bar_r + 8u * q, 0, a0.err);
         if (q < nr && ok) {
-            const uint32_t row = sbase + (uint32_t)q * (uint32_t)d * 2u;
+            const uint32_t row = sbase + (uint32_t)q * rowb;
 #pragma unroll
             for (int i = 0; i < 3; i++) {
                 const int c = c0 + lane + 32 * i;
@@ -753,8 +758,9 @@ K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, uint8_t *sm
         for (int w = 0; w < NWR; w++) l += s_logit[w * MX_ROUTER_ROWS + threadIdx.x];
         r.logits[e0 + threadIdx.x] = l;
     }
-    // the x image is read by other CTAs' bulk copies (async proxy)
-    asm volatile("fence.proxy.async.global;" ::: "memory");
+    // the x image is read by other CTAs' bulk copies (async proxy): its
+    // writers order their stores towards that proxy
+    if (encodes) asm volatile("fence.proxy.async.global;" ::: "memory");
     cta_sync_threads();
     if (threadIdx.x == 0) {
         bool good = ok;
@@ -835,8 +841,8 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bars0 = (uint64_t *)(sm + bar_off);
     uint64_t *bars1 = bars0 + MxBars<0>::N;
-    uint64_t *bar_r = bars1 + MxBars<1>::N;  // router rows landed
-    uint32_t *tmem_slot = (uint32_t *)(bar_r + 1);
+    uint64_t *bar_r = bars1 + MxBars<1>::N;  // router rows landed, one per row
+    uint32_t *tmem_slot = (uint32_t *)(bar_r + MX_ROUTER_ROWS);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
     unsigned *s_last = (unsigned *)(tmem_slot + 2);  // epilogue: this CTA completes the tile
     unsigned *s_stop = (unsigned *)(tmem_slot + 3);  // epilogue: no further segment
@@ -846,7 +852,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
         s_flag = 0;
         mx_init_bars<0>(bars0);
         mx_init_bars<1>(bars1);
-        mbar_init(smem_addr(bar_r), 1);
+        for (int q = 0; q < MX_ROUTER_ROWS; q++) mbar_init(smem_addr(bar_r + q), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }

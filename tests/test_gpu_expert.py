@@ -74,7 +74,7 @@ def test_nan_scale_and_extreme_exponents():
 def test_expert_gemv_vs_oracle(d, f):
     """One expert, one token (the single-expert workload at full size)."""
     pool = Pool(0, 0, 2, d, f)
-    ws = torch.empty(k.expert_gemv_workspace(d, f) // 4, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(k.expert_gemv_workspace(d, f) // 4, dtype=torch.float32, device="cuda")
     for e in range(2):
         x = synth.token_f32(0, e, d)
         y = torch.empty(d, dtype=torch.float32, device="cuda")
@@ -94,10 +94,26 @@ def test_expert_gemv_swapped_nibbles_fail():
         sw[kk] = ((ex[kk] >> 4) | (ex[kk] << 4)).astype(np.uint8)
     blob = torch.empty(k.expert_bytes(d, f), dtype=torch.uint8, device="cuda")
     k.pack_expert(blob, sw, d, f)
-    ws = torch.empty(f, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(k.expert_gemv_workspace(d, f) // 4, dtype=torch.float32, device="cuda")
     x = synth.token_f32(0, 1, d)
     y = torch.empty(d, dtype=torch.float32, device="cuda")
     k.expert_gemv(y, torch.from_numpy(x).cuda(), k.expert_view(blob.data_ptr(), d, f), d, f, ws)
     torch.cuda.synchronize()
     ref = oracle.expert_forward(ex, x.astype(np.float64))
     assert rel_err(y.cpu().numpy(), ref) > 0.1
+
+
+@pytest.mark.parametrize("d,f", [(512, 512), (1024, 512), (4096, 2048), (7168, 1536), (7168, 2048)])
+def test_expert_gemv_repeats_on_one_workspace(d, f):
+    """From fewer gate/up stages than CTAs to the full size: three calls in a
+    row on one workspace, each against the oracle."""
+    pool = Pool(0, 0, 3, d, f)
+    ws = torch.zeros(k.expert_gemv_workspace(d, f) // 4, dtype=torch.float32, device="cuda")
+    for e in range(3):
+        x = synth.token_f32(0, 100 + e, d)
+        y = torch.full((d,), float("nan"), dtype=torch.float32, device="cuda")
+        k.expert_gemv(y, torch.from_numpy(x).cuda(), pool.views[e], d, f, ws)
+        torch.cuda.synchronize()
+        ref = oracle.expert_forward(pool.planes(e), x.astype(np.float64))
+        assert rel_err(y.cpu().numpy(), ref) <= TOL, (d, f, e)
+    assert k.device_error() == 0

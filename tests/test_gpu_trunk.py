@@ -26,7 +26,7 @@ def test_streamed_layers_arrive_intact(ring):
             arr[...] = planes[nm]
     dev.copy_(host)
     x = torch.from_numpy(synth.token_f32(21, 0, d)).cuda()
-    ws = torch.empty(k.expert_gemv_workspace(d, f), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(k.expert_gemv_workspace(d, f), dtype=torch.uint8, device="cuda")
     ws2 = torch.empty_like(ws)
     pinned = 2 * ((eb + 255) // 256 * 256)  # layers 0 and 1 resident
     t = k.Trunk([host[l].data_ptr() for l in range(M)], [eb] * M, pinned, ring)

@@ -29,7 +29,7 @@ def test_wait_on_nothing_times_out_and_the_context_survives():
     k.pack_expert(blob, ex, d, f)
     x = synth.token_f32(31, 0, d)
     y = torch.empty(d, dtype=torch.float32, device="cuda")
-    ws = torch.empty(k.expert_gemv_workspace(d, f) // 4 + 4, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(k.expert_gemv_workspace(d, f) // 4 + 4, dtype=torch.float32, device="cuda")
     k.expert_gemv(y, torch.from_numpy(x).cuda(), k.expert_view(blob.data_ptr(), d, f), d, f, ws)
     torch.cuda.synchronize()
     assert rel_err(y.cpu().numpy(), oracle.expert_forward(ex, x)) <= 2e-3

@@ -37,7 +37,7 @@ def test_noalloc_matches_oracle_and_workspace_entry_point_on_two_calls(d, f):
     planes = [_planes(e, d, f) for e in range(2)]
     blobs = [_blob(p, d, f) for p in planes]
     views = [k.expert_view(b.data_ptr(), d, f) for b in blobs]
-    ws = torch.empty(k.expert_gemv_workspace(d, f) // 4, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(k.expert_gemv_workspace(d, f) // 4, dtype=torch.float32, device="cuda")
     for call in range(2):
         x = synth.token_f32(11, call, d)
         xd = torch.from_numpy(x).cuda()
