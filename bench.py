@@ -58,16 +58,17 @@ N_ROUTER_COPIES = 16
 # kept beside it, labelled.
 FUSED_TRAFFIC = None
 FUSED_TRAFFIC_LAST = 294038272
-# The same for the block-scaled batch-1 kernel (k3_mx_layer<float>).
-MX_TRAFFIC = None
-MX_TRAFFIC_LAST = 301050624
+# The same for the block-scaled batch-1 kernel (k3_mx_layer<float>): median
+# of five launches (read 297,614,336 B + write 3,495,680 B), this build.
+MX_TRAFFIC = 301110016
+MX_TRAFFIC_LAST = 301110016
 TRAFFIC_LAST_NOTE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch at this workload "
                      "(median of 3 launches), taken before the router rule became selectable; the "
                      "kernel has changed since, its memory accesses have not")
 N_TOKENS = 1024
 # Kernels of the secondary configurations (names for the roofline lines and
 # launches per step).  One expert: gate/up + SwiGLU, then down.
-EXPERT_GEMV_KERNEL = "k3_rows_t1 + k3_down_t1 (one expert: gate/up + SwiGLU, down)"
+EXPERT_GEMV_KERNEL = "k3_rows_pipe + k3_down_t1 (one expert: gate/up + SwiGLU, down)"
 EXPERT_GEMV_LAUNCHES = 2
 # Multi-token forwards: router GEMM + top-k, grouping, tile plan, token
 # scales, token gather, gate/up, h pieces, down + combine.
@@ -450,7 +451,7 @@ def run_decode1(args, ctx, rank, world):
     k_ms = per if (mx or fused) and not args.no_graph else eager_ms
     roof = _roofline(k_name, LAYER_BYTES, k_ms, traffic=traffic,
                      traffic_src=("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch at this "
-                                  "workload (median of 3 launches)") if traffic else None)
+                                  "workload (median of the captured launches)") if traffic else None)
     if traffic_last:
         roof["traffic_last_capture"] = traffic_last
     peak = roof["peak"]
