@@ -615,7 +615,8 @@ size_t k3moe_shared_workspace(int32_t n_shared, int32_t f);
  * added with weight 1 (a reading: the pages do not say how they combine;
  * an always-on expert has no router weight).  fp32 accumulation.
  *  x, out     device fp32 [T][d]; accumulate != 0 adds into out
- *  d, f       multiples of 256
+ *  d, f       multiples of 256, d <= 8192 and n_shared * f <= 4096 (the
+ *             lanes of a warp hold a whole down row of the n_shared experts)
  *  workspace  device, k3moe_shared_workspace(n_shared, f) bytes
  * Errors: K3MOE_EINVAL for null or misaligned pointers, bad sizes.
  */

@@ -311,18 +311,24 @@ __global__ void __launch_bounds__(256) k3_mxq_xtiles(const XT *__restrict__ X, i
             xrow = Xg + (size_t)tl.row0 * rowb;
             xsf = Xsf + (size_t)(s / MQ_TN) * sfb;
         }
-        for (int b = 0; b < nb; b++) {
-            float v;
-            if constexpr (sizeof(XT) == 2)
-                v = __uint_as_float((uint32_t)((const uint16_t *)X)[(size_t)t * d + 32 * b + lane] << 16);
-            else
-                v = ((const float *)X)[(size_t)t * d + 32 * b + lane];
-            uint32_t sb;
-            const uint4 ch = mxq_chunk(mxq_pack(mxq_code(v, &sb), lane));
-            if (lane < k) {
-                *(uint4 *)(xrow + mq_code_off(j, b, np)) = ch;
-                xsf[mq_sf_off(j, b)] = (uint8_t)sb;
+        // four blocks at a time: their scale bytes are four consecutive bytes
+        // of the row's atom (one word store instead of four byte stores)
+        for (int b0 = 0; b0 < nb; b0 += 4) {
+            uint32_t sw = 0;
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const int b = b0 + q;
+                float v;
+                if constexpr (sizeof(XT) == 2)
+                    v = __uint_as_float((uint32_t)((const uint16_t *)X)[(size_t)t * d + 32 * b + lane] << 16);
+                else
+                    v = ((const float *)X)[(size_t)t * d + 32 * b + lane];
+                uint32_t sb;
+                const uint4 ch = mxq_chunk(mxq_pack(mxq_code(v, &sb), lane));
+                sw |= sb << (8 * q);
+                if (lane < k) *(uint4 *)(xrow + mq_code_off(j, b, np)) = ch;
             }
+            if (lane < k) *(uint32_t *)(xsf + mq_sf_off(j, b0)) = sw;
         }
     }
 }

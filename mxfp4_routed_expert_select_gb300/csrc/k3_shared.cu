@@ -9,11 +9,14 @@
 //
 // At a few tokens per call the products are matrix-vector streams of bf16
 // rows (2 bytes per weight, no decode: a bf16 is the high half of an fp32),
-// so both kernels are bound by HBM: every lane loads 16 bytes (8 weights) of
-// a row per step with several steps in flight, one warp per row, the tokens
-// (gate/up) or h (down) held in shared memory.  Both are launched as
-// programmatic dependents: their first weight rows are requested before the
-// previous kernel on the stream has finished.
+// so both kernels are bound by HBM and by how many of their loads are in
+// flight: every lane requests all of its 16-byte chunks of a unit at once
+// (gate/up: four rows split along K over the CTA's warps; down: one output
+// row per warp), the next unit's before the current one is reduced, the
+// tokens (gate/up) or h (down) held in shared memory, and the grids are one
+// resident wave.  Both are launched as programmatic dependents: their first
+// weight rows are requested before the previous kernel on the stream has
+// finished.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -26,7 +29,9 @@ namespace k3 {
 constexpr int SH_MAX = 4;     // shared experts per call at most
 constexpr int SH_TMAX = 4;    // tokens per launch at most (x in shared memory)
 constexpr int SH_WARPS = 16;  // warps per CTA
-constexpr int SH_U = 4;       // 16-byte loads in flight per lane and matrix
+constexpr int SH_RG = 4;      // gate/up rows per unit
+constexpr int SH_CH = 2;      // 16-byte chunks per lane and row of a gate/up K-slice (d <= 8192)
+constexpr int SH_CHD = 16;    // 16-byte chunks per lane of a down row (n f <= 4096)
 
 struct SharedSrc {
     const uint16_t *gate[SH_MAX], *up[SH_MAX], *down[SH_MAX];
@@ -45,130 +50,132 @@ K3_DEV float sh_dot8(uint4 w, const float *v, float acc)
     return acc;
 }
 
-// h[t][s][r] = silu(gate_s[r] . x_t) * (up_s[r] . x_t), one warp per row
-// q = s f + r; x [T][d] staged in shared memory.  d a multiple of 256.
+// h[t][s][r] = silu(gate_s[r] . x_t) * (up_s[r] . x_t).  A unit is SH_RG rows
+// q = s f + r (of one expert: f % SH_RG == 0); warp w of the CTA takes K-slice
+// w of them (d / 8 / SH_WARPS chunks of 8 weights), every lane issuing all of
+// its loads for the unit at once, so that a row costs one memory round trip
+// instead of one per chunk; the slices' partial sums meet in shared memory.
+// x [T][d] is staged in shared memory.
 __global__ void __launch_bounds__(SH_WARPS * 32) k3_shared_gateup(const SharedSrc src, int n, const float *x, int T,
                                                                   int d, int f, float *h)
 {
-    extern __shared__ float xs[];  // [T][d]
+    extern __shared__ float xs[];  // [T][d], then red [SH_WARPS][SH_RG * 2 * SH_TMAX]
+    float *red = xs + (size_t)T * d;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nc = d / 8;  // 16-byte chunks per row
+    const int cpw = d / 8 / SH_WARPS;  // chunks per warp slice
+    const int nunits = n * f / SH_RG;
     griddep_launch_dependents();
-    const long nrows = (long)n * f, W = (long)gridDim.x * SH_WARPS;
-    long q = (long)blockIdx.x * SH_WARPS + warp;
-    // the first row's first chunks are requested before x can be read
-    uint4 pg[SH_U], pu[SH_U];
-    if (q < nrows) {
-        const int s = (int)(q / f), r = (int)(q % f);
+    int u = blockIdx.x;
+    // the first unit's weights are requested before x can be read
+    uint4 wg[SH_RG][SH_CH], wu[SH_RG][SH_CH];
+    auto load = [&](int uu) {
+        const int q0 = uu * SH_RG, s = q0 / f, r0 = q0 % f;
 #pragma unroll
-        for (int i = 0; i < SH_U; i++) {
-            const int c = lane + 32 * i;
-            pg[i] = c < nc ? sh_ld16(src.gate[s] + (size_t)r * d + 8 * c) : make_uint4(0, 0, 0, 0);
-            pu[i] = c < nc ? sh_ld16(src.up[s] + (size_t)r * d + 8 * c) : make_uint4(0, 0, 0, 0);
-        }
-    }
+        for (int r = 0; r < SH_RG; r++)
+#pragma unroll
+            for (int c = 0; c < SH_CH; c++) {
+                const int ch = lane + 32 * c;
+                const size_t off = (size_t)(r0 + r) * d + 8 * (size_t)(warp * cpw + ch);
+                wg[r][c] = ch < cpw ? sh_ld16(src.gate[s] + off) : make_uint4(0, 0, 0, 0);
+                wu[r][c] = ch < cpw ? sh_ld16(src.up[s] + off) : make_uint4(0, 0, 0, 0);
+            }
+    };
+    if (u < nunits) load(u);
     griddep_wait();  // x and h belong to the kernels around this one
     for (int i = threadIdx.x; i < T * d / 4; i += blockDim.x)
         reinterpret_cast<float4 *>(xs)[i] = reinterpret_cast<const float4 *>(x)[i];
     __syncthreads();
-    bool first = true;
-    for (; q < nrows; q += W, first = false) {
-        const int s = (int)(q / f), r = (int)(q % f);
-        const uint16_t *gr = src.gate[s] + (size_t)r * d, *ur = src.up[s] + (size_t)r * d;
-        float ag[SH_TMAX] = {}, au[SH_TMAX] = {};
-        for (int c0 = 0; c0 < nc; c0 += 32 * SH_U) {
-            uint4 wg[SH_U], wu[SH_U];
+    constexpr int NV = SH_RG * 2 * SH_TMAX;  // (row, matrix, token) partial sums of a lane
+    for (; u < nunits; u += gridDim.x) {
+        float v[NV];
 #pragma unroll
-            for (int i = 0; i < SH_U; i++) {
-                const int c = c0 + lane + 32 * i;
-                if (first && c0 == 0) {
-                    wg[i] = pg[i];
-                    wu[i] = pu[i];
-                } else {
-                    wg[i] = c < nc ? sh_ld16(gr + 8 * c) : make_uint4(0, 0, 0, 0);
-                    wu[i] = c < nc ? sh_ld16(ur + 8 * c) : make_uint4(0, 0, 0, 0);
-                }
-            }
+        for (int i = 0; i < NV; i++) v[i] = 0.f;
 #pragma unroll
-            for (int i = 0; i < SH_U; i++) {
-                const int c = c0 + lane + 32 * i;
-                if (c < nc) {
+        for (int c = 0; c < SH_CH; c++) {
+            const int ch = lane + 32 * c;
+            if (ch < cpw) {
+                const int col = 8 * (warp * cpw + ch);
 #pragma unroll
-                    for (int t = 0; t < SH_TMAX; t++)
-                        if (t < T) {
-                            ag[t] = sh_dot8(wg[i], xs + (size_t)t * d + 8 * c, ag[t]);
-                            au[t] = sh_dot8(wu[i], xs + (size_t)t * d + 8 * c, au[t]);
+                for (int t = 0; t < SH_TMAX; t++)
+                    if (t < T) {
+#pragma unroll
+                        for (int r = 0; r < SH_RG; r++) {
+                            v[(r * 2 + 0) * SH_TMAX + t] = sh_dot8(wg[r][c], xs + (size_t)t * d + col, v[(r * 2 + 0) * SH_TMAX + t]);
+                            v[(r * 2 + 1) * SH_TMAX + t] = sh_dot8(wu[r][c], xs + (size_t)t * d + col, v[(r * 2 + 1) * SH_TMAX + t]);
                         }
-                }
+                    }
             }
         }
-#pragma unroll
-        for (int t = 0; t < SH_TMAX; t++)
-            if (t < T) {
-                const float g = warp_sum(ag[t]), u = warp_sum(au[t]);
-                if (lane == 0) h[((size_t)t * n + s) * f + r] = silu(g) * u;
+        // the next unit's weights are requested before this one is reduced
+        const int un = u + gridDim.x;
+        if (un < nunits) load(un);
+        warp_transpose_reduce<NV>(v, lane);  // lane l: the warp's sum of value sel_of(l) = l
+        red[warp * NV + lane] = v[0];
+        __syncthreads();
+        if ((int)threadIdx.x < SH_RG * T) {
+            const int r = threadIdx.x / T, t = threadIdx.x % T;
+            float g = 0.f, up = 0.f;
+            for (int w2 = 0; w2 < SH_WARPS; w2++) {
+                g += red[w2 * NV + (r * 2 + 0) * SH_TMAX + t];
+                up += red[w2 * NV + (r * 2 + 1) * SH_TMAX + t];
             }
+            const int q = u * SH_RG + r, s = q / f;
+            h[((size_t)t * n + s) * f + (q % f)] = silu(g) * up;
+        }
+        __syncthreads();
     }
 }
 
-// out[t][c] (+)= sum_s down_s[c] . h[t][s], one warp per output row c; h
-// [T][n][f] staged in shared memory.  f a multiple of 256.
+// out[t][c] (+)= sum_s down_s[c] . h[t][s], one warp per output row c at a
+// time with every 16-byte chunk of the row (n f bf16 weights) requested at
+// once; h [T][n][f] staged in shared memory.
 __global__ void __launch_bounds__(SH_WARPS * 32) k3_shared_down(const SharedSrc src, int n, const float *h, int T,
                                                                 int d, int f, float *out, int accumulate)
 {
     extern __shared__ float hs[];  // [T][n][f]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nc = f / 8;
+    const int ncs = f / 8;          // chunks per row of one expert
+    const int nch = n * ncs;        // chunks of an output row
     griddep_launch_dependents();
-    const long W = (long)gridDim.x * SH_WARPS;
-    long c = (long)blockIdx.x * SH_WARPS + warp;
-    uint4 pw[SH_U];
-    if (c < d) {
+    const int W = gridDim.x * SH_WARPS;
+    int c = blockIdx.x * SH_WARPS + warp;
+    uint4 w[SH_CHD];
+    auto load = [&](int row) {
 #pragma unroll
-        for (int i = 0; i < SH_U; i++) {
-            const int k = lane + 32 * i;
-            pw[i] = k < nc ? sh_ld16(src.down[0] + (size_t)c * f + 8 * k) : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < SH_CHD; i++) {
+            const int ch = lane + 32 * i;
+            w[i] = ch < nch ? sh_ld16(src.down[ch / ncs] + (size_t)row * f + 8 * (ch % ncs)) : make_uint4(0, 0, 0, 0);
         }
-    }
+    };
+    if (c < d) load(c);
     griddep_wait();
     for (int i = threadIdx.x; i < T * n * f / 4; i += blockDim.x)
         reinterpret_cast<float4 *>(hs)[i] = reinterpret_cast<const float4 *>(h)[i];
     __syncthreads();
-    bool first = true;
-    for (; c < d; c += W, first = false) {
-        float acc[SH_TMAX] = {};
-        for (int s = 0; s < n; s++) {
-            const uint16_t *dr = src.down[s] + (size_t)c * f;
-            for (int k0 = 0; k0 < nc; k0 += 32 * SH_U) {
-                uint4 w[SH_U];
+    for (; c < d; c += W) {
+        float acc[SH_TMAX];
 #pragma unroll
-                for (int i = 0; i < SH_U; i++) {
-                    const int k = k0 + lane + 32 * i;
-                    if (first && s == 0 && k0 == 0)
-                        w[i] = pw[i];
-                    else
-                        w[i] = k < nc ? sh_ld16(dr + 8 * k) : make_uint4(0, 0, 0, 0);
-                }
+        for (int t = 0; t < SH_TMAX; t++) acc[t] = 0.f;
 #pragma unroll
-                for (int i = 0; i < SH_U; i++) {
-                    const int k = k0 + lane + 32 * i;
-                    if (k < nc) {
+        for (int i = 0; i < SH_CHD; i++) {
+            const int ch = lane + 32 * i;
+            if (ch < nch) {
+                const int s = ch / ncs, k = ch % ncs;
 #pragma unroll
-                        for (int t = 0; t < SH_TMAX; t++)
-                            if (t < T) acc[t] = sh_dot8(w[i], hs + ((size_t)t * n + s) * f + 8 * k, acc[t]);
-                    }
-                }
+                for (int t = 0; t < SH_TMAX; t++)
+                    if (t < T) acc[t] = sh_dot8(w[i], hs + ((size_t)t * n + s) * f + 8 * k, acc[t]);
             }
         }
-#pragma unroll
-        for (int t = 0; t < SH_TMAX; t++)
+        if (c + W < d) load(c + W);
+        warp_transpose_reduce<SH_TMAX>(acc, lane);
+        constexpr int LPV = 32 / SH_TMAX;
+        if ((lane % LPV) == 0) {
+            const int t = sel_of<SH_TMAX>(lane);
             if (t < T) {
-                const float a = warp_sum(acc[t]);
-                if (lane == 0) {
-                    float *o = out + (size_t)t * d + c;
-                    *o = accumulate ? *o + a : a;
-                }
+                float *o = out + (size_t)t * d + c;
+                *o = accumulate ? *o + acc[0] : acc[0];
             }
+        }
     }
 }
 
@@ -176,12 +183,25 @@ int num_sms();
 
 bool shared_supported(int n, int d, int f)
 {
-    return n >= 1 && n <= SH_MAX && d % 256 == 0 && f % 256 == 0 && d <= 16384 && f <= 8192 &&
-           (size_t)SH_TMAX * d * 4 <= 200 * 1024 && (size_t)SH_TMAX * n * f * 4 <= 200 * 1024;
+    return n >= 1 && n <= SH_MAX && d % 256 == 0 && f % 256 == 0 && d <= 8192 && (size_t)n * f <= 32 * SH_CHD * 8 &&
+           (d / 8) % SH_WARPS == 0 && (size_t)SH_TMAX * d * 4 + SH_WARPS * SH_RG * 2 * SH_TMAX * 4 <= 200 * 1024 &&
+           (size_t)SH_TMAX * n * f * 4 <= 200 * 1024;
+}
+
+template <typename K>
+static int resident_grid(K kernel, size_t smem, long want)
+{
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, SH_WARPS * 32, smem) != cudaSuccess || b < 1) {
+        cudaGetLastError();
+        b = 1;
+    }
+    return (int)std::max(1L, std::min<long>(want, (long)b * num_sms()));
 }
 
 // out (+)= the shared experts of T tokens, SH_TMAX tokens per launch pair;
-// h: the workspace, SH_TMAX * n * f floats.
+// h: the workspace, SH_TMAX * n * f floats.  Both grids are as large as can
+// be resident at once (one wave).
 int launch_shared(const uint16_t *const *gate, const uint16_t *const *up, const uint16_t *const *down, int n,
                   const float *x, int T, int d, int f, float *h, float *out, int accumulate, cudaStream_t s)
 {
@@ -191,15 +211,14 @@ int launch_shared(const uint16_t *const *gate, const uint16_t *const *up, const 
         src.up[i] = up[i];
         src.down[i] = down[i];
     }
-    const int sms = num_sms();
     for (int t0 = 0; t0 < T; t0 += SH_TMAX) {
         const int tt = std::min(SH_TMAX, T - t0);
-        const size_t sx = (size_t)tt * d * 4, sh = (size_t)tt * n * f * 4;
+        const size_t sx = (size_t)tt * d * 4 + SH_WARPS * SH_RG * 2 * SH_TMAX * 4, sh = (size_t)tt * n * f * 4;
         if (ensure_smem((const void *)k3_shared_gateup, sx) != K3MOE_OK ||
             ensure_smem((const void *)k3_shared_down, sh) != K3MOE_OK)
             return K3MOE_ECUDA;
-        const int g1 = (int)std::min<long>(((long)n * f + SH_WARPS - 1) / SH_WARPS, 4L * sms);
-        const int g2 = (int)std::min<long>(((long)d + SH_WARPS - 1) / SH_WARPS, 4L * sms);
+        const int g1 = resident_grid(k3_shared_gateup, sx, (long)n * f / SH_RG);
+        const int g2 = resident_grid(k3_shared_down, sh, ((long)d + SH_WARPS - 1) / SH_WARPS);
         if (launch_pdl(k3_shared_gateup, dim3(g1), dim3(SH_WARPS * 32), sx, s, src, n, x + (size_t)t0 * d, tt, d, f,
                        h) != cudaSuccess ||
             launch_pdl(k3_shared_down, dim3(g2), dim3(SH_WARPS * 32), sh, s, src, n, (const float *)h, tt, d, f,
