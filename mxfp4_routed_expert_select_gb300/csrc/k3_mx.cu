@@ -268,8 +268,32 @@ template <int PH>
 struct MxState {
     uint32_t it = 0, sg = 0;
     int nexp = 0, cur_j = -1;
+    int pre = 0;  // producer: units of the wave already issued by mx_preissue
     uint32_t issued[MxCfg<PH>::NS] = {};
 };
+
+// The copies of one unit into ring stage s: phase 0 the gate and up tiles
+// (K step uu of row tile t) with their scale boxes, phase 1 two K steps of
+// the down rows and their scale box; mp: the expert's six tensor maps.
+template <int PH>
+K3_DEV void mx_issue(uint32_t sbase, uint32_t full, int s, const CUtensorMap *mp, int uu, int t, uint64_t pol)
+{
+    using C = MxCfg<PH>;
+    const uint32_t st = sbase + (uint32_t)(s * C::STAGE), sc = st + (uint32_t)(C::NMAT * C::A_BYTES);
+    mbar_arrive_expect_tx(full, C::NMAT * C::A_BYTES + C::NSC * C::SC_BYTES);
+    if (PH == 0) {
+#pragma unroll
+        for (int m = 0; m < 2; m++) {  // gate, up
+            tma_load_2d_hint(st + (uint32_t)(m * C::A_BYTES), mp + m, uu * 128, t * MX_M, full, pol);
+            tma_load_2d_hint(sc + (uint32_t)(m * C::SC_BYTES), mp + 3 + m, 16 * (uu >> 1), t * MX_M, full, pol);
+        }
+    } else {
+#pragma unroll
+        for (int m = 0; m < 2; m++)  // two K steps of the down rows
+            tma_load_2d_hint(st + (uint32_t)(m * C::A_BYTES), mp + 2, (2 * uu + m) * 128, t * MX_M, full, pol);
+        tma_load_2d_hint(sc, mp + 5, 16 * uu, t * MX_M, full, pol);
+    }
+}
 
 // One wave of a phase on this CTA's share of its units.  sm: the
 // 1024-aligned shared memory (phase layouts overlap: the phases run one after
@@ -325,7 +349,7 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
             int cur_tile = -1;
             const CUtensorMap *mp = nullptr;
             int t = 0;
-            for (int u = ulo; u < uhi && ok && !*abort_flag; u++, it++) {
+            for (int u = ulo + st.pre; u < uhi && ok && !*abort_flag; u++, it++) {
                 const int tile = (int)(u / upt), uu = (int)(u % upt);
                 if (tile != cur_tile) {
                     cur_tile = tile;
@@ -351,22 +375,11 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(bar(B_FULL + s), NMAT * C::A_BYTES + C::NSC * C::SC_BYTES);
+                mx_issue<PH>(sbase, bar(B_FULL + s), s, mp, uu, t, pol);
                 st.issued[s]++;
-                if (PH == 0) {
-#pragma unroll
-                    for (int m = 0; m < 2; m++) {  // gate, up
-                        tma_load_2d_hint(a_at(s, m), mp + m, uu * 128, t * MX_M, bar(B_FULL + s), pol);
-                        tma_load_2d_hint(sc_at(s, m), mp + 3 + m, 16 * (uu >> 1), t * MX_M, bar(B_FULL + s), pol);
-                    }
-                } else {
-#pragma unroll
-                    for (int m = 0; m < 2; m++)  // two K steps of the down rows
-                        tma_load_2d_hint(a_at(s, m), mp + 2, (2 * uu + m) * 128, t * MX_M, bar(B_FULL + s), pol);
-                    tma_load_2d_hint(sc_at(s, 0), mp + 5, 16 * uu, t * MX_M, bar(B_FULL + s), pol);
-                }
             }
             st.it = it;
+            st.pre = 0;
         }
         if (lane == 0 && w.last) {
             // drain: every copy issued in this phase has landed before the CTA exits
@@ -652,6 +665,30 @@ K3_DEV void mx_body(const MxArgs &a, uint8_t *sm, uint64_t *bars, uint32_t tmem,
     }
 }
 
+// The producer's first NS - 1 units of phase 0's first wave, issued by the
+// producer thread as soon as the experts are known (right after the top-k,
+// before the code of the phase body is reached); the body's producer goes on
+// from there.  Stage NS - 1 is left to it: that stage holds the B scale atoms
+// until they are in TMEM.
+K3_DEV void mx_preissue(const MxArgs &a, uint8_t *sm, uint64_t *bars, const int32_t *sel_ids, const MxWave &w,
+                        MxState<0> &st)
+{
+    using C = MxCfg<0>;
+    const int tpe = a.f / MX_M, upt = a.d / C::UK;
+    const int U = w.Uw, G = (int)gridDim.x;
+    const int ulo = w.uw0 + U * (int)blockIdx.x / G, uhi = w.uw0 + U * ((int)blockIdx.x + 1) / G;
+    const uint64_t pol = l2_evict_first();
+    int n = 0;
+    for (int u = ulo; u < uhi && n < C::NS - 1; u++, n++) {
+        const int tile = u / upt;
+        mx_issue<0>(smem_addr(sm), smem_addr(bars + MxBars<0>::FULL + n), n, a.maps + 6 * (size_t)sel_ids[tile / tpe],
+                    u % upt, tile % tpe, pol);
+        st.issued[n]++;
+    }
+    st.it = (uint32_t)n;
+    st.pre = n;
+}
+
 // Expert slots in a phase's first wave: three quarters of k (all of them for
 // k < 4).  The second wave's gate/up time must cover the first wave's h
 // epilogue, and the first wave's down time the second wave's.
@@ -871,6 +908,20 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                       tk, &s_flag))
         *abort_flag = 1;
     cta_sync_threads();
+    // Two waves per phase: gate/up of the first kA expert slots, then of the
+    // rest; down of the first kA, then of the rest.  The first wave's h is
+    // complete while the second wave's gate/up rows still stream, so the down
+    // phase starts on h that is ready, and the second wave's h has the first
+    // wave's down products to be finished in.
+    const int kA = wave_split(a0.k), kB = a0.k - kA, nwave = kB > 0 ? 2 : 1;
+    const int upe0 = (a0.f / MX_M) * (a0.d / MxCfg<0>::UK), upe1 = (a0.d / MX_M) * (a0.f / MxCfg<1>::UK);
+    auto wave = [&](int wv, int upe) {
+        return wv == 0 ? MxWave{0, kA * upe, true, nwave == 1} : MxWave{kA * upe, kB * upe, false, true};
+    };
+    MxState<0> st0;
+    MxState<1> st1;
+    if (warp == MX_W_PROD && (threadIdx.x & 31) == 0 && *abort_flag == 0)
+        mx_preissue(a0, sm, bars0, sel_ids, wave(0, upe0), st0);
     // Each role goes on to phase 1 when it is done with phase 0; the roles
     // that write phase 1's shared memory (producer, h loader) first wait for
     // phase 0's MMAs to complete (its FIN barrier); phase 1's TMEM columns
@@ -883,25 +934,18 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     // the combine weights are needed only by the phase-1 epilogue warps, whose
     // first named barrier orders them for the others of the four
     if (warp == MX_W_EPI1 && *abort_flag == 0) mx_weights(r, a0.k, sel_ids, s_logit, sel_w, threadIdx.x & 31);
-    // Two waves per phase: gate/up of the first kA expert slots, then of the
-    // rest; down of the first kA, then of the rest.  The first wave's h is
-    // complete while the second wave's gate/up rows still stream, so the down
-    // phase starts on h that is ready, and the second wave's h has the first
-    // wave's down products to be finished in.
-    const int kA = wave_split(a0.k), kB = a0.k - kA;
-    const int upe0 = (a0.f / MX_M) * (a0.d / MxCfg<0>::UK), upe1 = (a0.d / MX_M) * (a0.f / MxCfg<1>::UK);
-    MxState<0> st0;
-    MxState<1> st1;
-    mx_body<0>(a0, sm, bars0, tmem, abort_flag, s_last, s_stop, hready, sel_ids, sel_w, 0u, &s_flag,
-               MxWave{0, kA * upe0, true, kB == 0}, st0);
-    if (kB > 0)
+    // The waves run in loops rather than as separate inlined bodies: the
+    // kernel's code is far larger than the SM's instruction cache, and one
+    // body per phase keeps it half as large (fewer instruction fetches from
+    // L2 where the roles move on to new code).
+#pragma unroll 1
+    for (int wv = 0; wv < nwave; wv++)
         mx_body<0>(a0, sm, bars0, tmem, abort_flag, s_last, s_stop, hready, sel_ids, sel_w, 0u, &s_flag,
-                   MxWave{kA * upe0, kB * upe0, false, true}, st0);
-    mx_body<1>(a1, sm, bars1, tmem, abort_flag, s_last, s_stop1, hready, sel_ids, sel_w, fin0, &s_flag,
-               MxWave{0, kA * upe1, true, kB == 0}, st1, bars0, st0.issued);
-    if (kB > 0)
+                   wave(wv, upe0), st0);
+#pragma unroll 1
+    for (int wv = 0; wv < nwave; wv++)
         mx_body<1>(a1, sm, bars1, tmem, abort_flag, s_last, s_stop1, hready, sel_ids, sel_w, fin0, &s_flag,
-                   MxWave{kA * upe1, kB * upe1, false, true}, st1, bars0, st0.issued);
+                   wave(wv, upe1), st1, bars0, st0.issued);
 
     tc_fence_before();
     cta_sync_threads();
