@@ -767,27 +767,23 @@ K3_DEV bool mx_route(const MxRoute &r, const MxArgs &a0, float *out, uint8_t *sm
             for (int j = 0; j < 8; j++) xr[i][j] = 0.f;
         }
     }
+    // (a loop, not unrolled over the row limit: the router runs once per
+    // launch from cold instruction caches, where code size is time)
     bool ok = true;
-    float acc[MX_ROUTER_ROWS];
-#pragma unroll
-    for (int q = 0; q < MX_ROUTER_ROWS; q++) {
-        acc[q] = 0.f;
-        if (q < nr && ok) ok = mbar_wait(bar_r + 8u * q, 0, a0.err);
-        if (q < nr && ok) {
+#pragma unroll 1
+    for (int q = 0; q < nr; q++) {
+        float acc = 0.f;
+        if (ok) ok = mbar_wait(bar_r + 8u * q, 0, a0.err);
+        if (ok) {
             const uint32_t row = sbase + (uint32_t)q * rowb;
 #pragma unroll
             for (int i = 0; i < 3; i++) {
                 const int c = c0 + lane + 32 * i;
-                if (c < c1) acc[q] = bf16x8_dot(lds128(row + 16u * (uint32_t)c), xr[i], acc[q]);
+                if (c < c1) acc = bf16x8_dot(lds128(row + 16u * (uint32_t)c), xr[i], acc);
             }
         }
-    }
-#pragma unroll
-    for (int q = 0; q < MX_ROUTER_ROWS; q++) {
-        if (q < nr) {
-            const float v = warp_sum(acc[q]);
-            if (lane == 0) s_logit[warp * MX_ROUTER_ROWS + q] = v;
-        }
+        const float v = warp_sum(acc);
+        if (lane == 0) s_logit[warp * MX_ROUTER_ROWS + q] = v;
     }
     cta_sync_threads();
     if ((int)threadIdx.x < nr) {
