@@ -638,165 +638,158 @@ K3_DEV void cta_topk_by(Logit logit_of, const Router &rt, int E, int k, int32_t 
         }
     }
 }
-// The first 256 threads of a CTA select the top k (k <= 16) of E <= 1024
-// selection keys router_select(rt, logit_of(e), e), ties to the lower id, with
-// the same result as cta_topk_by and warp_topk; ids_out[0..k) receives the
-// ids in ascending order (the combine weights are left to the caller, see
-// router_weight).  Keys are compared as 64-bit words
-// key << 32 | (2^32 - 1 - id), which order exactly like (key descending, id
-// ascending); ids >= E are padding (word 0).  Warp w holds the ids
-// w + 8 (4 l + r), r = 0..3, in lane l (interleaved, so that every warp holds
-// about E / 8 real keys; within a warp lower lanes still hold lower ids), each
-// lane's four sorted.
-//  1. Each warp takes its R = ceil(k / 8) largest words (R rounds of a warp
-//     maximum, redux.sync); T = the smallest of the eight warps' R-th largest.
-//     At least 8 R >= k words are >= T, so the k largest are all >= T.
-//  2. The words >= T (usually a few dozen) go to shared memory, and each one's
-//     place is the number of those words larger than it: the k whose place is
-//     below k are the result.
-//  3. If more than 128 words are >= T (keys with many ties at T, or fewer
-//     than R real keys in some warp), each warp takes its k largest instead
-//     (k rounds) and the 8 k candidates are ranked the same way.
-// Then warp 0 puts the k ids in ascending order.  sync() is a barrier over
-// all threads of the CTA; threads of warps 8 and up only take part in it.
+// A CTA of at least eight warps selects the top k (k <= 16) of E <= 1024
+// selection keys okey(router_select(rt, logit_of(e), e)), ties to the lower
+// id, with the same result as cta_topk_by and warp_topk; ids_out[0..k)
+// receives the ids in ascending order (the combine weights are left to the
+// caller, see router_weight).  Words key << 32 | (2^32 - 1 - id) order
+// exactly like (key descending, id ascending).  Warp w < 8 holds the
+// m = ceil(E / 8) ids [w m, w m + m), lane l the ids w m + l + 32 r (r < 4:
+// consecutive lanes read consecutive logits).
+//  1. T_w = the R-th largest (R = ceil(k / 8)) of warp w's lane maxima, the
+//     lanes tied at a maximum dropping out together, so that at least R of
+//     the warp's keys are >= T_w; T = the smallest T_w.  At least 8 R >= k
+//     keys are >= T, so the k largest words all have keys >= T.
+//  2. The words whose keys are >= T (a few dozen for untied keys) go to
+//     shared memory, and each one's place is the number of those words
+//     larger than it (eight lanes a word, each comparing it with every eighth
+//     word): the k whose place is below k are the result.
+//  3. If more than 128 keys are >= T (many ties at T, or fewer than R keys in
+//     some warp), each warp takes its k largest words instead (k rounds of an
+//     exact warp maximum) and the 8 k candidates are ranked the same way.
+// Then warp 0 puts the k ids in ascending order.  Every thread of the CTA
+// calls it; sync() is a barrier over all of them.
 struct CtaTopkRedSmem {
-    uint64_t cand[128];
-    uint64_t thr[8];
-    int32_t ids[16];
-    int32_t cnt;
+    alignas(16) uint64_t cand[128];  // candidate words (0: unused)
+    alignas(16) uint32_t thr[8];     // T_w
+    int32_t ids[16];                 // the k winners by place
+    int32_t cnt;                     // candidates
 };
-// (key, id) pairs a, b in order: key descending, id ascending on ties
-K3_DEV void topk_cmpswap(uint32_t &ka, int &ia, uint32_t &kb, int &ib)
-{
-    if (kb > ka || (kb == ka && ib < ia)) {
-        const uint32_t tk = ka;
-        const int ti = ia;
-        ka = kb;
-        ia = ib;
-        kb = tk;
-        ib = ti;
-    }
-}
-// The warp's k largest (k <= 32) of the 128 pairs held four per lane (each
-// lane's sorted): lane i < k receives the i-th largest in (rk, rid).
-K3_DEV void warp_take_k(uint32_t (&key)[4], int (&id)[4], int k, int lane, uint32_t &rk, int &rid)
-{
-    rk = 0u;
-    rid = 0;
-    for (int i = 0; i < k; i++) {
-        const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
-        const int w = __ffs(__ballot_sync(0xffffffffu, key[0] == m)) - 1;
-        const int wid = __shfl_sync(0xffffffffu, id[0], w);
-        if (lane == i) {
-            rk = m;
-            rid = wid;
-        }
-        if (lane == w) {
-            key[0] = key[1];
-            key[1] = key[2];
-            key[2] = key[3];
-            key[3] = 0u;
-            id[0] = id[1];
-            id[1] = id[2];
-            id[2] = id[3];
-            id[3] = 0x7fffffff;
-        }
-    }
-}
 K3_DEV uint64_t topk_word(uint32_t key, int id, int E)
 {
     return id < E ? ((uint64_t)key << 32) | (uint64_t)(0xffffffffu - (uint32_t)id) : 0ull;
 }
 K3_DEV int topk_word_id(uint64_t w) { return (int)(0xffffffffu - (uint32_t)w); }
-// the keys of warp w's four ids of this lane, sorted
-template <typename Logit>
-K3_DEV void topk_lane_keys(Logit logit_of, const Router &rt, int E, int warp, int lane, uint32_t (&key)[4],
-                           int (&id)[4])
+K3_DEV void topk_sort2(uint64_t &a, uint64_t &b)
 {
-#pragma unroll
-    for (int r = 0; r < 4; r++) {
-        const int e = warp + 8 * (4 * lane + r);
-        key[r] = 0u;  // below every real key (okey(-inf) = 0x007fffff)
-        id[r] = 0x7fffffff;
-        if (e < E) {
-            key[r] = okey(router_select(rt, logit_of(e), e));
-            id[r] = e;
-        }
-    }
-    topk_cmpswap(key[0], id[0], key[1], id[1]);
-    topk_cmpswap(key[2], id[2], key[3], id[3]);
-    topk_cmpswap(key[0], id[0], key[2], id[2]);
-    topk_cmpswap(key[1], id[1], key[3], id[3]);
-    topk_cmpswap(key[1], id[1], key[2], id[2]);
+    const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+    a = hi;
+    b = lo;
 }
-// places of the n (<= 128) candidate words: the k smallest places go to
-// sm.ids in descending word order
-K3_DEV void topk_rank(CtaTopkRedSmem &sm, int n, int k, int t)
+// the warp's largest of the lanes' words w (exact: key, then the lower id)
+K3_DEV uint64_t warp_max_word(uint64_t w)
 {
-    if (t < n) {
-        const uint64_t vc = sm.cand[t];
-        int ahead = 0;
-#pragma unroll 4
-        for (int q = 0; q < n; q++) ahead += sm.cand[q] > vc;
-        if (ahead < k) sm.ids[ahead] = topk_word_id(vc);
-    }
+    const uint32_t hk = (uint32_t)(w >> 32), lk = (uint32_t)w;
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, hk);
+    const uint32_t ml = __reduce_max_sync(0xffffffffu, hk == mk ? lk : 0u);
+    return ((uint64_t)mk << 32) | ml;
 }
 template <typename Sync, typename Logit>
 K3_DEV void cta_topk_red(Logit logit_of, const Router &rt, int E, int k, int32_t *ids_out, CtaTopkRedSmem &sm,
                          Sync sync)
 {
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int R = (k + 7) >> 3;
+    const int R = (k + 7) >> 3, m = (E + 7) >> 3;
+    const unsigned lt = (1u << lane) - 1u;
     uint32_t key[4];
-    int id[4];
-    uint64_t own[4];
+    unsigned valid = 0u;  // bit r: slot r holds an expert
+    if (t < 128) sm.cand[t] = 0ull;
     if (warp < 8) {
-        topk_lane_keys(logit_of, rt, E, warp, lane, key, id);
 #pragma unroll
-        for (int r = 0; r < 4; r++) own[r] = topk_word(key[r], id[r], E);
-        uint32_t rk;
-        int rid;
-        warp_take_k(key, id, R, lane, rk, rid);
-        const uint64_t tw = __shfl_sync(0xffffffffu, topk_word(rk, rid, E), R - 1);
+        for (int r = 0; r < 4; r++) {
+            const int j = lane + 32 * r, e = warp * m + j;
+            key[r] = 0u;
+            if (j < m && e < E) {
+                key[r] = okey(router_select(rt, logit_of(e), e));
+                valid |= 1u << r;
+            }
+        }
+        uint32_t lk = 0u;
+#pragma unroll
+        for (int r = 0; r < 4; r++)
+            if ((valid >> r) & 1u) lk = max(lk, key[r]);
+        uint32_t tw = 0u;
+        for (int i = 0; i < R; i++) {
+            tw = __reduce_max_sync(0xffffffffu, lk);
+            if (lk == tw) lk = 0u;
+        }
         if (lane == 0) sm.thr[warp] = tw;
         if (t == 0) sm.cnt = 0;
     }
     sync();
     if (warp < 8) {
-        uint64_t T = sm.thr[0];
+        const uint4 ta = *reinterpret_cast<const uint4 *>(&sm.thr[0]);
+        const uint4 tb = *reinterpret_cast<const uint4 *>(&sm.thr[4]);
+        const uint32_t T = min(min(min(ta.x, ta.y), min(ta.z, ta.w)), min(min(tb.x, tb.y), min(tb.z, tb.w)));
+        unsigned b[4];
+        int c = 0;
 #pragma unroll
-        for (int w = 1; w < 8; w++) T = sm.thr[w] < T ? sm.thr[w] : T;
+        for (int r = 0; r < 4; r++) {
+            b[r] = __ballot_sync(0xffffffffu, ((valid >> r) & 1u) && key[r] >= T);
+            c += __popc(b[r]);
+        }
+        int base = 0;
+        if (lane == 0 && c) base = atomicAdd(&sm.cnt, c);
+        base = __shfl_sync(0xffffffffu, base, 0);
 #pragma unroll
-        for (int r = 0; r < 4; r++)
-            if (own[r] != 0ull && own[r] >= T) {
-                const int pos = atomicAdd(&sm.cnt, 1);
-                if (pos < 128) sm.cand[pos] = own[r];
+        for (int r = 0; r < 4; r++) {
+            if ((b[r] >> lane) & 1u) {
+                const int pos = base + __popc(b[r] & lt);
+                if (pos < 128) sm.cand[pos] = topk_word(key[r], warp * m + lane + 32 * r, E);
             }
+            base += __popc(b[r]);
+        }
     }
     sync();
-    const int n = sm.cnt;
-    if (n <= 128) {
-        topk_rank(sm, n, k, t);
-    } else {
+    int n = sm.cnt;
+    if (n > 128) {
         sync();  // every thread has read the count
         if (warp < 8) {
-            topk_lane_keys(logit_of, rt, E, warp, lane, key, id);
-            uint32_t rk;
-            int rid;
-            warp_take_k(key, id, k, lane, rk, rid);
-            if (lane < 16) sm.cand[16 * warp + lane] = lane < k ? topk_word(rk, rid, E) : 0ull;
+            uint64_t w[4];
+#pragma unroll
+            for (int r = 0; r < 4; r++)
+                w[r] = ((valid >> r) & 1u) ? topk_word(key[r], warp * m + lane + 32 * r, E) : 0ull;
+            topk_sort2(w[0], w[1]);
+            topk_sort2(w[2], w[3]);
+            topk_sort2(w[0], w[2]);
+            topk_sort2(w[1], w[3]);
+            topk_sort2(w[1], w[2]);
+            uint64_t mine = 0ull;
+            for (int i = 0; i < k; i++) {
+                const uint64_t M = warp_max_word(w[0]);
+                if (lane == i) mine = M;
+                if (w[0] == M) {  // the lane holding it moves on to its next
+                    w[0] = w[1];
+                    w[1] = w[2];
+                    w[2] = w[3];
+                    w[3] = 0ull;
+                }
+            }
+            if (lane < 16) sm.cand[16 * warp + lane] = mine;
         }
+        n = 128;
         sync();
-        topk_rank(sm, 128, k, t);
+    }
+    {
+        const int s = lane & 7, n8 = (n + 7) >> 3, per = (int)(blockDim.x >> 5) * 4;
+        for (int c0 = 0; c0 < n; c0 += per) {
+            const int c = c0 + warp * 4 + (lane >> 3);
+            const uint64_t vc = c < n ? sm.cand[c] : 0ull;
+            int a = 0;
+            for (int q = 0; q < n8; q++) a += (int)(sm.cand[8 * q + s] > vc);
+            a += __shfl_xor_sync(0xffffffffu, a, 1);
+            a += __shfl_xor_sync(0xffffffffu, a, 2);
+            a += __shfl_xor_sync(0xffffffffu, a, 4);
+            if (s == 0 && vc != 0ull && a < k) sm.ids[a] = topk_word_id(vc);
+        }
     }
     sync();
     if (warp == 0) {
         // each winner's place in ascending id order
-        const int rid = lane < k ? sm.ids[lane] : 0;
-        __syncwarp();
+        const int rid = lane < k ? sm.ids[lane] : 0x7fffffff;
         int rank = 0;
-        if (lane < k)
-            for (int q = 0; q < k; q++) rank += sm.ids[q] < rid;
+#pragma unroll
+        for (int q = 0; q < 16; q++) rank += (int)(__shfl_sync(0xffffffffu, rid, q) < rid);
         if (lane < k) ids_out[rank] = rid;
     }
 }
