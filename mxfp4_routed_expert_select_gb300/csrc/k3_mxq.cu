@@ -881,29 +881,53 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) k3_mxq_down(const MqArgs a)
         // --------------------------------------------------------- epilogue
         const int q = warp & 3;
         uint32_t ut = 0;
+        // lane l of group g (rows 8 g .. 8 g + 7 of this warp's 32) takes
+        // tokens 8 i + (l mod 8) of the tile and adds their eight rows with
+        // two vector reductions.  Their output rows and combine weights are
+        // read once per run of a tile's row blocks (all loads in flight
+        // together), not once per token group of every unit.
+        constexpr int NJ = MQ_TN / 8;
+        int cur = -1, n = 0;
+        size_t orow[NJ];
+        float wv[NJ];
         Cursor cu = cur_init();
         for (long u = ulo; u < uhi && !*abort_flag; u++, ut++, cur_next(cu)) {
             const int ti = cur_tile(cu), rb = cur_rb(cu);
-            const MqTile tl = a.tiles[ti];
+            if (ti != cur) {
+                cur = ti;
+                const MqTile tl = a.tiles[ti];
+                n = tl.n;
+                int pr[NJ];
+#pragma unroll
+                for (int i = 0; i < NJ; i++) {
+                    const int j = 8 * i + (lane & 7);
+                    pr[i] = j < n ? a.perm[tl.pair_begin + j] : 0;
+                }
+#pragma unroll
+                for (int i = 0; i < NJ; i++) {
+                    const int j = 8 * i + (lane & 7);
+                    wv[i] = j < n ? a.wsel[pr[i]] : 0.f;
+                    orow[i] = (size_t)(pr[i] / a.k) * a.d;
+                }
+            }
             const int buf = (int)(ut & 1);
             if (!__all_sync(0xffffffffu, tc_wait(bar(B_ACCF + buf), (ut / 2) & 1, a.err, abort_flag))) break;
             tc_fence_after();
             const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(MD_TACC + buf * MQ_TN);
-            // lane l of group g (rows 8 g .. 8 g + 7 of this warp's 32) takes
-            // token j0 + (l mod 8) of the eight and adds its eight rows with
-            // two vector reductions
-            for (int j0 = 0; j0 < tl.n; j0 += 8) {
-                float y[8];
-                tmem_ld8(tacc + (uint32_t)j0, y);
-                tmem_wait_ld();
-                mq_transpose8(y, lane);
-                const int j = j0 + (lane & 7);
-                if (j < tl.n) {
-                    const int pair = a.perm[tl.pair_begin + j];
-                    const float w = a.wsel[pair];
-                    float *o = a.out + (size_t)(pair / a.k) * a.d + rb * MQ_M + q * 32 + (lane & ~7);
-                    mq_red_v4(o, w * y[0], w * y[1], w * y[2], w * y[3]);
-                    mq_red_v4(o + 4, w * y[4], w * y[5], w * y[6], w * y[7]);
+            const size_t col = (size_t)rb * MQ_M + q * 32 + (lane & ~7);
+#pragma unroll
+            for (int i = 0; i < NJ; i++) {
+                if (8 * i < n) {
+                    float y[8];
+                    tmem_ld8(tacc + (uint32_t)(8 * i), y);
+                    tmem_wait_ld();
+                    mq_transpose8(y, lane);
+                    if (8 * i + (lane & 7) < n) {
+                        float *o = a.out + orow[i] + col;
+                        const float w = wv[i];
+                        mq_red_v4(o, w * y[0], w * y[1], w * y[2], w * y[3]);
+                        mq_red_v4(o + 4, w * y[4], w * y[5], w * y[6], w * y[7]);
+                    }
                 }
             }
             tc_fence_before();
