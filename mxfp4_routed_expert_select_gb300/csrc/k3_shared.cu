@@ -179,6 +179,75 @@ __global__ void __launch_bounds__(SH_WARPS * 32) k3_shared_down(const SharedSrc 
     }
 }
 
+// The same product with two rows in flight per warp (n f <= 3072): the
+// loads of row c + 2W are issued as soon as row c is multiplied, so every
+// warp keeps the next row's loads outstanding while it works on one; eight
+// warps a CTA and two CTAs an SM hold as many rows in registers as the
+// register file allows.
+constexpr int SH2_WARPS = 8;
+constexpr int SH2_CH = 12;  // 16-byte chunks per lane of a down row (n f <= 3072)
+
+__global__ void __launch_bounds__(SH2_WARPS * 32, 2) k3_shared_down2(const SharedSrc src, int n, const float *h, int T,
+                                                                    int d, int f, float *out, int accumulate)
+{
+    extern __shared__ float hs[];  // [T][n][f]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ncs = f / 8;    // chunks per row of one expert
+    const int nch = n * ncs;  // chunks of an output row
+    griddep_launch_dependents();
+    const int W = gridDim.x * SH2_WARPS;
+    int c = blockIdx.x * SH2_WARPS + warp;
+    uint4 w0[SH2_CH], w1[SH2_CH];
+    auto load = [&](uint4(&w)[SH2_CH], int row) {
+#pragma unroll
+        for (int i = 0; i < SH2_CH; i++) {
+            const int ch = lane + 32 * i;
+            w[i] = ch < nch ? sh_ld16(src.down[ch / ncs] + (size_t)row * f + 8 * (ch % ncs)) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    auto dots = [&](const uint4(&w)[SH2_CH], float(&acc)[SH_TMAX]) {
+#pragma unroll
+        for (int t = 0; t < SH_TMAX; t++) acc[t] = 0.f;
+#pragma unroll
+        for (int i = 0; i < SH2_CH; i++) {
+            const int ch = lane + 32 * i;
+            if (ch < nch) {
+                const int s = ch / ncs, k = ch % ncs;
+#pragma unroll
+                for (int t = 0; t < SH_TMAX; t++)
+                    if (t < T) acc[t] = sh_dot8(w[i], hs + ((size_t)t * n + s) * f + 8 * k, acc[t]);
+            }
+        }
+    };
+    auto finish = [&](float(&acc)[SH_TMAX], int row) {
+        warp_transpose_reduce<SH_TMAX>(acc, lane);
+        constexpr int LPV = 32 / SH_TMAX;
+        if ((lane % LPV) == 0) {
+            const int t = sel_of<SH_TMAX>(lane);
+            if (t < T) {
+                float *o = out + (size_t)t * d + row;
+                *o = accumulate ? *o + acc[0] : acc[0];
+            }
+        }
+    };
+    if (c < d) load(w0, c);
+    if (c + W < d) load(w1, c + W);
+    griddep_wait();
+    for (int i = threadIdx.x; i < T * n * f / 4; i += blockDim.x)
+        reinterpret_cast<float4 *>(hs)[i] = reinterpret_cast<const float4 *>(h)[i];
+    __syncthreads();
+    for (; c < d; c += 2 * W) {
+        float acc[SH_TMAX];
+        dots(w0, acc);  // row c
+        if (c + 2 * W < d) load(w0, c + 2 * W);
+        finish(acc, c);
+        if (c + W >= d) break;
+        dots(w1, acc);  // row c + W
+        if (c + 3 * W < d) load(w1, c + 3 * W);
+        finish(acc, c + W);
+    }
+}
+
 int num_sms();
 
 bool shared_supported(int n, int d, int f)
@@ -189,10 +258,10 @@ bool shared_supported(int n, int d, int f)
 }
 
 template <typename K>
-static int resident_grid(K kernel, size_t smem, long want)
+static int resident_grid(K kernel, size_t smem, long want, int threads = SH_WARPS * 32)
 {
     int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, SH_WARPS * 32, smem) != cudaSuccess || b < 1) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, threads, smem) != cudaSuccess || b < 1) {
         cudaGetLastError();
         b = 1;
     }
@@ -214,15 +283,25 @@ int launch_shared(const uint16_t *const *gate, const uint16_t *const *up, const 
     for (int t0 = 0; t0 < T; t0 += SH_TMAX) {
         const int tt = std::min(SH_TMAX, T - t0);
         const size_t sx = (size_t)tt * d * 4 + SH_WARPS * SH_RG * 2 * SH_TMAX * 4, sh = (size_t)tt * n * f * 4;
+        const bool two = (long)n * f <= 32L * SH2_CH * 8;  // two rows in flight per warp
         if (ensure_smem((const void *)k3_shared_gateup, sx) != K3MOE_OK ||
-            ensure_smem((const void *)k3_shared_down, sh) != K3MOE_OK)
+            ensure_smem(two ? (const void *)k3_shared_down2 : (const void *)k3_shared_down, sh) != K3MOE_OK)
             return K3MOE_ECUDA;
         const int g1 = resident_grid(k3_shared_gateup, sx, (long)n * f / SH_RG);
-        const int g2 = resident_grid(k3_shared_down, sh, ((long)d + SH_WARPS - 1) / SH_WARPS);
-        if (launch_pdl(k3_shared_gateup, dim3(g1), dim3(SH_WARPS * 32), sx, s, src, n, x + (size_t)t0 * d, tt, d, f,
-                       h) != cudaSuccess ||
-            launch_pdl(k3_shared_down, dim3(g2), dim3(SH_WARPS * 32), sh, s, src, n, (const float *)h, tt, d, f,
-                       out + (size_t)t0 * d, accumulate) != cudaSuccess) {
+        cudaError_t e = launch_pdl(k3_shared_gateup, dim3(g1), dim3(SH_WARPS * 32), sx, s, src, n,
+                                   x + (size_t)t0 * d, tt, d, f, h);
+        if (e == cudaSuccess) {
+            if (two) {
+                const int g2 = resident_grid(k3_shared_down2, sh, ((long)d + SH2_WARPS - 1) / SH2_WARPS, SH2_WARPS * 32);
+                e = launch_pdl(k3_shared_down2, dim3(g2), dim3(SH2_WARPS * 32), sh, s, src, n, (const float *)h, tt, d,
+                               f, out + (size_t)t0 * d, accumulate);
+            } else {
+                const int g2 = resident_grid(k3_shared_down, sh, ((long)d + SH_WARPS - 1) / SH_WARPS);
+                e = launch_pdl(k3_shared_down, dim3(g2), dim3(SH_WARPS * 32), sh, s, src, n, (const float *)h, tt, d,
+                               f, out + (size_t)t0 * d, accumulate);
+            }
+        }
+        if (e != cudaSuccess) {
             cudaGetLastError();
             return K3MOE_ECUDA;
         }
